@@ -1,0 +1,251 @@
+"""fp64 CPU oracle of the DSpark Markov-head drafting hot path (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: the test-suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers.  The product path never imports this
+package.  The arithmetic lives in ``dspark_oracle.c`` (plain C, double
+precision, optional OpenMP); this module only builds it with gcc, marshals
+numpy arrays and reshapes outputs.  It shares no code with the CUDA path.
+
+Every function cites the passage of the DSpark pages it follows in the C
+source.  Every function here is pinned by ``tests/test_oracle_pins.py``
+(printed values, known answers, closed forms through numpy/scipy, exhaustive
+enumeration); ``tests/test_oracle_mutants.py`` compiles copies of the C source
+with planted mistakes and checks that a pin catches each one.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dspark_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no FP contraction); return the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    i32, i64, f64, u64, u32 = (ctypes.c_int, ctypes.c_int64, ctypes.c_double,
+                               ctypes.c_uint64, ctypes.c_uint32)
+    lib.orc_set_threads.argtypes = [i32]
+    lib.orc_max_threads.restype = i32
+    lib.orc_philox4x32_10.argtypes = [P, P, P]
+    lib.orc_uniform.argtypes = [u64, u32, u32, u32, u32]
+    lib.orc_uniform.restype = f64
+    lib.orc_gumbel.argtypes = [u64, u32, u32, u32]
+    lib.orc_gumbel.restype = f64
+    lib.orc_gate.argtypes = [P, P, i64, i32, i32, P]
+    lib.orc_markov_draft.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, u64, i32, i32,
+                                     P, P, P, P, P]
+    lib.orc_markov_draft.restype = i32
+    lib.orc_markov_logits.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P, P]
+    lib.orc_markov_logits.restype = i32
+    lib.orc_confidence.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32, i32, i32, f64,
+                                   P, P, P]
+    lib.orc_confidence.restype = i32
+    lib.orc_topk.argtypes = [P, i32, i32, i32, i32, P, P, P]
+    lib.orc_topk.restype = i32
+    lib.orc_pair_scores.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, P]
+    lib.orc_pair_scores.restype = i32
+    lib.orc_walk.argtypes = [P, P, i32, i32, i32, f64, u64, i32, i32, P, P, P, P, P]
+    lib.orc_walk.restype = i32
+    return lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+class Oracle:
+    """The oracle's functions bound to one compiled library (the default one, or a copy)."""
+
+    def __init__(self, lib_path: str):
+        self.lib_path = lib_path
+        self._lib = _bind(ctypes.CDLL(lib_path))
+
+    def set_threads(self, n: int) -> None:
+        self._lib.orc_set_threads(int(n))
+
+    def max_threads(self) -> int:
+        return int(self._lib.orc_max_threads())
+
+    def philox4x32_10(self, ctr, key) -> np.ndarray:
+        """One Philox4x32-10 block: ctr (4 x uint32), key (2 x uint32) -> 4 x uint32."""
+        c = np.ascontiguousarray(ctr, dtype=np.uint32)
+        k = np.ascontiguousarray(key, dtype=np.uint32)
+        out = np.zeros(4, np.uint32)
+        self._lib.orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+        return out
+
+    def uniform(self, seed: int, b: int, k: int, v: int, tag: int = 0) -> float:
+        return float(self._lib.orc_uniform(seed, b, k, v, tag))
+
+    def gumbel(self, seed: int, b: int, k: int, v: int) -> float:
+        return float(self._lib.orc_gumbel(seed, b, k, v))
+
+    def gate(self, h: np.ndarray, Wg: np.ndarray) -> np.ndarray:
+        """H = sigmoid(h . Wg) in fp64; h [..., d] bf16 bits, Wg [d, r] bf16 bits -> [..., r]."""
+        h = _c(h, np.uint16)
+        Wg = _c(Wg, np.uint16)
+        d, r = Wg.shape
+        M = h.size // d
+        H = np.zeros(h.shape[:-1] + (r,), np.float64)
+        self._lib.orc_gate(_ptr(h), _ptr(Wg), M, d, r, _ptr(H))
+        return H
+
+    def markov_draft(self, U, W1, W2, anchors, *, temperature: float, seed: int, H=None,
+                     b0: int = 0, nb: Optional[int] = None, forced=None) -> dict:
+        """Run the Markov-head draft for requests b0 .. b0+nb-1 (outputs compact [nb, K])."""
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        r = 0 if W1 is None else W1.shape[1]
+        W1 = _c(W1, np.uint16) if r > 0 else np.zeros((V, 1), np.uint16)
+        W2 = _c(W2, np.uint16) if r > 0 else np.zeros((1, V), np.uint16)
+        anchors = _c(anchors, np.int32)
+        H = _c(H, np.float64)
+        nb = B - b0 if nb is None else nb
+        forced = _c(forced, np.int32)
+        tokens = np.zeros((nb, K), np.int32)
+        logprobs = np.zeros((nb, K), np.float64)
+        margins = np.zeros((nb, K), np.float64)
+        flp = np.zeros((nb, K), np.float64) if forced is not None else None
+        rc = self._lib.orc_markov_draft(_ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), _ptr(H), B, K, V,
+                                      r, float(temperature), int(seed), b0, nb, _ptr(forced),
+                                      _ptr(tokens), _ptr(logprobs), _ptr(margins), _ptr(flp))
+        if rc != 0:
+            raise ValueError("oracle markov_draft rejected its arguments")
+        out = dict(tokens=tokens, logprobs=logprobs, margins=margins)
+        if forced is not None:
+            out["forced_logprobs"] = flp
+        return out
+
+    def markov_logits(self, U, W1, W2, prev, *, temperature: float = 1.0, H=None, b0: int = 0,
+                      nb: Optional[int] = None) -> dict:
+        """Teacher-forced calibrated logits [nb, K, V] (fp64) and lse [nb, K]."""
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        r = 0 if W1 is None else W1.shape[1]
+        W1 = _c(W1, np.uint16) if r > 0 else np.zeros((V, 1), np.uint16)
+        W2 = _c(W2, np.uint16) if r > 0 else np.zeros((1, V), np.uint16)
+        prev = _c(prev, np.int32)
+        H = _c(H, np.float64)
+        nb = B - b0 if nb is None else nb
+        logits = np.zeros((nb, K, V), np.float64)
+        lse = np.zeros((nb, K), np.float64)
+        rc = self._lib.orc_markov_logits(_ptr(U), _ptr(W1), _ptr(W2), _ptr(prev), _ptr(H), B, K, V, r,
+                                       float(temperature), b0, nb, _ptr(logits), _ptr(lse))
+        if rc != 0:
+            raise ValueError("oracle markov_logits rejected its arguments")
+        return dict(logits=logits, lse=lse)
+
+    def confidence(self, h, W1, anchors, tokens, w, *, bias: float = 0.0, with_markov: bool = True,
+                   threshold: float = 0.3, V: Optional[int] = None) -> dict:
+        """Confidence c_k, survival cumprod a_k and verify length per request."""
+        h = _c(h, np.uint16)
+        B, K, d = h.shape
+        r = W1.shape[1] if (with_markov and W1 is not None) else 0
+        V = (W1.shape[0] if W1 is not None else 1) if V is None else V
+        W1c = _c(W1, np.uint16) if W1 is not None else np.zeros((1, 1), np.uint16)
+        anchors = _c(anchors, np.int32)
+        tokens = _c(tokens, np.int32)
+        w = _c(w, np.uint16)
+        conf = np.zeros((B, K), np.float64)
+        cum = np.zeros((B, K), np.float64)
+        vl = np.zeros(B, np.int32)
+        rc = self._lib.orc_confidence(_ptr(h), _ptr(W1c), _ptr(anchors), _ptr(tokens), _ptr(w),
+                                    float(bias), int(bool(with_markov)), B, K, d, r, V,
+                                    float(threshold), _ptr(conf), _ptr(cum), _ptr(vl))
+        if rc != 0:
+            raise ValueError("oracle confidence rejected its arguments")
+        return dict(conf=conf, cumprod=cum, verify_len=vl)
+
+    def topk(self, U, k: int = 16) -> dict:
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        cand = np.zeros((B, K, k), np.int32)
+        cval = np.zeros((B, K, k), np.float64)
+        margin = np.zeros((B, K), np.float64)
+        rc = self._lib.orc_topk(_ptr(U), B, K, V, k, _ptr(cand), _ptr(cval), _ptr(margin))
+        if rc != 0:
+            raise ValueError("oracle topk rejected its arguments")
+        return dict(cand=cand, cval=cval, margin=margin)
+
+    def pair_scores(self, cand, cval, A, Bt, anchors, *, V: int, H=None) -> np.ndarray:
+        cand = _c(cand, np.int32)
+        cval = _c(cval, np.float64)
+        A = _c(A, np.uint16)
+        Bt = _c(Bt, np.uint16)
+        anchors = _c(anchors, np.int32)
+        H = _c(H, np.float64)
+        B, K, k = cand.shape
+        r = A.shape[1]
+        S = np.zeros((B, K, k, k), np.float64)
+        rc = self._lib.orc_pair_scores(_ptr(cand), _ptr(cval), _ptr(A), _ptr(Bt), _ptr(anchors),
+                                     _ptr(H), B, K, V, r, k, _ptr(S))
+        if rc != 0:
+            raise ValueError("oracle pair_scores rejected its arguments")
+        return S
+
+    def walk(self, cand, S, *, temperature: float, seed: int, b0: int = 0, nb: Optional[int] = None,
+             forced=None) -> dict:
+        cand = _c(cand, np.int32)
+        S = _c(S, np.float64)
+        B, K, k = cand.shape
+        nb = B - b0 if nb is None else nb
+        forced = _c(forced, np.int32)
+        tokens = np.zeros((nb, K), np.int32)
+        logprobs = np.zeros((nb, K), np.float64)
+        margins = np.zeros((nb, K), np.float64)
+        flp = np.zeros((nb, K), np.float64) if forced is not None else None
+        rc = self._lib.orc_walk(_ptr(cand), _ptr(S), B, K, k, float(temperature), int(seed), b0, nb,
+                              _ptr(forced), _ptr(tokens), _ptr(logprobs), _ptr(margins), _ptr(flp))
+        if rc != 0:
+            raise ValueError("oracle walk rejected its arguments")
+        out = dict(tokens=tokens, logprobs=logprobs, margins=margins)
+        if forced is not None:
+            out["forced_logprobs"] = flp
+        return out
+
+
+def default() -> Oracle:
+    """The oracle built from this directory's C source (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+_default: Optional[Oracle] = None
+
+
+def __getattr__(name):
+    # module-level access (oracle.markov_draft, ...) goes to the default instance
+    if name.startswith("_"):
+        raise AttributeError(name)
+    return getattr(default(), name)

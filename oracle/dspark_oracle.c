@@ -1,0 +1,526 @@
+/*
+ * dspark_oracle.c -- plain, slow, fp64 CPU oracle of the DSpark Markov-head
+ * drafting hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library.  It shares no
+ * code, header, table or constant generator with the CUDA path.
+ *
+ * Every floating-point step is carried out in double precision from the exact
+ * widening of the bf16 weights and the fp32 base logits.  Loops follow the
+ * pages' definitions in their order; the only parallelism is OpenMP over
+ * independent vocabulary entries (or independent rows), which does not change
+ * any sum's order.
+ *
+ * Sources (each function names the passage it follows):
+ *  [EQV]  "DFlash-2's Selector and DSpark's Markov Head: An Equivalence
+ *         Observation" (jialefu.github.io)
+ *  [EXPL] "DSpark" explainer (himanshu-arora.com): sections "Semi-autoregressive
+ *         generation", "The Markov head", "Confidence-scheduled verification"
+ *  [FIX]  "DSpark: Repair the Joint, Meter the Verify" (stable-lab.github.io):
+ *         "Fix 1: A First-Order Markov Head", "Why the normalization has to be
+ *         local"
+ *  [VLLM] "DSpark" (vLLM speculators user guide): "Markov Head", "Confidence
+ *         Head", "Sample From Anchor", "Key Parameters"
+ *
+ * Readings where the pages are silent (the same readings the CUDA path takes):
+ *  - x_0 is the anchor token, so every position k = 0..K-1 gets a bias
+ *    ([EXPL] "Semi-autoregressive generation": the anchor is the first
+ *    prediction position; [VLLM] "Sample From Anchor").
+ *  - Temperature T > 0 samples softmax(l / T) by Gumbel-max, argmax(l/T + g);
+ *    T == 0 is greedy argmax(l).  The returned log-probability is that of the
+ *    drawn token under softmax(l / T') with T' = T (T > 0) or 1 (T == 0).
+ *  - Ties in any argmax or top-k order go to the smaller token id.
+ *  - Noise: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+ *    Numbers: As Easy as 1, 2, 3", SC'11), key = (seed low 32, seed high 32),
+ *    counter = (v >> 2, k, b, 0); word v & 3 of the output gives
+ *    u = ((word >> 9) + 0.5) * 2^-23, exactly representable in fp32 and fp64
+ *    and strictly inside (0, 1); g = -ln(-ln u).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* helpers                                                             */
+/* ------------------------------------------------------------------ */
+
+static double bf16_to_double(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int orc_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------ */
+/* Philox4x32-10, from its published definition (SC'11, section 3.2):  */
+/* each round multiplies words 0 and 2 by fixed odd constants, takes   */
+/* the high and low halves of the 64-bit products, and mixes the high  */
+/* halves with words 1/3 and the round key; the key is bumped by the   */
+/* Weyl constants (golden ratio, sqrt(3) - 1) between rounds.          */
+/* ------------------------------------------------------------------ */
+
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  const uint32_t mul0 = 0xD2511F53u, mul1 = 0xCD9E8D57u;
+  const uint32_t weyl0 = 0x9E3779B9u, weyl1 = 0xBB67AE85u;
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += weyl0;
+      k1 += weyl1;
+    }
+    uint64_t p0 = (uint64_t)mul0 * (uint64_t)x0;
+    uint64_t p1 = (uint64_t)mul1 * (uint64_t)x2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t y0 = hi1 ^ x1 ^ k0;
+    uint32_t y1 = lo1;
+    uint32_t y2 = hi0 ^ x3 ^ k1;
+    uint32_t y3 = lo0;
+    x0 = y0;
+    x1 = y1;
+    x2 = y2;
+    x3 = y3;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+/* u(seed, b, k, v) in (0, 1) with stream tag `tag` (0 = token sampling). */
+double orc_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t v, uint32_t tag) {
+  uint32_t ctr[4] = {v >> 2, k, b, tag};
+  uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  uint32_t word = out[v & 3u];
+  return ((double)(word >> 9) + 0.5) * (1.0 / 8388608.0); /* 2^-23 */
+}
+
+/* Standard Gumbel variate g = -ln(-ln u). */
+double orc_gumbel(uint64_t seed, uint32_t b, uint32_t k, uint32_t v) {
+  double u = orc_uniform(seed, b, k, v, 0u);
+  return -log(-log(u));
+}
+
+/* ------------------------------------------------------------------ */
+/* Gate H(h_t) = sigmoid(h_t . Wg) of the gated head.                   */
+/* [EQV] "What the two methods do" (Selector score, gate H(h_t)) and   */
+/* "The equivalence..." (gated Markov-head rule).  The pages leave the  */
+/* gate's form open; this build reads it as a linear map of the current */
+/* position's hidden state followed by a logistic sigmoid, no bias.     */
+/* h [M, d] bf16, Wg [d, r] bf16 -> H [M, r] fp64.                       */
+/* ------------------------------------------------------------------ */
+void orc_gate(const uint16_t* h, const uint16_t* Wg, int64_t M, int d, int r, double* H) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    double* acc = H + m * (int64_t)r;
+    for (int i = 0; i < r; ++i) acc[i] = 0.0;
+    for (int j = 0; j < d; ++j) {
+      double hj = bf16_to_double(h[m * (int64_t)d + j]);
+      const uint16_t* wrow = Wg + (int64_t)j * r;
+      for (int i = 0; i < r; ++i) acc[i] += hj * bf16_to_double(wrow[i]);
+    }
+    for (int i = 0; i < r; ++i) acc[i] = sigmoid(acc[i]);
+  }
+}
+
+/* ------------------------------------------------------------------ */
+/* One position of the Markov head.                                    */
+/* [EQV] "What the two methods do": logits_k = U_k + W1[a]^T W2 with   */
+/* a the previously sampled token; gated form logits_t = U_t +         */
+/* (W1[a] (.) H(h_t))^T W2.  [EXPL] "The Markov head": B(x_{k-1}, .) = */
+/* W1[x_{k-1}] W2.  [FIX] "Fix 1": the per-position distribution is    */
+/* the local softmax exp(z_k(v) + B(t_{k-1}, v)) / sum_u exp(...).      */
+/* Writes l[v] (calibrated logits) for v in [0, V).                     */
+/* ------------------------------------------------------------------ */
+static void calibrated_logits(const float* Urow, const uint16_t* W1, const uint16_t* W2,
+                              const double* Hrow, int V, int r, int32_t prev, double* e,
+                              double* l) {
+  for (int i = 0; i < r; ++i) {
+    double w1 = bf16_to_double(W1[(int64_t)prev * r + i]);
+    e[i] = Hrow ? w1 * Hrow[i] : w1;
+  }
+#pragma omp parallel
+  {
+#ifdef _OPENMP
+    int nt = omp_get_num_threads(), tid = omp_get_thread_num();
+#else
+    int nt = 1, tid = 0;
+#endif
+    int64_t chunk = ((int64_t)V + nt - 1) / nt;
+    int64_t v0 = (int64_t)tid * chunk, v1 = v0 + chunk;
+    if (v1 > V) v1 = V;
+    if (v0 < v1) {
+      /* bias[v] = sum_i e[i] * W2[i, v], summed over i = 0..r-1 in order */
+      for (int64_t v = v0; v < v1; ++v) l[v] = 0.0;
+      for (int i = 0; i < r; ++i) {
+        const uint16_t* w2row = W2 + (int64_t)i * V;
+        double ei = e[i];
+        for (int64_t v = v0; v < v1; ++v) l[v] += ei * bf16_to_double(w2row[v]);
+      }
+      for (int64_t v = v0; v < v1; ++v) l[v] = (double)Urow[v] + l[v];
+    }
+  }
+}
+
+/* log sum_v exp(l[v] / Tp), max-shifted. */
+static double log_sum_exp_scaled(const double* l, int V, double Tp) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double z = l[v] / Tp;
+    if (z > m) m = z;
+  }
+  if (m == -INFINITY) return -INFINITY;
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += exp(l[v] / Tp - m);
+  return m + log(s);
+}
+
+/* ------------------------------------------------------------------ */
+/* Markov-head draft over a block (vanilla, or gated when H != NULL).   */
+/* [EXPL] "Semi-autoregressive generation" + "The Markov head": the    */
+/* head samples left to right, x_0 = anchor, position k's logits get   */
+/* the bias of x_{k-1}.  [FIX] "Why the normalization has to be local": */
+/* the returned per-token log-probability is exact under the local     */
+/* softmax.  [VLLM] "Key Parameters": rank 0 disables the head.         */
+/*                                                                    */
+/* Inputs are full arrays indexed by the global request b: U [B,K,V],   */
+/* anchors [B], H [B,K,r] or NULL.  Requests b0 .. b0+nb-1 are run;     */
+/* outputs are compact [nb, K]:                                         */
+/*   tokens    oracle's own choice at each position                    */
+/*   logprobs  log-probability of that choice                           */
+/*   margins   s(best) - s(second best) of the perturbed scores        */
+/* If `forced` ([nb, K]) is given, the path continues on forced tokens  */
+/* (x_k = forced[k]) and forced_logprobs receives their log-probability. */
+/* Returns 0, or -1 on bad arguments / allocation failure.              */
+/* ------------------------------------------------------------------ */
+/* One request of the draft; buffers l, s ([V]) and e ([r]) are the caller's. */
+static int draft_one_request(const float* U, const uint16_t* W1, const uint16_t* W2,
+                             const int32_t* anchors, const double* H, int K, int V, int r,
+                             double temperature, uint64_t seed, int b, int bi,
+                             const int32_t* forced, int32_t* tokens, double* logprobs,
+                             double* margins, double* forced_logprobs, double* l, double* s,
+                             double* e) {
+  const double Tp = temperature > 0.0 ? temperature : 1.0;
+  int32_t prev = anchors[b];
+  for (int k = 0; k < K; ++k) {
+    const float* Urow = U + ((int64_t)b * K + k) * V;
+    const double* Hrow = H ? H + ((int64_t)b * K + k) * r : NULL;
+    if (prev < 0 || prev >= V) return -1;
+    calibrated_logits(Urow, W1, W2, Hrow, V, r, prev, e, l);
+    /* perturbed scores */
+    if (temperature > 0.0) {
+#pragma omp parallel for schedule(static)
+      for (int v = 0; v < V; ++v)
+        s[v] = l[v] / temperature + orc_gumbel(seed, (uint32_t)b, (uint32_t)k, (uint32_t)v);
+    } else {
+      for (int v = 0; v < V; ++v) s[v] = l[v];
+    }
+    /* argmax, ties to the smaller token id; runner-up for the margin */
+    int best = 0;
+    for (int v = 1; v < V; ++v)
+      if (s[v] > s[best]) best = v;
+    double second = -INFINITY;
+    for (int v = 0; v < V; ++v)
+      if (v != best && s[v] > second) second = s[v];
+    const double lse = log_sum_exp_scaled(l, V, Tp);
+    const int64_t o = (int64_t)bi * K + k;
+    tokens[o] = best;
+    logprobs[o] = l[best] / Tp - lse;
+    margins[o] = s[best] - second;
+    if (forced) {
+      const int32_t f = forced[o];
+      if (f < 0 || f >= V) return -1;
+      if (forced_logprobs) forced_logprobs[o] = l[f] / Tp - lse;
+      prev = f;
+    } else {
+      prev = best;
+    }
+  }
+  return 0;
+}
+
+int orc_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
+                     const int32_t* anchors, const double* H, int B, int K, int V, int r,
+                     double temperature, uint64_t seed, int b0, int nb, const int32_t* forced,
+                     int32_t* tokens, double* logprobs, double* margins,
+                     double* forced_logprobs) {
+  if (B <= 0 || K <= 0 || V <= 0 || r < 0 || b0 < 0 || nb < 0 || b0 + nb > B) return -1;
+  int bad = 0;
+  /* Many small requests: one request per thread (the per-request vocabulary
+     loops then run on that thread alone); otherwise requests run one after
+     the other with the vocabulary loops shared by all threads. */
+  const int per_request = nb >= 4 * orc_max_threads() && V <= 8192;
+#pragma omp parallel if (per_request) reduction(| : bad)
+  {
+    double* l = (double*)malloc(sizeof(double) * (size_t)V);
+    double* s = (double*)malloc(sizeof(double) * (size_t)V);
+    double* e = (double*)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+    if (!l || !s || !e) {
+      bad = 1;
+    } else {
+#pragma omp for schedule(static)
+      for (int bi = 0; bi < nb; ++bi) {
+        if (draft_one_request(U, W1, W2, anchors, H, K, V, r, temperature, seed, b0 + bi, bi,
+                              forced, tokens, logprobs, margins, forced_logprobs, l, s, e) != 0)
+          bad = 1;
+      }
+    }
+    free(l);
+    free(s);
+    free(e);
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Teacher-forced calibrated logits: the Markov-head rule with the      */
+/* predecessor of every position given ([EQV] per-candidate form        */
+/* logits_k(b | a) = U_k(b) + W1[a]^T W2[:, b]).                        */
+/* prev [B, K] holds x_0 .. x_{K-1}.  Rows b0 .. b0+nb-1; outputs       */
+/* compact: logits [nb, K, V] fp64, lse [nb, K] = log sum exp(l / T').  */
+/* ------------------------------------------------------------------ */
+int orc_markov_logits(const float* U, const uint16_t* W1, const uint16_t* W2,
+                      const int32_t* prev, const double* H, int B, int K, int V, int r,
+                      double temperature, int b0, int nb, double* logits, double* lse) {
+  if (B <= 0 || K <= 0 || V <= 0 || r < 0 || b0 < 0 || nb < 0 || b0 + nb > B) return -1;
+  double* e = (double*)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+  if (!e) return -1;
+  const double Tp = temperature > 0.0 ? temperature : 1.0;
+  for (int bi = 0; bi < nb; ++bi) {
+    const int b = b0 + bi;
+    for (int k = 0; k < K; ++k) {
+      const int32_t a = prev[(int64_t)b * K + k];
+      if (a < 0 || a >= V) {
+        free(e);
+        return -1;
+      }
+      double* l = logits + ((int64_t)bi * K + k) * V;
+      calibrated_logits(U + ((int64_t)b * K + k) * V, W1, W2,
+                        H ? H + ((int64_t)b * K + k) * r : NULL, V, r, a, e, l);
+      lse[(int64_t)bi * K + k] = log_sum_exp_scaled(l, V, Tp);
+    }
+  }
+  free(e);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Confidence head and prefix survival.                                 */
+/* [EXPL] "Confidence-scheduled verification": c_k = sigmoid(w^T [h_k;  */
+/* W1[x_{k-1}]]), prefix survival a_j = prod_{i<=j} c_i.  [VLLM]         */
+/* "Confidence Head": a linear head on the hidden state, concatenated    */
+/* with the previous-token Markov embedding when that option is set.    */
+/* A scalar bias is added (0 in the pages' equation).  verify_len[b] is  */
+/* the longest prefix whose survival stays >= threshold.                */
+/* h [B,K,d], W1 [V,r], anchors [B], tokens [B,K] (x_1..x_K), w [d(+r)]. */
+/* Outputs full [B,K] / [B].                                            */
+/* ------------------------------------------------------------------ */
+int orc_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors,
+                   const int32_t* tokens, const uint16_t* w, double bias, int with_markov,
+                   int B, int K, int d, int r, int V, double threshold, double* conf,
+                   double* cumprod, int32_t* verify_len) {
+  if (B <= 0 || K <= 0 || d < 0 || r < 0) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int b = 0; b < B; ++b) {
+    double surv = 1.0;
+    int len = 0, open = 1;
+    for (int k = 0; k < K; ++k) {
+      const int32_t prev = (k == 0) ? anchors[b] : tokens[(int64_t)b * K + k - 1];
+      double z = bias;
+      const uint16_t* hk = h + ((int64_t)b * K + k) * d;
+      for (int j = 0; j < d; ++j) z += bf16_to_double(w[j]) * bf16_to_double(hk[j]);
+      if (with_markov) {
+        if (prev < 0 || prev >= V) {
+          bad = 1;
+          break;
+        }
+        for (int i = 0; i < r; ++i)
+          z += bf16_to_double(w[d + i]) * bf16_to_double(W1[(int64_t)prev * r + i]);
+      }
+      const double c = sigmoid(z);
+      surv *= c;
+      conf[(int64_t)b * K + k] = c;
+      cumprod[(int64_t)b * K + k] = surv;
+      if (open && surv >= threshold) {
+        len = k + 1;
+      } else {
+        open = 0;
+      }
+    }
+    verify_len[b] = len;
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Top-k candidate sets of the base logits.                             */
+/* [EQV] "Where the parallelism comes from", choice 1: at each position */
+/* keep the top-16 tokens under the base logits U; "Two implications",  */
+/* 2: the same top-k truncation for a trained DSpark head.               */
+/* Order: U descending, ties to the smaller token id.  margin =          */
+/* U(k-th) - U((k+1)-th) (+inf when V == k).                             */
+/* U [B,K,V] -> cand [B,K,topk] int32, cval [B,K,topk], margin [B,K].    */
+/* ------------------------------------------------------------------ */
+int orc_topk(const float* U, int B, int K, int V, int topk, int32_t* cand, double* cval,
+             double* margin) {
+  if (B <= 0 || K <= 0 || V <= 0 || topk <= 0 || topk > V || topk > 64) return -1;
+#pragma omp parallel for schedule(dynamic)
+  for (int64_t row = 0; row < (int64_t)B * K; ++row) {
+    const float* u = U + row * V;
+    /* insertion into a sorted list of the topk+1 best (value desc, id asc) */
+    int32_t ids[65];
+    double vals[65];
+    int n = 0, cap = topk + 1;
+    for (int v = 0; v < V; ++v) {
+      double x = (double)u[v];
+      if (n == cap && !(x > vals[n - 1])) continue; /* equal value: larger id loses */
+      int p = (n < cap) ? n : cap - 1;
+      while (p > 0 && x > vals[p - 1]) {
+        if (p < cap) {
+          vals[p] = vals[p - 1];
+          ids[p] = ids[p - 1];
+        }
+        --p;
+      }
+      vals[p] = x;
+      ids[p] = v;
+      if (n < cap) ++n;
+    }
+    for (int j = 0; j < topk; ++j) {
+      cand[row * topk + j] = ids[j];
+      cval[row * topk + j] = vals[j];
+    }
+    margin[row] = (n > topk) ? vals[topk - 1] - vals[topk] : INFINITY;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Adjacent-pair score tables.                                          */
+/* [EQV] "What the two methods do": S_t(a, b) = U_t(b) + <A(a) (.)     */
+/* H(h_t), B(b)>; "Where the parallelism comes from", choice 2: all     */
+/* k x k predecessor/candidate pairs of adjacent positions.  H == NULL  */
+/* is the ungated form (H = 1).  Predecessor set of position 0 is the   */
+/* anchor alone; its row is replicated over all k rows.                  */
+/* S [B,K,topk,topk] fp64: S[b,t,i,j] = cval[b,t,j] + sum_q             */
+/* A[p_i][q] * H[b,t,q] * Bt[c_j][q].                                    */
+/* ------------------------------------------------------------------ */
+int orc_pair_scores(const int32_t* cand, const double* cval, const uint16_t* A,
+                    const uint16_t* Bt, const int32_t* anchors, const double* H, int B, int K,
+                    int V, int r, int topk, double* S) {
+  if (B <= 0 || K <= 0 || V <= 0 || r < 0 || topk <= 0) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int64_t bt = 0; bt < (int64_t)B * K; ++bt) {
+    const int b = (int)(bt / K), t = (int)(bt % K);
+    const double* Hrow = H ? H + bt * r : NULL;
+    for (int i = 0; i < topk; ++i) {
+      const int32_t p = (t == 0) ? anchors[b] : cand[(bt - 1) * topk + i];
+      for (int j = 0; j < topk; ++j) {
+        const int32_t c = cand[bt * topk + j];
+        if (p < 0 || p >= V || c < 0 || c >= V) {
+          bad = 1;
+          continue;
+        }
+        double acc = 0.0;
+        for (int q = 0; q < r; ++q) {
+          double aq = bf16_to_double(A[(int64_t)p * r + q]);
+          if (Hrow) aq *= Hrow[q];
+          acc += aq * bf16_to_double(Bt[(int64_t)c * r + q]);
+        }
+        S[(bt * topk + i) * topk + j] = cval[bt * topk + j] + acc;
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Light sequential walk over the pair tables.                          */
+/* [EQV] "Where the parallelism comes from": a greedy walk, or sampling, */
+/* over the precomputed scores; "Two implications", 2, step 3.  The     */
+/* sampling rule is the Markov head's own restricted to the candidates: */
+/* Gumbel noise keyed by the candidate's token id, so with k = V the    */
+/* walk is the full head; log-probabilities are under the k-way softmax.*/
+/* cand [B,K,topk], S [B,K,topk,topk] -> compact outputs [nb, K].       */
+/* forced ([nb,K], nullable): continue on these tokens (must be in the  */
+/* candidate set); forced_logprobs receives their log-probability.      */
+/* ------------------------------------------------------------------ */
+int orc_walk(const int32_t* cand, const double* S, int B, int K, int topk, double temperature,
+             uint64_t seed, int b0, int nb, const int32_t* forced, int32_t* tokens,
+             double* logprobs, double* margins, double* forced_logprobs) {
+  if (B <= 0 || K <= 0 || topk <= 0 || topk > 64 || b0 < 0 || nb < 0 || b0 + nb > B) return -1;
+  const double Tp = temperature > 0.0 ? temperature : 1.0;
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int bi = 0; bi < nb; ++bi) {
+    const int b = b0 + bi;
+    int slot = 0; /* predecessor slot; position 0's rows all hold the anchor */
+    for (int t = 0; t < K; ++t) {
+      const int64_t bt = (int64_t)b * K + t;
+      const double* row = S + (bt * topk + slot) * topk;
+      const int32_t* c = cand + bt * topk;
+      double sc[64];
+      for (int j = 0; j < topk; ++j)
+        sc[j] = (temperature > 0.0)
+                    ? row[j] / temperature + orc_gumbel(seed, (uint32_t)b, (uint32_t)t, (uint32_t)c[j])
+                    : row[j];
+      int best = 0;
+      for (int j = 1; j < topk; ++j)
+        if (sc[j] > sc[best] || (sc[j] == sc[best] && c[j] < c[best])) best = j;
+      double second = -INFINITY;
+      for (int j = 0; j < topk; ++j)
+        if (j != best && sc[j] > second) second = sc[j];
+      double m = -INFINITY;
+      for (int j = 0; j < topk; ++j)
+        if (row[j] / Tp > m) m = row[j] / Tp;
+      double ssum = 0.0;
+      for (int j = 0; j < topk; ++j) ssum += exp(row[j] / Tp - m);
+      const double lse = m + log(ssum);
+      const int64_t o = (int64_t)bi * K + t;
+      tokens[o] = c[best];
+      logprobs[o] = row[best] / Tp - lse;
+      margins[o] = sc[best] - second;
+      int next = best;
+      if (forced) {
+        next = -1;
+        for (int j = 0; j < topk; ++j)
+          if (c[j] == forced[o]) next = j;
+        if (next < 0) {
+          bad = 1;
+          break;
+        }
+        if (forced_logprobs) forced_logprobs[o] = row[next] / Tp - lse;
+      }
+      slot = next;
+    }
+  }
+  return bad ? -1 : 0;
+}

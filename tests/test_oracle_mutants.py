@@ -1,0 +1,95 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each case copies the oracle's C source to a temporary directory, plants one
+plausible mistake (a dropped term, a wrong sign, a wrong index, a transposed
+operand, a wrong tie-break), compiles it with gcc and runs the pin that should
+catch it against the mutant.  The pins are only worth trusting if every mutant
+fails at least one of them.  Nothing here touches a GPU.
+"""
+
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import tests.test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "dspark_oracle.c")
+
+MUTANTS = [
+    # (name, original text, planted text, pins expected to catch it)
+    ("predecessor-not-carried", "      prev = best;\n", "      prev = anchors[b];\n",
+     ["test_sampler_matches_exhaustive_joint", "test_greedy_is_argmax_of_calibrated_logits"]),
+    ("gumbel-sign", "return -log(-log(u));", "return log(-log(u));",
+     ["test_uniform_grid_and_word_selection", "test_sampler_matches_exhaustive_joint"]),
+    ("w2-transposed", "l[v] += ei * bf16_to_double(w2row[v]);",
+     "l[v] += ei * bf16_to_double(W2[(int64_t)v * r + i]);",
+     ["test_teacher_forced_logits_match_numpy"]),
+    ("philox-9-rounds", "round < 10; ++round", "round < 9; ++round",
+     ["test_philox_known_answers"]),
+    ("logprob-without-temperature", "logprobs[o] = l[best] / Tp - lse;",
+     "logprobs[o] = l[best] - lse;", ["test_temperature_scales_the_sampled_softmax"]),
+    ("bias-dropped", "l[v] = (double)Urow[v] + l[v];", "l[v] = (double)Urow[v];",
+     ["test_teacher_forced_logits_match_numpy", "test_np_torch_worked_example"]),
+    ("topk-ties-to-larger-id", "while (p > 0 && x > vals[p - 1])",
+     "while (p > 0 && x >= vals[p - 1])", ["test_topk_matches_lexsort"]),
+    ("pair-predecessor-same-position", "cand[(bt - 1) * topk + i]", "cand[bt * topk + i]",
+     ["test_pair_scores_match_numpy", "test_walk_with_k_equal_V_is_the_full_head"]),
+    ("confidence-uses-current-token", "tokens[(int64_t)b * K + k - 1]", "tokens[(int64_t)b * K + k]",
+     ["test_confidence_closed_form"]),
+    ("gate-without-sigmoid", "for (int i = 0; i < r; ++i) acc[i] = sigmoid(acc[i]);", "",
+     ["test_gate_matches_numpy"]),
+    ("walk-slot-not-carried", "      slot = next;\n", "      slot = 0;\n",
+     ["test_walk_with_k_equal_V_is_the_full_head"]),
+    ("uniform-offset", "+ 0.5) * (1.0 / 8388608.0)", "+ 1.0) * (1.0 / 8388608.0)",
+     ["test_uniform_grid_and_word_selection"]),
+]
+
+
+def _compile(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found in the oracle source"
+    mutated = src.replace(old, new)
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"lib{name}.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                    "-ffp-contract=off", "-o", str(so), str(c), "-lm"], check=True)
+    return oracle.Oracle(str(so))
+
+
+def _run_pin(fn_name, orc):
+    fn = getattr(pins, fn_name)
+    marks = getattr(fn, "pytestmark", [])
+    params = [m for m in marks if m.name == "parametrize"]
+    combos = [{}]
+    for m in params:
+        names = [n.strip() for n in m.args[0].split(",")]
+        new = []
+        for c in combos:
+            for val in m.args[1]:
+                vals = val if len(names) > 1 else (val,)
+                new.append({**c, **dict(zip(names, vals))})
+        combos = new
+    for kw in combos:
+        fn(orc, **kw)
+
+
+@pytest.mark.parametrize("name,old,new,catchers", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, catchers):
+    mutant = _compile(tmp_path, name, old, new)
+    caught = []
+    for pin in catchers:
+        try:
+            _run_pin(pin, mutant)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin)
+    assert caught, f"planted mistake '{name}' passed every pin in {catchers}"
+
+
+def test_unmutated_source_passes_the_same_pins(tmp_path):
+    clean = _compile(tmp_path, "clean", "dspark_oracle", "dspark_oracle")
+    for *_, catchers in MUTANTS:
+        for pin in catchers:
+            _run_pin(pin, clean)

@@ -1,0 +1,353 @@
+"""Pins of the fp64 oracle against what the DSpark pages and the mathematics fix.
+
+None of these tests retypes the oracle's loops: each compares the oracle with
+a printed value (tests/golden), a known-answer vector, a closed form evaluated
+by an independent library routine (numpy/scipy), an exact special case the
+pages state, or an exhaustive enumeration of the sampled distribution.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+from synth import bf16_bits, bf16_to_f32, make_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f64(bits):
+    return bf16_to_f32(bits).astype(np.float64)
+
+
+def small_inputs(seed, B, K, V, r, std=0.02, d=0, **kw):
+    return make_inputs(seed, B, K, V, r, d=d, weight_std=std, **kw)
+
+
+# --------------------------------------------------------------------------- RNG
+def test_philox_known_answers(orc):
+    kat = json.load(open(os.path.join(GOLDEN, "philox4x32_10_kat.json")))
+    for vec in kat["vectors"]:
+        ctr = [int(x, 16) for x in vec["ctr"]]
+        key = [int(x, 16) for x in vec["key"]]
+        out = [int(x, 16) for x in vec["out"]]
+        assert list(orc.philox4x32_10(ctr, key)) == out
+
+
+def test_uniform_grid_and_word_selection(orc):
+    seed = 0x1234_5678_9ABC_DEF0
+    for (b, k, v) in [(0, 0, 0), (3, 7, 5), (127, 15, 151935), (1, 2, 4)]:
+        out = orc.philox4x32_10([v >> 2, k, b, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        u = orc.uniform(seed, b, k, v)
+        # u = (2 * (word >> 9) + 1) * 2^-24: an odd multiple of 2^-24, strictly inside (0, 1)
+        assert u == ((int(out[v & 3]) >> 9) * 2 + 1) * 2.0 ** -24
+        assert 0.0 < u < 1.0
+        assert np.float32(u) == u  # exactly representable in fp32
+        assert orc.gumbel(seed, b, k, v) == -np.log(-np.log(u))
+
+
+def test_uniform_is_uniform(orc):
+    us = np.array([orc.uniform(7, b, 3, v) for b in range(20) for v in range(2000)])
+    counts, _ = np.histogram(us, bins=50, range=(0, 1))
+    assert stats.chisquare(counts).pvalue > 1e-3
+    # neighbouring words of one block and neighbouring requests are uncorrelated
+    assert abs(np.corrcoef(us[:-1], us[1:])[0, 1]) < 0.02
+
+
+# ------------------------------------------------------------------- closed forms
+def test_rank_zero_reproduces_base_logits_exactly(orc):
+    """--markov-rank 0 disables the head, leaving the base logits (vLLM guide, "Markov Head")."""
+    inp = small_inputs(1, 3, 4, 200, 16)
+    prev = np.random.default_rng(0).integers(0, 200, size=(3, 4)).astype(np.int32)
+    out = orc.markov_logits(inp.U, None, None, prev, temperature=1.0)
+    assert np.array_equal(out["logits"], inp.U.astype(np.float64))
+    assert np.allclose(out["lse"], special.logsumexp(inp.U.astype(np.float64), axis=-1),
+                       rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("T", [1.0, 0.7, 0.0])
+def test_teacher_forced_logits_match_numpy(orc, gated, T):
+    """logits_k = U_k + (W1[a] (.) H)^T W2 (equivalence page, Markov-head and gated rules)."""
+    B, K, V, r, d = 3, 5, 96, 32, 24
+    inp = small_inputs(2, B, K, V, r, std=0.3, d=d, gated=gated)
+    prev = np.random.default_rng(1).integers(0, V, size=(B, K)).astype(np.int32)
+    H = orc.gate(inp.h, inp.Wg) if gated else None
+    out = orc.markov_logits(inp.U, inp.W1, inp.W2, prev, temperature=T, H=H)
+    e = f64(inp.W1)[prev]  # [B, K, r]
+    if gated:
+        e = e * special.expit(np.einsum("bkd,dr->bkr", f64(inp.h), f64(inp.Wg)))
+    ref = inp.U.astype(np.float64) + e @ f64(inp.W2)
+    assert np.allclose(out["logits"], ref, rtol=1e-13, atol=1e-12)
+    Tp = T if T > 0 else 1.0
+    assert np.allclose(out["lse"], special.logsumexp(ref / Tp, axis=-1), rtol=0, atol=1e-12)
+    # local normalisation: the per-position distribution sums to one
+    p = np.exp(out["logits"] / Tp - out["lse"][..., None])
+    assert np.allclose(p.sum(-1), 1.0, atol=1e-12)
+
+
+def test_teacher_forced_subset_rows(orc):
+    inp = small_inputs(3, 5, 3, 64, 16, std=0.3)
+    prev = np.random.default_rng(2).integers(0, 64, size=(5, 3)).astype(np.int32)
+    full = orc.markov_logits(inp.U, inp.W1, inp.W2, prev)
+    part = orc.markov_logits(inp.U, inp.W1, inp.W2, prev, b0=2, nb=2)
+    assert np.array_equal(part["logits"], full["logits"][2:4])
+    assert np.array_equal(part["lse"], full["lse"][2:4])
+
+
+def test_gate_matches_numpy(orc):
+    inp = small_inputs(4, 2, 3, 16, 32, d=40, gated=True)
+    H = orc.gate(inp.h, inp.Wg)
+    ref = special.expit(np.einsum("bkd,dr->bkr", f64(inp.h), f64(inp.Wg)))
+    assert np.allclose(H, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_gated_head_with_unit_gate_equals_vanilla(orc):
+    """H = 1 turns the gated rule into the vanilla Markov head (equivalence page)."""
+    B, K, V, r, d = 4, 5, 128, 32, 16
+    inp = small_inputs(5, B, K, V, r, std=0.3)
+    h = np.full((B, K, d), 0x3F80, np.uint16)        # 1.0
+    Wg = np.full((d, r), 0x4080, np.uint16)          # 4.0 -> h.Wg = 64, sigmoid == 1.0 in fp64
+    H = orc.gate(h, Wg)
+    assert np.all(H == 1.0)
+    for T in (1.0, 0.0):
+        a = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=T, seed=3)
+        g = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=T, seed=3, H=H)
+        for key in ("tokens", "logprobs", "margins"):
+            assert np.array_equal(a[key], g[key])
+
+
+# ----------------------------------------------------------------- sampling rule
+def _replicate(inp, n):
+    U = np.ascontiguousarray(np.broadcast_to(inp.U[:1], (n,) + inp.U.shape[1:]))
+    anchors = np.full(n, inp.anchors[0], np.int32)
+    return U, anchors
+
+
+def _chi2_pvalue(counts, expected):
+    small = expected < 5
+    obs = np.concatenate([counts[~small], [counts[small].sum()]]) if small.any() else counts
+    exp = np.concatenate([expected[~small], [expected[small].sum()]]) if small.any() else expected
+    keep = exp > 0
+    return stats.chisquare(obs[keep], exp[keep]).pvalue
+
+
+def test_sampler_matches_exhaustive_joint(orc):
+    """Empirical joint of 10^6 draws vs prod_k softmax(U_k + W1[x_{k-1}] W2) over all V^K paths."""
+    V, K, r, N = 8, 3, 8, 1_000_000
+    rng = np.random.default_rng(11)
+    U1 = rng.standard_normal((1, K, V)).astype(np.float32)
+    W1 = bf16_bits(rng.normal(0, 0.5, (V, r)).astype(np.float32))
+    W2 = bf16_bits(rng.normal(0, 0.5, (r, V)).astype(np.float32))
+    anchor = 5
+    U = np.ascontiguousarray(np.broadcast_to(U1, (N, K, V)))
+    anchors = np.full(N, anchor, np.int32)
+    out = orc.markov_draft(U, W1, W2, anchors, temperature=1.0, seed=2024)
+    paths = out["tokens"].astype(np.int64)
+    cell = (paths[:, 0] * V + paths[:, 1]) * V + paths[:, 2]
+    counts = np.bincount(cell, minlength=V ** K).astype(np.float64)
+    # exhaustive joint, with numpy softmax rows per predecessor
+    bias = f64(W1) @ f64(W2)                       # [V(prev), V]
+    P = np.zeros((V,) * K)
+    for x1 in range(V):
+        p1 = special.softmax(U1[0, 0] + bias[anchor])[x1]
+        for x2 in range(V):
+            p2 = special.softmax(U1[0, 1] + bias[x1])[x2]
+            p3 = special.softmax(U1[0, 2] + bias[x2])
+            P[x1, x2, :] = p1 * p2 * p3
+    assert abs(P.sum() - 1) < 1e-12
+    assert _chi2_pvalue(counts, P.reshape(-1) * N) > 0.01
+    # the log-probabilities returned with each draw are the exact conditionals
+    sel = slice(0, 2000)
+    joint_lp = out["logprobs"][sel].sum(1)
+    assert np.allclose(joint_lp, np.log(P.reshape(-1)[cell[sel]]), atol=1e-10)
+
+
+def test_temperature_scales_the_sampled_softmax(orc):
+    V, N, T = 16, 200_000, 0.5
+    rng = np.random.default_rng(12)
+    U1 = (rng.standard_normal((1, 1, V)) * 0.8).astype(np.float32)
+    U = np.ascontiguousarray(np.broadcast_to(U1, (N, 1, V)))
+    out = orc.markov_draft(U, None, None, np.zeros(N, np.int32), temperature=T, seed=99)
+    counts = np.bincount(out["tokens"][:, 0], minlength=V).astype(np.float64)
+    p = special.softmax(U1[0, 0].astype(np.float64) / T)
+    assert _chi2_pvalue(counts, p * N) > 0.01
+    assert np.allclose(out["logprobs"][:, 0], np.log(p[out["tokens"][:, 0]]), atol=1e-12)
+
+
+def test_greedy_is_argmax_of_calibrated_logits(orc):
+    inp = small_inputs(6, 3, 6, 256, 32, std=0.3)
+    out = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=0.0, seed=0)
+    prev = np.concatenate([inp.anchors[:, None], out["tokens"][:, :-1]], axis=1)
+    logits = inp.U.astype(np.float64) + f64(inp.W1)[prev] @ f64(inp.W2)
+    assert np.array_equal(out["tokens"], logits.argmax(-1))
+    srt = np.sort(logits, axis=-1)
+    assert np.allclose(out["margins"], srt[..., -1] - srt[..., -2], atol=1e-12)
+    assert np.allclose(out["logprobs"], logits.max(-1) - special.logsumexp(logits, -1),
+                       atol=1e-12)
+
+
+def test_forced_continuation_on_own_tokens_is_identity(orc):
+    inp = small_inputs(7, 4, 5, 128, 16, std=0.3)
+    a = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=5)
+    f = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=5,
+                         forced=a["tokens"])
+    assert np.array_equal(a["tokens"], f["tokens"])
+    assert np.array_equal(a["logprobs"], f["forced_logprobs"])
+    part = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=5,
+                            b0=1, nb=2)
+    assert np.array_equal(part["tokens"], a["tokens"][1:3])
+
+
+def test_np_torch_worked_example(orc):
+    """The np/torch tables: product of marginals without the head, the true joint with it."""
+    gold = json.load(open(os.path.join(GOLDEN, "np_torch_tables.json")))
+    NP, TORCH, ARRAY, TENSOR, PREFIX = 0, 1, 2, 3, 4
+    V, K, N = 5, 2, 20000
+    U1 = np.full((1, K, V), -30.0, np.float32)
+    U1[0, 0, [NP, TORCH]] = 0.0
+    U1[0, 1, [ARRAY, TENSOR]] = 0.0
+    U = np.ascontiguousarray(np.broadcast_to(U1, (N, K, V)))
+    anchors = np.full(N, PREFIX, np.int32)
+
+    def table(out):
+        t = np.zeros((2, 2))
+        for x1, x2 in out["tokens"]:
+            t[int(x1) - NP, int(x2) - ARRAY] += 1
+        return t / N
+
+    # mean-field (rank 0): every cell is the product of the two marginals
+    mf = orc.markov_draft(U, None, None, anchors, temperature=1.0, seed=1)
+    assert np.all(np.abs(table(mf) - np.array(gold["product_of_marginals"])) < 0.015)
+    lp = mf["logprobs"].sum(1)
+    assert np.allclose(np.exp(lp), gold["product_of_marginals"][0][0], atol=1e-9)
+
+    # Markov head with a rank-2 coupling: np -> .array, torch -> .tensor
+    r = 2
+    W1 = np.zeros((V, r), np.float32)
+    W1[NP] = (1, 0)
+    W1[TORCH] = (0, 1)
+    W2 = np.zeros((r, V), np.float32)
+    W2[:, ARRAY] = (0, -30)
+    W2[:, TENSOR] = (-30, 0)
+    mk = orc.markov_draft(U, bf16_bits(W1), bf16_bits(W2), anchors, temperature=1.0, seed=1)
+    t = table(mk)
+    joint = np.array(gold["true_joint"])
+    assert np.all(t[joint == 0] == 0)
+    assert np.all(np.abs(t - joint) < 0.015)
+    assert np.allclose(t.sum(1), gold["true_margins_rows"], atol=0.015)
+    assert np.allclose(t.sum(0), gold["true_margins_cols"], atol=0.015)
+    assert np.allclose(np.exp(mk["logprobs"].sum(1)), 0.5, atol=1e-9)
+
+
+# ----------------------------------------------------------------------- selector
+def test_topk_matches_lexsort(orc):
+    rng = np.random.default_rng(8)
+    U = np.round(rng.standard_normal((3, 4, 300)) * 2).astype(np.float32)  # many exact ties
+    for k in (1, 16, 32):
+        out = orc.topk(U, k)
+        for b in range(3):
+            for t in range(4):
+                order = np.lexsort((np.arange(300), -U[b, t].astype(np.float64)))
+                assert np.array_equal(out["cand"][b, t], order[:k])
+                assert np.array_equal(out["cval"][b, t], U[b, t, order[:k]])
+                assert out["margin"][b, t] == U[b, t, order[k - 1]] - U[b, t, order[k]]
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_pair_scores_match_numpy(orc, gated):
+    B, K, V, r, d, k = 2, 4, 300, 32, 24, 16
+    inp = small_inputs(9, B, K, V, r, std=0.3, d=d, gated=gated, selector=True)
+    top = orc.topk(inp.U, k)
+    H = orc.gate(inp.h, inp.Wg) if gated else None
+    S = orc.pair_scores(top["cand"], top["cval"], inp.A, inp.Bt, inp.anchors, V=V, H=H)
+    prev = np.concatenate([np.repeat(inp.anchors[:, None, None], k, axis=2),
+                           top["cand"][:, :-1]], axis=1)        # [B, K, k]
+    Ap = f64(inp.A)[prev]                                        # [B, K, k, r]
+    if gated:
+        Ap = Ap * H[:, :, None, :]
+    Bc = f64(inp.Bt)[top["cand"]]                                # [B, K, k, r]
+    ref = top["cval"][:, :, None, :] + np.einsum("btiq,btjq->btij", Ap, Bc)
+    assert np.allclose(S, ref, rtol=1e-13, atol=1e-12)
+
+
+def test_walk_with_k_equal_V_is_the_full_head(orc):
+    """Top-k execution with k = V recovers the Markov head exactly (equivalence page)."""
+    B, K, V, r = 64, 6, 32, 16
+    inp = small_inputs(10, B, K, V, r, std=0.4)
+    A, Bt = inp.W1, np.ascontiguousarray(inp.W2.T)
+    top = orc.topk(inp.U, V)
+    S = orc.pair_scores(top["cand"], top["cval"], A, Bt, inp.anchors, V=V)
+    for T in (1.0, 0.7, 0.0):
+        full = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=T, seed=21)
+        wk = orc.walk(top["cand"], S, temperature=T, seed=21)
+        assert np.array_equal(full["tokens"], wk["tokens"])
+        assert np.allclose(full["logprobs"], wk["logprobs"], atol=1e-12)
+
+
+def test_walk_top16_is_the_masked_full_head(orc):
+    """k = 16: the walk equals the full head with logits -inf outside each candidate set."""
+    B, K, V, r, k = 64, 6, 200, 16, 16
+    inp = small_inputs(12, B, K, V, r, std=0.4)
+    top = orc.topk(inp.U, k)
+    S = orc.pair_scores(top["cand"], top["cval"], inp.W1, np.ascontiguousarray(inp.W2.T),
+                        inp.anchors, V=V)
+    Um = np.full_like(inp.U, -np.inf)
+    np.put_along_axis(Um, top["cand"], np.take_along_axis(inp.U, top["cand"], -1), -1)
+    for T in (1.0, 0.0):
+        full = orc.markov_draft(Um, inp.W1, inp.W2, inp.anchors, temperature=T, seed=4)
+        wk = orc.walk(top["cand"], S, temperature=T, seed=4)
+        assert np.array_equal(full["tokens"], wk["tokens"])
+        assert np.allclose(full["logprobs"], wk["logprobs"], atol=1e-12)
+        assert np.all(np.isin(wk["tokens"], top["cand"].reshape(B, -1)))
+
+
+def test_walk_forced_continuation(orc):
+    B, K, V, r, k = 8, 5, 200, 16, 16
+    inp = small_inputs(13, B, K, V, r, std=0.4, selector=True)
+    top = orc.topk(inp.U, k)
+    S = orc.pair_scores(top["cand"], top["cval"], inp.A, inp.Bt, inp.anchors, V=V)
+    a = orc.walk(top["cand"], S, temperature=1.0, seed=8)
+    f = orc.walk(top["cand"], S, temperature=1.0, seed=8, forced=a["tokens"])
+    assert np.array_equal(a["tokens"], f["tokens"])
+    assert np.array_equal(a["logprobs"], f["forced_logprobs"])
+
+
+# --------------------------------------------------------------------- confidence
+@pytest.mark.parametrize("with_markov", [True, False])
+def test_confidence_closed_form(orc, with_markov):
+    B, K, V, r, d = 5, 7, 64, 16, 32
+    inp = small_inputs(14, B, K, V, r, d=d, confidence=True)
+    w = inp.w_conf if with_markov else inp.w_conf[:d]
+    tokens = np.random.default_rng(3).integers(0, V, size=(B, K)).astype(np.int32)
+    out = orc.confidence(inp.h, inp.W1, inp.anchors, tokens, w, bias=0.25,
+                         with_markov=with_markov, threshold=0.3, V=V)
+    prev = np.concatenate([inp.anchors[:, None], tokens[:, :-1]], axis=1)
+    z = np.einsum("bkd,d->bk", f64(inp.h), f64(w[:d])) + 0.25
+    if with_markov:
+        z = z + f64(inp.W1)[prev] @ f64(inp.w_conf[d:])
+    c = special.expit(z)
+    assert np.allclose(out["conf"], c, rtol=1e-13, atol=1e-15)
+    assert np.allclose(out["cumprod"], np.cumprod(c, axis=1), rtol=1e-13)
+    assert np.all(np.diff(out["cumprod"], axis=1) <= 0)        # survival never grows
+    assert np.array_equal(out["verify_len"], (np.cumprod(c, axis=1) >= 0.3).sum(1))
+
+
+def test_confidence_threshold_extremes_and_monotonicity(orc):
+    B, K, V, r, d = 6, 9, 64, 16, 32
+    inp = small_inputs(15, B, K, V, r, d=d, confidence=True)
+    tokens = np.random.default_rng(4).integers(0, V, size=(B, K)).astype(np.int32)
+    lens = []
+    for th in (0.0, 0.05, 0.1, 0.3, 0.6, 0.9, 1.0 + 1e-9):
+        out = orc.confidence(inp.h, inp.W1, inp.anchors, tokens, inp.w_conf, threshold=th, V=V)
+        lens.append(out["verify_len"])
+    assert np.all(lens[0] == K)          # threshold 0: verify the whole block
+    assert np.all(lens[-1] == 0)         # threshold above 1: verify nothing
+    assert np.all(np.diff(np.stack(lens), axis=0) <= 0)
+
+
+def test_head_parameter_count():
+    """2 * V * r = 77.8M parameters for a 151936-token vocabulary at rank 256 (explainer's ablation)."""
+    assert 2 * 151936 * 256 == 77_791_232
