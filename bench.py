@@ -1,0 +1,488 @@
+"""Benchmark of the DSpark Markov-head draft hot path on GB300.
+
+One step = one draft block for one batch: the fused Markov-head draft with the
+confidence head over B = 128 requests, K = 16 positions, V = 151936, r = 256
+(d = 2048, survival threshold 0.3, T = 1.0), i.e. every sampled token, its
+log-probability, the confidence values, survival products and verify lengths.
+
+Printed (rank 0, one JSON line): draft tokens/s for the whole job (value),
+device-timed with CUDA events over the draft kernel with inputs resident in
+HBM and the L2 flushed between steps; the same metric end to end (e2e)
+through the binding with host buffers (pinned host -> device copies of the
+step's inputs and device -> host copies of its outputs inside the timed
+region); the roofline of the draft kernel against the measured HBM peak; SM
+clocks sampled during the timed region; and the fp64 CPU oracle timed on a
+bounded sample of the same workload (cpu_baseline).
+
+``--impl reference`` times that oracle alone, per step one bounded sample of
+the workload, on the host cores (rank 0 only under torchrun).
+Multi-GPU: independent replicas, each rank drafts its own batch (weak scaling,
+no collective on the data path; the only collectives are the timing barrier
+and the max over ranks).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Markov-head draft tokens/s at B=128 K=16 V=151936; % of HBM roofline"
+L2_FLUSH_BYTES = 512 << 20       # larger than the 129 MB L2
+CONF_THRESHOLD = 0.3
+
+WORKLOADS = {
+    # name: (config index, description)
+    "serving": (2, "serving batch + confidence: B=128 K=16 V=151936 r=256 d=2048 T=1.0"),
+    "single": (1, "single request: B=1 K=16 V=151936 r=256 T=1.0"),
+    "gated": (3, "gated head: B=64 K=16 V=151936 r=256 d=4096 T=1.0"),
+    "selector": (4, "selector top-16 (gated): B=256 K=16 V=151936 r=256 d=4096 T=1.0"),
+    "tiny": (0, "tiny: B=1 K=4 V=4096 r=256 T=1.0"),
+}
+
+
+def algorithmic_bytes(cfg: int, c: dict) -> int:
+    """Bytes the step must move at least once per position (W2 + U + gathers [+ h, Wg])."""
+    B, K, V, r = c["B"], c["K"], c["V"], c["r"]
+    if cfg == 4:
+        d = c["d"]
+        # U scan + 32 gathered rows of A/B per (b, t) + candidate ids and score tables
+        # written + the gate's h and Wg
+        return (B * K * V * 4 + 2 * B * K * 16 * r * 2 + B * K * (16 * 4 + 16 * 16 * 4)
+                + B * K * d * 2 + d * r * 2)
+    per_step = r * V * 2 + B * V * 4 + B * r * 2
+    total = K * per_step
+    if c.get("confidence"):
+        total += B * K * c["d"] * 2
+    if c.get("gated"):
+        total += B * K * c["d"] * 2 + c["d"] * r * 2
+    return total
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="serving")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_seed(rank: int, step: int) -> int:
+    """Independent replicas draw independent samples: the Philox key differs per rank."""
+    return (rank << 32) | step
+
+
+def job_throughput(tokens_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank drafts its own batch; the slowest rank sets the time."""
+    return world * tokens_per_rank_step * steps / (max_ms / 1000.0)
+
+
+def gpu_id(dev) -> str:
+    """nvidia-smi -i selector of a torch device (its UUID when torch reports one)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("draft.cu", "sm103.cuh", "philox.cuh", "confidence.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "rank_markov_draft_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the draft kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"draft_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(inp, c, n_requests, b0=0, temperature=1.0, seed=0):
+    """Run the fp64 oracle on requests b0 .. b0+n-1 of the workload; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    out = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=temperature,
+                              seed=seed, b0=b0, nb=n_requests)
+    if c.get("confidence"):
+        B = inp.U.shape[0]
+        toks = np.zeros((B, c["K"]), np.int32)
+        toks[b0:b0 + n_requests] = out["tokens"]
+        sl = slice(b0, b0 + n_requests)
+        oracle.confidence(inp.h[sl], inp.W1, inp.anchors[sl], toks[sl], inp.w_conf,
+                          threshold=CONF_THRESHOLD)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, c, target_s):
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    K = c["K"]
+    done, spent = 0, 0.0
+    while spent < target_s and done < c["B"]:
+        spent += oracle_sample(inp, c, 1, b0=done)
+        done += 1
+    return {"value": done * K / spent, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of {c['B']} requests x {K} positions of the same workload "
+                      f"(fp64 oracle, {threads} OpenMP threads, {spent:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: per step one request of the workload."""
+    from synth import CONFIGS, config_inputs
+    cfg, desc = WORKLOADS[args.workload]
+    c = dict(CONFIGS[cfg])
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = config_inputs(cfg)
+    K = c["K"]
+    for i in range(args.warmup):
+        oracle_sample(inp, c, 1, b0=i % c["B"])
+    spent = 0.0
+    for i in range(args.steps):
+        spent += oracle_sample(inp, c, 1, b0=(args.warmup + i) % c["B"])
+    value = args.steps * K / spent
+    threads = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * spent / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "B": c["B"], "K": K, "V": c["V"], "r": c["r"],
+                   "sample_per_step": "1 request x K positions"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} steps x 1 request x {K} positions"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank, world, local):
+    import torch
+    from rank_markov_draft_gb300 import binding
+    from synth import CONFIGS, config_inputs
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    cfg, desc = WORKLOADS[args.workload]
+    c = dict(CONFIGS[cfg])
+    B, K, V, r = c["B"], c["K"], c["V"], c["r"]
+    T = 1.0
+    inp = config_inputs(cfg)
+
+    def up(a, bf=False):
+        a = np.ascontiguousarray(a)
+        if bf:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    ctx = binding.Context(local, B_max=max(B, 1), V_max=V, K_max=K)
+    stream = torch.cuda.current_stream(dev)
+    U = up(inp.U)
+    anchors = up(inp.anchors)
+    if cfg == 4:
+        A, Bt, h, Wg = up(inp.A, True), up(inp.Bt, True), up(inp.h, True), up(inp.Wg, True)
+        cand = torch.empty(B, K, 16, dtype=torch.int32, device=dev)
+        cval = torch.empty(B, K, 16, dtype=torch.float32, device=dev)
+        scores = torch.empty(B, K, 16, 16, dtype=torch.float32, device=dev)
+        tokens = torch.empty(B, K, dtype=torch.int32, device=dev)
+        logprobs = torch.empty(B, K, dtype=torch.float32, device=dev)
+
+        def step(seed):
+            binding.dspark_selector_scores(ctx, U, A, Bt, anchors, h, Wg, c["d"], B, K, V, r, 16,
+                                           cand, cval, scores, stream)
+            n = ctx.last_launches
+            binding.dspark_selector_walk(ctx, cand, scores, anchors, A, B, K, V, r, 16, T, seed,
+                                         tokens, logprobs, None, stream)
+            return n + ctx.last_launches
+    else:
+        W1, W2 = up(inp.W1, True), up(inp.W2, True)
+        tokens = torch.empty(B, K, dtype=torch.int32, device=dev)
+        logprobs = torch.empty(B, K, dtype=torch.float32, device=dev)
+        conf = None
+        if c.get("confidence"):
+            conf = binding.Confidence(h=up(inp.h, True), w=up(inp.w_conf, True), bias=0.0,
+                                      threshold=CONF_THRESHOLD).allocate(B, K)
+        h = up(inp.h, True) if c.get("gated") else None
+        Wg = up(inp.Wg, True) if c.get("gated") else None
+
+        def step(seed):
+            if h is None:
+                binding.dspark_markov_draft(ctx, U, W1, W2, anchors, B, K, V, r, T, seed, tokens,
+                                            logprobs, conf, stream)
+            else:
+                binding.dspark_gated_draft(ctx, U, W1, W2, anchors, h, Wg, c["d"], B, K, V, r, T,
+                                           seed, tokens, logprobs, conf, stream)
+            return ctx.last_launches
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for i in range(args.warmup):
+        step(1000 + i)
+    torch.cuda.synchronize(dev)
+    if ctx.status() != 0:
+        raise RuntimeError(f"device status {ctx.status()} after warm-up")
+
+    # -------- device-timed steps (inputs resident, L2 flushed between steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_id(dev))
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        launches += step(replica_seed(rank, i))
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+    if ctx.status() != 0:
+        raise RuntimeError(f"device status {ctx.status()} in the timed region")
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_ms = sum(per_step_ms)
+    dev_ms_max = max_over_ranks(dev_ms, world, dev)
+    value = job_throughput(B * K, args.steps, world, dev_ms_max)
+    ms_per_step = dev_ms_max / args.steps
+
+    # -------- roofline of the dominant kernel
+    peak, peak_kind = measured_peaks()
+    alg = algorithmic_bytes(cfg, c)
+    kernel_ms = statistics.median(per_step_ms)
+    achieved = alg / (kernel_ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
+                "kernel": "draft_kernel" if cfg != 4 else "topk_kernel + pair_scores + walk",
+                "median_launch_us": round(kernel_ms * 1000, 2)}
+
+    # -------- end to end through the binding with host buffers
+    e2e = None
+    if not args.skip_e2e and cfg != 4:
+        e2e = run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world)
+
+    line = None
+    if rank == 0:
+        cpu = None if args.skip_cpu else cpu_baseline(inp, c, args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": desc, "B": B, "K": K, "V": V, "r": r, "d": c.get("d", 0),
+                       "temperature": T, "l2": "flushed between steps (512 MB write)",
+                       "inputs_bytes": int(inp.U.nbytes), "parallelism": f"replicas x{world}"},
+            "us_per_block": round(ms_per_step * 1000, 2),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": launches, "wall_s_timed_region": round(wall, 4),
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world):
+    """Same metric with host inputs: pinned H2D of the step's inputs, D2H of its outputs."""
+    import torch
+    from rank_markov_draft_gb300 import binding
+    B, K, V, r = c["B"], c["K"], c["V"], c["r"]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    U_h = pin(inp.U)
+    anc_h = pin(inp.anchors)
+    hc_h = pin(inp.h.view(np.int16)) if conf is not None else None
+    U_d = torch.empty_like(U_h, device=dev)
+    anc_d = torch.empty_like(anc_h, device=dev)
+    hc_d = torch.empty_like(hc_h, device=dev) if hc_h is not None else None
+    tok_d = torch.empty(B, K, dtype=torch.int32, device=dev)
+    lp_d = torch.empty(B, K, dtype=torch.float32, device=dev)
+    outs_h = {"tokens": torch.empty(B, K, dtype=torch.int32).pin_memory(),
+              "logprobs": torch.empty(B, K, dtype=torch.float32).pin_memory()}
+    conf_e = None
+    if conf is not None:
+        conf_e = binding.Confidence(h=hc_d, w=conf.w, bias=conf.bias,
+                                    threshold=conf.threshold).allocate(B, K)
+        outs_h.update(conf=torch.empty(B, K).pin_memory(), cumprod=torch.empty(B, K).pin_memory(),
+                      verify_len=torch.empty(B, dtype=torch.int32).pin_memory())
+    h2d = U_h.numel() * 4 + anc_h.numel() * 4 + (hc_h.numel() * 2 if hc_h is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+
+    def one(seed):
+        U_d.copy_(U_h, non_blocking=True)
+        anc_d.copy_(anc_h, non_blocking=True)
+        if hc_h is not None:
+            hc_d.copy_(hc_h, non_blocking=True)
+        if h is None:
+            binding.dspark_markov_draft(ctx, U_d, W1, W2, anc_d, B, K, V, r, 1.0, seed, tok_d,
+                                        lp_d, conf_e, stream)
+        else:
+            binding.dspark_gated_draft(ctx, U_d, W1, W2, anc_d, h, Wg, c["d"], B, K, V, r, 1.0,
+                                       seed, tok_d, lp_d, conf_e, stream)
+        outs_h["tokens"].copy_(tok_d, non_blocking=True)
+        outs_h["logprobs"].copy_(lp_d, non_blocking=True)
+        if conf_e is not None:
+            outs_h["conf"].copy_(conf_e.conf, non_blocking=True)
+            outs_h["cumprod"].copy_(conf_e.cumprod, non_blocking=True)
+            outs_h["verify_len"].copy_(conf_e.verify_len, non_blocking=True)
+
+    for i in range(max(1, args.warmup)):
+        one(2000 + i)
+    torch.cuda.synchronize(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    s.record(stream)
+    for i in range(args.steps):
+        one(3000 + i)
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(s.elapsed_time(e), world, dev)
+    return {"value": round(job_throughput(B * K, args.steps, world, ms), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / args.steps, 4)}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

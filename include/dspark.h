@@ -1,0 +1,239 @@
+/*
+ * dspark.h -- C ABI of the DSpark Markov-head drafting hot path on GB300
+ * (sm_103a).  Every entry point takes plain pointers and sizes; no C++ or
+ * framework types cross this boundary.
+ *
+ * Conventions (all entry points)
+ * ------------------------------
+ * Memory.  Every tensor argument is a DEVICE pointer owned by the caller,
+ *   contiguous and row-major, on the context's device; the library neither
+ *   frees nor keeps them after the call's stream work finishes.  bf16 tensors
+ *   are passed as uint16_t bit patterns, tokens as int32_t.  Pointers must be
+ *   16-byte aligned.  The library allocates no device memory inside a hot
+ *   call: the context (dspark_ctx_create) owns all scratch (grid-barrier
+ *   counter, per-step argmax keys, cross-CTA partials, gate activations,
+ *   status word), sized for the B_max / V_max / K_max given at creation.
+ * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) and runs asynchronously; outputs are valid once the
+ *   stream has been synchronised.  A context holds one scratch area, so calls
+ *   on one context must not overlap: issue them on one stream.
+ * Errors.  Every call returns a dspark_status.  Argument errors are detected
+ *   on the host before anything is enqueued (argument checks come before the
+ *   context check, so they can be exercised with ctx == NULL).  Errors found
+ *   by kernels (a grid-barrier or pipeline wait that ran out of time, a token
+ *   id out of range) are written to the context's device status word; read it
+ *   with dspark_get_status after synchronising the stream.  After a device
+ *   error the context is poisoned: further hot calls return
+ *   DSPARK_ERR_CTX_POISONED until dspark_ctx_reset is called.
+ * Temperature.  temperature > 0 samples softmax(l / T) by Gumbel-max;
+ *   temperature == 0 is greedy.  Returned log-probabilities are those of the
+ *   drawn token under softmax(l / T'), T' = T (T > 0) or 1 (T == 0).
+ * Noise.  Philox4x32-10 (Salmon et al., SC'11) keyed by (seed low 32 bits,
+ *   seed high 32 bits) with counter (v >> 2, k, b, 0); word v & 3 gives
+ *   u = ((word >> 9) + 0.5) * 2^-23 and the Gumbel variate -ln(-ln u).  b is
+ *   the request's index in the call's batch, k its 0-based block position,
+ *   v the token id.  The same (seed, b, k, v) always yields the same noise.
+ * Ties.  Argmax and top-k orders break ties to the smaller token id.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSPARK_ABI_VERSION 1
+
+typedef struct dspark_ctx dspark_ctx;
+typedef struct CUstream_st* dspark_stream_t; /* same type as cudaStream_t */
+
+typedef enum dspark_status {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer */
+  DSPARK_ERR_UNSUPPORTED = 2,    /* shape outside what the kernels implement */
+  DSPARK_ERR_CUDA = 3,           /* a CUDA runtime or driver call failed */
+  DSPARK_ERR_TIMEOUT = 4,        /* device: a bounded wait ran out (kernel exited cleanly) */
+  DSPARK_ERR_DEVICE_OOB = 5,     /* device: a token id read on the device was out of range */
+  DSPARK_ERR_NO_DEVICE = 6,      /* no usable sm_103 device */
+  DSPARK_ERR_CTX_POISONED = 7,   /* a previous device error needs dspark_ctx_reset */
+  DSPARK_ERR_CAPACITY = 8        /* B, K or V above the context's creation limits */
+} dspark_status;
+
+/* Optional confidence head, fused into the draft / walk epilogues, or run
+ * standalone by dspark_confidence.
+ * Source: DSpark explainer, "Confidence-scheduled verification":
+ *   c_k = sigmoid(w^T [h_k ; W1[x_{k-1}]] + bias), survival a_j = prod_{i<=j} c_i;
+ * vLLM speculators "DSpark" guide, "Confidence Head" (the Markov embedding is
+ * concatenated only when with_markov is set).
+ * verify_len[b] = longest prefix j with a_j >= threshold (0 if none). */
+typedef struct dspark_conf_args {
+  const uint16_t* h;     /* [B, K, d] bf16 backbone hidden states */
+  const uint16_t* w;     /* [d + r] bf16 if with_markov, else [d] */
+  float bias;            /* scalar bias (0 in the pages' equation) */
+  int d;                 /* hidden size, > 0, multiple of 8 */
+  int with_markov;       /* 1: concatenate the previous token's Markov embedding */
+  float threshold;       /* survival threshold for verify_len */
+  float* conf;           /* out [B, K] fp32 */
+  float* cumprod;        /* out [B, K] fp32 */
+  int32_t* verify_len;   /* out [B] int32 */
+} dspark_conf_args;
+
+/* --------------------------------------------------------------------- */
+/* Context                                                                 */
+/* --------------------------------------------------------------------- */
+
+/* Create a context on `device` with scratch for up to B_max requests, K_max
+ * block positions (<= 64) and V_max vocabulary entries.  Allocates device
+ * memory (the only allocation the library makes).  *ctx receives the handle;
+ * release it with dspark_ctx_destroy. */
+int dspark_ctx_create(dspark_ctx** ctx, int device, int B_max, int V_max, int K_max);
+
+/* Free the context's device memory.  The caller must have synchronised every
+ * stream that used it. */
+int dspark_ctx_destroy(dspark_ctx* ctx);
+
+/* Clear the device status word, the barrier counter and the argmax keys on
+ * `stream`, and un-poison the context. */
+int dspark_ctx_reset(dspark_ctx* ctx, dspark_stream_t stream);
+
+/* Read the device status word (a dspark_status) into *device_status.  Reads
+ * with a blocking copy on the context's device; call after the work stream has
+ * been synchronised.  A non-OK value poisons the context. */
+int dspark_get_status(dspark_ctx* ctx, int* device_status);
+
+/* Testing knob: make CTA `cta` skip its grid-barrier arrival at step 0 in the
+ * next draft launch (so every CTA's bounded wait runs out and the kernel exits
+ * with DSPARK_ERR_TIMEOUT), with waits limited to timeout_ms.  cta = -1 turns
+ * the knob off and timeout_ms <= 0 restores the default limit (2000 ms). */
+int dspark_debug_set(dspark_ctx* ctx, int cta, int timeout_ms);
+
+/* Text of a status code (static storage). */
+const char* dspark_strerror(int code);
+
+/* DSPARK_ABI_VERSION of the loaded library. */
+int dspark_abi_version(void);
+
+/* Number of kernels the last hot call on `ctx` enqueued. */
+int dspark_last_launch_count(dspark_ctx* ctx);
+
+/* --------------------------------------------------------------------- */
+/* Markov-head draft                                                        */
+/* --------------------------------------------------------------------- */
+
+/* Vanilla Markov head, sampled left to right over a block.
+ * Source: "DFlash-2's Selector and DSpark's Markov Head: An Equivalence
+ * Observation", section "What the two methods do" (logits_k = U_k +
+ * W1[a]^T W2, W1 in R^{V x 256}, W2 in R^{256 x V}); DSpark explainer,
+ * "Semi-autoregressive generation" (anchor is the first prediction position;
+ * left-to-right sampling) and "The Markov head" (B(x_{k-1}, .) = W1[x_{k-1}]
+ * W2); "DSpark: Repair the Joint, Meter the Verify", "Fix 1" and "Why the
+ * normalization has to be local" (exact local softmax per position).
+ *   U        [B, K, V] fp32 base logits of the parallel backbone
+ *   W1       [V, r] bf16 (Markov embedding table), W2 [r, V] bf16
+ *   anchors  [B] int32: x_0, the token that feeds position 0's bias
+ *   r        rank: 0 (head disabled: logits = U) or a multiple of 16, <= 256
+ *   V        multiple of 8; K in [1, K_max]; B in [1, B_max]
+ *   tokens   out [B, K] int32: x_1 .. x_K
+ *   logprobs out [B, K] fp32: log q(x_k) under the local softmax
+ *   conf     optional fused confidence head (NULL = off); uses W1[x_{k-1}]
+ * One persistent cooperative kernel per 128 requests (requests are split in
+ * chunks of 128; the noise uses the request's index in the whole call). */
+int dspark_markov_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1,
+                        const uint16_t* W2, const int32_t* anchors, int B, int K, int V, int r,
+                        float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
+                        const dspark_conf_args* conf, dspark_stream_t stream);
+
+/* Gated Markov head: logits_t = U_t + (W1[a] (.) H(h_t))^T W2 with
+ * H(h_t) = sigmoid(h_t . Wg) (no bias).
+ * Source: equivalence page, "The equivalence: remove the gate, recover the
+ * Markov Head" (context-gated variant) and "What the two methods do" (gate
+ * H(h_t) computed from the current hidden state); vLLM guide, "Markov Head"
+ * (gated variant).  The gate's functional form is this library's reading.
+ *   h [B, K, d] bf16, Wg [d, r] bf16, d a multiple of 64; r a multiple of 64.
+ * The gated embedding W1[a] (.) H is rounded to bf16 as the MMA operand.
+ * Other arguments as dspark_markov_draft.  Launches the gate GEMM, its
+ * finaliser, then the draft kernel. */
+int dspark_gated_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1,
+                       const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
+                       const uint16_t* Wg, int d, int B, int K, int V, int r,
+                       float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
+                       const dspark_conf_args* conf, dspark_stream_t stream);
+
+/* The gate alone: H[m, :] = sigmoid(h[m, :] . Wg) for m < M.
+ * h [M, d] bf16, Wg [d, r] bf16, H out [M, r] fp32; d, r multiples of 64,
+ * M <= B_max * K_max. */
+int dspark_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int d, int r,
+                float* H, dspark_stream_t stream);
+
+/* --------------------------------------------------------------------- */
+/* Selector-style top-k execution                                           */
+/* --------------------------------------------------------------------- */
+
+/* Top-k candidate sets and adjacent-pair score tables.
+ * Source: equivalence page, "Where the parallelism comes from" (top-16 of the
+ * base logits; all 16 x 16 predecessor/candidate calibrations in parallel),
+ * "What the two methods do" (S_t(a, b) = U_t(b) + <A(a) (.) H(h_t), B(b)>)
+ * and "Two implications" (the same truncation for a trained Markov head,
+ * A = W1, B = W2^T).
+ *   U [B, K, V] fp32; A, Bt [V, r] bf16 (Bt row b is B(b)); anchors [B]
+ *   h, Wg: gate inputs as dspark_gated_draft, or both NULL (ungated, H = 1)
+ *   topk in [1, 32], topk <= V; r a multiple of 16 (64 if gated), <= 256
+ *   cand   out [B, K, topk] int32, ordered by (U desc, id asc)
+ *   cand_U out [B, K, topk] fp32 (U of each candidate)
+ *   scores out [B, K, topk, topk] fp32: scores[b,t,i,j] = S_t(p_i, c_j) with
+ *          p = cand[b, t-1, :] for t >= 1 and p_i = anchors[b] for t = 0. */
+int dspark_selector_scores(dspark_ctx* ctx, const float* U, const uint16_t* A,
+                           const uint16_t* Bt, const int32_t* anchors, const uint16_t* h,
+                           const uint16_t* Wg, int d, int B, int K, int V, int r, int topk,
+                           int32_t* cand, float* cand_U, float* scores, dspark_stream_t stream);
+
+/* The light sequential walk over the pair tables: per request, for t = 0..K-1
+ * pick candidate j of row `slot` (slot = 0 at t = 0) by Gumbel-max over
+ * scores/T with noise keyed by the candidate's token id (T = 0: greedy), then
+ * slot = j.  log-probabilities are under the topk-way softmax.
+ * Source: equivalence page, "Where the parallelism comes from" (a greedy walk,
+ * or sampling, over the precomputed scores) and "Two implications", step 3.
+ *   cand [B, K, topk], scores [B, K, topk, topk] as produced above
+ *   A [V, r], anchors [B]: only read by the fused confidence head (which uses
+ *   A[x_{t-1}] as the Markov embedding); may be NULL when conf == NULL. */
+int dspark_selector_walk(dspark_ctx* ctx, const int32_t* cand, const float* scores,
+                         const int32_t* anchors, const uint16_t* A, int B, int K, int V, int r,
+                         int topk, float temperature, uint64_t seed, int32_t* tokens,
+                         float* logprobs, const dspark_conf_args* conf, dspark_stream_t stream);
+
+/* --------------------------------------------------------------------- */
+/* Confidence head (standalone)                                             */
+/* --------------------------------------------------------------------- */
+
+/* c_k = sigmoid(w[:d] . h[b,k] + with_markov * w[d:] . W1[x_{k-1}] + bias),
+ * cumprod a_k, verify_len = longest prefix with a_k >= threshold.
+ * Source: as dspark_conf_args.  tokens [B, K] = x_1..x_K; x_0 = anchors[b].
+ * W1 may be NULL when with_markov == 0. */
+int dspark_confidence(dspark_ctx* ctx, const uint16_t* h, const uint16_t* W1,
+                      const int32_t* anchors, const int32_t* tokens, const uint16_t* w,
+                      float bias, int with_markov, int B, int K, int d, int r, int V,
+                      float threshold, float* conf, float* cumprod, int32_t* verify_len,
+                      dspark_stream_t stream);
+
+/* --------------------------------------------------------------------- */
+/* Teacher-forced calibrated logits (parity / test mode)                    */
+/* --------------------------------------------------------------------- */
+
+/* logits[b, k, :] = U[b, k, :] + (W1[x_{k-1}] (.) H)^T W2 for given
+ * predecessors prev_tokens[b, k] = x_{k-1} (x_0 = the anchor), and
+ * lse[b, k] = log sum_v exp(logits[b, k, v] / T').
+ * Source: equivalence page, per-candidate form logits_k(b | a) = U_k(b) +
+ * W1[a]^T W2[:, b].  h, Wg: NULL (vanilla) or the gate inputs (gated).
+ * Writes the full [B, K, V] fp32 logits: meant for checking, not speed. */
+int dspark_markov_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1,
+                         const uint16_t* W2, const int32_t* prev_tokens, const uint16_t* h,
+                         const uint16_t* Wg, int d, int B, int K, int V, int r,
+                         float temperature, float* logits, float* lse, dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

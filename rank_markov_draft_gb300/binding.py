@@ -1,0 +1,364 @@
+"""ctypes binding of libdspark (include/dspark.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  The low-level functions carry the C names (``dspark_*``) and
+take torch tensors (device memory, caller-owned) plus an optional CUDA
+stream; the convenience wrappers below them allocate the outputs.  There is no
+CPU fallback: if the compiled library is missing, loading raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdspark.so")
+
+STATUS = {
+    0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_UNSUPPORTED",
+    3: "DSPARK_ERR_CUDA", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_DEVICE_OOB",
+    6: "DSPARK_ERR_NO_DEVICE", 7: "DSPARK_ERR_CTX_POISONED", 8: "DSPARK_ERR_CAPACITY",
+}
+OK, INVALID_ARG, UNSUPPORTED, CUDA, TIMEOUT, DEVICE_OOB, NO_DEVICE, POISONED, CAPACITY = range(9)
+
+# Functions declared in include/dspark.h (checked against the header by the tests).
+EXPORTS = (
+    "dspark_ctx_create", "dspark_ctx_destroy", "dspark_ctx_reset", "dspark_get_status",
+    "dspark_debug_set", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
+    "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
+    "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
+)
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({strerror(code)})")
+
+
+class ConfArgs(ctypes.Structure):
+    _fields_ = [
+        ("h", ctypes.c_void_p), ("w", ctypes.c_void_p), ("bias", ctypes.c_float),
+        ("d", ctypes.c_int), ("with_markov", ctypes.c_int), ("threshold", ctypes.c_float),
+        ("conf", ctypes.c_void_p), ("cumprod", ctypes.c_void_p), ("verify_len", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libdspark.so; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libdspark.so not found at {path}: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    P, I, F, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
+    sig = {
+        "dspark_ctx_create": [ctypes.POINTER(P), I, I, I, I],
+        "dspark_ctx_destroy": [P],
+        "dspark_ctx_reset": [P, P],
+        "dspark_get_status": [P, ctypes.POINTER(I)],
+        "dspark_debug_set": [P, I, I],
+        "dspark_strerror": [I],
+        "dspark_abi_version": [],
+        "dspark_last_launch_count": [P],
+        "dspark_markov_draft": [P, P, P, P, P, I, I, I, I, F, U64, P, P, P, P],
+        "dspark_gated_draft": [P, P, P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P],
+        "dspark_gate": [P, P, P, I, I, I, P, P],
+        "dspark_selector_scores": [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P],
+        "dspark_selector_walk": [P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P],
+        "dspark_confidence": [P, P, P, P, P, P, F, I, I, I, I, I, I, F, P, P, P, P],
+        "dspark_markov_logits": [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "dspark_strerror" else ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().dspark_strerror(int(code)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+# ----------------------------------------------------------------- marshalling
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _ptr(t: Optional[torch.Tensor], dtypes=None, name: str = "tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must live in CUDA device memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise DSparkError(code, where)
+
+
+class Context:
+    """A dspark_ctx: per-device scratch for B_max requests, K_max positions, V_max tokens."""
+
+    def __init__(self, device: int = 0, B_max: int = 128, V_max: int = 151936, K_max: int = 16):
+        self.lib = load()
+        self.device = device
+        self.B_max, self.V_max, self.K_max = B_max, V_max, K_max
+        h = ctypes.c_void_p()
+        _check(self.lib.dspark_ctx_create(ctypes.byref(h), device, B_max, V_max, K_max),
+               "dspark_ctx_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            torch.cuda.synchronize(self.device)
+            self.lib.dspark_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def reset(self, stream=None):
+        _check(self.lib.dspark_ctx_reset(self.handle, _stream(stream, self.device)),
+               "dspark_ctx_reset")
+
+    def status(self) -> int:
+        v = ctypes.c_int(0)
+        _check(self.lib.dspark_get_status(self.handle, ctypes.byref(v)), "dspark_get_status")
+        return v.value
+
+    def debug_set(self, cta: int = -1, timeout_ms: int = 0):
+        _check(self.lib.dspark_debug_set(self.handle, cta, timeout_ms), "dspark_debug_set")
+
+    @property
+    def last_launches(self) -> int:
+        return int(self.lib.dspark_last_launch_count(self.handle))
+
+
+@dataclass
+class Confidence:
+    """Inputs and outputs of the confidence head (dspark_conf_args)."""
+    h: torch.Tensor            # [B, K, d] bf16
+    w: torch.Tensor            # [d + r] (with_markov) or [d] bf16
+    bias: float = 0.0
+    with_markov: bool = True
+    threshold: float = 0.3
+    conf: Optional[torch.Tensor] = None       # out [B, K] fp32
+    cumprod: Optional[torch.Tensor] = None    # out [B, K] fp32
+    verify_len: Optional[torch.Tensor] = None  # out [B] int32
+
+    def allocate(self, B: int, K: int):
+        dev = self.h.device
+        if self.conf is None:
+            self.conf = torch.empty(B, K, dtype=torch.float32, device=dev)
+        if self.cumprod is None:
+            self.cumprod = torch.empty(B, K, dtype=torch.float32, device=dev)
+        if self.verify_len is None:
+            self.verify_len = torch.empty(B, dtype=torch.int32, device=dev)
+        return self
+
+    def struct(self) -> ConfArgs:
+        return ConfArgs(_ptr(self.h, _BF16, "conf.h"), _ptr(self.w, _BF16, "conf.w"),
+                        float(self.bias), int(self.h.shape[-1]), int(bool(self.with_markov)),
+                        float(self.threshold), _ptr(self.conf, (torch.float32,), "conf.conf"),
+                        _ptr(self.cumprod, (torch.float32,), "conf.cumprod"),
+                        _ptr(self.verify_len, (torch.int32,), "conf.verify_len"))
+
+
+def _conf_ref(conf: Optional[Confidence]):
+    return None if conf is None else ctypes.byref(conf.struct())
+
+
+# ------------------------------------------------------- C-named entry points
+def dspark_markov_draft(ctx: Context, U, W1, W2, anchors, B, K, V, r, temperature, seed,
+                        tokens, logprobs, conf: Optional[Confidence] = None, stream=None):
+    code = ctx.lib.dspark_markov_draft(
+        ctx.handle, _ptr(U, (torch.float32,), "U"), _ptr(W1, _BF16, "W1"),
+        _ptr(W2, _BF16, "W2"), _ptr(anchors, (torch.int32,), "anchors"), B, K, V, r,
+        float(temperature), int(seed) & (2 ** 64 - 1), _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(logprobs, (torch.float32,), "logprobs"), _conf_ref(conf), _stream(stream, ctx.device))
+    _check(code, "dspark_markov_draft")
+
+
+def dspark_gated_draft(ctx: Context, U, W1, W2, anchors, h, Wg, d, B, K, V, r, temperature,
+                       seed, tokens, logprobs, conf: Optional[Confidence] = None, stream=None):
+    code = ctx.lib.dspark_gated_draft(
+        ctx.handle, _ptr(U, (torch.float32,), "U"), _ptr(W1, _BF16, "W1"),
+        _ptr(W2, _BF16, "W2"), _ptr(anchors, (torch.int32,), "anchors"), _ptr(h, _BF16, "h"),
+        _ptr(Wg, _BF16, "Wg"), d, B, K, V, r, float(temperature), int(seed) & (2 ** 64 - 1),
+        _ptr(tokens, (torch.int32,), "tokens"), _ptr(logprobs, (torch.float32,), "logprobs"),
+        _conf_ref(conf), _stream(stream, ctx.device))
+    _check(code, "dspark_gated_draft")
+
+
+def dspark_gate(ctx: Context, h, Wg, M, d, r, H, stream=None):
+    code = ctx.lib.dspark_gate(ctx.handle, _ptr(h, _BF16, "h"), _ptr(Wg, _BF16, "Wg"), M, d, r,
+                               _ptr(H, (torch.float32,), "H"), _stream(stream, ctx.device))
+    _check(code, "dspark_gate")
+
+
+def dspark_selector_scores(ctx: Context, U, A, Bt, anchors, h, Wg, d, B, K, V, r, topk, cand,
+                           cand_U, scores, stream=None):
+    code = ctx.lib.dspark_selector_scores(
+        ctx.handle, _ptr(U, (torch.float32,), "U"), _ptr(A, _BF16, "A"), _ptr(Bt, _BF16, "Bt"),
+        _ptr(anchors, (torch.int32,), "anchors"), _ptr(h, _BF16, "h"), _ptr(Wg, _BF16, "Wg"), d,
+        B, K, V, r, topk, _ptr(cand, (torch.int32,), "cand"),
+        _ptr(cand_U, (torch.float32,), "cand_U"), _ptr(scores, (torch.float32,), "scores"),
+        _stream(stream, ctx.device))
+    _check(code, "dspark_selector_scores")
+
+
+def dspark_selector_walk(ctx: Context, cand, scores, anchors, A, B, K, V, r, topk, temperature,
+                         seed, tokens, logprobs, conf: Optional[Confidence] = None, stream=None):
+    code = ctx.lib.dspark_selector_walk(
+        ctx.handle, _ptr(cand, (torch.int32,), "cand"), _ptr(scores, (torch.float32,), "scores"),
+        _ptr(anchors, (torch.int32,), "anchors"), _ptr(A, _BF16, "A"), B, K, V, r, topk,
+        float(temperature), int(seed) & (2 ** 64 - 1), _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(logprobs, (torch.float32,), "logprobs"), _conf_ref(conf), _stream(stream, ctx.device))
+    _check(code, "dspark_selector_walk")
+
+
+def dspark_confidence(ctx: Context, h, W1, anchors, tokens, w, bias, with_markov, B, K, d, r, V,
+                      threshold, conf, cumprod, verify_len, stream=None):
+    code = ctx.lib.dspark_confidence(
+        ctx.handle, _ptr(h, _BF16, "h"), _ptr(W1, _BF16, "W1"),
+        _ptr(anchors, (torch.int32,), "anchors"), _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(w, _BF16, "w"), float(bias), int(bool(with_markov)), B, K, d, r, V, float(threshold),
+        _ptr(conf, (torch.float32,), "conf"), _ptr(cumprod, (torch.float32,), "cumprod"),
+        _ptr(verify_len, (torch.int32,), "verify_len"), _stream(stream, ctx.device))
+    _check(code, "dspark_confidence")
+
+
+def dspark_markov_logits(ctx: Context, U, W1, W2, prev_tokens, h, Wg, d, B, K, V, r,
+                         temperature, logits, lse, stream=None):
+    code = ctx.lib.dspark_markov_logits(
+        ctx.handle, _ptr(U, (torch.float32,), "U"), _ptr(W1, _BF16, "W1"), _ptr(W2, _BF16, "W2"),
+        _ptr(prev_tokens, (torch.int32,), "prev_tokens"), _ptr(h, _BF16, "h"),
+        _ptr(Wg, _BF16, "Wg"), d, B, K, V, r, float(temperature),
+        _ptr(logits, (torch.float32,), "logits"), _ptr(lse, (torch.float32,), "lse"),
+        _stream(stream, ctx.device))
+    _check(code, "dspark_markov_logits")
+
+
+# ------------------------------------------------------ allocating wrappers
+def _rank(W1) -> int:
+    return 0 if W1 is None else int(W1.shape[1])
+
+
+def markov_draft(ctx: Context, U, W1, W2, anchors, *, temperature=1.0, seed=0, h=None, Wg=None,
+                 conf: Optional[Confidence] = None, stream=None) -> dict:
+    """Vanilla (h, Wg None) or gated draft; returns tokens and logprobs [B, K]."""
+    B, K, V = U.shape
+    r = _rank(W1)
+    tokens = torch.empty(B, K, dtype=torch.int32, device=U.device)
+    logprobs = torch.empty(B, K, dtype=torch.float32, device=U.device)
+    if conf is not None:
+        conf.allocate(B, K)
+    if h is None and Wg is None:
+        dspark_markov_draft(ctx, U, W1, W2, anchors, B, K, V, r, temperature, seed, tokens,
+                            logprobs, conf, stream)
+    else:
+        dspark_gated_draft(ctx, U, W1, W2, anchors, h, Wg, int(h.shape[-1]), B, K, V, r,
+                           temperature, seed, tokens, logprobs, conf, stream)
+    out = dict(tokens=tokens, logprobs=logprobs)
+    if conf is not None:
+        out.update(conf=conf.conf, cumprod=conf.cumprod, verify_len=conf.verify_len)
+    return out
+
+
+def gate(ctx: Context, h, Wg, stream=None) -> torch.Tensor:
+    d, r = Wg.shape
+    M = h.numel() // d
+    H = torch.empty(*h.shape[:-1], r, dtype=torch.float32, device=h.device)
+    dspark_gate(ctx, h, Wg, M, d, r, H, stream)
+    return H
+
+
+def selector_scores(ctx: Context, U, A, Bt, anchors, *, topk=16, h=None, Wg=None,
+                    stream=None) -> dict:
+    B, K, V = U.shape
+    r = int(A.shape[1])
+    cand = torch.empty(B, K, topk, dtype=torch.int32, device=U.device)
+    cand_U = torch.empty(B, K, topk, dtype=torch.float32, device=U.device)
+    scores = torch.empty(B, K, topk, topk, dtype=torch.float32, device=U.device)
+    d = 0 if h is None else int(h.shape[-1])
+    dspark_selector_scores(ctx, U, A, Bt, anchors, h, Wg, d, B, K, V, r, topk, cand, cand_U,
+                           scores, stream)
+    return dict(cand=cand, cand_U=cand_U, scores=scores)
+
+
+def selector_walk(ctx: Context, cand, scores, anchors, *, V, A=None, temperature=1.0, seed=0,
+                  conf: Optional[Confidence] = None, stream=None) -> dict:
+    B, K, topk = cand.shape
+    r = 0 if A is None else int(A.shape[1])
+    tokens = torch.empty(B, K, dtype=torch.int32, device=cand.device)
+    logprobs = torch.empty(B, K, dtype=torch.float32, device=cand.device)
+    if conf is not None:
+        conf.allocate(B, K)
+    dspark_selector_walk(ctx, cand, scores, anchors, A, B, K, V, r, topk, temperature, seed,
+                         tokens, logprobs, conf, stream)
+    out = dict(tokens=tokens, logprobs=logprobs)
+    if conf is not None:
+        out.update(conf=conf.conf, cumprod=conf.cumprod, verify_len=conf.verify_len)
+    return out
+
+
+def confidence(ctx: Context, h, W1, anchors, tokens, w, *, V, bias=0.0, with_markov=True,
+               threshold=0.3, stream=None) -> dict:
+    B, K, d = h.shape
+    r = _rank(W1) if with_markov else 0
+    conf = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    cum = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    vl = torch.empty(B, dtype=torch.int32, device=h.device)
+    dspark_confidence(ctx, h, W1 if with_markov else None, anchors, tokens, w, bias, with_markov,
+                      B, K, d, r, V, threshold, conf, cum, vl, stream)
+    return dict(conf=conf, cumprod=cum, verify_len=vl)
+
+
+def markov_logits(ctx: Context, U, W1, W2, prev_tokens, *, temperature=1.0, h=None, Wg=None,
+                  stream=None) -> dict:
+    B, K, V = U.shape
+    r = _rank(W1)
+    logits = torch.empty(B, K, V, dtype=torch.float32, device=U.device)
+    lse = torch.empty(B, K, dtype=torch.float32, device=U.device)
+    d = 0 if h is None else int(h.shape[-1])
+    dspark_markov_logits(ctx, U, W1, W2, prev_tokens, h, Wg, d, B, K, V, r, temperature, logits,
+                         lse, stream)
+    return dict(logits=logits, lse=lse)

@@ -1,0 +1,694 @@
+// draft.cu -- persistent Markov-head draft kernel for sm_103a.
+//
+// What it computes (DSpark explainer, "Semi-autoregressive generation" and
+// "The Markov head"; equivalence page, "What the two methods do"): for a
+// chunk of up to 128 requests and block positions k = 0 .. K-1,
+//     l[b, v] = U[b, k, v] + sum_i e_b[i] * W2[i, v],   e_b = W1[x_{k-1}[b]] (. H[b, k])
+//     x_k[b]  = argmax_v ( l[b, v] / T + Gumbel(seed, b, k, v) )      (T = 0: argmax l)
+//     logprob = l[b, x_k] / T' - log sum_v exp(l[b, v] / T')
+// with x_{-1} = the anchor ("Sample From Anchor" in the vLLM guide).  The
+// local softmax is exact, as rejection sampling needs ("Why the normalization
+// has to be local", "Repair the Joint, Meter the Verify").
+//
+// Layout of the work (one CTA per SM, cooperative launch, all K steps in one
+// launch):
+//   * the vocabulary is split into 64-token tiles; CTA c owns a fixed,
+//     contiguous range of tiles for every step;
+//   * warp 0 (one lane) streams W2 tiles [r x 64] and U tiles [rows x 64]
+//     with TMA into shared memory rings; these never depend on sampled
+//     tokens, so the producer runs ahead across step boundaries;
+//   * warp 1 (one lane) issues tcgen05.mma: D[128 requests x 64 tokens] =
+//     E[128 x r] * W2tile[r x 64] into one of four TMEM accumulators;
+//     E is the gathered Markov embedding of every request (K-major, 128B
+//     swizzle), W2 the MN-major tile exactly as TMA wrote it;
+//   * warps 2..17 (the epilogue) read the accumulator (one request per TMEM
+//     lane, 16 tokens per thread) and U from shared memory, and keep, per
+//     request, a running log-sum-exp and a running Gumbel-max winner, so the
+//     full-vocabulary logits never reach HBM;
+//   * at the end of a step each CTA publishes, per request, a 64-bit key
+//     (epoch | ordered score | inverted token id) by atomicMax and its
+//     log-sum-exp partial; after a bounded grid barrier every CTA decodes the
+//     winning tokens from the keys and gathers the next step's embeddings;
+//   * after the last step, CTA c reduces request c's partials into tokens and
+//     log-probabilities and runs the fused confidence head.
+//
+// Sampling epilogue, per element (Gumbel-max written as an exponential race):
+//   y = l * log2(e) / T, w = 2^(y - m) (shared with the log-sum-exp),
+//   E = -log2(u) (u from Philox), and the winner maximises w / E, which is
+//   the same argmax as y - log2(E) = log2(e) * (l/T + g) + const.  E comes
+//   from the fast lg2 approximation; an element is only examined exactly
+//   (with an accurate log) when its approximate ratio could beat the current
+//   winner, given the approximation's error bound.
+//
+// Every wait is bounded (mbarrier waits and the grid barrier give up after
+// timeout_ns, set the device status word and make the CTA exit cleanly after
+// draining its own TMA copies and MMAs and freeing its TMEM).
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "confidence.cuh"
+#include "internal.h"
+#include "philox.cuh"
+#include "sm103.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kTileV = kDraftTileV;              // 64 tokens per tile (MMA N)
+constexpr int kRows = kBatchChunk;               // 128 requests (MMA M)
+constexpr int kNumW2Stages = 3;
+constexpr int kNumUStages = 2;
+constexpr int kNumAcc = 4;                       // TMEM accumulators, 64 columns each
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = kEpiWarps * 32;      // 512
+constexpr int kThreads = 64 + kEpiThreads;       // 576
+constexpr uint32_t kABytes = kRows * kMaxRank * 2;           // 64 KB
+constexpr uint32_t kW2StageBytes = kMaxRank * kTileV * 2;    // 32 KB
+constexpr uint32_t kUBoxBytes = kRows * 32 * 4;              // 16 KB (32 tokens x 128 rows)
+constexpr uint32_t kUStageBytes = 2 * kUBoxBytes;            // 32 KB
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffW2 = kOffA + kABytes;
+constexpr uint32_t kOffU = kOffW2 + kNumW2Stages * kW2StageBytes;
+constexpr uint32_t kOffBar = kOffU + kNumUStages * kUStageBytes;
+constexpr uint32_t kBarRegion = 1024;
+constexpr uint32_t kSmemBytes = kOffBar + kBarRegion + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = kNumAcc * kTileV;             // 256
+constexpr uint32_t kEpiBarrier = 1;                          // named barrier id
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr uint32_t kTokenBits = 18;                          // V <= 2^18
+constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
+
+static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103 limit");
+
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Key order: larger epoch, then larger score, then smaller token id.
+__device__ __forceinline__ unsigned long long make_key(uint32_t epoch, float score, int v) {
+  return (static_cast<unsigned long long>(epoch) << 50) |
+         (static_cast<unsigned long long>(ordered_bits(score)) << kTokenBits) |
+         static_cast<unsigned long long>(kTokenMask - static_cast<uint32_t>(v));
+}
+
+__device__ __forceinline__ int key_token(unsigned long long key) {
+  return static_cast<int>(kTokenMask - static_cast<uint32_t>(key & kTokenMask));
+}
+
+__device__ __forceinline__ uint32_t key_epoch(unsigned long long key) {
+  return static_cast<uint32_t>(key >> 50);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat16 a = __float2bfloat16_rn(lo);
+  const __nv_bfloat16 b = __float2bfloat16_rn(hi);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// Gather the step's Markov embeddings into the K-major, 128B-swizzled MMA
+// operand: row b = request, 64-element K chunk c at c * 16 KB, 8-row groups of
+// 1024 B, 16-byte unit u of row b stored at unit (u ^ (b & 7)).
+// Thread etid handles row etid / 4 and K chunk etid % 4.
+__device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams& p, int k,
+                                                  int etid, int32_t tok) {
+  const int b = etid >> 2, c = etid & 3;
+  const bool live = b < p.B;
+  uint4 vals[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int kel = c * 64 + u * 8;
+    if (live && kel < p.r) {
+      vals[u] = __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel));
+    } else {
+      vals[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (p.H != nullptr && live) {
+    const float* hrow = p.H + (static_cast<size_t>(b) * p.K + k) * p.r;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int kel = c * 64 + u * 8;
+      if (kel < p.r) {
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(hrow + kel));
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(hrow + kel + 4));
+        uint4 x = vals[u];
+        x.x = pack_bf16(bf16_lo(x.x) * g0.x, bf16_hi(x.x) * g0.y);
+        x.y = pack_bf16(bf16_lo(x.y) * g0.z, bf16_hi(x.y) * g0.w);
+        x.z = pack_bf16(bf16_lo(x.z) * g1.x, bf16_hi(x.z) * g1.y);
+        x.w = pack_bf16(bf16_lo(x.w) * g1.z, bf16_hi(x.w) * g1.w);
+        vals[u] = x;
+      }
+    }
+  }
+  uint8_t* base = sA + c * 16384 + (b >> 3) * 1024 + (b & 7) * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    *reinterpret_cast<uint4*>(base + ((u ^ (b & 7)) << 4)) = vals[u];
+  }
+}
+
+__device__ __forceinline__ void load_partial(const DraftPartial* src, unsigned long long& key,
+                                             float& m2, float& sum, float& lbest) {
+  key = __ldcg(reinterpret_cast<const unsigned long long*>(src));
+  const float2 ms = __ldcg(reinterpret_cast<const float2*>(&src->m2));
+  m2 = ms.x;
+  sum = ms.y;
+  lbest = __ldcg(&src->lbest);
+}
+
+// Merge (m_b, s_b) into (m_a, s_a): log-sum-exp in base 2.
+__device__ __forceinline__ void lse_merge(float& ma, float& sa, float mb, float sb) {
+  if (mb == -INFINITY) return;
+  if (ma == -INFINITY) {
+    ma = mb;
+    sa = sb;
+    return;
+  }
+  if (mb > ma) {
+    sa = sa * ex2_approx(ma - mb) + sb;
+    ma = mb;
+  } else {
+    sa = sa + sb * ex2_approx(mb - ma);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
+  const DraftParams& p = args.p;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + kOffA;
+  uint8_t* sW = smem + kOffW2;
+  uint8_t* sU = smem + kOffU;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* w_full = bars;          // [3]
+  uint64_t* w_empty = bars + 3;     // [3]
+  uint64_t* u_full = bars + 6;      // [2]
+  uint64_t* u_empty = bars + 8;     // [2]
+  uint64_t* acc_full = bars + 10;   // [4]
+  uint64_t* acc_empty = bars + 14;  // [4]
+  uint64_t* a_full = bars + 18;
+  uint64_t* a_empty = bars + 19;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(bars + 22);   // [kMaxK]
+  float* s_conf = reinterpret_cast<float*>(s_tok + kMaxK);  // [kMaxK]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  const int t_begin = static_cast<int>(static_cast<int64_t>(cta) * p.n_tiles / ncta);
+  const int t_end = static_cast<int>(static_cast<int64_t>(cta + 1) * p.n_tiles / ncta);
+  const int nt = t_end - t_begin;
+  const int nkk = p.r / 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNumW2Stages; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int s = 0; s < kNumUStages; ++s) {
+      mbar_init(&u_full[s], 1);
+      mbar_init(&u_empty[s], kEpiWarps);
+    }
+    for (int s = 0; s < kNumAcc; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kEpiWarps);
+    }
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    if (nkk > 0) tma_prefetch_desc(&args.tm_w2);
+    tma_prefetch_desc(&args.tm_u);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_last();
+      const uint64_t pol_u = l2_policy_evict_first();
+      const uint32_t w_bytes = static_cast<uint32_t>(p.r) * kTileV * 2u;
+      const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
+      bool ok = true;
+      int w_issued = 0, u_issued = 0;
+      for (int k = 0; k < p.K && ok; ++k) {
+        for (int t = 0; t < nt; ++t) {
+          const int i = k * nt + t;
+          const int v0 = (t_begin + t) * kTileV;
+          if (nkk > 0) {
+            const int s = i % kNumW2Stages;
+            if (!mbar_wait(&w_empty[s], ((i / kNumW2Stages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&w_full[s], w_bytes);
+            tma_load_2d(sW + s * kW2StageBytes, &args.tm_w2, v0, 0, &w_full[s], pol_w);
+            w_issued = i + 1;
+          }
+          const int su = i % kNumUStages;
+          if (!mbar_wait(&u_empty[su], ((i / kNumUStages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&u_full[su], u_bytes);
+          tma_load_3d(sU + su * kUStageBytes, &args.tm_u, v0, k, 0, &u_full[su], pol_u);
+          tma_load_3d(sU + su * kUStageBytes + kUBoxBytes, &args.tm_u, v0 + 32, k, 0, &u_full[su],
+                      pol_u);
+          u_issued = i + 1;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.status, kStatusTimeout);
+        // Drain: every copy this thread started must land before the CTA exits.
+        // The last issue of each ring slot is the one in [issued - stages, issued).
+        for (int i = w_issued - 1; i >= 0 && i >= w_issued - kNumW2Stages; --i)
+          mbar_wait(&w_full[i % kNumW2Stages], (i / kNumW2Stages) & 1, p.timeout_ns, nullptr);
+        for (int i = u_issued - 1; i >= 0 && i >= u_issued - kNumUStages; --i)
+          mbar_wait(&u_full[i % kNumUStages], (i / kNumUStages) & 1, p.timeout_ns, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kRows, kTileV, /*a_mn=*/false, /*b_mn=*/true);
+      const uint32_t a0 = smem_addr(sA);
+      bool ok = true;
+      int last_i = -1;
+      for (int k = 0; k < p.K && ok; ++k) {
+        if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int t = 0; t < nt; ++t) {
+          const int i = k * nt + t;
+          const int s = i % kNumW2Stages, buf = i % kNumAcc;
+          if (nkk > 0 &&
+              !mbar_wait(&w_full[s], (i / kNumW2Stages) & 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&acc_empty[buf], ((i / kNumAcc) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (nkk > 0) {
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileV);
+            const uint32_t b0 = smem_addr(sW + s * kW2StageBytes);
+            for (int kk = 0; kk < nkk; ++kk) {
+              const uint64_t ad = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = smem_desc(b0 + kk * 2048, 1024, 1024);
+              umma_bf16(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&w_empty[s]);
+            umma_commit(&acc_full[buf]);
+            last_i = i;
+          } else {
+            mbar_arrive(&acc_full[buf]);  // rank 0: the bias is zero, nothing to multiply
+          }
+        }
+        if (!ok) break;
+        if (nkk > 0) {
+          umma_commit(a_empty);
+        } else {
+          mbar_arrive(a_empty);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.status, kStatusTimeout);
+      }
+      // Drain: the last MMA batch must finish before TMEM is released.
+      if (last_i >= 0)
+        mbar_wait(&acc_full[last_i % kNumAcc], (last_i / kNumAcc) & 1, p.timeout_ns, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int e = warp - 2;          // 0 .. 15
+    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int g = e >> 2;            // 16-token column group of the 64-token tile
+    const int b = q * 32 + lane;     // request row of this thread
+    const int etid = threadIdx.x - 64;
+    const bool row_ok = b < p.B;
+    const uint32_t b_global = static_cast<uint32_t>(p.b_global0 + b);
+    const float scale2 = p.inv_t * kLog2e;
+    float* merge = reinterpret_cast<float*>(sA);  // reused after a step's MMAs completed
+    bool fail = false;
+    bool aborted = false;
+
+    for (int k = 0; k < p.K; ++k) {
+      // ---- gather the step's embeddings (after the previous step's MMAs released E)
+      if (k > 0) {
+        if (!mbar_wait(a_empty, (k - 1) & 1, p.timeout_ns, abort_flag)) {
+          fail = true;
+          *abort_flag = 1;
+        }
+      }
+      {
+        const int grow = etid >> 2;
+        int32_t tok = 0;
+        if (grow < p.B) {
+          if (MODE == kModeTeacherForced) {
+            tok = __ldg(p.prev + static_cast<size_t>(grow) * p.K + k);
+          } else if (k == 0) {
+            tok = __ldg(p.anchors + grow);
+          } else {
+            const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + grow);
+            tok = key_token(key);
+          }
+          if (tok < 0 || tok >= p.V) {
+            record_error(p.status, kStatusDeviceOob);
+            tok = 0;
+          }
+        }
+        if (!fail) gather_embeddings(sA, p, k, etid, tok);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kEpiBarrier, kEpiThreads);
+      if (etid == 0) mbar_arrive(a_full);
+
+      // ---- stream the step's tiles
+      float m2 = -INFINITY, sum = 0.f;
+      float wb = 0.f, e2b = 1.f, wb1 = 0.f, wb2 = 0.f, yb = -INFINITY, lb = 0.f;
+      int vb = 0x7FFFFFFF;
+      for (int t = 0; t < nt && !fail; ++t) {
+        const int i = k * nt + t;
+        const int buf = i % kNumAcc, su = i % kNumUStages;
+        bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
+        ok = ok && mbar_wait(&u_full[su], (i / kNumUStages) & 1, p.timeout_ns, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+          fail = true;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        uint32_t acc[16];
+        if (nkk > 0) {
+          tmem_ld_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * kTileV + g * 16),
+                      acc);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = 0u;
+        }
+        float uval[16];
+        {
+          const uint8_t* rowp = sU + su * kUStageBytes + (g >> 1) * kUBoxBytes + b * 128;
+          const int c0 = (g & 1) * 4;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 x = *reinterpret_cast<const float4*>(rowp + (((c0 + c) ^ (b & 7)) << 4));
+            uval[4 * c + 0] = x.x;
+            uval[4 * c + 1] = x.y;
+            uval[4 * c + 2] = x.z;
+            uval[4 * c + 3] = x.w;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[buf]);
+          mbar_arrive(&u_empty[su]);
+        }
+        if (!row_ok) continue;
+
+        const int vbase = (t_begin + t) * kTileV + g * 16;
+        float l[16], y[16];
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          l[j] = uval[j] + __uint_as_float(acc[j]);
+          y[j] = (vbase + j < p.V) ? l[j] * scale2 : -INFINITY;
+          cmax = fmaxf(cmax, y[j]);
+        }
+        if (MODE == kModeTeacherForced) {
+          float* dst = p.logits + (static_cast<size_t>(b) * p.K + k) * p.V + vbase;
+          if (vbase + 16 <= p.V) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              reinterpret_cast<float4*>(dst)[c] =
+                  make_float4(l[4 * c], l[4 * c + 1], l[4 * c + 2], l[4 * c + 3]);
+          } else {
+            for (int j = 0; j < 16 && vbase + j < p.V; ++j) dst[j] = l[j];
+          }
+        }
+        if (cmax == -INFINITY) continue;  // nothing in this chunk can be drawn
+        if (cmax > m2) {
+          const float f = ex2_approx(m2 - cmax);
+          sum *= f;
+          wb *= f;
+          wb1 *= f;
+          wb2 *= f;
+          m2 = cmax;
+        }
+        if (MODE == kModeSample) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>((vbase >> 2) + jj),
+                                              static_cast<uint32_t>(k), b_global, 0u, p.seed_lo,
+                                              p.seed_hi);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int j = jj * 4 + w;
+              const float wv = ex2_approx(y[j] - m2);
+              sum += wv;
+              const float u = philox_uniform(rnd.w[w]);
+              const float e2f = -lg2_approx(u);
+              // fast reject: w / E cannot beat wb / e2b even with E at the low end of
+              // the approximation's error interval
+              if (wv * e2b > fmaf(wb1, e2f, -wb2)) {
+                const float e2 = neg_log_uniform_accurate(u) * kLog2e;
+                if (wv * e2b > wb * e2) {
+                  wb = wv;
+                  e2b = e2;
+                  wb1 = wv * (1.0f - 9.5367431640625e-7f);  // 1 - 2^-20
+                  wb2 = wv * 4.76837158203125e-7f;           // 2^-21
+                  vb = vbase + j;
+                  lb = l[j];
+                }
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            sum += ex2_approx(y[j] - m2);
+            if (MODE == kModeGreedy && y[j] > yb) {
+              yb = y[j];
+              vb = vbase + j;
+              lb = l[j];
+            }
+          }
+        }
+      }
+
+      // ---- merge the four column groups of each request, publish the CTA's partial
+      float score;
+      if (MODE == kModeSample) {
+        score = (vb != 0x7FFFFFFF) ? lb * scale2 - log2f(e2b) : -INFINITY;
+      } else {
+        score = yb;
+      }
+      if (!fail) {
+        merge[(g * 5 + 0) * kRows + b] = m2;
+        merge[(g * 5 + 1) * kRows + b] = sum;
+        merge[(g * 5 + 2) * kRows + b] = score;
+        merge[(g * 5 + 3) * kRows + b] = __int_as_float(vb);
+        merge[(g * 5 + 4) * kRows + b] = lb;
+      }
+      named_bar_sync(kEpiBarrier, kEpiThreads);
+      if (!fail && g == 0 && row_ok) {
+        float M = merge[0 * kRows + b], S = merge[1 * kRows + b];
+        float best_s = merge[2 * kRows + b], best_l = merge[4 * kRows + b];
+        int best_v = __float_as_int(merge[3 * kRows + b]);
+        for (int gg = 1; gg < 4; ++gg) {
+          lse_merge(M, S, merge[(gg * 5 + 0) * kRows + b], merge[(gg * 5 + 1) * kRows + b]);
+          const float s2 = merge[(gg * 5 + 2) * kRows + b];
+          const int v2 = __float_as_int(merge[(gg * 5 + 3) * kRows + b]);
+          if (v2 != 0x7FFFFFFF && (s2 > best_s || (s2 == best_s && v2 < best_v))) {
+            best_s = s2;
+            best_v = v2;
+            best_l = merge[(gg * 5 + 4) * kRows + b];
+          }
+        }
+        unsigned long long key = 0ull;
+        if (MODE != kModeTeacherForced && best_v != 0x7FFFFFFF) {
+          key = make_key(p.epoch, best_s, best_v);
+          atomicMax(p.keys + k * kRows + b, key);
+        }
+        DraftPartial* dst = p.partials + (static_cast<size_t>(k) * kRows + b) * ncta + cta;
+        dst->key = key;
+        dst->m2 = M;
+        dst->sum = S;
+        dst->lbest = best_l;
+      }
+      named_bar_sync(kEpiBarrier, kEpiThreads);
+
+      // ---- grid barrier (bounded)
+      bool bar_fail = false;
+      if (etid == 0 && !fail) {
+        const bool skip = (p.debug_skip_cta == cta) && (k == 0);
+        if (!skip) {
+          __threadfence();
+          red_release_gpu_add(p.bar, 1u);
+        }
+        const uint32_t target = p.bar_base + static_cast<uint32_t>((k + 1) * ncta);
+        uint64_t deadline = 0;
+        for (uint32_t it = 0;; ++it) {
+          const uint32_t cur = ld_acquire_gpu(p.bar);
+          if (static_cast<int32_t>(cur - target) >= 0) break;
+          if ((it & 15u) == 15u) {
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0) {
+              deadline = now + p.timeout_ns;
+            } else if (now > deadline || *abort_flag) {
+              bar_fail = true;
+              break;
+            }
+          }
+        }
+        __threadfence();
+      }
+      const bool any = named_bar_or(kEpiBarrier, kEpiThreads, fail || bar_fail || *abort_flag);
+      if (any) {
+        if (etid == 0) {
+          *abort_flag = 1;
+          record_error(p.status, kStatusTimeout);
+        }
+        aborted = true;
+        break;
+      }
+    }
+
+    // ---- final reduction: CTA c owns requests c, c + grid, ...
+    if (!aborted) {
+      for (int bb = cta; bb < p.B; bb += ncta) {
+        for (int k = e; k < p.K; k += kEpiWarps) {
+          const DraftPartial* src = p.partials + (static_cast<size_t>(k) * kRows + bb) * ncta;
+          const unsigned long long gkey =
+              (MODE == kModeTeacherForced) ? 0ull : __ldcg(p.keys + k * kRows + bb);
+          float M = -INFINITY, S = 0.f, lwin = 0.f;
+          int found = 0;
+          for (int c = lane; c < ncta; c += 32) {
+            unsigned long long key;
+            float m2, s, lbest;
+            load_partial(src + c, key, m2, s, lbest);
+            lse_merge(M, S, m2, s);
+            if (MODE != kModeTeacherForced && key == gkey) {
+              lwin = lbest;
+              found = 1;
+            }
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float Mo = __shfl_xor_sync(0xFFFFFFFFu, M, off);
+            const float So = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+            lse_merge(M, S, Mo, So);
+          }
+          const unsigned who = __ballot_sync(0xFFFFFFFFu, found);
+          lwin = __shfl_sync(0xFFFFFFFFu, lwin, who ? __ffs(who) - 1 : 0);
+          if (lane == 0) {
+            const float lse_nat = (M + log2f(S)) * kLn2;
+            const size_t o = static_cast<size_t>(bb) * p.K + k;
+            if (MODE == kModeTeacherForced) {
+              p.lse[o] = lse_nat;
+            } else {
+              int v = key_token(gkey);
+              if (who == 0 || key_epoch(gkey) != p.epoch || v < 0 || v >= p.V) {
+                record_error(p.status, kStatusDeviceOob);
+                v = 0;
+              }
+              p.tokens[o] = v;
+              p.logprobs[o] = lwin * p.inv_t - lse_nat;
+              s_tok[k] = v;
+            }
+          }
+        }
+        if (MODE != kModeTeacherForced && p.conf != nullptr) {
+          named_bar_sync(kEpiBarrier, kEpiThreads);
+          const int d = p.conf_d;
+          for (int k = e; k < p.K; k += kEpiWarps) {
+            const int32_t prev_tok = (k == 0) ? __ldg(p.anchors + bb) : s_tok[k - 1];
+            const uint16_t* emb =
+                p.conf_with_markov ? p.W1 + static_cast<size_t>(prev_tok) * p.r : nullptr;
+            const float z = confidence_logit(p.conf_h + (static_cast<size_t>(bb) * p.K + k) * d,
+                                             d, p.conf_w, emb, p.r, p.conf_bias, lane);
+            if (lane == 0) s_conf[k] = sigmoidf_accurate(z);
+          }
+          named_bar_sync(kEpiBarrier, kEpiThreads);
+          if (etid == 0) {
+            float surv = 1.f;
+            int len = 0;
+            bool open = true;
+            for (int k = 0; k < p.K; ++k) {
+              const float c = s_conf[k];
+              surv *= c;
+              const size_t o = static_cast<size_t>(bb) * p.K + k;
+              p.conf[o] = c;
+              p.cumprod[o] = surv;
+              if (open && surv >= p.conf_threshold) {
+                len = k + 1;
+              } else {
+                open = false;
+              }
+            }
+            p.verify_len[bb] = len;
+          }
+        }
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int draft_smem_bytes() { return static_cast<int>(kSmemBytes); }
+int draft_threads() { return kThreads; }
+
+cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream) {
+  const void* fn = nullptr;
+  switch (mode) {
+    case kModeSample: fn = reinterpret_cast<const void*>(&draft_kernel<kModeSample>); break;
+    case kModeGreedy: fn = reinterpret_cast<const void*>(&draft_kernel<kModeGreedy>); break;
+    case kModeTeacherForced:
+      fn = reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced>);
+      break;
+    default: return cudaErrorInvalidValue;
+  }
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  void* kargs[] = {const_cast<DraftArgs*>(&args)};
+  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), kargs, kSmemBytes, stream);
+}
+
+}  // namespace dspark

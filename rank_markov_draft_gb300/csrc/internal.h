@@ -1,0 +1,107 @@
+// internal.h -- host/device interface between the C ABI (api.cu) and the
+// kernels.  Not part of the public boundary.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr int kMaxK = 64;           // block positions per call
+constexpr int kMaxRank = 256;       // Markov rank
+constexpr int kBatchChunk = 128;    // requests per draft launch (MMA M)
+constexpr int kDraftTileV = 64;     // vocabulary entries per draft tile (MMA N)
+constexpr int kMaxTopk = 32;
+constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
+
+// Per-(step, request, CTA) record of the draft kernel's cross-CTA reduction.
+struct DraftPartial {
+  unsigned long long key;  // (epoch, Gumbel score, token) packed, see draft.cu
+  float m2;                // running max of l * log2(e) / T'
+  float sum;               // sum of 2^(y - m2)
+  float lbest;             // calibrated logit of this CTA's best token
+  float pad;
+};
+
+struct DraftParams {
+  const uint16_t* W1;       // [V, r]
+  const int32_t* anchors;   // [B] (chunk)
+  const int32_t* prev;      // teacher-forced predecessors [B, K] (chunk), or null
+  const float* H;           // gated: [B, K, r] (chunk) fp32, or null
+  int B, K, V, r;
+  int b_global0;            // index of the chunk's first request in the call (noise key)
+  int n_tiles;              // ceil(V / 64)
+  int box_rows;             // rows of the U TMA box (multiple of 8, >= B)
+  float inv_t;              // 1 / T' (T' = T, or 1 when greedy)
+  uint32_t seed_lo, seed_hi;
+  int32_t* tokens;          // [B, K] (chunk)
+  float* logprobs;          // [B, K] (chunk)
+  float* logits;            // teacher-forced: [B, K, V] (chunk)
+  float* lse;               // teacher-forced: [B, K] (chunk)
+  // fused confidence head (conf == null: off)
+  const uint16_t* conf_h;   // [B, K, d] (chunk)
+  const uint16_t* conf_w;   // [d (+ r)]
+  float conf_bias;
+  int conf_d;
+  int conf_with_markov;
+  float conf_threshold;
+  float* conf;              // [B, K] (chunk)
+  float* cumprod;           // [B, K] (chunk)
+  int32_t* verify_len;      // [B] (chunk)
+  // context scratch
+  unsigned long long* keys; // [kMaxK][128]
+  DraftPartial* partials;   // [kMaxK][128][grid]
+  uint32_t* bar;            // grid-barrier counter
+  int* status;              // device status word
+  uint32_t bar_base;        // counter value at launch
+  uint32_t epoch;           // key epoch of this launch (1 .. 16383)
+  int debug_skip_cta;       // fault injection: CTA skipping its step-0 arrival (-1: none)
+  uint64_t timeout_ns;      // per-wait limit
+};
+
+struct DraftArgs {
+  CUtensorMap tm_w2;  // W2 [r, V] bf16, box {64, r}, 128B swizzle
+  CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle
+  DraftParams p;
+};
+
+enum DraftMode { kModeSample = 0, kModeGreedy = 1, kModeTeacherForced = 2 };
+
+int draft_smem_bytes();
+int draft_threads();
+cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream);
+
+// Gate GEMM: partial[split][m][n] = sum_{j in split} h[m, j] * Wg[j, n].
+struct GateArgs {
+  CUtensorMap tm_h;   // h [M, d] bf16, box {64, 128}
+  CUtensorMap tm_wg;  // Wg [d, r] bf16, box {64, 64}
+  float* partial;     // [splits][M][r]
+  int M, d, r, splits, chunks_per_split;
+  int* status;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_gate_gemm(const GateArgs& args, cudaStream_t stream);
+cudaError_t launch_gate_finalize(const float* partial, int splits, int64_t n, float* H,
+                                 cudaStream_t stream);
+
+cudaError_t launch_topk(const float* U, int rows, int V, int topk, int32_t* cand, float* cval,
+                        cudaStream_t stream);
+cudaError_t launch_pair_scores(const int32_t* cand, const float* cval, const uint16_t* A,
+                               const uint16_t* Bt, const int32_t* anchors, const float* H,
+                               int B, int K, int V, int r, int topk, float* S, int* status,
+                               cudaStream_t stream);
+cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anchors,
+                        const uint16_t* A, int B, int K, int V, int r, int topk, float inv_t,
+                        int sample, uint32_t seed_lo, uint32_t seed_hi, int32_t* tokens,
+                        float* logprobs, const dspark_conf_args* conf, int* status,
+                        cudaStream_t stream);
+cudaError_t launch_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors,
+                              const int32_t* tokens, const uint16_t* w, float bias,
+                              int with_markov, int B, int K, int d, int r, int V,
+                              float threshold, float* conf, float* cumprod,
+                              int32_t* verify_len, int* status, cudaStream_t stream);
+
+}  // namespace dspark

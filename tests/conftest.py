@@ -18,3 +18,16 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def dsp():
+    """The CUDA library (built in-tree) and a context sized for the parity tests."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    from rank_markov_draft_gb300 import binding, build
+    build.build()
+    ctx = binding.Context(0, B_max=256, V_max=151936, K_max=64)
+    yield ctx
+    ctx.close()

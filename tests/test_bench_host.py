@@ -1,0 +1,64 @@
+"""Host-side logic of bench.py: byte accounting, replica seeding and the
+multi-rank timing reduction (two gloo ranks on CPU, no GPU)."""
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from synth import CONFIGS
+
+
+def test_algorithmic_bytes_per_block():
+    # W2 + U + gathered W1 rows per step, plus h for the confidence head / gate, plus Wg
+    assert bench.algorithmic_bytes(0, CONFIGS[0]) == 8_456_192
+    assert bench.algorithmic_bytes(1, CONFIGS[1]) == 1_254_391_808
+    assert bench.algorithmic_bytes(2, CONFIGS[2]) == 2_498_756_608
+    assert bench.algorithmic_bytes(3, CONFIGS[3]) == 1_877_999_616
+    assert bench.algorithmic_bytes(4, CONFIGS[4]) == 2_596_536_320
+
+
+def test_replica_seeds_are_distinct_per_rank_and_step():
+    seeds = {bench.replica_seed(r, s) for r in range(8) for s in range(100)}
+    assert len(seeds) == 800
+    assert bench.replica_seed(0, 7) == 7
+
+
+def test_job_throughput_is_weak_scaling():
+    one = bench.job_throughput(2048, 10, 1, 5.0)
+    assert bench.job_throughput(2048, 10, 4, 5.0) == pytest.approx(4 * one)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist = bench.init_dist(world, "gloo")
+    bench.barrier(world)
+    slowest = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+    value = bench.job_throughput(128 * 16, 20, world, slowest)
+    q.put((rank, slowest, value))
+    dist.destroy_process_group()
+
+
+def test_two_rank_timing_reduction_with_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # both ranks see the slowest rank's time and the same whole-job throughput
+    assert res[0][1] == res[1][1] == 15.0
+    assert res[0][2] == res[1][2] == pytest.approx(2 * 128 * 16 * 20 / 0.015)
