@@ -109,6 +109,16 @@ int dspark_get_status(dspark_ctx* ctx, int* device_status);
  * the knob off and timeout_ms <= 0 restores the default limit (2000 ms). */
 int dspark_debug_set(dspark_ctx* ctx, int cta, int timeout_ms);
 
+/* Profiling knob: the next draft launch (its first 128-request chunk) writes
+ * global-timer stamps (ns) of every CTA's step phases into device_buffer,
+ * laid out [grid][K][8] as unsigned 64-bit values: slot 0 step start, 1
+ * embeddings gathered, 2 first accumulator ready, 3 last tile done, 4 partial
+ * published, 5 grid barrier passed, 6 (last step only) final reduction done.
+ * Unused slots are left untouched.  capacity counts 64-bit entries; a launch
+ * whose trace would not fit writes nothing.  device_buffer == NULL turns the
+ * trace off.  Source: none on the pages (a measurement aid of this library). */
+int dspark_debug_trace(dspark_ctx* ctx, unsigned long long* device_buffer, int64_t capacity);
+
 /* Text of a status code (static storage). */
 const char* dspark_strerror(int code);
 

@@ -29,7 +29,7 @@ OK, INVALID_ARG, UNSUPPORTED, CUDA, TIMEOUT, DEVICE_OOB, NO_DEVICE, POISONED, CA
 # Functions declared in include/dspark.h (checked against the header by the tests).
 EXPORTS = (
     "dspark_ctx_create", "dspark_ctx_destroy", "dspark_ctx_reset", "dspark_get_status",
-    "dspark_debug_set", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
+    "dspark_debug_set", "dspark_debug_trace", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
 )
@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH):
         "dspark_ctx_reset": [P, P],
         "dspark_get_status": [P, ctypes.POINTER(I)],
         "dspark_debug_set": [P, I, I],
+        "dspark_debug_trace": [P, P, ctypes.c_int64],
         "dspark_strerror": [I],
         "dspark_abi_version": [],
         "dspark_last_launch_count": [P],
@@ -166,6 +167,14 @@ class Context:
 
     def debug_set(self, cta: int = -1, timeout_ms: int = 0):
         _check(self.lib.dspark_debug_set(self.handle, cta, timeout_ms), "dspark_debug_set")
+
+    def trace_next(self, buf: Optional[torch.Tensor]):
+        """Record the next draft launch's phase stamps into buf (int64, >= grid * K * 8)."""
+        if buf is None:
+            _check(self.lib.dspark_debug_trace(self.handle, None, 0), "dspark_debug_trace")
+            return
+        _check(self.lib.dspark_debug_trace(self.handle, _ptr(buf, (torch.int64,), "trace"),
+                                           buf.numel()), "dspark_debug_trace")
 
     @property
     def last_launches(self) -> int:

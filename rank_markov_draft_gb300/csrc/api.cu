@@ -13,6 +13,7 @@
 
 #include "../../include/dspark.h"
 #include "internal.h"
+#include "philox.cuh"
 
 using dspark::DraftArgs;
 using dspark::DraftParams;
@@ -35,6 +36,8 @@ struct dspark_ctx {
   int debug_skip_cta = -1;
   uint64_t timeout_ns = dspark::kDefaultTimeoutNs;
   int last_launches = 0;
+  unsigned long long* trace = nullptr;  // caller's device buffer for the next draft's phase trace
+  int64_t trace_capacity = 0;
 };
 
 namespace {
@@ -203,6 +206,7 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.inv_t = inv_t;
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    dspark::philox_round_keys(p.seed_lo, p.seed_hi, p.round_key0, p.round_key1);
     const size_t o = static_cast<size_t>(b0) * K;
     p.tokens = tokens ? tokens + o : nullptr;
     p.logprobs = logprobs ? logprobs + o : nullptr;
@@ -228,12 +232,16 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     if (st != DSPARK_OK) return st;
     p.debug_skip_cta = ctx->debug_skip_cta;
     p.timeout_ns = ctx->timeout_ns;
+    if (ctx->trace != nullptr &&
+        static_cast<int64_t>(grid) * K * dspark::kTraceSlots <= ctx->trace_capacity && b0 == 0)
+      p.trace = ctx->trace;
     cudaError_t e = dspark::launch_draft(args, mode, grid, stream);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
     ctx->bar_counter += static_cast<uint32_t>(K) * static_cast<uint32_t>(grid);
     ctx->last_launches += 1;
   }
-  ctx->debug_skip_cta = -1;  // the fault-injection knob covers one call
+  ctx->debug_skip_cta = -1;  // the fault-injection and trace knobs cover one call
+  ctx->trace = nullptr;
   return DSPARK_OK;
 }
 
@@ -379,6 +387,16 @@ int dspark_debug_set(dspark_ctx* ctx, int cta, int timeout_ms) {
 }
 
 int dspark_last_launch_count(dspark_ctx* ctx) { return ctx ? ctx->last_launches : -1; }
+
+int dspark_debug_trace(dspark_ctx* ctx, unsigned long long* device_buffer, int64_t capacity) {
+  if (ctx == nullptr || (device_buffer == nullptr && capacity != 0) || capacity < 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (device_buffer != nullptr && (reinterpret_cast<uintptr_t>(device_buffer) & 7u) != 0)
+    return DSPARK_ERR_INVALID_ARG;
+  ctx->trace = device_buffer;
+  ctx->trace_capacity = capacity;
+  return DSPARK_OK;
+}
 
 int dspark_markov_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1, const uint16_t* W2,
                         const int32_t* anchors, int B, int K, int V, int r, float temperature,

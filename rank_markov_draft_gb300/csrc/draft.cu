@@ -102,6 +102,12 @@ __device__ __forceinline__ uint32_t key_epoch(unsigned long long key) {
   return static_cast<uint32_t>(key >> 50);
 }
 
+// Optional phase trace: global-timer stamps of CTA `cta` at step k (thread etid 0).
+__device__ __forceinline__ void trace_stamp(const DraftParams& p, int cta, int k, int slot) {
+  if (p.trace != nullptr)
+    p.trace[(static_cast<size_t>(cta) * p.K + k) * kTraceSlots + slot] = globaltimer_ns();
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
@@ -356,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 
     for (int k = 0; k < p.K; ++k) {
       // ---- gather the step's embeddings (after the previous step's MMAs released E)
+      if (etid == 0) trace_stamp(p, cta, k, 0);
       if (k > 0) {
         if (!mbar_wait(a_empty, (k - 1) & 1, p.timeout_ns, abort_flag)) {
           fail = true;
@@ -383,11 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
       fence_proxy_async_smem();
       named_bar_sync(kEpiBarrier, kEpiThreads);
-      if (etid == 0) mbar_arrive(a_full);
+      if (etid == 0) {
+        mbar_arrive(a_full);
+        trace_stamp(p, cta, k, 1);
+      }
 
       // ---- stream the step's tiles
       float m2 = -INFINITY, sum = 0.f;
-      float wb = 0.f, e2b = 1.f, wb1 = 0.f, wb2 = 0.f, yb = -INFINITY, lb = 0.f;
+      float wb = 0.f, e2b = 1.f, yb = -INFINITY, lb = 0.f;
+      float cthr = INFINITY;  // ln2 * e2b / wb: candidates need 1 - u < w * cthr
       int vb = 0x7FFFFFFF;
       for (int t = 0; t < nt && !fail; ++t) {
         const int i = k * nt + t;
@@ -401,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           break;
         }
         tc_fence_after();
+        if (t == 0 && etid == 0) trace_stamp(p, cta, k, 2);
         uint32_t acc[16];
         if (nkk > 0) {
           tmem_ld_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -433,76 +445,97 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (!row_ok) continue;
 
         const int vbase = (t_begin + t) * kTileV + g * 16;
-        float l[16], y[16];
-        float cmax = -INFINITY;
+        const bool full_chunk = vbase + 16 <= p.V;  // warp-uniform
+        float y[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          l[j] = uval[j] + __uint_as_float(acc[j]);
-          y[j] = (vbase + j < p.V) ? l[j] * scale2 : -INFINITY;
-          cmax = fmaxf(cmax, y[j]);
+          const float l = uval[j] + __uint_as_float(acc[j]);
+          y[j] = (full_chunk || vbase + j < p.V) ? l * scale2 : -INFINITY;
         }
         if (MODE == kModeTeacherForced) {
           float* dst = p.logits + (static_cast<size_t>(b) * p.K + k) * p.V + vbase;
-          if (vbase + 16 <= p.V) {
+          if (full_chunk) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              reinterpret_cast<float4*>(dst)[c] =
-                  make_float4(l[4 * c], l[4 * c + 1], l[4 * c + 2], l[4 * c + 3]);
+              reinterpret_cast<float4*>(dst)[c] = make_float4(
+                  uval[4 * c] + __uint_as_float(acc[4 * c]),
+                  uval[4 * c + 1] + __uint_as_float(acc[4 * c + 1]),
+                  uval[4 * c + 2] + __uint_as_float(acc[4 * c + 2]),
+                  uval[4 * c + 3] + __uint_as_float(acc[4 * c + 3]));
           } else {
-            for (int j = 0; j < 16 && vbase + j < p.V; ++j) dst[j] = l[j];
+            for (int j = 0; j < 16 && vbase + j < p.V; ++j)
+              dst[j] = uval[j] + __uint_as_float(acc[j]);
           }
         }
+        // chunk maximum (tree)
+        float mx[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx[j] = fmaxf(y[j], y[j + 8]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
+        const float cmax = fmaxf(fmaxf(mx[0], mx[2]), fmaxf(mx[1], mx[3]));
         if (cmax == -INFINITY) continue;  // nothing in this chunk can be drawn
         if (cmax > m2) {
           const float f = ex2_approx(m2 - cmax);
           sum *= f;
           wb *= f;
-          wb1 *= f;
-          wb2 *= f;
           m2 = cmax;
+          cthr = (wb > 0.f) ? e2b * kLn2 / wb : INFINITY;
         }
+        float w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = ex2_approx(y[j] - m2);
+        float ps[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ps[c] = (w[4 * c] + w[4 * c + 1]) + (w[4 * c + 2] + w[4 * c + 3]);
+        sum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         if (MODE == kModeSample) {
+          // An element can only beat the running winner (ratio wb / e2b) if its
+          // E = -ln u is below w * cthr; since -ln u >= 1 - u, elements with
+          // 1 - u >= w * cthr are out without evaluating any logarithm.
+          uint32_t words[16];
+          philox4x32_10_x4(static_cast<uint32_t>(vbase >> 2), static_cast<uint32_t>(k), b_global,
+                           p.round_key0, p.round_key1, words);
+          uint32_t cand = 0;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const Philox4 rnd = philox4x32_10(static_cast<uint32_t>((vbase >> 2) + jj),
-                                              static_cast<uint32_t>(k), b_global, 0u, p.seed_lo,
-                                              p.seed_hi);
+          for (int j = 0; j < 16; ++j)
+            cand |= (philox_one_minus_uniform(words[j]) < w[j] * cthr ? 1u : 0u) << j;
+          if (cand != 0u) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const int j = jj * 4 + w;
-              const float wv = ex2_approx(y[j] - m2);
-              sum += wv;
-              const float u = philox_uniform(rnd.w[w]);
-              const float e2f = -lg2_approx(u);
-              // fast reject: w / E cannot beat wb / e2b even with E at the low end of
-              // the approximation's error interval
-              if (wv * e2b > fmaf(wb1, e2f, -wb2)) {
-                const float e2 = neg_log_uniform_accurate(u) * kLog2e;
-                if (wv * e2b > wb * e2) {
-                  wb = wv;
+            for (int j = 0; j < 16; ++j) {
+              if ((cand >> j) & 1u) {
+                const float tj = philox_one_minus_uniform(words[j]);
+                const float uj = 1.0f - tj;  // exact
+                const float e = (uj < 0.5f) ? -logf(uj) : -log1pf(-tj);
+                const float e2 = e * kLog2e;
+                if (w[j] * e2b > wb * e2) {
+                  wb = w[j];
                   e2b = e2;
-                  wb1 = wv * (1.0f - 9.5367431640625e-7f);  // 1 - 2^-20
-                  wb2 = wv * 4.76837158203125e-7f;           // 2^-21
                   vb = vbase + j;
-                  lb = l[j];
+                  lb = uval[j] + __uint_as_float(acc[j]);
+                  cthr = e2b * kLn2 / wb;
                 }
               }
             }
           }
-        } else {
+        } else if (MODE == kModeGreedy) {
+          if (cmax > yb) {
+            int jb = 15;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            sum += ex2_approx(y[j] - m2);
-            if (MODE == kModeGreedy && y[j] > yb) {
-              yb = y[j];
-              vb = vbase + j;
-              lb = l[j];
-            }
+            for (int j = 15; j >= 0; --j)
+              if (y[j] == cmax) jb = j;
+            yb = cmax;
+            vb = vbase + jb;
+            lb = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j == jb) lb = uval[j] + __uint_as_float(acc[j]);
           }
         }
       }
 
       // ---- merge the four column groups of each request, publish the CTA's partial
+      if (etid == 0) trace_stamp(p, cta, k, 3);
       float score;
       if (MODE == kModeSample) {
         score = (vb != 0x7FFFFFFF) ? lb * scale2 - log2f(e2b) : -INFINITY;
@@ -546,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 
       // ---- grid barrier (bounded)
       bool bar_fail = false;
+      if (etid == 0) trace_stamp(p, cta, k, 4);
       if (etid == 0 && !fail) {
         const bool skip = (p.debug_skip_cta == cta) && (k == 0);
         if (!skip) {
@@ -568,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
         }
         __threadfence();
+        trace_stamp(p, cta, k, 5);
       }
       const bool any = named_bar_or(kEpiBarrier, kEpiThreads, fail || bar_fail || *abort_flag);
       if (any) {
@@ -657,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         named_bar_sync(kEpiBarrier, kEpiThreads);
       }
+      if (etid == 0) trace_stamp(p, cta, p.K - 1, 6);
     }
   }
 

@@ -15,6 +15,7 @@ constexpr int kMaxRank = 256;       // Markov rank
 constexpr int kBatchChunk = 128;    // requests per draft launch (MMA M)
 constexpr int kDraftTileV = 64;     // vocabulary entries per draft tile (MMA N)
 constexpr int kMaxTopk = 32;
+constexpr int kTraceSlots = 8;      // timestamps per (CTA, step) in the draft trace
 constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
 
 // Per-(step, request, CTA) record of the draft kernel's cross-CTA reduction.
@@ -37,6 +38,8 @@ struct DraftParams {
   int box_rows;             // rows of the U TMA box (multiple of 8, >= B)
   float inv_t;              // 1 / T' (T' = T, or 1 when greedy)
   uint32_t seed_lo, seed_hi;
+  uint32_t round_key0[10];  // Philox key schedule (seed_lo + i * Weyl0), host-computed
+  uint32_t round_key1[10];  // (seed_hi + i * Weyl1)
   int32_t* tokens;          // [B, K] (chunk)
   float* logprobs;          // [B, K] (chunk)
   float* logits;            // teacher-forced: [B, K, V] (chunk)
@@ -59,6 +62,7 @@ struct DraftParams {
   uint32_t bar_base;        // counter value at launch
   uint32_t epoch;           // key epoch of this launch (1 .. 16383)
   int debug_skip_cta;       // fault injection: CTA skipping its step-0 arrival (-1: none)
+  unsigned long long* trace;  // optional phase timestamps [grid][K][kTraceSlots] (null: off)
   uint64_t timeout_ns;      // per-wait limit
 };
 
