@@ -34,7 +34,8 @@
  *  - Noise: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
  *    Numbers: As Easy as 1, 2, 3", SC'11), key = (seed low 32, seed high 32),
  *    counter = (v >> 2, k, b, 0); word v & 3 of the output gives
- *    u = ((word >> 9) + 0.5) * 2^-23, exactly representable in fp32 and fp64
+ *    u = ((word & 0x7FFFFF) + 0.5) * 2^-23 (the low 23 bits), exactly
+ *    representable in fp32 and fp64
  *    and strictly inside (0, 1); g = -ln(-ln u).
  */
 #include <math.h>
@@ -118,7 +119,7 @@ double orc_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t v, uint32_t t
   uint32_t out[4];
   orc_philox4x32_10(ctr, key, out);
   uint32_t word = out[v & 3u];
-  return ((double)(word >> 9) + 0.5) * (1.0 / 8388608.0); /* 2^-23 */
+  return ((double)(word & 0x7FFFFFu) + 0.5) * (1.0 / 8388608.0); /* 2^-23 */
 }
 
 /* Standard Gumbel variate g = -ln(-ln u). */

@@ -41,8 +41,8 @@ def test_uniform_grid_and_word_selection(orc):
     for (b, k, v) in [(0, 0, 0), (3, 7, 5), (127, 15, 151935), (1, 2, 4)]:
         out = orc.philox4x32_10([v >> 2, k, b, 0], [seed & 0xFFFFFFFF, seed >> 32])
         u = orc.uniform(seed, b, k, v)
-        # u = (2 * (word >> 9) + 1) * 2^-24: an odd multiple of 2^-24, strictly inside (0, 1)
-        assert u == ((int(out[v & 3]) >> 9) * 2 + 1) * 2.0 ** -24
+        # u = (2 * (word & 0x7FFFFF) + 1) * 2^-24: an odd multiple of 2^-24 inside (0, 1)
+        assert u == ((int(out[v & 3]) & 0x7FFFFF) * 2 + 1) * 2.0 ** -24
         assert 0.0 < u < 1.0
         assert np.float32(u) == u  # exactly representable in fp32
         assert orc.gumbel(seed, b, k, v) == -np.log(-np.log(u))
