@@ -30,7 +30,7 @@
  *   drawn token under softmax(l / T'), T' = T (T > 0) or 1 (T == 0).
  * Noise.  Philox4x32-10 (Salmon et al., SC'11) keyed by (seed low 32 bits,
  *   seed high 32 bits) with counter (v >> 2, k, b, 0); word v & 3 gives
- *   u = ((word >> 9) + 0.5) * 2^-23 and the Gumbel variate -ln(-ln u).  b is
+ *   u = ((word & 0x7FFFFF) + 0.5) * 2^-23 and the Gumbel variate -ln(-ln u).  b is
  *   the request's index in the call's batch, k its 0-based block position,
  *   v the token id.  The same (seed, b, k, v) always yields the same noise.
  * Ties.  Argmax and top-k orders break ties to the smaller token id.

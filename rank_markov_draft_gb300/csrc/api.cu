@@ -11,7 +11,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/dspark.h"
+#include "dspark.h"
 #include "internal.h"
 #include "philox.cuh"
 

@@ -47,6 +47,9 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#ifndef BOUND_REFRESH
+#define BOUND_REFRESH 2
+#endif
 #include "confidence.cuh"
 #include "internal.h"
 #include "philox.cuh"
@@ -57,8 +60,8 @@ namespace {
 
 constexpr int kTileV = kDraftTileV;              // 64 tokens per tile (MMA N)
 constexpr int kRows = kBatchChunk;               // 128 requests (MMA M)
-constexpr int kNumW2Stages = 3;
-constexpr int kNumUStages = 2;
+constexpr int kNumW2Stages = 2;
+constexpr int kNumUStages = 3;
 constexpr int kNumAcc = 4;                       // TMEM accumulators, 64 columns each
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;      // 512
@@ -71,16 +74,23 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffW2 = kOffA + kABytes;
 constexpr uint32_t kOffU = kOffW2 + kNumW2Stages * kW2StageBytes;
 constexpr uint32_t kOffBar = kOffU + kNumUStages * kUStageBytes;
-constexpr uint32_t kBarRegion = 1024;
+constexpr uint32_t kBarRegion = 2048;
 constexpr uint32_t kSmemBytes = kOffBar + kBarRegion + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = kNumAcc * kTileV;             // 256
 constexpr uint32_t kEpiBarrier = 1;                          // named barrier id
+constexpr int kBoundRefresh = BOUND_REFRESH;  // tiles between reads of the global bound
+constexpr uint32_t kBackoffControlNs = 200;  // sleep between polls of the TMA / MMA lanes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr uint32_t kTokenBits = 18;                          // V <= 2^18
 constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
 
 static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103 limit");
+static_assert((kNumAcc & (kNumAcc - 1)) == 0, "accumulator count must be a power of two");
+static_assert((2 * kNumW2Stages + 2 * kNumUStages + 2 * kNumAcc + 5) * 8 + 2 * kMaxK * 4 +
+                      kRows * 8 <=
+                  kBarRegion,
+              "barrier region too small");
 
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   const uint32_t b = __float_as_uint(f);
@@ -160,6 +170,44 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
   }
 }
 
+// The Philox word of token v (rare path: recomputed rather than kept live).
+__device__ __forceinline__ uint32_t philox_word(int v, uint32_t k, uint32_t b,
+                                                const DraftParams& p) {
+  uint32_t words[4];
+  philox4x32_10_xn<1>(static_cast<uint32_t>(v) >> 2, k, b, p.round_key0, p.round_key1, words);
+  const int sel = v & 3;
+  return sel == 0 ? words[0] : sel == 1 ? words[1] : sel == 2 ? words[2] : words[3];
+}
+
+// Exact comparison of one candidate of the exponential race against the
+// running winner (wb / e2b): E = -ln u evaluated accurately (log1p near u = 1),
+// kept out of line so the hot loop stays small.
+__device__ __forceinline__ bool exact_race_update(float wj, uint32_t word, float lj, int v,
+                                                  float& wb, float& e2b, int& vb, float& lb,
+                                                  float& cthr) {
+  const float tj = philox_one_minus_uniform(word);
+  const float uj = 1.0f - tj;  // exact
+  const float e = (uj < 0.5f) ? -logf(uj) : -log1pf(-tj);
+  const float e2 = e * kLog2e;
+  if (wj * e2b > wb * e2) {
+    wb = wj;
+    e2b = e2;
+    vb = v;
+    lb = lj;
+    cthr = e2b * kLn2 / wb;
+    return true;
+  }
+  return false;
+}
+
+// Score of a key (the ordered float in its middle bits); -inf for "no key".
+__device__ __forceinline__ float key_score(unsigned long long key) {
+  if (key == 0ull) return -INFINITY;
+  const uint32_t ob = static_cast<uint32_t>(key >> kTokenBits);
+  const uint32_t bits = (ob & 0x80000000u) ? (ob & 0x7FFFFFFFu) : ~ob;
+  return __uint_as_float(bits);
+}
+
 __device__ __forceinline__ void load_partial(const DraftPartial* src, unsigned long long& key,
                                              float& m2, float& sum, float& lbest) {
   key = __ldcg(reinterpret_cast<const unsigned long long*>(src));
@@ -195,18 +243,21 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   uint8_t* sW = smem + kOffW2;
   uint8_t* sU = smem + kOffU;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* w_full = bars;          // [3]
-  uint64_t* w_empty = bars + 3;     // [3]
-  uint64_t* u_full = bars + 6;      // [2]
-  uint64_t* u_empty = bars + 8;     // [2]
-  uint64_t* acc_full = bars + 10;   // [4]
-  uint64_t* acc_empty = bars + 14;  // [4]
-  uint64_t* a_full = bars + 18;
-  uint64_t* a_empty = bars + 19;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
-  int32_t* s_tok = reinterpret_cast<int32_t*>(bars + 22);   // [kMaxK]
+  uint64_t* w_full = bars;                          // [kNumW2Stages]
+  uint64_t* w_empty = w_full + kNumW2Stages;        // [kNumW2Stages]
+  uint64_t* u_full = w_empty + kNumW2Stages;        // [kNumUStages]
+  uint64_t* u_empty = u_full + kNumUStages;         // [kNumUStages]
+  uint64_t* acc_full = u_empty + kNumUStages;       // [kNumAcc]
+  uint64_t* acc_empty = acc_full + kNumAcc;         // [kNumAcc]
+  uint64_t* a_full = acc_empty + kNumAcc;
+  uint64_t* a_empty = a_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_empty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(a_empty + 2);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(a_empty + 3);  // [kMaxK]
   float* s_conf = reinterpret_cast<float*>(s_tok + kMaxK);  // [kMaxK]
+  // best key (epoch | score | token) any thread of this CTA reached for each
+  // request in the current step: a lower bound on the step's winner
+  unsigned long long* s_bound = reinterpret_cast<unsigned long long*>(s_conf + kMaxK);  // [128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x, ncta = gridDim.x;
@@ -259,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           const int v0 = (t_begin + t) * kTileV;
           if (nkk > 0) {
             const int s = i % kNumW2Stages;
-            if (!mbar_wait(&w_empty[s], ((i / kNumW2Stages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            if (!mbar_wait(&w_empty[s], ((i / kNumW2Stages) & 1) ^ 1, p.timeout_ns, abort_flag,
+                           kBackoffControlNs)) {
               ok = false;
               break;
             }
@@ -268,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             w_issued = i + 1;
           }
           const int su = i % kNumUStages;
-          if (!mbar_wait(&u_empty[su], ((i / kNumUStages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+          if (!mbar_wait(&u_empty[su], ((i / kNumUStages) & 1) ^ 1, p.timeout_ns, abort_flag,
+                         kBackoffControlNs)) {
             ok = false;
             break;
           }
@@ -298,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       bool ok = true;
       int last_i = -1;
       for (int k = 0; k < p.K && ok; ++k) {
-        if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag)) {
+        if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag, kBackoffControlNs)) {
           ok = false;
           break;
         }
@@ -307,11 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           const int i = k * nt + t;
           const int s = i % kNumW2Stages, buf = i % kNumAcc;
           if (nkk > 0 &&
-              !mbar_wait(&w_full[s], (i / kNumW2Stages) & 1, p.timeout_ns, abort_flag)) {
+              !mbar_wait(&w_full[s], (i / kNumW2Stages) & 1, p.timeout_ns, abort_flag,
+                        kBackoffControlNs)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&acc_empty[buf], ((i / kNumAcc) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+          if (!mbar_wait(&acc_empty[buf], ((i / kNumAcc) & 1) ^ 1, p.timeout_ns, abort_flag,
+                         kBackoffControlNs)) {
             ok = false;
             break;
           }
@@ -357,8 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     const uint32_t b_global = static_cast<uint32_t>(p.b_global0 + b);
     const float scale2 = p.inv_t * kLog2e;
     float* merge = reinterpret_cast<float*>(sA);  // reused after a step's MMAs completed
+    // this thread's four 16-byte pieces of its U row within a stage (128B swizzle)
+    uint32_t u_off[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      u_off[c] = (g >> 1) * kUBoxBytes + b * 128 + ((((g & 1) * 4 + c) ^ (b & 7)) << 4);
     bool fail = false;
     bool aborted = false;
+    int u_stage = 0;        // U ring slot of the next tile
+    uint32_t u_phase = 0;   // its mbarrier phase parity
 
     for (int k = 0; k < p.K; ++k) {
       // ---- gather the step's embeddings (after the previous step's MMAs released E)
@@ -387,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
         }
         if (!fail) gather_embeddings(sA, p, k, etid, tok);
+        if (etid < kRows) s_bound[etid] = 0ull;
       }
       fence_proxy_async_smem();
       named_bar_sync(kEpiBarrier, kEpiThreads);
@@ -400,11 +463,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       float wb = 0.f, e2b = 1.f, yb = -INFINITY, lb = 0.f;
       float cthr = INFINITY;  // ln2 * e2b / wb: candidates need 1 - u < w * cthr
       int vb = 0x7FFFFFFF;
+      unsigned long long gkey = 0ull;  // global key of this request and step, as last read
       for (int t = 0; t < nt && !fail; ++t) {
+        if (MODE == kModeSample && row_ok && (t & (kBoundRefresh - 1)) == 0) {
+          // the freshest bound matters most early in the step; the load overlaps the
+          // tile's barrier waits and operand loads before its first use
+          const unsigned long long kk = __ldcg(p.keys + k * kRows + b);
+          if (key_epoch(kk) == p.epoch && kk > gkey) gkey = kk;
+        }
         const int i = k * nt + t;
-        const int buf = i % kNumAcc, su = i % kNumUStages;
+        const int buf = i & (kNumAcc - 1);
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
-        ok = ok && mbar_wait(&u_full[su], (i / kNumUStages) & 1, p.timeout_ns, abort_flag);
+        ok = ok && mbar_wait(&u_full[u_stage], u_phase, p.timeout_ns, abort_flag);
+        const int su = u_stage;
+        if (++u_stage == kNumUStages) {
+          u_stage = 0;
+          u_phase ^= 1u;
+        }
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
           fail = true;
@@ -425,11 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         float uval[16];
         {
-          const uint8_t* rowp = sU + su * kUStageBytes + (g >> 1) * kUBoxBytes + b * 128;
-          const int c0 = (g & 1) * 4;
+          const uint8_t* ubase = sU + su * kUStageBytes;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const float4 x = *reinterpret_cast<const float4*>(rowp + (((c0 + c) ^ (b & 7)) << 4));
+            const float4 x = *reinterpret_cast<const float4*>(ubase + u_off[c]);
             uval[4 * c + 0] = x.x;
             uval[4 * c + 1] = x.y;
             uval[4 * c + 2] = x.z;
@@ -446,25 +520,32 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 
         const int vbase = (t_begin + t) * kTileV + g * 16;
         const bool full_chunk = vbase + 16 <= p.V;  // warp-uniform
-        float y[16];
+        float l[16], y[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float l = uval[j] + __uint_as_float(acc[j]);
-          y[j] = (full_chunk || vbase + j < p.V) ? l * scale2 : -INFINITY;
+        for (int j = 0; j < 16; j += 2) {
+          const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
+                                       make_float2(__uint_as_float(acc[j]),
+                                                   __uint_as_float(acc[j + 1])));
+          const float2 yj = __fmul2_rn(lj, make_float2(scale2, scale2));
+          l[j] = lj.x;
+          l[j + 1] = lj.y;
+          y[j] = yj.x;
+          y[j + 1] = yj.y;
+        }
+        if (!full_chunk) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (vbase + j >= p.V) y[j] = -INFINITY;
         }
         if (MODE == kModeTeacherForced) {
           float* dst = p.logits + (static_cast<size_t>(b) * p.K + k) * p.V + vbase;
           if (full_chunk) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              reinterpret_cast<float4*>(dst)[c] = make_float4(
-                  uval[4 * c] + __uint_as_float(acc[4 * c]),
-                  uval[4 * c + 1] + __uint_as_float(acc[4 * c + 1]),
-                  uval[4 * c + 2] + __uint_as_float(acc[4 * c + 2]),
-                  uval[4 * c + 3] + __uint_as_float(acc[4 * c + 3]));
+              reinterpret_cast<float4*>(dst)[c] =
+                  make_float4(l[4 * c], l[4 * c + 1], l[4 * c + 2], l[4 * c + 3]);
           } else {
-            for (int j = 0; j < 16 && vbase + j < p.V; ++j)
-              dst[j] = uval[j] + __uint_as_float(acc[j]);
+            for (int j = 0; j < 16 && vbase + j < p.V; ++j) dst[j] = l[j];
           }
         }
         // chunk maximum (tree)
@@ -484,38 +565,87 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         float w[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = ex2_approx(y[j] - m2);
-        float ps[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ps[c] = (w[4 * c] + w[4 * c + 1]) + (w[4 * c + 2] + w[4 * c + 3]);
-        sum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        for (int j = 0; j < 16; j += 2) {
+          const float2 dj = __fadd2_rn(make_float2(y[j], y[j + 1]), make_float2(-m2, -m2));
+          w[j] = ex2_approx(dj.x);
+          w[j + 1] = ex2_approx(dj.y);
+        }
+        {
+          float2 s0 = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
+          float2 s1 = __fadd2_rn(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
+          float2 s2 = __fadd2_rn(make_float2(w[8], w[9]), make_float2(w[10], w[11]));
+          float2 s3 = __fadd2_rn(make_float2(w[12], w[13]), make_float2(w[14], w[15]));
+          s0 = __fadd2_rn(__fadd2_rn(s0, s1), __fadd2_rn(s2, s3));
+          sum += s0.x + s0.y;
+        }
         if (MODE == kModeSample) {
           // An element can only beat the running winner (ratio wb / e2b) if its
           // E = -ln u is below w * cthr; since -ln u >= 1 - u, elements with
           // 1 - u >= w * cthr are out without evaluating any logarithm.
-          uint32_t words[16];
-          philox4x32_10_x4(static_cast<uint32_t>(vbase >> 2), static_cast<uint32_t>(k), b_global,
-                           p.round_key0, p.round_key1, words);
+          const uint32_t kc = static_cast<uint32_t>(k);
+          if (wb == 0.f) {
+            // first live chunk of the step: seed the winner with the chunk's largest
+            // weight (exactly evaluated) so the bound below is finite
+            int js = 0;
+            float wj = 0.f, lj = 0.f;
+#pragma unroll
+            for (int q2 = 15; q2 >= 0; --q2) {
+              if (w[q2] == 1.0f) {  // y == cmax == m2 in the first live chunk
+                js = q2;
+                wj = w[q2];
+                lj = l[q2];
+              }
+            }
+            if (exact_race_update(wj, philox_word(vbase + js, kc, b_global, p), lj, vbase + js,
+                                  wb, e2b, vb, lb, cthr))
+              atomicMax(&s_bound[b], make_key(p.epoch, lb * scale2 - log2f(e2b), vb));
+          }
+          // Any score already reached for this request (here, in this CTA, or
+          // published by another CTA) bounds the winner from below: an element
+          // needs y - log2(E2) > S, i.e. E < w * ln2 * 2^(m2 - S).
+          const unsigned long long bkey = s_bound[b] > gkey ? s_bound[b] : gkey;
+          const float S = key_score(bkey);
+          const float cth = fminf(cthr, kLn2 * ex2_approx(m2 - S));
+          const float2 cth2 = make_float2(cth, cth);
+          const float2 negc = make_float2(-0.99999994039535522461f, -0.99999994039535522461f);
           uint32_t cand = 0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            cand |= (philox_one_minus_uniform(words[j]) < w[j] * cthr ? 1u : 0u) << j;
-          if (cand != 0u) {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t words[8];
+            philox4x32_10_xn<2>(static_cast<uint32_t>(vbase >> 2) + 2 * half, kc, b_global,
+                                p.round_key0, p.round_key1, words);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if ((cand >> j) & 1u) {
-                const float tj = philox_one_minus_uniform(words[j]);
-                const float uj = 1.0f - tj;  // exact
-                const float e = (uj < 0.5f) ? -logf(uj) : -log1pf(-tj);
-                const float e2 = e * kLog2e;
-                if (w[j] * e2b > wb * e2) {
-                  wb = w[j];
-                  e2b = e2;
-                  vb = vbase + j;
-                  lb = uval[j] + __uint_as_float(acc[j]);
-                  cthr = e2b * kLn2 / wb;
-                }
+            for (int j = 0; j < 8; j += 2) {
+              const int jj = 8 * half + j;
+              const float2 t2 = __fadd2_rn(make_float2(philox_one_plus_complement(words[j]),
+                                                       philox_one_plus_complement(words[j + 1])),
+                                           negc);  // 1 - u, exact
+              const float2 x2 = __fmul2_rn(make_float2(w[jj], w[jj + 1]), cth2);
+              if (t2.x < x2.x) cand |= 1u << jj;
+              if (t2.y < x2.y) cand |= 2u << jj;
+            }
+          }
+          while (cand != 0u) {  // rare: a few per thread and step
+            const int j = __ffs(cand) - 1;
+            cand &= cand - 1u;
+            float wj = 0.f, lj = 0.f;
+#pragma unroll
+            for (int q2 = 0; q2 < 16; ++q2) {
+              if (q2 == j) {
+                wj = w[q2];
+                lj = l[q2];
               }
+            }
+            if (exact_race_update(wj, philox_word(vbase + j, kc, b_global, p), lj, vbase + j, wb,
+                                  e2b, vb, lb, cthr))
+              atomicMax(&s_bound[b], make_key(p.epoch, lb * scale2 - log2f(e2b), vb));
+          }
+          if ((t & 1) == 1 && g == 0) {
+            // share this CTA's best with the other CTAs (rate-limited)
+            const unsigned long long mine = s_bound[b];
+            if (mine > gkey) {
+              atomicMax(p.keys + k * kRows + b, mine);
+              gkey = mine;
             }
           }
         } else if (MODE == kModeGreedy) {
@@ -529,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             lb = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (j == jb) lb = uval[j] + __uint_as_float(acc[j]);
+              if (j == jb) lb = l[j];
           }
         }
       }

@@ -6,7 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/dspark.h"
+#include "dspark.h"
 
 namespace dspark {
 

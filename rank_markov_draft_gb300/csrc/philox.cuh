@@ -8,7 +8,7 @@
 // Token-sampling noise of the Markov head (the pages ask for a counter-based
 // generator keyed on request, position and token): counter = (v >> 2, k, b, 0),
 // key = (seed low, seed high); word v & 3 becomes
-// u = ((word >> 9) + 0.5) * 2^-23, an odd multiple of 2^-24 in (0, 1).
+// u = ((word & 0x7FFFFF) + 0.5) * 2^-23, an odd multiple of 2^-24 in (0, 1).
 #pragma once
 
 #include <cstdint>
@@ -53,18 +53,20 @@ __host__ __device__ inline void philox_round_keys(uint32_t k0, uint32_t k1, uint
   }
 }
 
-// Four Philox4x32-10 blocks with counters (c0 + q, c1, c2, 0), q = 0..3, and a
+// N Philox4x32-10 blocks with counters (c0 + q, c1, c2, 0), q = 0..N-1, and a
 // precomputed key schedule, interleaved round by round for instruction-level
 // parallelism; out[4 q + w] = word w of block q.  Round 0 of every block shares
 // the product M1 * c2, computed once.
-__device__ __forceinline__ void philox4x32_10_x4(uint32_t c0, uint32_t c1, uint32_t c2,
+template <int N>
+__device__ __forceinline__ void philox4x32_10_xn(uint32_t c0, uint32_t c1, uint32_t c2,
                                                  const uint32_t (&rk0)[10],
-                                                 const uint32_t (&rk1)[10], uint32_t (&out)[16]) {
-  uint32_t x0[4], x1[4], x2[4], x3[4];
+                                                 const uint32_t (&rk1)[10],
+                                                 uint32_t (&out)[4 * N]) {
+  uint32_t x0[N], x1[N], x2[N], x3[N];
   const uint64_t pb0 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
   const uint32_t n0_r0 = static_cast<uint32_t>(pb0 >> 32) ^ c1 ^ rk0[0];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < N; ++q) {
     const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * (c0 + q);
     x0[q] = n0_r0;
     x1[q] = static_cast<uint32_t>(pb0);
@@ -74,7 +76,7 @@ __device__ __forceinline__ void philox4x32_10_x4(uint32_t c0, uint32_t c1, uint3
 #pragma unroll
   for (int round = 1; round < 10; ++round) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < N; ++q) {
       const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * x0[q];
       const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * x2[q];
       const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ x1[q] ^ rk0[round];
@@ -86,7 +88,7 @@ __device__ __forceinline__ void philox4x32_10_x4(uint32_t c0, uint32_t c1, uint3
     }
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < N; ++q) {
     out[4 * q + 0] = x0[q];
     out[4 * q + 1] = x1[q];
     out[4 * q + 2] = x2[q];
@@ -94,18 +96,24 @@ __device__ __forceinline__ void philox4x32_10_x4(uint32_t c0, uint32_t c1, uint3
   }
 }
 
-// t = 1 - u for the uniform u of `word`: with n = word >> 9, u = (n + 0.5) 2^-23
-// and 1 - u = (n' + 0.5) 2^-23 with n' = 2^23 - 1 - n, built exactly like u.
+// t = 1 - u for the uniform u of `word`: with n = word & 0x7FFFFF,
+// u = (n + 0.5) 2^-23 and 1 - u = (n' + 0.5) 2^-23 with n' = 2^23 - 1 - n, the
+// low 23 bits of ~word; built exactly like u.
 __device__ __forceinline__ float philox_one_minus_uniform(uint32_t word) {
-  const float one_plus = __uint_as_float(0x3F800000u | ((~word) >> 9));
-  return one_plus - 0.99999994039535522461f;  // 1 - 2^-24
+  const float one_plus = __uint_as_float(0x3F800000u | (~word & 0x7FFFFFu));
+  return one_plus - 0.99999994039535522461f;  // 1 - 2^-24, exact result
 }
 
-// u = ((word >> 9) + 0.5) * 2^-23 computed without an int->float conversion:
-// 1 + n * 2^-23 is built from the mantissa bits, and subtracting 1 - 2^-24 is
-// exact (the result is an odd multiple of 2^-24 below 1).
+// 1 + n' 2^-23 (the operand of the subtraction above), one logic op.
+__device__ __forceinline__ float philox_one_plus_complement(uint32_t word) {
+  return __uint_as_float(0x3F800000u | (~word & 0x7FFFFFu));
+}
+
+// u = ((word & 0x7FFFFF) + 0.5) * 2^-23 computed without an int->float
+// conversion: 1 + n * 2^-23 is built from the mantissa bits, and subtracting
+// 1 - 2^-24 is exact (the result is an odd multiple of 2^-24 below 1).
 __device__ __forceinline__ float philox_uniform(uint32_t word) {
-  const float one_plus = __uint_as_float(0x3F800000u | (word >> 9));
+  const float one_plus = __uint_as_float(0x3F800000u | (word & 0x7FFFFFu));
   return one_plus - 0.99999994039535522461f;  // 1 - 2^-24
 }
 

@@ -54,14 +54,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One bounded wait attempt: the thread is suspended until the phase completes
+// or `suspend_ns` elapses, so a waiting warp issues no instructions meanwhile.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t suspend_ns = 1000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -69,13 +72,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when the CTA-wide abort flag is raised (if given) or when
 // `timeout_ns` of global time has passed since the first check; never spins
-// without bound.
+// without bound.  After a failed poll the thread sleeps `backoff_ns`, so that
+// waiting warps leave the issue slots to the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint32_t backoff_ns = 64u) {
+  if (mbar_try_wait(bar, parity)) return true;
   uint64_t deadline = 0;
   for (uint32_t it = 0;; ++it) {
+    __nanosleep(backoff_ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 31u) {
+    if ((it & 7u) == 7u) {
       if (abort_flag != nullptr && *abort_flag) return false;
       const uint64_t now = globaltimer_ns();
       if (deadline == 0) {
@@ -127,6 +133,22 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
       "l"(policy)
       : "memory");
+}
+
+// L2 prefetch of a tensor tile (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
