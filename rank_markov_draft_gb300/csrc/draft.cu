@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       bool ok = true;
       int last_i = -1;
       for (int k = 0; k < p.K && ok; ++k) {
-        if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag, kBackoffControlNs)) {
+        if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag, 32u)) {
           ok = false;
           break;
         }
@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     const bool row_ok = b < p.B;
     const uint32_t b_global = static_cast<uint32_t>(p.b_global0 + b);
     const float scale2 = p.inv_t * kLog2e;
+    const float inv_scale2 = 1.0f / scale2;  // logit of the winner from its scaled value
     float* merge = reinterpret_cast<float*>(sA);  // reused after a step's MMAs completed
     // this thread's four 16-byte pieces of its U row within a stage (128B swizzle)
     uint32_t u_off[4];
@@ -422,33 +423,35 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     int u_stage = 0;        // U ring slot of the next tile
     uint32_t u_phase = 0;   // its mbarrier phase parity
 
+    unsigned long long spec_key = 0ull;  // winner key this thread's row was gathered for
     for (int k = 0; k < p.K; ++k) {
-      // ---- gather the step's embeddings (after the previous step's MMAs released E)
+      // ---- the step's embeddings: position 0 is gathered here; later positions were
+      // gathered speculatively before the previous grid barrier and are re-checked now
       if (etid == 0) trace_stamp(p, cta, k, 0);
-      if (k > 0) {
-        if (!mbar_wait(a_empty, (k - 1) & 1, p.timeout_ns, abort_flag)) {
-          fail = true;
-          *abort_flag = 1;
-        }
-      }
       {
         const int grow = etid >> 2;
-        int32_t tok = 0;
-        if (grow < p.B) {
-          if (MODE == kModeTeacherForced) {
-            tok = __ldg(p.prev + static_cast<size_t>(grow) * p.K + k);
-          } else if (k == 0) {
-            tok = __ldg(p.anchors + grow);
-          } else {
-            const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + grow);
-            tok = key_token(key);
+        if (k == 0) {
+          int32_t tok = 0;
+          if (grow < p.B) {
+            tok = (MODE == kModeTeacherForced) ? __ldg(p.prev + static_cast<size_t>(grow) * p.K)
+                                               : __ldg(p.anchors + grow);
+            if (tok < 0 || tok >= p.V) {
+              record_error(p.status, kStatusDeviceOob);
+              tok = 0;
+            }
           }
-          if (tok < 0 || tok >= p.V) {
-            record_error(p.status, kStatusDeviceOob);
-            tok = 0;
+          if (!fail) gather_embeddings(sA, p, 0, etid, tok);
+        } else if (MODE != kModeTeacherForced && grow < p.B) {
+          const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + grow);
+          if (key != spec_key) {  // the winner changed after the speculative gather
+            int32_t tok = key_token(key);
+            if (key_epoch(key) != p.epoch || tok < 0 || tok >= p.V) {
+              record_error(p.status, kStatusDeviceOob);
+              tok = 0;
+            }
+            if (!fail) gather_embeddings(sA, p, k, etid, tok);
           }
         }
-        if (!fail) gather_embeddings(sA, p, k, etid, tok);
         if (etid < kRows) s_bound[etid] = 0ull;
       }
       fence_proxy_async_smem();
@@ -520,15 +523,17 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 
         const int vbase = (t_begin + t) * kTileV + g * 16;
         const bool full_chunk = vbase + 16 <= p.V;  // warp-uniform
-        float l[16], y[16];
+        float y[16];
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
           const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
                                        make_float2(__uint_as_float(acc[j]),
                                                    __uint_as_float(acc[j + 1])));
+          if (MODE == kModeTeacherForced) {
+            uval[j] = lj.x;  // keep the logits for the store below
+            uval[j + 1] = lj.y;
+          }
           const float2 yj = __fmul2_rn(lj, make_float2(scale2, scale2));
-          l[j] = lj.x;
-          l[j + 1] = lj.y;
           y[j] = yj.x;
           y[j + 1] = yj.y;
         }
@@ -543,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 #pragma unroll
             for (int c = 0; c < 4; ++c)
               reinterpret_cast<float4*>(dst)[c] =
-                  make_float4(l[4 * c], l[4 * c + 1], l[4 * c + 2], l[4 * c + 3]);
+                  make_float4(uval[4 * c], uval[4 * c + 1], uval[4 * c + 2], uval[4 * c + 3]);
           } else {
-            for (int j = 0; j < 16 && vbase + j < p.V; ++j) dst[j] = l[j];
+            for (int j = 0; j < 16 && vbase + j < p.V; ++j) dst[j] = uval[j];
           }
         }
         // chunk maximum (tree)
@@ -593,13 +598,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               if (w[q2] == 1.0f) {  // y == cmax == m2 in the first live chunk
                 js = q2;
                 wj = w[q2];
-                lj = l[q2];
+                lj = y[q2] * inv_scale2;
               }
             }
             if (exact_race_update(wj, philox_word(vbase + js, kc, b_global, p), lj, vbase + js,
                                   wb, e2b, vb, lb, cthr))
               atomicMax(&s_bound[b], make_key(p.epoch, lb * scale2 - log2f(e2b), vb));
           }
+          uint32_t words[16];
+          philox4x32_10_xn<4>(static_cast<uint32_t>(vbase >> 2), kc, b_global, p.round_key0,
+                              p.round_key1, words);
           // Any score already reached for this request (here, in this CTA, or
           // published by another CTA) bounds the winner from below: an element
           // needs y - log2(E2) > S, i.e. E < w * ln2 * 2^(m2 - S).
@@ -610,20 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           const float2 negc = make_float2(-0.99999994039535522461f, -0.99999994039535522461f);
           uint32_t cand = 0;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t words[8];
-            philox4x32_10_xn<2>(static_cast<uint32_t>(vbase >> 2) + 2 * half, kc, b_global,
-                                p.round_key0, p.round_key1, words);
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-              const int jj = 8 * half + j;
-              const float2 t2 = __fadd2_rn(make_float2(philox_one_plus_complement(words[j]),
-                                                       philox_one_plus_complement(words[j + 1])),
-                                           negc);  // 1 - u, exact
-              const float2 x2 = __fmul2_rn(make_float2(w[jj], w[jj + 1]), cth2);
-              if (t2.x < x2.x) cand |= 1u << jj;
-              if (t2.y < x2.y) cand |= 2u << jj;
-            }
+          for (int j = 0; j < 16; j += 2) {
+            const float2 t2 = __fadd2_rn(make_float2(philox_one_plus_complement(words[j]),
+                                                     philox_one_plus_complement(words[j + 1])),
+                                         negc);  // 1 - u, exact
+            const float2 x2 = __fmul2_rn(make_float2(w[j], w[j + 1]), cth2);
+            if (t2.x < x2.x) cand |= 1u << j;
+            if (t2.y < x2.y) cand |= 2u << j;
           }
           while (cand != 0u) {  // rare: a few per thread and step
             const int j = __ffs(cand) - 1;
@@ -633,9 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             for (int q2 = 0; q2 < 16; ++q2) {
               if (q2 == j) {
                 wj = w[q2];
-                lj = l[q2];
+                lj = y[q2];
               }
             }
+            lj *= inv_scale2;
             if (exact_race_update(wj, philox_word(vbase + j, kc, b_global, p), lj, vbase + j, wb,
                                   e2b, vb, lb, cthr))
               atomicMax(&s_bound[b], make_key(p.epoch, lb * scale2 - log2f(e2b), vb));
@@ -659,7 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             lb = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (j == jb) lb = l[j];
+              if (j == jb) lb = y[j];
+            lb *= inv_scale2;
+            atomicMax(&s_bound[b], make_key(p.epoch, yb, vb));
+          }
+          if ((t & 1) == 1 && g == 0) {
+            // publish this CTA's best so far (lets other CTAs gather the next
+            // position's embeddings speculatively before the grid barrier)
+            const unsigned long long mine = s_bound[b];
+            if (mine > gkey) {
+              atomicMax(p.keys + k * kRows + b, mine);
+              gkey = mine;
+            }
           }
         }
       }
@@ -698,6 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (MODE != kModeTeacherForced && best_v != 0x7FFFFFFF) {
           key = make_key(p.epoch, best_s, best_v);
           atomicMax(p.keys + k * kRows + b, key);
+          if (key >= gkey && k + 1 < p.K) {
+            // this CTA may hold the winner: pull its Markov embedding into L2 so that
+            // every CTA's gather for the next position hits L2
+            const char* row = reinterpret_cast<const char*>(p.W1 + static_cast<size_t>(best_v) * p.r);
+            for (int off = 0; off < p.r * 2; off += 128)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+          }
         }
         DraftPartial* dst = p.partials + (static_cast<size_t>(k) * kRows + b) * ncta + cta;
         dst->key = key;
@@ -707,15 +727,48 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
       named_bar_sync(kEpiBarrier, kEpiThreads);
 
-      // ---- grid barrier (bounded)
-      bool bar_fail = false;
-      if (etid == 0) trace_stamp(p, cta, k, 4);
+      // ---- arrive at the grid barrier (the wait comes after the speculative gather)
       if (etid == 0 && !fail) {
         const bool skip = (p.debug_skip_cta == cta) && (k == 0);
         if (!skip) {
           __threadfence();
           red_release_gpu_add(p.bar, 1u);
         }
+      }
+
+      // ---- speculative gather for the next position: the winners are mostly final by
+      // now (eager publication), so fetch their embeddings while other CTAs finish
+      if (k + 1 < p.K && !fail) {
+        if (!mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag)) {  // MMAs done reading E
+          fail = true;
+          *abort_flag = 1;
+        } else {
+          const int grow = etid >> 2;
+          int32_t tok = 0;
+          if (grow < p.B) {
+            if (MODE == kModeTeacherForced) {
+              tok = __ldg(p.prev + static_cast<size_t>(grow) * p.K + k + 1);
+              if (tok < 0 || tok >= p.V) {
+                record_error(p.status, kStatusDeviceOob);
+                tok = 0;
+              }
+            } else {
+              spec_key = __ldcg(p.keys + k * kRows + grow);
+              tok = key_token(spec_key);
+              if (key_epoch(spec_key) != p.epoch || tok < 0 || tok >= p.V) {
+                spec_key = ~0ull;  // never matches: refetched after the barrier
+                tok = 0;
+              }
+            }
+          }
+          gather_embeddings(sA, p, k + 1, etid, tok);
+        }
+      }
+
+      // ---- grid barrier (bounded)
+      bool bar_fail = false;
+      if (etid == 0) trace_stamp(p, cta, k, 4);
+      if (etid == 0 && !fail) {
         const uint32_t target = p.bar_base + static_cast<uint32_t>((k + 1) * ncta);
         uint64_t deadline = 0;
         for (uint32_t it = 0;; ++it) {
