@@ -177,6 +177,31 @@ int dspark_gated_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1,
 int dspark_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int d, int r,
                 float* H, dspark_stream_t stream);
 
+/* Context-free variant of dspark_markov_draft that allocates no device memory.
+ * The pages have no counterpart: this is an integration aid of this library.
+ * For callers that may not allocate device memory themselves (a library inside
+ * a host framework that owns all device memory through its own pool, or a
+ * serving loop that forbids cudaMalloc / cudaFree because they can synchronise
+ * the device).  Inputs and outputs are the caller's, as in dspark_markov_draft
+ * (no confidence head); the kernel's scratch is one fixed array of about 7.9 MB
+ * compiled into the library, present on every GPU that loads it until the
+ * process exits.
+ *   Limits: K <= 16 (else DSPARK_ERR_CAPACITY), other shape rules as
+ *   dspark_markov_draft; the current device must be sm_103 and hold the
+ *   pointers.
+ *   device_status: optional device int that receives the launch's device
+ *   status (a dspark_status) in stream order; NULL to skip.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call on a device uses the same array and starts by clearing
+ *   its counters and keys on `stream`; calls that overlap on the GPU (other
+ *   streams or host threads) race and must be serialised by the caller. */
+int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, const uint16_t* W2,
+                                const int32_t* anchors, int B, int K, int V, int r,
+                                float temperature, uint64_t seed, int32_t* tokens,
+                                float* logprobs, int* device_status, dspark_stream_t stream);
+
 /* --------------------------------------------------------------------- */
 /* Selector-style top-k execution                                           */
 /* --------------------------------------------------------------------- */

@@ -32,6 +32,7 @@ EXPORTS = (
     "dspark_debug_set", "dspark_debug_trace", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
+    "dspark_markov_draft_noalloc",
 )
 
 
@@ -79,6 +80,7 @@ def load(path: str = LIB_PATH):
         "dspark_selector_walk": [P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P],
         "dspark_confidence": [P, P, P, P, P, P, F, I, I, I, I, I, I, F, P, P, P, P],
         "dspark_markov_logits": [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P],
+        "dspark_markov_draft_noalloc": [P, P, P, P, I, I, I, I, F, U64, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -284,6 +286,26 @@ def dspark_markov_logits(ctx: Context, U, W1, W2, prev_tokens, h, Wg, d, B, K, V
         _ptr(logits, (torch.float32,), "logits"), _ptr(lse, (torch.float32,), "lse"),
         _stream(stream, ctx.device))
     _check(code, "dspark_markov_logits")
+
+
+def dspark_markov_draft_noalloc(U, W1, W2, anchors, B, K, V, r, temperature, seed, tokens,
+                                logprobs, device_status=None, stream=None):
+    """Context-free draft that allocates no device memory (scratch compiled into the library).
+
+    For callers that may not allocate device memory themselves; the current CUDA
+    device must hold every tensor.  Calls that overlap on the GPU race on the
+    shared scratch.  device_status: optional int32 device tensor receiving the
+    launch's device status.
+    """
+    lib = load()
+    code = lib.dspark_markov_draft_noalloc(
+        _ptr(U, (torch.float32,), "U"), _ptr(W1, _BF16, "W1"), _ptr(W2, _BF16, "W2"),
+        _ptr(anchors, (torch.int32,), "anchors"), B, K, V, r, float(temperature),
+        int(seed) & (2 ** 64 - 1), _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(logprobs, (torch.float32,), "logprobs"),
+        _ptr(device_status, (torch.int32,), "device_status"),
+        _stream(stream, U.device))
+    _check(code, "dspark_markov_draft_noalloc")
 
 
 # ------------------------------------------------------ allocating wrappers
