@@ -45,11 +45,11 @@ CONF_THRESHOLD = 0.3
 
 WORKLOADS = {
     # name: (config index, description)
-    "serving": (2, "serving batch + confidence: B=128 K=16 V=151936 r=256 d=2048 T=1.0"),
-    "single": (1, "single request: B=1 K=16 V=151936 r=256 T=1.0"),
-    "gated": (3, "gated head: B=64 K=16 V=151936 r=256 d=4096 T=1.0"),
-    "selector": (4, "selector top-16 (gated): B=256 K=16 V=151936 r=256 d=4096 T=1.0"),
-    "tiny": (0, "tiny: B=1 K=4 V=4096 r=256 T=1.0"),
+    "serving": (2, "serving batch + confidence: B=128 K=16 V=151936 r=256 d=2048"),
+    "single": (1, "single request: B=1 K=16 V=151936 r=256"),
+    "gated": (3, "gated head: B=64 K=16 V=151936 r=256 d=4096"),
+    "selector": (4, "selector top-16 (gated): B=256 K=16 V=151936 r=256 d=4096"),
+    "tiny": (0, "tiny: B=1 K=4 V=4096 r=256"),
 }
 
 
@@ -78,6 +78,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="serving")
+    ap.add_argument("--temperature", type=float, default=1.0,
+                    help="sampling temperature (0 = greedy); the workloads are quoted at 1.0")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -260,10 +262,11 @@ def run_reference(args, rank, world):
     inp = config_inputs(cfg)
     K = c["K"]
     for i in range(args.warmup):
-        oracle_sample(inp, c, 1, b0=i % c["B"])
+        oracle_sample(inp, c, 1, b0=i % c["B"], temperature=args.temperature)
     spent = 0.0
     for i in range(args.steps):
-        spent += oracle_sample(inp, c, 1, b0=(args.warmup + i) % c["B"])
+        spent += oracle_sample(inp, c, 1, b0=(args.warmup + i) % c["B"],
+                               temperature=args.temperature)
     value = args.steps * K / spent
     threads = oracle.max_threads()
     line = {
@@ -293,7 +296,7 @@ def run_ours(args, rank, world, local):
     cfg, desc = WORKLOADS[args.workload]
     c = dict(CONFIGS[cfg])
     B, K, V, r = c["B"], c["K"], c["V"], c["r"]
-    T = 1.0
+    T = float(args.temperature)
     inp = config_inputs(cfg)
 
     def up(a, bf=False):
@@ -420,6 +423,7 @@ def run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world):
     import torch
     from rank_markov_draft_gb300 import binding
     B, K, V, r = c["B"], c["K"], c["V"], c["r"]
+    T = float(args.temperature)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     U_h = pin(inp.U)
     anc_h = pin(inp.anchors)
@@ -446,10 +450,10 @@ def run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world):
         if hc_h is not None:
             hc_d.copy_(hc_h, non_blocking=True)
         if h is None:
-            binding.dspark_markov_draft(ctx, U_d, W1, W2, anc_d, B, K, V, r, 1.0, seed, tok_d,
+            binding.dspark_markov_draft(ctx, U_d, W1, W2, anc_d, B, K, V, r, T, seed, tok_d,
                                         lp_d, conf_e, stream)
         else:
-            binding.dspark_gated_draft(ctx, U_d, W1, W2, anc_d, h, Wg, c["d"], B, K, V, r, 1.0,
+            binding.dspark_gated_draft(ctx, U_d, W1, W2, anc_d, h, Wg, c["d"], B, K, V, r, T,
                                        seed, tok_d, lp_d, conf_e, stream)
         outs_h["tokens"].copy_(tok_d, non_blocking=True)
         outs_h["logprobs"].copy_(lp_d, non_blocking=True)
