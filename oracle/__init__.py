@@ -53,8 +53,12 @@ def _bind(lib):
     lib.orc_philox4x32_10.argtypes = [P, P, P]
     lib.orc_uniform.argtypes = [u64, u32, u32, u32, u32]
     lib.orc_uniform.restype = f64
-    lib.orc_gumbel.argtypes = [u64, u32, u32, u32]
-    lib.orc_gumbel.restype = f64
+    lib.orc_uniform_ctr.argtypes = [u64, u32, u32, u32, u32, u32]
+    lib.orc_uniform_ctr.restype = f64
+    lib.orc_block_uniform.argtypes = [u64, u32, u32, u32]
+    lib.orc_block_uniform.restype = f64
+    lib.orc_within_uniform.argtypes = [u64, u32, u32, u32]
+    lib.orc_within_uniform.restype = f64
     lib.orc_gate.argtypes = [P, P, i64, i32, i32, P]
     lib.orc_markov_draft.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, u64, i32, i32,
                                      P, P, P, P, P]
@@ -105,8 +109,13 @@ class Oracle:
     def uniform(self, seed: int, b: int, k: int, v: int, tag: int = 0) -> float:
         return float(self._lib.orc_uniform(seed, b, k, v, tag))
 
-    def gumbel(self, seed: int, b: int, k: int, v: int) -> float:
-        return float(self._lib.orc_gumbel(seed, b, k, v))
+    def block_uniform(self, seed: int, b: int, k: int, blk: int) -> float:
+        """Stage-1 uniform of 16-token block `blk` (request b, position k)."""
+        return float(self._lib.orc_block_uniform(seed, b, k, blk))
+
+    def within_uniform(self, seed: int, b: int, k: int, blk: int) -> float:
+        """Stage-2 uniform of 16-token block `blk` (request b, position k)."""
+        return float(self._lib.orc_within_uniform(seed, b, k, blk))
 
     def gate(self, h: np.ndarray, Wg: np.ndarray) -> np.ndarray:
         """H = sigmoid(h . Wg) in fp64; h [..., d] bf16 bits, Wg [d, r] bf16 bits -> [..., r]."""

@@ -27,16 +27,27 @@
  *  - x_0 is the anchor token, so every position k = 0..K-1 gets a bias
  *    ([EXPL] "Semi-autoregressive generation": the anchor is the first
  *    prediction position; [VLLM] "Sample From Anchor").
- *  - Temperature T > 0 samples softmax(l / T) by Gumbel-max, argmax(l/T + g);
+ *  - Temperature T > 0 draws from softmax(l / T) in two exact stages over
+ *    blocks of 16 consecutive token ids (block beta = v >> 4):
+ *      1. block race: beta* = argmax_beta  ln Z_beta - ln E_beta, where
+ *         Z_beta = sum_{v in beta} exp(l_v / T) and E_beta = -ln u1(beta) is a
+ *         unit exponential (the exponential race / Gumbel-max over blocks:
+ *         P(beta* = beta) = Z_beta / Z);
+ *      2. inverse CDF inside beta*: the smallest v in beta* whose cumulative
+ *         mass (in token-id order) exceeds u2(beta*) * Z_beta*.
+ *    So P(v) = (Z_beta / Z) (exp(l_v / T) / Z_beta) = softmax(l / T)_v.
  *    T == 0 is greedy argmax(l).  The returned log-probability is that of the
  *    drawn token under softmax(l / T') with T' = T (T > 0) or 1 (T == 0).
- *  - Ties in any argmax or top-k order go to the smaller token id.
+ *  - Ties in any argmax or top-k order go to the smaller token id (block id).
  *  - Noise: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
- *    Numbers: As Easy as 1, 2, 3", SC'11), key = (seed low 32, seed high 32),
- *    counter = (v >> 2, k, b, 0); word v & 3 of the output gives
- *    u = ((word & 0x7FFFFF) + 0.5) * 2^-23 (the low 23 bits), exactly
- *    representable in fp32 and fp64
- *    and strictly inside (0, 1); g = -ln(-ln u).
+ *    Numbers: As Easy as 1, 2, 3", SC'11), key = (seed low 32, seed high 32).
+ *    A counter (c0, c1, c2, c3) and an output word w give
+ *    u = ((word_w & 0x7FFFFF) + 0.5) * 2^-23 (the low 23 bits), exactly
+ *    representable in fp32 and fp64 and strictly inside (0, 1).
+ *      counter (beta >> 3, k, b, 1 + (beta & 3)), h = (beta >> 2) & 1:
+ *      u1(beta) = word 2h, u2(beta) = word 2h + 1
+ *    (so whoever owns every fourth block of a range draws both stages of two
+ *    consecutive ones of its blocks from one Philox call).
  */
 #include <math.h>
 #include <stdint.h>
@@ -112,21 +123,32 @@ void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
   out[3] = x3;
 }
 
-/* u(seed, b, k, v) in (0, 1) with stream tag `tag` (0 = token sampling). */
-double orc_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t v, uint32_t tag) {
-  uint32_t ctr[4] = {v >> 2, k, b, tag};
+/* u in (0, 1) from word `w` of Philox4x32-10(counter (c0, c1, c2, c3), seed). */
+double orc_uniform_ctr(uint64_t seed, uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                       uint32_t w) {
+  uint32_t ctr[4] = {c0, c1, c2, c3};
   uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
   uint32_t out[4];
   orc_philox4x32_10(ctr, key, out);
-  uint32_t word = out[v & 3u];
+  uint32_t word = out[w & 3u];
   return ((double)(word & 0x7FFFFFu) + 0.5) * (1.0 / 8388608.0); /* 2^-23 */
 }
 
-/* Standard Gumbel variate g = -ln(-ln u). */
-double orc_gumbel(uint64_t seed, uint32_t b, uint32_t k, uint32_t v) {
-  double u = orc_uniform(seed, b, k, v, 0u);
-  return -log(-log(u));
+/* u(seed, b, k, v) with stream tag `tag`: counter (v >> 2, k, b, tag), word v & 3. */
+double orc_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t v, uint32_t tag) {
+  return orc_uniform_ctr(seed, v >> 2, k, b, tag, v & 3u);
 }
+
+/* Stage-1 uniform of block `blk` (request b, position k). */
+double orc_block_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk) {
+  return orc_uniform_ctr(seed, blk >> 3, k, b, 1u + (blk & 3u), 2u * ((blk >> 2) & 1u));
+}
+
+/* Stage-2 uniform of block `blk` (request b, position k). */
+double orc_within_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk) {
+  return orc_uniform_ctr(seed, blk >> 3, k, b, 1u + (blk & 3u), 2u * ((blk >> 2) & 1u) + 1u);
+}
+
 
 /* ------------------------------------------------------------------ */
 /* Gate H(h_t) = sigmoid(h_t . Wg) of the gated head.                   */
@@ -203,6 +225,68 @@ static double log_sum_exp_scaled(const double* l, int V, double Tp) {
 }
 
 /* ------------------------------------------------------------------ */
+/* One draw from softmax(z) over n items with token ids ids[0..n-1]    */
+/* (ascending; NULL: ids are 0..n-1), by the two-stage block race of   */
+/* the header.  w[0..n-1] is scratch.  Returns the index of the drawn   */
+/* item (-1 if every z is -inf) and its decision margin: the smaller of */
+/* the stage-1 gap (best block score - runner-up, in nats) and the      */
+/* stage-2 distance of u2 * Z from the nearest cumulative boundary,     */
+/* relative to Z (either is the relative error that would flip it).     */
+/* ------------------------------------------------------------------ */
+static int block_race_draw(const int32_t* ids, const double* z, double* w, int n, uint64_t seed,
+                           uint32_t b, uint32_t k, double* margin) {
+  double m = -INFINITY;
+  for (int i = 0; i < n; ++i)
+    if (z[i] > m) m = z[i];
+  if (m == -INFINITY) return -1;
+#pragma omp parallel for schedule(static) if (n > 65536)
+  for (int i = 0; i < n; ++i) w[i] = exp(z[i] - m);
+  /* stage 1: one unit exponential per block, ln Z - ln E */
+  double best = -INFINITY, second = -INFINITY, bestZ = 0.0;
+  int bs = -1, be = -1;
+  uint32_t bblk = 0;
+  for (int i = 0; i < n;) {
+    const uint32_t blk = (uint32_t)(ids ? ids[i] : i) >> 4;
+    double Z = 0.0;
+    int j = i;
+    while (j < n && ((uint32_t)(ids ? ids[j] : j) >> 4) == blk) Z += w[j++];
+    if (Z > 0.0) {
+      const double E = -log(orc_block_uniform(seed, b, k, blk));
+      const double score = log(Z) - log(E);
+      if (score > best) {
+        second = best;
+        best = score;
+        bs = i;
+        be = j;
+        bblk = blk;
+        bestZ = Z;
+      } else if (score > second) {
+        second = score;
+      }
+    }
+    i = j;
+  }
+  /* stage 2: inverse CDF inside the winning block, in token-id order */
+  const double target = orc_within_uniform(seed, b, k, bblk) * bestZ;
+  double C = 0.0, m2 = 0.0;
+  int pick = -1, last = -1;
+  for (int i = bs; i < be; ++i) {
+    if (w[i] == 0.0) continue;
+    const double prevC = C;
+    C += w[i];
+    last = i;
+    if (target < C) {
+      pick = i;
+      m2 = fmin(target - prevC, C - target) / bestZ;
+      break;
+    }
+  }
+  if (pick < 0) pick = last; /* target at the very top (rounding): the last live item */
+  *margin = fmin(best - second, m2);
+  return pick;
+}
+
+/* ------------------------------------------------------------------ */
 /* Markov-head draft over a block (vanilla, or gated when H != NULL).   */
 /* [EXPL] "Semi-autoregressive generation" + "The Markov head": the    */
 /* head samples left to right, x_0 = anchor, position k's logits get   */
@@ -234,26 +318,27 @@ static int draft_one_request(const float* U, const uint16_t* W1, const uint16_t*
     const double* Hrow = H ? H + ((int64_t)b * K + k) * r : NULL;
     if (prev < 0 || prev >= V) return -1;
     calibrated_logits(Urow, W1, W2, Hrow, V, r, prev, e, l);
-    /* perturbed scores */
-    if (temperature > 0.0) {
-#pragma omp parallel for schedule(static)
-      for (int v = 0; v < V; ++v)
-        s[v] = l[v] / temperature + orc_gumbel(seed, (uint32_t)b, (uint32_t)k, (uint32_t)v);
-    } else {
-      for (int v = 0; v < V; ++v) s[v] = l[v];
-    }
-    /* argmax, ties to the smaller token id; runner-up for the margin */
-    int best = 0;
-    for (int v = 1; v < V; ++v)
-      if (s[v] > s[best]) best = v;
-    double second = -INFINITY;
-    for (int v = 0; v < V; ++v)
-      if (v != best && s[v] > second) second = s[v];
-    const double lse = log_sum_exp_scaled(l, V, Tp);
     const int64_t o = (int64_t)bi * K + k;
+    int best = 0;
+    if (temperature > 0.0) {
+      /* z = l / T, then the two-stage block race (header) */
+      double* z = s;
+      double* w = s + V;
+      for (int v = 0; v < V; ++v) z[v] = l[v] / temperature;
+      best = block_race_draw(NULL, z, w, V, seed, (uint32_t)b, (uint32_t)k, &margins[o]);
+      if (best < 0) return -1;
+    } else {
+      /* argmax, ties to the smaller token id; runner-up for the margin */
+      for (int v = 1; v < V; ++v)
+        if (l[v] > l[best]) best = v;
+      double second = -INFINITY;
+      for (int v = 0; v < V; ++v)
+        if (v != best && l[v] > second) second = l[v];
+      margins[o] = l[best] - second;
+    }
+    const double lse = log_sum_exp_scaled(l, V, Tp);
     tokens[o] = best;
     logprobs[o] = l[best] / Tp - lse;
-    margins[o] = s[best] - second;
     if (forced) {
       const int32_t f = forced[o];
       if (f < 0 || f >= V) return -1;
@@ -280,7 +365,7 @@ int orc_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
 #pragma omp parallel if (per_request) reduction(| : bad)
   {
     double* l = (double*)malloc(sizeof(double) * (size_t)V);
-    double* s = (double*)malloc(sizeof(double) * (size_t)V);
+    double* s = (double*)malloc(sizeof(double) * 2 * (size_t)V);
     double* e = (double*)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
     if (!l || !s || !e) {
       bad = 1;
@@ -468,8 +553,10 @@ int orc_pair_scores(const int32_t* cand, const double* cval, const uint16_t* A,
 /* [EQV] "Where the parallelism comes from": a greedy walk, or sampling, */
 /* over the precomputed scores; "Two implications", 2, step 3.  The     */
 /* sampling rule is the Markov head's own restricted to the candidates: */
-/* Gumbel noise keyed by the candidate's token id, so with k = V the    */
-/* walk is the full head; log-probabilities are under the k-way softmax.*/
+/* the block race over the candidates' token ids (noise keyed by block  */
+/* id), so with k = V the walk is the full head and with k < V it is    */
+/* the head with every other token masked; log-probabilities are under  */
+/* the k-way softmax.                                                   */
 /* cand [B,K,topk], S [B,K,topk,topk] -> compact outputs [nb, K].       */
 /* forced ([nb,K], nullable): continue on these tokens (must be in the  */
 /* candidate set); forced_logprobs receives their log-probability.      */
@@ -488,17 +575,40 @@ int orc_walk(const int32_t* cand, const double* S, int B, int K, int topk, doubl
       const int64_t bt = (int64_t)b * K + t;
       const double* row = S + (bt * topk + slot) * topk;
       const int32_t* c = cand + bt * topk;
-      double sc[64];
-      for (int j = 0; j < topk; ++j)
-        sc[j] = (temperature > 0.0)
-                    ? row[j] / temperature + orc_gumbel(seed, (uint32_t)b, (uint32_t)t, (uint32_t)c[j])
-                    : row[j];
       int best = 0;
-      for (int j = 1; j < topk; ++j)
-        if (sc[j] > sc[best] || (sc[j] == sc[best] && c[j] < c[best])) best = j;
-      double second = -INFINITY;
-      for (int j = 0; j < topk; ++j)
-        if (j != best && sc[j] > second) second = sc[j];
+      double margin = 0.0;
+      if (temperature > 0.0) {
+        /* the head's block race restricted to the candidates: candidates in
+           token-id order, z = S / T (tokens outside the set have mass 0) */
+        int ord[64];
+        int32_t ids[64];
+        double z[64], w[64];
+        for (int j = 0; j < topk; ++j) {
+          int p = j;
+          while (p > 0 && c[ord[p - 1]] > c[j]) {
+            ord[p] = ord[p - 1];
+            --p;
+          }
+          ord[p] = j;
+        }
+        for (int q = 0; q < topk; ++q) {
+          ids[q] = c[ord[q]];
+          z[q] = row[ord[q]] / temperature;
+        }
+        const int q = block_race_draw(ids, z, w, topk, seed, (uint32_t)b, (uint32_t)t, &margin);
+        if (q < 0) {
+          bad = 1;
+          break;
+        }
+        best = ord[q];
+      } else {
+        for (int j = 1; j < topk; ++j)
+          if (row[j] > row[best] || (row[j] == row[best] && c[j] < c[best])) best = j;
+        double second = -INFINITY;
+        for (int j = 0; j < topk; ++j)
+          if (j != best && row[j] > second) second = row[j];
+        margin = row[best] - second;
+      }
       double m = -INFINITY;
       for (int j = 0; j < topk; ++j)
         if (row[j] / Tp > m) m = row[j] / Tp;
@@ -508,7 +618,7 @@ int orc_walk(const int32_t* cand, const double* S, int B, int K, int topk, doubl
       const int64_t o = (int64_t)bi * K + t;
       tokens[o] = c[best];
       logprobs[o] = row[best] / Tp - lse;
-      margins[o] = sc[best] - second;
+      margins[o] = margin;
       int next = best;
       if (forced) {
         next = -1;

@@ -21,8 +21,15 @@ MUTANTS = [
     # (name, original text, planted text, pins expected to catch it)
     ("predecessor-not-carried", "      prev = best;\n", "      prev = anchors[b];\n",
      ["test_sampler_matches_exhaustive_joint", "test_greedy_is_argmax_of_calibrated_logits"]),
-    ("gumbel-sign", "return -log(-log(u));", "return log(-log(u));",
-     ["test_uniform_grid_and_word_selection", "test_sampler_matches_exhaustive_joint"]),
+    ("block-race-exponential-not-logged", "const double score = log(Z) - log(E);",
+     "const double score = log(Z) - E;", ["test_temperature_scales_the_sampled_softmax"]),
+    ("stage2-reuses-stage1-uniform", "orc_within_uniform(seed, b, k, bblk) * bestZ",
+     "orc_block_uniform(seed, b, k, bblk) * bestZ",
+     ["test_temperature_scales_the_sampled_softmax"]),
+    ("block-mass-drops-first-token",
+     "while (j < n && ((uint32_t)(ids ? ids[j] : j) >> 4) == blk) Z += w[j++];",
+     "while (j < n && ((uint32_t)(ids ? ids[j] : j) >> 4) == blk) { if (j > i) Z += w[j]; ++j; }",
+     ["test_temperature_scales_the_sampled_softmax", "test_sampler_matches_exhaustive_joint"]),
     ("w2-transposed", "l[v] += ei * bf16_to_double(w2row[v]);",
      "l[v] += ei * bf16_to_double(W2[(int64_t)v * r + i]);",
      ["test_teacher_forced_logits_match_numpy"]),

@@ -45,7 +45,16 @@ def test_uniform_grid_and_word_selection(orc):
         assert u == ((int(out[v & 3]) & 0x7FFFFF) * 2 + 1) * 2.0 ** -24
         assert 0.0 < u < 1.0
         assert np.float32(u) == u  # exactly representable in fp32
-        assert orc.gumbel(seed, b, k, v) == -np.log(-np.log(u))
+        # the block-race streams: one call per two blocks of the same residue mod 4,
+        # words (2h, 2h + 1) = (stage 1, stage 2) of the block with h = (blk >> 2) & 1
+        blk = v >> 4
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        o = orc.philox4x32_10([blk >> 3, k, b, 1 + (blk & 3)], key)
+        h = (blk >> 2) & 1
+        assert orc.block_uniform(seed, b, k, blk) == \
+            ((int(o[2 * h]) & 0x7FFFFF) * 2 + 1) * 2.0 ** -24
+        assert orc.within_uniform(seed, b, k, blk) == \
+            ((int(o[2 * h + 1]) & 0x7FFFFF) * 2 + 1) * 2.0 ** -24
 
 
 def test_uniform_is_uniform(orc):
@@ -54,6 +63,13 @@ def test_uniform_is_uniform(orc):
     assert stats.chisquare(counts).pvalue > 1e-3
     # neighbouring words of one block and neighbouring requests are uncorrelated
     assert abs(np.corrcoef(us[:-1], us[1:])[0, 1]) < 0.02
+    # the block-race streams: uniform, and stage 1 / stage 2 of a block independent
+    u1 = np.array([orc.block_uniform(7, b, 3, blk) for b in range(20) for blk in range(1000)])
+    u2 = np.array([orc.within_uniform(7, b, 3, blk) for b in range(20) for blk in range(1000)])
+    for x in (u1, u2):
+        assert stats.chisquare(np.histogram(x, bins=50, range=(0, 1))[0]).pvalue > 1e-3
+    assert abs(np.corrcoef(u1, u2)[0, 1]) < 0.03
+    assert abs(np.corrcoef(u1[:-1], u1[1:])[0, 1]) < 0.03
 
 
 # ------------------------------------------------------------------- closed forms
@@ -166,15 +182,23 @@ def test_sampler_matches_exhaustive_joint(orc):
 
 
 def test_temperature_scales_the_sampled_softmax(orc):
-    V, N, T = 16, 200_000, 0.5
+    """V = 40 spans three 16-token blocks (the last one ragged): the draw's token,
+    block and within-block frequencies all follow softmax(U / T)."""
+    V, N, T = 40, 300_000, 0.5
     rng = np.random.default_rng(12)
     U1 = (rng.standard_normal((1, 1, V)) * 0.8).astype(np.float32)
+    U1[0, 0, 16:32] -= 0.6   # unequal block masses
     U = np.ascontiguousarray(np.broadcast_to(U1, (N, 1, V)))
     out = orc.markov_draft(U, None, None, np.zeros(N, np.int32), temperature=T, seed=99)
-    counts = np.bincount(out["tokens"][:, 0], minlength=V).astype(np.float64)
+    tok = out["tokens"][:, 0]
+    counts = np.bincount(tok, minlength=V).astype(np.float64)
     p = special.softmax(U1[0, 0].astype(np.float64) / T)
     assert _chi2_pvalue(counts, p * N) > 0.01
-    assert np.allclose(out["logprobs"][:, 0], np.log(p[out["tokens"][:, 0]]), atol=1e-12)
+    pb = np.add.reduceat(p, [0, 16, 32])
+    assert _chi2_pvalue(np.bincount(tok >> 4, minlength=3).astype(np.float64), pb * N) > 0.01
+    assert np.allclose(out["logprobs"][:, 0], np.log(p[tok]), atol=1e-12)
+    # margins are the smaller of the block gap and the in-block distance: in (0, ...)
+    assert np.all(out["margins"] >= 0) and np.median(out["margins"]) > 1e-3
 
 
 def test_greedy_is_argmax_of_calibrated_logits(orc):
