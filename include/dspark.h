@@ -25,14 +25,20 @@
  *   with dspark_get_status after synchronising the stream.  After a device
  *   error the context is poisoned: further hot calls return
  *   DSPARK_ERR_CTX_POISONED until dspark_ctx_reset is called.
- * Temperature.  temperature > 0 samples softmax(l / T) by Gumbel-max;
- *   temperature == 0 is greedy.  Returned log-probabilities are those of the
- *   drawn token under softmax(l / T'), T' = T (T > 0) or 1 (T == 0).
+ * Temperature.  temperature > 0 draws from softmax(l / T) exactly, in two
+ *   stages over blocks of 16 consecutive token ids (block beta = v >> 4):
+ *   (1) the block maximising ln Z_beta - ln E_beta wins, Z_beta the block's
+ *   sum of exp(l / T) and E_beta = -ln u1(beta) a unit exponential (a race
+ *   won with probability Z_beta / Z); (2) inside it, the first token (by id)
+ *   whose cumulative exp(l / T) exceeds u2(beta) * Z_beta.  temperature == 0
+ *   is greedy.  Returned log-probabilities are those of the drawn token under
+ *   softmax(l / T'), T' = T (T > 0) or 1 (T == 0).
  * Noise.  Philox4x32-10 (Salmon et al., SC'11) keyed by (seed low 32 bits,
- *   seed high 32 bits) with counter (v >> 2, k, b, 0); word v & 3 gives
- *   u = ((word & 0x7FFFFF) + 0.5) * 2^-23 and the Gumbel variate -ln(-ln u).  b is
- *   the request's index in the call's batch, k its 0-based block position,
- *   v the token id.  The same (seed, b, k, v) always yields the same noise.
+ *   seed high 32 bits) with counter (beta >> 3, k, b, 1 + (beta & 3)); with
+ *   h = (beta >> 2) & 1, word 2h gives u1(beta) and word 2h + 1 gives
+ *   u2(beta), each as u = ((word & 0x7FFFFF) + 0.5) * 2^-23.  b is the
+ *   request's index in the call's batch, k its 0-based block position.  The
+ *   same (seed, b, k, beta) always yields the same noise.
  * Ties.  Argmax and top-k orders break ties to the smaller token id.
  */
 #ifndef DSPARK_H
@@ -225,9 +231,12 @@ int dspark_selector_scores(dspark_ctx* ctx, const float* U, const uint16_t* A,
                            int32_t* cand, float* cand_U, float* scores, dspark_stream_t stream);
 
 /* The light sequential walk over the pair tables: per request, for t = 0..K-1
- * pick candidate j of row `slot` (slot = 0 at t = 0) by Gumbel-max over
- * scores/T with noise keyed by the candidate's token id (T = 0: greedy), then
- * slot = j.  log-probabilities are under the topk-way softmax.
+ * draw candidate j from row `slot` (slot = 0 at t = 0) by the head's own
+ * two-stage block race (above) over scores/T, restricted to the candidates:
+ * the candidates of one 16-token block race with their summed mass, tokens
+ * outside the set have none (T = 0: greedy); then slot = j.  With topk = V
+ * this is the full head's draw.  log-probabilities are under the topk-way
+ * softmax.
  * Source: equivalence page, "Where the parallelism comes from" (a greedy walk,
  * or sampling, over the precomputed scores) and "Two implications", step 3.
  *   cand [B, K, topk], scores [B, K, topk, topk] as produced above

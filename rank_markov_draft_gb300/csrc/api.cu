@@ -30,6 +30,8 @@ struct dspark_ctx {
   DraftPartial* d_partials = nullptr;    // [K_max][128][num_sms]
   float* d_H = nullptr;                  // [B_max * K_max][256]
   float* d_gate_part = nullptr;          // [kGateSplitsMax][B_max * K_max][256]
+  int32_t* d_topk_part_i = nullptr;      // [kTopkPartUnits][kMaxTopk] per-piece top-k lists
+  float* d_topk_part_v = nullptr;
   uint32_t bar_counter = 0;              // host copy of the grid-barrier counter
   uint32_t epoch = 0;                    // last key epoch used
   int poisoned = 0;
@@ -321,7 +323,11 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
                                              dspark::kBatchChunk * ctx->num_sms) == cudaSuccess &&
             cudaMalloc(&ctx->d_H, sizeof(float) * rows * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_gate_part,
-                       sizeof(float) * kGateSplitsMax * rows * dspark::kMaxRank) == cudaSuccess;
+                       sizeof(float) * kGateSplitsMax * rows * dspark::kMaxRank) == cudaSuccess &&
+            cudaMalloc(&ctx->d_topk_part_i, sizeof(int32_t) * dspark::kTopkPartUnits *
+                                                dspark::kMaxTopk) == cudaSuccess &&
+            cudaMalloc(&ctx->d_topk_part_v,
+                       sizeof(float) * dspark::kTopkPartUnits * dspark::kMaxTopk) == cudaSuccess;
   ok = ok && cudaMemset(ctx->d_status, 0, sizeof(int)) == cudaSuccess &&
        cudaMemset(ctx->d_bar, 0, sizeof(uint32_t)) == cudaSuccess &&
        cudaMemset(ctx->d_keys, 0, sizeof(unsigned long long) * K_max * dspark::kBatchChunk) ==
@@ -344,6 +350,8 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_partials);
   cudaFree(ctx->d_H);
   cudaFree(ctx->d_gate_part);
+  cudaFree(ctx->d_topk_part_i);
+  cudaFree(ctx->d_topk_part_v);
   delete ctx;
   return DSPARK_OK;
 }
@@ -469,15 +477,18 @@ int dspark_selector_scores(dspark_ctx* ctx, const float* U, const uint16_t* A,
     return DSPARK_ERR_CAPACITY;
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dspark::launch_topk(U, B * K, V, topk, cand, cand_U, s);
+  int n_topk = 0;
+  cudaError_t e = dspark::launch_topk(U, B * K, V, topk, cand, cand_U, ctx->d_topk_part_i,
+                                      ctx->d_topk_part_v, dspark::kTopkPartUnits, ctx->d_status,
+                                      ctx->timeout_ns, &n_topk, s);
+  ctx->last_launches += n_topk;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  ctx->last_launches += 1;
   if (gated) {
     st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
     if (st != DSPARK_OK) return st;
   }
   e = dspark::launch_pair_scores(cand, cand_U, A, Bt, anchors, gated ? ctx->d_H : nullptr, B, K,
-                                 V, r, topk, scores, ctx->d_status, s);
+                                 V, r, topk, scores, ctx->d_status, ctx->timeout_ns, s);
   ctx->last_launches += 1;
   return cuda_status(e);
 }

@@ -4,7 +4,8 @@
 // "The Markov head"; equivalence page, "What the two methods do"): for a
 // chunk of up to 128 requests and block positions k = 0 .. K-1,
 //     l[b, v] = U[b, k, v] + sum_i e_b[i] * W2[i, v],   e_b = W1[x_{k-1}[b]] (. H[b, k])
-//     x_k[b]  = argmax_v ( l[b, v] / T + Gumbel(seed, b, k, v) )      (T = 0: argmax l)
+//     x_k[b]  ~ softmax(l[b, :] / T), drawn by the two-stage block race below
+//               (T = 0: argmax l)
 //     logprob = l[b, x_k] / T' - log sum_v exp(l[b, v] / T')
 // with x_{-1} = the anchor ("Sample From Anchor" in the vLLM guide).  The
 // local softmax is exact, as rejection sampling needs ("Why the normalization
@@ -23,7 +24,7 @@
 //     swizzle), W2 the MN-major tile exactly as TMA wrote it;
 //   * warps 2..17 (the epilogue) read the accumulator (one request per TMEM
 //     lane, 16 tokens per thread) and U from shared memory, and keep, per
-//     request, a running log-sum-exp and a running Gumbel-max winner, so the
+//     request, a running log-sum-exp and a running block-race winner, so the
 //     full-vocabulary logits never reach HBM;
 //   * at the end of a step each CTA publishes, per request, a 64-bit key
 //     (epoch | ordered score | inverted token id) by atomicMax and its
@@ -32,13 +33,17 @@
 //   * after the last step, CTA c reduces request c's partials into tokens and
 //     log-probabilities and runs the fused confidence head.
 //
-// Sampling epilogue, per element (Gumbel-max written as an exponential race):
-//   y = l * log2(e) / T, w = 2^(y - m) (shared with the log-sum-exp),
-//   E = -log2(u) (u from Philox), and the winner maximises w / E, which is
-//   the same argmax as y - log2(E) = log2(e) * (l/T + g) + const.  E comes
-//   from the fast lg2 approximation; an element is only examined exactly
-//   (with an accurate log) when its approximate ratio could beat the current
-//   winner, given the approximation's error bound.
+// Sampling epilogue (an exact draw from softmax(l / T) in two stages over
+// 16-token blocks; each thread's 16 columns of a tile are one block beta):
+//   y = l * log2(e) / T, w = 2^(y - m) (shared with the log-sum-exp), and the
+//   block's mass relative to m is s = sum w;
+//   stage 1, a race between blocks: the block maximising
+//     G = m + log2(s) - log2(E),  E = -ln u1 (a unit exponential)
+//   wins with probability Z_beta / Z (argmax Z_beta / E_beta);
+//   stage 2, only for a block that can still beat the best G any thread has
+//   reached for the request: the first token whose cumulative w exceeds
+//   u2 * s.  Both uniforms come from one Philox call per two of the thread's
+//   tiles.  The (G, token) winner is merged across threads and CTAs as a key.
 //
 // Every wait is bounded (mbarrier waits and the grid barrier give up after
 // timeout_ns, set the device status word and make the CTA exit cleanly after
@@ -168,36 +173,6 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
   for (int u = 0; u < 8; ++u) {
     *reinterpret_cast<uint4*>(base + ((u ^ (b & 7)) << 4)) = vals[u];
   }
-}
-
-// The Philox word of token v (rare path: recomputed rather than kept live).
-__device__ __forceinline__ uint32_t philox_word(int v, uint32_t k, uint32_t b,
-                                                const DraftParams& p) {
-  uint32_t words[4];
-  philox4x32_10_xn<1>(static_cast<uint32_t>(v) >> 2, k, b, p.round_key0, p.round_key1, words);
-  const int sel = v & 3;
-  return sel == 0 ? words[0] : sel == 1 ? words[1] : sel == 2 ? words[2] : words[3];
-}
-
-// Exact comparison of one candidate of the exponential race against the
-// running winner (wb / e2b): E = -ln u evaluated accurately (log1p near u = 1),
-// kept out of line so the hot loop stays small.
-__device__ __forceinline__ bool exact_race_update(float wj, uint32_t word, float lj, int v,
-                                                  float& wb, float& e2b, int& vb, float& lb,
-                                                  float& cthr) {
-  const float tj = philox_one_minus_uniform(word);
-  const float uj = 1.0f - tj;  // exact
-  const float e = (uj < 0.5f) ? -logf(uj) : -log1pf(-tj);
-  const float e2 = e * kLog2e;
-  if (wj * e2b > wb * e2) {
-    wb = wj;
-    e2b = e2;
-    vb = v;
-    lb = lj;
-    cthr = e2b * kLn2 / wb;
-    return true;
-  }
-  return false;
 }
 
 // Score of a key (the ordered float in its middle bits); -inf for "no key".
@@ -463,10 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 
       // ---- stream the step's tiles
       float m2 = -INFINITY, sum = 0.f;
-      float wb = 0.f, e2b = 1.f, yb = -INFINITY, lb = 0.f;
-      float cthr = INFINITY;  // ln2 * e2b / wb: candidates need 1 - u < w * cthr
+      float yb = -INFINITY, lb = 0.f;  // best score (G, or y when greedy) and its logit
       int vb = 0x7FFFFFFF;
+      unsigned long long bkey = 0ull;  // key of (yb, vb)
       unsigned long long gkey = 0ull;  // global key of this request and step, as last read
+      uint32_t nz[4] = {0u, 0u, 0u, 0u};  // Philox words of this thread's current tile pair
       for (int t = 0; t < nt && !fail; ++t) {
         if (MODE == kModeSample && row_ok && (t & (kBoundRefresh - 1)) == 0) {
           // the freshest bound matters most early in the step; the load overlaps the
@@ -562,13 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         const float cmax = fmaxf(fmaxf(mx[0], mx[2]), fmaxf(mx[1], mx[3]));
         if (cmax == -INFINITY) continue;  // nothing in this chunk can be drawn
         if (cmax > m2) {
-          const float f = ex2_approx(m2 - cmax);
-          sum *= f;
-          wb *= f;
+          sum *= ex2_approx(m2 - cmax);
           m2 = cmax;
-          cthr = (wb > 0.f) ? e2b * kLn2 / wb : INFINITY;
         }
         float w[16];
+        float bsum;  // the block's mass relative to 2^m2
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
           const float2 dj = __fadd2_rn(make_float2(y[j], y[j + 1]), make_float2(-m2, -m2));
@@ -581,66 +555,48 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           float2 s2 = __fadd2_rn(make_float2(w[8], w[9]), make_float2(w[10], w[11]));
           float2 s3 = __fadd2_rn(make_float2(w[12], w[13]), make_float2(w[14], w[15]));
           s0 = __fadd2_rn(__fadd2_rn(s0, s1), __fadd2_rn(s2, s3));
-          sum += s0.x + s0.y;
+          bsum = s0.x + s0.y;
+          sum += bsum;
         }
         if (MODE == kModeSample) {
-          // An element can only beat the running winner (ratio wb / e2b) if its
-          // E = -ln u is below w * cthr; since -ln u >= 1 - u, elements with
-          // 1 - u >= w * cthr are out without evaluating any logarithm.
-          const uint32_t kc = static_cast<uint32_t>(k);
-          if (wb == 0.f) {
-            // first live chunk of the step: seed the winner with the chunk's largest
-            // weight (exactly evaluated) so the bound below is finite
-            int js = 0;
-            float wj = 0.f, lj = 0.f;
+          const int tile = t_begin + t;
+          if (t == 0 || (tile & 1) == 0)
+            philox4x32_10_rk(static_cast<uint32_t>(tile >> 1), static_cast<uint32_t>(k), b_global,
+                             1u + static_cast<uint32_t>(g), p.round_key0, p.round_key1, nz);
+          const uint32_t word1 = (tile & 1) ? nz[2] : nz[0];
+          const uint32_t word2 = (tile & 1) ? nz[3] : nz[1];
+          // stage 1: the block's race score (log2 units)
+          const float G = m2 + lg2_approx(bsum) - lg2_approx(neg_log_uniform_fast(word1));
+          // Any key already reached for this request (by this thread, this CTA or,
+          // as last read, another CTA) bounds the winner from below.
+          const unsigned long long sb = s_bound[b];
+          const float S = key_score(sb > gkey ? sb : gkey);
+          if (bsum > 0.f && G >= S) {
+            // stage 2: inverse CDF inside the block (cumulative mass in token order)
+            float C[16];
+            C[0] = w[0];
 #pragma unroll
-            for (int q2 = 15; q2 >= 0; --q2) {
-              if (w[q2] == 1.0f) {  // y == cmax == m2 in the first live chunk
-                js = q2;
-                wj = w[q2];
-                lj = y[q2] * inv_scale2;
-              }
+            for (int j = 1; j < 16; ++j) C[j] = C[j - 1] + w[j];
+            const float target = philox_uniform(word2) * C[15];
+            int js = -1, jl = 0;
+#pragma unroll
+            for (int j = 15; j >= 0; --j) {
+              if (target < C[j]) js = j;
+              if (jl == 0 && w[j] > 0.f) jl = j;
             }
-            if (exact_race_update(wj, philox_word(vbase + js, kc, b_global, p), lj, vbase + js,
-                                  wb, e2b, vb, lb, cthr))
-              atomicMax(&s_bound[b], make_key(p.epoch, lb * scale2 - log2f(e2b), vb));
-          }
-          uint32_t words[16];
-          philox4x32_10_xn<4>(static_cast<uint32_t>(vbase >> 2), kc, b_global, p.round_key0,
-                              p.round_key1, words);
-          // Any score already reached for this request (here, in this CTA, or
-          // published by another CTA) bounds the winner from below: an element
-          // needs y - log2(E2) > S, i.e. E < w * ln2 * 2^(m2 - S).
-          const unsigned long long bkey = s_bound[b] > gkey ? s_bound[b] : gkey;
-          const float S = key_score(bkey);
-          const float cth = fminf(cthr, kLn2 * ex2_approx(m2 - S));
-          const float2 cth2 = make_float2(cth, cth);
-          const float2 negc = make_float2(-0.99999994039535522461f, -0.99999994039535522461f);
-          uint32_t cand = 0;
+            if (js < 0) js = jl;  // target at the very top (rounding): the last live token
+            float yj = 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            const float2 t2 = __fadd2_rn(make_float2(philox_one_plus_complement(words[j]),
-                                                     philox_one_plus_complement(words[j + 1])),
-                                         negc);  // 1 - u, exact
-            const float2 x2 = __fmul2_rn(make_float2(w[j], w[j + 1]), cth2);
-            if (t2.x < x2.x) cand |= 1u << j;
-            if (t2.y < x2.y) cand |= 2u << j;
-          }
-          while (cand != 0u) {  // rare: a few per thread and step
-            const int j = __ffs(cand) - 1;
-            cand &= cand - 1u;
-            float wj = 0.f, lj = 0.f;
-#pragma unroll
-            for (int q2 = 0; q2 < 16; ++q2) {
-              if (q2 == j) {
-                wj = w[q2];
-                lj = y[q2];
-              }
+            for (int j = 0; j < 16; ++j)
+              if (j == js) yj = y[j];
+            const unsigned long long key = make_key(p.epoch, G, vbase + js);
+            if (key > bkey) {
+              bkey = key;
+              yb = G;
+              vb = vbase + js;
+              lb = yj * inv_scale2;
+              atomicMax(&s_bound[b], key);
             }
-            lj *= inv_scale2;
-            if (exact_race_update(wj, philox_word(vbase + j, kc, b_global, p), lj, vbase + j, wb,
-                                  e2b, vb, lb, cthr))
-              atomicMax(&s_bound[b], make_key(p.epoch, lb * scale2 - log2f(e2b), vb));
           }
           if ((t & 1) == 1 && g == 0) {
             // share this CTA's best with the other CTAs (rate-limited)
@@ -679,12 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 
       // ---- merge the four column groups of each request, publish the CTA's partial
       if (etid == 0) trace_stamp(p, cta, k, 3);
-      float score;
-      if (MODE == kModeSample) {
-        score = (vb != 0x7FFFFFFF) ? lb * scale2 - log2f(e2b) : -INFINITY;
-      } else {
-        score = yb;
-      }
+      const float score = yb;
       if (!fail) {
         merge[(g * 5 + 0) * kRows + b] = m2;
         merge[(g * 5 + 1) * kRows + b] = sum;

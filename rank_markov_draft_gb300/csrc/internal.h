@@ -15,12 +15,13 @@ constexpr int kMaxRank = 256;       // Markov rank
 constexpr int kBatchChunk = 128;    // requests per draft launch (MMA M)
 constexpr int kDraftTileV = 64;     // vocabulary entries per draft tile (MMA N)
 constexpr int kMaxTopk = 32;
+constexpr int kTopkPartUnits = 4096;  // per-piece top-k lists the context can hold
 constexpr int kTraceSlots = 8;      // timestamps per (CTA, step) in the draft trace
 constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s per wait
 
 // Per-(step, request, CTA) record of the draft kernel's cross-CTA reduction.
 struct DraftPartial {
-  unsigned long long key;  // (epoch, Gumbel score, token) packed, see draft.cu
+  unsigned long long key;  // (epoch, race score, token) packed, see draft.cu
   float m2;                // running max of l * log2(e) / T'
   float sum;               // sum of 2^(y - m2)
   float lbest;             // calibrated logit of this CTA's best token
@@ -91,12 +92,16 @@ cudaError_t launch_gate_gemm(const GateArgs& args, cudaStream_t stream);
 cudaError_t launch_gate_finalize(const float* partial, int splits, int64_t n, float* H,
                                  cudaStream_t stream);
 
+// Top-k of each row of U [rows][V] (V a multiple of 4).  part_i / part_v: scratch
+// for up to part_units per-piece lists of kMaxTopk entries (null: whole rows
+// only).  *launches receives the number of kernels launched.
 cudaError_t launch_topk(const float* U, int rows, int V, int topk, int32_t* cand, float* cval,
-                        cudaStream_t stream);
+                        int32_t* part_i, float* part_v, int part_units, int* status,
+                        uint64_t timeout_ns, int* launches, cudaStream_t stream);
 cudaError_t launch_pair_scores(const int32_t* cand, const float* cval, const uint16_t* A,
                                const uint16_t* Bt, const int32_t* anchors, const float* H,
                                int B, int K, int V, int r, int topk, float* S, int* status,
-                               cudaStream_t stream);
+                               uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anchors,
                         const uint16_t* A, int B, int K, int V, int r, int topk, float inv_t,
                         int sample, uint32_t seed_lo, uint32_t seed_hi, int32_t* tokens,

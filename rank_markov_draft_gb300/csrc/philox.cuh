@@ -5,9 +5,11 @@
 // mixing the high halves with words 1 and 3 and the round key; the key is
 // advanced by the Weyl increments between rounds.
 //
-// Token-sampling noise of the Markov head (the pages ask for a counter-based
-// generator keyed on request, position and token): counter = (v >> 2, k, b, 0),
-// key = (seed low, seed high); word v & 3 becomes
+// Noise of the Markov head's draw (a counter-based generator keyed on request
+// b, position k and 16-token block beta = v >> 4): key = (seed low, seed high),
+// counter = (beta >> 3, k, b, 1 + (beta & 3)); with h = (beta >> 2) & 1, word 2h
+// is the block's stage-1 uniform (the race between blocks) and word 2h + 1 its
+// stage-2 uniform (the inverse CDF inside the block).  A word becomes
 // u = ((word & 0x7FFFFF) + 0.5) * 2^-23, an odd multiple of 2^-24 in (0, 1).
 #pragma once
 
@@ -42,6 +44,27 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
   r.w[2] = c2;
   r.w[3] = c3;
   return r;
+}
+
+// One block with counter (c0, c1, c2, c3) and a precomputed key schedule.
+__device__ __forceinline__ void philox4x32_10_rk(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                 uint32_t c3, const uint32_t (&rk0)[10],
+                                                 const uint32_t (&rk1)[10], uint32_t (&out)[4]) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ c1 ^ rk0[round];
+    const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ c3 ^ rk1[round];
+    c0 = n0;
+    c1 = static_cast<uint32_t>(pb);
+    c2 = n2;
+    c3 = static_cast<uint32_t>(pa);
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
 }
 
 // Philox key schedule: round i uses (k0 + i * 0x9E3779B9, k1 + i * 0xBB67AE85).
@@ -117,8 +140,28 @@ __device__ __forceinline__ float philox_uniform(uint32_t word) {
   return one_plus - 0.99999994039535522461f;  // 1 - 2^-24
 }
 
+// E = -ln(u) for the uniform u of `word`, to about 1e-6 relative, without a
+// branch: with t = 1 - u (exact), the Taylor series of -ln(1 - t) to t^8 / 8
+// for t < 1/8 (remainder below t^8 / 8 relative), else -log2(u) ln 2 from the
+// hardware base-2 logarithm (|ln u| >= 0.13 there, so its absolute error of
+// about 2^-22 stays near 1e-6 relative).
+__device__ __forceinline__ float neg_log_uniform_fast(uint32_t word) {
+  const float t = philox_one_minus_uniform(word);
+  float sr = fmaf(t, 0.125f, 0.142857142857f);
+  sr = fmaf(t, sr, 0.166666666667f);
+  sr = fmaf(t, sr, 0.2f);
+  sr = fmaf(t, sr, 0.25f);
+  sr = fmaf(t, sr, 0.333333333333f);
+  sr = fmaf(t, sr, 0.5f);
+  sr = fmaf(t, sr, 1.0f);
+  sr *= t;
+  float l2;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(1.0f - t));
+  return (t < 0.125f) ? sr : -l2 * 0.69314718055994531f;
+}
+
 // Accurate E = -ln(u) for u in (0, 1): -log(u) below 1/2; above it, with
-// t = 1 - u exact, -log1p(-t), so the small values (large Gumbel noise) keep
+// t = 1 - u exact, -log1p(-t), so the small values (the race's fast arrivals) keep
 // their relative accuracy.
 __device__ __forceinline__ float neg_log_uniform_accurate(float u) {
   return (u < 0.5f) ? -logf(u) : -log1pf(-(1.0f - u));

@@ -18,9 +18,12 @@
 //                      candidate rows of B into shared memory, then computes
 //                      the k x k dot products on CUDA cores (0.5 GFLOP for a
 //                      256 x 16 block: not worth the tensor cores).
-//   walk_kernel        one warp per request, lanes = candidates: Gumbel-max
-//                      with noise keyed by the candidate's token id, softmax
-//                      over the k candidates, optional fused confidence head.
+//   walk_kernel        one CTA per request: the candidates' noise and score
+//                      tables are staged in shared memory by all warps, then
+//                      one warp walks the positions (lanes = candidates) with
+//                      the Markov head's own two-stage block race restricted
+//                      to the candidates, softmax over the k candidates; the
+//                      optional confidence head runs for all positions at once.
 
 #include <cstdint>
 
@@ -83,57 +86,314 @@ struct WarpTopk {
   }
 };
 
-constexpr int kTopkWarps = 8;
+constexpr int kTopkWarps = 8;                          // scanning warps
+constexpr int kTopkThreads = (kTopkWarps + 1) * 32;   // + one copy warp
+constexpr int kTopkChunk = 4096;                      // floats per ring stage (16 KB)
+constexpr int kTopkStages = 4;
+constexpr uint32_t kTopkRingBytes = kTopkStages * kTopkChunk * 4;
+constexpr int kNoIndex = 0x7FFFFFFF;
+constexpr uint32_t kTopkBar = 1;                      // named barrier of the scanning warps
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ U, int V,
-                                                               int topk, int32_t* __restrict__ cand,
-                                                               float* __restrict__ cval) {
+__device__ __forceinline__ uint32_t ordered_u32(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered_u32(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+struct TopkArgs {
+  const float* U;      // [rows][V]
+  int rows, V, topk;
+  int pieces;          // pieces per row (1: each CTA scans whole rows)
+  int piece_len;       // tokens per piece, a multiple of 4
+  int32_t* cand;       // pieces == 1: [rows][topk]
+  float* cval;
+  int32_t* part_i;     // pieces > 1: [rows * pieces][topk]
+  float* part_v;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+// Streaming top-k of each row of U.  Work unit = (row, piece); CTA c takes
+// units c, c + grid, ...  One lane of the copy warp streams the unit's floats
+// through a 4-stage shared-memory ring with bulk copies; each scanning warp
+// takes a 512-float slice of every stage and keeps a sorted top-k list in its
+// lanes.  The k-th value of any full list is a lower bound on the row's k-th
+// value (it has k real elements above it), so the CTA shares the largest one
+// and every warp skips elements below it: a warp touches its list only for
+// the few elements that can still enter the row's top-k.
+__global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_constant__ TopkArgs a) {
+  extern __shared__ __align__(128) uint8_t topk_smem[];
+  float* ring = reinterpret_cast<float*>(topk_smem);
+  __shared__ __align__(8) uint64_t full[kTopkStages];
+  __shared__ __align__(8) uint64_t empty[kTopkStages];
   __shared__ float s_v[kTopkWarps][32];
   __shared__ int s_i[kTopkWarps][32];
+  __shared__ uint32_t s_floor;  // ordered bits of the best k-th value held by a full list
+  __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = blockIdx.x;
-  const float* u = U + row * V;
-  // contiguous segment per warp, a multiple of 4 tokens
-  const int seg = ((V + kTopkWarps - 1) / kTopkWarps + 3) & ~3;
-  const int s0 = warp * seg;
-  const int s1 = min(V, s0 + seg);
+  const int units = a.rows * a.pieces;
+  volatile int* abort_flag = &s_abort;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTopkStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTopkWarps);
+    }
+    s_floor = ordered_u32(-INFINITY);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kTopkWarps) {
+    // ------------------------------------------------------------ copy warp
+    if (lane != 0) return;
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t issued = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
+      const int row = unit / a.pieces, piece = unit - row * a.pieces;
+      const int e0 = piece * a.piece_len, e1 = min(a.V, e0 + a.piece_len);
+      const float* src = a.U + static_cast<size_t>(row) * a.V;
+      for (int c0 = e0; c0 < e1; c0 += kTopkChunk) {
+        const int s = static_cast<int>(issued % kTopkStages);
+        if (!mbar_wait(&empty[s], ((issued / kTopkStages) & 1u) ^ 1u, a.timeout_ns, abort_flag,
+                       200u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bytes = static_cast<uint32_t>(min(kTopkChunk, e1 - c0)) * 4u;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(ring + s * kTopkChunk, src + c0, bytes, &full[s], pol);
+        ++issued;
+      }
+    }
+    if (!ok) {
+      s_abort = 1;
+      record_error(a.status, kStatusTimeout);
+      // every copy in flight must land before the CTA exits
+      for (uint32_t j = issued > kTopkStages ? issued - kTopkStages : 0u; j < issued; ++j)
+        mbar_wait(&full[j % kTopkStages], (j / kTopkStages) & 1u, a.timeout_ns, nullptr);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- scanning warps
+  uint32_t consumed = 0;
+  bool ok = true;
+  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int row = unit / a.pieces, piece = unit - row * a.pieces;
+    const int e0 = piece * a.piece_len, e1 = min(a.V, e0 + a.piece_len);
+    WarpTopk list;
+    list.init();
+    for (int c0 = e0; c0 < e1; c0 += kTopkChunk, ++consumed) {
+      const int s = static_cast<int>(consumed % kTopkStages);
+      if (ok) ok = mbar_wait(&full[s], (consumed / kTopkStages) & 1u, a.timeout_ns, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) continue;  // keep walking the units so the named barriers below still meet
+      const int n = min(kTopkChunk, e1 - c0);
+      const float* chunk = ring + s * kTopkChunk;
+      float4 x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int off = warp * 512 + j * 128 + lane * 4;
+        x[j] = (off < n) ? *reinterpret_cast<const float4*>(chunk + off)
+                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the slice is in registers: free the stage
+      const float floor_v = fmaxf(list.tv, from_ordered_u32(s_floor));
+      float mx = fmaxf(fmaxf(fmaxf(x[0].x, x[0].y), fmaxf(x[0].z, x[0].w)),
+                       fmaxf(fmaxf(x[1].x, x[1].y), fmaxf(x[1].z, x[1].w)));
+      mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(x[2].x, x[2].y), fmaxf(x[2].z, x[2].w)),
+                           fmaxf(fmaxf(x[3].x, x[3].y), fmaxf(x[3].z, x[3].w))));
+      if (!__any_sync(0xFFFFFFFFu, mx >= floor_v)) continue;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int off = warp * 512 + j * 128 + lane * 4;
+        const bool in = off < n;
+        const int idx = c0 + off;
+        list.offer(x[j].x, idx + 0, in && x[j].x >= floor_v, lane, a.topk);
+        list.offer(x[j].y, idx + 1, in && x[j].y >= floor_v, lane, a.topk);
+        list.offer(x[j].z, idx + 2, in && x[j].z >= floor_v, lane, a.topk);
+        list.offer(x[j].w, idx + 3, in && x[j].w >= floor_v, lane, a.topk);
+      }
+      if (lane == 0 && list.ti != kNoIndex) atomicMax(&s_floor, ordered_u32(list.tv));
+    }
+    // ---- merge the warps' lists
+    s_v[warp][lane] = list.lv;
+    s_i[warp][lane] = list.li;
+    named_bar_sync(kTopkBar, kTopkWarps * 32);
+    if (warp == 0 && !*abort_flag) {
+      for (int w = 1; w < kTopkWarps; ++w) {
+        const float v = s_v[w][lane];
+        const int vi = s_i[w][lane];
+        list.offer(v, vi, lane < a.topk && vi != kNoIndex, lane, a.topk);
+      }
+      if (lane < a.topk) {
+        if (a.pieces == 1) {
+          a.cand[static_cast<size_t>(row) * a.topk + lane] = list.li;
+          a.cval[static_cast<size_t>(row) * a.topk + lane] = list.lv;
+        } else {
+          a.part_i[static_cast<size_t>(unit) * a.topk + lane] = list.li;
+          a.part_v[static_cast<size_t>(unit) * a.topk + lane] = list.lv;
+        }
+      }
+    }
+    if (threadIdx.x == 0) s_floor = ordered_u32(-INFINITY);
+    named_bar_sync(kTopkBar, kTopkWarps * 32);
+  }
+}
+
+// Row-wise merge of the pieces' lists (one warp per row).
+__global__ void __launch_bounds__(128) topk_merge_kernel(const int32_t* __restrict__ part_i,
+                                                         const float* __restrict__ part_v,
+                                                         int rows, int pieces, int topk,
+                                                         int32_t* __restrict__ cand,
+                                                         float* __restrict__ cval) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int n = pieces * topk;
+  const size_t base = static_cast<size_t>(row) * n;
   WarpTopk list;
   list.init();
-  constexpr int kUnroll = 4;
-  for (int base = s0; base < s1; base += 128 * kUnroll) {
-    float4 x[kUnroll];
+  for (int e0 = 0; e0 < n; e0 += 32) {
+    const int e = e0 + lane;
+    const int vi = (e < n) ? __ldg(part_i + base + e) : kNoIndex;
+    const float v = (e < n) ? __ldg(part_v + base + e) : -INFINITY;
+    list.offer(v, vi, vi != kNoIndex, lane, topk);
+  }
+  if (lane < topk) {
+    cand[static_cast<size_t>(row) * topk + lane] = list.li;
+    cval[static_cast<size_t>(row) * topk + lane] = list.lv;
+  }
+}
+
+constexpr int kPairWarps = 4;  // (request, position) pairs per CTA, one per warp
+
+// Shared bytes of one warp of pair_scores16_kernel: 32 gathered bf16 rows of
+// r + 8 elements (the 16-byte pad spreads the 4 x 4 register tiles' loads over
+// all banks) and, when gated, the fp32 gate row.
+__host__ __device__ __forceinline__ int pair16_warp_bytes(int r, bool gated) {
+  return 32 * (2 * r + 16) + (gated ? 4 * r : 0);
+}
+
+// k <= 16 candidates: one warp per (request, position).  Lanes 0..15 bulk-copy
+// the k predecessor rows of A, lanes 16..31 the k candidate rows of B (and
+// lane 0 the gate row) into shared memory on one mbarrier; then lane
+// (half, blk) accumulates a 4 x 4 tile of S (rows blk % 4 + 4m, columns
+// blk / 4 + 4n) over half of the rank, and the halves are summed by a shuffle.
+__global__ void __launch_bounds__(kPairWarps * 32) pair_scores16_kernel(
+    const int32_t* __restrict__ cand, const float* __restrict__ cval,
+    const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bt,
+    const int32_t* __restrict__ anchors, const float* __restrict__ H, int BK, int K, int V,
+    int r, int topk, float* __restrict__ S, int* status, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t pair_smem[];
+  __shared__ __align__(8) uint64_t bar[kPairWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool gated = H != nullptr;
+  const int row_bytes = 2 * r + 16;
+  uint8_t* wbase = pair_smem + warp * pair16_warp_bytes(r, gated);
+  if (lane == 0) {
+    mbar_init(&bar[warp], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const size_t bt = static_cast<size_t>(blockIdx.x) * kPairWarps + warp;
+  if (bt >= static_cast<size_t>(BK)) return;
+  const int b = static_cast<int>(bt / K), t = static_cast<int>(bt % K);
+  // lanes i and 16 + i fetch row i; rows past k repeat row 0 (their outputs are dropped)
+  const int i = (lane & 15) < topk ? (lane & 15) : 0;
+  int tok;
+  if (lane < 16) {
+    tok = (t == 0) ? __ldg(anchors + b) : __ldg(cand + (bt - 1) * topk + i);
+  } else {
+    tok = __ldg(cand + bt * topk + i);
+  }
+  if (tok < 0 || tok >= V) {
+    record_error(status, kStatusDeviceOob);
+    tok = min(max(tok, 0), V - 1);
+  }
+  const uint64_t pol = l2_policy_evict_last();
+  if (lane == 0) mbar_arrive_expect_tx(&bar[warp], 32u * 2u * r + (gated ? 4u * r : 0u));
+  __syncwarp();
+  bulk_load(wbase + lane * row_bytes, (lane < 16 ? A : Bt) + static_cast<size_t>(tok) * r,
+            2u * r, &bar[warp], pol);
+  if (gated && lane == 0) bulk_load(wbase + 32 * row_bytes, H + bt * r, 4u * r, &bar[warp], pol);
+  if (!mbar_wait(&bar[warp], 0, timeout_ns, nullptr)) {
+    record_error(status, kStatusTimeout);
+    return;
+  }
+  const int half = lane >> 4, blk = lane & 15;
+  const int ib = blk & 3, jb = blk >> 2;
+  const float* hrow = reinterpret_cast<const float*>(wbase + 32 * row_bytes);
+  float acc[4][4];
 #pragma unroll
-    for (int r = 0; r < kUnroll; ++r) {
-      const int idx = base + r * 128 + lane * 4;
-      x[r] = (idx < s1) ? __ldcs(reinterpret_cast<const float4*>(u + idx))
-                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
+  for (int m = 0; m < 4; ++m)
 #pragma unroll
-    for (int r = 0; r < kUnroll; ++r) {
-      const int idx = base + r * 128 + lane * 4;
-      const bool in = idx < s1;
-      list.offer(x[r].x, idx + 0, in, lane, topk);
-      list.offer(x[r].y, idx + 1, in, lane, topk);
-      list.offer(x[r].z, idx + 2, in, lane, topk);
-      list.offer(x[r].w, idx + 3, in, lane, topk);
+    for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
+  // half h takes rank elements [64 c + 32 h, 64 c + 32 h + 32) of every 64
+  for (int q0 = half * 32; q0 < r; q0 += 64) {
+#pragma unroll
+    for (int sub = 0; sub < 4; ++sub) {
+      const int q = q0 + sub * 8;
+      if (q >= r) break;
+      uint4 av[4], bv[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        av[m] = *reinterpret_cast<const uint4*>(wbase + (ib + 4 * m) * row_bytes + 2 * q);
+        bv[m] = *reinterpret_cast<const uint4*>(wbase + (16 + jb + 4 * m) * row_bytes + 2 * q);
+      }
+      float g[8];
+      if (gated) {
+        const float4 g0 = *reinterpret_cast<const float4*>(hrow + q);
+        const float4 g1 = *reinterpret_cast<const float4*>(hrow + q + 4);
+        g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+        g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float a[4], bb[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t aw = (e >> 1) == 0 ? av[m].x : (e >> 1) == 1 ? av[m].y
+                            : (e >> 1) == 2 ? av[m].z : av[m].w;
+          const uint32_t bw = (e >> 1) == 0 ? bv[m].x : (e >> 1) == 1 ? bv[m].y
+                            : (e >> 1) == 2 ? bv[m].z : bv[m].w;
+          a[m] = (e & 1) ? __uint_as_float(aw & 0xFFFF0000u) : __uint_as_float(aw << 16);
+          bb[m] = (e & 1) ? __uint_as_float(bw & 0xFFFF0000u) : __uint_as_float(bw << 16);
+          if (gated) a[m] *= g[e];
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(a[m], bb[n], acc[m][n]);
+      }
     }
   }
-  s_v[warp][lane] = list.lv;
-  s_i[warp][lane] = list.li;
-  __syncthreads();
-  if (warp == 0) {
-    for (int w = 1; w < kTopkWarps; ++w) {
-      const float x = s_v[w][lane];
-      const int xi = s_i[w][lane];
-      list.offer(x, xi, lane < topk && xi != 0x7FFFFFFF, lane, topk);
-    }
-    if (lane < topk) {
-      cand[row * topk + lane] = list.li;
-      cval[row * topk + lane] = list.lv;
+#pragma unroll
+  for (int m = 0; m < 4; ++m)
+#pragma unroll
+    for (int n = 0; n < 4; ++n) acc[m][n] += __shfl_xor_sync(0xFFFFFFFFu, acc[m][n], 16);
+  if (half == 0) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int ii = ib + 4 * m;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int jj = jb + 4 * n;
+        if (ii < topk && jj < topk)
+          S[(bt * topk + ii) * topk + jj] = __ldg(cval + bt * topk + jj) + acc[m][n];
+      }
     }
   }
 }
 
+// k in 17..32: one CTA per (request, position), operands widened to fp32 in
+// shared memory, one thread per score.
 __global__ void __launch_bounds__(256) pair_scores_kernel(
     const int32_t* __restrict__ cand, const float* __restrict__ cval,
     const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bt,
@@ -190,103 +450,255 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
   }
 }
 
-__global__ void __launch_bounds__(128) walk_kernel(
+constexpr int kWalkWarps = 16;
+constexpr int kWalkWindowBytes = 32768;  // score tables staged per window
+
+// One CTA per request.  Per window of positions, all warps stage the k x k
+// score tables and the candidates' noise (it depends on the candidate's block
+// of token ids, not on the path) in shared memory; warp 0 then walks the
+// window: at each position it selects the row of the previous pick and draws
+// with the head's block race over the candidates (the candidates of one
+// 16-token block race as one block with their summed mass, then the inverse
+// CDF in token order inside the winning block; tokens outside the candidate
+// set have no mass), and takes the log-softmax over the k candidates.
+// After the walk, the confidence head runs for all positions at once (one
+// warp per position) and thread 0 forms the survival products.
+__global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(
     const int32_t* __restrict__ cand, const float* __restrict__ S,
     const int32_t* __restrict__ anchors, const uint16_t* __restrict__ A, int B, int K, int V,
-    int r, int topk, float inv_t, int sample, uint32_t seed_lo, uint32_t seed_hi,
+    int r, int topk, int window, float inv_t, int sample, uint32_t seed_lo, uint32_t seed_hi,
     int32_t* __restrict__ tokens, float* __restrict__ logprobs, dspark_conf_args conf,
     int conf_on, int* status) {
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (b >= B) return;
+  extern __shared__ __align__(16) float walk_smem[];
+  float* s_S = walk_smem;                          // [window][topk][topk]
+  float* s_L = s_S + window * topk * topk;         // [window][32] -ln E of the block race
+  float* s_U2 = s_L + window * 32;                 // [window][32] stage-2 uniform
+  int* s_C = reinterpret_cast<int*>(s_U2 + window * 32);  // [window][32] candidates
+  __shared__ int s_tok[kMaxK];
+  __shared__ float s_conf[kMaxK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  const int tile = topk * topk;
   int slot = 0;
-  int prev_tok = anchors[b];
-  float surv = 1.f;
-  int len = 0;
-  bool open = true;
-  for (int t = 0; t < K; ++t) {
-    const size_t bt = static_cast<size_t>(b) * K + t;
-    const bool live = lane < topk;
-    const float sv = live ? S[(bt * topk + slot) * topk + lane] : -INFINITY;
-    const int c = live ? cand[bt * topk + lane] : 0x7FFFFFFF;
-    const float z = sv * inv_t;
-    float s = z;
-    if (sample && live) {
-      const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(c) >> 2, static_cast<uint32_t>(t),
-                                        static_cast<uint32_t>(b), 0u, seed_lo, seed_hi);
-      const float u = philox_uniform(rnd.w[c & 3]);
-      s = z - logf(neg_log_uniform_accurate(u));
+  for (int t0 = 0; t0 < K; t0 += window) {
+    const int nt = min(window, K - t0);
+    const size_t base = (static_cast<size_t>(b) * K + t0) * tile;
+    for (int e = threadIdx.x; e < nt * tile; e += blockDim.x) s_S[e] = __ldg(S + base + e);
+    for (int w = warp; w < nt; w += kWalkWarps) {
+      const int t = t0 + w;
+      const size_t bt = static_cast<size_t>(b) * K + t;
+      const int c = lane < topk ? __ldg(cand + bt * topk + lane) : 0x7FFFFFFF;
+      float lnE = 0.f, u2 = 0.f;
+      if (sample && lane < topk) {
+        const uint32_t blk = static_cast<uint32_t>(c) >> 4;
+        const Philox4 rnd = philox4x32_10(blk >> 3, static_cast<uint32_t>(t),
+                                          static_cast<uint32_t>(b), 1u + (blk & 3u), seed_lo,
+                                          seed_hi);
+        const int h = (blk >> 2) & 1u;
+        lnE = -logf(neg_log_uniform_accurate(philox_uniform(h ? rnd.w[2] : rnd.w[0])));
+        u2 = philox_uniform(h ? rnd.w[3] : rnd.w[1]);
+      }
+      s_L[w * 32 + lane] = lnE;
+      s_U2[w * 32 + lane] = u2;
+      s_C[w * 32 + lane] = c;
     }
-    // argmax by (score desc, token id asc)
-    float best_s = live ? s : -INFINITY;
-    int best_c = c, best_j = lane;
+    __syncthreads();
+    if (warp == 0) {
+      const bool live = lane < topk;
+      for (int w = 0; w < nt; ++w) {
+        const int t = t0 + w;
+        const size_t bt = static_cast<size_t>(b) * K + t;
+        const float z = live ? s_S[(w * topk + slot) * topk + lane] * inv_t : -INFINITY;
+        const int c = s_C[w * 32 + lane];
+        float m = z;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float os = __shfl_xor_sync(0xFFFFFFFFu, best_s, off);
-      const int oc = __shfl_xor_sync(0xFFFFFFFFu, best_c, off);
-      const int oj = __shfl_xor_sync(0xFFFFFFFFu, best_j, off);
-      if (better(os, oc, best_s, best_c)) {
-        best_s = os;
-        best_c = oc;
-        best_j = oj;
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        const float e = live ? expf(z - m) : 0.f;
+        int best_c, best_j;
+        if (sample) {
+          // stage 1: the mass of this candidate's block (candidates of the same block)
+          const int blk = live ? (c >> 4) : -1;
+          float Z = 0.f;
+          for (int i = 0; i < topk; ++i) {
+            const int bi = __shfl_sync(0xFFFFFFFFu, blk, i);
+            const float ei = __shfl_sync(0xFFFFFFFFu, e, i);
+            if (bi == blk) Z += ei;
+          }
+          float bs = (live && Z > 0.f) ? logf(Z) + s_L[w * 32 + lane] : -INFINITY;
+          int bb = live ? blk : 0x7FFFFFFF;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
+            const int ob = __shfl_xor_sync(0xFFFFFFFFu, bb, off);
+            if (os > bs || (os == bs && ob < bb)) {
+              bs = os;
+              bb = ob;
+            }
+          }
+          // stage 2: inverse CDF in token order inside the winning block
+          const bool inb = live && blk == bb;
+          float C = 0.f;
+          for (int i = 0; i < topk; ++i) {
+            const int bi = __shfl_sync(0xFFFFFFFFu, blk, i);
+            const int ci = __shfl_sync(0xFFFFFFFFu, c, i);
+            const float ei = __shfl_sync(0xFFFFFFFFu, e, i);
+            if (bi == bb && ci <= c) C += ei;
+          }
+          const int src = __ffs(__ballot_sync(0xFFFFFFFFu, inb)) - 1;
+          const float Zb = __shfl_sync(0xFFFFFFFFu, Z, src);
+          const float target = s_U2[w * 32 + src] * Zb;
+          // smallest crossing token, else the largest live token of the block
+          int pick = (inb && e > 0.f && target < C) ? c : 0x7FFFFFFF;
+          int last = (inb && e > 0.f) ? c : -1;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            pick = min(pick, __shfl_xor_sync(0xFFFFFFFFu, pick, off));
+            last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, off));
+          }
+          best_c = (pick != 0x7FFFFFFF) ? pick : last;
+          best_j = __ffs(__ballot_sync(0xFFFFFFFFu, live && c == best_c)) - 1;
+        } else {
+          // greedy: argmax by (score desc, token id asc)
+          float best_s = z;
+          best_c = c;
+          best_j = lane;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float os = __shfl_xor_sync(0xFFFFFFFFu, best_s, off);
+            const int oc = __shfl_xor_sync(0xFFFFFFFFu, best_c, off);
+            const int oj = __shfl_xor_sync(0xFFFFFFFFu, best_j, off);
+            if (better(os, oc, best_s, best_c)) {
+              best_s = os;
+              best_c = oc;
+              best_j = oj;
+            }
+          }
+        }
+        float ex = e;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ex += __shfl_xor_sync(0xFFFFFFFFu, ex, off);
+        const float zw = __shfl_sync(0xFFFFFFFFu, z, best_j);
+        if (best_c < 0 || best_c >= V) {
+          if (lane == 0) record_error(status, kStatusDeviceOob);
+          best_c = 0;
+        }
+        if (lane == 0) {
+          tokens[bt] = best_c;
+          logprobs[bt] = zw - (m + logf(ex));
+          s_tok[t] = best_c;
+        }
+        slot = best_j;
       }
     }
-    float m = live ? z : -INFINITY;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    float e = live ? expf(z - m) : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
-    const float zw = __shfl_sync(0xFFFFFFFFu, z, best_j);
-    if (best_c < 0 || best_c >= V) {
-      if (lane == 0) record_error(status, kStatusDeviceOob);
-      best_c = 0;
-    }
-    if (lane == 0) {
-      tokens[bt] = best_c;
-      logprobs[bt] = zw - (m + logf(e));
-    }
-    if (conf_on) {
-      const uint16_t* emb = conf.with_markov ? A + static_cast<size_t>(prev_tok) * r : nullptr;
-      const float zc = confidence_logit(conf.h + bt * conf.d, conf.d, conf.w, emb, r, conf.bias,
-                                        lane);
-      const float cc = sigmoidf_accurate(zc);
+    __syncthreads();
+  }
+  if (!conf_on) return;
+  for (int t = warp; t < K; t += kWalkWarps) {
+    const size_t bt = static_cast<size_t>(b) * K + t;
+    const int prev_tok = (t == 0) ? __ldg(anchors + b) : s_tok[t - 1];
+    const uint16_t* emb = conf.with_markov ? A + static_cast<size_t>(prev_tok) * r : nullptr;
+    const float zc = confidence_logit(conf.h + bt * conf.d, conf.d, conf.w, emb, r, conf.bias,
+                                      lane);
+    if (lane == 0) s_conf[t] = sigmoidf_accurate(zc);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float surv = 1.f;
+    int len = 0;
+    bool open = true;
+    for (int t = 0; t < K; ++t) {
+      const size_t bt = static_cast<size_t>(b) * K + t;
+      const float cc = s_conf[t];
       surv *= cc;
       if (open && surv >= conf.threshold) {
         len = t + 1;
       } else {
         open = false;
       }
-      if (lane == 0) {
-        conf.conf[bt] = cc;
-        conf.cumprod[bt] = surv;
-      }
+      conf.conf[bt] = cc;
+      conf.cumprod[bt] = surv;
     }
-    slot = best_j;
-    prev_tok = best_c;
+    conf.verify_len[b] = len;
   }
-  if (conf_on && lane == 0) conf.verify_len[b] = len;
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const float* U, int rows, int V, int topk, int32_t* cand, float* cval,
-                        cudaStream_t stream) {
-  topk_kernel<<<rows, kTopkWarps * 32, 0, stream>>>(U, V, topk, cand, cval);
-  return cudaGetLastError();
+                        int32_t* part_i, float* part_v, int part_units, int* status,
+                        uint64_t timeout_ns, int* launches, cudaStream_t stream) {
+  *launches = 0;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  int sms = 0, occ = 0;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return err;
+  const void* fn = reinterpret_cast<const void*>(&topk_stream_kernel);
+  if ((err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kTopkRingBytes))) != cudaSuccess)
+    return err;
+  // three 66 KB rings per SM need the largest shared-memory carveout
+  if ((err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+    return err;
+  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kTopkThreads,
+                                                           kTopkRingBytes)) != cudaSuccess)
+    return err;
+  const int capacity = sms * (occ > 0 ? occ : 1);
+  // Few rows: split each into pieces (of at least one ring stage) so that the
+  // grid fills the GPU; the pieces' lists are merged by a second kernel.
+  int pieces = 1;
+  if (rows < 2 * capacity && part_i != nullptr && part_units >= 2 * rows) {
+    const int want = (2 * capacity + rows - 1) / rows;
+    const int most = (V + kTopkChunk - 1) / kTopkChunk;
+    pieces = min(min(want, most), part_units / rows);
+  }
+  int piece_len = V;
+  if (pieces > 1) {
+    piece_len = (((V + pieces - 1) / pieces) + 3) & ~3;
+    pieces = (V + piece_len - 1) / piece_len;
+  }
+  TopkArgs a{U, rows, V, topk, pieces, piece_len, cand, cval, part_i, part_v, status, timeout_ns};
+  const int units = rows * pieces;
+  const int grid = min(units, capacity);
+  topk_stream_kernel<<<grid, kTopkThreads, kTopkRingBytes, stream>>>(a);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  *launches = 1;
+  if (pieces == 1) return cudaSuccess;
+  topk_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(part_i, part_v, rows, pieces, topk, cand,
+                                                        cval);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  *launches = 2;
+  return cudaSuccess;
 }
 
 cudaError_t launch_pair_scores(const int32_t* cand, const float* cval, const uint16_t* A,
                                const uint16_t* Bt, const int32_t* anchors, const float* H,
                                int B, int K, int V, int r, int topk, float* S, int* status,
-                               cudaStream_t stream) {
+                               uint64_t timeout_ns, cudaStream_t stream) {
+  cudaError_t err;
+  const int BK = B * K;
+  if (topk <= 16) {
+    const size_t smem = static_cast<size_t>(kPairWarps) * pair16_warp_bytes(r, H != nullptr);
+    err = cudaFuncSetAttribute(reinterpret_cast<const void*>(&pair_scores16_kernel),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(reinterpret_cast<const void*>(&pair_scores16_kernel),
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    pair_scores16_kernel<<<(BK + kPairWarps - 1) / kPairWarps, kPairWarps * 32, smem, stream>>>(
+        cand, cval, A, Bt, anchors, H, BK, K, V, r, topk, S, status, timeout_ns);
+    return cudaGetLastError();
+  }
   const size_t smem = 2ull * topk * (r + 1) * sizeof(float);
-  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(&pair_scores_kernel),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  err = cudaFuncSetAttribute(reinterpret_cast<const void*>(&pair_scores_kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  pair_scores_kernel<<<B * K, 256, smem, stream>>>(cand, cval, A, Bt, anchors, H, K, V, r, topk,
-                                                  S, status);
+  pair_scores_kernel<<<BK, 256, smem, stream>>>(cand, cval, A, Bt, anchors, H, K, V, r, topk, S,
+                                                status);
   return cudaGetLastError();
 }
 
@@ -297,10 +709,16 @@ cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anch
                         cudaStream_t stream) {
   dspark_conf_args c{};
   if (conf != nullptr) c = *conf;
-  const int warps = 4;
-  walk_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(
-      cand, S, anchors, A, B, K, V, r, topk, inv_t, sample, seed_lo, seed_hi, tokens, logprobs, c,
-      conf != nullptr ? 1 : 0, status);
+  const int tile_bytes = topk * topk * 4;
+  const int window = max(1, min(K, kWalkWindowBytes / tile_bytes));
+  const size_t smem = static_cast<size_t>(window) * (tile_bytes + 3 * 32 * 4);
+  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(&walk_kernel),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  walk_kernel<<<B, kWalkWarps * 32, smem, stream>>>(cand, S, anchors, A, B, K, V, r, topk, window,
+                                                    inv_t, sample, seed_lo, seed_hi, tokens,
+                                                    logprobs, c, conf != nullptr ? 1 : 0, status);
   return cudaGetLastError();
 }
 

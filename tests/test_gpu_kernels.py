@@ -238,6 +238,46 @@ def test_topk_ties_and_ragged_rows(dsp):
         assert np.array_equal(host(out["cand"]), ref["cand"])
 
 
+@pytest.mark.parametrize("B,K,V", [(2, 3, 50012), (50, 20, 1012), (1, 2, 151936)])
+def test_topk_streaming_shapes(dsp, B, K, V):
+    """Rows split into pieces (few rows, long vocabulary) and CTAs scanning several
+    rows in turn (many short rows); heavy ties across pieces and warp slices, plus an
+    ascending row (every element enters a list) and a descending one."""
+    rng = np.random.default_rng(B * 100003 + V)
+    U = np.round(rng.standard_normal((B, K, V)) * 3).astype(np.float32)
+    U[0, 0] = np.arange(V, dtype=np.float32)
+    U[0, 1] = -np.arange(V, dtype=np.float32)
+    A = bf16_bits((rng.standard_normal((V, 16)) * 0.02).astype(np.float32))
+    anchors = np.zeros(B, np.int32)
+    for k in (1, 16, 32):
+        out = binding.selector_scores(dsp, dev(U), bf(A), bf(A), dev(anchors), topk=k)
+        torch.cuda.synchronize()
+        assert dsp.status() == 0
+        ref = oracle.topk(U, k)
+        assert np.array_equal(host(out["cand"]), ref["cand"]), k
+        assert np.array_equal(host(out["cand_U"]), ref["cval"].astype(np.float32)), k
+
+
+@pytest.mark.parametrize("r,gated", [(64, True), (48, False)])
+def test_pair_scores_k_below_16_and_above(dsp, r, gated):
+    """The 4 x 4 register-tiled path (k <= 16, here 5 and 16) and the one-thread-per-
+    score path (k = 24) against the oracle; gated, and with a rank that is not a
+    multiple of the 64-element split between the two half-warps."""
+    B, K, V, d = 7, 5, 2000, 64
+    inp = _selector_inputs(36, B, K, V, r, d=d, gated=gated)
+    H = oracle.gate(inp.h, inp.Wg) if gated else None
+    for k in (5, 16, 24):
+        out = binding.selector_scores(dsp, dev(inp.U), bf(inp.A), bf(inp.Bt), dev(inp.anchors),
+                                      topk=k, h=bf(inp.h) if gated else None,
+                                      Wg=bf(inp.Wg) if gated else None)
+        torch.cuda.synchronize()
+        assert dsp.status() == 0
+        top = oracle.topk(inp.U, k)
+        assert np.array_equal(host(out["cand"]), top["cand"])
+        S = oracle.pair_scores(top["cand"], top["cval"], inp.A, inp.Bt, inp.anchors, V=V, H=H)
+        assert np.abs(host(out["scores"]) - S).max() <= LOGPROB_TOL, k
+
+
 @pytest.mark.parametrize("T", [1.0, 0.0])
 def test_walk_matches_oracle(dsp, T):
     B, K, V, r, d, k = 40, 6, 1000, 256, 128, 16
