@@ -443,12 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       unsigned long long bkey = 0ull;  // key of (yb, vb)
       unsigned long long gkey = 0ull;  // global key of this request and step, as last read
       uint32_t nz[4] = {0u, 0u, 0u, 0u};  // Philox words of this thread's current tile pair
+      unsigned long long kpre = 0ull;  // global key, read one tile ahead of its use
       for (int t = 0; t < nt && !fail; ++t) {
-        if (MODE == kModeSample && row_ok && (t & (kBoundRefresh - 1)) == 0) {
-          // the freshest bound matters most early in the step; the load overlaps the
-          // tile's barrier waits and operand loads before its first use
-          const unsigned long long kk = __ldcg(p.keys + k * kRows + b);
-          if (key_epoch(kk) == p.epoch && kk > gkey) gkey = kk;
+        if (MODE == kModeSample && row_ok) {
+          // every other tile, refresh the bound with the key read a tile earlier, so
+          // the load's latency is covered by a whole tile's work
+          if (t > 0 && (t & (kBoundRefresh - 1)) == 0 && key_epoch(kpre) == p.epoch &&
+              kpre > gkey)
+            gkey = kpre;
+          if (((t + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
         }
         const int i = k * nt + t;
         const int buf = i & (kNumAcc - 1);

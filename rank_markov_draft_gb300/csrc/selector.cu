@@ -8,16 +8,19 @@
 // A = W1 and B = W2^T); the score S_t(a, b) = U_t(b) + <A(a) (.) H(h_t), B(b)>
 // is from "What the two methods do".
 //
-// Three kernels:
-//   topk_kernel        one CTA per (request, position) row of U, a pure
-//                      streaming scan: each warp keeps a sorted top-k list in
-//                      its lanes and only touches it for the rare element that
-//                      beats the current k-th entry; the CTA merges its 8 lists.
-//   pair_scores_kernel one CTA per (request, position): gathers the k
-//                      predecessor rows of A (times the gate) and the k
-//                      candidate rows of B into shared memory, then computes
-//                      the k x k dot products on CUDA cores (0.5 GFLOP for a
-//                      256 x 16 block: not worth the tensor cores).
+// Kernels:
+//   topk_stream_kernel persistent CTAs over (row, piece) units: a bulk-copy
+//                      ring streams U through shared memory at HBM speed; each
+//                      warp keeps a sorted top-k list in its lanes and touches
+//                      it only for elements above a CTA-wide floor; the lists
+//                      are merged by rank (topk_merge_kernel merges pieces of
+//                      rows split across CTAs when rows are few).
+//   pair_scores16_kernel (k <= 16) one warp per (request, position): bulk-copies
+//                      the k predecessor rows of A (and the gate row) and the k
+//                      candidate rows of B into shared memory and accumulates
+//                      4 x 4 register tiles of the k x k dot products on CUDA
+//                      cores (0.5 GFLOP for a 256 x 16 block: not worth the
+//                      tensor cores); pair_scores_kernel covers k up to 32.
 //   walk_kernel        one CTA per request: the candidates' noise and score
 //                      tables are staged in shared memory by all warps, then
 //                      one warp walks the positions (lanes = candidates) with
@@ -89,7 +92,7 @@ struct WarpTopk {
 constexpr int kTopkWarps = 8;                          // scanning warps
 constexpr int kTopkThreads = (kTopkWarps + 1) * 32;   // + one copy warp
 constexpr int kTopkChunk = 4096;                      // floats per ring stage (16 KB)
-constexpr int kTopkStages = 4;
+constexpr int kTopkStages = 3;                     // 48 KB: four CTAs per SM
 constexpr uint32_t kTopkRingBytes = kTopkStages * kTopkChunk * 4;
 constexpr int kNoIndex = 0x7FFFFFFF;
 constexpr uint32_t kTopkBar = 1;                      // named barrier of the scanning warps
@@ -118,12 +121,17 @@ struct TopkArgs {
 
 // Streaming top-k of each row of U.  Work unit = (row, piece); CTA c takes
 // units c, c + grid, ...  One lane of the copy warp streams the unit's floats
-// through a 4-stage shared-memory ring with bulk copies; each scanning warp
+// through a 3-stage shared-memory ring with bulk copies; each scanning warp
 // takes a 512-float slice of every stage and keeps a sorted top-k list in its
-// lanes.  The k-th value of any full list is a lower bound on the row's k-th
-// value (it has k real elements above it), so the CTA shares the largest one
-// and every warp skips elements below it: a warp touches its list only for
-// the few elements that can still enter the row's top-k.
+// lanes.  A warp touches its list only for elements at or above a floor, a
+// lower bound on the unit's k-th value built from values the CTA has seen:
+//   * the k-th value of any full list (k real elements lie at or above it);
+//   * the smallest of the warps' m-th values, m = ceil(k / 8) (the m best of
+//     every list are >= k distinct elements), which tracks the k-th value of
+//     everything the CTA has seen so far;
+//   * on a unit's first chunk, the k-th largest of the warp's 32 lane maxima.
+// At the end of a unit the 8 lists are merged by rank: each candidate counts
+// the candidates ahead of it and lands in that output slot.
 __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_constant__ TopkArgs a) {
   extern __shared__ __align__(128) uint8_t topk_smem[];
   float* ring = reinterpret_cast<float*>(topk_smem);
@@ -132,6 +140,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_
   __shared__ float s_v[kTopkWarps][32];
   __shared__ int s_i[kTopkWarps][32];
   __shared__ uint32_t s_floor;  // ordered bits of the best k-th value held by a full list
+  __shared__ uint32_t s_mth[kTopkWarps];  // ordered bits of each warp's m-th best value
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = a.rows * a.pieces;
@@ -142,10 +151,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_
       mbar_init(&empty[s], kTopkWarps);
     }
     s_floor = ordered_u32(-INFINITY);
+    for (int w = 0; w < kTopkWarps; ++w) s_mth[w] = ordered_u32(-INFINITY);
     s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  // m = ceil(k / warps): the m best entries of every warp's list are >= k distinct
+  // elements, so the smallest of the warps' m-th values bounds the k-th value too
+  const int mth = (a.topk + kTopkWarps - 1) / kTopkWarps;
 
   if (warp == kTopkWarps) {
     // ------------------------------------------------------------ copy warp
@@ -204,11 +217,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // the slice is in registers: free the stage
-      const float floor_v = fmaxf(list.tv, from_ordered_u32(s_floor));
       float mx = fmaxf(fmaxf(fmaxf(x[0].x, x[0].y), fmaxf(x[0].z, x[0].w)),
                        fmaxf(fmaxf(x[1].x, x[1].y), fmaxf(x[1].z, x[1].w)));
       mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(x[2].x, x[2].y), fmaxf(x[2].z, x[2].w)),
                            fmaxf(fmaxf(x[3].x, x[3].y), fmaxf(x[3].z, x[3].w))));
+      uint32_t mmin = s_mth[0];
+#pragma unroll
+      for (int w = 1; w < kTopkWarps; ++w) mmin = min(mmin, s_mth[w]);
+      float floor_v = fmaxf(list.tv, from_ordered_u32(max(s_floor, mmin)));
+      if (c0 == e0) {
+        // First chunk of the unit, list still empty: the k-th largest of the 32
+        // lane maxima (k distinct elements of the unit) bounds the unit's k-th
+        // value from below, so the warp starts filtering at once instead of
+        // inserting most of its first slice.
+        int ge = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ge += (__shfl_sync(0xFFFFFFFFu, mx, i) >= mx) ? 1 : 0;
+        float seed = (ge >= a.topk) ? mx : -INFINITY;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          seed = fmaxf(seed, __shfl_xor_sync(0xFFFFFFFFu, seed, off));
+        if (lane == 0 && seed > -INFINITY) atomicMax(&s_floor, ordered_u32(seed));
+        floor_v = fmaxf(floor_v, seed);
+      }
       if (!__any_sync(0xFFFFFFFFu, mx >= floor_v)) continue;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -221,27 +252,41 @@ __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_
         list.offer(x[j].w, idx + 3, in && x[j].w >= floor_v, lane, a.topk);
       }
       if (lane == 0 && list.ti != kNoIndex) atomicMax(&s_floor, ordered_u32(list.tv));
+      const float vm = __shfl_sync(0xFFFFFFFFu, list.lv, mth - 1);
+      const int im = __shfl_sync(0xFFFFFFFFu, list.li, mth - 1);
+      if (lane == 0 && im != kNoIndex) s_mth[warp] = ordered_u32(vm);
     }
-    // ---- merge the warps' lists
+    // ---- merge the warps' lists: candidate c = (warp c / k, slot c % k) goes to
+    // output slot rank(c), the number of candidates ahead of it (distinct ids)
     s_v[warp][lane] = list.lv;
     s_i[warp][lane] = list.li;
     named_bar_sync(kTopkBar, kTopkWarps * 32);
-    if (warp == 0 && !*abort_flag) {
-      for (int w = 1; w < kTopkWarps; ++w) {
-        const float v = s_v[w][lane];
-        const int vi = s_i[w][lane];
-        list.offer(v, vi, lane < a.topk && vi != kNoIndex, lane, a.topk);
-      }
-      if (lane < a.topk) {
-        if (a.pieces == 1) {
-          a.cand[static_cast<size_t>(row) * a.topk + lane] = list.li;
-          a.cval[static_cast<size_t>(row) * a.topk + lane] = list.lv;
-        } else {
-          a.part_i[static_cast<size_t>(unit) * a.topk + lane] = list.li;
-          a.part_v[static_cast<size_t>(unit) * a.topk + lane] = list.lv;
+    const int ncand = kTopkWarps * a.topk;
+    if (threadIdx.x < ncand && !*abort_flag) {
+      const int cw = threadIdx.x / a.topk, cs = threadIdx.x - cw * a.topk;
+      const float cv = s_v[cw][cs];
+      const int ci = s_i[cw][cs];
+      if (ci != kNoIndex) {
+        int rank = 0;
+        for (int w = 0; w < kTopkWarps; ++w) {
+          for (int j = 0; j < a.topk; ++j) {
+            const float v = s_v[w][j];
+            const int vi = s_i[w][j];
+            rank += (vi != kNoIndex && better(v, vi, cv, ci)) ? 1 : 0;
+          }
+        }
+        if (rank < a.topk) {
+          if (a.pieces == 1) {
+            a.cand[static_cast<size_t>(row) * a.topk + rank] = ci;
+            a.cval[static_cast<size_t>(row) * a.topk + rank] = cv;
+          } else {
+            a.part_i[static_cast<size_t>(unit) * a.topk + rank] = ci;
+            a.part_v[static_cast<size_t>(unit) * a.topk + rank] = cv;
+          }
         }
       }
     }
+    if (threadIdx.x < kTopkWarps) s_mth[threadIdx.x] = ordered_u32(-INFINITY);
     if (threadIdx.x == 0) s_floor = ordered_u32(-INFINITY);
     named_bar_sync(kTopkBar, kTopkWarps * 32);
   }
@@ -638,7 +683,7 @@ cudaError_t launch_topk(const float* U, int rows, int V, int topk, int32_t* cand
   if ((err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kTopkRingBytes))) != cudaSuccess)
     return err;
-  // three 66 KB rings per SM need the largest shared-memory carveout
+  // four 48 KB rings per SM need the largest shared-memory carveout
   if ((err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
     return err;
