@@ -684,10 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       // ---- arrive at the grid barrier (the wait comes after the speculative gather)
       if (etid == 0 && !fail) {
         const bool skip = (p.debug_skip_cta == cta) && (k == 0);
-        if (!skip) {
-          __threadfence();
-          red_release_gpu_add(p.bar, 1u);
-        }
+        // the release add orders every epilogue thread's partial and key writes
+        // (synchronised by the named barrier above) before the arrival
+        if (!skip) red_release_gpu_add(p.bar, 1u);
       }
 
       // ---- speculative gather for the next position: the winners are mostly final by
@@ -738,8 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
           }
         }
-        __threadfence();
-        trace_stamp(p, cta, k, 5);
+        trace_stamp(p, cta, k, 5);  // the acquire load above orders the reads that follow
       }
       const bool any = named_bar_or(kEpiBarrier, kEpiThreads, fail || bar_fail || *abort_flag);
       if (any) {
