@@ -66,7 +66,8 @@ namespace {
 constexpr int kTileV = kDraftTileV;              // 64 tokens per tile (MMA N)
 constexpr int kRows = kBatchChunk;               // 128 requests (MMA M)
 constexpr int kNumW2Stages = 2;
-constexpr int kNumUStages = 3;
+constexpr int kNumUStages = 3;                   // U ring slots of 32 KB (B > 64)
+constexpr int kNumUStagesSmall = 4;              // slots of 16 KB when B <= 64 (box <= 64 rows)
 constexpr int kNumAcc = 4;                       // TMEM accumulators, 64 columns each
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;      // 512
@@ -92,7 +93,7 @@ constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
 
 static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103 limit");
 static_assert((kNumAcc & (kNumAcc - 1)) == 0, "accumulator count must be a power of two");
-static_assert((2 * kNumW2Stages + 2 * kNumUStages + 2 * kNumAcc + 5) * 8 + 2 * kMaxK * 4 +
+static_assert((2 * kNumW2Stages + 2 * kNumUStagesSmall + 2 * kNumAcc + 5) * 8 + 2 * kMaxK * 4 +
                       kRows * 8 <=
                   kBarRegion,
               "barrier region too small");
@@ -133,14 +134,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
+// Small batches: with B <= 32 (64) requests, the 128 MMA rows hold 4 (2) copies
+// of the batch, row m serving request m mod rows_per_copy, so that the TMEM lane
+// quadrants of every epilogue warp hold real rows; the copies split the tiles.
+__device__ __forceinline__ int rows_per_copy(int B) { return B <= 32 ? 32 : (B <= 64 ? 64 : 128); }
+
 // Gather the step's Markov embeddings into the K-major, 128B-swizzled MMA
-// operand: row b = request, 64-element K chunk c at c * 16 KB, 8-row groups of
-// 1024 B, 16-byte unit u of row b stored at unit (u ^ (b & 7)).
-// Thread etid handles row etid / 4 and K chunk etid % 4.
+// operand: row b (request b mod rows_per_copy), 64-element K chunk c at
+// c * 16 KB, 8-row groups of 1024 B, 16-byte unit u of row b stored at unit
+// (u ^ (b & 7)).  Thread etid handles row etid / 4 and K chunk etid % 4.
 __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams& p, int k,
                                                   int etid, int32_t tok) {
   const int b = etid >> 2, c = etid & 3;
-  const bool live = b < p.B;
+  const int req = b & (rows_per_copy(p.B) - 1);
+  const bool live = req < p.B;
   uint4 vals[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
@@ -152,7 +159,7 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
     }
   }
   if (p.H != nullptr && live) {
-    const float* hrow = p.H + (static_cast<size_t>(b) * p.K + k) * p.r;
+    const float* hrow = p.H + (static_cast<size_t>(req) * p.K + k) * p.r;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int kel = c * 64 + u * 8;
@@ -220,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* w_full = bars;                          // [kNumW2Stages]
   uint64_t* w_empty = w_full + kNumW2Stages;        // [kNumW2Stages]
-  uint64_t* u_full = w_empty + kNumW2Stages;        // [kNumUStages]
-  uint64_t* u_empty = u_full + kNumUStages;         // [kNumUStages]
-  uint64_t* acc_full = u_empty + kNumUStages;       // [kNumAcc]
+  uint64_t* u_full = w_empty + kNumW2Stages;        // [kNumUStagesSmall]
+  uint64_t* u_empty = u_full + kNumUStagesSmall;    // [kNumUStagesSmall]
+  uint64_t* acc_full = u_empty + kNumUStagesSmall;  // [kNumAcc]
   uint64_t* acc_empty = acc_full + kNumAcc;         // [kNumAcc]
   uint64_t* a_full = acc_empty + kNumAcc;
   uint64_t* a_empty = a_full + 1;
@@ -240,19 +247,27 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   const int t_end = static_cast<int>(static_cast<int64_t>(cta + 1) * p.n_tiles / ncta);
   const int nt = t_end - t_begin;
   const int nkk = p.r / 16;
+  // Small batches use 4 U slots of 16 KB (a multiple of the batch copies, so every
+  // use of a slot -- and of an accumulator -- is read by the same copy and its
+  // warps see each mbarrier phase in order); larger ones 3 slots of 32 KB.
+  const int ncopy_all = kRows / rows_per_copy(p.B);
+  const int nus = ncopy_all > 1 ? kNumUStagesSmall : kNumUStages;
+  const uint32_t ubox = ncopy_all > 1 ? kUBoxBytes / 2 : kUBoxBytes;  // one 32-token box
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNumW2Stages; ++s) {
       mbar_init(&w_full[s], 1);
       mbar_init(&w_empty[s], 1);
     }
-    for (int s = 0; s < kNumUStages; ++s) {
+    // a tile is read (and released) by the epilogue warps of one copy of the batch
+    const uint32_t readers = static_cast<uint32_t>(kEpiWarps * rows_per_copy(p.B) / kRows);
+    for (int s = 0; s < nus; ++s) {
       mbar_init(&u_full[s], 1);
-      mbar_init(&u_empty[s], kEpiWarps);
+      mbar_init(&u_empty[s], readers);
     }
     for (int s = 0; s < kNumAcc; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], kEpiWarps);
+      mbar_init(&acc_empty[s], readers);
     }
     mbar_init(a_full, 1);
     mbar_init(a_empty, 1);
@@ -294,15 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             tma_load_2d(sW + s * kW2StageBytes, &args.tm_w2, v0, 0, &w_full[s], pol_w);
             w_issued = i + 1;
           }
-          const int su = i % kNumUStages;
-          if (!mbar_wait(&u_empty[su], ((i / kNumUStages) & 1) ^ 1, p.timeout_ns, abort_flag,
+          const int su = i % nus;
+          if (!mbar_wait(&u_empty[su], ((i / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
                          kBackoffControlNs)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&u_full[su], u_bytes);
-          tma_load_3d(sU + su * kUStageBytes, &args.tm_u, v0, k, 0, &u_full[su], pol_u);
-          tma_load_3d(sU + su * kUStageBytes + kUBoxBytes, &args.tm_u, v0 + 32, k, 0, &u_full[su],
+          tma_load_3d(sU + su * 2 * ubox, &args.tm_u, v0, k, 0, &u_full[su], pol_u);
+          tma_load_3d(sU + su * 2 * ubox + ubox, &args.tm_u, v0 + 32, k, 0, &u_full[su],
                       pol_u);
           u_issued = i + 1;
         }
@@ -314,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         // The last issue of each ring slot is the one in [issued - stages, issued).
         for (int i = w_issued - 1; i >= 0 && i >= w_issued - kNumW2Stages; --i)
           mbar_wait(&w_full[i % kNumW2Stages], (i / kNumW2Stages) & 1, p.timeout_ns, nullptr);
-        for (int i = u_issued - 1; i >= 0 && i >= u_issued - kNumUStages; --i)
-          mbar_wait(&u_full[i % kNumUStages], (i / kNumUStages) & 1, p.timeout_ns, nullptr);
+        for (int i = u_issued - 1; i >= 0 && i >= u_issued - nus; --i)
+          mbar_wait(&u_full[i % nus], (i / nus) & 1, p.timeout_ns, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -381,7 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     const int e = warp - 2;          // 0 .. 15
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int g = e >> 2;            // 16-token column group of the 64-token tile
-    const int b = q * 32 + lane;     // request row of this thread
+    const int rpc = rows_per_copy(p.B);
+    const int ncopy = kRows / rpc;   // copies of the batch in the MMA rows
+    const int b = (q * 32 + lane) & (rpc - 1);  // request of this thread's TMEM lane
+    const int copy = (q * 32) / rpc;  // its copy: it reads tiles i (global index) with
+                                      // i % ncopy == copy
     const int etid = threadIdx.x - 64;
     const bool row_ok = b < p.B;
     const uint32_t b_global = static_cast<uint32_t>(p.b_global0 + b);
@@ -392,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     uint32_t u_off[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      u_off[c] = (g >> 1) * kUBoxBytes + b * 128 + ((((g & 1) * 4 + c) ^ (b & 7)) << 4);
+      u_off[c] = (g >> 1) * ubox + b * 128 + ((((g & 1) * 4 + c) ^ (b & 7)) << 4);
     bool fail = false;
     bool aborted = false;
     int u_stage = 0;        // U ring slot of the next tile
@@ -404,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       // gathered speculatively before the previous grid barrier and are re-checked now
       if (etid == 0) trace_stamp(p, cta, k, 0);
       {
-        const int grow = etid >> 2;
+        const int grow = (etid >> 2) & (rpc - 1);  // request of this thread's gather row
         if (k == 0) {
           int32_t tok = 0;
           if (grow < p.B) {
@@ -444,24 +463,29 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       unsigned long long gkey = 0ull;  // global key of this request and step, as last read
       uint32_t nz[4] = {0u, 0u, 0u, 0u};  // Philox words of this thread's current tile pair
       unsigned long long kpre = 0ull;  // global key, read one tile ahead of its use
+      int tt = -1;                      // tiles of this step this thread has taken
+      int nz_pair = -1;                 // tile pair whose Philox words nz holds
       for (int t = 0; t < nt && !fail; ++t) {
-        if (MODE == kModeSample && row_ok) {
-          // every other tile, refresh the bound with the key read a tile earlier, so
-          // the load's latency is covered by a whole tile's work
-          if (t > 0 && (t & (kBoundRefresh - 1)) == 0 && key_epoch(kpre) == p.epoch &&
-              kpre > gkey)
-            gkey = kpre;
-          if (((t + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
-        }
         const int i = k * nt + t;
         const int buf = i & (kNumAcc - 1);
-        bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
-        ok = ok && mbar_wait(&u_full[u_stage], u_phase, p.timeout_ns, abort_flag);
         const int su = u_stage;
-        if (++u_stage == kNumUStages) {
+        const uint32_t uph = u_phase;
+        if (++u_stage == nus) {
           u_stage = 0;
           u_phase ^= 1u;
         }
+        if (ncopy > 1 && i % ncopy != copy) continue;  // another copy's tile
+        ++tt;
+        if (MODE == kModeSample && row_ok) {
+          // every other tile, refresh the bound with the key read a tile earlier, so
+          // the load's latency is covered by a whole tile's work
+          if (tt > 0 && (tt & (kBoundRefresh - 1)) == 0 && key_epoch(kpre) == p.epoch &&
+              kpre > gkey)
+            gkey = kpre;
+          if (((tt + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
+        }
+        bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
+        ok = ok && mbar_wait(&u_full[su], uph, p.timeout_ns, abort_flag);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
           fail = true;
@@ -469,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           break;
         }
         tc_fence_after();
-        if (t == 0 && etid == 0) trace_stamp(p, cta, k, 2);
+        if (tt == 0 && etid == 0) trace_stamp(p, cta, k, 2);
         uint32_t acc[16];
         if (nkk > 0) {
           tmem_ld_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -482,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         float uval[16];
         {
-          const uint8_t* ubase = sU + su * kUStageBytes;
+          const uint8_t* ubase = sU + su * 2 * ubox;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float4 x = *reinterpret_cast<const float4*>(ubase + u_off[c]);
@@ -563,9 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         if (MODE == kModeSample) {
           const int tile = t_begin + t;
-          if (t == 0 || (tile & 1) == 0)
+          if ((tile >> 1) != nz_pair) {
+            nz_pair = tile >> 1;
             philox4x32_10_rk(static_cast<uint32_t>(tile >> 1), static_cast<uint32_t>(k), b_global,
                              1u + static_cast<uint32_t>(g), p.round_key0, p.round_key1, nz);
+          }
           const uint32_t word1 = (tile & 1) ? nz[2] : nz[0];
           const uint32_t word2 = (tile & 1) ? nz[3] : nz[1];
           // stage 1: the block's race score (log2 units)
@@ -601,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               atomicMax(&s_bound[b], key);
             }
           }
-          if ((t & 1) == 1 && g == 0) {
+          if ((tt & 1) == 1 && g == 0) {
             // share this CTA's best with the other CTAs (rate-limited)
             const unsigned long long mine = s_bound[b];
             if (mine > gkey) {
@@ -624,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             lb *= inv_scale2;
             atomicMax(&s_bound[b], make_key(p.epoch, yb, vb));
           }
-          if ((t & 1) == 1 && g == 0) {
+          if ((tt & 1) == 1 && g == 0) {
             // publish this CTA's best so far (lets other CTAs gather the next
             // position's embeddings speculatively before the grid barrier)
             const unsigned long long mine = s_bound[b];
@@ -636,29 +662,37 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
       }
 
-      // ---- merge the four column groups of each request, publish the CTA's partial
+      // ---- merge the column groups (and copies) of each request, publish the CTA's
+      // partial; record slot sl = copy * 4 + g, rpc rows per record field
       if (etid == 0) trace_stamp(p, cta, k, 3);
       const float score = yb;
+      const int slot = copy * 4 + g;
+      // the merge records live in the operand's memory: with several copies a warp can
+      // get here while the MMAs of other copies' last tiles still read it
+      if (!fail && !mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag)) {
+        fail = true;
+        *abort_flag = 1;
+      }
       if (!fail) {
-        merge[(g * 5 + 0) * kRows + b] = m2;
-        merge[(g * 5 + 1) * kRows + b] = sum;
-        merge[(g * 5 + 2) * kRows + b] = score;
-        merge[(g * 5 + 3) * kRows + b] = __int_as_float(vb);
-        merge[(g * 5 + 4) * kRows + b] = lb;
+        merge[(slot * 5 + 0) * rpc + b] = m2;
+        merge[(slot * 5 + 1) * rpc + b] = sum;
+        merge[(slot * 5 + 2) * rpc + b] = score;
+        merge[(slot * 5 + 3) * rpc + b] = __int_as_float(vb);
+        merge[(slot * 5 + 4) * rpc + b] = lb;
       }
       named_bar_sync(kEpiBarrier, kEpiThreads);
-      if (!fail && g == 0 && row_ok) {
-        float M = merge[0 * kRows + b], S = merge[1 * kRows + b];
-        float best_s = merge[2 * kRows + b], best_l = merge[4 * kRows + b];
-        int best_v = __float_as_int(merge[3 * kRows + b]);
-        for (int gg = 1; gg < 4; ++gg) {
-          lse_merge(M, S, merge[(gg * 5 + 0) * kRows + b], merge[(gg * 5 + 1) * kRows + b]);
-          const float s2 = merge[(gg * 5 + 2) * kRows + b];
-          const int v2 = __float_as_int(merge[(gg * 5 + 3) * kRows + b]);
+      if (!fail && slot == 0 && row_ok) {
+        float M = merge[0 * rpc + b], S = merge[1 * rpc + b];
+        float best_s = merge[2 * rpc + b], best_l = merge[4 * rpc + b];
+        int best_v = __float_as_int(merge[3 * rpc + b]);
+        for (int ss = 1; ss < 4 * ncopy; ++ss) {
+          lse_merge(M, S, merge[(ss * 5 + 0) * rpc + b], merge[(ss * 5 + 1) * rpc + b]);
+          const float s2 = merge[(ss * 5 + 2) * rpc + b];
+          const int v2 = __float_as_int(merge[(ss * 5 + 3) * rpc + b]);
           if (v2 != 0x7FFFFFFF && (s2 > best_s || (s2 == best_s && v2 < best_v))) {
             best_s = s2;
             best_v = v2;
-            best_l = merge[(gg * 5 + 4) * kRows + b];
+            best_l = merge[(ss * 5 + 4) * rpc + b];
           }
         }
         unsigned long long key = 0ull;
@@ -696,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           fail = true;
           *abort_flag = 1;
         } else {
-          const int grow = etid >> 2;
+          const int grow = (etid >> 2) & (rpc - 1);
           int32_t tok = 0;
           if (grow < p.B) {
             if (MODE == kModeTeacherForced) {
