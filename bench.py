@@ -387,7 +387,8 @@ def run_ours(args, rank, world, local):
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
-                "kernel": "draft_kernel" if cfg != 4 else "topk_kernel + pair_scores + walk",
+                "kernel": "draft_kernel" if cfg != 4 else
+                "selector step (top-k scan, gate, pair scores, walk)",
                 "median_launch_us": round(kernel_ms * 1000, 2)}
 
     # -------- end to end through the binding with host buffers
