@@ -182,6 +182,38 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
   }
 }
 
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Asynchronous form of gather_embeddings without a gate: the thread's 128-byte
+// piece of W1[tok] goes to the operand by 16-byte cp.async copies (rows of no
+// request and K chunks past r are zeroed with plain stores).
+__device__ __forceinline__ void copy_embedding_async(uint8_t* sA, const DraftParams& p, int etid,
+                                                     int32_t tok) {
+  const int b = etid >> 2, c = etid & 3;
+  const int req = b & (rows_per_copy(p.B) - 1);
+  const bool live = req < p.B;
+  uint8_t* base = sA + c * 16384 + (b >> 3) * 1024 + (b & 7) * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int kel = c * 64 + u * 8;
+    uint8_t* dst = base + ((u ^ (b & 7)) << 4);
+    if (live && kel < p.r) {
+      cp_async_16(dst, p.W1 + static_cast<size_t>(tok) * p.r + kel);
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // Score of a key (the ordered float in its middle bits); -inf for "no key".
 __device__ __forceinline__ float key_score(unsigned long long key) {
   if (key == 0ull) return -INFINITY;
@@ -215,7 +247,7 @@ __device__ __forceinline__ void lse_merge(float& ma, float& sa, float mb, float 
   }
 }
 
-template <int MODE>
+template <int MODE, bool COPIES>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
   extern __shared__ uint8_t smem_raw[];
@@ -250,9 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   // Small batches use 4 U slots of 16 KB (a multiple of the batch copies, so every
   // use of a slot -- and of an accumulator -- is read by the same copy and its
   // warps see each mbarrier phase in order); larger ones 3 slots of 32 KB.
-  const int ncopy_all = kRows / rows_per_copy(p.B);
-  const int nus = ncopy_all > 1 ? kNumUStagesSmall : kNumUStages;
-  const uint32_t ubox = ncopy_all > 1 ? kUBoxBytes / 2 : kUBoxBytes;  // one 32-token box
+  // (COPIES: B <= 64; the B > 64 instantiation keeps these compile-time constants)
+  const int nus = COPIES ? kNumUStagesSmall : kNumUStages;
+  const uint32_t ubox = COPIES ? kUBoxBytes / 2 : kUBoxBytes;  // one 32-token box
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNumW2Stages; ++s) {
@@ -260,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       mbar_init(&w_empty[s], 1);
     }
     // a tile is read (and released) by the epilogue warps of one copy of the batch
-    const uint32_t readers = static_cast<uint32_t>(kEpiWarps * rows_per_copy(p.B) / kRows);
+    const uint32_t readers =
+        COPIES ? static_cast<uint32_t>(kEpiWarps * rows_per_copy(p.B) / kRows) : kEpiWarps;
     for (int s = 0; s < nus; ++s) {
       mbar_init(&u_full[s], 1);
       mbar_init(&u_empty[s], readers);
@@ -396,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     const int e = warp - 2;          // 0 .. 15
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int g = e >> 2;            // 16-token column group of the 64-token tile
-    const int rpc = rows_per_copy(p.B);
-    const int ncopy = kRows / rpc;   // copies of the batch in the MMA rows
+    const int rpc = COPIES ? rows_per_copy(p.B) : kRows;
+    const int ncopy = COPIES ? kRows / rpc : 1;  // copies of the batch in the MMA rows
     const int b = (q * 32 + lane) & (rpc - 1);  // request of this thread's TMEM lane
     const int copy = (q * 32) / rpc;  // its copy: it reads tiles i (global index) with
                                       // i % ncopy == copy
@@ -436,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
           if (!fail) gather_embeddings(sA, p, 0, etid, tok);
         } else if (MODE != kModeTeacherForced && grow < p.B) {
+          cp_async_wait_all();  // the speculative copy must land before any rewrite
           const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + grow);
           if (key != spec_key) {  // the winner changed after the speculative gather
             int32_t tok = key_token(key);
@@ -447,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
         }
         if (etid < kRows) s_bound[etid] = 0ull;
+        cp_async_wait_all();
       }
       fence_proxy_async_smem();
       named_bar_sync(kEpiBarrier, kEpiThreads);
@@ -474,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           u_stage = 0;
           u_phase ^= 1u;
         }
-        if (ncopy > 1 && i % ncopy != copy) continue;  // another copy's tile
+        if (COPIES && (i & (ncopy - 1)) != copy) continue;  // another copy's tile
         ++tt;
         if (MODE == kModeSample && row_ok) {
           // every other tile, refresh the bound with the key read a tile earlier, so
@@ -723,8 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (!skip) red_release_gpu_add(p.bar, 1u);
       }
 
-      // ---- speculative gather for the next position: the winners are mostly final by
-      // now (eager publication), so fetch their embeddings while other CTAs finish
+      if (etid == 0) trace_stamp(p, cta, k, 7);
+      // ---- speculative gather for the next position: the likely winner is the better
+      // of the global key (read before the merge) and this CTA's best (complete now);
+      // without a gate its row is copied asynchronously and lands while the grid
+      // barrier completes
       if (k + 1 < p.K && !fail) {
         if (!mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag)) {  // MMAs done reading E
           fail = true;
@@ -740,7 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                 tok = 0;
               }
             } else {
-              spec_key = __ldcg(p.keys + k * kRows + grow);
+              const unsigned long long gk = __ldcg(p.keys + k * kRows + grow);
+              const unsigned long long lk = s_bound[grow];
+              spec_key = (key_epoch(gk) == p.epoch && gk > lk) ? gk : lk;
               tok = key_token(spec_key);
               if (key_epoch(spec_key) != p.epoch || tok < 0 || tok >= p.V) {
                 spec_key = ~0ull;  // never matches: refetched after the barrier
@@ -748,7 +788,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               }
             }
           }
-          gather_embeddings(sA, p, k + 1, etid, tok);
+          if (p.H == nullptr) {
+            copy_embedding_async(sA, p, etid, tok);
+          } else {
+            gather_embeddings(sA, p, k + 1, etid, tok);
+          }
         }
       }
 
@@ -881,11 +925,19 @@ int draft_threads() { return kThreads; }
 
 cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream) {
   const void* fn = nullptr;
+  const bool copies = args.p.B <= 64;  // small batches fill the MMA rows with copies
   switch (mode) {
-    case kModeSample: fn = reinterpret_cast<const void*>(&draft_kernel<kModeSample>); break;
-    case kModeGreedy: fn = reinterpret_cast<const void*>(&draft_kernel<kModeGreedy>); break;
+    case kModeSample:
+      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeSample, true>)
+                  : reinterpret_cast<const void*>(&draft_kernel<kModeSample, false>);
+      break;
+    case kModeGreedy:
+      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeGreedy, true>)
+                  : reinterpret_cast<const void*>(&draft_kernel<kModeGreedy, false>);
+      break;
     case kModeTeacherForced:
-      fn = reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced>);
+      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, true>)
+                  : reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, false>);
       break;
     default: return cudaErrorInvalidValue;
   }
