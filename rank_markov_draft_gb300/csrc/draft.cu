@@ -182,16 +182,6 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
   }
 }
 
-__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
-               "l"(reinterpret_cast<uint64_t>(src))
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Asynchronous form of gather_embeddings without a gate: the thread's 128-byte
 // piece of W1[tok] goes to the operand by 16-byte cp.async copies (rows of no
 // request and K chunks past r are zeroed with plain stores).
@@ -211,7 +201,7 @@ __device__ __forceinline__ void copy_embedding_async(uint8_t* sA, const DraftPar
       *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  cp_async_commit();
 }
 
 // Score of a key (the ordered float in its middle bits); -inf for "no key".

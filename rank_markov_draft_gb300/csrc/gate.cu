@@ -161,13 +161,26 @@ __global__ void __launch_bounds__(kThreads, 1) gate_gemm_kernel(const __grid_con
   }
 }
 
-__global__ void gate_finalize_kernel(const float* __restrict__ partial, int splits, int64_t n,
-                                     float* __restrict__ H) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+// H = sigmoid(sum over splits, in split order); n4 float4 per split, all of a
+// thread's split loads in flight before the sum.
+__global__ void gate_finalize_kernel(const float4* __restrict__ partial, int splits, int64_t n4,
+                                     float4* __restrict__ H) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float z = 0.f;
-    for (int s = 0; s < splits; ++s) z += partial[s * n + i];
-    H[i] = 1.0f / (1.0f + expf(-z));
+    float4 pv[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      pv[s] = (s < splits) ? __ldcs(partial + s * n4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 z = pv[0];
+#pragma unroll
+    for (int s = 1; s < 8; ++s) {
+      z.x += pv[s].x;
+      z.y += pv[s].y;
+      z.z += pv[s].z;
+      z.w += pv[s].w;
+    }
+    H[i] = make_float4(1.0f / (1.0f + expf(-z.x)), 1.0f / (1.0f + expf(-z.y)),
+                       1.0f / (1.0f + expf(-z.z)), 1.0f / (1.0f + expf(-z.w)));
   }
 }
 
@@ -185,9 +198,12 @@ cudaError_t launch_gate_gemm(const GateArgs& args, cudaStream_t stream) {
 
 cudaError_t launch_gate_finalize(const float* partial, int splits, int64_t n, float* H,
                                  cudaStream_t stream) {
-  int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096));
+  // n = M * r is a multiple of 64 (r % 64 == 0) and splits <= 8
+  const int64_t n4 = n / 4;
+  int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 4096));
   if (blocks < 1) blocks = 1;
-  gate_finalize_kernel<<<blocks, 256, 0, stream>>>(partial, splits, n, H);
+  gate_finalize_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(partial), splits,
+                                                   n4, reinterpret_cast<float4*>(H));
   return cudaGetLastError();
 }
 

@@ -495,19 +495,22 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(
   }
 }
 
-constexpr int kWalkWarps = 16;
+constexpr int kWalkWarps = 8;
 constexpr int kWalkWindowBytes = 32768;  // score tables staged per window
 
-// One CTA per request.  Per window of positions, all warps stage the k x k
-// score tables and the candidates' noise (it depends on the candidate's block
-// of token ids, not on the path) in shared memory; warp 0 then walks the
-// window: at each position it selects the row of the previous pick and draws
-// with the head's block race over the candidates (the candidates of one
-// 16-token block race as one block with their summed mass, then the inverse
-// CDF in token order inside the winning block; tokens outside the candidate
-// set have no mass), and takes the log-softmax over the k candidates.
-// After the walk, the confidence head runs for all positions at once (one
-// warp per position) and thread 0 forms the survival products.
+// One CTA per request.  The draw at position t depends on the path only through
+// the predecessor slot i (the row S_t(i, .)); the candidates' noise depends on
+// their blocks of token ids, not on the path.  So, per window of positions:
+//   1. the k x k score tables and, per candidate, its token, its block's
+//      -ln E, its block's stage-2 uniform and the mask of candidates sharing its
+//      16-token block are staged in shared memory (one warp per position);
+//   2. every thread draws for one (position, predecessor slot) pair at a time --
+//      the head's block race restricted to the candidates: candidates of one
+//      block race with their summed mass, then the inverse CDF in token order --
+//      and records the chosen slot and its log-softmax over the k candidates;
+//   3. thread 0 follows the chain slot_{t+1} = next(t, slot_t).
+// After the walk, the confidence head runs for all positions at once (one warp
+// per position) and thread 0 forms the survival products.
 __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(
     const int32_t* __restrict__ cand, const float* __restrict__ S,
     const int32_t* __restrict__ anchors, const uint16_t* __restrict__ A, int B, int K, int V,
@@ -515,124 +518,138 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(
     int32_t* __restrict__ tokens, float* __restrict__ logprobs, dspark_conf_args conf,
     int conf_on, int* status) {
   extern __shared__ __align__(16) float walk_smem[];
-  float* s_S = walk_smem;                          // [window][topk][topk]
-  float* s_L = s_S + window * topk * topk;         // [window][32] -ln E of the block race
-  float* s_U2 = s_L + window * 32;                 // [window][32] stage-2 uniform
-  int* s_C = reinterpret_cast<int*>(s_U2 + window * 32);  // [window][32] candidates
+  const int tile = topk * topk;
+  float* s_S = walk_smem;                                   // [window][topk][topk]
+  float* s_L = s_S + window * tile;                         // [window][32] -ln E of the block
+  float* s_U2 = s_L + window * 32;                          // [window][32] stage-2 uniform
+  int* s_C = reinterpret_cast<int*>(s_U2 + window * 32);    // [window][32] candidate token
+  uint32_t* s_M = reinterpret_cast<uint32_t*>(s_C + window * 32);  // [window][32] block mates
+  int* s_next = reinterpret_cast<int*>(s_M + window * 32);  // [window][32] slot drawn from row i
+  float* s_lp = reinterpret_cast<float*>(s_next + window * 32);  // [window][32] its logprob
   __shared__ int s_tok[kMaxK];
   __shared__ float s_conf[kMaxK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;
-  const int tile = topk * topk;
   int slot = 0;
   for (int t0 = 0; t0 < K; t0 += window) {
     const int nt = min(window, K - t0);
     const size_t base = (static_cast<size_t>(b) * K + t0) * tile;
-    for (int e = threadIdx.x; e < nt * tile; e += blockDim.x) s_S[e] = __ldg(S + base + e);
+    // the window's score tables: 16-byte asynchronous copies, all in flight at once
+    // (nt * topk^2 floats; topk^2 is a multiple of 4 except for odd topk)
+    if ((tile & 3) == 0 && (reinterpret_cast<uintptr_t>(S) & 15u) == 0) {
+      for (int e = threadIdx.x * 4; e < nt * tile; e += blockDim.x * 4)
+        cp_async_16(s_S + e, S + base + e);
+      cp_async_commit();
+    } else {
+      for (int e = threadIdx.x; e < nt * tile; e += blockDim.x) s_S[e] = __ldg(S + base + e);
+    }
     for (int w = warp; w < nt; w += kWalkWarps) {
       const int t = t0 + w;
       const size_t bt = static_cast<size_t>(b) * K + t;
-      const int c = lane < topk ? __ldg(cand + bt * topk + lane) : 0x7FFFFFFF;
+      const bool live = lane < topk;
+      const int c = live ? __ldg(cand + bt * topk + lane) : 0x7FFFFFFF;
+      const int blk = live ? (c >> 4) : -1 - lane;  // distinct for dead lanes
       float lnE = 0.f, u2 = 0.f;
-      if (sample && lane < topk) {
-        const uint32_t blk = static_cast<uint32_t>(c) >> 4;
-        const Philox4 rnd = philox4x32_10(blk >> 3, static_cast<uint32_t>(t),
-                                          static_cast<uint32_t>(b), 1u + (blk & 3u), seed_lo,
+      if (sample && live) {
+        const uint32_t ub = static_cast<uint32_t>(blk);
+        const Philox4 rnd = philox4x32_10(ub >> 3, static_cast<uint32_t>(t),
+                                          static_cast<uint32_t>(b), 1u + (ub & 3u), seed_lo,
                                           seed_hi);
-        const int h = (blk >> 2) & 1u;
+        const int h = (ub >> 2) & 1u;
         lnE = -logf(neg_log_uniform_accurate(philox_uniform(h ? rnd.w[2] : rnd.w[0])));
         u2 = philox_uniform(h ? rnd.w[3] : rnd.w[1]);
       }
       s_L[w * 32 + lane] = lnE;
       s_U2[w * 32 + lane] = u2;
       s_C[w * 32 + lane] = c;
+      s_M[w * 32 + lane] = __match_any_sync(0xFFFFFFFFu, blk) & (live ? 0xFFFFFFFFu : 0u);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // every (position, predecessor slot) draw of the window
+    for (int d = threadIdx.x; d < nt * topk; d += blockDim.x) {
+      const int w = d / topk, i = d - w * topk;
+      const float* row = s_S + (w * topk + i) * topk;
+      const float* L = s_L + w * 32;
+      const int* C = s_C + w * 32;
+      const uint32_t* M = s_M + w * 32;
+      float m = -INFINITY;
+      for (int j = 0; j < topk; ++j) m = fmaxf(m, row[j] * inv_t);
+      float tot = 0.f;
+      for (int j = 0; j < topk; ++j) tot += expf(row[j] * inv_t - m);
+      int pick = 0;
+      if (!sample) {
+        // greedy: argmax by (score desc, token id asc)
+        float bz = row[0] * inv_t;
+        for (int j = 1; j < topk; ++j) {
+          const float z = row[j] * inv_t;
+          if (z > bz || (z == bz && C[j] < C[pick])) {
+            bz = z;
+            pick = j;
+          }
+        }
+      } else {
+        // stage 1: each block (represented by its lowest slot) races with its mass
+        float best = -INFINITY, bestZ = 0.f;
+        int bestj = 0;
+        for (int j = 0; j < topk; ++j) {
+          const uint32_t mates = M[j];
+          if ((__ffs(mates) - 1) != j) continue;  // not the block's first slot
+          float Z = 0.f;
+          for (uint32_t mm = mates; mm != 0u; mm &= mm - 1u) {
+            const int jj = __ffs(mm) - 1;
+            Z += expf(row[jj] * inv_t - m);
+          }
+          const float sc = (Z > 0.f) ? logf(Z) + L[j] : -INFINITY;
+          if (sc > best || (sc == best && (C[j] >> 4) < (C[bestj] >> 4))) {
+            best = sc;
+            bestZ = Z;
+            bestj = j;
+          }
+        }
+        // stage 2: inverse CDF over the block's candidates in token order
+        const float target = s_U2[w * 32 + bestj] * bestZ;
+        uint32_t left = M[bestj];
+        float Cum = 0.f;
+        int last = bestj;
+        pick = -1;
+        while (left != 0u) {
+          int jmin = __ffs(left) - 1;
+          for (uint32_t mm = left & (left - 1u); mm != 0u; mm &= mm - 1u) {
+            const int jj = __ffs(mm) - 1;
+            if (C[jj] < C[jmin]) jmin = jj;
+          }
+          left &= ~(1u << jmin);
+          const float e = expf(row[jmin] * inv_t - m);
+          if (e > 0.f) {
+            Cum += e;
+            last = jmin;
+            if (target < Cum) {
+              pick = jmin;
+              break;
+            }
+          }
+        }
+        if (pick < 0) pick = last;  // target at the very top (rounding): the last live one
+      }
+      s_next[w * 32 + i] = pick;
+      s_lp[w * 32 + i] = row[pick] * inv_t - (m + logf(tot));
     }
     __syncthreads();
-    if (warp == 0) {
-      const bool live = lane < topk;
+    if (threadIdx.x == 0) {
       for (int w = 0; w < nt; ++w) {
         const int t = t0 + w;
         const size_t bt = static_cast<size_t>(b) * K + t;
-        const float z = live ? s_S[(w * topk + slot) * topk + lane] * inv_t : -INFINITY;
-        const int c = s_C[w * 32 + lane];
-        float m = z;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-        const float e = live ? expf(z - m) : 0.f;
-        int best_c, best_j;
-        if (sample) {
-          // stage 1: the mass of this candidate's block (candidates of the same block)
-          const int blk = live ? (c >> 4) : -1;
-          float Z = 0.f;
-          for (int i = 0; i < topk; ++i) {
-            const int bi = __shfl_sync(0xFFFFFFFFu, blk, i);
-            const float ei = __shfl_sync(0xFFFFFFFFu, e, i);
-            if (bi == blk) Z += ei;
-          }
-          float bs = (live && Z > 0.f) ? logf(Z) + s_L[w * 32 + lane] : -INFINITY;
-          int bb = live ? blk : 0x7FFFFFFF;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
-            const int ob = __shfl_xor_sync(0xFFFFFFFFu, bb, off);
-            if (os > bs || (os == bs && ob < bb)) {
-              bs = os;
-              bb = ob;
-            }
-          }
-          // stage 2: inverse CDF in token order inside the winning block
-          const bool inb = live && blk == bb;
-          float C = 0.f;
-          for (int i = 0; i < topk; ++i) {
-            const int bi = __shfl_sync(0xFFFFFFFFu, blk, i);
-            const int ci = __shfl_sync(0xFFFFFFFFu, c, i);
-            const float ei = __shfl_sync(0xFFFFFFFFu, e, i);
-            if (bi == bb && ci <= c) C += ei;
-          }
-          const int src = __ffs(__ballot_sync(0xFFFFFFFFu, inb)) - 1;
-          const float Zb = __shfl_sync(0xFFFFFFFFu, Z, src);
-          const float target = s_U2[w * 32 + src] * Zb;
-          // smallest crossing token, else the largest live token of the block
-          int pick = (inb && e > 0.f && target < C) ? c : 0x7FFFFFFF;
-          int last = (inb && e > 0.f) ? c : -1;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            pick = min(pick, __shfl_xor_sync(0xFFFFFFFFu, pick, off));
-            last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, off));
-          }
-          best_c = (pick != 0x7FFFFFFF) ? pick : last;
-          best_j = __ffs(__ballot_sync(0xFFFFFFFFu, live && c == best_c)) - 1;
-        } else {
-          // greedy: argmax by (score desc, token id asc)
-          float best_s = z;
-          best_c = c;
-          best_j = lane;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            const float os = __shfl_xor_sync(0xFFFFFFFFu, best_s, off);
-            const int oc = __shfl_xor_sync(0xFFFFFFFFu, best_c, off);
-            const int oj = __shfl_xor_sync(0xFFFFFFFFu, best_j, off);
-            if (better(os, oc, best_s, best_c)) {
-              best_s = os;
-              best_c = oc;
-              best_j = oj;
-            }
-          }
+        const int j = s_next[w * 32 + slot];
+        int c = s_C[w * 32 + j];
+        if (c < 0 || c >= V) {
+          record_error(status, kStatusDeviceOob);
+          c = 0;
         }
-        float ex = e;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ex += __shfl_xor_sync(0xFFFFFFFFu, ex, off);
-        const float zw = __shfl_sync(0xFFFFFFFFu, z, best_j);
-        if (best_c < 0 || best_c >= V) {
-          if (lane == 0) record_error(status, kStatusDeviceOob);
-          best_c = 0;
-        }
-        if (lane == 0) {
-          tokens[bt] = best_c;
-          logprobs[bt] = zw - (m + logf(ex));
-          s_tok[t] = best_c;
-        }
-        slot = best_j;
+        tokens[bt] = c;
+        logprobs[bt] = s_lp[w * 32 + slot];
+        s_tok[t] = c;
+        slot = j;
       }
     }
     __syncthreads();
@@ -756,7 +773,7 @@ cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anch
   if (conf != nullptr) c = *conf;
   const int tile_bytes = topk * topk * 4;
   const int window = max(1, min(K, kWalkWindowBytes / tile_bytes));
-  const size_t smem = static_cast<size_t>(window) * (tile_bytes + 3 * 32 * 4);
+  const size_t smem = static_cast<size_t>(window) * (tile_bytes + 6 * 32 * 4);
   cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(&walk_kernel),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
