@@ -59,6 +59,11 @@ def _bind(lib):
     lib.orc_block_uniform.restype = f64
     lib.orc_within_uniform.argtypes = [u64, u32, u32, u32]
     lib.orc_within_uniform.restype = f64
+    lib.orc_accept_uniform.argtypes = [u64, u32, u32]
+    lib.orc_accept_uniform.restype = f64
+    lib.orc_verify.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, f64, f64, u64, i32,
+                               i32, P, P, P, P]
+    lib.orc_verify.restype = i32
     lib.orc_gate.argtypes = [P, P, i64, i32, i32, P]
     lib.orc_markov_draft.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, u64, i32, i32,
                                      P, P, P, P, P]
@@ -116,6 +121,39 @@ class Oracle:
     def within_uniform(self, seed: int, b: int, k: int, blk: int) -> float:
         """Stage-2 uniform of 16-token block `blk` (request b, position k)."""
         return float(self._lib.orc_within_uniform(seed, b, k, blk))
+
+    def accept_uniform(self, seed: int, b: int, k: int) -> float:
+        """The verifier's acceptance uniform of position k of request b."""
+        return float(self._lib.orc_accept_uniform(seed, b, k))
+
+    def verify(self, P, U, W1, W2, anchors, tokens, *, draft_temperature: float,
+               target_temperature: float, seed: int, ell=None, H=None, b0: int = 0,
+               nb: Optional[int] = None) -> dict:
+        """Speculative verification of drafted tokens [B, K] against target logits
+        P [B, K+1, V]: accepted prefix length and the next token per request."""
+        P = _c(P, np.float32)
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        assert P.shape == (B, K + 1, V)
+        r = 0 if W1 is None else W1.shape[1]
+        W1 = _c(W1, np.uint16) if r > 0 else np.zeros((V, 1), np.uint16)
+        W2 = _c(W2, np.uint16) if r > 0 else np.zeros((1, V), np.uint16)
+        anchors = _c(anchors, np.int32)
+        tokens = _c(tokens, np.int32)
+        ell = _c(ell, np.int32)
+        H = _c(H, np.float64)
+        nb = B - b0 if nb is None else nb
+        n_acc = np.zeros(nb, np.int32)
+        nxt = np.zeros(nb, np.int32)
+        accept_prob = np.zeros((nb, K), np.float64)
+        margins = np.zeros(nb, np.float64)
+        rc = self._lib.orc_verify(_ptr(P), _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), _ptr(H),
+                                  _ptr(tokens), _ptr(ell), B, K, V, r, float(draft_temperature),
+                                  float(target_temperature), seed, b0, nb, _ptr(n_acc), _ptr(nxt),
+                                  _ptr(accept_prob), _ptr(margins))
+        if rc != 0:
+            raise ValueError("oracle verify rejected its arguments")
+        return dict(n_acc=n_acc, next_token=nxt, accept_prob=accept_prob, margins=margins)
 
     def gate(self, h: np.ndarray, Wg: np.ndarray) -> np.ndarray:
         """H = sigmoid(h . Wg) in fp64; h [..., d] bf16 bits, Wg [d, r] bf16 bits -> [..., r]."""

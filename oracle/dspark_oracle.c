@@ -139,14 +139,30 @@ double orc_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t v, uint32_t t
   return orc_uniform_ctr(seed, v >> 2, k, b, tag, v & 3u);
 }
 
-/* Stage-1 uniform of block `blk` (request b, position k). */
-double orc_block_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk) {
-  return orc_uniform_ctr(seed, blk >> 3, k, b, 1u + (blk & 3u), 2u * ((blk >> 2) & 1u));
+/* Stage-1 / stage-2 uniforms of block `blk` (request b, position k) on the race
+   streams starting at tag `tag0` (1: the draft; 9: the verifier's resample). */
+static double race_u1(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk, uint32_t tag0) {
+  return orc_uniform_ctr(seed, blk >> 3, k, b, tag0 + (blk & 3u), 2u * ((blk >> 2) & 1u));
 }
 
-/* Stage-2 uniform of block `blk` (request b, position k). */
+static double race_u2(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk, uint32_t tag0) {
+  return orc_uniform_ctr(seed, blk >> 3, k, b, tag0 + (blk & 3u), 2u * ((blk >> 2) & 1u) + 1u);
+}
+
+/* Stage-1 uniform of block `blk` (request b, position k) of the draft. */
+double orc_block_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk) {
+  return race_u1(seed, b, k, blk, 1u);
+}
+
+/* Stage-2 uniform of block `blk` (request b, position k) of the draft. */
 double orc_within_uniform(uint64_t seed, uint32_t b, uint32_t k, uint32_t blk) {
-  return orc_uniform_ctr(seed, blk >> 3, k, b, 1u + (blk & 3u), 2u * ((blk >> 2) & 1u) + 1u);
+  return race_u2(seed, b, k, blk, 1u);
+}
+
+/* The verifier's acceptance uniform of position k of request b:
+   counter (k, 0, b, 13), word 0. */
+double orc_accept_uniform(uint64_t seed, uint32_t b, uint32_t k) {
+  return orc_uniform_ctr(seed, k, 0u, b, 13u, 0u);
 }
 
 
@@ -234,7 +250,7 @@ static double log_sum_exp_scaled(const double* l, int V, double Tp) {
 /* relative to Z (either is the relative error that would flip it).     */
 /* ------------------------------------------------------------------ */
 static int block_race_draw(const int32_t* ids, const double* z, double* w, int n, uint64_t seed,
-                           uint32_t b, uint32_t k, double* margin) {
+                           uint32_t b, uint32_t k, uint32_t tag0, double* margin) {
   double m = -INFINITY;
   for (int i = 0; i < n; ++i)
     if (z[i] > m) m = z[i];
@@ -251,7 +267,7 @@ static int block_race_draw(const int32_t* ids, const double* z, double* w, int n
     int j = i;
     while (j < n && ((uint32_t)(ids ? ids[j] : j) >> 4) == blk) Z += w[j++];
     if (Z > 0.0) {
-      const double E = -log(orc_block_uniform(seed, b, k, blk));
+      const double E = -log(race_u1(seed, b, k, blk, tag0));
       const double score = log(Z) - log(E);
       if (score > best) {
         second = best;
@@ -267,7 +283,7 @@ static int block_race_draw(const int32_t* ids, const double* z, double* w, int n
     i = j;
   }
   /* stage 2: inverse CDF inside the winning block, in token-id order */
-  const double target = orc_within_uniform(seed, b, k, bblk) * bestZ;
+  const double target = race_u2(seed, b, k, bblk, tag0) * bestZ;
   double C = 0.0, m2 = 0.0;
   int pick = -1, last = -1;
   for (int i = bs; i < be; ++i) {
@@ -325,7 +341,7 @@ static int draft_one_request(const float* U, const uint16_t* W1, const uint16_t*
       double* z = s;
       double* w = s + V;
       for (int v = 0; v < V; ++v) z[v] = l[v] / temperature;
-      best = block_race_draw(NULL, z, w, V, seed, (uint32_t)b, (uint32_t)k, &margins[o]);
+      best = block_race_draw(NULL, z, w, V, seed, (uint32_t)b, (uint32_t)k, 1u, &margins[o]);
       if (best < 0) return -1;
     } else {
       /* argmax, ties to the smaller token id; runner-up for the margin */
@@ -595,7 +611,7 @@ int orc_walk(const int32_t* cand, const double* S, int B, int K, int topk, doubl
           ids[q] = c[ord[q]];
           z[q] = row[ord[q]] / temperature;
         }
-        const int q = block_race_draw(ids, z, w, topk, seed, (uint32_t)b, (uint32_t)t, &margin);
+        const int q = block_race_draw(ids, z, w, topk, seed, (uint32_t)b, (uint32_t)t, 1u, &margin);
         if (q < 0) {
           bad = 1;
           break;
@@ -633,5 +649,137 @@ int orc_walk(const int32_t* cand, const double* S, int B, int K, int topk, doubl
       slot = next;
     }
   }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Speculative verification of a drafted block.                        */
+/* [FIX] "Watch the Mass Land Wrong": the target verifies a drafted     */
+/* token by accepting it with probability min(1, p/q), and resamples    */
+/* when it rejects.  [EXPL] "Confidence-scheduled verification": that   */
+/* acceptance probability is 1 - TV(p^d_k, p^t_k); "Hardware-aware      */
+/* prefix scheduling": every retained token goes through the target's   */
+/* accept-or-correct rule, and truncating the verified prefix changes   */
+/* the work, not the output distribution; "Two bottlenecks after you    */
+/* already have a parallel drafter": the target adds a bonus token when */
+/* the whole draft survives.  Reading (the pages say "resamples"): at   */
+/* the first rejection, at position j, the token is drawn from the      */
+/* normalised residual max(0, p_j - q_j), which makes the committed     */
+/* tokens exactly the target's; when all ell verified tokens survive,   */
+/* the bonus is drawn from p_ell.                                       */
+/*                                                                    */
+/* P [B, K+1, V] fp32 target logits (row k: the target's distribution   */
+/* at position k; row K: after a fully accepted block); p_k =           */
+/* softmax(P[b,k]/Tt) (Tt = 0: one-hot at the argmax, ties to the       */
+/* smaller id).  q_k = the draft's distribution at position k given the */
+/* drafted predecessor (x_{-1} = anchor): softmax(l_k/Td) with l_k the  */
+/* calibrated logits (gated when H != NULL); Td = 0: one-hot at x_k.    */
+/* ell [B] verified positions (NULL: K).  Position k's acceptance       */
+/* uniform is orc_accept_uniform(seed, b, k); draws use the block race  */
+/* on the verifier's streams (tag 9) at the position drawn for.         */
+/* Outputs (compact [nb]): n_acc = accepted prefix length, next_token,  */
+/* accept_prob [nb, K] = min(1, p_k(x_k)/q_k(x_k)) for k < ell (else    */
+/* -1), margins [nb] = the smallest decision margin (|u - a| of every  */
+/* acceptance test, and the draw's margin).                            */
+/* ------------------------------------------------------------------ */
+static void target_probs(const float* Prow, int V, double Tt, double* pv) {
+  if (Tt > 0.0) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v)
+      if ((double)Prow[v] / Tt > m) m = (double)Prow[v] / Tt;
+    double sum = 0.0;
+    for (int v = 0; v < V; ++v) sum += exp((double)Prow[v] / Tt - m);
+    for (int v = 0; v < V; ++v) pv[v] = exp((double)Prow[v] / Tt - m) / sum;
+  } else {
+    int best = 0;
+    for (int v = 1; v < V; ++v)
+      if (Prow[v] > Prow[best]) best = v;
+    for (int v = 0; v < V; ++v) pv[v] = (v == best) ? 1.0 : 0.0;
+  }
+}
+
+static void draft_probs(const double* l, int V, double Td, int32_t x, double* qv) {
+  if (Td > 0.0) {
+    const double lse = log_sum_exp_scaled(l, V, Td);
+    for (int v = 0; v < V; ++v) qv[v] = exp(l[v] / Td - lse);
+  } else {
+    for (int v = 0; v < V; ++v) qv[v] = (v == x) ? 1.0 : 0.0;
+  }
+}
+
+int orc_verify(const float* P, const float* U, const uint16_t* W1, const uint16_t* W2,
+               const int32_t* anchors, const double* H, const int32_t* tokens,
+               const int32_t* ell, int B, int K, int V, int r, double Td, double Tt,
+               uint64_t seed, int b0, int nb, int32_t* n_acc, int32_t* next_token,
+               double* accept_prob, double* margins) {
+  if (B <= 0 || K <= 0 || V <= 0 || r < 0 || b0 < 0 || nb < 0 || b0 + nb > B) return -1;
+  double* l = (double*)malloc(sizeof(double) * (size_t)V);
+  double* pv = (double*)malloc(sizeof(double) * (size_t)V);
+  double* qv = (double*)malloc(sizeof(double) * (size_t)V);
+  double* z = (double*)malloc(sizeof(double) * (size_t)V);
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  double* e = (double*)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+  int bad = (!l || !pv || !qv || !z || !w || !e);
+  for (int bi = 0; bi < nb && !bad; ++bi) {
+    const int b = b0 + bi;
+    const int L = ell ? ell[b] : K;
+    if (L < 0 || L > K) {
+      bad = 1;
+      break;
+    }
+    double margin = INFINITY;
+    int32_t prev = anchors[b];
+    int n = 0, pos = L, rejected = 0;
+    for (int k = 0; k < K; ++k) accept_prob[(int64_t)bi * K + k] = -1.0;
+    for (int k = 0; k < L; ++k) {
+      const int32_t x = tokens[(int64_t)b * K + k];
+      if (prev < 0 || prev >= V || x < 0 || x >= V) {
+        bad = 1;
+        break;
+      }
+      calibrated_logits(U + ((int64_t)b * K + k) * V, W1, W2,
+                        H ? H + ((int64_t)b * K + k) * r : NULL, V, r, prev, e, l);
+      target_probs(P + ((int64_t)b * (K + 1) + k) * V, V, Tt, pv);
+      draft_probs(l, V, Td, x, qv);
+      const double a = (qv[x] > 0.0) ? fmin(1.0, pv[x] / qv[x]) : 1.0;
+      accept_prob[(int64_t)bi * K + k] = a;
+      const double u = orc_accept_uniform(seed, (uint32_t)b, (uint32_t)k);
+      margin = fmin(margin, fabs(u - a));
+      if (u < a) {
+        ++n;
+        prev = x;
+        continue;
+      }
+      /* rejected: the residual max(0, p - q), as log-weights for the race */
+      for (int v = 0; v < V; ++v) {
+        const double d = pv[v] - qv[v];
+        z[v] = d > 0.0 ? log(d) : -INFINITY;
+      }
+      pos = k;
+      rejected = 1;
+      break;
+    }
+    if (bad) break;
+    if (!rejected) {
+      /* bonus: the target's own draw at position ell */
+      target_probs(P + ((int64_t)b * (K + 1) + L) * V, V, Tt, pv);
+      for (int v = 0; v < V; ++v) z[v] = pv[v] > 0.0 ? log(pv[v]) : -INFINITY;
+    }
+    double dm = 0.0;
+    const int y = block_race_draw(NULL, z, w, V, seed, (uint32_t)b, (uint32_t)pos, 9u, &dm);
+    if (y < 0) {
+      bad = 1;
+      break;
+    }
+    n_acc[bi] = n;
+    next_token[bi] = y;
+    margins[bi] = fmin(margin, dm);
+  }
+  free(l);
+  free(pv);
+  free(qv);
+  free(z);
+  free(w);
+  free(e);
   return bad ? -1 : 0;
 }

@@ -23,8 +23,8 @@ MUTANTS = [
      ["test_sampler_matches_exhaustive_joint", "test_greedy_is_argmax_of_calibrated_logits"]),
     ("block-race-exponential-not-logged", "const double score = log(Z) - log(E);",
      "const double score = log(Z) - E;", ["test_temperature_scales_the_sampled_softmax"]),
-    ("stage2-reuses-stage1-uniform", "orc_within_uniform(seed, b, k, bblk) * bestZ",
-     "orc_block_uniform(seed, b, k, bblk) * bestZ",
+    ("stage2-reuses-stage1-uniform", "race_u2(seed, b, k, bblk, tag0) * bestZ",
+     "race_u1(seed, b, k, bblk, tag0) * bestZ",
      ["test_temperature_scales_the_sampled_softmax"]),
     ("block-mass-drops-first-token",
      "while (j < n && ((uint32_t)(ids ? ids[j] : j) >> 4) == blk) Z += w[j++];",
@@ -51,6 +51,15 @@ MUTANTS = [
      ["test_walk_with_k_equal_V_is_the_full_head"]),
     ("uniform-offset", "+ 0.5) * (1.0 / 8388608.0)", "+ 1.0) * (1.0 / 8388608.0)",
      ["test_uniform_grid_and_word_selection"]),
+    ("verify-ratio-inverted", "fmin(1.0, pv[x] / qv[x])", "fmin(1.0, qv[x] / pv[x])",
+     ["test_verify_commits_the_target_distribution"]),
+    ("verify-resample-from-target", "z[v] = d > 0.0 ? log(d) : -INFINITY;",
+     "z[v] = pv[v] > 0.0 ? log(pv[v]) : -INFINITY;",
+     ["test_verify_commits_the_target_distribution",
+      "test_verify_greedy_draft_accepts_with_the_target_probability"]),
+    ("verify-bonus-row-before-the-window", "target_probs(P + ((int64_t)b * (K + 1) + L) * V, V, Tt, pv);",
+     "target_probs(P + ((int64_t)b * (K + 1) + (L > 0 ? L - 1 : 0)) * V, V, Tt, pv);",
+     ["test_verify_target_equal_to_draft_accepts_every_token"]),
 ]
 
 

@@ -375,3 +375,113 @@ def test_confidence_threshold_extremes_and_monotonicity(orc):
 def test_head_parameter_count():
     """2 * V * r = 77.8M parameters for a 151936-token vocabulary at rank 256 (explainer's ablation)."""
     assert 2 * 151936 * 256 == 77_791_232
+
+
+# ------------------------------------------------------------------ verification
+def _verify_case(orc, N, V, K, r, seed, Td=1.0, Tt=1.0, std=0.5, ell=None):
+    """N requests sharing one draft head and one target table; the drafted tokens
+    are the oracle draft's own draws (tokens must be draws from q for the
+    acceptance rule to be lossless)."""
+    rng = np.random.default_rng(seed)
+    U1 = rng.standard_normal((1, K, V)).astype(np.float32)
+    W1 = bf16_bits(rng.normal(0, std, (V, r)).astype(np.float32))
+    W2 = bf16_bits(rng.normal(0, std, (r, V)).astype(np.float32))
+    P1 = (rng.standard_normal((1, K + 1, V)) * 1.2).astype(np.float32)
+    U = np.ascontiguousarray(np.broadcast_to(U1, (N, K, V)))
+    P = np.ascontiguousarray(np.broadcast_to(P1, (N, K + 1, V)))
+    anchors = np.full(N, 3, np.int32)
+    drafted = orc.markov_draft(U, W1, W2, anchors, temperature=Td, seed=seed + 1)
+    out = orc.verify(P, U, W1, W2, anchors, drafted["tokens"], draft_temperature=Td,
+                     target_temperature=Tt, seed=seed + 2, ell=ell)
+    return U1, W1, W2, P1, drafted, out
+
+
+def _softmax_rows(x, T):
+    return special.softmax(x.astype(np.float64) / T, axis=-1)
+
+
+def test_verify_commits_the_target_distribution(orc):
+    """Lossless acceptance: the first committed token is distributed as p_0, and, once
+    position 1 is reached, the second as p_1; the acceptance rate at position 0 is
+    1 - TV(p_0, q_0) (the confidence label's definition)."""
+    N, V, K, r = 200_000, 40, 2, 8
+    U1, W1, W2, P1, drafted, out = _verify_case(orc, N, V, K, r, seed=41)
+    x, n, y = drafted["tokens"], out["n_acc"], out["next_token"]
+    c0 = np.where(n >= 1, x[:, 0], y)
+    p0 = _softmax_rows(P1[0, 0], 1.0)
+    assert _chi2_pvalue(np.bincount(c0, minlength=V).astype(np.float64), p0 * N) > 0.01
+    reached = n >= 1
+    c1 = np.where(n[reached] >= 2, x[reached, 1], y[reached])
+    p1 = _softmax_rows(P1[0, 1], 1.0)
+    assert _chi2_pvalue(np.bincount(c1, minlength=V).astype(np.float64), p1 * reached.sum()) > 0.01
+    # q_0: the draft's softmax after the anchor
+    q0 = _softmax_rows(U1[0, 0] + f64(W1)[3] @ f64(W2), 1.0)
+    acc = 1.0 - 0.5 * np.abs(p0 - q0).sum()
+    rate = reached.mean()
+    assert abs(rate - acc) < 4 * np.sqrt(acc * (1 - acc) / N)
+    # the reported acceptance probabilities are min(1, p/q) of the drafted tokens
+    assert np.allclose(out["accept_prob"][:, 0], np.minimum(1.0, p0[x[:, 0]] / q0[x[:, 0]]),
+                       atol=1e-12)
+
+
+def test_verify_greedy_target_is_the_argmax_rule(orc):
+    N, V, K, r = 300, 64, 4, 8
+    U1, W1, W2, P1, drafted, out = _verify_case(orc, N, V, K, r, seed=42, Tt=0.0)
+    am = P1[0].argmax(-1)                               # [K+1]
+    x = drafted["tokens"]
+    match = x == am[None, :K]
+    n_ref = np.where(match.all(1), K, np.argmin(match, axis=1))
+    assert np.array_equal(out["n_acc"], n_ref)
+    assert np.array_equal(out["next_token"], am[n_ref])
+
+
+def test_verify_target_equal_to_draft_accepts_every_token(orc):
+    """p == q: every min(1, p/q) is one, so the whole window is accepted and the bonus
+    comes from the target's row after it."""
+    N, V, K, r = 20_000, 48, 3, 8
+    rng = np.random.default_rng(43)
+    inp = make_inputs(44, N, K, V, r, weight_std=0.5)
+    drafted = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=0.8, seed=5)
+    prev = np.concatenate([inp.anchors[:, None], drafted["tokens"][:, :-1]], axis=1)
+    lg = orc.markov_logits(inp.U, inp.W1, inp.W2, prev)["logits"]
+    bonus = np.broadcast_to(rng.standard_normal((1, 1, V)), (N, 1, V))
+    P = np.concatenate([lg, bonus], axis=1).astype(np.float32)
+    # the fp32 rounding of P makes p and q differ by ~1e-7: use P's own rounding on both sides
+    U32 = (P[:, :K] - (lg - inp.U)).astype(np.float32)
+    out = orc.verify(P, U32, inp.W1, inp.W2, inp.anchors, drafted["tokens"], draft_temperature=0.8,
+                     target_temperature=0.8, seed=6)
+    assert (out["n_acc"] == K).mean() > 0.995
+    full = out["n_acc"] == K
+    pb = _softmax_rows(P[0, K], 0.8)
+    cnt = np.bincount(out["next_token"][full], minlength=V).astype(np.float64)
+    assert _chi2_pvalue(cnt, pb * full.sum()) > 0.01
+
+
+def test_verify_window_zero_draws_the_bonus_at_position_zero(orc):
+    N, V, K, r = 100_000, 40, 3, 8
+    U1, W1, W2, P1, drafted, out = _verify_case(orc, N, V, K, r, seed=45,
+                                                ell=np.zeros(100_000, np.int32))
+    assert np.all(out["n_acc"] == 0)
+    p0 = _softmax_rows(P1[0, 0], 1.0)
+    assert _chi2_pvalue(np.bincount(out["next_token"], minlength=V).astype(np.float64), p0 * N) > 0.01
+    assert np.all(out["accept_prob"] == -1.0)
+
+
+def test_verify_greedy_draft_accepts_with_the_target_probability(orc):
+    """Td = 0: q is one-hot at the drafted token, so it survives with probability p(x)."""
+    N, V, K, r = 100_000, 40, 1, 8
+    U1, W1, W2, P1, drafted, out = _verify_case(orc, N, V, K, r, seed=46, Td=0.0)
+    x = drafted["tokens"][0, 0]
+    assert np.all(drafted["tokens"][:, 0] == x)        # greedy draft: one token
+    p = _softmax_rows(P1[0, 0], 1.0)[x]
+    rate = (out["n_acc"] >= 1).mean()
+    assert abs(rate - p) < 4 * np.sqrt(p * (1 - p) / N)
+    # the rejections resample from p with x removed
+    rej = out["n_acc"] == 0
+    pr = _softmax_rows(P1[0, 0], 1.0)
+    pr[x] = 0.0
+    pr /= pr.sum()
+    cnt = np.bincount(out["next_token"][rej], minlength=V).astype(np.float64)
+    assert cnt[x] == 0
+    keep = np.arange(V) != x
+    assert _chi2_pvalue(cnt[keep], pr[keep] * rej.sum()) > 0.01
