@@ -276,6 +276,48 @@ int dspark_markov_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1,
                          const uint16_t* Wg, int d, int B, int K, int V, int r,
                          float temperature, float* logits, float* lse, dspark_stream_t stream);
 
+/* --------------------------------------------------------------------- */
+/* Speculative verification of a drafted block                             */
+/* --------------------------------------------------------------------- */
+
+/* The target's accept-or-correct rule over each request's verify window.
+ * Source: "DSpark: Repair the Joint, Meter the Verify", "Watch the Mass Land
+ * Wrong" (accept a drafted token with probability min(1, p/q); on a rejection
+ * the target resamples); DSpark explainer, "Confidence-scheduled
+ * verification" (that probability is 1 - TV(p^d_k, p^t_k)), "Hardware-aware
+ * prefix scheduling" (every retained token goes through this rule) and "Two
+ * bottlenecks after you already have a parallel drafter" (a bonus token when
+ * the whole draft survives).  For k = 0 .. ell[b]-1 in order, drafted token
+ * x_k survives with probability min(1, p_k(x_k) / q_k(x_k)); at the first
+ * rejection (position j) the next token is drawn from the normalised residual
+ * max(0, p_j - q_j); if all ell[b] survive, it is drawn from p_{ell[b]}.
+ *   P [B, K+1, V] fp32 target logits (row k: position k; row K: after a fully
+ *     accepted block); p_k = softmax(P[b,k] / target_temperature), one-hot at
+ *     the argmax (ties to the smaller id) when target_temperature == 0.
+ *   U, W1, W2, anchors (and h, Wg, d when gated): the draft head's inputs, as
+ *     given to the draft call; q_k = softmax(l_k / draft_temperature) of its
+ *     calibrated logits given the drafted predecessor (one-hot at x_k when
+ *     draft_temperature == 0).
+ *   tokens [B, K] drafted tokens; draft_logprobs [B, K] their log q_k(x_k) as
+ *     returned by the draft call (required when draft_temperature > 0).
+ *   ell [B] verified positions per request in [0, K] (NULL: K; values outside
+ *     are clamped), e.g. the confidence head's verify_len.
+ * Outputs: n_acc [B] accepted prefix length; next_token [B] the target's token
+ * after it; accept_prob [B, K] (NULL: not written) min(1, p/q) for k < ell[b],
+ * -1 beyond.  Noise: Philox4x32-10 keyed by the seed; position k's acceptance
+ * uniform from counter (k, 0, b, 13) word 0; the draw at position j uses the
+ * block race of the draft (16-token blocks) on counter (beta >> 3, j, b,
+ * 9 + (beta & 3)).  Sizes within the context's B_max, K_max, V_max; V % 8 == 0
+ * and 16-byte aligned P and U.  Drafted tokens out of [0, V) are reported as
+ * DSPARK_ERR_DEVICE_OOB.  Scratch: the context's verification buffers
+ * (2 * B_max * V_max floats, allocated at creation). */
+int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
+                  const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
+                  const uint16_t* Wg, int d, const int32_t* tokens, const float* draft_logprobs,
+                  const int32_t* ell, int B, int K, int V, int r, float draft_temperature,
+                  float target_temperature, uint64_t seed, int32_t* n_acc, int32_t* next_token,
+                  float* accept_prob, dspark_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ EXPORTS = (
     "dspark_debug_set", "dspark_debug_trace", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
-    "dspark_markov_draft_noalloc",
+    "dspark_markov_draft_noalloc", "dspark_verify",
 )
 
 
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH):
         "dspark_confidence": [P, P, P, P, P, P, F, I, I, I, I, I, I, F, P, P, P, P],
         "dspark_markov_logits": [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P],
         "dspark_markov_draft_noalloc": [P, P, P, P, I, I, I, I, F, U64, P, P, P, P],
+        "dspark_verify": [P, P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, F, F, U64, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +289,20 @@ def dspark_markov_logits(ctx: Context, U, W1, W2, prev_tokens, h, Wg, d, B, K, V
     _check(code, "dspark_markov_logits")
 
 
+def dspark_verify(ctx: Context, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_logprobs, ell,
+                  B, K, V, r, draft_temperature, target_temperature, seed, n_acc, next_token,
+                  accept_prob, stream=None):
+    code = ctx.lib.dspark_verify(
+        ctx.handle, _ptr(P, (torch.float32,), "P"), _ptr(U, (torch.float32,), "U"),
+        _ptr(W1, _BF16, "W1"), _ptr(W2, _BF16, "W2"), _ptr(anchors, (torch.int32,), "anchors"),
+        _ptr(h, _BF16, "h"), _ptr(Wg, _BF16, "Wg"), d, _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(draft_logprobs, (torch.float32,), "draft_logprobs"), _ptr(ell, (torch.int32,), "ell"),
+        B, K, V, r, float(draft_temperature), float(target_temperature), int(seed) & (2 ** 64 - 1),
+        _ptr(n_acc, (torch.int32,), "n_acc"), _ptr(next_token, (torch.int32,), "next_token"),
+        _ptr(accept_prob, (torch.float32,), "accept_prob"), _stream(stream, ctx.device))
+    _check(code, "dspark_verify")
+
+
 def dspark_markov_draft_noalloc(U, W1, W2, anchors, B, K, V, r, temperature, seed, tokens,
                                 logprobs, device_status=None, stream=None):
     """Context-free draft that allocates no device memory (scratch compiled into the library).
@@ -381,6 +396,21 @@ def confidence(ctx: Context, h, W1, anchors, tokens, w, *, V, bias=0.0, with_mar
     dspark_confidence(ctx, h, W1 if with_markov else None, anchors, tokens, w, bias, with_markov,
                       B, K, d, r, V, threshold, conf, cum, vl, stream)
     return dict(conf=conf, cumprod=cum, verify_len=vl)
+
+
+def verify(ctx: Context, P, U, W1, W2, anchors, tokens, draft_logprobs, *, draft_temperature,
+           target_temperature, seed=0, ell=None, h=None, Wg=None, stream=None) -> dict:
+    """Speculative verification of drafted tokens [B, K] against target logits P [B, K+1, V]."""
+    B, K, V = U.shape
+    r = _rank(W1)
+    n_acc = torch.empty(B, dtype=torch.int32, device=U.device)
+    next_token = torch.empty(B, dtype=torch.int32, device=U.device)
+    accept_prob = torch.empty(B, K, dtype=torch.float32, device=U.device)
+    d = 0 if h is None else int(h.shape[-1])
+    dspark_verify(ctx, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_logprobs, ell, B, K, V, r,
+                  draft_temperature, target_temperature, seed, n_acc, next_token, accept_prob,
+                  stream)
+    return dict(n_acc=n_acc, next_token=next_token, accept_prob=accept_prob)
 
 
 def markov_logits(ctx: Context, U, W1, W2, prev_tokens, *, temperature=1.0, h=None, Wg=None,

@@ -31,6 +31,16 @@ struct dspark_ctx {
   float* d_H = nullptr;                  // [B_max * K_max][256]
   float* d_gate_part = nullptr;          // [kGateSplitsMax][B_max * K_max][256]
   int32_t* d_topk_part_i = nullptr;      // [kTopkPartUnits][kMaxTopk] per-piece top-k lists
+  // verification scratch
+  float* d_v_lse_t = nullptr;            // [B_max][K_max + 1]
+  int32_t* d_v_argmax_t = nullptr;       // [B_max][K_max + 1]
+  dspark::VerifySel* d_v_sel = nullptr;  // [B_max]
+  float* d_v_U = nullptr;                // [B_max][V_max]
+  float* d_v_H = nullptr;                // [B_max][256]
+  int32_t* d_v_prev = nullptr;           // [B_max]
+  float* d_v_Lq = nullptr;               // [B_max][V_max]
+  float* d_v_lse_q = nullptr;            // [B_max]
+  dspark::VerifyRec* d_v_rec = nullptr;  // [B_max][kVerifyMaxPieces]
   float* d_topk_part_v = nullptr;
   uint32_t bar_counter = 0;              // host copy of the grid-barrier counter
   uint32_t epoch = 0;                    // last key epoch used
@@ -327,7 +337,19 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
             cudaMalloc(&ctx->d_topk_part_i, sizeof(int32_t) * dspark::kTopkPartUnits *
                                                 dspark::kMaxTopk) == cudaSuccess &&
             cudaMalloc(&ctx->d_topk_part_v,
-                       sizeof(float) * dspark::kTopkPartUnits * dspark::kMaxTopk) == cudaSuccess;
+                       sizeof(float) * dspark::kTopkPartUnits * dspark::kMaxTopk) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_lse_t, sizeof(float) * B_max * (K_max + 1)) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_argmax_t, sizeof(int32_t) * B_max * (K_max + 1)) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_sel, sizeof(dspark::VerifySel) * B_max) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_U, sizeof(float) * static_cast<size_t>(B_max) * V_max) ==
+                cudaSuccess &&
+            cudaMalloc(&ctx->d_v_H, sizeof(float) * B_max * dspark::kMaxRank) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_prev, sizeof(int32_t) * B_max) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_Lq, sizeof(float) * static_cast<size_t>(B_max) * V_max) ==
+                cudaSuccess &&
+            cudaMalloc(&ctx->d_v_lse_q, sizeof(float) * B_max) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_rec, sizeof(dspark::VerifyRec) * B_max * dspark::kVerifyMaxPieces) ==
+                cudaSuccess;
   ok = ok && cudaMemset(ctx->d_status, 0, sizeof(int)) == cudaSuccess &&
        cudaMemset(ctx->d_bar, 0, sizeof(uint32_t)) == cudaSuccess &&
        cudaMemset(ctx->d_keys, 0, sizeof(unsigned long long) * K_max * dspark::kBatchChunk) ==
@@ -351,6 +373,15 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_H);
   cudaFree(ctx->d_gate_part);
   cudaFree(ctx->d_topk_part_i);
+  cudaFree(ctx->d_v_lse_t);
+  cudaFree(ctx->d_v_argmax_t);
+  cudaFree(ctx->d_v_sel);
+  cudaFree(ctx->d_v_U);
+  cudaFree(ctx->d_v_H);
+  cudaFree(ctx->d_v_prev);
+  cudaFree(ctx->d_v_Lq);
+  cudaFree(ctx->d_v_lse_q);
+  cudaFree(ctx->d_v_rec);
   cudaFree(ctx->d_topk_part_v);
   delete ctx;
   return DSPARK_OK;
@@ -571,6 +602,78 @@ int dspark_markov_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, co
   return run_draft(ctx, dspark::kModeTeacherForced, U, W1, W2, prev_tokens, prev_tokens,
                    gated ? ctx->d_H : nullptr, B, K, V, r, temperature, 0, nullptr, nullptr,
                    logits, lse, nullptr, s);
+}
+
+int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
+                  const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
+                  const uint16_t* Wg, int d, const int32_t* tokens, const float* draft_logprobs,
+                  const int32_t* ell, int B, int K, int V, int r, float draft_temperature,
+                  float target_temperature, uint64_t seed, int32_t* n_acc, int32_t* next_token,
+                  float* accept_prob, dspark_stream_t stream) {
+  if (P == nullptr || tokens == nullptr || n_acc == nullptr || next_token == nullptr)
+    return DSPARK_ERR_INVALID_ARG;
+  int st = check_draft_args(U, W1, W2, anchors, B, K, V, r, draft_temperature, n_acc, next_token);
+  if (st != DSPARK_OK) return st;
+  if (!(target_temperature >= 0.f) || target_temperature > 3.0e38f) return DSPARK_ERR_INVALID_ARG;
+  if (draft_temperature > 0.f && draft_logprobs == nullptr) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(P)) return DSPARK_ERR_INVALID_ARG;
+  const bool gated = (h != nullptr) || (Wg != nullptr);
+  if (gated && (st = check_gate_args(h, Wg, d, r)) != DSPARK_OK) return st;
+  if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
+  if (B > ctx->B_max || K > ctx->K_max || V > ctx->V_max) return DSPARK_ERR_CAPACITY;
+  ctx->last_launches = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (gated) {
+    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+    if (st != DSPARK_OK) return st;
+  }
+  dspark::VerifyArgs v{};
+  v.P = P;
+  v.U = U;
+  v.H = gated ? ctx->d_H : nullptr;
+  v.tokens = tokens;
+  v.logq = draft_logprobs;
+  v.anchors = anchors;
+  v.ell = ell;
+  v.B = B;
+  v.K = K;
+  v.V = V;
+  v.r = r;
+  v.draft_temperature = draft_temperature;
+  v.target_temperature = target_temperature;
+  v.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
+  v.seed_hi = static_cast<uint32_t>(seed >> 32);
+  v.n_acc = n_acc;
+  v.next_token = next_token;
+  v.accept_prob = accept_prob;
+  v.status = ctx->d_status;
+  v.lse_t = ctx->d_v_lse_t;
+  v.argmax_t = ctx->d_v_argmax_t;
+  v.sel = ctx->d_v_sel;
+  v.U_sel = ctx->d_v_U;
+  v.H_sel = ctx->d_v_H;
+  v.prev_sel = ctx->d_v_prev;
+  v.Lq = ctx->d_v_Lq;
+  v.lse_q = ctx->d_v_lse_q;
+  v.rec = ctx->d_v_rec;
+  int n = 0;
+  cudaError_t e = dspark::launch_verify(v, s, &n);
+  ctx->last_launches += n;
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (target_temperature > 0.f && draft_temperature > 0.f) {
+    // q over the vocabulary at each request's draw position: the draft head in
+    // teacher-forced mode over one position of gathered rows
+    e = dspark::launch_verify_gather(v, s);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    ctx->last_launches += 1;
+    st = run_draft(ctx, dspark::kModeTeacherForced, ctx->d_v_U, W1, W2, ctx->d_v_prev,
+                   ctx->d_v_prev, gated ? ctx->d_v_H : nullptr, B, 1, V, r, draft_temperature, 0,
+                   nullptr, nullptr, ctx->d_v_Lq, ctx->d_v_lse_q, nullptr, s);
+    if (st != DSPARK_OK) return st;
+  }
+  e = dspark::launch_verify_race(v, ctx->num_sms, s, &n);
+  ctx->last_launches += n;
+  return cuda_status(e);
 }
 
 }  // extern "C"

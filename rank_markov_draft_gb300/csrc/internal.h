@@ -107,6 +107,54 @@ cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anch
                         int sample, uint32_t seed_lo, uint32_t seed_hi, int32_t* tokens,
                         float* logprobs, const dspark_conf_args* conf, int* status,
                         cudaStream_t stream);
+// ---- speculative verification (verify.cu)
+constexpr int kVerifyMaxPieces = 64;
+
+struct VerifySel {  // where a request's draw happens and what feeds it
+  int pos;          // position of the draw: the first rejection, or the window end (bonus)
+  int residual;     // 1: residual max(0, p - q) at a rejection; 0: bonus from p
+  int x;            // the rejected drafted token (residual), else -1
+  int prev;         // its predecessor (the anchor at position 0)
+};
+
+struct VerifyRec {  // best stage-1 block of one (request, piece) unit
+  float score;
+  float Z;
+  int blk;
+  int pad;
+};
+
+struct VerifyArgs {
+  const float* P;             // [B, K+1, V] target logits
+  const float* U;             // [B, K, V] base logits of the draft
+  const float* H;             // [B, K, r] gate (null: ungated)
+  const int32_t* tokens;      // [B, K] drafted tokens
+  const float* logq;          // [B, K] the draft's log-probabilities of them (draft T > 0)
+  const int32_t* anchors;     // [B]
+  const int32_t* ell;         // [B] verified positions (null: K)
+  int B, K, V, r;
+  float draft_temperature, target_temperature;
+  uint32_t seed_lo, seed_hi;
+  int32_t* n_acc;             // [B]
+  int32_t* next_token;        // [B]
+  float* accept_prob;         // [B, K] or null
+  int* status;
+  // context scratch
+  float* lse_t;               // [B, K+1]
+  int32_t* argmax_t;          // [B, K+1]
+  VerifySel* sel;             // [B]
+  float* U_sel;               // [B, V]
+  float* H_sel;               // [B, r]
+  int32_t* prev_sel;          // [B]
+  float* Lq;                  // [B, V] draft logits at the draw position
+  float* lse_q;               // [B]
+  VerifyRec* rec;             // [B, kVerifyMaxPieces]
+};
+cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches);
+cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream);
+cudaError_t launch_verify_race(const VerifyArgs& v, int num_sms, cudaStream_t stream,
+                               int* launches);
+
 cudaError_t launch_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors,
                               const int32_t* tokens, const uint16_t* w, float bias,
                               int with_markov, int B, int K, int d, int r, int V,

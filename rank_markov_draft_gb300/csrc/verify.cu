@@ -1,0 +1,462 @@
+// verify.cu -- speculative verification of a drafted block on sm_103a.
+//
+// Source: "DSpark: Repair the Joint, Meter the Verify", "Watch the Mass Land
+// Wrong" (the target accepts a drafted token with probability min(1, p/q) and
+// resamples when it rejects); DSpark explainer, "Confidence-scheduled
+// verification" (that probability is 1 - TV(p^d_k, p^t_k)), "Hardware-aware
+// prefix scheduling" (every retained token goes through the target's
+// accept-or-correct rule; truncation changes the work, not the output) and
+// "Two bottlenecks after you already have a parallel drafter" (a bonus token
+// when the whole draft survives).  The first rejection is corrected by a draw
+// from the normalised residual max(0, p - q); a fully accepted window draws
+// the bonus from the target's next row.
+//
+// Kernels (all stream-ordered, no host synchronisation):
+//   verify_stats_kernel  one CTA per (request, position <= window) row of the
+//                        target logits: log-sum-exp of P / Tt (argmax when
+//                        Tt = 0), a pure HBM scan of the row;
+//   verify_accept_kernel one warp per request, lanes = positions: every
+//                        acceptance test at once (the draft's own
+//                        log-probabilities give q(x)), the first failure ends
+//                        the prefix; records where the draw happens and what
+//                        feeds it;
+//   verify_gather_kernel copies the base-logit row (and gate row) of each
+//                        request's draw position, so that the draft kernel in
+//                        teacher-forced mode can rebuild q over the vocabulary;
+//   verify_race_kernel   (request, piece) units: stage 1 of the block race
+//                        over the residual (or, for a bonus, the target's)
+//                        weights, 16-token blocks per lane, two at a time;
+//   verify_finish_kernel one warp per request: the best block over pieces and
+//                        stage 2, the inverse CDF inside it.
+// Noise: acceptance uniform of position k: Philox4x32-10 counter (k, 0, b, 13),
+// word 0; the draw's block race at position j: counter (beta >> 3, j, b,
+// 9 + (beta & 3)), words 2h (stage 1) and 2h + 1 (stage 2), h = (beta >> 2) & 1.
+
+#include <cstdint>
+
+#include "internal.h"
+#include "philox.cuh"
+#include "sm103.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr float kLog2eV = 1.4426950408889634f;
+constexpr float kLn2V = 0.69314718055994531f;
+constexpr int kStatsThreads = 256;
+constexpr int kRaceThreads = 256;
+
+__device__ __forceinline__ float uniform_of(uint32_t word) { return philox_uniform(word); }
+
+// Merge (ma, sa) with (mb, sb): log-sum-exp partials in base 2.
+__device__ __forceinline__ void lse2_merge(float& ma, float& sa, float mb, float sb) {
+  if (mb == -INFINITY) return;
+  if (ma == -INFINITY) {
+    ma = mb;
+    sa = sb;
+    return;
+  }
+  if (mb > ma) {
+    sa = sa * ex2_approx(ma - mb) + sb;
+    ma = mb;
+  } else {
+    sa += sb * ex2_approx(mb - ma);
+  }
+}
+
+__global__ void __launch_bounds__(kStatsThreads) verify_stats_kernel(
+    const float* __restrict__ P, const int32_t* __restrict__ ell, int K, int V, float inv_tt,
+    int greedy, float* __restrict__ lse_t, int32_t* __restrict__ argmax_t) {
+  const int row = blockIdx.x;             // b * (K + 1) + k
+  const int b = row / (K + 1), k = row - b * (K + 1);
+  const int L = ell ? min(max(__ldg(ell + b), 0), K) : K;
+  if (k > L) return;
+  const float4* p4 = reinterpret_cast<const float4*>(P + static_cast<size_t>(row) * V);
+  const int n4 = V / 4;
+  __shared__ float s_m[kStatsThreads / 32], s_s[kStatsThreads / 32];
+  __shared__ int s_i[kStatsThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (greedy) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int i = threadIdx.x; i < n4; i += kStatsThreads) {
+      const float4 x = __ldcs(p4 + i);
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (xs[c] > bv || (xs[c] == bv && 4 * i + c < bi)) {
+          bv = xs[c];
+          bi = 4 * i + c;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      s_m[warp] = bv;
+      s_i[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kStatsThreads / 32; ++w)
+        if (s_m[w] > bv || (s_m[w] == bv && s_i[w] < bi)) {
+          bv = s_m[w];
+          bi = s_i[w];
+        }
+      argmax_t[row] = bi;
+    }
+    return;
+  }
+  // online log-sum-exp of y = P * log2(e) / Tt, four float4 loads in flight
+  const float sc = inv_tt * kLog2eV;
+  float m = -INFINITY, s = 0.f;
+  for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kStatsThreads) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kStatsThreads;
+      x[u] = (i < n4) ? __ldcs(p4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    float cm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)) * sc);
+    if (cm == -INFINITY) continue;
+    if (cm > m) {
+      s = (m == -INFINITY) ? 0.f : s * ex2_approx(m - cm);
+      m = cm;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      s += ex2_approx(x[u].x * sc - m) + ex2_approx(x[u].y * sc - m) +
+           ex2_approx(x[u].z * sc - m) + ex2_approx(x[u].w * sc - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    lse2_merge(m, s, __shfl_xor_sync(0xFFFFFFFFu, m, off), __shfl_xor_sync(0xFFFFFFFFu, s, off));
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_s[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kStatsThreads / 32; ++w) lse2_merge(m, s, s_m[w], s_s[w]);
+    lse_t[row] = (m + log2f(s)) * kLn2V;  // natural-log units of P / Tt
+  }
+}
+
+// One warp per request: lanes evaluate the acceptance tests of positions
+// lane, lane + 32 (K <= 64) at once; the first failed test ends the prefix.
+__global__ void verify_accept_kernel(const float* __restrict__ P, const int32_t* __restrict__ tokens,
+                                     const float* __restrict__ logq, const int32_t* __restrict__ anchors,
+                                     const int32_t* __restrict__ ell, const float* __restrict__ lse_t,
+                                     const int32_t* __restrict__ argmax_t, int B, int K, int V,
+                                     float inv_tt, int target_greedy, int draft_greedy,
+                                     uint32_t seed_lo, uint32_t seed_hi, int32_t* __restrict__ n_acc,
+                                     int32_t* __restrict__ next_token, float* __restrict__ accept_prob,
+                                     VerifySel* __restrict__ sel, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int L = ell ? min(max(__ldg(ell + b), 0), K) : K;
+  uint32_t ok_lo = 0u, ok_hi = 0u;  // bit k: position k's token survives its test
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int k = half * 32 + lane;
+    bool pass = true;
+    if (k < L) {
+      int x = __ldg(tokens + static_cast<size_t>(b) * K + k);
+      if (x < 0 || x >= V) {
+        record_error(status, kStatusDeviceOob);
+        x = 0;
+      }
+      const size_t row = static_cast<size_t>(b) * (K + 1) + k;
+      const float pr = target_greedy ? ((x == argmax_t[row]) ? 1.f : 0.f)
+                                     : expf(__ldg(P + row * V + x) * inv_tt - lse_t[row]);
+      const float q = draft_greedy ? 1.f : expf(__ldg(logq + static_cast<size_t>(b) * K + k));
+      const float a = (q > 0.f) ? fminf(1.f, pr / q) : 1.f;
+      if (accept_prob) accept_prob[static_cast<size_t>(b) * K + k] = a;
+      const Philox4 rnd = philox4x32_10(static_cast<uint32_t>(k), 0u, static_cast<uint32_t>(b),
+                                        13u, seed_lo, seed_hi);
+      pass = uniform_of(rnd.w[0]) < a;
+    } else if (k < K && accept_prob) {
+      accept_prob[static_cast<size_t>(b) * K + k] = -1.f;
+    }
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+    if (half == 0) ok_lo = bal; else ok_hi = bal;
+  }
+  // first failed test below L
+  int n = L;
+  if (~ok_lo != 0u && __ffs(~ok_lo) - 1 < L) {
+    n = __ffs(~ok_lo) - 1;
+  } else if (~ok_hi != 0u && 32 + __ffs(~ok_hi) - 1 < L) {
+    n = 32 + __ffs(~ok_hi) - 1;
+  }
+  if (lane == 0) {
+    const int rejected = n < L ? 1 : 0;
+    const int pos = n;
+    n_acc[b] = n;
+    VerifySel s;
+    s.pos = pos;
+    s.residual = rejected;
+    s.x = rejected ? __ldg(tokens + static_cast<size_t>(b) * K + pos) : -1;
+    int prev = (pos == 0) ? __ldg(anchors + b) : __ldg(tokens + static_cast<size_t>(b) * K + pos - 1);
+    if (prev < 0 || prev >= V) {
+      record_error(status, kStatusDeviceOob);
+      prev = 0;
+    }
+    if (s.x >= V || (rejected && s.x < 0)) s.x = 0;
+    s.prev = prev;
+    sel[b] = s;
+    if (target_greedy) next_token[b] = argmax_t[static_cast<size_t>(b) * (K + 1) + pos];
+  }
+}
+
+// Base-logit (and gate) rows of each request's draw position, for the draft
+// kernel's teacher-forced pass over one position.
+__global__ void verify_gather_kernel(const float* __restrict__ U, const float* __restrict__ H,
+                                     const VerifySel* __restrict__ sel, int K, int V, int r,
+                                     float* __restrict__ U_sel, float* __restrict__ H_sel,
+                                     int32_t* __restrict__ prev_sel) {
+  const int b = blockIdx.y;
+  const VerifySel s = sel[b];
+  const int pos = min(s.pos, K - 1);  // a bonus row needs no q; any valid row will do
+  const float4* src = reinterpret_cast<const float4*>(U + (static_cast<size_t>(b) * K + pos) * V);
+  float4* dst = reinterpret_cast<float4*>(U_sel + static_cast<size_t>(b) * V);
+  // this CTA's 4096-float4 slice of the row, four loads in flight per thread
+  const int i0 = blockIdx.x * 4096;
+  const int i1 = min(V / 4, i0 + 4096);
+#pragma unroll 4
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) dst[i] = __ldcs(src + i);
+  if (blockIdx.x != 0) return;
+  if (H != nullptr) {
+    const float* hs = H + (static_cast<size_t>(b) * K + pos) * r;
+    for (int i = threadIdx.x; i < r; i += blockDim.x) H_sel[static_cast<size_t>(b) * r + i] = hs[i];
+  }
+  if (threadIdx.x == 0) prev_sel[b] = s.prev;
+}
+
+// Weight of token v for request b (16 values of one block at a time).
+struct RaceIn {
+  const float* P;       // [B, K+1, V]
+  const float* Lq;      // [B, V] draft logits at the draw position (null: draft greedy)
+  const float* lse_t;   // [B, K+1]
+  const float* lse_q;   // [B]
+  const VerifySel* sel;
+  int B, K, V, pieces, piece_len;
+  float inv_tt, inv_td;
+  uint32_t seed_lo, seed_hi;
+  VerifyRec* rec;       // [B][pieces]
+};
+
+__device__ __forceinline__ void block_weights(const RaceIn& a, int b, const VerifySel& s, int v0,
+                                              float (&w)[16]) {
+  const size_t prow = (static_cast<size_t>(b) * (a.K + 1) + s.pos) * a.V;
+  const float lt = a.lse_t[static_cast<size_t>(b) * (a.K + 1) + s.pos];
+  const float lq = (a.Lq != nullptr) ? a.lse_q[b] : 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int v = v0 + 4 * c;
+    float4 pv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 qv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (v < a.V) {
+      pv = __ldcs(reinterpret_cast<const float4*>(a.P + prow + v));
+      if (s.residual && a.Lq != nullptr)
+        qv = __ldcs(reinterpret_cast<const float4*>(a.Lq + static_cast<size_t>(b) * a.V + v));
+    }
+    const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
+    const float qs[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float p = expf(ps[e] * a.inv_tt - lt);
+      float q = 0.f;
+      if (s.residual) q = (a.Lq != nullptr) ? expf(qs[e] * a.inv_td - lq) : ((v + e == s.x) ? 1.f : 0.f);
+      w[4 * c + e] = s.residual ? fmaxf(0.f, p - q) : p;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRaceThreads) verify_race_kernel(const __grid_constant__ RaceIn a) {
+  const int unit = blockIdx.x;
+  const int b = unit / a.pieces, piece = unit - b * a.pieces;
+  const VerifySel s = a.sel[b];
+  const int v_begin = piece * a.piece_len, v_end = min(a.V, v_begin + a.piece_len);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float best = -INFINITY, bestZ = 0.f;
+  int bestblk = 0x7FFFFFFF;
+  for (int v00 = v_begin + threadIdx.x * 16; v00 < v_end; v00 += 2 * kRaceThreads * 16) {
+    float w2[2][16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) block_weights(a, b, s, v00 + h * kRaceThreads * 16, w2[h]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+    const int v0 = v00 + h * kRaceThreads * 16;
+    if (v0 >= v_end) break;
+    float Z = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) Z += w2[h][j];
+    if (!(Z > 0.f)) continue;
+    const uint32_t blk = static_cast<uint32_t>(v0 >> 4);
+    const Philox4 rnd = philox4x32_10(blk >> 3, static_cast<uint32_t>(s.pos), static_cast<uint32_t>(b),
+                                      9u + (blk & 3u), a.seed_lo, a.seed_hi);
+    const uint32_t word1 = ((blk >> 2) & 1u) ? rnd.w[2] : rnd.w[0];
+    const float sc = logf(Z) - logf(neg_log_uniform_accurate(uniform_of(word1)));
+    if (sc > best || (sc == best && static_cast<int>(blk) < bestblk)) {
+      best = sc;
+      bestZ = Z;
+      bestblk = static_cast<int>(blk);
+    }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+    const float oz = __shfl_xor_sync(0xFFFFFFFFu, bestZ, off);
+    const int ok = __shfl_xor_sync(0xFFFFFFFFu, bestblk, off);
+    if (ob > best || (ob == best && ok < bestblk)) {
+      best = ob;
+      bestZ = oz;
+      bestblk = ok;
+    }
+  }
+  __shared__ float s_b[kRaceThreads / 32], s_z[kRaceThreads / 32];
+  __shared__ int s_k[kRaceThreads / 32];
+  if (lane == 0) {
+    s_b[warp] = best;
+    s_z[warp] = bestZ;
+    s_k[warp] = bestblk;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRaceThreads / 32; ++w)
+      if (s_b[w] > best || (s_b[w] == best && s_k[w] < bestblk)) {
+        best = s_b[w];
+        bestZ = s_z[w];
+        bestblk = s_k[w];
+      }
+    VerifyRec rc;
+    rc.score = best;
+    rc.Z = bestZ;
+    rc.blk = bestblk;
+    a.rec[unit] = rc;
+  }
+}
+
+__global__ void verify_finish_kernel(const __grid_constant__ RaceIn a, int32_t* __restrict__ next_token,
+                                     int* status) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= a.B) return;
+  // best block over the pieces
+  float best = -INFINITY, bestZ = 0.f;
+  int bestblk = 0x7FFFFFFF;
+  for (int pc = 0; pc < a.pieces; ++pc) {
+    const VerifyRec rc = a.rec[static_cast<size_t>(b) * a.pieces + pc];
+    if (rc.score > best || (rc.score == best && rc.blk < bestblk)) {
+      best = rc.score;
+      bestZ = rc.Z;
+      bestblk = rc.blk;
+    }
+  }
+  if (bestblk == 0x7FFFFFFF) {  // no mass anywhere: nothing valid to draw
+    if (lane == 0) {
+      record_error(status, kStatusDeviceOob);
+      next_token[b] = 0;
+    }
+    return;
+  }
+  const VerifySel s = a.sel[b];
+  // stage 2: the inverse CDF of the block's weights, in token order (lanes 0..15)
+  float w[16];
+  block_weights(a, b, s, bestblk * 16, w);
+  const uint32_t blk = static_cast<uint32_t>(bestblk);
+  const Philox4 rnd = philox4x32_10(blk >> 3, static_cast<uint32_t>(s.pos), static_cast<uint32_t>(b),
+                                    9u + (blk & 3u), a.seed_lo, a.seed_hi);
+  const uint32_t word2 = ((blk >> 2) & 1u) ? rnd.w[3] : rnd.w[1];
+  const float target = uniform_of(word2) * bestZ;
+  float C = 0.f;
+  int pick = -1, last = -1;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (w[j] > 0.f) {
+      C += w[j];
+      last = j;
+      if (pick < 0 && target < C) pick = j;
+    }
+  }
+  if (pick < 0) pick = last;  // target at the very top (rounding): the last live token
+  if (lane == 0) next_token[b] = bestblk * 16 + pick;
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches) {
+  *launches = 0;
+  const int greedy_t = v.target_temperature > 0.f ? 0 : 1;
+  const int greedy_d = v.draft_temperature > 0.f ? 0 : 1;
+  const float inv_tt = greedy_t ? 1.f : 1.0f / v.target_temperature;
+  const float inv_td = greedy_d ? 1.f : 1.0f / v.draft_temperature;
+  verify_stats_kernel<<<v.B * (v.K + 1), kStatsThreads, 0, stream>>>(
+      v.P, v.ell, v.K, v.V, inv_tt, greedy_t, v.lse_t, v.argmax_t);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  verify_accept_kernel<<<(v.B + 3) / 4, 128, 0, stream>>>(
+      v.P, v.tokens, v.logq, v.anchors, v.ell, v.lse_t, v.argmax_t, v.B, v.K, v.V, inv_tt,
+      greedy_t, greedy_d, v.seed_lo, v.seed_hi, v.n_acc, v.next_token, v.accept_prob, v.sel,
+      v.status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ++*launches;
+  return cudaSuccess;
+}
+
+cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream) {
+  const dim3 grid((v.V / 4 + 4095) / 4096, v.B);
+  verify_gather_kernel<<<grid, 256, 0, stream>>>(v.U, v.H, v.sel, v.K, v.V, v.r, v.U_sel, v.H_sel,
+                                                 v.prev_sel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_race(const VerifyArgs& v, int num_sms, cudaStream_t stream,
+                               int* launches) {
+  *launches = 0;
+  if (v.target_temperature <= 0.f) return cudaSuccess;  // greedy target: decided already
+  RaceIn a{};
+  a.P = v.P;
+  a.Lq = (v.draft_temperature > 0.f) ? v.Lq : nullptr;
+  a.lse_t = v.lse_t;
+  a.lse_q = v.lse_q;
+  a.sel = v.sel;
+  a.B = v.B;
+  a.K = v.K;
+  a.V = v.V;
+  a.inv_tt = 1.0f / v.target_temperature;
+  a.inv_td = (v.draft_temperature > 0.f) ? 1.0f / v.draft_temperature : 1.f;
+  a.seed_lo = v.seed_lo;
+  a.seed_hi = v.seed_hi;
+  a.rec = v.rec;
+  // pieces of whole 4096-token chunks so that about four units run per SM
+  const int chunk = kRaceThreads * 16;
+  const int most = (v.V + chunk - 1) / chunk;
+  int pieces = (4 * num_sms + v.B - 1) / v.B;
+  pieces = pieces < 1 ? 1 : (pieces > most ? most : pieces);
+  if (pieces > kVerifyMaxPieces) pieces = kVerifyMaxPieces;
+  const int per = (most + pieces - 1) / pieces;
+  a.piece_len = per * chunk;
+  a.pieces = (v.V + a.piece_len - 1) / a.piece_len;
+  verify_race_kernel<<<v.B * a.pieces, kRaceThreads, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  verify_finish_kernel<<<(v.B + 3) / 4, 128, 0, stream>>>(a, v.next_token, v.status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  *launches = 2;
+  return cudaSuccess;
+}
+
+}  // namespace dspark
