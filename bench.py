@@ -40,6 +40,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "Markov-head draft tokens/s at B=128 K=16 V=151936; % of HBM roofline"
+VERIFY_METRIC = "verified draft tokens/s (speculative verification) at B=128 K=16 V=151936"
 L2_FLUSH_BYTES = 512 << 20       # larger than the 129 MB L2
 CONF_THRESHOLD = 0.3
 
@@ -50,7 +51,18 @@ WORKLOADS = {
     "gated": (3, "gated head: B=64 K=16 V=151936 r=256 d=4096"),
     "selector": (4, "selector top-16 (gated): B=256 K=16 V=151936 r=256 d=4096"),
     "tiny": (0, "tiny: B=1 K=4 V=4096 r=256"),
+    "verify": (2, "speculative verification of the serving batch: B=128 K=16 V=151936 r=256, "
+                  "synthetic target logits (draft base logits + N(0,1)), T_draft = T_target = 1"),
 }
+VERIFY_TARGET_SEED = 2002
+
+
+def verify_bytes(c: dict) -> int:
+    """Bytes one full-window verification must move: every verified target row and
+    the bonus row, then, for the draw, W2, each request's base-logit row, its
+    embedding row and its target row again."""
+    B, K, V, r = c["B"], c["K"], c["V"], c["r"]
+    return B * (K + 1) * V * 4 + r * V * 2 + B * V * 4 + B * r * 2 + B * V * 4
 
 
 def algorithmic_bytes(cfg: int, c: dict) -> int:
@@ -250,6 +262,27 @@ def cpu_baseline(inp, c, target_s):
                       f"(fp64 oracle, {threads} OpenMP threads, {spent:.1f} s)"}
 
 
+def verify_cpu_baseline(inp, c, target_s, dtok):
+    """The fp64 oracle's verification of whole requests, timed one after the other."""
+    import oracle
+    from synth import target_logits
+    oracle.build()
+    threads = oracle.max_threads()
+    K, B = c["K"], c["B"]
+    tokens = dtok.cpu().numpy()
+    P = target_logits(VERIFY_TARGET_SEED, inp.U)
+    done, spent = 0, 0.0
+    while spent < target_s and done < B:
+        t0 = time.perf_counter()
+        oracle.verify(P, inp.U, inp.W1, inp.W2, inp.anchors, tokens, draft_temperature=1.0,
+                      target_temperature=1.0, seed=done, b0=done, nb=1)
+        spent += time.perf_counter() - t0
+        done += 1
+    return {"value": done * K / spent, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"verification of {done} of {B} requests x {K} positions "
+                      f"(fp64 oracle, {threads} OpenMP threads, {spent:.1f} s)"}
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: per step one request of the workload."""
     from synth import CONFIGS, config_inputs
@@ -261,16 +294,33 @@ def run_reference(args, rank, world):
     oracle.build()
     inp = config_inputs(cfg)
     K = c["K"]
+    if args.workload == "verify":
+        # the oracle's draft of the batch's first requests, then their verification
+        from synth import target_logits
+        P = target_logits(VERIFY_TARGET_SEED, inp.U)
+        n = args.warmup + args.steps
+        toks = np.zeros((c["B"], K), np.int32)
+        toks[:n] = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0,
+                                       seed=77, nb=min(n, c["B"]))["tokens"]
+
+        def one(b):
+            t0 = time.perf_counter()
+            oracle.verify(P, inp.U, inp.W1, inp.W2, inp.anchors, toks, draft_temperature=1.0,
+                          target_temperature=1.0, seed=b, b0=b % c["B"], nb=1)
+            return time.perf_counter() - t0
+    else:
+        def one(b):
+            return oracle_sample(inp, c, 1, b0=b % c["B"], temperature=args.temperature)
     for i in range(args.warmup):
-        oracle_sample(inp, c, 1, b0=i % c["B"], temperature=args.temperature)
+        one(i)
     spent = 0.0
     for i in range(args.steps):
-        spent += oracle_sample(inp, c, 1, b0=(args.warmup + i) % c["B"],
-                               temperature=args.temperature)
+        spent += one(args.warmup + i)
     value = args.steps * K / spent
     threads = oracle.max_threads()
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": VERIFY_METRIC if args.workload == "verify" else METRIC,
+        "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * spent / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -324,6 +374,21 @@ def run_ours(args, rank, world, local):
             binding.dspark_selector_walk(ctx, cand, scores, anchors, A, B, K, V, r, 16, T, seed,
                                          tokens, logprobs, None, stream)
             return n + ctx.last_launches
+    elif args.workload == "verify":
+        from synth import target_logits
+        W1, W2 = up(inp.W1, True), up(inp.W2, True)
+        P = up(target_logits(VERIFY_TARGET_SEED, inp.U))
+        dtok = torch.empty(B, K, dtype=torch.int32, device=dev)
+        dlp = torch.empty(B, K, dtype=torch.float32, device=dev)
+        binding.dspark_markov_draft(ctx, U, W1, W2, anchors, B, K, V, r, T, 77, dtok, dlp, None,
+                                    stream)
+        n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+        nxt = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def step(seed):
+            binding.dspark_verify(ctx, P, U, W1, W2, anchors, None, None, 0, dtok, dlp, None, B, K,
+                                  V, r, T, T, seed, n_acc, nxt, None, stream)
+            return ctx.last_launches
     else:
         W1, W2 = up(inp.W1, True), up(inp.W2, True)
         tokens = torch.empty(B, K, dtype=torch.int32, device=dev)
@@ -380,27 +445,33 @@ def run_ours(args, rank, world, local):
 
     # -------- roofline of the dominant kernel
     peak, peak_kind = measured_peaks()
-    alg = algorithmic_bytes(cfg, c)
+    alg = verify_bytes(c) if args.workload == "verify" else algorithmic_bytes(cfg, c)
     kernel_ms = statistics.median(per_step_ms)
     achieved = alg / (kernel_ms / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
-                "kernel": "draft_kernel" if cfg != 4 else
-                "selector step (top-k scan, gate, pair scores, walk)",
+                "kernel": ("verify step (target-row scan, acceptance, gather, one-position "
+                           "draft logits, residual race)" if args.workload == "verify" else
+                           "draft_kernel" if cfg != 4 else
+                           "selector step (top-k scan, gate, pair scores, walk)"),
                 "median_launch_us": round(kernel_ms * 1000, 2)}
 
     # -------- end to end through the binding with host buffers
     e2e = None
-    if not args.skip_e2e and cfg != 4:
+    if not args.skip_e2e and cfg != 4 and args.workload != "verify":
         e2e = run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world)
 
     line = None
     if rank == 0:
-        cpu = None if args.skip_cpu else cpu_baseline(inp, c, args.cpu_seconds)
+        cpu = None
+        if not args.skip_cpu:
+            cpu = (verify_cpu_baseline(inp, c, args.cpu_seconds, dtok) if args.workload == "verify"
+                   else cpu_baseline(inp, c, args.cpu_seconds))
         line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "metric": VERIFY_METRIC if args.workload == "verify" else METRIC,
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",

@@ -14,7 +14,10 @@ Recipe (the shape of the workloads on the DSpark pages; no dataset is used):
   weight ``Wg [d, r]`` and confidence weight ``w [d (+ r)]``: ``N(0, 0.02)``
   rounded to bf16 (round to nearest even);
 * hidden states ``h [B, K, d]``: ``N(0, 1)`` rounded to bf16;
-* anchors: uniform in ``[0, V)``.
+* anchors: uniform in ``[0, V)``;
+* target logits for verification (``target_logits``): the draft's base logits
+  plus ``N(0, 1)`` per token for the K draft positions, and a bonus row of
+  ``3 * N(0, 1)``.
 
 bf16 tensors are returned as ``uint16`` bit patterns.
 """
@@ -137,6 +140,19 @@ CONFIGS = {
             V=VOCAB_FULL, r=256, d=4096, gated=True, selector=True, topk=16,
             temperatures=(1.0,), seeds=tuple(range(4))),
 }
+
+
+def target_logits(seed: int, U: np.ndarray, noise: float = 1.0, bonus_std: float = 3.0) -> np.ndarray:
+    """Synthetic target logits P [B, K+1, V] for verification: the draft's base
+    logits plus N(0, noise^2) per token (a target that mostly agrees with the
+    draft), and a bonus row of N(0, bonus_std^2) after the block."""
+    B, K, V = U.shape
+    rng = np.random.default_rng(seed)
+    P = np.empty((B, K + 1, V), np.float32)
+    for b in range(B):
+        P[b, :K] = U[b] + rng.standard_normal((K, V), dtype=np.float32) * np.float32(noise)
+        P[b, K] = rng.standard_normal(V, dtype=np.float32) * np.float32(bonus_std)
+    return P
 
 
 def config_inputs(cfg: int) -> DraftInputs:
