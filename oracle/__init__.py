@@ -64,6 +64,8 @@ def _bind(lib):
     lib.orc_verify.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, f64, f64, u64, i32,
                                i32, P, P, P, P]
     lib.orc_verify.restype = i32
+    lib.orc_schedule.argtypes = [P, i32, i32, P, P, P, P]
+    lib.orc_schedule.restype = i32
     lib.orc_gate.argtypes = [P, P, i64, i32, i32, P]
     lib.orc_markov_draft.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, u64, i32, i32,
                                      P, P, P, P, P]
@@ -154,6 +156,21 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle verify rejected its arguments")
         return dict(n_acc=n_acc, next_token=nxt, accept_prob=accept_prob, margins=margins)
+
+    def schedule(self, a, sps) -> dict:
+        """Greedy load-aware prefix scheduler: survival a [R, K], SPS(B) table
+        [R * (K + 1) + 1] -> verify lengths ell [R], Theta and the stopping margin."""
+        a = _c(a, np.float64)
+        R, K = a.shape
+        sps = _c(sps, np.float64)
+        assert sps.shape[0] >= R * (K + 1) + 1
+        ell = np.zeros(R, np.int32)
+        theta = np.zeros(1, np.float64)
+        margin = np.zeros(1, np.float64)
+        rc = self._lib.orc_schedule(_ptr(a), R, K, _ptr(sps), _ptr(ell), _ptr(theta), _ptr(margin))
+        if rc != 0:
+            raise ValueError("oracle schedule rejected its arguments")
+        return dict(ell=ell, theta=float(theta[0]), margin=float(margin[0]))
 
     def gate(self, h: np.ndarray, Wg: np.ndarray) -> np.ndarray:
         """H = sigmoid(h . Wg) in fp64; h [..., d] bf16 bits, Wg [d, r] bf16 bits -> [..., r]."""

@@ -783,3 +783,72 @@ int orc_verify(const float* P, const float* U, const uint16_t* W1, const uint16_
   free(e);
   return bad ? -1 : 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Load-aware prefix scheduler.                                         */
+/* [EXPL] "Hardware-aware prefix scheduling": R requests, request r may  */
+/* verify a prefix of length ell_r; the target batch is B = sum_r (1 +   */
+/* ell_r) tokens; with survival a_{r,j} of extension (r, j) the          */
+/* objective is Theta(S) = (R + sum_{(r,j) in S} a_{r,j}) SPS(B).  The    */
+/* greedy: start at B = R, rank the candidate extensions globally by     */
+/* survival probability, admit them while Theta increases and stop when  */
+/* admitting the next one would not increase it; request r cannot admit  */
+/* position j+1 without j.  Readings: candidates are ranked by (a desc,  */
+/* position asc, request asc) -- a_{r,j} = prod_{i<=j} c_{r,i} never     */
+/* increases along a request, so this order keeps every prefix whole;   */
+/* "increases" is strict.                                                */
+/* a [R, K] (position k = 0..K-1 is extension k of request r),          */
+/* sps [R * (K + 1) + 1] = SPS(B) for B = 0 .. R (K + 1).               */
+/* Outputs ell [R] and *theta = Theta of the admitted set; margin =     */
+/* the smallest relative gap |Theta_next - Theta| / Theta over every    */
+/* admission test made (the stopping one included).                     */
+/* ------------------------------------------------------------------ */
+typedef struct {
+  double a;
+  int k, r;
+} sched_cand;
+
+static int sched_before(const sched_cand* x, const sched_cand* y) {
+  if (x->a != y->a) return x->a > y->a;
+  if (x->k != y->k) return x->k < y->k;
+  return x->r < y->r;
+}
+
+int orc_schedule(const double* a, int R, int K, const double* sps, int32_t* ell, double* theta,
+                 double* margin) {
+  if (R <= 0 || K < 0) return -1;
+  const int n = R * K;
+  sched_cand* c = (sched_cand*)malloc(sizeof(sched_cand) * (size_t)(n > 0 ? n : 1));
+  if (!c) return -1;
+  for (int r = 0; r < R; ++r)
+    for (int k = 0; k < K; ++k) {
+      c[r * K + k].a = a[(int64_t)r * K + k];
+      c[r * K + k].k = k;
+      c[r * K + k].r = r;
+    }
+  /* insertion sort: plain and obviously ordered */
+  for (int i = 1; i < n; ++i) {
+    sched_cand x = c[i];
+    int p = i;
+    while (p > 0 && sched_before(&x, &c[p - 1])) {
+      c[p] = c[p - 1];
+      --p;
+    }
+    c[p] = x;
+  }
+  for (int r = 0; r < R; ++r) ell[r] = 0;
+  double sum = (double)R;
+  double th = sum * sps[R];
+  *margin = INFINITY;
+  for (int i = 0; i < n; ++i) {
+    const double next = (sum + c[i].a) * sps[R + i + 1];
+    *margin = fmin(*margin, fabs(next - th) / (th > 0.0 ? th : 1.0));
+    if (!(next > th)) break;
+    sum += c[i].a;
+    th = next;
+    ell[c[i].r] += 1;
+  }
+  *theta = th;
+  free(c);
+  return 0;
+}

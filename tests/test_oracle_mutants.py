@@ -51,6 +51,13 @@ MUTANTS = [
      ["test_walk_with_k_equal_V_is_the_full_head"]),
     ("uniform-offset", "+ 0.5) * (1.0 / 8388608.0)", "+ 1.0) * (1.0 / 8388608.0)",
      ["test_uniform_grid_and_word_selection"]),
+    ("schedule-batch-size-off-by-one", "const double next = (sum + c[i].a) * sps[R + i + 1];",
+     "const double next = (sum + c[i].a) * sps[R + i];",
+     ["test_schedule_stops_at_the_first_dip_of_a_jagged_curve",
+      "test_schedule_matches_exhaustive_search_when_theta_is_unimodal"]),
+    ("schedule-ranks-ascending", "if (x->a != y->a) return x->a > y->a;",
+     "if (x->a != y->a) return x->a < y->a;",
+     ["test_schedule_matches_exhaustive_search_when_theta_is_unimodal"]),
     ("verify-ratio-inverted", "fmin(1.0, pv[x] / qv[x])", "fmin(1.0, qv[x] / pv[x])",
      ["test_verify_commits_the_target_distribution"]),
     ("verify-resample-from-target", "z[v] = d > 0.0 ? log(d) : -INFINITY;",

@@ -485,3 +485,62 @@ def test_verify_greedy_draft_accepts_with_the_target_probability(orc):
     assert cnt[x] == 0
     keep = np.arange(V) != x
     assert _chi2_pvalue(cnt[keep], pr[keep] * rej.sum()) > 0.01
+
+
+# ------------------------------------------------------------------ scheduler
+def _survival(rng, R, K, lo=0.55, hi=0.98):
+    return np.cumprod(rng.uniform(lo, hi, (R, K)), axis=1)
+
+
+def test_schedule_constant_throughput_admits_everything(orc):
+    a = _survival(np.random.default_rng(70), 6, 5)
+    out = orc.schedule(a, np.full(6 * 6 + 1, 3.0))
+    assert np.all(out["ell"] == 5)
+    assert np.isclose(out["theta"], (6 + a.sum()) * 3.0)
+
+
+def test_schedule_fixed_token_budget_admits_nothing(orc):
+    """SPS(B) = s / B: Theta is s times the mean survival per verified token, and every
+    extension survives with probability below the baseline token's 1."""
+    R, K = 5, 4
+    a = _survival(np.random.default_rng(71), R, K)
+    sps = np.array([0.0] + [7.0 / B for B in range(1, R * (K + 1) + 1)])
+    out = orc.schedule(a, sps)
+    assert np.all(out["ell"] == 0)
+    assert np.isclose(out["theta"], 7.0)
+
+
+def test_schedule_matches_exhaustive_search_when_theta_is_unimodal(orc):
+    """For a fixed number of admitted tokens the best set is the top survivors, so with a
+    smooth, saturating SPS the greedy's Theta is the optimum over every set of prefixes
+    (checked by enumerating all (K+1)^R verify-length vectors)."""
+    import itertools
+    rng = np.random.default_rng(72)
+    R, K = 3, 4
+    for trial in range(20):
+        a = _survival(rng, R, K, 0.3, 0.99)
+        B0 = rng.uniform(3.0, 12.0)
+        sps = np.array([1000.0 / (1.0 + (B / B0) ** 2) for B in range(R * (K + 1) + 1)])
+        out = orc.schedule(a, sps)
+        best = -1.0
+        for ell in itertools.product(range(K + 1), repeat=R):
+            n = sum(ell)
+            th = (R + sum(a[r, :ell[r]].sum() for r in range(R))) * sps[R + n]
+            best = max(best, th)
+        assert np.isclose(out["theta"], best, rtol=1e-12), trial
+        # the reported Theta is the objective of the reported lengths
+        th = (R + sum(a[r, :out["ell"][r]].sum() for r in range(R))) * sps[R + out["ell"].sum()]
+        assert np.isclose(out["theta"], th, rtol=1e-12)
+
+
+def test_schedule_stops_at_the_first_dip_of_a_jagged_curve(orc):
+    """The greedy stops when the next admission would lower Theta, even if a larger batch
+    further on would be better (a jagged SPS, as profiled engines have)."""
+    R, K = 4, 4
+    a = np.full((R, K), 0.9) ** np.arange(1, K + 1)[None, :]
+    sps = np.full(R * (K + 1) + 1, 100.0)
+    sps[R + 2] = 60.0                                     # a dip at B = R + 2
+    out = orc.schedule(a, sps)
+    assert out["ell"].sum() == 1                          # admits one, refuses the second
+    assert out["ell"][0] == 1                             # ties go to the first request
+    assert 0.0 < out["margin"] < 1.0
