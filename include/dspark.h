@@ -318,6 +318,26 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
                   float target_temperature, uint64_t seed, int32_t* n_acc, int32_t* next_token,
                   float* accept_prob, dspark_stream_t stream);
 
+/* --------------------------------------------------------------------- */
+/* Load-aware prefix scheduler                                              */
+/* --------------------------------------------------------------------- */
+
+/* Verify lengths that maximise the target's throughput by the greedy rule.
+ * Source: DSpark explainer, "Hardware-aware prefix scheduling": with R
+ * requests, request r verifying a prefix of length ell_r and the target batch
+ * B = sum_r (1 + ell_r), the objective is Theta = (R + sum of the admitted
+ * extensions' survival) * SPS(B); start at B = R, rank candidate extensions
+ * globally by survival probability, admit them while Theta increases
+ * (strictly) and stop at the first one that would not.  Candidates are ranked
+ * by (survival desc, position asc, request asc), which keeps every prefix
+ * whole because survival never grows along a request.
+ *   a [R, K] survival of extension (r, k) (e.g. the confidence head's cumprod)
+ *   sps [sps_len] SPS(B) for B = 0 .. sps_len - 1, sps_len >= R (K + 1) + 1
+ * Outputs ell [R] (device) and theta (device scalar, may be NULL).  R * K <=
+ * 16384.  All arrays are device pointers; one kernel, no host synchronisation. */
+int dspark_schedule(dspark_ctx* ctx, const float* a, int R, int K, const float* sps, int sps_len,
+                    int32_t* ell, float* theta, dspark_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ EXPORTS = (
     "dspark_debug_set", "dspark_debug_trace", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
-    "dspark_markov_draft_noalloc", "dspark_verify",
+    "dspark_markov_draft_noalloc", "dspark_verify", "dspark_schedule",
 )
 
 
@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH):
         "dspark_markov_logits": [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P],
         "dspark_markov_draft_noalloc": [P, P, P, P, I, I, I, I, F, U64, P, P, P, P],
         "dspark_verify": [P, P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, F, F, U64, P, P, P, P],
+        "dspark_schedule": [P, P, I, I, P, I, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -303,6 +304,14 @@ def dspark_verify(ctx: Context, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_l
     _check(code, "dspark_verify")
 
 
+def dspark_schedule(ctx: Context, a, R, K, sps, ell, theta, stream=None):
+    code = ctx.lib.dspark_schedule(
+        ctx.handle, _ptr(a, (torch.float32,), "a"), R, K, _ptr(sps, (torch.float32,), "sps"),
+        int(sps.numel()), _ptr(ell, (torch.int32,), "ell"), _ptr(theta, (torch.float32,), "theta"),
+        _stream(stream, ctx.device))
+    _check(code, "dspark_schedule")
+
+
 def dspark_markov_draft_noalloc(U, W1, W2, anchors, B, K, V, r, temperature, seed, tokens,
                                 logprobs, device_status=None, stream=None):
     """Context-free draft that allocates no device memory (scratch compiled into the library).
@@ -411,6 +420,15 @@ def verify(ctx: Context, P, U, W1, W2, anchors, tokens, draft_logprobs, *, draft
                   draft_temperature, target_temperature, seed, n_acc, next_token, accept_prob,
                   stream)
     return dict(n_acc=n_acc, next_token=next_token, accept_prob=accept_prob)
+
+
+def schedule(ctx: Context, a, sps, stream=None) -> dict:
+    """Greedy load-aware verify lengths: survival a [R, K], SPS(B) table [>= R (K+1) + 1]."""
+    R, K = a.shape
+    ell = torch.empty(R, dtype=torch.int32, device=a.device)
+    theta = torch.empty(1, dtype=torch.float32, device=a.device)
+    dspark_schedule(ctx, a, R, K, sps, ell, theta, stream)
+    return dict(ell=ell, theta=theta)
 
 
 def markov_logits(ctx: Context, U, W1, W2, prev_tokens, *, temperature=1.0, h=None, Wg=None,

@@ -676,4 +676,21 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   return cuda_status(e);
 }
 
+int dspark_schedule(dspark_ctx* ctx, const float* a, int R, int K, const float* sps,
+                    int sps_len, int32_t* ell, float* theta, dspark_stream_t stream) {
+  if (a == nullptr || sps == nullptr || ell == nullptr) return DSPARK_ERR_INVALID_ARG;
+  if (R <= 0 || K < 0) return DSPARK_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(R) * K > dspark::kScheduleMaxCandidates || R > 65535 || K > 65535)
+    return DSPARK_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(sps_len) < static_cast<int64_t>(R) * (K + 1) + 1)
+    return DSPARK_ERR_INVALID_ARG;
+  int st;
+  if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
+  ctx->last_launches = 0;
+  cudaError_t e = dspark::launch_schedule(a, R, K, sps, ell, theta,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  ctx->last_launches = 1;
+  return cuda_status(e);
+}
+
 }  // extern "C"

@@ -155,6 +155,11 @@ cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream);
 cudaError_t launch_verify_race(const VerifyArgs& v, int num_sms, cudaStream_t stream,
                                int* launches);
 
+// ---- load-aware prefix scheduler (schedule.cu)
+constexpr int kScheduleMaxCandidates = 16384;  // R * K
+cudaError_t launch_schedule(const float* a, int R, int K, const float* sps, int32_t* ell,
+                            float* theta, cudaStream_t stream);
+
 cudaError_t launch_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors,
                               const int32_t* tokens, const uint16_t* w, float bias,
                               int with_markov, int B, int K, int d, int r, int V,
