@@ -66,6 +66,8 @@ def _bind(lib):
     lib.orc_verify.restype = i32
     lib.orc_schedule.argtypes = [P, i32, i32, P, P, P, P]
     lib.orc_schedule.restype = i32
+    lib.orc_accept_label.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f64, f64, P]
+    lib.orc_accept_label.restype = i32
     lib.orc_gate.argtypes = [P, P, i64, i32, i32, P]
     lib.orc_markov_draft.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, u64, i32, i32,
                                      P, P, P, P, P]
@@ -156,6 +158,28 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle verify rejected its arguments")
         return dict(n_acc=n_acc, next_token=nxt, accept_prob=accept_prob, margins=margins)
+
+    def accept_label(self, P, U, W1, W2, anchors, tokens, *, draft_temperature: float,
+                     target_temperature: float, H=None) -> np.ndarray:
+        """c*_k = 1 - TV(p^d_k, p^t_k) of every drafted position [B, K]."""
+        P = _c(P, np.float32)
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        assert P.shape == (B, K + 1, V)
+        r = 0 if W1 is None else W1.shape[1]
+        W1 = _c(W1, np.uint16) if r > 0 else np.zeros((V, 1), np.uint16)
+        W2 = _c(W2, np.uint16) if r > 0 else np.zeros((1, V), np.uint16)
+        anchors = _c(anchors, np.int32)
+        tokens = _c(tokens, np.int32)
+        H = _c(H, np.float64)
+        label = np.zeros((B, K), np.float64)
+        rc = self._lib.orc_accept_label(_ptr(P), _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors),
+                                        _ptr(H), _ptr(tokens), B, K, V, r,
+                                        float(draft_temperature), float(target_temperature),
+                                        _ptr(label))
+        if rc != 0:
+            raise ValueError("oracle accept_label rejected its arguments")
+        return label
 
     def schedule(self, a, sps) -> dict:
         """Greedy load-aware prefix scheduler: survival a [R, K], SPS(B) table

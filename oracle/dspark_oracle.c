@@ -852,3 +852,48 @@ int orc_schedule(const double* a, int R, int K, const double* sps, int32_t* ell,
   free(c);
   return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Acceptance label of each drafted position.                          */
+/* [EXPL] "Confidence-scheduled verification": the confidence head's    */
+/* training label is c*_k = 1 - TV(p^d_k, p^t_k) = 1 - 1/2 ||p^d_k -     */
+/* p^t_k||_1, the per-step acceptance probability under speculative     */
+/* decoding.  p^d_k: the draft head's softmax at position k given the   */
+/* drafted predecessor (one-hot at x_k when drafted greedily, Td = 0);  */
+/* p^t_k = softmax(P[b,k] / Tt) (one-hot at the argmax when Tt = 0).    */
+/* Computed as sum_v min(p^d_k(v), p^t_k(v)), which equals 1 - TV.     */
+/* P [B, K+1, V] (row K unused), tokens [B, K] -> label [B, K] (full).  */
+/* ------------------------------------------------------------------ */
+int orc_accept_label(const float* P, const float* U, const uint16_t* W1, const uint16_t* W2,
+                     const int32_t* anchors, const double* H, const int32_t* tokens, int B, int K,
+                     int V, int r, double Td, double Tt, double* label) {
+  if (B <= 0 || K <= 0 || V <= 0 || r < 0) return -1;
+  double* l = (double*)malloc(sizeof(double) * (size_t)V);
+  double* pv = (double*)malloc(sizeof(double) * (size_t)V);
+  double* qv = (double*)malloc(sizeof(double) * (size_t)V);
+  double* e = (double*)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+  int bad = (!l || !pv || !qv || !e);
+  for (int b = 0; b < B && !bad; ++b) {
+    int32_t prev = anchors[b];
+    for (int k = 0; k < K; ++k) {
+      const int32_t x = tokens[(int64_t)b * K + k];
+      if (prev < 0 || prev >= V || x < 0 || x >= V) {
+        bad = 1;
+        break;
+      }
+      calibrated_logits(U + ((int64_t)b * K + k) * V, W1, W2,
+                        H ? H + ((int64_t)b * K + k) * r : NULL, V, r, prev, e, l);
+      target_probs(P + ((int64_t)b * (K + 1) + k) * V, V, Tt, pv);
+      draft_probs(l, V, Td, x, qv);
+      double s = 0.0;
+      for (int v = 0; v < V; ++v) s += fmin(pv[v], qv[v]);
+      label[(int64_t)b * K + k] = s;
+      prev = x;
+    }
+  }
+  free(l);
+  free(pv);
+  free(qv);
+  free(e);
+  return bad ? -1 : 0;
+}

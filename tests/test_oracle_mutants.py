@@ -67,6 +67,11 @@ MUTANTS = [
     ("verify-bonus-row-before-the-window", "target_probs(P + ((int64_t)b * (K + 1) + L) * V, V, Tt, pv);",
      "target_probs(P + ((int64_t)b * (K + 1) + (L > 0 ? L - 1 : 0)) * V, V, Tt, pv);",
      ["test_verify_target_equal_to_draft_accepts_every_token"]),
+    ("label-overlap-by-max", "s += fmin(pv[v], qv[v]);", "s += fmax(pv[v], qv[v]);",
+     ["test_accept_label_special_cases", "test_accept_label_is_the_verifier_acceptance_rate"]),
+    ("label-predecessor-not-carried", "      label[(int64_t)b * K + k] = s;\n      prev = x;\n",
+     "      label[(int64_t)b * K + k] = s;\n",
+     ["test_accept_label_special_cases", "test_accept_label_is_the_verifier_acceptance_rate"]),
 ]
 
 

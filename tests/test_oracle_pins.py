@@ -544,3 +544,51 @@ def test_schedule_stops_at_the_first_dip_of_a_jagged_curve(orc):
     assert out["ell"].sum() == 1                          # admits one, refuses the second
     assert out["ell"][0] == 1                             # ties go to the first request
     assert 0.0 < out["margin"] < 1.0
+
+
+# ------------------------------------------------------------------ acceptance label
+def test_accept_label_is_the_verifier_acceptance_rate(orc):
+    """c*_k is the per-step acceptance probability: across requests sharing one head and
+    one target table, the verifier accepts position 0 at rate c*_0, and position 1 (given
+    position 0 survived, with its own predecessor) at the mean of c*_1 over those requests."""
+    N, V, K, r = 100_000, 40, 2, 8
+    U1, W1, W2, P1, drafted, out = _verify_case(orc, N, V, K, r, seed=91)
+    U = np.ascontiguousarray(np.broadcast_to(U1, (N, K, V)))
+    P = np.ascontiguousarray(np.broadcast_to(P1, (N, K + 1, V)))
+    anchors = np.full(N, 3, np.int32)
+    lab = orc.accept_label(P, U, W1, W2, anchors, drafted["tokens"], draft_temperature=1.0,
+                           target_temperature=1.0)
+    c0 = lab[0, 0]
+    assert np.allclose(lab[:, 0], c0)                      # same predecessor for everyone
+    rate0 = (out["n_acc"] >= 1).mean()
+    assert abs(rate0 - c0) < 4 * np.sqrt(c0 * (1 - c0) / N)
+    reached = out["n_acc"] >= 1
+    c1 = lab[reached, 1].mean()
+    rate1 = (out["n_acc"][reached] >= 2).mean()
+    assert abs(rate1 - c1) < 4 * np.sqrt(c1 * (1 - c1) / reached.sum())
+
+
+def test_accept_label_special_cases(orc):
+    V, K, r = 48, 3, 8
+    inp = make_inputs(92, 5, K, V, r, weight_std=0.5)
+    drafted = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=3)
+    prev = np.concatenate([inp.anchors[:, None], drafted["tokens"][:, :-1]], axis=1)
+    lg = orc.markov_logits(inp.U, inp.W1, inp.W2, prev)["logits"]
+    # the target equal to the draft: label 1
+    P = np.concatenate([lg, np.zeros((5, 1, V))], axis=1).astype(np.float32)
+    U32 = (P[:, :K] - (lg - inp.U)).astype(np.float32)
+    lab = orc.accept_label(P, U32, inp.W1, inp.W2, inp.anchors, drafted["tokens"],
+                           draft_temperature=1.0, target_temperature=1.0)
+    assert np.allclose(lab, 1.0, atol=1e-6)
+    # greedy draft: the label is the target probability of the drafted token
+    Pr = np.random.default_rng(93).standard_normal((5, K + 1, V)).astype(np.float32)
+    lab = orc.accept_label(Pr, inp.U, inp.W1, inp.W2, inp.anchors, drafted["tokens"],
+                           draft_temperature=0.0, target_temperature=1.0)
+    pt = special.softmax(Pr[:, :K].astype(np.float64), axis=-1)
+    assert np.allclose(lab, np.take_along_axis(pt, drafted["tokens"][..., None], -1)[..., 0],
+                       atol=1e-12)
+    # both greedy: 1 where the drafted token is the target's argmax, else 0
+    lab = orc.accept_label(Pr, inp.U, inp.W1, inp.W2, inp.anchors, drafted["tokens"],
+                           draft_temperature=0.0, target_temperature=0.0)
+    assert np.array_equal(lab, (drafted["tokens"] == Pr[:, :K].argmax(-1)).astype(np.float64))
+    assert np.all((lab >= 0) & (lab <= 1))
