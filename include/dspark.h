@@ -319,6 +319,37 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
                   float* accept_prob, dspark_stream_t stream);
 
 /* --------------------------------------------------------------------- */
+/* Acceptance label of each drafted position                               */
+/* --------------------------------------------------------------------- */
+
+/* c*_k = 1 - TV(p^d_k, p^t_k) = sum_v min(p^d_k(v), p^t_k(v)) for every
+ * drafted position.  Source: DSpark explainer, "Confidence-scheduled
+ * verification": the confidence head is trained on this label, the
+ * probability that the target accepts position k under speculative decoding.
+ *   P [B, K+1, V] fp32 target logits, laid out as for dspark_verify (row K is
+ *     not read); p^t_k = softmax(P[b,k] / target_temperature), one-hot at the
+ *     argmax (ties to the smaller id) when target_temperature == 0.  P must be
+ *     32-byte aligned.
+ *   U, W1, W2, anchors (and h, Wg, d when gated): the draft head's inputs;
+ *     p^d_k = softmax(l_k / draft_temperature) of its calibrated logits given
+ *     the drafted predecessor (one-hot at x_k when draft_temperature == 0).
+ *   tokens [B, K] drafted tokens; draft_logprobs [B, K] their log p^d_k(x_k)
+ *     as returned by the draft call at draft_temperature (required when it is
+ *     > 0: they supply the draft's normaliser).
+ * Output label [B, K] fp32 in [0, 1].  When both temperatures are positive
+ * the sum over the vocabulary runs in the draft kernel (one pass over U, W2
+ * and P); when either side is greedy the label is one probability.  Sizes
+ * within the context's B_max, K_max, V_max; V % 8 == 0.  Drafted tokens out of
+ * [0, V) are reported as DSPARK_ERR_DEVICE_OOB.  Device pointers; no host
+ * synchronisation. */
+int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
+                        const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
+                        const uint16_t* Wg, int d, const int32_t* tokens,
+                        const float* draft_logprobs, int B, int K, int V, int r,
+                        float draft_temperature, float target_temperature, float* label,
+                        dspark_stream_t stream);
+
+/* --------------------------------------------------------------------- */
 /* Load-aware prefix scheduler                                              */
 /* --------------------------------------------------------------------- */
 

@@ -32,7 +32,7 @@ EXPORTS = (
     "dspark_debug_set", "dspark_debug_trace", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
-    "dspark_markov_draft_noalloc", "dspark_verify", "dspark_schedule",
+    "dspark_markov_draft_noalloc", "dspark_verify", "dspark_schedule", "dspark_accept_label",
 )
 
 
@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH):
         "dspark_markov_draft_noalloc": [P, P, P, P, I, I, I, I, F, U64, P, P, P, P],
         "dspark_verify": [P, P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, F, F, U64, P, P, P, P],
         "dspark_schedule": [P, P, I, I, P, I, P, P, P],
+        "dspark_accept_label": [P, P, P, P, P, P, P, P, I, P, P, I, I, I, I, F, F, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -304,6 +305,18 @@ def dspark_verify(ctx: Context, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_l
     _check(code, "dspark_verify")
 
 
+def dspark_accept_label(ctx: Context, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_logprobs,
+                        B, K, V, r, draft_temperature, target_temperature, label, stream=None):
+    code = ctx.lib.dspark_accept_label(
+        ctx.handle, _ptr(P, (torch.float32,), "P"), _ptr(U, (torch.float32,), "U"),
+        _ptr(W1, _BF16, "W1"), _ptr(W2, _BF16, "W2"), _ptr(anchors, (torch.int32,), "anchors"),
+        _ptr(h, _BF16, "h"), _ptr(Wg, _BF16, "Wg"), d, _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(draft_logprobs, (torch.float32,), "draft_logprobs"), B, K, V, r,
+        float(draft_temperature), float(target_temperature), _ptr(label, (torch.float32,), "label"),
+        _stream(stream, ctx.device))
+    _check(code, "dspark_accept_label")
+
+
 def dspark_schedule(ctx: Context, a, R, K, sps, ell, theta, stream=None):
     code = ctx.lib.dspark_schedule(
         ctx.handle, _ptr(a, (torch.float32,), "a"), R, K, _ptr(sps, (torch.float32,), "sps"),
@@ -420,6 +433,18 @@ def verify(ctx: Context, P, U, W1, W2, anchors, tokens, draft_logprobs, *, draft
                   draft_temperature, target_temperature, seed, n_acc, next_token, accept_prob,
                   stream)
     return dict(n_acc=n_acc, next_token=next_token, accept_prob=accept_prob)
+
+
+def accept_label(ctx: Context, P, U, W1, W2, anchors, tokens, draft_logprobs=None, *,
+                 draft_temperature, target_temperature, h=None, Wg=None, stream=None):
+    """Acceptance label 1 - TV(draft, target) [B, K] of drafted tokens [B, K]."""
+    B, K, V = U.shape
+    r = _rank(W1)
+    label = torch.empty(B, K, dtype=torch.float32, device=U.device)
+    d = 0 if h is None else int(h.shape[-1])
+    dspark_accept_label(ctx, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_logprobs, B, K, V, r,
+                        draft_temperature, target_temperature, label, stream)
+    return label
 
 
 def schedule(ctx: Context, a, sps, stream=None) -> dict:

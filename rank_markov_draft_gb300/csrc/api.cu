@@ -41,6 +41,9 @@ struct dspark_ctx {
   float* d_v_Lq = nullptr;               // [B_max][V_max]
   float* d_v_lse_q = nullptr;            // [B_max]
   dspark::VerifyRec* d_v_rec = nullptr;  // [B_max][kVerifyMaxPieces]
+  // acceptance-label scratch
+  int32_t* d_l_prev = nullptr;           // [B_max * K_max] predecessors of the drafted tokens
+  float* d_l_offq2 = nullptr;            // [B_max * K_max] log2 q offsets
   float* d_topk_part_v = nullptr;
   uint32_t bar_counter = 0;              // host copy of the grid-barrier counter
   uint32_t epoch = 0;                    // last key epoch used
@@ -182,11 +185,21 @@ int run_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int 
   return cuda_status(e);
 }
 
+// Inputs of the draft kernel's acceptance-label mode (whole call; chunked below).
+struct LabelIn {
+  const float* target;  // [B, K+1, V]
+  const float* lse_t;   // [B, K+1]
+  const float* offq2;   // [B, K]
+  float* label;         // [B, K]
+  float target_scale2;  // log2(e) / Tt
+};
+
 // The persistent draft kernel over chunks of 128 requests.
 int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, const uint16_t* W2,
               const int32_t* anchors, const int32_t* prev, const float* H, int B, int K, int V,
               int r, float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
-              float* logits, float* lse, const dspark_conf_args* conf, cudaStream_t stream) {
+              float* logits, float* lse, const dspark_conf_args* conf, cudaStream_t stream,
+              const LabelIn* lab = nullptr) {
   const int n_tiles = (V + dspark::kDraftTileV - 1) / dspark::kDraftTileV;
   const int grid = n_tiles < ctx->num_sms ? n_tiles : ctx->num_sms;
   const float inv_t = temperature > 0.f ? 1.0f / temperature : 1.0f;
@@ -224,6 +237,13 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.logprobs = logprobs ? logprobs + o : nullptr;
     p.logits = logits ? logits + o * V : nullptr;
     p.lse = lse ? lse + o : nullptr;
+    if (lab != nullptr) {
+      p.target = lab->target + static_cast<size_t>(b0) * (K + 1) * V;
+      p.lse_t = lab->lse_t + static_cast<size_t>(b0) * (K + 1);
+      p.offq2 = lab->offq2 + o;
+      p.label = lab->label + o;
+      p.target_scale2 = lab->target_scale2;
+    }
     if (conf != nullptr) {
       p.conf_h = conf->h + o * conf->d;
       p.conf_w = conf->w;
@@ -349,7 +369,9 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
                 cudaSuccess &&
             cudaMalloc(&ctx->d_v_lse_q, sizeof(float) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_rec, sizeof(dspark::VerifyRec) * B_max * dspark::kVerifyMaxPieces) ==
-                cudaSuccess;
+                cudaSuccess &&
+            cudaMalloc(&ctx->d_l_prev, sizeof(int32_t) * rows) == cudaSuccess &&
+            cudaMalloc(&ctx->d_l_offq2, sizeof(float) * rows) == cudaSuccess;
   ok = ok && cudaMemset(ctx->d_status, 0, sizeof(int)) == cudaSuccess &&
        cudaMemset(ctx->d_bar, 0, sizeof(uint32_t)) == cudaSuccess &&
        cudaMemset(ctx->d_keys, 0, sizeof(unsigned long long) * K_max * dspark::kBatchChunk) ==
@@ -382,6 +404,8 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_v_Lq);
   cudaFree(ctx->d_v_lse_q);
   cudaFree(ctx->d_v_rec);
+  cudaFree(ctx->d_l_prev);
+  cudaFree(ctx->d_l_offq2);
   cudaFree(ctx->d_topk_part_v);
   delete ctx;
   return DSPARK_OK;
@@ -674,6 +698,67 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   e = dspark::launch_verify_race(v, ctx->num_sms, s, &n);
   ctx->last_launches += n;
   return cuda_status(e);
+}
+
+int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
+                        const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
+                        const uint16_t* Wg, int d, const int32_t* tokens,
+                        const float* draft_logprobs, int B, int K, int V, int r,
+                        float draft_temperature, float target_temperature, float* label,
+                        dspark_stream_t stream) {
+  if (P == nullptr) return DSPARK_ERR_INVALID_ARG;
+  int st = check_draft_args(U, W1, W2, anchors, B, K, V, r, draft_temperature, tokens, label);
+  if (st != DSPARK_OK) return st;
+  if (!(target_temperature >= 0.f) || target_temperature > 3.0e38f) return DSPARK_ERR_INVALID_ARG;
+  if (draft_temperature > 0.f && draft_logprobs == nullptr) return DSPARK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(P) & 31u) != 0) return DSPARK_ERR_INVALID_ARG;
+  const bool gated = (h != nullptr) || (Wg != nullptr);
+  if (gated && (st = check_gate_args(h, Wg, d, r)) != DSPARK_OK) return st;
+  if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
+  if (B > ctx->B_max || K > ctx->K_max || V > ctx->V_max) return DSPARK_ERR_CAPACITY;
+  ctx->last_launches = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (gated) {
+    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+    if (st != DSPARK_OK) return st;
+  }
+  // the target's normaliser (or argmax) of rows k < K
+  cudaError_t e = dspark::launch_target_stats(P, nullptr, B, K, K - 1, V, target_temperature,
+                                              ctx->d_v_lse_t, ctx->d_v_argmax_t, s);
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  ctx->last_launches += 1;
+  dspark::LabelPrepArgs a{};
+  a.P = P;
+  a.U = U;
+  a.W1 = W1;
+  a.W2 = W2;
+  a.H = gated ? ctx->d_H : nullptr;
+  a.anchors = anchors;
+  a.tokens = tokens;
+  a.logq = draft_logprobs;
+  a.lse_t = ctx->d_v_lse_t;
+  a.argmax_t = ctx->d_v_argmax_t;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.r = r;
+  a.inv_td = draft_temperature > 0.f ? 1.0f / draft_temperature : 0.f;
+  a.inv_tt = target_temperature > 0.f ? 1.0f / target_temperature : 0.f;
+  a.prev = ctx->d_l_prev;
+  a.offq2 = ctx->d_l_offq2;
+  a.label = label;
+  a.status = ctx->d_status;
+  if ((e = dspark::launch_label_prep(a, s)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  ctx->last_launches += 1;
+  if (draft_temperature > 0.f && target_temperature > 0.f) {
+    LabelIn lab{P, ctx->d_v_lse_t, ctx->d_l_offq2, label,
+                1.4426950408889634f / target_temperature};
+    st = run_draft(ctx, dspark::kModeLabel, U, W1, W2, anchors, ctx->d_l_prev,
+                   gated ? ctx->d_H : nullptr, B, K, V, r, draft_temperature, 0, nullptr, nullptr,
+                   nullptr, nullptr, nullptr, s, &lab);
+    if (st != DSPARK_OK) return st;
+  }
+  return DSPARK_OK;
 }
 
 int dspark_schedule(dspark_ctx* ctx, const float* a, int R, int K, const float* sps,

@@ -33,6 +33,16 @@
 //   * after the last step, CTA c reduces request c's partials into tokens and
 //     log-probabilities and runs the fused confidence head.
 //
+// Teacher-forced modes take every position's predecessor from the caller, so
+// positions do not depend on one another: the next position's embeddings are
+// gathered as soon as the MMAs are done with the current ones and the grid
+// barrier is waited on only before the final reduction.  The label mode
+// (DSpark explainer, "Confidence-scheduled verification": c*_k = 1 - TV of the
+// draft head's and the target's distributions) streams the target's row
+// beside U and sums 2^min(log2 q(v), log2 p(v)) over the vocabulary, both
+// normalisers known beforehand (the target's from a row scan, the draft's
+// from its own log-probability of the drafted token).
+//
 // Sampling epilogue (an exact draw from softmax(l / T) in two stages over
 // 16-token blocks; each thread's 16 columns of a tile are one block beta):
 //   y = l * log2(e) / T, w = 2^(y - m) (shared with the log-sum-exp), and the
@@ -94,7 +104,7 @@ constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
 static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103 limit");
 static_assert((kNumAcc & (kNumAcc - 1)) == 0, "accumulator count must be a power of two");
 static_assert((2 * kNumW2Stages + 2 * kNumUStagesSmall + 2 * kNumAcc + 5) * 8 + 2 * kMaxK * 4 +
-                      kRows * 8 <=
+                      kRows * 8 + 16 <=
                   kBarRegion,
               "barrier region too small");
 
@@ -240,6 +250,7 @@ __device__ __forceinline__ void lse_merge(float& ma, float& sa, float mb, float 
 template <int MODE, bool COPIES>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
+  constexpr bool kTF = MODE == kModeTeacherForced || MODE == kModeLabel;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -262,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   // best key (epoch | score | token) any thread of this CTA reached for each
   // request in the current step: a lower bound on the step's winner
   unsigned long long* s_bound = reinterpret_cast<unsigned long long*>(s_conf + kMaxK);  // [128]
+  uint32_t* s_sink = reinterpret_cast<uint32_t*>(s_bound + kRows);  // scratch word (U releases)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x, ncta = gridDim.x;
@@ -450,15 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (k == 0) {
           int32_t tok = 0;
           if (grow < p.B) {
-            tok = (MODE == kModeTeacherForced) ? __ldg(p.prev + static_cast<size_t>(grow) * p.K)
-                                               : __ldg(p.anchors + grow);
+            tok = kTF ? __ldg(p.prev + static_cast<size_t>(grow) * p.K) : __ldg(p.anchors + grow);
             if (tok < 0 || tok >= p.V) {
               record_error(p.status, kStatusDeviceOob);
               tok = 0;
             }
           }
           if (!fail) gather_embeddings(sA, p, 0, etid, tok);
-        } else if (MODE != kModeTeacherForced && grow < p.B) {
+        } else if (!kTF && grow < p.B) {
           cp_async_wait_all();  // the speculative copy must land before any rewrite
           const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + grow);
           if (key != spec_key) {  // the winner changed after the speculative gather
@@ -481,7 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
 
       // ---- stream the step's tiles
-      float m2 = -INFINITY, sum = 0.f;
+      float m2 = (MODE == kModeLabel) ? 0.f : -INFINITY, sum = 0.f;  // label: a plain sum
+      float offq2 = 0.f, offp2 = 0.f;  // label: log2 q = l * scale2 + offq2, log2 p likewise
+      const float* trow = nullptr;     // label: this request's target row at position k
+      if (MODE == kModeLabel && row_ok) {
+        const size_t o = static_cast<size_t>(b) * p.K + k;
+        offq2 = __ldg(p.offq2 + o);
+        offp2 = -__ldg(p.lse_t + o + b) * kLog2e;  // target row b * (K + 1) + k
+        trow = p.target + (o + b) * static_cast<size_t>(p.V);
+      }
       float yb = -INFINITY, lb = 0.f;  // best score (G, or y when greedy) and its logit
       int vb = 0x7FFFFFFF;
       unsigned long long bkey = 0ull;  // key of (yb, vb)
@@ -508,6 +527,19 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               kpre > gkey)
             gkey = kpre;
           if (((tt + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
+        }
+        float pt[16];  // label: the target logits of this thread's 16 columns
+        if (MODE == kModeLabel) {
+          const int v0 = (t_begin + t) * kTileV + g * 16;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (row_ok && v0 + 8 * h + 8 <= p.V) {  // V is a multiple of 8
+              ld_nc_v8(trow + v0 + 8 * h, pt + 8 * h);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) pt[8 * h + j] = -INFINITY;
+            }
+          }
         }
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
         ok = ok && mbar_wait(&u_full[su], uph, p.timeout_ns, abort_flag);
@@ -543,11 +575,32 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&acc_empty[buf]);
-          mbar_arrive(&u_empty[su]);
-        }
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);  // tcgen05.wait::ld returned the values
+        arrive_after_reads(&u_empty[su],
+                           __float_as_uint(uval[0]) ^ __float_as_uint(uval[4]) ^
+                               __float_as_uint(uval[8]) ^ __float_as_uint(uval[12]),
+                           s_sink, lane);
         if (!row_ok) continue;
+
+        if (MODE == kModeLabel) {
+          // sum of min(q, p) over the thread's columns (columns past V: p = 0)
+          const float2 sq = make_float2(scale2, scale2), oq = make_float2(offq2, offq2);
+          const float2 sp = make_float2(p.target_scale2, p.target_scale2);
+          const float2 op = make_float2(offp2, offp2);
+          float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
+                                         make_float2(__uint_as_float(acc[j]),
+                                                     __uint_as_float(acc[j + 1])));
+            const float2 aq = __ffma2_rn(lj, sq, oq);
+            const float2 ap = __ffma2_rn(make_float2(pt[j], pt[j + 1]), sp, op);
+            acc2 = __fadd2_rn(acc2, make_float2(ex2_approx(fminf(aq.x, ap.x)),
+                                                ex2_approx(fminf(aq.y, ap.y))));
+          }
+          sum += acc2.x + acc2.y;
+          continue;
+        }
 
         const int vbase = (t_begin + t) * kTileV + g * 16;
         const bool full_chunk = vbase + 16 <= p.V;  // warp-uniform
@@ -721,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
         }
         unsigned long long key = 0ull;
-        if (MODE != kModeTeacherForced && best_v != 0x7FFFFFFF) {
+        if (!kTF && best_v != 0x7FFFFFFF) {
           key = make_key(p.epoch, best_s, best_v);
           atomicMax(p.keys + k * kRows + b, key);
           if (key >= gkey && k + 1 < p.K) {
@@ -761,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           const int grow = (etid >> 2) & (rpc - 1);
           int32_t tok = 0;
           if (grow < p.B) {
-            if (MODE == kModeTeacherForced) {
+            if (kTF) {
               tok = __ldg(p.prev + static_cast<size_t>(grow) * p.K + k + 1);
               if (tok < 0 || tok >= p.V) {
                 record_error(p.status, kStatusDeviceOob);
@@ -786,10 +839,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
       }
 
-      // ---- grid barrier (bounded)
+      // ---- grid barrier (bounded); teacher-forced positions are independent, so
+      // those modes wait only before the final reduction
       bool bar_fail = false;
       if (etid == 0) trace_stamp(p, cta, k, 4);
-      if (etid == 0 && !fail) {
+      if (etid == 0 && !fail && (!kTF || k + 1 == p.K)) {
         const uint32_t target = p.bar_base + static_cast<uint32_t>((k + 1) * ncta);
         uint64_t deadline = 0;
         for (uint32_t it = 0;; ++it) {
@@ -824,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         for (int k = e; k < p.K; k += kEpiWarps) {
           const DraftPartial* src = p.partials + (static_cast<size_t>(k) * kRows + bb) * ncta;
           const unsigned long long gkey =
-              (MODE == kModeTeacherForced) ? 0ull : __ldcg(p.keys + k * kRows + bb);
+              kTF ? 0ull : __ldcg(p.keys + k * kRows + bb);
           float M = -INFINITY, S = 0.f, lwin = 0.f;
           int found = 0;
           for (int c = lane; c < ncta; c += 32) {
@@ -832,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             float m2, s, lbest;
             load_partial(src + c, key, m2, s, lbest);
             lse_merge(M, S, m2, s);
-            if (MODE != kModeTeacherForced && key == gkey) {
+            if (!kTF && key == gkey) {
               lwin = lbest;
               found = 1;
             }
@@ -850,6 +904,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             const size_t o = static_cast<size_t>(bb) * p.K + k;
             if (MODE == kModeTeacherForced) {
               p.lse[o] = lse_nat;
+            } else if (MODE == kModeLabel) {
+              const float tot = (M == -INFINITY) ? 0.f : S * exp2f(M);
+              p.label[o] = fminf(fmaxf(tot, 0.f), 1.f);
             } else {
               int v = key_token(gkey);
               if (who == 0 || key_epoch(gkey) != p.epoch || v < 0 || v >= p.V) {
@@ -862,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
           }
         }
-        if (MODE != kModeTeacherForced && p.conf != nullptr) {
+        if (!kTF && p.conf != nullptr) {
           named_bar_sync(kEpiBarrier, kEpiThreads);
           const int d = p.conf_d;
           for (int k = e; k < p.K; k += kEpiWarps) {
@@ -928,6 +985,10 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
     case kModeTeacherForced:
       fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, true>)
                   : reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, false>);
+      break;
+    case kModeLabel:
+      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeLabel, true>)
+                  : reinterpret_cast<const void*>(&draft_kernel<kModeLabel, false>);
       break;
     default: return cudaErrorInvalidValue;
   }

@@ -65,6 +65,12 @@ struct DraftParams {
   int debug_skip_cta;       // fault injection: CTA skipping its step-0 arrival (-1: none)
   unsigned long long* trace;  // optional phase timestamps [grid][K][kTraceSlots] (null: off)
   uint64_t timeout_ns;      // per-wait limit
+  // acceptance-label mode (null otherwise)
+  const float* target;      // [B, K+1, V] (chunk) target logits, 32-byte aligned rows
+  const float* lse_t;       // [B, K+1] (chunk) log sum_v exp(target / Tt)
+  const float* offq2;       // [B, K] (chunk) log2 q(v) = l(v) * log2(e) / Td + offq2
+  float* label;             // [B, K] (chunk) 1 - TV(q, p)
+  float target_scale2;      // log2(e) / Tt
 };
 
 struct DraftArgs {
@@ -73,7 +79,7 @@ struct DraftArgs {
   DraftParams p;
 };
 
-enum DraftMode { kModeSample = 0, kModeGreedy = 1, kModeTeacherForced = 2 };
+enum DraftMode { kModeSample = 0, kModeGreedy = 1, kModeTeacherForced = 2, kModeLabel = 3 };
 
 int draft_smem_bytes();
 int draft_threads();
@@ -151,9 +157,38 @@ struct VerifyArgs {
   VerifyRec* rec;             // [B, kVerifyMaxPieces]
 };
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches);
+// Log-sum-exp of P / Tt (argmax when greedy) of the rows (b, k <= min(ell[b], kmax))
+// of P [B, K+1, V]; ell null: every request's rows up to kmax.
+cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,
+                                float target_temperature, float* lse_t, int32_t* argmax_t,
+                                cudaStream_t stream);
 cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream);
 cudaError_t launch_verify_race(const VerifyArgs& v, int num_sms, cudaStream_t stream,
                                int* launches);
+
+// ---- acceptance label (label.cu)
+// One warp per drafted position: its predecessor, the offset that turns the
+// draft head's logits into log2 q (draft T > 0), and the label itself where one
+// side is greedy (the other cases are summed by the draft kernel's label mode).
+struct LabelPrepArgs {
+  const float* P;             // [B, K+1, V]
+  const float* U;             // [B, K, V]
+  const uint16_t* W1;         // [V, r]
+  const uint16_t* W2;         // [r, V]
+  const float* H;             // [B, K, r] or null
+  const int32_t* anchors;     // [B]
+  const int32_t* tokens;      // [B, K]
+  const float* logq;          // [B, K] (draft T > 0)
+  const float* lse_t;         // [B, K+1] (target T > 0)
+  const int32_t* argmax_t;    // [B, K+1] (target T = 0)
+  int B, K, V, r;
+  float inv_td, inv_tt;       // 0: greedy
+  int32_t* prev;              // [B, K] out
+  float* offq2;               // [B, K] out (draft T > 0)
+  float* label;               // [B, K] out where one side is greedy
+  int* status;
+};
+cudaError_t launch_label_prep(const LabelPrepArgs& a, cudaStream_t stream);
 
 // ---- load-aware prefix scheduler (schedule.cu)
 constexpr int kScheduleMaxCandidates = 16384;  // R * K

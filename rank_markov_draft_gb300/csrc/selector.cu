@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_
   __shared__ uint32_t s_floor;  // ordered bits of the best k-th value held by a full list
   __shared__ uint32_t s_mth[kTopkWarps];  // ordered bits of each warp's m-th best value
   __shared__ int s_abort;
+  __shared__ uint32_t s_sink;  // scratch word of the stage releases
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = a.rows * a.pieces;
   volatile int* abort_flag = &s_abort;
@@ -215,8 +216,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_stream_kernel(const __grid_
         x[j] = (off < n) ? *reinterpret_cast<const float4*>(chunk + off)
                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // the slice is in registers: free the stage
+      // free the stage once every lane's slice is in registers
+      arrive_after_reads(&empty[s],
+                         __float_as_uint(x[0].x) ^ __float_as_uint(x[1].x) ^
+                             __float_as_uint(x[2].x) ^ __float_as_uint(x[3].x),
+                         &s_sink, lane);
       float mx = fmaxf(fmaxf(fmaxf(x[0].x, x[0].y), fmaxf(x[0].z, x[0].w)),
                        fmaxf(fmaxf(x[1].x, x[1].y), fmaxf(x[1].z, x[1].w)));
       mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(x[2].x, x[2].y), fmaxf(x[2].z, x[2].w)),

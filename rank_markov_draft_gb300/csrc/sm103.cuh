@@ -25,6 +25,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Record the first device error of a launch (later ones are dropped).
+// 32-byte read-only global load (sm_100+); the address must be 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const float* src, float* x) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]),
+                 "=f"(x[6]), "=f"(x[7])
+               : "l"(src));
+}
+
 __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, kStatusOk, code);
 }
@@ -44,6 +52,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       "{\n\t.reg .b64 st;\n\t"
       "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
       : "memory");
+}
+
+// Release a ring slot that this warp has just read with shared-memory loads,
+// from lane 0 (call on every lane).  The arrive's release orders lane 0's own
+// accesses only; a warp's loads can still be in flight for other lanes (and
+// behind global loads in the same queue) when the arrive, handled by the
+// mbarrier unit, completes -- and the producer's next copy then overwrites
+// data not yet read.  So lane 0 first stores `dep`, a value computed from one
+// register of each of the warp's loads, to a shared scratch word: that store
+// cannot issue before the loads have written back for every lane (a warp issues
+// in order and a register's readiness is tracked for the whole warp), and the
+// release keeps the store before the arrive.
+__device__ __forceinline__ void arrive_after_reads(uint64_t* bar, uint32_t dep, uint32_t* sink,
+                                                   int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_addr(sink)), "r"(dep) : "memory");
+    mbar_arrive(bar);
+  }
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {

@@ -65,11 +65,11 @@ __device__ __forceinline__ void lse2_merge(float& ma, float& sa, float mb, float
 }
 
 __global__ void __launch_bounds__(kStatsThreads) verify_stats_kernel(
-    const float* __restrict__ P, const int32_t* __restrict__ ell, int K, int V, float inv_tt,
-    int greedy, float* __restrict__ lse_t, int32_t* __restrict__ argmax_t) {
+    const float* __restrict__ P, const int32_t* __restrict__ ell, int K, int kmax, int V,
+    float inv_tt, int greedy, float* __restrict__ lse_t, int32_t* __restrict__ argmax_t) {
   const int row = blockIdx.x;             // b * (K + 1) + k
   const int b = row / (K + 1), k = row - b * (K + 1);
-  const int L = ell ? min(max(__ldg(ell + b), 0), K) : K;
+  const int L = min(ell ? min(max(__ldg(ell + b), 0), K) : K, kmax);
   if (k > L) return;
   const float4* p4 = reinterpret_cast<const float4*>(P + static_cast<size_t>(row) * V);
   const int n4 = V / 4;
@@ -396,15 +396,23 @@ __global__ void verify_finish_kernel(const __grid_constant__ RaceIn a, int32_t* 
 
 }  // namespace
 
+cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,
+                                float target_temperature, float* lse_t, int32_t* argmax_t,
+                                cudaStream_t stream) {
+  const int greedy_t = target_temperature > 0.f ? 0 : 1;
+  const float inv_tt = greedy_t ? 1.f : 1.0f / target_temperature;
+  verify_stats_kernel<<<B * (K + 1), kStatsThreads, 0, stream>>>(P, ell, K, kmax, V, inv_tt,
+                                                                 greedy_t, lse_t, argmax_t);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches) {
   *launches = 0;
   const int greedy_t = v.target_temperature > 0.f ? 0 : 1;
   const int greedy_d = v.draft_temperature > 0.f ? 0 : 1;
   const float inv_tt = greedy_t ? 1.f : 1.0f / v.target_temperature;
-  const float inv_td = greedy_d ? 1.f : 1.0f / v.draft_temperature;
-  verify_stats_kernel<<<v.B * (v.K + 1), kStatsThreads, 0, stream>>>(
-      v.P, v.ell, v.K, v.V, inv_tt, greedy_t, v.lse_t, v.argmax_t);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_target_stats(v.P, v.ell, v.B, v.K, v.K, v.V, v.target_temperature,
+                                      v.lse_t, v.argmax_t, stream);
   if (e != cudaSuccess) return e;
   ++*launches;
   verify_accept_kernel<<<(v.B + 3) / 4, 128, 0, stream>>>(
