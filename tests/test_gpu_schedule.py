@@ -63,8 +63,12 @@ def test_draft_schedule_verify_chain(dsp):
     torch.cuda.synchronize()
     assert dsp.status() == 0
     ell, n = host(sc["ell"]), host(out["n_acc"])
-    ref = oracle.schedule(host(dr["cumprod"]).astype(np.float64), host(sps).astype(np.float64))
-    if ref["margin"] > 1e-5:
+    # the oracle's own chain: its draft, its confidence, its schedule
+    od = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=3)
+    oc = oracle.confidence(inp.h, inp.W1, inp.anchors, od["tokens"], inp.w_conf, bias=1.5,
+                           threshold=0.3)
+    ref = oracle.schedule(oc["cumprod"], host(sps).astype(np.float64))
+    if np.array_equal(host(dr["tokens"]), od["tokens"]) and ref["margin"] > 1e-5:
         assert np.array_equal(ell, ref["ell"])
     assert np.all(n <= ell)
     assert np.all(host(out["accept_prob"])[np.arange(K)[None, :] >= ell[:, None]] == -1.0)

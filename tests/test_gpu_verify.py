@@ -1,7 +1,8 @@
 """GPU parity of speculative verification (dspark_verify) against the fp64 oracle.
 
-The drafted tokens and their log-probabilities come from the GPU draft; the
-oracle recomputes q from the draft head's inputs in fp64.  Accepted lengths
+The drafted tokens and their log-probabilities come from the oracle's draft and
+are handed to both sides (no GPU output enters the oracle); the oracle
+recomputes q from the draft head's inputs in fp64.  Accepted lengths
 and next tokens must match wherever the oracle's smallest decision margin
 (|u - min(1, p/q)| of every acceptance test, and the draw's block-race
 margin) exceeds 1e-3.
@@ -32,15 +33,15 @@ def _target_logits(rng, U, noise=0.8):
 
 def _run(dsp, inp, P, Td, Tt, seed, ell=None, gated=False):
     args = dict(h=bf(inp.h) if gated else None, Wg=bf(inp.Wg) if gated else None)
-    dr = binding.markov_draft(dsp, dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
-                              temperature=Td, seed=seed, **args)
+    H = oracle.gate(inp.h, inp.Wg) if gated else None
+    dr = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=Td, seed=seed, H=H)
     out = binding.verify(dsp, dev(P), dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
-                         dr["tokens"], dr["logprobs"], draft_temperature=Td,
-                         target_temperature=Tt, seed=seed + 1,
+                         dev(dr["tokens"]), dev(dr["logprobs"].astype(np.float32)),
+                         draft_temperature=Td, target_temperature=Tt, seed=seed + 1,
                          ell=dev(ell) if ell is not None else None, **args)
     torch.cuda.synchronize()
     assert dsp.status() == 0
-    return host(dr["tokens"]), {k: host(v) for k, v in out.items()}
+    return dr["tokens"], {k: host(v) for k, v in out.items()}
 
 
 def _check(inp, P, tokens, out, Td, Tt, seed, ell=None, H=None, requests=None):
