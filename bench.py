@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 
 METRIC = "Markov-head draft tokens/s at B=128 K=16 V=151936; % of HBM roofline"
 VERIFY_METRIC = "verified draft tokens/s (speculative verification) at B=128 K=16 V=151936"
+LABEL_METRIC = "acceptance labels/s (1 - TV of draft and target) at B=128 K=16 V=151936"
 L2_FLUSH_BYTES = 512 << 20       # larger than the 129 MB L2
 CONF_THRESHOLD = 0.3
 
@@ -53,6 +54,9 @@ WORKLOADS = {
     "tiny": (0, "tiny: B=1 K=4 V=4096 r=256"),
     "verify": (2, "speculative verification of the serving batch: B=128 K=16 V=151936 r=256, "
                   "synthetic target logits (draft base logits + N(0,1)), T_draft = T_target = 1"),
+    "label": (2, "acceptance labels of the serving batch's drafted block: B=128 K=16 V=151936 "
+                 "r=256, synthetic target logits (draft base logits + N(0,1)), "
+                 "T_draft = T_target = 1"),
 }
 VERIFY_TARGET_SEED = 2002
 
@@ -63,6 +67,17 @@ def verify_bytes(c: dict) -> int:
     embedding row and its target row again."""
     B, K, V, r = c["B"], c["K"], c["V"], c["r"]
     return B * (K + 1) * V * 4 + r * V * 2 + B * V * 4 + B * r * 2 + B * V * 4
+
+
+def label_bytes(c: dict) -> int:
+    """Bytes the labels of a drafted block must move at least once: every base-logit
+    row and target row of the K positions, W2 once, the gathered embeddings."""
+    B, K, V, r = c["B"], c["K"], c["V"], c["r"]
+    return 2 * B * K * V * 4 + r * V * 2 + B * K * r * 2
+
+
+def metric_of(workload: str) -> str:
+    return {"verify": VERIFY_METRIC, "label": LABEL_METRIC}.get(workload, METRIC)
 
 
 def algorithmic_bytes(cfg: int, c: dict) -> int:
@@ -283,6 +298,28 @@ def verify_cpu_baseline(inp, c, target_s, dtok):
                       f"(fp64 oracle, {threads} OpenMP threads, {spent:.1f} s)"}
 
 
+def label_cpu_baseline(inp, c, target_s, dtok):
+    """The fp64 oracle's labels of whole requests, timed one after the other."""
+    import oracle
+    from synth import target_logits
+    oracle.build()
+    threads = oracle.max_threads()
+    K, B = c["K"], c["B"]
+    tokens = dtok.cpu().numpy() if hasattr(dtok, "cpu") else dtok
+    P = target_logits(VERIFY_TARGET_SEED, inp.U)
+    done, spent = 0, 0.0
+    while spent < target_s and done < B:
+        sl = slice(done, done + 1)
+        t0 = time.perf_counter()
+        oracle.accept_label(P[sl], inp.U[sl], inp.W1, inp.W2, inp.anchors[sl], tokens[sl],
+                            draft_temperature=1.0, target_temperature=1.0)
+        spent += time.perf_counter() - t0
+        done += 1
+    return {"value": done * K / spent, "unit": "labels/s", "cores": threads, "kind": "oracle",
+            "sample": f"labels of {done} of {B} requests x {K} positions "
+                      f"(fp64 oracle, {threads} OpenMP threads, {spent:.1f} s)"}
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: per step one request of the workload."""
     from synth import CONFIGS, config_inputs
@@ -294,8 +331,9 @@ def run_reference(args, rank, world):
     oracle.build()
     inp = config_inputs(cfg)
     K = c["K"]
-    if args.workload == "verify":
+    if args.workload in ("verify", "label"):
         # the oracle's draft of the batch's first requests, then their verification
+        # (or labels)
         from synth import target_logits
         P = target_logits(VERIFY_TARGET_SEED, inp.U)
         n = args.warmup + args.steps
@@ -305,8 +343,13 @@ def run_reference(args, rank, world):
 
         def one(b):
             t0 = time.perf_counter()
-            oracle.verify(P, inp.U, inp.W1, inp.W2, inp.anchors, toks, draft_temperature=1.0,
-                          target_temperature=1.0, seed=b, b0=b % c["B"], nb=1)
+            if args.workload == "verify":
+                oracle.verify(P, inp.U, inp.W1, inp.W2, inp.anchors, toks, draft_temperature=1.0,
+                              target_temperature=1.0, seed=b, b0=b % c["B"], nb=1)
+            else:
+                sl = slice(b % c["B"], b % c["B"] + 1)
+                oracle.accept_label(P[sl], inp.U[sl], inp.W1, inp.W2, inp.anchors[sl], toks[sl],
+                                    draft_temperature=1.0, target_temperature=1.0)
             return time.perf_counter() - t0
     else:
         def one(b):
@@ -318,17 +361,18 @@ def run_reference(args, rank, world):
         spent += one(args.warmup + i)
     value = args.steps * K / spent
     threads = oracle.max_threads()
+    unit = "labels/s" if args.workload == "label" else "tokens/s"
     line = {
-        "impl": "reference", "metric": VERIFY_METRIC if args.workload == "verify" else METRIC,
-        "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": metric_of(args.workload),
+        "value": value, "unit": "labels/s" if args.workload == "label" else "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * spent / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": desc, "B": c["B"], "K": K, "V": c["V"], "r": c["r"],
                    "sample_per_step": "1 request x K positions"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} steps x 1 request x {K} positions"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -374,6 +418,20 @@ def run_ours(args, rank, world, local):
             binding.dspark_selector_walk(ctx, cand, scores, anchors, A, B, K, V, r, 16, T, seed,
                                          tokens, logprobs, None, stream)
             return n + ctx.last_launches
+    elif args.workload == "label":
+        from synth import target_logits
+        W1, W2 = up(inp.W1, True), up(inp.W2, True)
+        P = up(target_logits(VERIFY_TARGET_SEED, inp.U))
+        dtok = torch.empty(B, K, dtype=torch.int32, device=dev)
+        dlp = torch.empty(B, K, dtype=torch.float32, device=dev)
+        binding.dspark_markov_draft(ctx, U, W1, W2, anchors, B, K, V, r, T, 77, dtok, dlp, None,
+                                    stream)
+        label = torch.empty(B, K, dtype=torch.float32, device=dev)
+
+        def step(seed):
+            binding.dspark_accept_label(ctx, P, U, W1, W2, anchors, None, None, 0, dtok, dlp, B, K,
+                                        V, r, T, T, label, stream)
+            return ctx.last_launches
     elif args.workload == "verify":
         from synth import target_logits
         W1, W2 = up(inp.W1, True), up(inp.W2, True)
@@ -445,7 +503,8 @@ def run_ours(args, rank, world, local):
 
     # -------- roofline of the dominant kernel
     peak, peak_kind = measured_peaks()
-    alg = verify_bytes(c) if args.workload == "verify" else algorithmic_bytes(cfg, c)
+    alg = (verify_bytes(c) if args.workload == "verify" else
+           label_bytes(c) if args.workload == "label" else algorithmic_bytes(cfg, c))
     kernel_ms = statistics.median(per_step_ms)
     achieved = alg / (kernel_ms / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -454,13 +513,15 @@ def run_ours(args, rank, world, local):
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
                 "kernel": ("verify step (target-row scan, acceptance, gather, one-position "
                            "draft logits, residual race)" if args.workload == "verify" else
+                           "label step (target-row scan, per-row offsets, draft kernel in "
+                           "label mode)" if args.workload == "label" else
                            "draft_kernel" if cfg != 4 else
                            "selector step (top-k scan, gate, pair scores, walk)"),
                 "median_launch_us": round(kernel_ms * 1000, 2)}
 
     # -------- end to end through the binding with host buffers
     e2e = None
-    if not args.skip_e2e and cfg != 4 and args.workload != "verify":
+    if not args.skip_e2e and cfg != 4 and args.workload not in ("verify", "label"):
         e2e = run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world)
 
     line = None
@@ -468,10 +529,12 @@ def run_ours(args, rank, world, local):
         cpu = None
         if not args.skip_cpu:
             cpu = (verify_cpu_baseline(inp, c, args.cpu_seconds, dtok) if args.workload == "verify"
-                   else cpu_baseline(inp, c, args.cpu_seconds))
+                   else label_cpu_baseline(inp, c, args.cpu_seconds, dtok)
+                   if args.workload == "label" else cpu_baseline(inp, c, args.cpu_seconds))
         line = {
-            "metric": VERIFY_METRIC if args.workload == "verify" else METRIC,
-            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "metric": metric_of(args.workload),
+            "value": round(value, 1), "unit": "labels/s" if args.workload == "label" else "tokens/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",

@@ -328,8 +328,7 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
  * probability that the target accepts position k under speculative decoding.
  *   P [B, K+1, V] fp32 target logits, laid out as for dspark_verify (row K is
  *     not read); p^t_k = softmax(P[b,k] / target_temperature), one-hot at the
- *     argmax (ties to the smaller id) when target_temperature == 0.  P must be
- *     32-byte aligned.
+ *     argmax (ties to the smaller id) when target_temperature == 0.
  *   U, W1, W2, anchors (and h, Wg, d when gated): the draft head's inputs;
  *     p^d_k = softmax(l_k / draft_temperature) of its calibrated logits given
  *     the drafted predecessor (one-hot at x_k when draft_temperature == 0).
@@ -339,9 +338,9 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
  * Output label [B, K] fp32 in [0, 1].  When both temperatures are positive
  * the sum over the vocabulary runs in the draft kernel (one pass over U, W2
  * and P); when either side is greedy the label is one probability.  Sizes
- * within the context's B_max, K_max, V_max; V % 8 == 0.  Drafted tokens out of
- * [0, V) are reported as DSPARK_ERR_DEVICE_OOB.  Device pointers; no host
- * synchronisation. */
+ * within the context's B_max, K_max, V_max; V % 8 == 0; 16-byte aligned P and
+ * U.  Drafted tokens out of [0, V) are reported as DSPARK_ERR_DEVICE_OOB.
+ * Device pointers; no host synchronisation. */
 int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
                         const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
                         const uint16_t* Wg, int d, const int32_t* tokens,

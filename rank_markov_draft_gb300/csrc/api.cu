@@ -97,7 +97,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
 
 bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t d0,
                uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
-               uint32_t b2) {
+               uint32_t b2, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
@@ -105,7 +105,7 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
   const cuuint32_t box[3] = {b0, b1, b2};
   const cuuint32_t elem[3] = {1, 1, 1};
   return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, elem,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -238,6 +238,11 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.logits = logits ? logits + o * V : nullptr;
     p.lse = lse ? lse + o : nullptr;
     if (lab != nullptr) {
+      if (!encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                     lab->target + static_cast<size_t>(b0) * (K + 1) * V, V, K + 1, Bc,
+                     static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(K + 1) * V * 4, 32, 1,
+                     box_rows))
+        return DSPARK_ERR_CUDA;
       p.target = lab->target + static_cast<size_t>(b0) * (K + 1) * V;
       p.lse_t = lab->lse_t + static_cast<size_t>(b0) * (K + 1);
       p.offq2 = lab->offq2 + o;
@@ -711,7 +716,7 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
   if (st != DSPARK_OK) return st;
   if (!(target_temperature >= 0.f) || target_temperature > 3.0e38f) return DSPARK_ERR_INVALID_ARG;
   if (draft_temperature > 0.f && draft_logprobs == nullptr) return DSPARK_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(P) & 31u) != 0) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(P)) return DSPARK_ERR_INVALID_ARG;
   const bool gated = (h != nullptr) || (Wg != nullptr);
   if (gated && (st = check_gate_args(h, Wg, d, r)) != DSPARK_OK) return st;
   if ((st = check_ctx(ctx)) != DSPARK_OK) return st;

@@ -38,10 +38,14 @@
 // gathered as soon as the MMAs are done with the current ones and the grid
 // barrier is waited on only before the final reduction.  The label mode
 // (DSpark explainer, "Confidence-scheduled verification": c*_k = 1 - TV of the
-// draft head's and the target's distributions) streams the target's row
+// draft head's and the target's distributions) streams the target's rows
 // beside U and sums 2^min(log2 q(v), log2 p(v)) over the vocabulary, both
 // normalisers known beforehand (the target's from a row scan, the draft's
-// from its own log-probability of the drafted token).
+// from its own log-probability of the drafted token).  Its ring slots hold U
+// and target for half a tile (32 tokens each), two slots per tile, so the
+// same 96 KB of shared memory keeps twice the bytes per tile in flight; every
+// epilogue warp reads both halves (8 tokens of each per thread), so each slot
+// has one group of readers that takes its fills in order.
 //
 // Sampling epilogue (an exact draw from softmax(l / T) in two stages over
 // 16-token blocks; each thread's 16 columns of a tile are one block beta):
@@ -251,6 +255,7 @@ template <int MODE, bool COPIES>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
   constexpr bool kTF = MODE == kModeTeacherForced || MODE == kModeLabel;
+  constexpr bool kHalf = MODE == kModeLabel;  // ring slots of half tiles: U and target
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -310,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     fence_mbar_init();
     if (nkk > 0) tma_prefetch_desc(&args.tm_w2);
     tma_prefetch_desc(&args.tm_u);
+    if (kHalf) tma_prefetch_desc(&args.tm_p);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       const uint32_t w_bytes = static_cast<uint32_t>(p.r) * kTileV * 2u;
       const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
       bool ok = true;
-      int w_issued = 0, u_issued = 0;
+      int w_issued = 0, u_issued = 0;  // u_issued: ring slot fills
       for (int k = 0; k < p.K && ok; ++k) {
         for (int t = 0; t < nt; ++t) {
           const int i = k * nt + t;
@@ -343,6 +349,24 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             mbar_arrive_expect_tx(&w_full[s], w_bytes);
             tma_load_2d(sW + s * kW2StageBytes, &args.tm_w2, v0, 0, &w_full[s], pol_w);
             w_issued = i + 1;
+          }
+          if (kHalf) {
+            // two fills per tile: U and target tokens [v0 + 32 h, v0 + 32 h + 32)
+            for (int h = 0; h < 2 && ok; ++h) {
+              const int j = 2 * i + h, su = j % nus;
+              if (!mbar_wait(&u_empty[su], ((j / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
+                             kBackoffControlNs)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&u_full[su], u_bytes);
+              tma_load_3d(sU + su * 2 * ubox, &args.tm_u, v0 + 32 * h, k, 0, &u_full[su], pol_u);
+              tma_load_3d(sU + su * 2 * ubox + ubox, &args.tm_p, v0 + 32 * h, k, 0, &u_full[su],
+                          pol_u);
+              u_issued = j + 1;
+            }
+            if (!ok) break;
+            continue;
           }
           const int su = i % nus;
           if (!mbar_wait(&u_empty[su], ((i / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
@@ -494,12 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       // ---- stream the step's tiles
       float m2 = (MODE == kModeLabel) ? 0.f : -INFINITY, sum = 0.f;  // label: a plain sum
       float offq2 = 0.f, offp2 = 0.f;  // label: log2 q = l * scale2 + offq2, log2 p likewise
-      const float* trow = nullptr;     // label: this request's target row at position k
       if (MODE == kModeLabel && row_ok) {
         const size_t o = static_cast<size_t>(b) * p.K + k;
         offq2 = __ldg(p.offq2 + o);
         offp2 = -__ldg(p.lse_t + o + b) * kLog2e;  // target row b * (K + 1) + k
-        trow = p.target + (o + b) * static_cast<size_t>(p.V);
       }
       float yb = -INFINITY, lb = 0.f;  // best score (G, or y when greedy) and its logit
       int vb = 0x7FFFFFFF;
@@ -520,6 +542,89 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         if (COPIES && (i & (ncopy - 1)) != copy) continue;  // another copy's tile
         ++tt;
+        if (kHalf) {
+          // label: tile i is ring fills 2 i (tokens 0-31) and 2 i + 1 (32-63), each
+          // holding U and the target; this thread takes tokens 8 g .. 8 g + 7 of both
+          bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) {
+            fail = true;
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          uint32_t acc[16];
+          if (nkk > 0) {
+            const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(buf * kTileV + g * 8);
+            tmem_ld_x8(ta, acc);
+            tmem_ld_x8(ta + 32, acc + 8);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0u;
+          }
+          float uval[16], pt[16];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = 2 * i + h, sh = j % nus;
+            bool okh = mbar_wait(&u_full[sh], static_cast<uint32_t>(j / nus) & 1u, p.timeout_ns,
+                                 abort_flag);
+            okh = __all_sync(0xFFFFFFFFu, okh);
+            if (!okh) {
+              fail = true;
+              *abort_flag = 1;
+              break;
+            }
+            const uint8_t* row = sU + sh * 2 * ubox + b * 128;
+            uint32_t dep = 0u;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t off = static_cast<uint32_t>(((2 * g + c) ^ (b & 7)) << 4);
+              const float4 x = *reinterpret_cast<const float4*>(row + off);
+              const float4 y = *reinterpret_cast<const float4*>(row + ubox + off);
+              uval[8 * h + 4 * c + 0] = x.x;
+              uval[8 * h + 4 * c + 1] = x.y;
+              uval[8 * h + 4 * c + 2] = x.z;
+              uval[8 * h + 4 * c + 3] = x.w;
+              pt[8 * h + 4 * c + 0] = y.x;
+              pt[8 * h + 4 * c + 1] = y.y;
+              pt[8 * h + 4 * c + 2] = y.z;
+              pt[8 * h + 4 * c + 3] = y.w;
+              dep ^= __float_as_uint(x.x) ^ __float_as_uint(y.x);
+            }
+            arrive_after_reads(&u_empty[sh], dep, s_sink, lane);
+          }
+          if (fail) break;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          if (!row_ok) continue;
+          // past V the boxes read zeros; the target side is masked to p = 0
+          const int vt = (t_begin + t) * kTileV;
+          if (vt + kTileV > p.V) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (vt + (j >> 3) * 32 + g * 8 + (j & 7) >= p.V) pt[j] = -INFINITY;
+          }
+          // sum of min(q, p) over the thread's columns
+          const float2 sq = make_float2(scale2, scale2), oq = make_float2(offq2, offq2);
+          const float2 sp = make_float2(p.target_scale2, p.target_scale2);
+          const float2 op = make_float2(offp2, offp2);
+          float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
+                                         make_float2(__uint_as_float(acc[j]),
+                                                     __uint_as_float(acc[j + 1])));
+            const float2 aq = __ffma2_rn(lj, sq, oq);
+            const float2 ap = __ffma2_rn(make_float2(pt[j], pt[j + 1]), sp, op);
+            acc2 = __fadd2_rn(acc2, make_float2(ex2_approx(fminf(aq.x, ap.x)),
+                                                ex2_approx(fminf(aq.y, ap.y))));
+          }
+          sum += acc2.x + acc2.y;
+          continue;
+        }
         if (MODE == kModeSample && row_ok) {
           // every other tile, refresh the bound with the key read a tile earlier, so
           // the load's latency is covered by a whole tile's work
@@ -527,19 +632,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               kpre > gkey)
             gkey = kpre;
           if (((tt + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
-        }
-        float pt[16];  // label: the target logits of this thread's 16 columns
-        if (MODE == kModeLabel) {
-          const int v0 = (t_begin + t) * kTileV + g * 16;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (row_ok && v0 + 8 * h + 8 <= p.V) {  // V is a multiple of 8
-              ld_nc_v8(trow + v0 + 8 * h, pt + 8 * h);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) pt[8 * h + j] = -INFINITY;
-            }
-          }
         }
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
         ok = ok && mbar_wait(&u_full[su], uph, p.timeout_ns, abort_flag);
@@ -581,26 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                                __float_as_uint(uval[8]) ^ __float_as_uint(uval[12]),
                            s_sink, lane);
         if (!row_ok) continue;
-
-        if (MODE == kModeLabel) {
-          // sum of min(q, p) over the thread's columns (columns past V: p = 0)
-          const float2 sq = make_float2(scale2, scale2), oq = make_float2(offq2, offq2);
-          const float2 sp = make_float2(p.target_scale2, p.target_scale2);
-          const float2 op = make_float2(offp2, offp2);
-          float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
-                                         make_float2(__uint_as_float(acc[j]),
-                                                     __uint_as_float(acc[j + 1])));
-            const float2 aq = __ffma2_rn(lj, sq, oq);
-            const float2 ap = __ffma2_rn(make_float2(pt[j], pt[j + 1]), sp, op);
-            acc2 = __fadd2_rn(acc2, make_float2(ex2_approx(fminf(aq.x, ap.x)),
-                                                ex2_approx(fminf(aq.y, ap.y))));
-          }
-          sum += acc2.x + acc2.y;
-          continue;
-        }
 
         const int vbase = (t_begin + t) * kTileV + g * 16;
         const bool full_chunk = vbase + 16 <= p.V;  // warp-uniform
@@ -986,9 +1058,8 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
       fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, true>)
                   : reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, false>);
       break;
-    case kModeLabel:
-      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeLabel, true>)
-                  : reinterpret_cast<const void*>(&draft_kernel<kModeLabel, false>);
+    case kModeLabel:  // half-tile ring slots: always the 128-row instantiation
+      fn = reinterpret_cast<const void*>(&draft_kernel<kModeLabel, false>);
       break;
     default: return cudaErrorInvalidValue;
   }

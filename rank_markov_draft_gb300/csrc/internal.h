@@ -66,7 +66,7 @@ struct DraftParams {
   unsigned long long* trace;  // optional phase timestamps [grid][K][kTraceSlots] (null: off)
   uint64_t timeout_ns;      // per-wait limit
   // acceptance-label mode (null otherwise)
-  const float* target;      // [B, K+1, V] (chunk) target logits, 32-byte aligned rows
+  const float* target;      // [B, K+1, V] (chunk) target logits (read through tm_p)
   const float* lse_t;       // [B, K+1] (chunk) log sum_v exp(target / Tt)
   const float* offq2;       // [B, K] (chunk) log2 q(v) = l(v) * log2(e) / Td + offq2
   float* label;             // [B, K] (chunk) 1 - TV(q, p)
@@ -76,6 +76,8 @@ struct DraftParams {
 struct DraftArgs {
   CUtensorMap tm_w2;  // W2 [r, V] bf16, box {64, r}, 128B swizzle
   CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle
+  CUtensorMap tm_p;   // label mode: target chunk [B, K+1, V] fp32, box {32, 1, box_rows},
+                      // 128B swizzle
   DraftParams p;
 };
 

@@ -25,14 +25,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Record the first device error of a launch (later ones are dropped).
-// 32-byte read-only global load (sm_100+); the address must be 32-byte aligned.
-__device__ __forceinline__ void ld_nc_v8(const float* src, float* x) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]),
-                 "=f"(x[6]), "=f"(x[7])
-               : "l"(src));
-}
-
 __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, kStatusOk, code);
 }
@@ -260,6 +252,16 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The same for 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
       : "r"(taddr)
       : "memory");
 }

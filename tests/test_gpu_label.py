@@ -142,10 +142,10 @@ def test_label_argument_errors(dsp):
     with pytest.raises(binding.DSparkError) as err:  # sampled draft without its log-probabilities
         binding.accept_label(dsp, P, *args, None, draft_temperature=1.0, target_temperature=1.0)
     assert err.value.code == binding.INVALID_ARG
-    buf = torch.zeros(B * (K + 1) * V + 4, dtype=torch.float32, device="cuda")
-    P16 = buf[4:].view(B, K + 1, V)  # 16-byte but not 32-byte aligned
+    buf = torch.zeros(B * (K + 1) * V + 2, dtype=torch.float32, device="cuda")
+    P8 = buf[2:].view(B, K + 1, V)  # 8-byte but not 16-byte aligned
     with pytest.raises(binding.DSparkError) as err:
-        binding.accept_label(dsp, P16, *args, dev(np.zeros((B, K), np.float32)),
+        binding.accept_label(dsp, P8, *args, dev(np.zeros((B, K), np.float32)),
                              draft_temperature=1.0, target_temperature=1.0)
     assert err.value.code == binding.INVALID_ARG
 
