@@ -224,24 +224,36 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Committed ncu summaries by workload, and the sources their kernels are built from:
+# a summary's traffic is used only while those sources hash as when it was taken.
+_HEADERS = ("sm103.cuh", "philox.cuh", "confidence.cuh", "internal.h")
+PROFILES = {
+    "serving": ("draft_kernel_serving.md", ("draft.cu",) + _HEADERS),
+    "label": ("label_step_serving.md", ("draft.cu", "label.cu", "verify.cu") + _HEADERS),
+    "verify": ("verify_step_serving.md", ("draft.cu", "verify.cu") + _HEADERS),
+}
+
+
+def kernel_source_hash(workload: str = "serving") -> str:
     h = hashlib.sha256()
-    for name in ("draft.cu", "sm103.cuh", "philox.cuh", "confidence.cuh", "internal.h"):
+    for name in PROFILES[workload][1]:
         with open(os.path.join(ROOT, "rank_markov_draft_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the draft kernel from the committed ncu summary,
-    if it was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"draft_kernel_{workload}.md")
+    """DRAM bytes per launch (per step, for multi-kernel steps) from the committed
+    ncu summary, if it was taken on the current kernel sources (else None)."""
+    if workload not in PROFILES:
+        return None
+    path = os.path.join(ROOT, "profiles", PROFILES[workload][0])
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_hash = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
     m_bytes = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(workload):
         return None
     return int(m_bytes.group(1))
 
