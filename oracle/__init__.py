@@ -75,8 +75,10 @@ def _bind(lib):
     lib.orc_markov_logits.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P, P]
     lib.orc_markov_logits.restype = i32
     lib.orc_confidence.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32, i32, i32, f64,
-                                   P, P, P]
+                                   P, P, P, P]
     lib.orc_confidence.restype = i32
+    lib.orc_sts_fit.argtypes = [P, P, i32, i32, f64, f64, P, P]
+    lib.orc_sts_fit.restype = i32
     lib.orc_topk.argtypes = [P, i32, i32, i32, i32, P, P, P]
     lib.orc_topk.restype = i32
     lib.orc_pair_scores.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, P]
@@ -252,8 +254,9 @@ class Oracle:
         return dict(logits=logits, lse=lse)
 
     def confidence(self, h, W1, anchors, tokens, w, *, bias: float = 0.0, with_markov: bool = True,
-                   threshold: float = 0.3, V: Optional[int] = None) -> dict:
-        """Confidence c_k, survival cumprod a_k and verify length per request."""
+                   threshold: float = 0.3, V: Optional[int] = None, tau=None) -> dict:
+        """Confidence c_k (calibrated by per-position temperatures tau [K] when given),
+        survival cumprod a_k and verify length per request."""
         h = _c(h, np.uint16)
         B, K, d = h.shape
         r = W1.shape[1] if (with_markov and W1 is not None) else 0
@@ -265,12 +268,28 @@ class Oracle:
         conf = np.zeros((B, K), np.float64)
         cum = np.zeros((B, K), np.float64)
         vl = np.zeros(B, np.int32)
+        tau = _c(tau, np.float64)
         rc = self._lib.orc_confidence(_ptr(h), _ptr(W1c), _ptr(anchors), _ptr(tokens), _ptr(w),
                                     float(bias), int(bool(with_markov)), B, K, d, r, V,
-                                    float(threshold), _ptr(conf), _ptr(cum), _ptr(vl))
+                                    float(threshold), _ptr(tau), _ptr(conf), _ptr(cum), _ptr(vl))
         if rc != 0:
             raise ValueError("oracle confidence rejected its arguments")
         return dict(conf=conf, cumprod=cum, verify_len=vl)
+
+    def sts_fit(self, conf, label, *, lo: float = 1.0 / 64, hi: float = 64.0) -> dict:
+        """Sequential temperature scaling: one temperature per position [K] from raw
+        confidences and acceptance labels [N, K]."""
+        conf = _c(conf, np.float32)
+        label = _c(label, np.float32)
+        N, K = conf.shape
+        assert label.shape == (N, K)
+        tau = np.zeros(K, np.float64)
+        loss = np.zeros(K, np.float64)
+        rc = self._lib.orc_sts_fit(_ptr(conf), _ptr(label), N, K, float(lo), float(hi), _ptr(tau),
+                                   _ptr(loss))
+        if rc != 0:
+            raise ValueError("oracle sts_fit rejected its arguments")
+        return dict(tau=tau, loss=loss)
 
     def topk(self, U, k: int = 16) -> dict:
         U = _c(U, np.float32)

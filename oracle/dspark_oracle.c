@@ -445,8 +445,8 @@ int orc_markov_logits(const float* U, const uint16_t* W1, const uint16_t* W2,
 /* ------------------------------------------------------------------ */
 int orc_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors,
                    const int32_t* tokens, const uint16_t* w, double bias, int with_markov,
-                   int B, int K, int d, int r, int V, double threshold, double* conf,
-                   double* cumprod, int32_t* verify_len) {
+                   int B, int K, int d, int r, int V, double threshold, const double* tau,
+                   double* conf, double* cumprod, int32_t* verify_len) {
   if (B <= 0 || K <= 0 || d < 0 || r < 0) return -1;
   int bad = 0;
 #pragma omp parallel for schedule(static) reduction(| : bad)
@@ -466,7 +466,7 @@ int orc_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors
         for (int i = 0; i < r; ++i)
           z += bf16_to_double(w[d + i]) * bf16_to_double(W1[(int64_t)prev * r + i]);
       }
-      const double c = sigmoid(z);
+      const double c = sigmoid(tau ? z / tau[k] : z); /* STS: one temperature per position */
       surv *= c;
       conf[(int64_t)b * K + k] = c;
       cumprod[(int64_t)b * K + k] = surv;
@@ -896,4 +896,87 @@ int orc_accept_label(const float* P, const float* U, const uint16_t* W1, const u
   free(qv);
   free(e);
   return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Sequential temperature scaling (STS) of the confidence head.         */
+/* [EXPL] "Confidence-scheduled verification": the raw head is          */
+/* calibrated with one temperature per position, fitted left to right   */
+/* against cumulative prefix-survival probabilities, which keeps the    */
+/* ranking.  Reading: the calibrated confidence is c_k = sigmoid(z_k /   */
+/* tau_k), z_k the head's logit; tau_k minimises, over the N             */
+/* calibration rows, the binary cross-entropy between the model's        */
+/* prefix survival a_k = prod_{i<=k} sigmoid(z_i / tau_i) (tau_0 ..      */
+/* tau_{k-1} already fitted) and the target survival                     */
+/* y_k = prod_{i<=k} label_i (acceptance labels c*_i, or 0/1 outcomes).  */
+/* z_k = ln(c_k / (1 - c_k)) of the raw confidence clamped to            */
+/* [2^-24, 1 - 2^-24]; the survival inside the cross-entropy is clamped  */
+/* to [1e-7, 1 - 1e-7].  The 1-D minimisation over x = ln tau in         */
+/* [ln lo, ln hi]: STS_G evenly spaced points, keep the best (ties to     */
+/* the smaller), narrow to the interval between its neighbours, STS_R    */
+/* rounds.                                                                */
+/* conf, label [N, K] fp32 -> tau [K], loss [K] (mean cross-entropy).    */
+/* ------------------------------------------------------------------ */
+#define STS_G 32
+#define STS_R 8
+
+static double sts_loss(const double* z, const double* a, const double* y, int N, double inv_tau) {
+  double L = 0.0;
+  for (int n = 0; n < N; ++n) {
+    double q = a[n] * sigmoid(z[n] * inv_tau);
+    if (q < 1e-7) q = 1e-7;
+    if (q > 1.0 - 1e-7) q = 1.0 - 1e-7;
+    L -= y[n] * log(q) + (1.0 - y[n]) * log1p(-q);
+  }
+  return L;
+}
+
+int orc_sts_fit(const float* conf, const float* label, int N, int K, double lo, double hi,
+                double* tau, double* loss) {
+  if (N <= 0 || K <= 0 || !(lo > 0.0) || !(hi > lo)) return -1;
+  double* z = (double*)malloc(sizeof(double) * (size_t)N);
+  double* a = (double*)malloc(sizeof(double) * (size_t)N);
+  double* y = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!z || !a || !y) {
+    free(z);
+    free(a);
+    free(y);
+    return -1;
+  }
+  for (int n = 0; n < N; ++n) a[n] = y[n] = 1.0;
+  const double cmin = 1.0 / 16777216.0;
+  for (int k = 0; k < K; ++k) {
+    for (int n = 0; n < N; ++n) {
+      double c = conf[(int64_t)n * K + k];
+      if (c < cmin) c = cmin;
+      if (c > 1.0 - cmin) c = 1.0 - cmin;
+      z[n] = log(c / (1.0 - c));
+      y[n] *= (double)label[(int64_t)n * K + k];
+    }
+    double x0 = log(lo), x1 = log(hi), xb = x0, Lb = 0.0;
+    for (int round = 0; round < STS_R; ++round) {
+      int best = -1;
+      const double step = (x1 - x0) / (STS_G - 1);
+      for (int g = 0; g < STS_G; ++g) {
+        const double x = x0 + step * g;
+        const double L = sts_loss(z, a, y, N, exp(-x));
+        if (best < 0 || L < Lb) {
+          best = g;
+          Lb = L;
+          xb = x;
+        }
+      }
+      const double nx0 = x0 + step * (best > 0 ? best - 1 : 0);
+      const double nx1 = x0 + step * (best < STS_G - 1 ? best + 1 : STS_G - 1);
+      x0 = nx0;
+      x1 = nx1;
+    }
+    tau[k] = exp(xb);
+    if (loss) loss[k] = Lb / N;
+    for (int n = 0; n < N; ++n) a[n] *= sigmoid(z[n] / tau[k]);
+  }
+  free(z);
+  free(a);
+  free(y);
+  return 0;
 }

@@ -69,6 +69,16 @@ MUTANTS = [
      ["test_verify_target_equal_to_draft_accepts_every_token"]),
     ("label-overlap-by-max", "s += fmin(pv[v], qv[v]);", "s += fmax(pv[v], qv[v]);",
      ["test_accept_label_special_cases", "test_accept_label_is_the_verifier_acceptance_rate"]),
+    ("sts-targets-not-cumulative", "y[n] *= (double)label[(int64_t)n * K + k];",
+     "y[n] = (double)label[(int64_t)n * K + k];",
+     ["test_sts_recovers_the_generating_temperatures", "test_sts_matches_a_dense_scan"]),
+    ("sts-survival-not-carried", "for (int n = 0; n < N; ++n) a[n] *= sigmoid(z[n] / tau[k]);", "",
+     ["test_sts_recovers_the_generating_temperatures", "test_sts_matches_a_dense_scan"]),
+    ("sts-temperature-inverted", "const double L = sts_loss(z, a, y, N, exp(-x));",
+     "const double L = sts_loss(z, a, y, N, exp(x));",
+     ["test_sts_recovers_the_generating_temperatures"]),
+    ("confidence-temperature-ignored", "sigmoid(tau ? z / tau[k] : z)", "sigmoid(z)",
+     ["test_confidence_applies_per_position_temperatures"]),
     ("label-predecessor-not-carried", "      label[(int64_t)b * K + k] = s;\n      prev = x;\n",
      "      label[(int64_t)b * K + k] = s;\n",
      ["test_accept_label_special_cases", "test_accept_label_is_the_verifier_acceptance_rate"]),

@@ -592,3 +592,86 @@ def test_accept_label_special_cases(orc):
                            draft_temperature=0.0, target_temperature=0.0)
     assert np.array_equal(lab, (drafted["tokens"] == Pr[:, :K].argmax(-1)).astype(np.float64))
     assert np.all((lab >= 0) & (lab <= 1))
+
+
+# ------------------------------------------------------------------ sequential temperature scaling
+def _raw_confidences(rng, N, K, spread=2.0):
+    z = rng.normal(0.0, spread, (N, K))
+    conf = special.expit(z).astype(np.float32)
+    c = np.clip(conf.astype(np.float64), 2.0 ** -24, 1 - 2.0 ** -24)
+    return conf, np.log(c / (1 - c))  # the logit the fit sees
+
+
+def test_sts_recovers_the_generating_temperatures(orc):
+    """Labels drawn as sigmoid(z_k / tau_k): the cross-entropy of the cumulative survival is
+    minimised exactly there, position after position."""
+    rng = np.random.default_rng(101)
+    N, K = 4000, 5
+    conf, z = _raw_confidences(rng, N, K)
+    tau_true = np.array([0.5, 1.7, 1.0, 3.0, 0.8])
+    label = special.expit(z / tau_true).astype(np.float32)
+    out = orc.sts_fit(conf, label)
+    assert np.abs(np.log(out["tau"]) - np.log(tau_true)).max() < 1e-4, out["tau"]
+
+
+def test_sts_leaves_calibrated_confidences_alone(orc):
+    rng = np.random.default_rng(102)
+    conf, _ = _raw_confidences(rng, 3000, 4)
+    out = orc.sts_fit(conf, conf)
+    assert np.abs(np.log(out["tau"])).max() < 1e-4, out["tau"]
+
+
+def test_sts_matches_a_dense_scan(orc):
+    """Each temperature is the minimiser of its position's loss over a fine scan of ln tau
+    (earlier temperatures fixed at the fitted ones)."""
+    rng = np.random.default_rng(103)
+    N, K = 300, 3
+    conf, z = _raw_confidences(rng, N, K, spread=1.5)
+    label = rng.uniform(0.2, 1.0, (N, K)).astype(np.float32)
+    out = orc.sts_fit(conf, label)
+    xs = np.linspace(np.log(1 / 64), np.log(64), 200001)
+    a = np.ones(N)
+    y = np.ones(N)
+    for k in range(K):
+        y = y * label[:, k].astype(np.float64)
+        q = np.clip(a[None, :] * special.expit(z[None, :, k] * np.exp(-xs)[:, None]), 1e-7, 1 - 1e-7)
+        L = -(y * np.log(q) + (1 - y) * np.log1p(-q)).sum(axis=1)
+        assert abs(np.log(out["tau"][k]) - xs[np.argmin(L)]) < 2e-4, k
+        assert out["loss"][k] <= L.min() / N + 1e-12
+        a = a * special.expit(z[:, k] / out["tau"][k])
+
+
+def test_sts_calibrates_and_keeps_the_ranking(orc):
+    """A head that is overconfident at every position: after STS the predicted survival
+    matches the realised one (expected calibration error drops) and the order of
+    confidences within a position is unchanged."""
+    rng = np.random.default_rng(104)
+    N, K = 20000, 4
+    conf, z = _raw_confidences(rng, N, K, spread=3.0)
+    true_p = special.expit(z / 2.5)                    # the head is too sharp by 2.5x
+    acc = (rng.uniform(size=(N, K)) < true_p).astype(np.float32)  # 0/1 outcomes
+    out = orc.sts_fit(conf, acc)
+    assert np.all(np.abs(out["tau"] - 2.5) < 0.25), out["tau"]
+    cal = special.expit(z / out["tau"])
+    surv_true = np.cumprod(acc, axis=1)
+    def ece(p, y, bins=10):
+        idx = np.minimum((p * bins).astype(int), bins - 1)
+        return sum(abs(p[idx == i].mean() - y[idx == i].mean()) * (idx == i).mean()
+                   for i in range(bins) if (idx == i).any())
+    before = ece(np.cumprod(conf, axis=1).ravel(), surv_true.ravel())
+    after = ece(np.cumprod(cal, axis=1).ravel(), surv_true.ravel())
+    assert after < 0.5 * before and after < 0.02, (before, after)
+    for k in range(K):
+        assert np.array_equal(np.argsort(conf[:, k], kind="stable"), np.argsort(cal[:, k], kind="stable"))
+
+
+def test_confidence_applies_per_position_temperatures(orc):
+    V, K, r, d = 64, 3, 16, 32
+    inp = make_inputs(105, 4, K, V, r, d=d, confidence=True, weight_std=0.3)
+    toks = np.random.default_rng(106).integers(0, V, (4, K)).astype(np.int32)
+    tau = np.array([0.5, 2.0, 1.0])
+    raw = orc.confidence(inp.h, inp.W1, inp.anchors, toks, inp.w_conf, bias=0.3)
+    cal = orc.confidence(inp.h, inp.W1, inp.anchors, toks, inp.w_conf, bias=0.3, tau=tau)
+    z = special.logit(raw["conf"])
+    assert np.allclose(cal["conf"], special.expit(z / tau), atol=1e-12)
+    assert np.allclose(cal["cumprod"], np.cumprod(cal["conf"], axis=1), atol=1e-12)
