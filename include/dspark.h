@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define DSPARK_ABI_VERSION 1
+#define DSPARK_ABI_VERSION 2
 
 typedef struct dspark_ctx dspark_ctx;
 typedef struct CUstream_st* dspark_stream_t; /* same type as cudaStream_t */
@@ -84,6 +84,8 @@ typedef struct dspark_conf_args {
   float* conf;           /* out [B, K] fp32 */
   float* cumprod;        /* out [B, K] fp32 */
   int32_t* verify_len;   /* out [B] int32 */
+  const float* tau;      /* [K] per-position temperatures from sequential temperature
+                            scaling (c_k = sigmoid(z_k / tau_k)), device; NULL: all 1 */
 } dspark_conf_args;
 
 /* --------------------------------------------------------------------- */
@@ -251,15 +253,35 @@ int dspark_selector_walk(dspark_ctx* ctx, const int32_t* cand, const float* scor
 /* Confidence head (standalone)                                             */
 /* --------------------------------------------------------------------- */
 
-/* c_k = sigmoid(w[:d] . h[b,k] + with_markov * w[d:] . W1[x_{k-1}] + bias),
+/* c_k = sigmoid((w[:d] . h[b,k] + with_markov * w[d:] . W1[x_{k-1}] + bias) / tau_k),
  * cumprod a_k, verify_len = longest prefix with a_k >= threshold.
  * Source: as dspark_conf_args.  tokens [B, K] = x_1..x_K; x_0 = anchors[b].
- * W1 may be NULL when with_markov == 0. */
+ * W1 may be NULL when with_markov == 0; tau [K] device (NULL: all 1). */
 int dspark_confidence(dspark_ctx* ctx, const uint16_t* h, const uint16_t* W1,
                       const int32_t* anchors, const int32_t* tokens, const uint16_t* w,
                       float bias, int with_markov, int B, int K, int d, int r, int V,
-                      float threshold, float* conf, float* cumprod, int32_t* verify_len,
-                      dspark_stream_t stream);
+                      float threshold, const float* tau, float* conf, float* cumprod,
+                      int32_t* verify_len, dspark_stream_t stream);
+
+/* Sequential temperature scaling (STS) of the confidence head: one temperature
+ * per position, fitted left to right against cumulative prefix survival.
+ * Source: DSpark explainer, "Confidence-scheduled verification" (the raw head's
+ * calibration error is brought down by fitting one temperature per position,
+ * left to right, against cumulative prefix-survival probabilities; the
+ * ranking is kept).  tau_k minimises, over the N calibration rows, the binary
+ * cross-entropy between prod_{i<=k} sigmoid(z_i / tau_i) (tau_0 .. tau_{k-1}
+ * already fitted) and prod_{i<=k} label_i, with z_i the logit of the raw
+ * confidence (clamped to [2^-24, 1 - 2^-24]) and the survival clamped to
+ * [1e-7, 1 - 1e-7] inside the logarithms.  The 1-D search over ln tau in
+ * [ln tau_lo, ln tau_hi]: 32 evenly spaced points, keep the best (ties to the
+ * smaller), narrow to the interval between its neighbours, 8 rounds.
+ *   conf [N, K] fp32 raw confidences (the head with tau = 1)
+ *   label [N, K] fp32 acceptance labels (dspark_accept_label) or 0/1 outcomes
+ * Outputs tau [K] fp32 and loss [K] (mean cross-entropy at tau_k; may be
+ * NULL).  Device pointers; one kernel, no host synchronisation.  0 < tau_lo <
+ * tau_hi; K <= 64. */
+int dspark_sts_fit(dspark_ctx* ctx, const float* conf, const float* label, int N, int K,
+                   float tau_lo, float tau_hi, float* tau, float* loss, dspark_stream_t stream);
 
 /* --------------------------------------------------------------------- */
 /* Teacher-forced calibrated logits (parity / test mode)                    */

@@ -33,6 +33,7 @@ EXPORTS = (
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
     "dspark_markov_draft_noalloc", "dspark_verify", "dspark_schedule", "dspark_accept_label",
+    "dspark_sts_fit",
 )
 
 
@@ -47,6 +48,7 @@ class ConfArgs(ctypes.Structure):
         ("h", ctypes.c_void_p), ("w", ctypes.c_void_p), ("bias", ctypes.c_float),
         ("d", ctypes.c_int), ("with_markov", ctypes.c_int), ("threshold", ctypes.c_float),
         ("conf", ctypes.c_void_p), ("cumprod", ctypes.c_void_p), ("verify_len", ctypes.c_void_p),
+        ("tau", ctypes.c_void_p),
     ]
 
 
@@ -78,12 +80,13 @@ def load(path: str = LIB_PATH):
         "dspark_gate": [P, P, P, I, I, I, P, P],
         "dspark_selector_scores": [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P],
         "dspark_selector_walk": [P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P],
-        "dspark_confidence": [P, P, P, P, P, P, F, I, I, I, I, I, I, F, P, P, P, P],
+        "dspark_confidence": [P, P, P, P, P, P, F, I, I, I, I, I, I, F, P, P, P, P, P],
         "dspark_markov_logits": [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P],
         "dspark_markov_draft_noalloc": [P, P, P, P, I, I, I, I, F, U64, P, P, P, P],
         "dspark_verify": [P, P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, F, F, U64, P, P, P, P],
         "dspark_schedule": [P, P, I, I, P, I, P, P, P],
         "dspark_accept_label": [P, P, P, P, P, P, P, P, I, P, P, I, I, I, I, F, F, P, P],
+        "dspark_sts_fit": [P, P, P, I, I, F, F, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -197,6 +200,7 @@ class Confidence:
     conf: Optional[torch.Tensor] = None       # out [B, K] fp32
     cumprod: Optional[torch.Tensor] = None    # out [B, K] fp32
     verify_len: Optional[torch.Tensor] = None  # out [B] int32
+    tau: Optional[torch.Tensor] = None         # [K] fp32 STS temperatures (None: all 1)
 
     def allocate(self, B: int, K: int):
         dev = self.h.device
@@ -213,7 +217,8 @@ class Confidence:
                         float(self.bias), int(self.h.shape[-1]), int(bool(self.with_markov)),
                         float(self.threshold), _ptr(self.conf, (torch.float32,), "conf.conf"),
                         _ptr(self.cumprod, (torch.float32,), "conf.cumprod"),
-                        _ptr(self.verify_len, (torch.int32,), "conf.verify_len"))
+                        _ptr(self.verify_len, (torch.int32,), "conf.verify_len"),
+                        _ptr(self.tau, (torch.float32,), "conf.tau"))
 
 
 def _conf_ref(conf: Optional[Confidence]):
@@ -270,12 +275,12 @@ def dspark_selector_walk(ctx: Context, cand, scores, anchors, A, B, K, V, r, top
 
 
 def dspark_confidence(ctx: Context, h, W1, anchors, tokens, w, bias, with_markov, B, K, d, r, V,
-                      threshold, conf, cumprod, verify_len, stream=None):
+                      threshold, tau, conf, cumprod, verify_len, stream=None):
     code = ctx.lib.dspark_confidence(
         ctx.handle, _ptr(h, _BF16, "h"), _ptr(W1, _BF16, "W1"),
         _ptr(anchors, (torch.int32,), "anchors"), _ptr(tokens, (torch.int32,), "tokens"),
         _ptr(w, _BF16, "w"), float(bias), int(bool(with_markov)), B, K, d, r, V, float(threshold),
-        _ptr(conf, (torch.float32,), "conf"), _ptr(cumprod, (torch.float32,), "cumprod"),
+        _ptr(tau, (torch.float32,), "tau"), _ptr(conf, (torch.float32,), "conf"), _ptr(cumprod, (torch.float32,), "cumprod"),
         _ptr(verify_len, (torch.int32,), "verify_len"), _stream(stream, ctx.device))
     _check(code, "dspark_confidence")
 
@@ -315,6 +320,14 @@ def dspark_accept_label(ctx: Context, P, U, W1, W2, anchors, h, Wg, d, tokens, d
         float(draft_temperature), float(target_temperature), _ptr(label, (torch.float32,), "label"),
         _stream(stream, ctx.device))
     _check(code, "dspark_accept_label")
+
+
+def dspark_sts_fit(ctx: Context, conf, label, N, K, tau_lo, tau_hi, tau, loss, stream=None):
+    code = ctx.lib.dspark_sts_fit(
+        ctx.handle, _ptr(conf, (torch.float32,), "conf"), _ptr(label, (torch.float32,), "label"),
+        N, K, float(tau_lo), float(tau_hi), _ptr(tau, (torch.float32,), "tau"),
+        _ptr(loss, (torch.float32,), "loss"), _stream(stream, ctx.device))
+    _check(code, "dspark_sts_fit")
 
 
 def dspark_schedule(ctx: Context, a, R, K, sps, ell, theta, stream=None):
@@ -409,14 +422,14 @@ def selector_walk(ctx: Context, cand, scores, anchors, *, V, A=None, temperature
 
 
 def confidence(ctx: Context, h, W1, anchors, tokens, w, *, V, bias=0.0, with_markov=True,
-               threshold=0.3, stream=None) -> dict:
+               threshold=0.3, tau=None, stream=None) -> dict:
     B, K, d = h.shape
     r = _rank(W1) if with_markov else 0
     conf = torch.empty(B, K, dtype=torch.float32, device=h.device)
     cum = torch.empty(B, K, dtype=torch.float32, device=h.device)
     vl = torch.empty(B, dtype=torch.int32, device=h.device)
     dspark_confidence(ctx, h, W1 if with_markov else None, anchors, tokens, w, bias, with_markov,
-                      B, K, d, r, V, threshold, conf, cum, vl, stream)
+                      B, K, d, r, V, threshold, tau, conf, cum, vl, stream)
     return dict(conf=conf, cumprod=cum, verify_len=vl)
 
 
@@ -445,6 +458,15 @@ def accept_label(ctx: Context, P, U, W1, W2, anchors, tokens, draft_logprobs=Non
     dspark_accept_label(ctx, P, U, W1, W2, anchors, h, Wg, d, tokens, draft_logprobs, B, K, V, r,
                         draft_temperature, target_temperature, label, stream)
     return label
+
+
+def sts_fit(ctx: Context, conf, label, *, tau_lo=1.0 / 64, tau_hi=64.0, stream=None) -> dict:
+    """Sequential temperature scaling: temperatures [K] from raw confidences and labels [N, K]."""
+    N, K = conf.shape
+    tau = torch.empty(K, dtype=torch.float32, device=conf.device)
+    loss = torch.empty(K, dtype=torch.float32, device=conf.device)
+    dspark_sts_fit(ctx, conf, label, N, K, tau_lo, tau_hi, tau, loss, stream)
+    return dict(tau=tau, loss=loss)
 
 
 def schedule(ctx: Context, a, sps, stream=None) -> dict:

@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libdspark.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "draft.cu", "gate.cu", "selector.cu", "confidence.cu", "noalloc.cu", "verify.cu",
-           "schedule.cu", "label.cu"]
+           "schedule.cu", "label.cu", "calibrate.cu"]
 
 
 def nvcc() -> str:

@@ -256,6 +256,7 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
       p.conf_d = conf->d;
       p.conf_with_markov = conf->with_markov;
       p.conf_threshold = conf->threshold;
+      p.conf_tau = conf->tau;
       p.conf = conf->conf + o;
       p.cumprod = conf->cumprod + o;
       p.verify_len = conf->verify_len + b0;
@@ -585,8 +586,8 @@ int dspark_selector_walk(dspark_ctx* ctx, const int32_t* cand, const float* scor
 int dspark_confidence(dspark_ctx* ctx, const uint16_t* h, const uint16_t* W1,
                       const int32_t* anchors, const int32_t* tokens, const uint16_t* w,
                       float bias, int with_markov, int B, int K, int d, int r, int V,
-                      float threshold, float* conf, float* cumprod, int32_t* verify_len,
-                      dspark_stream_t stream) {
+                      float threshold, const float* tau, float* conf, float* cumprod,
+                      int32_t* verify_len, dspark_stream_t stream) {
   if (h == nullptr || w == nullptr || conf == nullptr || cumprod == nullptr ||
       verify_len == nullptr)
     return DSPARK_ERR_INVALID_ARG;
@@ -603,7 +604,7 @@ int dspark_confidence(dspark_ctx* ctx, const uint16_t* h, const uint16_t* W1,
   if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
   ctx->last_launches = 1;
   return cuda_status(dspark::launch_confidence(h, W1, anchors, tokens, w, bias, with_markov, B, K,
-                                               d, with_markov ? r : 0, V, threshold, conf,
+                                               d, with_markov ? r : 0, V, threshold, tau, conf,
                                                cumprod, verify_len, ctx->d_status,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -764,6 +765,19 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
     if (st != DSPARK_OK) return st;
   }
   return DSPARK_OK;
+}
+
+int dspark_sts_fit(dspark_ctx* ctx, const float* conf, const float* label, int N, int K,
+                   float tau_lo, float tau_hi, float* tau, float* loss, dspark_stream_t stream) {
+  if (conf == nullptr || label == nullptr || tau == nullptr) return DSPARK_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || !(tau_lo > 0.f) || !(tau_hi > tau_lo) || tau_hi > 3.0e38f)
+    return DSPARK_ERR_INVALID_ARG;
+  if (K > dspark::kMaxK) return DSPARK_ERR_UNSUPPORTED;
+  int st;
+  if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
+  ctx->last_launches = 1;
+  return cuda_status(dspark::launch_sts_fit(conf, label, N, K, tau_lo, tau_hi, tau, loss,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_schedule(dspark_ctx* ctx, const float* a, int R, int K, const float* sps,

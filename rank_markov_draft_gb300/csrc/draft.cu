@@ -1000,7 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                 p.conf_with_markov ? p.W1 + static_cast<size_t>(prev_tok) * p.r : nullptr;
             const float z = confidence_logit(p.conf_h + (static_cast<size_t>(bb) * p.K + k) * d,
                                              d, p.conf_w, emb, p.r, p.conf_bias, lane);
-            if (lane == 0) s_conf[k] = sigmoidf_accurate(z);
+            if (lane == 0)
+              s_conf[k] = sigmoidf_accurate(p.conf_tau ? z / __ldg(p.conf_tau + k) : z);
           }
           named_bar_sync(kEpiBarrier, kEpiThreads);
           if (etid == 0) {

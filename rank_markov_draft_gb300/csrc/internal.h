@@ -52,6 +52,7 @@ struct DraftParams {
   int conf_d;
   int conf_with_markov;
   float conf_threshold;
+  const float* conf_tau;    // [K] STS temperatures, or null (all 1)
   float* conf;              // [B, K] (chunk)
   float* cumprod;           // [B, K] (chunk)
   int32_t* verify_len;      // [B] (chunk)
@@ -200,7 +201,11 @@ cudaError_t launch_schedule(const float* a, int R, int K, const float* sps, int3
 cudaError_t launch_confidence(const uint16_t* h, const uint16_t* W1, const int32_t* anchors,
                               const int32_t* tokens, const uint16_t* w, float bias,
                               int with_markov, int B, int K, int d, int r, int V,
-                              float threshold, float* conf, float* cumprod,
+                              float threshold, const float* tau, float* conf, float* cumprod,
                               int32_t* verify_len, int* status, cudaStream_t stream);
+
+// ---- sequential temperature scaling (calibrate.cu)
+cudaError_t launch_sts_fit(const float* conf, const float* label, int N, int K, float tau_lo,
+                           float tau_hi, float* tau, float* loss, cudaStream_t stream);
 
 }  // namespace dspark

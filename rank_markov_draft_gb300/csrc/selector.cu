@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(
     const uint16_t* emb = conf.with_markov ? A + static_cast<size_t>(prev_tok) * r : nullptr;
     const float zc = confidence_logit(conf.h + bt * conf.d, conf.d, conf.w, emb, r, conf.bias,
                                       lane);
-    if (lane == 0) s_conf[t] = sigmoidf_accurate(zc);
+    if (lane == 0) s_conf[t] = sigmoidf_accurate(conf.tau ? zc / __ldg(conf.tau + t) : zc);
   }
   __syncthreads();
   if (threadIdx.x == 0) {

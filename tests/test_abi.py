@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.dspark_abi_version() == 1
+    assert lib.dspark_abi_version() == 2
     for code in range(9):
         assert lib.dspark_strerror(code).decode() != "unknown status"
 

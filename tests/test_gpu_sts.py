@@ -1,0 +1,151 @@
+"""GPU parity of sequential temperature scaling (dspark_sts_fit) and of the
+confidence head with per-position temperatures, against the fp64 oracle.
+
+Tolerance of the fitted temperatures.  Both sides run the same search; the GPU
+evaluates each row's cross-entropy in fp32 (about 1e-7 relative) and sums them
+with compensation, so the loss it minimises differs from the oracle's by a few
+1e-6 of its value.  Near the optimum the loss is quadratic in ln tau, so the
+two minimisers may sit apart by about sqrt(2 * 1e-5 / curvature) in ln tau;
+with the curvatures of these calibration sets that is below 2e-3, and 5e-3 is
+asserted.  The losses at the fitted temperatures agree to 1e-4 relative.
+"""
+
+import numpy as np
+import pytest
+import torch
+from scipy import special
+
+import oracle
+from rank_markov_draft_gb300 import binding
+from synth import make_inputs
+from tests.gpu_util import bf, dev, first_difference, host
+
+pytestmark = pytest.mark.gpu
+
+TAU_TOL = 5e-3
+
+
+def _raw(rng, N, K, spread):
+    z = rng.normal(0.0, spread, (N, K))
+    return special.expit(z).astype(np.float32)
+
+
+def _cases():
+    rng = np.random.default_rng(201)
+    conf = _raw(rng, 4000, 5, 2.0)
+    c = np.clip(conf.astype(np.float64), 2.0 ** -24, 1 - 2.0 ** -24)
+    z = np.log(c / (1 - c))
+    yield "generating temperatures", conf, special.expit(
+        z / np.array([0.5, 1.7, 1.0, 3.0, 0.8])).astype(np.float32)
+    conf = _raw(rng, 3000, 8, 1.5)
+    yield "soft labels", conf, rng.uniform(0.3, 1.0, conf.shape).astype(np.float32)
+    conf = _raw(rng, 20000, 4, 3.0)
+    c = np.clip(conf.astype(np.float64), 2.0 ** -24, 1 - 2.0 ** -24)
+    outcome = rng.uniform(size=conf.shape) < special.expit(np.log(c / (1 - c)) / 2.5)
+    yield "0/1 outcomes of an overconfident head", conf, outcome.astype(np.float32)
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_sts_fit_matches_oracle(dsp, case):
+    name, conf, label = list(_cases())[case]
+    out = binding.sts_fit(dsp, dev(conf), dev(label))
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    ref = oracle.sts_fit(conf, label)
+    tau, loss = host(out["tau"]).astype(np.float64), host(out["loss"]).astype(np.float64)
+    err = np.abs(np.log(tau) - np.log(ref["tau"])).max()
+    assert err <= TAU_TOL, (name, tau, ref["tau"])
+    assert np.allclose(loss, ref["loss"], rtol=1e-4), (name, loss, ref["loss"])
+
+
+def test_confidence_with_temperatures(dsp):
+    B, K, V, r, d = 11, 7, 500, 64, 96
+    inp = make_inputs(202, B, K, V, r, d=d, confidence=True)
+    tokens = np.random.default_rng(203).integers(0, V, size=(B, K)).astype(np.int32)
+    tau = np.array([0.5, 2.0, 1.0, 1.25, 4.0, 0.75, 1.5], np.float32)
+    out = binding.confidence(dsp, bf(inp.h), bf(inp.W1), dev(inp.anchors), dev(tokens),
+                             bf(inp.w_conf), V=V, bias=0.1, threshold=0.2, tau=dev(tau))
+    torch.cuda.synchronize()
+    ref = oracle.confidence(inp.h, inp.W1, inp.anchors, tokens, inp.w_conf, bias=0.1,
+                            threshold=0.2, tau=tau.astype(np.float64))
+    assert np.abs(host(out["conf"]) - ref["conf"]).max() < 1e-5
+    assert np.abs(host(out["cumprod"]) - ref["cumprod"]).max() < 1e-5
+    near = np.abs(ref["cumprod"] - 0.2) < 1e-5
+    assert np.all((host(out["verify_len"]) == ref["verify_len"]) | near.any(axis=1))
+
+
+@pytest.mark.parametrize("path", ["draft", "walk"])
+def test_fused_confidence_with_temperatures(dsp, path):
+    B, K, V, r, d = 9, 6, 1000, 64, 128
+    inp = make_inputs(204, B, K, V, r, d=d, confidence=True, selector=(path == "walk"))
+    tau = dev(np.array([0.5, 2.0, 1.0, 1.25, 4.0, 0.75], np.float32))
+    conf = binding.Confidence(h=bf(inp.h), w=bf(inp.w_conf), bias=0.0, threshold=0.3, tau=tau)
+    if path == "draft":
+        out = binding.markov_draft(dsp, dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
+                                   temperature=1.0, seed=6, conf=conf)
+        ref_tok = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0,
+                                      seed=6)["tokens"]
+        emb = inp.W1
+    else:
+        sc = binding.selector_scores(dsp, dev(inp.U), bf(inp.A), bf(inp.Bt), dev(inp.anchors),
+                                     topk=16)
+        out = binding.selector_walk(dsp, sc["cand"], sc["scores"], dev(inp.anchors), V=V,
+                                    A=bf(inp.A), temperature=1.0, seed=6, conf=conf)
+        top = oracle.topk(inp.U, 16)
+        S = oracle.pair_scores(top["cand"], top["cval"], inp.A, inp.Bt, inp.anchors, V=V)
+        ref_tok = oracle.walk(top["cand"], S, temperature=1.0, seed=6)["tokens"]
+        emb = inp.A
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    ref = oracle.confidence(inp.h, emb, inp.anchors, ref_tok, inp.w_conf, threshold=0.3,
+                            tau=host(tau).astype(np.float64))
+    gt = host(out["tokens"])
+    whole = 0
+    for b in range(B):
+        n = min(first_difference(gt[b], ref_tok[b]) + 1, K)
+        assert np.abs(host(out["conf"])[b, :n] - ref["conf"][b, :n]).max() < 1e-5
+        assert np.abs(host(out["cumprod"])[b, :n] - ref["cumprod"][b, :n]).max() < 1e-5
+        whole += int(first_difference(gt[b], ref_tok[b]) == K)
+    assert whole >= B // 2
+
+
+def test_draft_label_sts_chain_calibrates(dsp):
+    """Raw confidences from the draft, acceptance labels from the label kernel, STS from
+    both, all on the GPU: the calibrated survival tracks the cumulative labels better."""
+    B, K, V, r, d = 256, 8, 2048, 64, 128
+    inp = make_inputs(205, B, K, V, r, d=d, confidence=True, weight_std=0.1)
+    rng = np.random.default_rng(206)
+    P = np.concatenate([inp.U + rng.standard_normal(inp.U.shape).astype(np.float32),
+                        rng.standard_normal((B, 1, V)).astype(np.float32)], axis=1)
+    conf = binding.Confidence(h=bf(inp.h), w=bf(inp.w_conf), bias=2.0)
+    dr = binding.markov_draft(dsp, dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
+                              temperature=1.0, seed=8, conf=conf)
+    lab = binding.accept_label(dsp, dev(P), dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
+                               dr["tokens"], dr["logprobs"], draft_temperature=1.0,
+                               target_temperature=1.0)
+    fit = binding.sts_fit(dsp, dr["conf"], lab)
+    cal = binding.Confidence(h=bf(inp.h), w=bf(inp.w_conf), bias=2.0, tau=fit["tau"])
+    dr2 = binding.markov_draft(dsp, dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
+                               temperature=1.0, seed=8, conf=cal)
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    assert torch.equal(dr["tokens"], dr2["tokens"])  # calibration never changes the draft
+    y = np.cumprod(host(lab).astype(np.float64), axis=1)
+    before = np.abs(host(dr["cumprod"]) - y).mean()
+    after = np.abs(host(dr2["cumprod"]) - y).mean()
+    assert after < before, (before, after, host(fit["tau"]))
+    ranks_kept = all(np.array_equal(np.argsort(host(dr["conf"])[:, k], kind="stable"),
+                                    np.argsort(host(dr2["conf"])[:, k], kind="stable"))
+                     for k in range(K))
+    assert ranks_kept
+
+
+def test_sts_argument_errors(dsp):
+    c = dev(np.full((4, 3), 0.5, np.float32))
+    with pytest.raises(binding.DSparkError) as err:
+        binding.sts_fit(dsp, c, c, tau_lo=2.0, tau_hi=1.0)
+    assert err.value.code == binding.INVALID_ARG
+    big = dev(np.full((2, 65), 0.5, np.float32))
+    with pytest.raises(binding.DSparkError) as err:
+        binding.sts_fit(dsp, big, big)
+    assert err.value.code == binding.UNSUPPORTED
