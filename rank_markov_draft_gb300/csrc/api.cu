@@ -38,9 +38,8 @@ struct dspark_ctx {
   float* d_v_U = nullptr;                // [B_max][V_max]
   float* d_v_H = nullptr;                // [B_max][256]
   int32_t* d_v_prev = nullptr;           // [B_max]
-  float* d_v_Lq = nullptr;               // [B_max][V_max]
-  float* d_v_lse_q = nullptr;            // [B_max]
-  dspark::VerifyRec* d_v_rec = nullptr;  // [B_max][kVerifyMaxPieces]
+  float* d_v_P = nullptr;                // [B_max][V_max] target rows at the draw position
+  dspark::ResRow* d_v_rows = nullptr;    // [B_max]
   // acceptance-label scratch
   int32_t* d_l_prev = nullptr;           // [B_max * K_max] predecessors of the drafted tokens
   float* d_l_offq2 = nullptr;            // [B_max * K_max] log2 q offsets
@@ -187,11 +186,12 @@ int run_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int 
 
 // Inputs of the draft kernel's acceptance-label mode (whole call; chunked below).
 struct LabelIn {
-  const float* target;  // [B, K+1, V]
-  const float* lse_t;   // [B, K+1]
-  const float* offq2;   // [B, K]
-  float* label;         // [B, K]
+  const float* target;  // [B, K+1, V] (label) or [B, V] target rows (residual, K = 1)
+  const float* lse_t;   // [B, K+1] (label)
+  const float* offq2;   // [B, K] (label)
+  float* label;         // [B, K] (label)
   float target_scale2;  // log2(e) / Tt
+  const dspark::ResRow* rows;  // [B] (residual), else null
 };
 
 // The persistent draft kernel over chunks of 128 requests.
@@ -238,16 +238,22 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.logits = logits ? logits + o * V : nullptr;
     p.lse = lse ? lse + o : nullptr;
     if (lab != nullptr) {
-      if (!encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                     lab->target + static_cast<size_t>(b0) * (K + 1) * V, V, K + 1, Bc,
-                     static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(K + 1) * V * 4, 32, 1,
+      // target rows per request: K + 1 of them (label), or the one draw row (residual)
+      const int trows = lab->rows ? K : K + 1;
+      const float* tchunk = lab->target + static_cast<size_t>(b0) * trows * V;
+      if (!encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tchunk, V, trows, Bc,
+                     static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(trows) * V * 4, 32, 1,
                      box_rows))
         return DSPARK_ERR_CUDA;
-      p.target = lab->target + static_cast<size_t>(b0) * (K + 1) * V;
-      p.lse_t = lab->lse_t + static_cast<size_t>(b0) * (K + 1);
-      p.offq2 = lab->offq2 + o;
-      p.label = lab->label + o;
+      p.target = tchunk;
       p.target_scale2 = lab->target_scale2;
+      if (lab->rows) {
+        p.rows = lab->rows + b0;
+      } else {
+        p.lse_t = lab->lse_t + static_cast<size_t>(b0) * (K + 1);
+        p.offq2 = lab->offq2 + o;
+        p.label = lab->label + o;
+      }
     }
     if (conf != nullptr) {
       p.conf_h = conf->h + o * conf->d;
@@ -371,11 +377,9 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
                 cudaSuccess &&
             cudaMalloc(&ctx->d_v_H, sizeof(float) * B_max * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_prev, sizeof(int32_t) * B_max) == cudaSuccess &&
-            cudaMalloc(&ctx->d_v_Lq, sizeof(float) * static_cast<size_t>(B_max) * V_max) ==
+            cudaMalloc(&ctx->d_v_P, sizeof(float) * static_cast<size_t>(B_max) * V_max) ==
                 cudaSuccess &&
-            cudaMalloc(&ctx->d_v_lse_q, sizeof(float) * B_max) == cudaSuccess &&
-            cudaMalloc(&ctx->d_v_rec, sizeof(dspark::VerifyRec) * B_max * dspark::kVerifyMaxPieces) ==
-                cudaSuccess &&
+            cudaMalloc(&ctx->d_v_rows, sizeof(dspark::ResRow) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_prev, sizeof(int32_t) * rows) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_offq2, sizeof(float) * rows) == cudaSuccess;
   ok = ok && cudaMemset(ctx->d_status, 0, sizeof(int)) == cudaSuccess &&
@@ -407,9 +411,8 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_v_U);
   cudaFree(ctx->d_v_H);
   cudaFree(ctx->d_v_prev);
-  cudaFree(ctx->d_v_Lq);
-  cudaFree(ctx->d_v_lse_q);
-  cudaFree(ctx->d_v_rec);
+  cudaFree(ctx->d_v_P);
+  cudaFree(ctx->d_v_rows);
   cudaFree(ctx->d_l_prev);
   cudaFree(ctx->d_l_offq2);
   cudaFree(ctx->d_topk_part_v);
@@ -660,6 +663,8 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   dspark::VerifyArgs v{};
   v.P = P;
   v.U = U;
+  v.W1 = W1;
+  v.W2 = W2;
   v.H = gated ? ctx->d_H : nullptr;
   v.tokens = tokens;
   v.logq = draft_logprobs;
@@ -681,29 +686,28 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   v.argmax_t = ctx->d_v_argmax_t;
   v.sel = ctx->d_v_sel;
   v.U_sel = ctx->d_v_U;
+  v.P_sel = ctx->d_v_P;
   v.H_sel = ctx->d_v_H;
   v.prev_sel = ctx->d_v_prev;
-  v.Lq = ctx->d_v_Lq;
-  v.lse_q = ctx->d_v_lse_q;
-  v.rec = ctx->d_v_rec;
+  v.rows = ctx->d_v_rows;
   int n = 0;
   cudaError_t e = dspark::launch_verify(v, s, &n);
   ctx->last_launches += n;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (target_temperature > 0.f && draft_temperature > 0.f) {
-    // q over the vocabulary at each request's draw position: the draft head in
-    // teacher-forced mode over one position of gathered rows
+  if (target_temperature > 0.f) {
+    // the draw: gathered rows and per-row constants, then the draft kernel's residual
+    // mode over one position (a greedy target's token is its argmax, set above)
     e = dspark::launch_verify_gather(v, s);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-    ctx->last_launches += 1;
-    st = run_draft(ctx, dspark::kModeTeacherForced, ctx->d_v_U, W1, W2, ctx->d_v_prev,
-                   ctx->d_v_prev, gated ? ctx->d_v_H : nullptr, B, 1, V, r, draft_temperature, 0,
-                   nullptr, nullptr, ctx->d_v_Lq, ctx->d_v_lse_q, nullptr, s);
+    ctx->last_launches += 2;
+    LabelIn res{ctx->d_v_P, nullptr, nullptr, nullptr, 1.4426950408889634f / target_temperature,
+                ctx->d_v_rows};
+    st = run_draft(ctx, dspark::kModeResidual, ctx->d_v_U, W1, W2, ctx->d_v_prev, ctx->d_v_prev,
+                   gated ? ctx->d_v_H : nullptr, B, 1, V, r, draft_temperature, seed, next_token,
+                   nullptr, nullptr, nullptr, nullptr, s, &res);
     if (st != DSPARK_OK) return st;
   }
-  e = dspark::launch_verify_race(v, ctx->num_sms, s, &n);
-  ctx->last_launches += n;
-  return cuda_status(e);
+  return DSPARK_OK;
 }
 
 int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
@@ -758,7 +762,7 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
   ctx->last_launches += 1;
   if (draft_temperature > 0.f && target_temperature > 0.f) {
     LabelIn lab{P, ctx->d_v_lse_t, ctx->d_l_offq2, label,
-                1.4426950408889634f / target_temperature};
+                1.4426950408889634f / target_temperature, nullptr};
     st = run_draft(ctx, dspark::kModeLabel, U, W1, W2, anchors, ctx->d_l_prev,
                    gated ? ctx->d_H : nullptr, B, K, V, r, draft_temperature, 0, nullptr, nullptr,
                    nullptr, nullptr, nullptr, s, &lab);

@@ -251,11 +251,59 @@ __device__ __forceinline__ void lse_merge(float& ma, float& sa, float mb, float 
   }
 }
 
+// One 16-token block's part in the two-stage race (w: the block's weights relative to
+// 2^m2, s = their sum, y: their scaled logits): stage 1 scores the block by
+// G = m2 + log2(s) - log2(E), E = -ln u1; a block that can still beat the best key
+// known for the request (this thread's, the CTA's, or the global one as last read)
+// runs stage 2, the first token whose cumulative weight exceeds u2 * s.
+__device__ __forceinline__ void race_block(const float (&w)[16], const float (&y)[16], float m2,
+                                           float bsum, uint32_t word1, uint32_t word2, int vbase,
+                                           uint32_t epoch, float inv_scale2,
+                                           unsigned long long* bound, unsigned long long gkey,
+                                           unsigned long long& bkey, float& yb, int& vb,
+                                           float& lb) {
+  const float G = m2 + lg2_approx(bsum) - lg2_approx(neg_log_uniform_fast(word1));
+  const unsigned long long sb = *bound;
+  const float S = key_score(sb > gkey ? sb : gkey);
+  if (bsum > 0.f && G >= S) {
+    float C[16];
+    C[0] = w[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) C[j] = C[j - 1] + w[j];
+    const float target = philox_uniform(word2) * C[15];
+    int js = -1, jl = 0;
+#pragma unroll
+    for (int j = 15; j >= 0; --j) {
+      if (target < C[j]) js = j;
+      if (jl == 0 && w[j] > 0.f) jl = j;
+    }
+    if (js < 0) js = jl;  // target at the very top (rounding): the last live token
+    float yj = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j == js) yj = y[j];
+    const unsigned long long key = make_key(epoch, G, vbase + js);
+    if (key > bkey) {
+      bkey = key;
+      yb = G;
+      vb = vbase + js;
+      lb = yj * inv_scale2;
+      atomicMax(bound, key);
+    }
+  }
+}
+
 template <int MODE, bool COPIES>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
-  constexpr bool kTF = MODE == kModeTeacherForced || MODE == kModeLabel;
-  constexpr bool kHalf = MODE == kModeLabel;  // ring slots of half tiles: U and target
+  // teacher-forced modes take the predecessors from the caller
+  constexpr bool kTF = MODE == kModeTeacherForced || MODE == kModeLabel || MODE == kModeResidual;
+  // ring slots of half tiles holding U and the target rows
+  constexpr bool kHalf = MODE == kModeLabel || MODE == kModeResidual;
+  // modes that draw a token by the block race
+  constexpr bool kRace = MODE == kModeSample || MODE == kModeResidual;
+  // modes whose per-request winners are published as 64-bit keys
+  constexpr bool kKeys = !kTF || MODE == kModeResidual;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -518,10 +566,18 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       // ---- stream the step's tiles
       float m2 = (MODE == kModeLabel) ? 0.f : -INFINITY, sum = 0.f;  // label: a plain sum
       float offq2 = 0.f, offp2 = 0.f;  // label: log2 q = l * scale2 + offq2, log2 p likewise
+      int res_pos = 0, res_excl = -1;  // residual: draw position, excluded token
       if (MODE == kModeLabel && row_ok) {
         const size_t o = static_cast<size_t>(b) * p.K + k;
         offq2 = __ldg(p.offq2 + o);
         offp2 = -__ldg(p.lse_t + o + b) * kLog2e;  // target row b * (K + 1) + k
+      }
+      if (MODE == kModeResidual && row_ok) {
+        const ResRow rr = p.rows[b];
+        offq2 = rr.offq2;
+        offp2 = rr.offp2;
+        res_pos = rr.pos;
+        res_excl = rr.excl;
       }
       float yb = -INFINITY, lb = 0.f;  // best score (G, or y when greedy) and its logit
       int vb = 0x7FFFFFFF;
@@ -542,6 +598,106 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         if (COPIES && (i & (ncopy - 1)) != copy) continue;  // another copy's tile
         ++tt;
+        if (kRace && row_ok) {
+          // every other tile, refresh the bound with the key read a tile earlier, so
+          // the load's latency is covered by a whole tile's work
+          if (tt > 0 && (tt & (kBoundRefresh - 1)) == 0 && key_epoch(kpre) == p.epoch &&
+              kpre > gkey)
+            gkey = kpre;
+          if (((tt + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
+        }
+        if (MODE == kModeResidual) {
+          // the verification draw: this thread's 16 tokens [16 g, 16 g + 16) of tile i
+          // (one block) come from fill 2 i + g / 2; every warp waits for and releases
+          // both fills, so each slot keeps one group of readers taking its fills in order
+          bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) {
+            fail = true;
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          uint32_t acc[16];
+          if (nkk > 0) {
+            tmem_ld_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(buf * kTileV + g * 16),
+                        acc);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0u;
+          }
+          float uval[16], pt[16];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = 2 * i + h, sh = j % nus;
+            bool okh = mbar_wait(&u_full[sh], static_cast<uint32_t>(j / nus) & 1u, p.timeout_ns,
+                                 abort_flag);
+            okh = __all_sync(0xFFFFFFFFu, okh);
+            if (!okh) {
+              fail = true;
+              *abort_flag = 1;
+              break;
+            }
+            uint32_t dep = 0u;
+            if (h == (g >> 1)) {
+              const uint8_t* row = sU + sh * 2 * ubox + b * 128;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint32_t off = static_cast<uint32_t>((((g & 1) * 4 + c) ^ (b & 7)) << 4);
+                const float4 x = *reinterpret_cast<const float4*>(row + off);
+                const float4 z = *reinterpret_cast<const float4*>(row + ubox + off);
+                uval[4 * c + 0] = x.x;
+                uval[4 * c + 1] = x.y;
+                uval[4 * c + 2] = x.z;
+                uval[4 * c + 3] = x.w;
+                pt[4 * c + 0] = z.x;
+                pt[4 * c + 1] = z.y;
+                pt[4 * c + 2] = z.z;
+                pt[4 * c + 3] = z.w;
+                dep ^= __float_as_uint(x.x) ^ __float_as_uint(z.x);
+              }
+            }
+            arrive_after_reads(&u_empty[sh], dep, s_sink, lane);
+          }
+          if (fail) break;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          if (!row_ok) continue;
+          const int tile = t_begin + t;
+          const int vbase = tile * kTileV + g * 16;
+          // weights max(0, p - q) (p alone for a bonus draw), relative to 2^0
+          float w[16];
+          float bsum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float lj = uval[j] + __uint_as_float(acc[j]);
+            const float pj = ex2_approx(fmaf(pt[j], p.target_scale2, offp2));
+            const float qj = ex2_approx(fmaf(lj, scale2, offq2));  // 0 when offq2 = -inf
+            float wj = fmaxf(0.f, pj - qj);
+            if (vbase + j >= p.V || vbase + j == res_excl) wj = 0.f;
+            w[j] = wj;
+            bsum += wj;
+          }
+          if ((tile >> 1) != nz_pair) {
+            nz_pair = tile >> 1;
+            philox4x32_10_rk(static_cast<uint32_t>(tile >> 1), static_cast<uint32_t>(res_pos),
+                             b_global, 9u + static_cast<uint32_t>(g), p.round_key0, p.round_key1,
+                             nz);
+          }
+          race_block(w, w, 0.f, bsum, (tile & 1) ? nz[2] : nz[0], (tile & 1) ? nz[3] : nz[1],
+                     vbase, p.epoch, inv_scale2, &s_bound[b], gkey, bkey, yb, vb, lb);
+          if ((tt & 1) == 1 && g == 0) {
+            const unsigned long long mine = s_bound[b];
+            if (mine > gkey) {
+              atomicMax(p.keys + k * kRows + b, mine);
+              gkey = mine;
+            }
+          }
+          continue;
+        }
         if (kHalf) {
           // label: tile i is ring fills 2 i (tokens 0-31) and 2 i + 1 (32-63), each
           // holding U and the target; this thread takes tokens 8 g .. 8 g + 7 of both
@@ -624,14 +780,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
           sum += acc2.x + acc2.y;
           continue;
-        }
-        if (MODE == kModeSample && row_ok) {
-          // every other tile, refresh the bound with the key read a tile earlier, so
-          // the load's latency is covered by a whole tile's work
-          if (tt > 0 && (tt & (kBoundRefresh - 1)) == 0 && key_epoch(kpre) == p.epoch &&
-              kpre > gkey)
-            gkey = kpre;
-          if (((tt + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
         }
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
         ok = ok && mbar_wait(&u_full[su], uph, p.timeout_ns, abort_flag);
@@ -742,41 +890,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             philox4x32_10_rk(static_cast<uint32_t>(tile >> 1), static_cast<uint32_t>(k), b_global,
                              1u + static_cast<uint32_t>(g), p.round_key0, p.round_key1, nz);
           }
-          const uint32_t word1 = (tile & 1) ? nz[2] : nz[0];
-          const uint32_t word2 = (tile & 1) ? nz[3] : nz[1];
-          // stage 1: the block's race score (log2 units)
-          const float G = m2 + lg2_approx(bsum) - lg2_approx(neg_log_uniform_fast(word1));
-          // Any key already reached for this request (by this thread, this CTA or,
-          // as last read, another CTA) bounds the winner from below.
-          const unsigned long long sb = s_bound[b];
-          const float S = key_score(sb > gkey ? sb : gkey);
-          if (bsum > 0.f && G >= S) {
-            // stage 2: inverse CDF inside the block (cumulative mass in token order)
-            float C[16];
-            C[0] = w[0];
-#pragma unroll
-            for (int j = 1; j < 16; ++j) C[j] = C[j - 1] + w[j];
-            const float target = philox_uniform(word2) * C[15];
-            int js = -1, jl = 0;
-#pragma unroll
-            for (int j = 15; j >= 0; --j) {
-              if (target < C[j]) js = j;
-              if (jl == 0 && w[j] > 0.f) jl = j;
-            }
-            if (js < 0) js = jl;  // target at the very top (rounding): the last live token
-            float yj = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j == js) yj = y[j];
-            const unsigned long long key = make_key(p.epoch, G, vbase + js);
-            if (key > bkey) {
-              bkey = key;
-              yb = G;
-              vb = vbase + js;
-              lb = yj * inv_scale2;
-              atomicMax(&s_bound[b], key);
-            }
-          }
+          race_block(w, y, m2, bsum, (tile & 1) ? nz[2] : nz[0], (tile & 1) ? nz[3] : nz[1], vbase,
+                     p.epoch, inv_scale2, &s_bound[b], gkey, bkey, yb, vb, lb);
           if ((tt & 1) == 1 && g == 0) {
             // share this CTA's best with the other CTAs (rate-limited)
             const unsigned long long mine = s_bound[b];
@@ -846,10 +961,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
         }
         unsigned long long key = 0ull;
-        if (!kTF && best_v != 0x7FFFFFFF) {
+        if (kKeys && best_v != 0x7FFFFFFF) {
           key = make_key(p.epoch, best_s, best_v);
           atomicMax(p.keys + k * kRows + b, key);
-          if (key >= gkey && k + 1 < p.K) {
+          if (!kTF && key >= gkey && k + 1 < p.K) {
             // this CTA may hold the winner: pull its Markov embedding into L2 so that
             // every CTA's gather for the next position hits L2
             const char* row = reinterpret_cast<const char*>(p.W1 + static_cast<size_t>(best_v) * p.r);
@@ -950,7 +1065,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         for (int k = e; k < p.K; k += kEpiWarps) {
           const DraftPartial* src = p.partials + (static_cast<size_t>(k) * kRows + bb) * ncta;
           const unsigned long long gkey =
-              kTF ? 0ull : __ldcg(p.keys + k * kRows + bb);
+              kKeys ? __ldcg(p.keys + k * kRows + bb) : 0ull;
           float M = -INFINITY, S = 0.f, lwin = 0.f;
           int found = 0;
           for (int c = lane; c < ncta; c += 32) {
@@ -958,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             float m2, s, lbest;
             load_partial(src + c, key, m2, s, lbest);
             lse_merge(M, S, m2, s);
-            if (!kTF && key == gkey) {
+            if (kKeys && key == gkey) {
               lwin = lbest;
               found = 1;
             }
@@ -986,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                 v = 0;
               }
               p.tokens[o] = v;
-              p.logprobs[o] = lwin * p.inv_t - lse_nat;
+              if (MODE != kModeResidual) p.logprobs[o] = lwin * p.inv_t - lse_nat;
               s_tok[k] = v;
             }
           }
@@ -1061,6 +1176,9 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
       break;
     case kModeLabel:  // half-tile ring slots: always the 128-row instantiation
       fn = reinterpret_cast<const void*>(&draft_kernel<kModeLabel, false>);
+      break;
+    case kModeResidual:
+      fn = reinterpret_cast<const void*>(&draft_kernel<kModeResidual, false>);
       break;
     default: return cudaErrorInvalidValue;
   }

@@ -28,6 +28,14 @@ struct DraftPartial {
   float pad;
 };
 
+// Per-request inputs of the draft kernel's residual mode (the verification draw).
+struct ResRow {
+  float offq2;  // log2 q(v) = l(v) * log2(e) / Td + offq2; -inf: no draft mass subtracted
+  float offp2;  // log2 p(v) = P(v) * log2(e) / Tt + offp2
+  int pos;      // draw position (noise counter)
+  int excl;     // token whose weight is zero (a greedy draft's rejected token), or -1
+};
+
 struct DraftParams {
   const uint16_t* W1;       // [V, r]
   const int32_t* anchors;   // [B] (chunk)
@@ -72,6 +80,8 @@ struct DraftParams {
   const float* offq2;       // [B, K] (chunk) log2 q(v) = l(v) * log2(e) / Td + offq2
   float* label;             // [B, K] (chunk) 1 - TV(q, p)
   float target_scale2;      // log2(e) / Tt
+  // residual mode (verification draw, K = 1): target rows through tm_p, per-row constants
+  const ResRow* rows;       // [B] (chunk), or null
 };
 
 struct DraftArgs {
@@ -82,7 +92,13 @@ struct DraftArgs {
   DraftParams p;
 };
 
-enum DraftMode { kModeSample = 0, kModeGreedy = 1, kModeTeacherForced = 2, kModeLabel = 3 };
+enum DraftMode {
+  kModeSample = 0,
+  kModeGreedy = 1,
+  kModeTeacherForced = 2,
+  kModeLabel = 3,
+  kModeResidual = 4,  // one position: block race over max(0, p - q) (the verification draw)
+};
 
 int draft_smem_bytes();
 int draft_threads();
@@ -117,8 +133,6 @@ cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anch
                         float* logprobs, const dspark_conf_args* conf, int* status,
                         cudaStream_t stream);
 // ---- speculative verification (verify.cu)
-constexpr int kVerifyMaxPieces = 64;
-
 struct VerifySel {  // where a request's draw happens and what feeds it
   int pos;          // position of the draw: the first rejection, or the window end (bonus)
   int residual;     // 1: residual max(0, p - q) at a rejection; 0: bonus from p
@@ -126,16 +140,11 @@ struct VerifySel {  // where a request's draw happens and what feeds it
   int prev;         // its predecessor (the anchor at position 0)
 };
 
-struct VerifyRec {  // best stage-1 block of one (request, piece) unit
-  float score;
-  float Z;
-  int blk;
-  int pad;
-};
-
 struct VerifyArgs {
   const float* P;             // [B, K+1, V] target logits
   const float* U;             // [B, K, V] base logits of the draft
+  const uint16_t* W1;         // [V, r]
+  const uint16_t* W2;         // [r, V]
   const float* H;             // [B, K, r] gate (null: ungated)
   const int32_t* tokens;      // [B, K] drafted tokens
   const float* logq;          // [B, K] the draft's log-probabilities of them (draft T > 0)
@@ -152,14 +161,15 @@ struct VerifyArgs {
   float* lse_t;               // [B, K+1]
   int32_t* argmax_t;          // [B, K+1]
   VerifySel* sel;             // [B]
-  float* U_sel;               // [B, V]
+  float* U_sel;               // [B, V] base-logit rows at the draw position
+  float* P_sel;               // [B, V] target rows at the draw position
   float* H_sel;               // [B, r]
   int32_t* prev_sel;          // [B]
-  float* Lq;                  // [B, V] draft logits at the draw position
-  float* lse_q;               // [B]
-  VerifyRec* rec;             // [B, kVerifyMaxPieces]
+  ResRow* rows;               // [B] the residual mode's per-row constants
 };
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches);
+// The draw's inputs: gathered rows and per-row constants (two kernels).
+cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream);
 // Log-sum-exp of P / Tt (argmax when greedy) of the rows (b, k <= min(ell[b], kmax))
 // of P [B, K+1, V]; ell null: every request's rows up to kmax.
 cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,

@@ -20,8 +20,8 @@
 //     target greedy: q(a), a the target's argmax.
 
 #include <cstdint>
-#include <cuda_bf16.h>
 
+#include "headlogit.cuh"
 #include "internal.h"
 #include "sm103.cuh"
 
@@ -29,24 +29,6 @@ namespace dspark {
 namespace {
 
 constexpr float kLog2eL = 1.4426950408889634f;
-
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t x) {
-  return __uint_as_float(static_cast<uint32_t>(x) << 16);
-}
-
-// l(v) of the draft head at (b, k) for one token v: warp-cooperative dot product.
-__device__ float head_logit(const LabelPrepArgs& a, int b, int k, int prev, int v, int lane) {
-  float acc = 0.f;
-  const float* hrow = a.H ? a.H + (static_cast<size_t>(b) * a.K + k) * a.r : nullptr;
-  for (int i = lane; i < a.r; i += 32) {
-    float e = bf16_bits_to_float(__ldg(a.W1 + static_cast<size_t>(prev) * a.r + i));
-    if (hrow) e = __bfloat162float(__float2bfloat16_rn(e * __ldg(hrow + i)));
-    acc = fmaf(e, bf16_bits_to_float(__ldg(a.W2 + static_cast<size_t>(i) * a.V + v)), acc);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  return acc + __ldg(a.U + (static_cast<size_t>(b) * a.K + k) * a.V + v);
-}
 
 __global__ void label_prep_kernel(const LabelPrepArgs a) {
   const int lane = threadIdx.x & 31;
@@ -70,7 +52,9 @@ __global__ void label_prep_kernel(const LabelPrepArgs a) {
     }
     return;
   }
-  const float lx = head_logit(a, b, k, prev, x, lane);
+  const float* urow = a.U + (static_cast<size_t>(b) * a.K + k) * a.V;
+  const float* hrow = a.H ? a.H + (static_cast<size_t>(b) * a.K + k) * a.r : nullptr;
+  const float lx = head_logit(urow, a.W1, a.W2, hrow, a.V, a.r, prev, x, lane);
   const float offq2 = (__ldg(a.logq + row) - lx * a.inv_td) * kLog2eL;
   if (lane == 0) a.offq2[row] = offq2;
   if (a.inv_tt == 0.f) {
@@ -79,7 +63,7 @@ __global__ void label_prep_kernel(const LabelPrepArgs a) {
       if (lane == 0) record_error(a.status, kStatusDeviceOob);
       am = 0;
     }
-    const float la = head_logit(a, b, k, prev, am, lane);
+    const float la = head_logit(urow, a.W1, a.W2, hrow, a.V, a.r, prev, am, lane);
     if (lane == 0) a.label[row] = fminf(1.f, exp2f(la * a.inv_td * kLog2eL + offq2));
   }
 }

@@ -20,20 +20,22 @@
 //                        log-probabilities give q(x)), the first failure ends
 //                        the prefix; records where the draw happens and what
 //                        feeds it;
-//   verify_gather_kernel copies the base-logit row (and gate row) of each
-//                        request's draw position, so that the draft kernel in
-//                        teacher-forced mode can rebuild q over the vocabulary;
-//   verify_race_kernel   (request, piece) units: stage 1 of the block race
-//                        over the residual (or, for a bonus, the target's)
-//                        weights, 16-token blocks per lane, two at a time;
-//   verify_finish_kernel one warp per request: the best block over pieces and
-//                        stage 2, the inverse CDF inside it.
+//   verify_gather_kernel copies the base-logit row (and gate row) and the target
+//                        row of each request's draw position;
+//   verify_prep_kernel   one warp per request: the offsets that turn the draft
+//                        head's logits and the target logits at the draw
+//                        position into log2 q and log2 p (the draft's
+//                        normaliser from its own log-probability of the
+//                        rejected token, rebuilt l(x) by a dot product);
+// then the draft kernel's residual mode streams the gathered rows and draws
+// from max(0, p - q) (p alone for a bonus) by the block race.
 // Noise: acceptance uniform of position k: Philox4x32-10 counter (k, 0, b, 13),
 // word 0; the draw's block race at position j: counter (beta >> 3, j, b,
 // 9 + (beta & 3)), words 2h (stage 1) and 2h + 1 (stage 2), h = (beta >> 2) & 1.
 
 #include <cstdint>
 
+#include "headlogit.cuh"
 #include "internal.h"
 #include "philox.cuh"
 #include "sm103.cuh"
@@ -44,7 +46,6 @@ namespace {
 constexpr float kLog2eV = 1.4426950408889634f;
 constexpr float kLn2V = 0.69314718055994531f;
 constexpr int kStatsThreads = 256;
-constexpr int kRaceThreads = 256;
 
 __device__ __forceinline__ float uniform_of(uint32_t word) { return philox_uniform(word); }
 
@@ -218,22 +219,29 @@ __global__ void verify_accept_kernel(const float* __restrict__ P, const int32_t*
   }
 }
 
-// Base-logit (and gate) rows of each request's draw position, for the draft
-// kernel's teacher-forced pass over one position.
-__global__ void verify_gather_kernel(const float* __restrict__ U, const float* __restrict__ H,
+// Base-logit (and gate) row and target row of each request's draw position, for
+// the draft kernel's residual mode.
+__global__ void verify_gather_kernel(const float* __restrict__ U, const float* __restrict__ P,
+                                     const float* __restrict__ H,
                                      const VerifySel* __restrict__ sel, int K, int V, int r,
-                                     float* __restrict__ U_sel, float* __restrict__ H_sel,
-                                     int32_t* __restrict__ prev_sel) {
+                                     float* __restrict__ U_sel, float* __restrict__ P_sel,
+                                     float* __restrict__ H_sel, int32_t* __restrict__ prev_sel) {
   const int b = blockIdx.y;
   const VerifySel s = sel[b];
   const int pos = min(s.pos, K - 1);  // a bonus row needs no q; any valid row will do
   const float4* src = reinterpret_cast<const float4*>(U + (static_cast<size_t>(b) * K + pos) * V);
+  const float4* psrc =
+      reinterpret_cast<const float4*>(P + (static_cast<size_t>(b) * (K + 1) + s.pos) * V);
   float4* dst = reinterpret_cast<float4*>(U_sel + static_cast<size_t>(b) * V);
-  // this CTA's 4096-float4 slice of the row, four loads in flight per thread
+  float4* pdst = reinterpret_cast<float4*>(P_sel + static_cast<size_t>(b) * V);
+  // this CTA's 4096-float4 slice of both rows
   const int i0 = blockIdx.x * 4096;
   const int i1 = min(V / 4, i0 + 4096);
 #pragma unroll 4
-  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) dst[i] = __ldcs(src + i);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    dst[i] = __ldcs(src + i);
+    pdst[i] = __ldcs(psrc + i);
+  }
   if (blockIdx.x != 0) return;
   if (H != nullptr) {
     const float* hs = H + (static_cast<size_t>(b) * K + pos) * r;
@@ -242,156 +250,28 @@ __global__ void verify_gather_kernel(const float* __restrict__ U, const float* _
   if (threadIdx.x == 0) prev_sel[b] = s.prev;
 }
 
-// Weight of token v for request b (16 values of one block at a time).
-struct RaceIn {
-  const float* P;       // [B, K+1, V]
-  const float* Lq;      // [B, V] draft logits at the draw position (null: draft greedy)
-  const float* lse_t;   // [B, K+1]
-  const float* lse_q;   // [B]
-  const VerifySel* sel;
-  int B, K, V, pieces, piece_len;
-  float inv_tt, inv_td;
-  uint32_t seed_lo, seed_hi;
-  VerifyRec* rec;       // [B][pieces]
-};
-
-__device__ __forceinline__ void block_weights(const RaceIn& a, int b, const VerifySel& s, int v0,
-                                              float (&w)[16]) {
-  const size_t prow = (static_cast<size_t>(b) * (a.K + 1) + s.pos) * a.V;
-  const float lt = a.lse_t[static_cast<size_t>(b) * (a.K + 1) + s.pos];
-  const float lq = (a.Lq != nullptr) ? a.lse_q[b] : 0.f;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int v = v0 + 4 * c;
-    float4 pv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    float4 qv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (v < a.V) {
-      pv = __ldcs(reinterpret_cast<const float4*>(a.P + prow + v));
-      if (s.residual && a.Lq != nullptr)
-        qv = __ldcs(reinterpret_cast<const float4*>(a.Lq + static_cast<size_t>(b) * a.V + v));
-    }
-    const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
-    const float qs[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float p = expf(ps[e] * a.inv_tt - lt);
-      float q = 0.f;
-      if (s.residual) q = (a.Lq != nullptr) ? expf(qs[e] * a.inv_td - lq) : ((v + e == s.x) ? 1.f : 0.f);
-      w[4 * c + e] = s.residual ? fmaxf(0.f, p - q) : p;
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kRaceThreads) verify_race_kernel(const __grid_constant__ RaceIn a) {
-  const int unit = blockIdx.x;
-  const int b = unit / a.pieces, piece = unit - b * a.pieces;
-  const VerifySel s = a.sel[b];
-  const int v_begin = piece * a.piece_len, v_end = min(a.V, v_begin + a.piece_len);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float best = -INFINITY, bestZ = 0.f;
-  int bestblk = 0x7FFFFFFF;
-  for (int v00 = v_begin + threadIdx.x * 16; v00 < v_end; v00 += 2 * kRaceThreads * 16) {
-    float w2[2][16];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) block_weights(a, b, s, v00 + h * kRaceThreads * 16, w2[h]);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-    const int v0 = v00 + h * kRaceThreads * 16;
-    if (v0 >= v_end) break;
-    float Z = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) Z += w2[h][j];
-    if (!(Z > 0.f)) continue;
-    const uint32_t blk = static_cast<uint32_t>(v0 >> 4);
-    const Philox4 rnd = philox4x32_10(blk >> 3, static_cast<uint32_t>(s.pos), static_cast<uint32_t>(b),
-                                      9u + (blk & 3u), a.seed_lo, a.seed_hi);
-    const uint32_t word1 = ((blk >> 2) & 1u) ? rnd.w[2] : rnd.w[0];
-    const float sc = logf(Z) - logf(neg_log_uniform_accurate(uniform_of(word1)));
-    if (sc > best || (sc == best && static_cast<int>(blk) < bestblk)) {
-      best = sc;
-      bestZ = Z;
-      bestblk = static_cast<int>(blk);
-    }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-    const float oz = __shfl_xor_sync(0xFFFFFFFFu, bestZ, off);
-    const int ok = __shfl_xor_sync(0xFFFFFFFFu, bestblk, off);
-    if (ob > best || (ob == best && ok < bestblk)) {
-      best = ob;
-      bestZ = oz;
-      bestblk = ok;
-    }
-  }
-  __shared__ float s_b[kRaceThreads / 32], s_z[kRaceThreads / 32];
-  __shared__ int s_k[kRaceThreads / 32];
-  if (lane == 0) {
-    s_b[warp] = best;
-    s_z[warp] = bestZ;
-    s_k[warp] = bestblk;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kRaceThreads / 32; ++w)
-      if (s_b[w] > best || (s_b[w] == best && s_k[w] < bestblk)) {
-        best = s_b[w];
-        bestZ = s_z[w];
-        bestblk = s_k[w];
-      }
-    VerifyRec rc;
-    rc.score = best;
-    rc.Z = bestZ;
-    rc.blk = bestblk;
-    a.rec[unit] = rc;
-  }
-}
-
-__global__ void verify_finish_kernel(const __grid_constant__ RaceIn a, int32_t* __restrict__ next_token,
-                                     int* status) {
+// One warp per request: the residual mode's per-row constants.
+__global__ void verify_prep_kernel(const float* __restrict__ U, const uint16_t* __restrict__ W1,
+                                   const uint16_t* __restrict__ W2, const float* __restrict__ H,
+                                   const float* __restrict__ logq, const float* __restrict__ lse_t,
+                                   const VerifySel* __restrict__ sel, int B, int K, int V, int r,
+                                   float inv_td, int draft_greedy, ResRow* __restrict__ rows) {
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (b >= a.B) return;
-  // best block over the pieces
-  float best = -INFINITY, bestZ = 0.f;
-  int bestblk = 0x7FFFFFFF;
-  for (int pc = 0; pc < a.pieces; ++pc) {
-    const VerifyRec rc = a.rec[static_cast<size_t>(b) * a.pieces + pc];
-    if (rc.score > best || (rc.score == best && rc.blk < bestblk)) {
-      best = rc.score;
-      bestZ = rc.Z;
-      bestblk = rc.blk;
-    }
+  if (b >= B) return;
+  const VerifySel s = sel[b];
+  ResRow rr;
+  rr.pos = s.pos;
+  rr.offp2 = -lse_t[static_cast<size_t>(b) * (K + 1) + s.pos] * kLog2eV;
+  rr.offq2 = -INFINITY;  // bonus, or a greedy draft: no draft mass to subtract
+  rr.excl = (s.residual && draft_greedy) ? s.x : -1;
+  if (s.residual && !draft_greedy) {
+    const size_t row = static_cast<size_t>(b) * K + s.pos;
+    const float lx = head_logit(U + row * V, W1, W2, H ? H + row * r : nullptr, V, r, s.prev,
+                                s.x, lane);
+    rr.offq2 = (__ldg(logq + row) - lx * inv_td) * kLog2eV;
   }
-  if (bestblk == 0x7FFFFFFF) {  // no mass anywhere: nothing valid to draw
-    if (lane == 0) {
-      record_error(status, kStatusDeviceOob);
-      next_token[b] = 0;
-    }
-    return;
-  }
-  const VerifySel s = a.sel[b];
-  // stage 2: the inverse CDF of the block's weights, in token order (lanes 0..15)
-  float w[16];
-  block_weights(a, b, s, bestblk * 16, w);
-  const uint32_t blk = static_cast<uint32_t>(bestblk);
-  const Philox4 rnd = philox4x32_10(blk >> 3, static_cast<uint32_t>(s.pos), static_cast<uint32_t>(b),
-                                    9u + (blk & 3u), a.seed_lo, a.seed_hi);
-  const uint32_t word2 = ((blk >> 2) & 1u) ? rnd.w[3] : rnd.w[1];
-  const float target = uniform_of(word2) * bestZ;
-  float C = 0.f;
-  int pick = -1, last = -1;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (w[j] > 0.f) {
-      C += w[j];
-      last = j;
-      if (pick < 0 && target < C) pick = j;
-    }
-  }
-  if (pick < 0) pick = last;  // target at the very top (rounding): the last live token
-  if (lane == 0) next_token[b] = bestblk * 16 + pick;
+  if (lane == 0) rows[b] = rr;
 }
 
 }  // namespace
@@ -426,45 +306,16 @@ cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launche
 
 cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream) {
   const dim3 grid((v.V / 4 + 4095) / 4096, v.B);
-  verify_gather_kernel<<<grid, 256, 0, stream>>>(v.U, v.H, v.sel, v.K, v.V, v.r, v.U_sel, v.H_sel,
-                                                 v.prev_sel);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_verify_race(const VerifyArgs& v, int num_sms, cudaStream_t stream,
-                               int* launches) {
-  *launches = 0;
-  if (v.target_temperature <= 0.f) return cudaSuccess;  // greedy target: decided already
-  RaceIn a{};
-  a.P = v.P;
-  a.Lq = (v.draft_temperature > 0.f) ? v.Lq : nullptr;
-  a.lse_t = v.lse_t;
-  a.lse_q = v.lse_q;
-  a.sel = v.sel;
-  a.B = v.B;
-  a.K = v.K;
-  a.V = v.V;
-  a.inv_tt = 1.0f / v.target_temperature;
-  a.inv_td = (v.draft_temperature > 0.f) ? 1.0f / v.draft_temperature : 1.f;
-  a.seed_lo = v.seed_lo;
-  a.seed_hi = v.seed_hi;
-  a.rec = v.rec;
-  // pieces of whole 4096-token chunks so that about four units run per SM
-  const int chunk = kRaceThreads * 16;
-  const int most = (v.V + chunk - 1) / chunk;
-  int pieces = (4 * num_sms + v.B - 1) / v.B;
-  pieces = pieces < 1 ? 1 : (pieces > most ? most : pieces);
-  if (pieces > kVerifyMaxPieces) pieces = kVerifyMaxPieces;
-  const int per = (most + pieces - 1) / pieces;
-  a.piece_len = per * chunk;
-  a.pieces = (v.V + a.piece_len - 1) / a.piece_len;
-  verify_race_kernel<<<v.B * a.pieces, kRaceThreads, 0, stream>>>(a);
+  verify_gather_kernel<<<grid, 256, 0, stream>>>(v.U, v.P, v.H, v.sel, v.K, v.V, v.r, v.U_sel,
+                                                 v.P_sel, v.H_sel, v.prev_sel);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  verify_finish_kernel<<<(v.B + 3) / 4, 128, 0, stream>>>(a, v.next_token, v.status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  *launches = 2;
-  return cudaSuccess;
+  const int greedy_d = v.draft_temperature > 0.f ? 0 : 1;
+  const float inv_td = greedy_d ? 1.f : 1.0f / v.draft_temperature;
+  verify_prep_kernel<<<(v.B + 7) / 8, 256, 0, stream>>>(v.U, v.W1, v.W2, v.H, v.logq, v.lse_t,
+                                                        v.sel, v.B, v.K, v.V, v.r, inv_td,
+                                                        greedy_d, v.rows);
+  return cudaGetLastError();
 }
 
 }  // namespace dspark
