@@ -20,8 +20,11 @@
 //     tokens, so the producer runs ahead across step boundaries;
 //   * warp 1 (one lane) issues tcgen05.mma: D[128 requests x 64 tokens] =
 //     E[128 x r] * W2tile[r x 64] into one of four TMEM accumulators;
-//     E is the gathered Markov embedding of every request (K-major, 128B
-//     swizzle), W2 the MN-major tile exactly as TMA wrote it;
+//     E is the gathered Markov embedding of every request, gathered into
+//     shared memory (K-major, 128B swizzle) and copied once per position into
+//     TMEM (row m in lane m, two bf16 per column), from where the MMAs read it
+//     (each MMA would otherwise re-read its A slice from shared memory); W2 is
+//     the MN-major tile exactly as TMA wrote it;
 //   * warps 2..17 (the epilogue) read the accumulator (one request per TMEM
 //     lane, 16 tokens per thread) and U from shared memory, and keep, per
 //     request, a running log-sum-exp and a running block-race winner, so the
@@ -96,7 +99,10 @@ constexpr uint32_t kOffU = kOffW2 + kNumW2Stages * kW2StageBytes;
 constexpr uint32_t kOffBar = kOffU + kNumUStages * kUStageBytes;
 constexpr uint32_t kBarRegion = 2048;
 constexpr uint32_t kSmemBytes = kOffBar + kBarRegion + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = kNumAcc * kTileV;             // 256
+// TMEM: kNumAcc accumulators of 64 columns, then the MMA's A operand ([128 x r] bf16,
+// two elements per column: r / 2 <= 128 columns)
+constexpr uint32_t kTmemA = kNumAcc * kTileV;                // 256
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;                          // named barrier id
 constexpr int kBoundRefresh = BOUND_REFRESH;  // tiles between reads of the global bound
 constexpr uint32_t kBackoffControlNs = 200;  // sleep between polls of the TMA / MMA lanes
@@ -106,6 +112,7 @@ constexpr uint32_t kTokenBits = 18;                          // V <= 2^18
 constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
 
 static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103 limit");
+static_assert(kTmemA + kMaxRank / 2 <= kTmemCols, "TMEM columns");
 static_assert((kNumAcc & (kNumAcc - 1)) == 0, "accumulator count must be a power of two");
 static_assert((2 * kNumW2Stages + 2 * kNumUStagesSmall + 2 * kNumAcc + 5) * 8 + 2 * kMaxK * 4 +
                       kRows * 8 + 16 <=
@@ -472,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileV);
             const uint32_t b0 = smem_addr(sW + s * kW2StageBytes);
             for (int kk = 0; kk < nkk; ++kk) {
-              const uint64_t ad = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = smem_desc(b0 + kk * 2048, 1024, 1024);
-              umma_bf16(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+              umma_bf16_ts(d_tmem, tmem_base + kTmemA + static_cast<uint32_t>(kk * 8), bd, idesc,
+                           kk > 0 ? 1u : 0u);
             }
             umma_commit(&w_empty[s]);
             umma_commit(&acc_full[buf]);
@@ -558,6 +565,28 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
       fence_proxy_async_smem();
       named_bar_sync(kEpiBarrier, kEpiThreads);
+      {
+        // copy the operand into TMEM: each warp its lane quadrant's rows m = q*32 + lane,
+        // K chunk e / 4 (64 bf16 = 32 columns); the previous position's MMAs finished
+        // with the TMEM copy before the speculative gather (a_empty)
+        const int m = q * 32 + lane, cc = e >> 2;
+        const uint8_t* src = sA + cc * 16384 + (m >> 3) * 1024 + (m & 7) * 128;
+        uint32_t wv[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + ((u ^ (m & 7)) << 4));
+          wv[4 * u + 0] = x.x;
+          wv[4 * u + 1] = x.y;
+          wv[4 * u + 2] = x.z;
+          wv[4 * u + 3] = x.w;
+        }
+        tmem_st_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kTmemA +
+                        static_cast<uint32_t>(cc * 32),
+                    wv);
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+      }
       if (etid == 0) {
         mbar_arrive(a_full);
         trace_stamp(p, cta, k, 1);
