@@ -20,6 +20,20 @@ def test_algorithmic_bytes_per_block():
     assert bench.algorithmic_bytes(4, CONFIGS[4]) == 2_596_536_320
 
 
+def test_verify_and_label_bytes():
+    B, K, V, r = 128, 16, 151936, 256
+    c = CONFIGS[2]
+    # every verified target row (window and bonus), W2, and the base-logit, embedding and
+    # target rows at the draw position
+    assert bench.verify_bytes(c) == (B * (K + 1) * V * 4 + r * V * 2 + B * V * 4 + B * r * 2
+                                     + B * V * 4)
+    # U and the target rows of the K positions once, W2 once, the gathered embeddings
+    assert bench.label_bytes(c) == 2 * B * K * V * 4 + r * V * 2 + B * K * r * 2
+    assert bench.metric_of("label") == bench.LABEL_METRIC
+    assert bench.metric_of("verify") == bench.VERIFY_METRIC
+    assert bench.metric_of("serving") == bench.METRIC
+
+
 def test_replica_seeds_are_distinct_per_rank_and_step():
     seeds = {bench.replica_seed(r, s) for r in range(8) for s in range(100)}
     assert len(seeds) == 800
