@@ -134,3 +134,15 @@ def test_verify_serving_size(dsp):
     tokens, out = _run(dsp, inp, P, 1.0, 1.0, seed=11)
     assert np.all(out["n_acc"] <= 16)
     _check(inp, P, tokens, out, 1.0, 1.0, seed=11, requests=[0, 77, 127])
+
+
+@pytest.mark.parametrize("Td", [1.0, 0.0])
+def test_verify_two_request_chunks(dsp, Td):
+    """130 requests: the draw runs over two chunks of 128 rows (per-row constants, target
+    rows and noise counters offset by the chunk)."""
+    B, K, V, r = 130, 3, 1000, 64
+    inp = make_inputs(68, B, K, V, r, weight_std=0.1)
+    P = _target_logits(np.random.default_rng(69), inp.U)
+    tokens, out = _run(dsp, inp, P, Td, 1.0, seed=13)
+    assert np.all((out["next_token"] >= 0) & (out["next_token"] < V))
+    _check(inp, P, tokens, out, Td, 1.0, seed=13)
