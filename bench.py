@@ -42,6 +42,10 @@ if ROOT not in sys.path:
 METRIC = "Markov-head draft tokens/s at B=128 K=16 V=151936; % of HBM roofline"
 VERIFY_METRIC = "verified draft tokens/s (speculative verification) at B=128 K=16 V=151936"
 LABEL_METRIC = "acceptance labels/s (1 - TV of draft and target) at B=128 K=16 V=151936"
+SCHEDULE_METRIC = "load-aware verify-window schedules/s at R=128 requests K=16"
+STS_METRIC = "sequential temperature scaling fits/s at N=8192 rows K=16"
+# single-CTA kernels (the scheduler, the STS fit): one SM's 32-bit lanes at the maximum clock
+SM_LANE_OPS = 128 * 2.07e9
 L2_FLUSH_BYTES = 512 << 20       # larger than the 129 MB L2
 CONF_THRESHOLD = 0.3
 
@@ -57,7 +61,12 @@ WORKLOADS = {
     "label": (2, "acceptance labels of the serving batch's drafted block: B=128 K=16 V=151936 "
                  "r=256, synthetic target logits (draft base logits + N(0,1)), "
                  "T_draft = T_target = 1"),
+    "schedule": (None, "load-aware prefix scheduler: R=128 requests x K=16 extensions, survival "
+                       "products of U(0.4, 0.995) confidences, smooth saturating SPS(B)"),
+    "sts": (None, "sequential temperature scaling: N=8192 calibration rows x K=16, raw "
+                  "confidences of a head 2.5x too sharp, 0/1 acceptance outcomes"),
 }
+SMALL = {"schedule": dict(R=128, K=16, seed=3003), "sts": dict(N=8192, K=16, seed=3004)}
 VERIFY_TARGET_SEED = 2002
 
 
@@ -77,7 +86,23 @@ def label_bytes(c: dict) -> int:
 
 
 def metric_of(workload: str) -> str:
-    return {"verify": VERIFY_METRIC, "label": LABEL_METRIC}.get(workload, METRIC)
+    return {"verify": VERIFY_METRIC, "label": LABEL_METRIC, "schedule": SCHEDULE_METRIC,
+            "sts": STS_METRIC}.get(workload, METRIC)
+
+
+def schedule_ops(R: int, K: int) -> int:
+    """Element-steps of the scheduler: the bitonic network over the candidates padded to a
+    power of two (every stage touches every element), the prefix sum and the cut."""
+    n = 1
+    while n < R * K:
+        n <<= 1
+    lg = n.bit_length() - 1
+    return n * lg * (lg + 1) // 2 + 2 * R * K
+
+
+def sts_ops(N: int, K: int) -> int:
+    """Cross-entropy evaluations of the fit: every row, position, round and grid point."""
+    return N * K * 8 * 32
 
 
 def algorithmic_bytes(cfg: int, c: dict) -> int:
@@ -332,9 +357,141 @@ def label_cpu_baseline(inp, c, target_s, dtok):
                       f"(fp64 oracle, {threads} OpenMP threads, {spent:.1f} s)"}
 
 
+def small_inputs(workload: str):
+    from synth import schedule_inputs, sts_inputs
+    c = SMALL[workload]
+    if workload == "schedule":
+        return schedule_inputs(c["seed"], c["R"], c["K"])
+    return sts_inputs(c["seed"], c["N"], c["K"])
+
+
+def run_reference_small(args, rank, world):
+    """The oracle's scheduler or STS fit, one call per step."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    x, y = small_inputs(args.workload)
+    c = SMALL[args.workload]
+
+    def one():
+        t0 = time.perf_counter()
+        if args.workload == "schedule":
+            oracle.schedule(x.astype(np.float64), y.astype(np.float64))
+        else:
+            oracle.sts_fit(x, y)
+        return time.perf_counter() - t0
+    for _ in range(args.warmup):
+        one()
+    spent = sum(one() for _ in range(args.steps))
+    value = args.steps / spent
+    unit = "schedules/s" if args.workload == "schedule" else "fits/s"
+    threads = oracle.max_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": metric_of(args.workload), "value": value, "unit": unit,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * spent / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload][1], **c},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} whole calls"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours_small(args, rank, world, local):
+    """The scheduler or the STS fit on the GPU: device time per call, inputs resident, L2
+    flushed between calls; roofline against one SM's 32-bit lane rate (single-CTA kernels)."""
+    import torch
+    from rank_markov_draft_gb300 import binding
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    c = SMALL[args.workload]
+    x, y = small_inputs(args.workload)
+    X, Y = torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev)
+    ctx = binding.Context(local, B_max=c.get("R", 1), V_max=8, K_max=c["K"])
+    stream = torch.cuda.current_stream(dev)
+    if args.workload == "schedule":
+        R, K = c["R"], c["K"]
+        ell = torch.empty(R, dtype=torch.int32, device=dev)
+        theta = torch.empty(1, dtype=torch.float32, device=dev)
+        step = lambda: binding.dspark_schedule(ctx, X, R, K, Y, ell, theta, stream)
+        ops, unit = schedule_ops(R, K), "schedules/s"
+    else:
+        N, K = c["N"], c["K"]
+        tau = torch.empty(K, dtype=torch.float32, device=dev)
+        loss = torch.empty(K, dtype=torch.float32, device=dev)
+        step = lambda: binding.dspark_sts_fit(ctx, X, Y, N, K, 1.0 / 64, 64.0, tau, loss, stream)
+        ops, unit = sts_ops(N, K), "fits/s"
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_id(dev))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    if ctx.status() != 0:
+        raise RuntimeError(f"device status {ctx.status()} in the timed region")
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_max = max_over_ranks(sum(per_ms), world, dev)
+    value = world * args.steps / (ms_max / 1000.0)
+    med = statistics.median(per_ms)
+    achieved = ops / (med / 1000.0)
+    if rank == 0:
+        cpu = None
+        if not args.skip_cpu:
+            import oracle
+            oracle.build()
+            t0, n = time.perf_counter(), 0
+            while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0) or n == 0:
+                if args.workload == "schedule":
+                    oracle.schedule(x.astype(np.float64), y.astype(np.float64))
+                else:
+                    oracle.sts_fit(x, y)
+                n += 1
+            spent = time.perf_counter() - t0
+            cpu = {"value": n / spent, "unit": unit, "cores": oracle.max_threads(),
+                   "kind": "oracle", "sample": f"{n} whole calls ({spent:.1f} s)"}
+        print(json.dumps({
+            "metric": metric_of(args.workload), "value": round(value, 1), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.workload][1], **c,
+                       "l2": "flushed between calls (512 MB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "alu", "achieved": round(achieved / 1e9, 3),
+                         "peak": round(SM_LANE_OPS / 1e9, 1), "unit": "Gop/s",
+                         "frac": round(achieved / SM_LANE_OPS, 4), "traffic": None,
+                         "peak_source": "one SM's 32-bit lanes (128) at 2070 MHz: the kernel "
+                                        "is one CTA by design",
+                         "kernel": "schedule_kernel" if args.workload == "schedule"
+                         else "sts_fit_kernel",
+                         "ops_per_launch": ops, "median_launch_us": round(med * 1000, 2)},
+            "cpu_baseline": cpu, "e2e": None, "clocks": clk, "gpu_launches": args.steps,
+        }), flush=True)
+    ctx.close()
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: per step one request of the workload."""
     from synth import CONFIGS, config_inputs
+    if args.workload in SMALL:
+        run_reference_small(args, rank, world)
+        return
     cfg, desc = WORKLOADS[args.workload]
     c = dict(CONFIGS[cfg])
     if rank != 0:
@@ -631,6 +788,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload in SMALL:
+        run_ours_small(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
 

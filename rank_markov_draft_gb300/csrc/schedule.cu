@@ -12,7 +12,8 @@
 // One CTA: the R x K candidates are packed into 64-bit keys (ordered survival
 // bits | inverted position | inverted request), sorted descending by a bitonic
 // network in shared memory, their survivals summed by a block scan in that
-// order, and the first admission that would not raise Theta cuts the list.
+// order, and the first admission that would not raise Theta cuts the list; each
+// request's length is one past its last admitted position (no atomics).
 
 #include <cstdint>
 
@@ -55,23 +56,31 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* __
   }
   if (tid == 0) s_cut = n;
   __syncthreads();
-  // bitonic sort, descending
+  // bitonic sort, descending: every stage is n_pow2 / 2 compare-exchanges, one pair per
+  // thread at a time; a stage with stride < 32 keeps each warp inside its own 64-key
+  // block (pairs 32w .. 32w + 31 cover keys 64w .. 64w + 63), so it needs only a warp
+  // barrier, and a block barrier is taken only after a stage with a larger stride
+  const int pairs = n_pow2 >> 1;
   for (int size = 2; size <= n_pow2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n_pow2; i += kSchedThreads) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const unsigned long long x = s_key[i], y = s_key[j];
-          const bool desc = (i & size) == 0;
-          if (desc ? (x < y) : (x > y)) {
-            s_key[i] = y;
-            s_key[j] = x;
-          }
+      for (int t = tid; t < pairs; t += kSchedThreads) {
+        // pair t: (t / stride) * 2 * stride + t % stride (stride is a power of two)
+        const int i = 2 * t - (t & (stride - 1)), j = i + stride;
+        const unsigned long long x = s_key[i], y = s_key[j];
+        const bool desc = (i & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          s_key[i] = y;
+          s_key[j] = x;
         }
       }
-      __syncthreads();
+      if (stride >= 32 || pairs > kSchedThreads || (stride == 1 && size >= 64)) {
+        __syncthreads();
+      } else {
+        __syncwarp();
+      }
     }
   }
+  __syncthreads();
   // inclusive prefix sums of the survivals in rank order: each thread sums a
   // contiguous slice, the slice totals are scanned by warp 0
   const int per = (n_pow2 + kSchedThreads - 1) / kSchedThreads;
@@ -104,22 +113,40 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* __
   const float base = incl - tot + (warp > 0 ? s_part[warp - 1] : 0.f);
   for (int i = i0; i < i1; ++i) s_sum[i] += base;
   __syncthreads();
-  // the first candidate whose admission would not raise Theta
+  // the first candidate whose admission would not raise Theta: each thread's first such
+  // candidate (its indices ascend), the warp's minimum, one shared atomic per warp
+  int mine = n;
   for (int i = tid; i < n; i += kSchedThreads) {
     const float prev = static_cast<float>(R) + (i > 0 ? s_sum[i - 1] : 0.f);
     const float cur = static_cast<float>(R) + s_sum[i];
     const float th_prev = prev * sps[R + i];
     const float th_next = cur * sps[R + i + 1];
-    if (!(th_next > th_prev)) atomicMin(&s_cut, i);
+    if (!(th_next > th_prev)) {
+      mine = i;
+      break;
+    }
   }
+  mine = __reduce_min_sync(0xFFFFFFFFu, mine);
+  if (lane == 0 && mine < n) atomicMin(&s_cut, mine);
   __syncthreads();
   const int cut = s_cut;
-  for (int i = tid; i < cut; i += kSchedThreads) {
-    const int r = static_cast<int>(0xFFFFu - static_cast<uint32_t>(s_key[i] & 0xFFFFull));
-    atomicAdd(&ell[r], 1);
-  }
   if (tid == 0 && theta != nullptr)
     *theta = (static_cast<float>(R) + (cut > 0 ? s_sum[cut - 1] : 0.f)) * sps[R + cut];
+  __syncthreads();
+  // every candidate's rank (reusing the prefix sums' storage); the admitted positions of a
+  // request form a prefix, so its last admitted position k gives ell = k + 1 (no atomics)
+  int* s_rank = reinterpret_cast<int*>(s_sum);
+  for (int i = tid; i < n; i += kSchedThreads) {
+    const unsigned long long key = s_key[i];
+    const int r = static_cast<int>(0xFFFFu - static_cast<uint32_t>(key & 0xFFFFull));
+    const int k = static_cast<int>(0xFFFFu - static_cast<uint32_t>((key >> 16) & 0xFFFFull));
+    s_rank[r * K + k] = i;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < n; idx += kSchedThreads) {
+    const int r = idx / K, k = idx - r * K;
+    if (s_rank[idx] < cut && (k + 1 == K || s_rank[idx + 1] >= cut)) ell[r] = k + 1;
+  }
 }
 
 }  // namespace

@@ -162,3 +162,24 @@ def config_inputs(cfg: int) -> DraftInputs:
                        gated=c.get("gated", False), confidence=c.get("confidence", False),
                        selector=c.get("selector", False),
                        selector_tables_only=c.get("selector", False))
+
+
+def schedule_inputs(seed: int, R: int, K: int):
+    """Survival products a [R, K] (cumulative products of per-position confidences drawn
+    from U(0.4, 0.995)) and a smooth saturating steps-per-second table SPS(B),
+    B = 0 .. R (K + 1), as float32."""
+    rng = np.random.default_rng(seed)
+    a = np.cumprod(rng.uniform(0.4, 0.995, (R, K)), axis=1).astype(np.float32)
+    B = np.arange(R * (K + 1) + 1, dtype=np.float64)
+    sps = (3000.0 / (1.0 + (B / (0.6 * R * (K + 1))) ** 2)).astype(np.float32)
+    return a, sps
+
+
+def sts_inputs(seed: int, N: int, K: int, spread: float = 2.0, sharpness: float = 2.5):
+    """Raw confidences [N, K] = sigmoid(z), z ~ N(0, spread^2), of a head that is too sharp by
+    `sharpness`, and 0/1 acceptance outcomes drawn at sigmoid(z / sharpness), as float32."""
+    rng = np.random.default_rng(seed)
+    z = rng.normal(0.0, spread, (N, K))
+    conf = (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+    outcome = (rng.uniform(size=(N, K)) < 1.0 / (1.0 + np.exp(-z / sharpness))).astype(np.float32)
+    return conf, outcome

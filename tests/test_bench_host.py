@@ -34,6 +34,17 @@ def test_verify_and_label_bytes():
     assert bench.metric_of("serving") == bench.METRIC
 
 
+def test_single_cta_kernel_op_counts():
+    # 2048 candidates: a bitonic network of 11 * 12 / 2 = 66 stages over every element,
+    # then the prefix sum and the cut
+    assert bench.schedule_ops(128, 16) == 2048 * 66 + 2 * 2048
+    assert bench.schedule_ops(7, 3) == 32 * 15 + 2 * 21  # 21 candidates padded to 32
+    # every row x position x round (8) x grid point (32)
+    assert bench.sts_ops(8192, 16) == 8192 * 16 * 8 * 32
+    assert bench.metric_of("schedule") == bench.SCHEDULE_METRIC
+    assert bench.metric_of("sts") == bench.STS_METRIC
+
+
 def test_replica_seeds_are_distinct_per_rank_and_step():
     seeds = {bench.replica_seed(r, s) for r in range(8) for s in range(100)}
     assert len(seeds) == 800
