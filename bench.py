@@ -44,8 +44,14 @@ VERIFY_METRIC = "verified draft tokens/s (speculative verification) at B=128 K=1
 LABEL_METRIC = "acceptance labels/s (1 - TV of draft and target) at B=128 K=16 V=151936"
 SCHEDULE_METRIC = "load-aware verify-window schedules/s at R=128 requests K=16"
 STS_METRIC = "sequential temperature scaling fits/s at N=8192 rows K=16"
-# single-CTA kernels (the scheduler, the STS fit): one SM's 32-bit lanes at the maximum clock
+# the scheduler is one CTA: one SM's 32-bit lanes at the maximum clock
 SM_LANE_OPS = 128 * 2.07e9
+# the STS fit is one 16-CTA cluster; each cross-entropy evaluation needs four transcendental
+# results (exponential, reciprocal, two logarithms), and an SM's special-function units
+# deliver 16 a clock
+STS_CLUSTER_SMS = 16
+STS_SFU_OPS = STS_CLUSTER_SMS * 16 * 2.07e9
+STS_SFU_PER_EVAL = 4
 L2_FLUSH_BYTES = 512 << 20       # larger than the 129 MB L2
 CONF_THRESHOLD = 0.3
 
@@ -101,8 +107,9 @@ def schedule_ops(R: int, K: int) -> int:
 
 
 def sts_ops(N: int, K: int) -> int:
-    """Cross-entropy evaluations of the fit: every row, position, round and grid point."""
-    return N * K * 8 * 32
+    """Special-function results of the fit: four per cross-entropy evaluation, one evaluation
+    per row, position, round and grid point."""
+    return STS_SFU_PER_EVAL * N * K * 8 * 32
 
 
 def algorithmic_bytes(cfg: int, c: dict) -> int:
@@ -401,7 +408,8 @@ def run_reference_small(args, rank, world):
 
 def run_ours_small(args, rank, world, local):
     """The scheduler or the STS fit on the GPU: device time per call, inputs resident, L2
-    flushed between calls; roofline against one SM's 32-bit lane rate (single-CTA kernels)."""
+    flushed between calls; roofline against the lanes (scheduler) or special-function units
+    (STS fit) of the SMs the kernel runs on."""
     import torch
     from rank_markov_draft_gb300 import binding
     torch.cuda.set_device(local)
@@ -450,6 +458,14 @@ def run_ours_small(args, rank, world, local):
     value = world * args.steps / (ms_max / 1000.0)
     med = statistics.median(per_ms)
     achieved = ops / (med / 1000.0)
+    if args.workload == "schedule":
+        peak = SM_LANE_OPS
+        peak_source = "one SM's 32-bit lanes (128) at 2070 MHz: the kernel is one CTA by design"
+    else:
+        peak = STS_SFU_OPS
+        peak_source = (f"special-function units of the {STS_CLUSTER_SMS} SMs of the fit's "
+                       f"cluster (16 results a clock each) at 2070 MHz; "
+                       f"{STS_SFU_PER_EVAL} per evaluation")
     if rank == 0:
         cpu = None
         if not args.skip_cpu:
@@ -474,10 +490,9 @@ def run_ours_small(args, rank, world, local):
                        "l2": "flushed between calls (512 MB write)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "alu", "achieved": round(achieved / 1e9, 3),
-                         "peak": round(SM_LANE_OPS / 1e9, 1), "unit": "Gop/s",
-                         "frac": round(achieved / SM_LANE_OPS, 4), "traffic": None,
-                         "peak_source": "one SM's 32-bit lanes (128) at 2070 MHz: the kernel "
-                                        "is one CTA by design",
+                         "peak": round(peak / 1e9, 1), "unit": "Gop/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": peak_source,
                          "kernel": "schedule_kernel" if args.workload == "schedule"
                          else "sts_fit_kernel",
                          "ops_per_launch": ops, "median_launch_us": round(med * 1000, 2)},

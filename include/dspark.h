@@ -386,7 +386,9 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
  *   a [R, K] survival of extension (r, k) (e.g. the confidence head's cumprod)
  *   sps [sps_len] SPS(B) for B = 0 .. sps_len - 1, sps_len >= R (K + 1) + 1
  * Outputs ell [R] (device) and theta (device scalar, may be NULL).  R * K <=
- * 16384.  All arrays are device pointers; one kernel, no host synchronisation. */
+ * 16384; with K = 0 nothing is admitted (ell = 0, theta = R SPS(R)) and a may
+ * be NULL.  All arrays are device pointers; one kernel, no host
+ * synchronisation. */
 int dspark_schedule(dspark_ctx* ctx, const float* a, int R, int K, const float* sps, int sps_len,
                     int32_t* ell, float* theta, dspark_stream_t stream);
 

@@ -786,7 +786,7 @@ int dspark_sts_fit(dspark_ctx* ctx, const float* conf, const float* label, int N
 
 int dspark_schedule(dspark_ctx* ctx, const float* a, int R, int K, const float* sps,
                     int sps_len, int32_t* ell, float* theta, dspark_stream_t stream) {
-  if (a == nullptr || sps == nullptr || ell == nullptr) return DSPARK_ERR_INVALID_ARG;
+  if ((a == nullptr && K > 0) || sps == nullptr || ell == nullptr) return DSPARK_ERR_INVALID_ARG;
   if (R <= 0 || K < 0) return DSPARK_ERR_INVALID_ARG;
   if (static_cast<int64_t>(R) * K > dspark::kScheduleMaxCandidates || R > 65535 || K > 65535)
     return DSPARK_ERR_UNSUPPORTED;

@@ -10,10 +10,12 @@
 // along a request (a product of probabilities), so this keeps prefixes whole.
 //
 // One CTA: the R x K candidates are packed into 64-bit keys (ordered survival
-// bits | inverted position | inverted request), sorted descending by a bitonic
-// network in shared memory, their survivals summed by a block scan in that
-// order, and the first admission that would not raise Theta cuts the list; each
-// request's length is one past its last admitted position (no atomics).
+// bits | inverted position | inverted request) and sorted descending by a
+// bitonic network held in registers (E keys a thread: strides inside a thread
+// in registers, inside a warp by shuffles, wider ones through shared memory);
+// their survivals are summed by a block scan in that order, the first admission
+// that would not raise Theta cuts the list, and each request's length is the
+// number of its admitted candidates.
 
 #include <cstdint>
 
@@ -33,137 +35,200 @@ __device__ __forceinline__ float from_ordered32(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+// one compare-exchange in a bitonic stage (size, stride), sorting descending: the lower index
+// of a pair in a descending block keeps the larger key, and so does the upper index of a pair
+// in an ascending block.  For stride >= E the answer is the same for all of a thread's keys
+// (their indices differ only below bit log2 E), so it is taken once per stage.
+__device__ __forceinline__ bool bitonic_keeps_max(int i, int size, int stride) {
+  return ((i & stride) == 0) == ((i & size) == 0);
+}
+
+__device__ __forceinline__ unsigned long long bitonic_keep(unsigned long long x,
+                                                           unsigned long long y, bool keep_max) {
+  return ((x > y) == keep_max) ? x : y;  // equal keys: either
+}
+
+// E keys per thread, thread t holding sorted positions t * E .. t * E + E - 1; the block has
+// n_pow2 / E threads (at least one warp)
+template <int E>
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* __restrict__ a, int R,
                                                                  int K, const float* __restrict__ sps,
-                                                                 int n_pow2, int32_t* __restrict__ ell,
+                                                                 int32_t* __restrict__ ell,
                                                                  float* __restrict__ theta) {
-  extern __shared__ __align__(16) unsigned long long s_key[];  // [n_pow2]
-  float* s_sum = reinterpret_cast<float*>(s_key + n_pow2);     // [n_pow2] inclusive prefix sums
-  __shared__ int s_cut;
+  extern __shared__ __align__(16) unsigned long long s_key[];  // [n_pow2]: exchange, then counts
   __shared__ float s_part[kSchedThreads / 32];
-  const int n = R * K;
-  const int tid = threadIdx.x;
-  for (int i = tid; i < R; i += kSchedThreads) ell[i] = 0;
-  for (int i = tid; i < n_pow2; i += kSchedThreads) {
-    unsigned long long key = 0ull;  // padding sorts after every candidate
-    if (i < n) {
-      const int r = i / K, k = i - r * K;
-      key = (static_cast<unsigned long long>(ordered_bits32(a[i])) << 32) |
-            (static_cast<unsigned long long>(0xFFFFu - static_cast<uint32_t>(k)) << 16) |
-            static_cast<unsigned long long>(0xFFFFu - static_cast<uint32_t>(r));
-    }
-    s_key[i] = key;
+  __shared__ int s_min[kSchedThreads / 32];
+  const int T = blockDim.x, n_pow2 = T * E, n = R * K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = T >> 5;
+  if (n == 0) {  // nothing to admit: B = R
+    for (int i = tid; i < R; i += T) ell[i] = 0;
+    if (tid == 0 && theta != nullptr) *theta = static_cast<float>(R) * sps[R];
+    return;
   }
-  if (tid == 0) s_cut = n;
-  __syncthreads();
-  // bitonic sort, descending: every stage is n_pow2 / 2 compare-exchanges, one pair per
-  // thread at a time; a stage with stride < 32 keeps each warp inside its own 64-key
-  // block (pairs 32w .. 32w + 31 cover keys 64w .. 64w + 63), so it needs only a warp
-  // barrier, and a block barrier is taken only after a stage with a larger stride
-  const int pairs = n_pow2 >> 1;
+  const int i0 = tid * E;
+  // the SPS values this thread's cut test reads, loaded before the sort (E + 1 entries)
+  constexpr bool kPreload = E <= 4;
+  float sp[kPreload ? E + 1 : 1];
+  if (kPreload) {
+#pragma unroll
+    for (int e = 0; e <= E; ++e) sp[e] = i0 + e <= n ? __ldg(sps + R + i0 + e) : 0.f;
+  }
+  // keys: ordered survival bits | inverted position | inverted request (0 pads, sorting last)
+  unsigned long long x[E];
+  {
+    int r = i0 / K, k = i0 - r * K;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      x[e] = 0ull;
+      if (i0 + e < n)
+        x[e] = (static_cast<unsigned long long>(ordered_bits32(__ldg(a + i0 + e))) << 32) |
+               (static_cast<unsigned long long>(0xFFFFu - static_cast<uint32_t>(k)) << 16) |
+               static_cast<unsigned long long>(0xFFFFu - static_cast<uint32_t>(r));
+      if (++k == K) {
+        k = 0;
+        ++r;
+      }
+    }
+  }
+  // bitonic sort, descending: strides of 32 E and more exchange through shared memory, the
+  // others between the lanes of a warp (stride / E) or inside a thread (stride < E)
   for (int size = 2; size <= n_pow2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = tid; t < pairs; t += kSchedThreads) {
-        // pair t: (t / stride) * 2 * stride + t % stride (stride is a power of two)
-        const int i = 2 * t - (t & (stride - 1)), j = i + stride;
-        const unsigned long long x = s_key[i], y = s_key[j];
-        const bool desc = (i & size) == 0;
-        if (desc ? (x < y) : (x > y)) {
-          s_key[i] = y;
-          s_key[j] = x;
+    int stride = size >> 1;
+    for (; stride >= 32 * E; stride >>= 1) {
+      __syncthreads();  // the last stage's readers are done
+#pragma unroll
+      for (int e = 0; e < E; ++e) s_key[i0 + e] = x[e];
+      __syncthreads();
+      const bool keep_max = bitonic_keeps_max(i0, size, stride);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = bitonic_keep(x[e], s_key[(i0 + e) ^ stride], keep_max);
+    }
+    for (; stride >= E; stride >>= 1) {
+      const int m = stride / E;
+      const bool keep_max = bitonic_keeps_max(i0, size, stride);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = bitonic_keep(x[e], shfl_xor_u64(x[e], m), keep_max);
+    }
+#pragma unroll
+    for (int s = E / 2; s > 0; s >>= 1) {
+      if (s < size) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & s) == 0) {
+            const bool desc = ((i0 + e) & size) == 0;
+            const unsigned long long p = x[e], q = x[e + s];
+            const unsigned long long hi = p > q ? p : q, lo = p > q ? q : p;
+            x[e] = desc ? hi : lo;
+            x[e + s] = desc ? lo : hi;
+          }
         }
       }
-      if (stride >= 32 || pairs > kSchedThreads || (stride == 1 && size >= 64)) {
-        __syncthreads();
-      } else {
-        __syncwarp();
-      }
     }
   }
-  __syncthreads();
-  // inclusive prefix sums of the survivals in rank order: each thread sums a
-  // contiguous slice, the slice totals are scanned by warp 0
-  const int per = (n_pow2 + kSchedThreads - 1) / kSchedThreads;
-  const int i0 = tid * per, i1 = min(n, i0 + per);
-  float run = 0.f;
-  for (int i = i0; i < i1; ++i) {
-    run += from_ordered32(static_cast<uint32_t>(s_key[i] >> 32));
-    s_sum[i] = run;
+  // inclusive prefix sums of the survivals in rank order: the thread's own run, then an
+  // exclusive scan of the thread totals
+  float run[E];
+  float tot = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    tot += i0 + e < n ? from_ordered32(static_cast<uint32_t>(x[e] >> 32)) : 0.f;
+    run[e] = tot;
   }
-  // exclusive scan of the per-thread totals
-  const int lane = tid & 31, warp = tid >> 5;
-  float tot = run, incl = run;
+  float incl = tot;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
     if (lane >= off) incl += o;
   }
   if (lane == 31) s_part[warp] = incl;
-  __syncthreads();
+  __syncthreads();  // also: every thread is past its last read of the exchange buffer
   if (warp == 0) {
-    float w = s_part[lane];
+    float w = lane < nw ? s_part[lane] : 0.f;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float o = __shfl_up_sync(0xFFFFFFFFu, w, off);
       if (lane >= off) w += o;
     }
-    s_part[lane] = w;  // inclusive over warps
+    if (lane < nw) s_part[lane] = w;  // inclusive over warps
   }
+  int* s_cnt = reinterpret_cast<int*>(s_key);  // admitted candidates per request (R <= n)
+  for (int i = tid; i < R; i += T) s_cnt[i] = 0;
   __syncthreads();
   const float base = incl - tot + (warp > 0 ? s_part[warp - 1] : 0.f);
-  for (int i = i0; i < i1; ++i) s_sum[i] += base;
-  __syncthreads();
-  // the first candidate whose admission would not raise Theta: each thread's first such
-  // candidate (its indices ascend), the warp's minimum, one shared atomic per warp
+  // the first candidate whose admission would not raise Theta = (R + sum) * SPS(R + i)
+  const float Rf = static_cast<float>(R);
   int mine = n;
-  for (int i = tid; i < n; i += kSchedThreads) {
-    const float prev = static_cast<float>(R) + (i > 0 ? s_sum[i - 1] : 0.f);
-    const float cur = static_cast<float>(R) + s_sum[i];
-    const float th_prev = prev * sps[R + i];
-    const float th_next = cur * sps[R + i + 1];
-    if (!(th_next > th_prev)) {
-      mine = i;
-      break;
+  float th_cut = 0.f;  // Theta with this thread's admitted prefix, at its first failure
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = i0 + e;
+    if (i < n && mine == n) {
+      const float s0 = kPreload ? sp[e] : __ldg(sps + R + i);
+      const float s1 = kPreload ? sp[e + 1] : __ldg(sps + R + i + 1);
+      const float th_prev = (Rf + (base + (e > 0 ? run[e - 1] : 0.f))) * s0;
+      const float th_next = (Rf + (base + run[e])) * s1;
+      if (!(th_next > th_prev)) {
+        mine = i;
+        th_cut = th_prev;
+      }
     }
   }
-  mine = __reduce_min_sync(0xFFFFFFFFu, mine);
-  if (lane == 0 && mine < n) atomicMin(&s_cut, mine);
+  const int wmin = __reduce_min_sync(0xFFFFFFFFu, mine);
+  if (lane == 0) s_min[warp] = wmin;
   __syncthreads();
-  const int cut = s_cut;
-  if (tid == 0 && theta != nullptr)
-    *theta = (static_cast<float>(R) + (cut > 0 ? s_sum[cut - 1] : 0.f)) * sps[R + cut];
-  __syncthreads();
-  // every candidate's rank (reusing the prefix sums' storage); the admitted positions of a
-  // request form a prefix, so its last admitted position k gives ell = k + 1 (no atomics)
-  int* s_rank = reinterpret_cast<int*>(s_sum);
-  for (int i = tid; i < n; i += kSchedThreads) {
-    const unsigned long long key = s_key[i];
-    const int r = static_cast<int>(0xFFFFu - static_cast<uint32_t>(key & 0xFFFFull));
-    const int k = static_cast<int>(0xFFFFu - static_cast<uint32_t>((key >> 16) & 0xFFFFull));
-    s_rank[r * K + k] = i;
+  int cut = n;
+  for (int w = 0; w < nw; ++w) cut = min(cut, s_min[w]);
+  if (theta != nullptr) {
+    if (cut < n && mine == cut) *theta = th_cut;  // the thread that holds the cut
+    if (cut == n) {  // everything admitted: the holder of the last candidate
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (i0 + e == n - 1) *theta = (Rf + (base + run[e])) * __ldg(sps + R + n);
+    }
   }
+  // each request's length is the number of its admitted candidates
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (i0 + e < cut)
+      atomicAdd(&s_cnt[static_cast<int>(0xFFFFu - static_cast<uint32_t>(x[e] & 0xFFFFull))], 1);
   __syncthreads();
-  for (int idx = tid; idx < n; idx += kSchedThreads) {
-    const int r = idx / K, k = idx - r * K;
-    if (s_rank[idx] < cut && (k + 1 == K || s_rank[idx + 1] >= cut)) ell[r] = k + 1;
-  }
+  for (int i = tid; i < R; i += T) ell[i] = s_cnt[i];
 }
 
 }  // namespace
 
-size_t schedule_smem_bytes(int n_pow2) { return static_cast<size_t>(n_pow2) * (8 + 4); }
+size_t schedule_smem_bytes(int n_pow2) { return static_cast<size_t>(n_pow2) * 8; }
 
-cudaError_t launch_schedule(const float* a, int R, int K, const float* sps, int32_t* ell,
-                            float* theta, cudaStream_t stream) {
-  int n_pow2 = 1;
-  while (n_pow2 < R * K) n_pow2 <<= 1;
+template <int E>
+static cudaError_t launch_schedule_e(const float* a, int R, int K, const float* sps, int32_t* ell,
+                                     float* theta, int n_pow2, cudaStream_t stream) {
   const size_t smem = schedule_smem_bytes(n_pow2);
-  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&schedule_kernel),
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&schedule_kernel<E>),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kSchedThreads, smem, stream>>>(a, R, K, sps, n_pow2, ell, theta);
+  schedule_kernel<E><<<1, n_pow2 / E, smem, stream>>>(a, R, K, sps, ell, theta);
   return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const float* a, int R, int K, const float* sps, int32_t* ell,
+                            float* theta, cudaStream_t stream) {
+  int n_pow2 = 32;  // at least one warp of one key each
+  while (n_pow2 < R * K) n_pow2 <<= 1;
+  switch (n_pow2 <= kSchedThreads ? 1 : n_pow2 / kSchedThreads) {
+    case 1: return launch_schedule_e<1>(a, R, K, sps, ell, theta, n_pow2, stream);
+    case 2: return launch_schedule_e<2>(a, R, K, sps, ell, theta, n_pow2, stream);
+    case 4: return launch_schedule_e<4>(a, R, K, sps, ell, theta, n_pow2, stream);
+    case 8: return launch_schedule_e<8>(a, R, K, sps, ell, theta, n_pow2, stream);
+    case 16: return launch_schedule_e<16>(a, R, K, sps, ell, theta, n_pow2, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace dspark

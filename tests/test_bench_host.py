@@ -40,7 +40,7 @@ def test_single_cta_kernel_op_counts():
     assert bench.schedule_ops(128, 16) == 2048 * 66 + 2 * 2048
     assert bench.schedule_ops(7, 3) == 32 * 15 + 2 * 21  # 21 candidates padded to 32
     # every row x position x round (8) x grid point (32)
-    assert bench.sts_ops(8192, 16) == 8192 * 16 * 8 * 32
+    assert bench.sts_ops(8192, 16) == 4 * 8192 * 16 * 8 * 32  # four SFU results per evaluation
     assert bench.metric_of("schedule") == bench.SCHEDULE_METRIC
     assert bench.metric_of("sts") == bench.STS_METRIC
 

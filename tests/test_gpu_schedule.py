@@ -26,7 +26,10 @@ def _tables(rng, R, K, kind):
     return a, sps.astype(np.float32)
 
 
-@pytest.mark.parametrize("R,K", [(1, 1), (7, 3), (128, 16), (300, 40)])
+# candidate counts padded to 32, 2048, 4096, 8192 and 16384: one, two, four, eight and sixteen
+# keys a thread; K = 0 admits nothing
+@pytest.mark.parametrize("R,K", [(1, 1), (7, 3), (128, 16), (200, 16), (500, 16), (300, 40),
+                                 (5, 0)])
 @pytest.mark.parametrize("kind", ["smooth", "flat", "jagged"])
 def test_schedule_matches_oracle(dsp, R, K, kind):
     rng = np.random.default_rng(R * 1000 + K)

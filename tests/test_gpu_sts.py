@@ -58,6 +58,25 @@ def test_sts_fit_matches_oracle(dsp, case):
     assert np.allclose(loss, ref["loss"], rtol=1e-4), (name, loss, ref["loss"])
 
 
+@pytest.mark.parametrize("N,t", [(140000, [0.7, 2.0, 1.3]), (37, [0.5, 1.5, 3.0, 1.0])])
+def test_sts_fit_row_tiles_and_small_sets(dsp, N, t):
+    """140000 rows: more than a CTA of the cluster keeps in shared memory, so every round
+    rebuilds its rows tile by tile; 37 rows: a one-CTA cluster.  Soft labels generated at
+    known temperatures put each optimum inside the search interval."""
+    K = len(t)
+    rng = np.random.default_rng(207 + N)
+    conf = special.expit(rng.normal(0.0, 2.0, (N, K))).astype(np.float32)
+    c = np.clip(conf.astype(np.float64), 2.0 ** -24, 1 - 2.0 ** -24)
+    label = special.expit(np.log(c / (1 - c)) / np.array(t)).astype(np.float32)
+    out = binding.sts_fit(dsp, dev(conf), dev(label))
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    ref = oracle.sts_fit(conf, label)
+    tau, loss = host(out["tau"]).astype(np.float64), host(out["loss"]).astype(np.float64)
+    assert np.abs(np.log(tau) - np.log(ref["tau"])).max() <= TAU_TOL, (tau, ref["tau"])
+    assert np.allclose(loss, ref["loss"], rtol=1e-4), (loss, ref["loss"])
+
+
 def test_confidence_with_temperatures(dsp):
     B, K, V, r, d = 11, 7, 500, 64, 96
     inp = make_inputs(202, B, K, V, r, d=d, confidence=True)
