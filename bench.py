@@ -695,8 +695,8 @@ def run_ours(args, rank, world, local):
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
-                "kernel": ("verify step (target-row scan, acceptance, gather, one-position "
-                           "draft logits, residual race)" if args.workload == "verify" else
+                "kernel": ("verify step (target-row scan, acceptance, per-row prep, residual "
+                           "draw reading the draw rows in place)" if args.workload == "verify" else
                            "label step (target-row scan, per-row offsets, draft kernel in "
                            "label mode)" if args.workload == "label" else
                            "draft_kernel" if cfg != 4 else

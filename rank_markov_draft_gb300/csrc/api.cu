@@ -35,10 +35,8 @@ struct dspark_ctx {
   float* d_v_lse_t = nullptr;            // [B_max][K_max + 1]
   int32_t* d_v_argmax_t = nullptr;       // [B_max][K_max + 1]
   dspark::VerifySel* d_v_sel = nullptr;  // [B_max]
-  float* d_v_U = nullptr;                // [B_max][V_max]
   float* d_v_H = nullptr;                // [B_max][256]
   int32_t* d_v_prev = nullptr;           // [B_max]
-  float* d_v_P = nullptr;                // [B_max][V_max] target rows at the draw position
   dspark::ResRow* d_v_rows = nullptr;    // [B_max]
   // acceptance-label scratch
   int32_t* d_l_prev = nullptr;           // [B_max * K_max] predecessors of the drafted tokens
@@ -186,12 +184,13 @@ int run_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int 
 
 // Inputs of the draft kernel's acceptance-label mode (whole call; chunked below).
 struct LabelIn {
-  const float* target;  // [B, K+1, V] (label) or [B, V] target rows (residual, K = 1)
+  const float* target;  // [B, K+1, V] target logits (label; residual: with K = res_K)
   const float* lse_t;   // [B, K+1] (label)
   const float* offq2;   // [B, K] (label)
   float* label;         // [B, K] (label)
   float target_scale2;  // log2(e) / Tt
   const dspark::ResRow* rows;  // [B] (residual), else null
+  int res_K;            // residual: K of the caller's U [B, K, V] (passed as U) and target
 };
 
 // The persistent draft kernel over chunks of 128 requests.
@@ -211,11 +210,22 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
                             static_cast<uint64_t>(V) * 2, dspark::kDraftTileV, r))
       return DSPARK_ERR_CUDA;
     const int box_rows = (Bc + 7) & ~7;
-    const float* Uc = U + static_cast<size_t>(b0) * K * V;
-    if (!encode_3d(&args.tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Uc, V, K, Bc,
-                   static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(K) * V * 4, 32, 1,
-                   box_rows))
-      return DSPARK_ERR_CUDA;
+    const bool res = lab != nullptr && lab->rows != nullptr;
+    if (res) {
+      // the draw rows are gathered in place: U and the target as plain row arrays
+      const uint64_t Kr = static_cast<uint64_t>(lab->res_K);
+      if (!encode_2d(&args.tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, U, V, B * Kr,
+                     static_cast<uint64_t>(V) * 4, 32, 1) ||
+          !encode_2d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, lab->target, V, B * (Kr + 1),
+                     static_cast<uint64_t>(V) * 4, 32, 1))
+        return DSPARK_ERR_CUDA;
+    } else {
+      const float* Uc = U + static_cast<size_t>(b0) * K * V;
+      if (!encode_3d(&args.tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Uc, V, K, Bc,
+                     static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(K) * V * 4, 32, 1,
+                     box_rows))
+        return DSPARK_ERR_CUDA;
+    }
     DraftParams& p = args.p;
     p.W1 = W1;
     p.anchors = anchors + b0;
@@ -238,18 +248,17 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.logits = logits ? logits + o * V : nullptr;
     p.lse = lse ? lse + o : nullptr;
     if (lab != nullptr) {
-      // target rows per request: K + 1 of them (label), or the one draw row (residual)
-      const int trows = lab->rows ? K : K + 1;
-      const float* tchunk = lab->target + static_cast<size_t>(b0) * trows * V;
-      if (!encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tchunk, V, trows, Bc,
-                     static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(trows) * V * 4, 32, 1,
-                     box_rows))
-        return DSPARK_ERR_CUDA;
-      p.target = tchunk;
       p.target_scale2 = lab->target_scale2;
-      if (lab->rows) {
+      if (res) {
         p.rows = lab->rows + b0;
+        p.res_K = lab->res_K;
       } else {
+        const float* tchunk = lab->target + static_cast<size_t>(b0) * (K + 1) * V;
+        if (!encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tchunk, V, K + 1, Bc,
+                       static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(K + 1) * V * 4, 32,
+                       1, box_rows))
+          return DSPARK_ERR_CUDA;
+        p.target = tchunk;
         p.lse_t = lab->lse_t + static_cast<size_t>(b0) * (K + 1);
         p.offq2 = lab->offq2 + o;
         p.label = lab->label + o;
@@ -373,12 +382,8 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
             cudaMalloc(&ctx->d_v_lse_t, sizeof(float) * B_max * (K_max + 1)) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_argmax_t, sizeof(int32_t) * B_max * (K_max + 1)) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_sel, sizeof(dspark::VerifySel) * B_max) == cudaSuccess &&
-            cudaMalloc(&ctx->d_v_U, sizeof(float) * static_cast<size_t>(B_max) * V_max) ==
-                cudaSuccess &&
             cudaMalloc(&ctx->d_v_H, sizeof(float) * B_max * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_prev, sizeof(int32_t) * B_max) == cudaSuccess &&
-            cudaMalloc(&ctx->d_v_P, sizeof(float) * static_cast<size_t>(B_max) * V_max) ==
-                cudaSuccess &&
             cudaMalloc(&ctx->d_v_rows, sizeof(dspark::ResRow) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_prev, sizeof(int32_t) * rows) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_offq2, sizeof(float) * rows) == cudaSuccess;
@@ -408,10 +413,8 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_v_lse_t);
   cudaFree(ctx->d_v_argmax_t);
   cudaFree(ctx->d_v_sel);
-  cudaFree(ctx->d_v_U);
   cudaFree(ctx->d_v_H);
   cudaFree(ctx->d_v_prev);
-  cudaFree(ctx->d_v_P);
   cudaFree(ctx->d_v_rows);
   cudaFree(ctx->d_l_prev);
   cudaFree(ctx->d_l_offq2);
@@ -685,8 +688,6 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   v.lse_t = ctx->d_v_lse_t;
   v.argmax_t = ctx->d_v_argmax_t;
   v.sel = ctx->d_v_sel;
-  v.U_sel = ctx->d_v_U;
-  v.P_sel = ctx->d_v_P;
   v.H_sel = ctx->d_v_H;
   v.prev_sel = ctx->d_v_prev;
   v.rows = ctx->d_v_rows;
@@ -695,14 +696,15 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   ctx->last_launches += n;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   if (target_temperature > 0.f) {
-    // the draw: gathered rows and per-row constants, then the draft kernel's residual
-    // mode over one position (a greedy target's token is its argmax, set above)
-    e = dspark::launch_verify_gather(v, s);
+    // the draw: per-row constants, then the draft kernel's residual mode over one
+    // position, reading each request's draw rows of U and P in place (a greedy target's
+    // token is its argmax, set above)
+    e = dspark::launch_verify_prep(v, s);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-    ctx->last_launches += 2;
-    LabelIn res{ctx->d_v_P, nullptr, nullptr, nullptr, 1.4426950408889634f / target_temperature,
-                ctx->d_v_rows};
-    st = run_draft(ctx, dspark::kModeResidual, ctx->d_v_U, W1, W2, ctx->d_v_prev, ctx->d_v_prev,
+    ctx->last_launches += 1;
+    LabelIn res{P, nullptr, nullptr, nullptr, 1.4426950408889634f / target_temperature,
+                ctx->d_v_rows, K};
+    st = run_draft(ctx, dspark::kModeResidual, U, W1, W2, ctx->d_v_prev, ctx->d_v_prev,
                    gated ? ctx->d_v_H : nullptr, B, 1, V, r, draft_temperature, seed, next_token,
                    nullptr, nullptr, nullptr, nullptr, s, &res);
     if (st != DSPARK_OK) return st;

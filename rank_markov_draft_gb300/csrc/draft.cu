@@ -381,7 +381,80 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && MODE == kModeResidual) {
+    // ------------------------------------------------ TMA producer, residual mode
+    // The draw rows are read in place: each request's base-logit row and target row at
+    // its own draw position (tile::gather4 over 2-D row maps of U [B K, V] and
+    // P [B (K + 1), V]), lane l fetching requests 4 l .. 4 l + 3 of every half tile into
+    // the same slot layout as the 3-D boxes; lane 0 waits for the slots and loads W2.
+    const uint64_t pol_w = l2_policy_evict_last();
+    const uint64_t pol_u = l2_policy_evict_first();
+    const uint32_t w_bytes = static_cast<uint32_t>(p.r) * kTileV * 2u;
+    const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
+    const bool mine = 4 * lane < p.box_rows;
+    // the lane's four requests (past the batch: request 0 again, never read) and their draw
+    // positions, a byte each (a position is at most K <= 64)
+    uint32_t pos4 = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int b = 4 * lane + q < p.B ? 4 * lane + q : 0;
+      pos4 |= static_cast<uint32_t>(p.rows[b].pos) << (8 * q);
+    }
+    // row of request q of the lane in U (a bonus row reads no q: any valid row) or P
+    auto draw_row = [&](int q, bool target) {
+      const int gb = p.b_global0 + (4 * lane + q < p.B ? 4 * lane + q : 0);
+      const int pos = static_cast<int>((pos4 >> (8 * q)) & 0xFFu);
+      return target ? gb * (p.res_K + 1) + pos : gb * p.res_K + min(pos, p.res_K - 1);
+    };
+    bool ok = true;
+    int w_issued = 0, u_issued = 0;
+    for (int k = 0; k < p.K && ok; ++k) {
+      for (int t = 0; t < nt; ++t) {
+        const int i = k * nt + t;
+        const int v0 = (t_begin + t) * kTileV;
+        if (lane == 0 && nkk > 0) {
+          const int s = i % kNumW2Stages;
+          ok = mbar_wait(&w_empty[s], ((i / kNumW2Stages) & 1) ^ 1, p.timeout_ns, abort_flag,
+                         kBackoffControlNs);
+          if (ok) {
+            mbar_arrive_expect_tx(&w_full[s], w_bytes);
+            tma_load_2d(sW + s * kW2StageBytes, &args.tm_w2, v0, 0, &w_full[s], pol_w);
+            w_issued = i + 1;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        for (int h = 0; h < 2 && ok; ++h) {
+          const int j = 2 * i + h, su = j % nus;
+          if (lane == 0) {
+            ok = mbar_wait(&u_empty[su], ((j / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
+                           kBackoffControlNs);
+            if (ok) mbar_arrive_expect_tx(&u_full[su], u_bytes);
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) break;
+          if (mine) {
+            uint8_t* dst = sU + su * 2 * ubox + lane * 512;
+            tma_gather4_2d(dst, &args.tm_u, v0 + 32 * h, draw_row(0, false), draw_row(1, false),
+                           draw_row(2, false), draw_row(3, false), &u_full[su], pol_u);
+            tma_gather4_2d(dst + ubox, &args.tm_p, v0 + 32 * h, draw_row(0, true),
+                           draw_row(1, true), draw_row(2, true), draw_row(3, true), &u_full[su],
+                           pol_u);
+          }
+          u_issued = j + 1;
+        }
+        if (!ok) break;
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      record_error(p.status, kStatusTimeout);
+      // Drain: every copy the warp started completes on the full barriers of its fills.
+      for (int i = w_issued - 1; i >= 0 && i >= w_issued - kNumW2Stages; --i)
+        mbar_wait(&w_full[i % kNumW2Stages], (i / kNumW2Stages) & 1, p.timeout_ns, nullptr);
+      for (int i = u_issued - 1; i >= 0 && i >= u_issued - nus; --i)
+        mbar_wait(&u_full[i % nus], (i / nus) & 1, p.timeout_ns, nullptr);
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_last();

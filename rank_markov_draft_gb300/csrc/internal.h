@@ -80,15 +80,18 @@ struct DraftParams {
   const float* offq2;       // [B, K] (chunk) log2 q(v) = l(v) * log2(e) / Td + offq2
   float* label;             // [B, K] (chunk) 1 - TV(q, p)
   float target_scale2;      // log2(e) / Tt
-  // residual mode (verification draw, K = 1): target rows through tm_p, per-row constants
+  // residual mode (verification draw, K = 1): per-row constants; the draw rows of the
+  // caller's U [B, res_K, V] and P [B, res_K + 1, V] gathered in place through tm_u, tm_p
   const ResRow* rows;       // [B] (chunk), or null
+  int res_K;
 };
 
 struct DraftArgs {
   CUtensorMap tm_w2;  // W2 [r, V] bf16, box {64, r}, 128B swizzle
-  CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle
+  CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle;
+                      // residual mode: U as rows [B K, V], box {32, 1} (gathered by four)
   CUtensorMap tm_p;   // label mode: target chunk [B, K+1, V] fp32, box {32, 1, box_rows},
-                      // 128B swizzle
+                      // 128B swizzle; residual mode: P as rows [B (K + 1), V], box {32, 1}
   DraftParams p;
 };
 
@@ -161,23 +164,19 @@ struct VerifyArgs {
   float* lse_t;               // [B, K+1]
   int32_t* argmax_t;          // [B, K+1]
   VerifySel* sel;             // [B]
-  float* U_sel;               // [B, V] base-logit rows at the draw position
-  float* P_sel;               // [B, V] target rows at the draw position
-  float* H_sel;               // [B, r]
+  float* H_sel;               // [B, r] gate rows at the draw position
   int32_t* prev_sel;          // [B]
   ResRow* rows;               // [B] the residual mode's per-row constants
 };
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches);
-// The draw's inputs: gathered rows and per-row constants (two kernels).
-cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream);
+// The draw's per-row constants, gate row and predecessor (one kernel; the draft kernel's
+// residual mode reads the draw rows of U and P in place).
+cudaError_t launch_verify_prep(const VerifyArgs& v, cudaStream_t stream);
 // Log-sum-exp of P / Tt (argmax when greedy) of the rows (b, k <= min(ell[b], kmax))
 // of P [B, K+1, V]; ell null: every request's rows up to kmax.
 cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,
                                 float target_temperature, float* lse_t, int32_t* argmax_t,
                                 cudaStream_t stream);
-cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream);
-cudaError_t launch_verify_race(const VerifyArgs& v, int num_sms, cudaStream_t stream,
-                               int* launches);
 
 // ---- acceptance label (label.cu)
 // One warp per drafted position: its predecessor, the offset that turns the

@@ -171,6 +171,20 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Four rows y0..y3 of a 2-D tensor map whose box is one row high, columns [x, x + box
+// width), landing one after another at smem_dst (tile::gather4); x * element size a
+// multiple of 16 bytes, the rows in range.
+__device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const CUtensorMap* map, int32_t x,
+                                               int32_t y0, int32_t y1, int32_t y2, int32_t y3,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Untiled bulk copy global -> shared, completing on `bar` by transaction count.
 // Both addresses 16-byte aligned, `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,

@@ -20,15 +20,15 @@
 //                        log-probabilities give q(x)), the first failure ends
 //                        the prefix; records where the draw happens and what
 //                        feeds it;
-//   verify_gather_kernel copies the base-logit row (and gate row) and the target
-//                        row of each request's draw position;
 //   verify_prep_kernel   one warp per request: the offsets that turn the draft
 //                        head's logits and the target logits at the draw
 //                        position into log2 q and log2 p (the draft's
 //                        normaliser from its own log-probability of the
-//                        rejected token, rebuilt l(x) by a dot product);
-// then the draft kernel's residual mode streams the gathered rows and draws
-// from max(0, p - q) (p alone for a bonus) by the block race.
+//                        rejected token, rebuilt l(x) by a dot product), and
+//                        the draw position's predecessor and gate row;
+// then the draft kernel's residual mode streams each request's base-logit row
+// and target row at its draw position, read in place, and draws from
+// max(0, p - q) (p alone for a bonus) by the block race.
 // Noise: acceptance uniform of position k: Philox4x32-10 counter (k, 0, b, 13),
 // word 0; the draw's block race at position j: counter (beta >> 3, j, b,
 // 9 + (beta & 3)), words 2h (stage 1) and 2h + 1 (stage 2), h = (beta >> 2) & 1.
@@ -221,45 +221,23 @@ __global__ void verify_accept_kernel(const float* __restrict__ P, const int32_t*
 
 // Base-logit (and gate) row and target row of each request's draw position, for
 // the draft kernel's residual mode.
-__global__ void verify_gather_kernel(const float* __restrict__ U, const float* __restrict__ P,
-                                     const float* __restrict__ H,
-                                     const VerifySel* __restrict__ sel, int K, int V, int r,
-                                     float* __restrict__ U_sel, float* __restrict__ P_sel,
-                                     float* __restrict__ H_sel, int32_t* __restrict__ prev_sel) {
-  const int b = blockIdx.y;
-  const VerifySel s = sel[b];
-  const int pos = min(s.pos, K - 1);  // a bonus row needs no q; any valid row will do
-  const float4* src = reinterpret_cast<const float4*>(U + (static_cast<size_t>(b) * K + pos) * V);
-  const float4* psrc =
-      reinterpret_cast<const float4*>(P + (static_cast<size_t>(b) * (K + 1) + s.pos) * V);
-  float4* dst = reinterpret_cast<float4*>(U_sel + static_cast<size_t>(b) * V);
-  float4* pdst = reinterpret_cast<float4*>(P_sel + static_cast<size_t>(b) * V);
-  // this CTA's 4096-float4 slice of both rows
-  const int i0 = blockIdx.x * 4096;
-  const int i1 = min(V / 4, i0 + 4096);
-#pragma unroll 4
-  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    dst[i] = __ldcs(src + i);
-    pdst[i] = __ldcs(psrc + i);
-  }
-  if (blockIdx.x != 0) return;
-  if (H != nullptr) {
-    const float* hs = H + (static_cast<size_t>(b) * K + pos) * r;
-    for (int i = threadIdx.x; i < r; i += blockDim.x) H_sel[static_cast<size_t>(b) * r + i] = hs[i];
-  }
-  if (threadIdx.x == 0) prev_sel[b] = s.prev;
-}
-
-// One warp per request: the residual mode's per-row constants.
+// One warp per request: the residual mode's per-row constants, and the predecessor and
+// gate row of the draw position (the one position the residual mode drafts over).
 __global__ void verify_prep_kernel(const float* __restrict__ U, const uint16_t* __restrict__ W1,
                                    const uint16_t* __restrict__ W2, const float* __restrict__ H,
                                    const float* __restrict__ logq, const float* __restrict__ lse_t,
                                    const VerifySel* __restrict__ sel, int B, int K, int V, int r,
-                                   float inv_td, int draft_greedy, ResRow* __restrict__ rows) {
+                                   float inv_td, int draft_greedy, ResRow* __restrict__ rows,
+                                   float* __restrict__ H_sel, int32_t* __restrict__ prev_sel) {
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
   const VerifySel s = sel[b];
+  if (H != nullptr) {  // a bonus row needs no q: any valid gate row will do
+    const float* hs = H + (static_cast<size_t>(b) * K + min(s.pos, K - 1)) * r;
+    for (int i = lane; i < r; i += 32) H_sel[static_cast<size_t>(b) * r + i] = hs[i];
+  }
+  if (lane == 0) prev_sel[b] = s.prev;
   ResRow rr;
   rr.pos = s.pos;
   rr.offp2 = -lse_t[static_cast<size_t>(b) * (K + 1) + s.pos] * kLog2eV;
@@ -304,17 +282,12 @@ cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launche
   return cudaSuccess;
 }
 
-cudaError_t launch_verify_gather(const VerifyArgs& v, cudaStream_t stream) {
-  const dim3 grid((v.V / 4 + 4095) / 4096, v.B);
-  verify_gather_kernel<<<grid, 256, 0, stream>>>(v.U, v.P, v.H, v.sel, v.K, v.V, v.r, v.U_sel,
-                                                 v.P_sel, v.H_sel, v.prev_sel);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+cudaError_t launch_verify_prep(const VerifyArgs& v, cudaStream_t stream) {
   const int greedy_d = v.draft_temperature > 0.f ? 0 : 1;
   const float inv_td = greedy_d ? 1.f : 1.0f / v.draft_temperature;
   verify_prep_kernel<<<(v.B + 7) / 8, 256, 0, stream>>>(v.U, v.W1, v.W2, v.H, v.logq, v.lse_t,
                                                         v.sel, v.B, v.K, v.V, v.r, inv_td,
-                                                        greedy_d, v.rows);
+                                                        greedy_d, v.rows, v.H_sel, v.prev_sel);
   return cudaGetLastError();
 }
 
