@@ -331,8 +331,9 @@ int dspark_markov_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1,
  * block race of the draft (16-token blocks) on counter (beta >> 3, j, b,
  * 9 + (beta & 3)).  Sizes within the context's B_max, K_max, V_max; V % 8 == 0
  * and 16-byte aligned P and U.  Drafted tokens out of [0, V) are reported as
- * DSPARK_ERR_DEVICE_OOB.  Scratch: the context's verification buffers
- * (2 * B_max * V_max floats, allocated at creation). */
+ * DSPARK_ERR_DEVICE_OOB.  Scratch: the context's per-request verification
+ * buffers (allocated at creation); the draw reads the rows of U and P at each
+ * request's draw position in place. */
 int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
                   const uint16_t* W2, const int32_t* anchors, const uint16_t* h,
                   const uint16_t* Wg, int d, const int32_t* tokens, const float* draft_logprobs,
