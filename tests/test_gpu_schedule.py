@@ -46,6 +46,47 @@ def test_schedule_matches_oracle(dsp, R, K, kind):
     assert np.all((ell >= 0) & (ell <= K))
 
 
+def test_schedule_bench_workload(dsp):
+    """The scheduler line the bench times: R = 128 requests x K = 16, its own seeded inputs."""
+    import bench
+    from synth import schedule_inputs
+    c = bench.SMALL["schedule"]
+    a, sps = schedule_inputs(c["seed"], c["R"], c["K"])
+    out = binding.schedule(dsp, dev(a), dev(sps))
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    ref = oracle.schedule(a.astype(np.float64), sps.astype(np.float64))
+    ell = host(out["ell"])
+    if ref["margin"] > 1e-5:
+        assert np.array_equal(ell, ref["ell"])
+    else:  # a near-tie at the cut (this input has one): one admission either way
+        assert abs(int(ell.sum()) - int(ref["ell"].sum())) <= 1
+        assert np.all(np.abs(ell - ref["ell"]) <= 1)
+    assert np.isclose(host(out["theta"])[0], ref["theta"], rtol=1e-5)
+
+
+@pytest.mark.parametrize("R,K", [(64, 16), (200, 16)])
+def test_schedule_equal_survivals(dsp, R, K):
+    """Survivals on a grid of 1/20: many candidates share a value, so the order among equals
+    (position ascending, then request ascending) decides who is admitted at the cut."""
+    rng = np.random.default_rng(R + 7)
+    a = np.cumprod(rng.choice([0.5, 0.75, 0.9, 1.0], (R, K)), axis=1)
+    a = (np.round(a * 20.0) / 20.0).astype(np.float32)
+    a = np.minimum.accumulate(a, axis=1)  # still non-increasing along each request
+    Bmax = R * (K + 1)
+    sps = (2000.0 / (1.0 + (np.arange(Bmax + 1) / (0.4 * Bmax)) ** 2)).astype(np.float32)
+    out = binding.schedule(dsp, dev(a), dev(sps))
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    ref = oracle.schedule(a.astype(np.float64), sps.astype(np.float64))
+    ell = host(out["ell"])
+    if ref["margin"] > 1e-5:
+        assert np.array_equal(ell, ref["ell"])
+    else:  # the same number admitted, all prefixes whole
+        assert ell.sum() == ref["ell"].sum()
+    assert np.all((ell >= 0) & (ell <= K))
+
+
 def test_draft_schedule_verify_chain(dsp):
     """The confidence head's survival feeds the scheduler, whose lengths feed the
     verifier: every step on the GPU, in stream order."""

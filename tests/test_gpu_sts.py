@@ -77,6 +77,64 @@ def test_sts_fit_row_tiles_and_small_sets(dsp, N, t):
     assert np.allclose(loss, ref["loss"], rtol=1e-4), (loss, ref["loss"])
 
 
+def _bce_mean(conf, label, tau, k):
+    """Mean cross-entropy of position k under temperatures tau[:k + 1], written out in fp64
+    from the definition (survival prod_i sigmoid(z_i / tau_i) against prod_i label_i, z the
+    clamped logit, survival clamped to [1e-7, 1 - 1e-7])."""
+    c = np.clip(conf[:, :k + 1].astype(np.float64), 2.0 ** -24, 1 - 2.0 ** -24)
+    z = np.log(c / (1 - c))
+    a = np.prod(special.expit(z / np.asarray(tau[:k + 1], np.float64)), axis=1)
+    y = np.prod(label[:, :k + 1].astype(np.float64), axis=1)
+    q = np.clip(a, 1e-7, 1 - 1e-7)
+    return float(-(y * np.log(q) + (1 - y) * np.log1p(-q)).mean())
+
+
+def test_sts_fit_bench_workload(dsp):
+    """The STS line the bench times: N = 8192 rows x K = 16, 0/1 outcomes of a head 2.5x too
+    sharp, its own seeded inputs.  The losses are flat in tau (noisy 0/1 targets; late
+    positions have almost no surviving rows), so the minimiser is not unique, and a different
+    but equally good choice at one position shifts every later position's loss.  Checked: the
+    oracle's losses are the definition's (written out in numpy); each GPU loss is its own
+    temperatures' loss; each GPU temperature minimises its position's loss given the GPU's
+    earlier ones (a scan of ln tau); and temperatures and losses equal the oracle's while
+    every position so far is well curved (a 5% change of tau, inside the interval, raises
+    the oracle's loss by more than 1e-4 of its value)."""
+    import bench
+    from synth import sts_inputs
+    c = bench.SMALL["sts"]
+    conf, label = sts_inputs(c["seed"], c["N"], c["K"])
+    out = binding.sts_fit(dsp, dev(conf), dev(label))
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    ref = oracle.sts_fit(conf, label)
+    tau, loss = host(out["tau"]).astype(np.float64), host(out["loss"]).astype(np.float64)
+    assert np.all((tau >= 1.0 / 64 * (1 - 1e-6)) & (tau <= 64.0 * (1 + 1e-6)))
+    scan = np.exp(np.linspace(np.log(1.0 / 64), np.log(64.0), 401))
+    curved_so_far = True
+    for k in range(c["K"]):
+        base = _bce_mean(conf, label, ref["tau"], k)
+        assert np.isclose(base, ref["loss"][k], rtol=1e-9)  # the oracle's loss is the definition's
+        mine = _bce_mean(conf, label, tau, k)
+        assert np.isclose(mine, loss[k], rtol=1e-4), (k, mine, loss[k])
+        t2 = tau.copy()
+        best = np.inf
+        for x in scan:
+            t2[k] = x
+            best = min(best, _bce_mean(conf, label, t2, k))
+        assert mine <= best * (1 + 2e-5), (k, mine, best)
+        rise = []
+        for f in (np.exp(0.05), np.exp(-0.05)):
+            t3 = ref["tau"].copy()
+            t3[k] *= f
+            if 1.0 / 64 <= t3[k] <= 64.0:
+                rise.append(_bce_mean(conf, label, t3, k) - base)
+        assert min(rise) >= -1e-9 * base  # the oracle's tau is a minimum within the interval
+        curved_so_far = curved_so_far and min(rise) > 1e-4 * base
+        if curved_so_far:
+            assert abs(np.log(tau[k]) - np.log(ref["tau"][k])) <= TAU_TOL, (k, tau, ref["tau"])
+            assert np.isclose(loss[k], ref["loss"][k], rtol=1e-4), (k, loss, ref["loss"])
+
+
 def test_confidence_with_temperatures(dsp):
     B, K, V, r, d = 11, 7, 500, 64, 96
     inp = make_inputs(202, B, K, V, r, d=d, confidence=True)
