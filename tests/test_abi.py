@@ -121,3 +121,36 @@ def test_context_creation_without_a_device(lib):
     assert lib.dspark_ctx_create(ctypes.byref(h), 0, 0, 4096, 4) == binding.INVALID_ARG
     assert lib.dspark_ctx_create(ctypes.byref(h), 0, 1, 4096, 65) == binding.UNSUPPORTED
     assert lib.dspark_get_status(None, None) == binding.INVALID_ARG
+
+
+def test_verify_label_schedule_sts_argument_checks(lib):
+    """Size limits of the verification, label, scheduler and STS calls are enforced on the
+    host before the context is looked at (with a NULL context every other valid call
+    returns INVALID_ARG, so only the size codes below tell the checks apart)."""
+    E = binding
+    v = lambda B=4, K=16, V=4096, r=256, Td=1.0, Tt=1.0: lib.dspark_verify(
+        None, GOOD, GOOD, GOOD, GOOD, GOOD, None, None, 0, GOOD, GOOD, None, B, K, V, r, Td, Tt,
+        0, GOOD, GOOD, None, None)
+    assert v() == E.INVALID_ARG
+    assert v(K=65) == E.UNSUPPORTED
+    assert v(r=17) == E.UNSUPPORTED
+    assert v(V=4100) == E.UNSUPPORTED
+    assert v(Tt=-1.0) == E.INVALID_ARG
+    a = lambda B=4, K=16, V=4096, r=256: lib.dspark_accept_label(
+        None, GOOD, GOOD, GOOD, GOOD, GOOD, None, None, 0, GOOD, GOOD, B, K, V, r, 1.0, 1.0, GOOD,
+        None)
+    assert a() == E.INVALID_ARG
+    assert a(K=65) == E.UNSUPPORTED
+    assert a(r=272) == E.UNSUPPORTED
+    s = lambda R=128, K=16, sps_len=None, A=GOOD: lib.dspark_schedule(
+        None, A, R, K, GOOD, R * (K + 1) + 1 if sps_len is None else sps_len, GOOD, None, None)
+    assert s() == E.INVALID_ARG
+    assert s(R=1025, K=16) == E.UNSUPPORTED            # more than 16384 candidates
+    assert s(R=70000, K=0, A=None) == E.UNSUPPORTED    # R above 65535
+    assert s(R=5, K=0, A=None) == E.INVALID_ARG        # nothing to admit: only the context
+    assert s(sps_len=128 * 17) == E.INVALID_ARG        # SPS one entry short
+    f = lambda N=8192, K=16, lo=1.0 / 64, hi=64.0: lib.dspark_sts_fit(
+        None, GOOD, GOOD, N, K, lo, hi, GOOD, None, None)
+    assert f() == E.INVALID_ARG
+    assert f(K=65) == E.UNSUPPORTED
+    assert f(lo=2.0, hi=1.0) == E.INVALID_ARG
