@@ -263,6 +263,7 @@ PROFILES = {
     "serving": ("draft_kernel_serving.md", ("draft.cu",) + _HEADERS),
     "label": ("label_step_serving.md", ("draft.cu", "label.cu", "verify.cu") + _HEADERS),
     "verify": ("verify_step_serving.md", ("draft.cu", "verify.cu") + _HEADERS),
+    "selector": ("topk_stream_kernel_selector.md", ("selector.cu", "gate.cu") + _HEADERS),
 }
 
 
