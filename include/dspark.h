@@ -180,6 +180,10 @@ int dspark_gated_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1,
                        const dspark_conf_args* conf, dspark_stream_t stream);
 
 /* The gate alone: H[m, :] = sigmoid(h[m, :] . Wg) for m < M.
+ * Source: equivalence page, "What the two methods do" (the gate H(h_t) is a
+ * function of the current hidden state alone, so every (request, position)
+ * is gated at once, ahead of the draft); its sigmoid(h . Wg) form is this
+ * library's reading (the gated workload fixes it).
  * h [M, d] bf16, Wg [d, r] bf16, H out [M, r] fp32; d, r multiples of 64,
  * M <= B_max * K_max. */
 int dspark_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int d, int r,
@@ -194,14 +198,16 @@ int dspark_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, i
  * (no confidence head); the kernel's scratch is one fixed array of about 7.9 MB
  * compiled into the library, present on every GPU that loads it until the
  * process exits.
- *   Limits: K <= 16 (else DSPARK_ERR_CAPACITY), other shape rules as
- *   dspark_markov_draft; the current device must be sm_103 and hold the
- *   pointers.
+ *   Limits: K <= 16 and B <= 16383 * 128 (else DSPARK_ERR_CAPACITY), other
+ *   shape rules as dspark_markov_draft; the current device must be sm_103
+ *   and hold the pointers.
  *   device_status: optional device int that receives the launch's device
  *   status (a dspark_status) in stream order; NULL to skip.
- *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   Set-up: the first call in a CUDA context (per device: its primary
+ *   context) looks up the array's device address (cudaGetSymbolAddress) with
+ *   that device current; make that first call before any stream capture.  A
+ *   new context on the device (after cudaDeviceReset, say) triggers a new
+ *   look-up at its first call, since the array may have moved.
  *   Sharing: every call on a device uses the same array and starts by clearing
  *   its counters and keys on `stream`; calls that overlap on the GPU (other
  *   streams or host threads) race and must be serialised by the caller. */

@@ -13,8 +13,11 @@
 // __device__ array of a fixed size, loaded with the library on every GPU and
 // kept until the process exits.  Host code cannot use the array's name as a
 // device address (on the host it is only a stand-in symbol), so its device
-// address is looked up once per device with cudaGetSymbolAddress while that
-// device is current, and passed to the kernel.
+// address is looked up with cudaGetSymbolAddress while the device is current,
+// and passed to the kernel.  The look-up is done once per CUDA context: the
+// cache is keyed on the current context's process-unique id (cuCtxGetId), so a
+// context created after cudaDeviceReset (which reloads the module and can
+// move the array) gets a fresh look-up instead of a stale address.
 //
 // The array is shared by every call on a device and keeps the contents of the
 // last call: each call clears the counter, status and keys on its stream
@@ -37,6 +40,9 @@ namespace {
 constexpr int kNaMaxK = 16;       // block positions
 constexpr int kNaMaxGrid = 160;   // CTAs (one per SM; GB300 has 152)
 constexpr int kNaMaxDevices = 64;
+// key epochs of the draft kernel are 14-bit (1 .. 16383): one per 128-request chunk
+constexpr int kNaMaxChunks = 16383;
+constexpr int kNaMaxBatch = kNaMaxChunks * dspark::kBatchChunk;
 
 constexpr size_t kNaOffBar = 0;         // uint32_t grid-barrier counter
 constexpr size_t kNaOffStatus = 4;      // int device status
@@ -53,7 +59,9 @@ static_assert(kNaOffPartials % 256 == 0, "partials must stay 256-byte aligned");
 static __device__ __align__(256) unsigned char g_draft_scratch[kNaScratchBytes];
 
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kNaMaxDevices] = {};  // device address of g_draft_scratch, per device
+// device address of g_draft_scratch per device, valid for the context it was looked up in
+void* g_scratch_ptr[kNaMaxDevices] = {};
+unsigned long long g_scratch_ctx[kNaMaxDevices] = {};  // that context's id (0: none yet)
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -86,15 +94,50 @@ bool encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int rank
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// One-time set-up on the current device: the scratch's device address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the calling thread's current CUDA context (0 on failure).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Set-up on the current device, once per CUDA context: the scratch's device address.
+// If no context is current yet on this thread, cudaGetSymbolAddress initialises the
+// device's primary context (and makes it current) before the id is read.
 int scratch_for_current_device(int device, unsigned char** out) {
   if (device < 0 || device >= kNaMaxDevices) return DSPARK_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[device] == nullptr) {
+  unsigned long long ctx_id = current_context_id();  // 0: no context current yet
+  if (ctx_id == 0 || g_scratch_ptr[device] == nullptr || g_scratch_ctx[device] != ctx_id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_draft_scratch) != cudaSuccess || ptr == nullptr)
       return DSPARK_ERR_CUDA;
+    ctx_id = current_context_id();
+    if (ctx_id == 0) return DSPARK_ERR_CUDA;
     g_scratch_ptr[device] = ptr;
+    g_scratch_ctx[device] = ctx_id;
   }
   *out = static_cast<unsigned char*>(g_scratch_ptr[device]);
   return DSPARK_OK;
@@ -112,6 +155,7 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, c
     return DSPARK_ERR_INVALID_ARG;
   if (B <= 0 || K <= 0 || V <= 0) return DSPARK_ERR_INVALID_ARG;
   if (K > kNaMaxK) return DSPARK_ERR_CAPACITY;  // the fixed scratch holds 16 positions
+  if (B > kNaMaxBatch) return DSPARK_ERR_CAPACITY;  // one 14-bit key epoch per 128 requests
   if (V > (1 << 18) || (V % 8) != 0) return DSPARK_ERR_UNSUPPORTED;
   if (r < 0) return DSPARK_ERR_INVALID_ARG;
   if (r > dspark::kMaxRank || (r % 16) != 0) return DSPARK_ERR_UNSUPPORTED;

@@ -154,3 +154,20 @@ def test_verify_label_schedule_sts_argument_checks(lib):
     assert f() == E.INVALID_ARG
     assert f(K=65) == E.UNSUPPORTED
     assert f(lo=2.0, hi=1.0) == E.INVALID_ARG
+
+
+def test_noalloc_host_limits(lib):
+    """The allocation-free draft checks its fixed limits on the host, before any CUDA call:
+    16 positions (its scratch holds 16 key rows) and 16383 chunks of 128 requests (one
+    14-bit key epoch per chunk)."""
+    E = binding
+    na = lambda B=4, K=16, V=4096, r=256, T=1.0, U=GOOD: lib.dspark_markov_draft_noalloc(
+        U, GOOD, GOOD, GOOD, B, K, V, r, T, 0, GOOD, GOOD, None, None)
+    assert na(K=17) == E.CAPACITY
+    assert na(B=16383 * 128 + 1) == E.CAPACITY
+    assert na(B=0) == E.INVALID_ARG
+    assert na(U=None) == E.INVALID_ARG
+    assert na(V=4100) == E.UNSUPPORTED
+    assert na(r=17) == E.UNSUPPORTED
+    assert na(T=-1.0) == E.INVALID_ARG
+    assert na(U=ODD) == E.INVALID_ARG
