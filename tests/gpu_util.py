@@ -5,6 +5,7 @@ import torch
 
 LOGPROB_TOL = 2e-3     # teacher-forced logits / log-probabilities, absolute
 MARGIN = 1e-3          # tokens must match wherever the oracle's top-2 margin exceeds this
+COVERAGE = 0.95        # share of the replayed (request, position) pairs that must be compared
 
 
 def dev(a):
@@ -44,6 +45,17 @@ def check_sequences(gpu_tokens, gpu_logprobs, ref, margin=MARGIN, tol=LOGPROB_TO
         compared += n
     assert np.all(gpu_logprobs <= 1e-6)
     return diverged, compared
+
+
+def assert_coverage(what, diverged, compared, total, min_share=COVERAGE):
+    """Print how many replayed positions were compared and how many requests stopped at a
+    near tie, and fail when fewer than min_share of the replayed positions were compared
+    (a run in which most positions went uncompared would otherwise pass)."""
+    share = compared / total if total else 1.0
+    print(f"{what}: compared {compared} of {total} positions ({share:.4f}); "
+          f"{diverged} requests diverged at a near tie")
+    assert share >= min_share, (
+        f"{what}: only {compared} of {total} positions compared ({share:.3f} < {min_share})")
 
 
 def first_difference(a, b):

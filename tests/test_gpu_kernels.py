@@ -217,6 +217,48 @@ def test_gpu_sampler_matches_exhaustive_joint(dsp):
     assert np.allclose(lp, np.log(P.reshape(-1)[cell[:5000]]), atol=3 * LOGPROB_TOL)
 
 
+def test_gpu_block_race_over_several_blocks_matches_exhaustive_joint(dsp):
+    """The draw's first stage (the exponential race between 16-token blocks) on the GPU:
+    V = 56 spans four blocks (the last one ragged, 8 tokens) with unequal masses, K = 2,
+    T = 0.8.  10^6 draws vs prod_k softmax((U_k + W1[x_{k-1}] W2) / T) enumerated over
+    all V^2 paths, and the block frequencies at each position vs the blocks' masses."""
+    V, K, r, N, T = 56, 2, 16, 1_000_000, 0.8
+    rng = np.random.default_rng(12)
+    offset = np.repeat([0.0, 1.5, -1.0, 0.8], 16)[:V]
+    U1 = (rng.standard_normal((1, K, V)) + offset).astype(np.float32)
+    W1 = bf16_bits(rng.normal(0, 0.3, (V, r)).astype(np.float32))
+    W2 = bf16_bits(rng.normal(0, 0.3, (r, V)).astype(np.float32))
+    anchor = 9
+    U = torch.from_numpy(U1).cuda().expand(N, K, V).contiguous()
+    anchors = torch.full((N,), anchor, dtype=torch.int32, device="cuda")
+    out = binding.markov_draft(dsp, U, bf(W1), bf(W2), anchors, temperature=T, seed=77)
+    torch.cuda.synchronize()
+    assert dsp.status() == 0
+    paths = host(out["tokens"]).astype(np.int64)
+    w1 = (W1.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w2 = (W2.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bias = w1 @ w2
+    p1 = special.softmax((U1[0, 0] + bias[anchor]) / T)
+    P = np.stack([p1[x] * special.softmax((U1[0, 1] + bias[x]) / T) for x in range(V)])
+    counts = np.bincount(paths[:, 0] * V + paths[:, 1], minlength=V * V).astype(np.float64)
+    exp = P.reshape(-1) * N
+    small = exp < 5
+    obs = np.concatenate([counts[~small], [counts[small].sum()]])
+    ex = np.concatenate([exp[~small], [exp[small].sum()]])
+    assert stats.chisquare(obs, ex).pvalue > 0.01
+    # the block marginal at each position (stage 1 alone)
+    blocks0 = np.bincount(paths[:, 0] // 16, minlength=4)
+    mass0 = np.add.reduceat(p1, [0, 16, 32, 48])
+    assert stats.chisquare(blocks0, mass0 * N).pvalue > 0.01
+    blocks1 = np.bincount(paths[:, 1] // 16, minlength=4)
+    mass1 = np.add.reduceat(P.sum(axis=0), [0, 16, 32, 48])
+    assert stats.chisquare(blocks1, mass1 * N).pvalue > 0.01
+    assert mass0.max() / mass0.min() > 3  # the blocks' masses are far from equal
+    lp = host(out["logprobs"])[:5000].sum(1)
+    assert np.allclose(lp, np.log(P.reshape(-1)[paths[:5000, 0] * V + paths[:5000, 1]]),
+                       atol=3 * LOGPROB_TOL)
+
+
 # --------------------------------------------------------------------- selector
 def _selector_inputs(seed, B, K, V, r, d=0, gated=False):
     return make_inputs(seed, B, K, V, r, d=d, gated=gated, selector=True)

@@ -16,7 +16,7 @@ from scipy import special, stats
 import oracle
 from rank_markov_draft_gb300 import binding
 from synth import bf16_bits, make_inputs
-from tests.gpu_util import MARGIN, bf, dev, host
+from tests.gpu_util import COVERAGE, MARGIN, bf, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def _run(dsp, inp, P, Td, Tt, seed, ell=None, gated=False):
 def _check(inp, P, tokens, out, Td, Tt, seed, ell=None, H=None, requests=None):
     B = P.shape[0]
     requests = range(B) if requests is None else requests
-    hard = 0
+    hard = near = 0
     for b in requests:
         ref = oracle.verify(P, inp.U, inp.W1, inp.W2, inp.anchors, tokens,
                             draft_temperature=Td, target_temperature=Tt, seed=seed + 1,
@@ -55,12 +55,17 @@ def _check(inp, P, tokens, out, Td, Tt, seed, ell=None, H=None, requests=None):
         same = (out["n_acc"][b] == ref["n_acc"][0]) and (out["next_token"][b] == ref["next_token"][0])
         if not same and ref["margins"][0] > MARGIN:
             hard += 1
+        elif not same:
+            near += 1
         if same:
             n = out["n_acc"][b]
             k = min(n + 1, P.shape[1] - 1, (ell[b] if ell is not None else P.shape[1] - 1))
             a_gpu, a_ref = out["accept_prob"][b, :k], ref["accept_prob"][0, :k]
             assert np.allclose(a_gpu, a_ref, rtol=2e-3, atol=2e-5), (b, a_gpu, a_ref)
     assert hard == 0, f"{hard} requests differ from the oracle with margin > {MARGIN}"
+    n = len(requests)
+    print(f"verify: {n - near} of {n} requests match the oracle; {near} differ at a near tie")
+    assert near <= max(1, (1 - COVERAGE) * n), f"{near} of {n} requests stopped at a near tie"
 
 
 @pytest.mark.parametrize("Td,Tt", [(1.0, 1.0), (0.7, 1.3), (0.0, 1.0), (1.0, 0.0), (0.0, 0.0)])
@@ -127,13 +132,14 @@ def test_verify_first_committed_token_is_the_target_distribution(dsp):
 
 
 def test_verify_serving_size(dsp):
-    """B=128, K=16, V=151936: the whole batch on the GPU, sampled requests replayed."""
+    """B=128, K=16, V=151936: the whole batch on the GPU, every request replayed by the
+    oracle."""
     from synth import config_inputs
     inp = config_inputs(2)
     P = _target_logits(np.random.default_rng(67), inp.U, noise=1.0)
     tokens, out = _run(dsp, inp, P, 1.0, 1.0, seed=11)
     assert np.all(out["n_acc"] <= 16)
-    _check(inp, P, tokens, out, 1.0, 1.0, seed=11, requests=[0, 77, 127])
+    _check(inp, P, tokens, out, 1.0, 1.0, seed=11)
 
 
 @pytest.mark.parametrize("Td", [1.0, 0.0])
