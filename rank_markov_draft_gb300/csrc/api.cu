@@ -199,7 +199,7 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
               int r, float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
               float* logits, float* lse, const dspark_conf_args* conf, cudaStream_t stream,
               const LabelIn* lab = nullptr) {
-  const int n_tiles = (V + dspark::kDraftTileV - 1) / dspark::kDraftTileV;
+  const int n_tiles = (V + dspark::kDraftTileN - 1) / dspark::kDraftTileN;
   const int grid = n_tiles < ctx->num_sms ? n_tiles : ctx->num_sms;
   const float inv_t = temperature > 0.f ? 1.0f / temperature : 1.0f;
   for (int b0 = 0; b0 < B; b0 += dspark::kBatchChunk) {
@@ -207,7 +207,8 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     DraftArgs args;
     std::memset(&args, 0, sizeof(args));
     if (r > 0 && !encode_2d(&args.tm_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W2, V, r,
-                            static_cast<uint64_t>(V) * 2, dspark::kDraftTileV, r))
+                            static_cast<uint64_t>(V) * 2, dspark::kDraftBoxV,
+                            dspark::draft_slice_rows(r)))
       return DSPARK_ERR_CUDA;
     const int box_rows = (Bc + 7) & ~7;
     const bool res = lab != nullptr && lab->rows != nullptr;

@@ -13,45 +13,53 @@
 //
 // Layout of the work (one CTA per SM, cooperative launch, all K steps in one
 // launch):
-//   * the vocabulary is split into 64-token tiles; CTA c owns a fixed,
-//     contiguous range of tiles for every step;
-//   * warp 0 (one lane) streams W2 tiles [r x 64] and U tiles [rows x 64]
-//     with TMA into shared memory rings; these never depend on sampled
-//     tokens, so the producer runs ahead across step boundaries;
-//   * warp 1 (one lane) issues tcgen05.mma: D[128 requests x 64 tokens] =
-//     E[128 x r] * W2tile[r x 64] into one of four TMEM accumulators;
-//     E is the gathered Markov embedding of every request, gathered into
-//     shared memory (K-major, 128B swizzle) and copied once per position into
-//     TMEM (row m in lane m, two bf16 per column), from where the MMAs read it
-//     (each MMA would otherwise re-read its A slice from shared memory); W2 is
-//     the MN-major tile exactly as TMA wrote it;
-//   * warps 2..17 (the epilogue) read the accumulator (one request per TMEM
-//     lane, 16 tokens per thread) and U from shared memory, and keep, per
-//     request, a running log-sum-exp and a running block-race winner, so the
-//     full-vocabulary logits never reach HBM;
+//   * the vocabulary is split into 128-token tiles (the MMA's N); CTA c owns
+//     a fixed, contiguous range of tiles for every step.  A tcgen05.mma of
+//     M = 128 rows and K = 16 costs about the same time for N = 64, 128 or 256,
+//     so the tile is as wide as the tensor memory allows: three 128-column
+//     accumulators plus the 128 columns of the A operand fill the 512 columns;
+//   * warp 0 (one lane) streams W2 with TMA in slices of [128 rows x 128
+//     tokens] (a tile is one slice per 128 of the rank) into a 3-slot ring;
+//     warp 2 (one lane) streams U in 64-token sub-tiles [rows x 64] into its
+//     own ring.  Neither depends on sampled tokens, so both run ahead across
+//     step boundaries, and neither waits for the other's ring;
+//   * warp 1 (one lane) issues tcgen05.mma: D[128 requests x 128 tokens] =
+//     E[128 x r] * W2tile[r x 128] into one of three TMEM accumulators.  E,
+//     the gathered Markov embedding of every request, lives in TMEM (row m in
+//     lane m, two bf16 per column), written there by the epilogue threads
+//     straight from global memory (no shared-memory staging); W2 is the
+//     MN-major slice exactly as TMA wrote it;
+//   * warps 3..18 (the epilogue) read the accumulator (one request per TMEM
+//     lane, 16 tokens of each 64-token sub-tile per thread) and U from shared
+//     memory, and keep, per request, a running log-sum-exp and a running
+//     block-race winner, so the full-vocabulary logits never reach HBM;
 //   * at the end of a step each CTA publishes, per request, a 64-bit key
 //     (epoch | ordered score | inverted token id) by atomicMax and its
-//     log-sum-exp partial; after a bounded grid barrier every CTA decodes the
-//     winning tokens from the keys and gathers the next step's embeddings;
+//     log-sum-exp partial; it arrives at a bounded grid barrier and, while the
+//     others finish, writes the next step's operand for the winners known so
+//     far; after the barrier only rows whose winner changed are rewritten;
 //   * after the last step, CTA c reduces request c's partials into tokens and
 //     log-probabilities and runs the fused confidence head.
 //
+// Small batches (B <= 64): the 128 MMA rows hold two copies of the batch (row
+// m serves request m mod 64); copy c takes the 64-token sub-tile c of every
+// tile, so every TMEM lane quadrant holds real rows.
+//
 // Teacher-forced modes take every position's predecessor from the caller, so
-// positions do not depend on one another: the next position's embeddings are
-// gathered as soon as the MMAs are done with the current ones and the grid
+// positions do not depend on one another: the next position's operand is
+// written as soon as the MMAs are done with the current one and the grid
 // barrier is waited on only before the final reduction.  The label mode
 // (DSpark explainer, "Confidence-scheduled verification": c*_k = 1 - TV of the
 // draft head's and the target's distributions) streams the target's rows
 // beside U and sums 2^min(log2 q(v), log2 p(v)) over the vocabulary, both
 // normalisers known beforehand (the target's from a row scan, the draft's
 // from its own log-probability of the drafted token).  Its ring slots hold U
-// and target for half a tile (32 tokens each), two slots per tile, so the
-// same 96 KB of shared memory keeps twice the bytes per tile in flight; every
-// epilogue warp reads both halves (8 tokens of each per thread), so each slot
-// has one group of readers that takes its fills in order.
+// and target for half a sub-tile (32 tokens each), two slots per sub-tile;
+// every epilogue warp reads both halves (8 tokens of each per thread), so each
+// slot has one group of readers that takes its fills in order.
 //
 // Sampling epilogue (an exact draw from softmax(l / T) in two stages over
-// 16-token blocks; each thread's 16 columns of a tile are one block beta):
+// 16-token blocks; each thread's 16 columns of a sub-tile are one block beta):
 //   y = l * log2(e) / T, w = 2^(y - m) (shared with the log-sum-exp), and the
 //   block's mass relative to m is s = sum w;
 //   stage 1, a race between blocks: the block maximising
@@ -59,8 +67,9 @@
 //   wins with probability Z_beta / Z (argmax Z_beta / E_beta);
 //   stage 2, only for a block that can still beat the best G any thread has
 //   reached for the request: the first token whose cumulative w exceeds
-//   u2 * s.  Both uniforms come from one Philox call per two of the thread's
-//   tiles.  The (G, token) winner is merged across threads and CTAs as a key.
+//   u2 * s.  Both uniforms of both of a thread's blocks in a tile come from one
+//   Philox call.  The (G, token) winner is merged across threads and CTAs as a
+//   key.
 //
 // Every wait is bounded (mbarrier waits and the grid barrier give up after
 // timeout_ns, set the device status word and make the CTA exit cleanly after
@@ -69,9 +78,6 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
-#ifndef BOUND_REFRESH
-#define BOUND_REFRESH 2
-#endif
 #include "confidence.cuh"
 #include "internal.h"
 #include "philox.cuh"
@@ -80,31 +86,40 @@
 namespace dspark {
 namespace {
 
-constexpr int kTileV = kDraftTileV;              // 64 tokens per tile (MMA N)
+constexpr int kTileN = kDraftTileN;              // 128 tokens per MMA tile (MMA N)
+constexpr int kSubV = 64;                        // tokens per epilogue sub-tile (U ring slot)
 constexpr int kRows = kBatchChunk;               // 128 requests (MMA M)
-constexpr int kNumW2Stages = 2;
+constexpr int kNumW2Slots = 3;                   // W2 ring: slices of [128 rows x 128 tokens]
 constexpr int kNumUStages = 3;                   // U ring slots of 32 KB (B > 64)
 constexpr int kNumUStagesSmall = 4;              // slots of 16 KB when B <= 64 (box <= 64 rows)
-constexpr int kNumAcc = 4;                       // TMEM accumulators, 64 columns each
-constexpr int kEpiWarps = 16;
-constexpr int kEpiThreads = kEpiWarps * 32;      // 512
-constexpr int kThreads = 64 + kEpiThreads;       // 576
-constexpr uint32_t kABytes = kRows * kMaxRank * 2;           // 64 KB
-constexpr uint32_t kW2StageBytes = kMaxRank * kTileV * 2;    // 32 KB
+constexpr int kNumAcc = 3;                       // TMEM accumulators, 128 columns each
+constexpr int kCtlWarps = 2;                     // U producer; MMA issuer and W2 producer
+// Eight epilogue warps: two per TMEM lane quadrant, each thread taking 32 tokens (two
+// 16-token blocks) of every 64-token sub-tile.  Ten warps in all leave up to 168
+// registers a thread (three warps on a scheduler), enough for two blocks at once.
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;      // 256
+constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;  // 320
+constexpr uint32_t kW2SlotBytes = kDraftSliceRows * kTileN * 2;  // 32 KB
 constexpr uint32_t kUBoxBytes = kRows * 32 * 4;              // 16 KB (32 tokens x 128 rows)
 constexpr uint32_t kUStageBytes = 2 * kUBoxBytes;            // 32 KB
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffW2 = kOffA + kABytes;
-constexpr uint32_t kOffU = kOffW2 + kNumW2Stages * kW2StageBytes;
-constexpr uint32_t kOffBar = kOffU + kNumUStages * kUStageBytes;
+// merge records: (2 column groups x batch copies) slots x 5 fields x rows per copy
+constexpr uint32_t kMergeBytes = 2 * 5 * kRows * 4;          // 5 KB
+constexpr uint32_t kOffW2 = 0;
+constexpr uint32_t kOffU = kOffW2 + kNumW2Slots * kW2SlotBytes;
+// each epilogue thread's best block of the position so far: 16 floats, stored as four
+// float4 planes [4][threads] so that a warp's stores are contiguous
+constexpr uint32_t kBestBytes = kEpiThreads * 16 * 4;        // 16 KB
+constexpr uint32_t kOffMerge = kOffU + kNumUStages * kUStageBytes;
+constexpr uint32_t kOffBest = kOffMerge + kMergeBytes;
+constexpr uint32_t kOffBar = kOffBest + kBestBytes;
 constexpr uint32_t kBarRegion = 2048;
 constexpr uint32_t kSmemBytes = kOffBar + kBarRegion + 1024;  // + alignment slack
-// TMEM: kNumAcc accumulators of 64 columns, then the MMA's A operand ([128 x r] bf16,
+// TMEM: kNumAcc accumulators of 128 columns, then the MMA's A operand ([128 x r] bf16,
 // two elements per column: r / 2 <= 128 columns)
-constexpr uint32_t kTmemA = kNumAcc * kTileV;                // 256
+constexpr uint32_t kTmemA = kNumAcc * kTileN;                // 384
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;                          // named barrier id
-constexpr int kBoundRefresh = BOUND_REFRESH;  // tiles between reads of the global bound
 constexpr uint32_t kBackoffControlNs = 200;  // sleep between polls of the TMA / MMA lanes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -113,8 +128,9 @@ constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
 
 static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103 limit");
 static_assert(kTmemA + kMaxRank / 2 <= kTmemCols, "TMEM columns");
-static_assert((kNumAcc & (kNumAcc - 1)) == 0, "accumulator count must be a power of two");
-static_assert((2 * kNumW2Stages + 2 * kNumUStagesSmall + 2 * kNumAcc + 5) * 8 + 2 * kMaxK * 4 +
+static_assert(kNumUStagesSmall * kUStageBytes / 2 <= kNumUStages * kUStageBytes, "U ring");
+static_assert(kTileN == 2 * kSubV, "a tile is two sub-tiles");
+static_assert((2 * kNumW2Slots + 2 * kNumUStagesSmall + 2 * kNumAcc + 6) * 8 + 2 * kMaxK * 4 +
                       kRows * 8 + 16 <=
                   kBarRegion,
               "barrier region too small");
@@ -155,24 +171,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// Small batches: with B <= 32 (64) requests, the 128 MMA rows hold 4 (2) copies
-// of the batch, row m serving request m mod rows_per_copy, so that the TMEM lane
-// quadrants of every epilogue warp hold real rows; the copies split the tiles.
-__device__ __forceinline__ int rows_per_copy(int B) { return B <= 32 ? 32 : (B <= 64 ? 64 : 128); }
+// Small batches: with B <= 64 requests the 128 MMA rows hold two copies of the batch,
+// row m serving request m mod 64, so that every TMEM lane quadrant holds real rows.
+__device__ __forceinline__ int rows_per_copy(int B) { return B <= 64 ? 64 : kRows; }
 
-// Gather the step's Markov embeddings into the K-major, 128B-swizzled MMA
-// operand: row b (request b mod rows_per_copy), 64-element K chunk c at
-// c * 16 KB, 8-row groups of 1024 B, 16-byte unit u of row b stored at unit
-// (u ^ (b & 7)).  Thread etid handles row etid / 4 and K chunk etid % 4.
-__device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams& p, int k,
-                                                  int etid, int32_t tok) {
-  const int b = etid >> 2, c = etid & 3;
-  const int req = b & (rows_per_copy(p.B) - 1);
-  const bool live = req < p.B;
+// One K chunk (elements [64 cc, 64 cc + 64)) of the Markov embedding of token `tok` --
+// gated: times H[req, k] and rounded to bf16 -- packed the way the MMA reads its A
+// operand from TMEM: elements 2j and 2j + 1 of the chunk in column j.  A dead row
+// (no request) and elements past r are zero.
+__device__ __forceinline__ void load_embedding(const DraftParams& p, int k, int req, bool live,
+                                               int cc, int32_t tok, uint32_t (&wv)[32]) {
   uint4 vals[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int kel = c * 64 + u * 8;
+    const int kel = cc * 64 + u * 8;
     if (live && kel < p.r) {
       vals[u] = __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel));
     } else {
@@ -183,7 +195,7 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
     const float* hrow = p.H + (static_cast<size_t>(req) * p.K + k) * p.r;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int kel = c * 64 + u * 8;
+      const int kel = cc * 64 + u * 8;
       if (kel < p.r) {
         const float4 g0 = __ldg(reinterpret_cast<const float4*>(hrow + kel));
         const float4 g1 = __ldg(reinterpret_cast<const float4*>(hrow + kel + 4));
@@ -196,33 +208,13 @@ __device__ __forceinline__ void gather_embeddings(uint8_t* sA, const DraftParams
       }
     }
   }
-  uint8_t* base = sA + c * 16384 + (b >> 3) * 1024 + (b & 7) * 128;
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    *reinterpret_cast<uint4*>(base + ((u ^ (b & 7)) << 4)) = vals[u];
+    wv[4 * u + 0] = vals[u].x;
+    wv[4 * u + 1] = vals[u].y;
+    wv[4 * u + 2] = vals[u].z;
+    wv[4 * u + 3] = vals[u].w;
   }
-}
-
-// Asynchronous form of gather_embeddings without a gate: the thread's 128-byte
-// piece of W1[tok] goes to the operand by 16-byte cp.async copies (rows of no
-// request and K chunks past r are zeroed with plain stores).
-__device__ __forceinline__ void copy_embedding_async(uint8_t* sA, const DraftParams& p, int etid,
-                                                     int32_t tok) {
-  const int b = etid >> 2, c = etid & 3;
-  const int req = b & (rows_per_copy(p.B) - 1);
-  const bool live = req < p.B;
-  uint8_t* base = sA + c * 16384 + (b >> 3) * 1024 + (b & 7) * 128;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int kel = c * 64 + u * 8;
-    uint8_t* dst = base + ((u ^ (b & 7)) << 4);
-    if (live && kel < p.r) {
-      cp_async_16(dst, p.W1 + static_cast<size_t>(tok) * p.r + kel);
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  cp_async_commit();
 }
 
 // Score of a key (the ordered float in its middle bits); -inf for "no key".
@@ -258,46 +250,67 @@ __device__ __forceinline__ void lse_merge(float& ma, float& sa, float mb, float 
   }
 }
 
-// One 16-token block's part in the two-stage race (w: the block's weights relative to
-// 2^m2, s = their sum, y: their scaled logits): stage 1 scores the block by
-// G = m2 + log2(s) - log2(E), E = -ln u1; a block that can still beat the best key
-// known for the request (this thread's, the CTA's, or the global one as last read)
-// runs stage 2, the first token whose cumulative weight exceeds u2 * s.
-__device__ __forceinline__ void race_block(const float (&w)[16], const float (&y)[16], float m2,
-                                           float bsum, uint32_t word1, uint32_t word2, int vbase,
-                                           uint32_t epoch, float inv_scale2,
-                                           unsigned long long* bound, unsigned long long gkey,
-                                           unsigned long long& bkey, float& yb, int& vb,
-                                           float& lb) {
-  const float G = m2 + lg2_approx(bsum) - lg2_approx(neg_log_uniform_fast(word1));
-  const unsigned long long sb = *bound;
-  const float S = key_score(sb > gkey ? sb : gkey);
-  if (bsum > 0.f && G >= S) {
-    float C[16];
-    C[0] = w[0];
+// Store four float4 to shared memory if `pred` (predicated, no branch).
+__device__ __forceinline__ void st_shared_v4_if(bool pred, float4* dst, float4 v) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 0;\n\t"
+      "@p st.shared.v4.f32 [%1], {%2, %3, %4, %5};\n\t}" ::"r"(pred ? 1u : 0u),
+      "r"(smem_addr(dst)), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+      : "memory");
+}
+
+// Keep the better of this thread's best block so far and a new one: the block's score
+// (the race's G, or the greedy maximum), its first token, its stage-2 uniform word and
+// its 16 values (logits, or the weights themselves in the residual draw), which go to
+// this thread's slot of the shared best-block store.  Ties keep the earlier block, which
+// holds the smaller token ids.
+__device__ __forceinline__ void keep_best(float score, int vbase, uint32_t word2, const float* v,
+                                          float4* slot, int stride, float& best, int& best_v,
+                                          uint32_t& best_w) {
+  const bool better = score > best;
+  best = better ? score : best;
+  best_v = better ? vbase : best_v;
+  best_w = better ? word2 : best_w;
 #pragma unroll
-    for (int j = 1; j < 16; ++j) C[j] = C[j - 1] + w[j];
-    const float target = philox_uniform(word2) * C[15];
-    int js = -1, jl = 0;
+  for (int c = 0; c < 4; ++c)
+    st_shared_v4_if(better, slot + c * stride,
+                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+}
+
+// Stage 2 of the race in the thread's best block, once per position: the first token whose
+// cumulative weight exceeds u2 times the block's mass; w are the block's weights (any
+// common scale).  Returns the index in the block.
+__device__ __forceinline__ int race_stage2(const float (&w)[16], uint32_t word2) {
+  float C[16];
+  C[0] = w[0];
 #pragma unroll
-    for (int j = 15; j >= 0; --j) {
-      if (target < C[j]) js = j;
-      if (jl == 0 && w[j] > 0.f) jl = j;
-    }
-    if (js < 0) js = jl;  // target at the very top (rounding): the last live token
-    float yj = 0.f;
+  for (int j = 1; j < 16; ++j) C[j] = C[j - 1] + w[j];
+  const float target = philox_uniform(word2) * C[15];
+  int js = -1, jl = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j == js) yj = y[j];
-    const unsigned long long key = make_key(epoch, G, vbase + js);
-    if (key > bkey) {
-      bkey = key;
-      yb = G;
-      vb = vbase + js;
-      lb = yj * inv_scale2;
-      atomicMax(bound, key);
-    }
+  for (int j = 15; j >= 0; --j) {
+    if (target < C[j]) js = j;
+    if (jl == 0 && w[j] > 0.f) jl = j;
   }
+  return js < 0 ? jl : js;  // target at the very top (rounding): the last live token
+}
+
+// Largest of 16 values (three-input maxima).
+__device__ __forceinline__ float max16(const float* x) {
+  const float a0 = fmax3(x[0], x[1], x[2]), a1 = fmax3(x[3], x[4], x[5]);
+  const float a2 = fmax3(x[6], x[7], x[8]), a3 = fmax3(x[9], x[10], x[11]);
+  const float a4 = fmax3(x[12], x[13], x[14]);
+  return fmaxf(fmax3(a0, a1, a2), fmax3(a3, a4, x[15]));
+}
+
+// Sum of 16 values as a pairwise tree of packed additions.
+__device__ __forceinline__ float sum16(const float* w) {
+  float2 s0 = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
+  float2 s1 = __fadd2_rn(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
+  float2 s2 = __fadd2_rn(make_float2(w[8], w[9]), make_float2(w[10], w[11]));
+  float2 s3 = __fadd2_rn(make_float2(w[12], w[13]), make_float2(w[14], w[15]));
+  s0 = __fadd2_rn(__fadd2_rn(s0, s1), __fadd2_rn(s2, s3));
+  return s0.x + s0.y;
 }
 
 template <int MODE, bool COPIES>
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   const DraftParams& p = args.p;
   // teacher-forced modes take the predecessors from the caller
   constexpr bool kTF = MODE == kModeTeacherForced || MODE == kModeLabel || MODE == kModeResidual;
-  // ring slots of half tiles holding U and the target rows
+  // ring slots of half sub-tiles holding U and the target rows
   constexpr bool kHalf = MODE == kModeLabel || MODE == kModeResidual;
   // modes that draw a token by the block race
   constexpr bool kRace = MODE == kModeSample || MODE == kModeResidual;
@@ -314,21 +327,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem + kOffA;
   uint8_t* sW = smem + kOffW2;
   uint8_t* sU = smem + kOffU;
+  float* merge = reinterpret_cast<float*>(smem + kOffMerge);
+  float4* s_best = reinterpret_cast<float4*>(smem + kOffBest);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* w_full = bars;                          // [kNumW2Stages]
-  uint64_t* w_empty = w_full + kNumW2Stages;        // [kNumW2Stages]
-  uint64_t* u_full = w_empty + kNumW2Stages;        // [kNumUStagesSmall]
+  uint64_t* w_full = bars;                          // [kNumW2Slots]
+  uint64_t* w_empty = w_full + kNumW2Slots;         // [kNumW2Slots]
+  uint64_t* u_full = w_empty + kNumW2Slots;         // [kNumUStagesSmall]
   uint64_t* u_empty = u_full + kNumUStagesSmall;    // [kNumUStagesSmall]
   uint64_t* acc_full = u_empty + kNumUStagesSmall;  // [kNumAcc]
   uint64_t* acc_empty = acc_full + kNumAcc;         // [kNumAcc]
   uint64_t* a_full = acc_empty + kNumAcc;
   uint64_t* a_empty = a_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_empty + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(a_empty + 2);
-  int32_t* s_tok = reinterpret_cast<int32_t*>(a_empty + 3);  // [kMaxK]
+  uint64_t* mma_drain = a_empty + 1;  // an aborting MMA lane waits here for its MMAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_drain + 2);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(mma_drain + 3);  // [kMaxK]
   float* s_conf = reinterpret_cast<float*>(s_tok + kMaxK);  // [kMaxK]
   // best key (epoch | score | token) any thread of this CTA reached for each
   // request in the current step: a lower bound on the step's winner
@@ -341,31 +356,33 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   const int t_end = static_cast<int>(static_cast<int64_t>(cta + 1) * p.n_tiles / ncta);
   const int nt = t_end - t_begin;
   const int nkk = p.r / 16;
-  // Small batches use 4 U slots of 16 KB (a multiple of the batch copies, so every
-  // use of a slot -- and of an accumulator -- is read by the same copy and its
-  // warps see each mbarrier phase in order); larger ones 3 slots of 32 KB.
-  // (COPIES: B <= 64; the B > 64 instantiation keeps these compile-time constants)
+  // W2 slices per tile and rows per slice
+  const int sr = p.r < kDraftSliceRows ? p.r : kDraftSliceRows;
+  const int ns = nkk > 0 ? (p.r + kDraftSliceRows - 1) / kDraftSliceRows : 0;
+  // Small batches use 4 U slots of 16 KB (sub-tile j in slot j % 4, read by copy j % 2
+  // only, so each slot keeps one group of readers); larger ones 3 slots of 32 KB.
   const int nus = COPIES ? kNumUStagesSmall : kNumUStages;
   const uint32_t ubox = COPIES ? kUBoxBytes / 2 : kUBoxBytes;  // one 32-token box
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumW2Stages; ++s) {
+    for (int s = 0; s < kNumW2Slots; ++s) {
       mbar_init(&w_full[s], 1);
       mbar_init(&w_empty[s], 1);
     }
-    // a tile is read (and released) by the epilogue warps of one copy of the batch
-    const uint32_t readers =
-        COPIES ? static_cast<uint32_t>(kEpiWarps * rows_per_copy(p.B) / kRows) : kEpiWarps;
+    // a sub-tile's U slot is read (and released) by the epilogue warps of one copy
+    const uint32_t u_readers = COPIES ? static_cast<uint32_t>(kEpiWarps / 2) : kEpiWarps;
+    static_assert(kEpiWarps % 2 == 0, "the copies split the epilogue warps");
     for (int s = 0; s < nus; ++s) {
       mbar_init(&u_full[s], 1);
-      mbar_init(&u_empty[s], readers);
+      mbar_init(&u_empty[s], u_readers);
     }
     for (int s = 0; s < kNumAcc; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], readers);
+      mbar_init(&acc_empty[s], kEpiWarps);  // every epilogue warp reads every accumulator
     }
     mbar_init(a_full, 1);
     mbar_init(a_empty, 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     if (nkk > 0) tma_prefetch_desc(&args.tm_w2);
@@ -382,14 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0 && MODE == kModeResidual) {
-    // ------------------------------------------------ TMA producer, residual mode
+    // --------------------------------------------------- U producer, residual mode
     // The draw rows are read in place: each request's base-logit row and target row at
     // its own draw position (tile::gather4 over 2-D row maps of U [B K, V] and
-    // P [B (K + 1), V]), lane l fetching requests 4 l .. 4 l + 3 of every half tile into
-    // the same slot layout as the 3-D boxes; lane 0 waits for the slots and loads W2.
-    const uint64_t pol_w = l2_policy_evict_last();
+    // P [B (K + 1), V]), lane l fetching requests 4 l .. 4 l + 3 of every half
+    // sub-tile into the same slot layout as the 3-D boxes; lane 0 waits for the slots.
     const uint64_t pol_u = l2_policy_evict_first();
-    const uint32_t w_bytes = static_cast<uint32_t>(p.r) * kTileV * 2u;
     const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
     const bool mine = 4 * lane < p.box_rows;
     // the lane's four requests (past the batch: request 0 again, never read) and their draw
@@ -407,24 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       return target ? gb * (p.res_K + 1) + pos : gb * p.res_K + min(pos, p.res_K - 1);
     };
     bool ok = true;
-    int w_issued = 0, u_issued = 0;
+    int issued = 0;
     for (int k = 0; k < p.K && ok; ++k) {
-      for (int t = 0; t < nt; ++t) {
-        const int i = k * nt + t;
-        const int v0 = (t_begin + t) * kTileV;
-        if (lane == 0 && nkk > 0) {
-          const int s = i % kNumW2Stages;
-          ok = mbar_wait(&w_empty[s], ((i / kNumW2Stages) & 1) ^ 1, p.timeout_ns, abort_flag,
-                         kBackoffControlNs);
-          if (ok) {
-            mbar_arrive_expect_tx(&w_full[s], w_bytes);
-            tma_load_2d(sW + s * kW2StageBytes, &args.tm_w2, v0, 0, &w_full[s], pol_w);
-            w_issued = i + 1;
-          }
-        }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int j = 2 * i + h, su = j % nus;
+      for (int t = 0; t < nt && ok; ++t) {
+        for (int f = 0; f < 4; ++f) {  // sub-tile f / 2, half f % 2
+          const int j = 4 * (k * nt + t) + f, su = j % nus;
           if (lane == 0) {
             ok = mbar_wait(&u_empty[su], ((j / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
                            kBackoffControlNs);
@@ -432,101 +434,97 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
           if (!ok) break;
+          const int x = (t_begin + t) * kTileN + 32 * f;
           if (mine) {
             uint8_t* dst = sU + su * 2 * ubox + lane * 512;
-            tma_gather4_2d(dst, &args.tm_u, v0 + 32 * h, draw_row(0, false), draw_row(1, false),
+            tma_gather4_2d(dst, &args.tm_u, x, draw_row(0, false), draw_row(1, false),
                            draw_row(2, false), draw_row(3, false), &u_full[su], pol_u);
-            tma_gather4_2d(dst + ubox, &args.tm_p, v0 + 32 * h, draw_row(0, true),
-                           draw_row(1, true), draw_row(2, true), draw_row(3, true), &u_full[su],
-                           pol_u);
+            tma_gather4_2d(dst + ubox, &args.tm_p, x, draw_row(0, true), draw_row(1, true),
+                           draw_row(2, true), draw_row(3, true), &u_full[su], pol_u);
           }
-          u_issued = j + 1;
+          issued = j + 1;
         }
-        if (!ok) break;
       }
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
       record_error(p.status, kStatusTimeout);
-      // Drain: every copy the warp started completes on the full barriers of its fills.
-      for (int i = w_issued - 1; i >= 0 && i >= w_issued - kNumW2Stages; --i)
-        mbar_wait(&w_full[i % kNumW2Stages], (i / kNumW2Stages) & 1, p.timeout_ns, nullptr);
-      for (int i = u_issued - 1; i >= 0 && i >= u_issued - nus; --i)
-        mbar_wait(&u_full[i % nus], (i / nus) & 1, p.timeout_ns, nullptr);
+      for (int j = issued - 1; j >= 0 && j >= issued - nus; --j)
+        mbar_wait(&u_full[j % nus], (j / nus) & 1, p.timeout_ns, nullptr);
     }
   } else if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ U producer
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_last();
       const uint64_t pol_u = l2_policy_evict_first();
-      const uint32_t w_bytes = static_cast<uint32_t>(p.r) * kTileV * 2u;
       const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
+      // fills per tile: two sub-tiles (U boxes of 32 tokens, two per fill), or four half
+      // sub-tiles of U and target (label mode)
+      constexpr int kFills = kHalf ? 4 : 2;
       bool ok = true;
-      int w_issued = 0, u_issued = 0;  // u_issued: ring slot fills
+      int issued = 0;
       for (int k = 0; k < p.K && ok; ++k) {
-        for (int t = 0; t < nt; ++t) {
-          const int i = k * nt + t;
-          const int v0 = (t_begin + t) * kTileV;
-          if (nkk > 0) {
-            const int s = i % kNumW2Stages;
-            if (!mbar_wait(&w_empty[s], ((i / kNumW2Stages) & 1) ^ 1, p.timeout_ns, abort_flag,
+        for (int t = 0; t < nt && ok; ++t) {
+          for (int f = 0; f < kFills; ++f) {
+            const int j = kFills * (k * nt + t) + f, su = j % nus;
+            if (!mbar_wait(&u_empty[su], ((j / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
                            kBackoffControlNs)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&w_full[s], w_bytes);
-            tma_load_2d(sW + s * kW2StageBytes, &args.tm_w2, v0, 0, &w_full[s], pol_w);
-            w_issued = i + 1;
-          }
-          if (kHalf) {
-            // two fills per tile: U and target tokens [v0 + 32 h, v0 + 32 h + 32)
-            for (int h = 0; h < 2 && ok; ++h) {
-              const int j = 2 * i + h, su = j % nus;
-              if (!mbar_wait(&u_empty[su], ((j / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
-                             kBackoffControlNs)) {
-                ok = false;
-                break;
-              }
-              mbar_arrive_expect_tx(&u_full[su], u_bytes);
-              tma_load_3d(sU + su * 2 * ubox, &args.tm_u, v0 + 32 * h, k, 0, &u_full[su], pol_u);
-              tma_load_3d(sU + su * 2 * ubox + ubox, &args.tm_p, v0 + 32 * h, k, 0, &u_full[su],
-                          pol_u);
-              u_issued = j + 1;
+            mbar_arrive_expect_tx(&u_full[su], u_bytes);
+            uint8_t* dst = sU + su * 2 * ubox;
+            if (kHalf) {  // U and target tokens [x, x + 32)
+              const int x = (t_begin + t) * kTileN + 32 * f;
+              tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
+              tma_load_3d(dst + ubox, &args.tm_p, x, k, 0, &u_full[su], pol_u);
+            } else {  // U tokens [x, x + 64)
+              const int x = (t_begin + t) * kTileN + kSubV * f;
+              tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
+              tma_load_3d(dst + ubox, &args.tm_u, x + 32, k, 0, &u_full[su], pol_u);
             }
-            if (!ok) break;
-            continue;
+            issued = j + 1;
           }
-          const int su = i % nus;
-          if (!mbar_wait(&u_empty[su], ((i / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
-                         kBackoffControlNs)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&u_full[su], u_bytes);
-          tma_load_3d(sU + su * 2 * ubox, &args.tm_u, v0, k, 0, &u_full[su], pol_u);
-          tma_load_3d(sU + su * 2 * ubox + ubox, &args.tm_u, v0 + 32, k, 0, &u_full[su],
-                      pol_u);
-          u_issued = i + 1;
         }
       }
       if (!ok) {
         *abort_flag = 1;
         record_error(p.status, kStatusTimeout);
-        // Drain: every copy this thread started must land before the CTA exits.
-        // The last issue of each ring slot is the one in [issued - stages, issued).
-        for (int i = w_issued - 1; i >= 0 && i >= w_issued - kNumW2Stages; --i)
-          mbar_wait(&w_full[i % kNumW2Stages], (i / kNumW2Stages) & 1, p.timeout_ns, nullptr);
-        for (int i = u_issued - 1; i >= 0 && i >= u_issued - nus; --i)
-          mbar_wait(&u_full[i % nus], (i / nus) & 1, p.timeout_ns, nullptr);
+        for (int j = issued - 1; j >= 0 && j >= issued - nus; --j)
+          mbar_wait(&u_full[j % nus], (j / nus) & 1, p.timeout_ns, nullptr);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------- MMA issuer and W2 producer (one lane)
+    // W2 slices are loaded kNumW2Slots - 1 ahead of the MMAs: slice j + 2 goes into the
+    // slot of slice j - 1 as soon as slice j's MMAs are issued (they queue behind slice
+    // j - 1's in the tensor pipe, so waiting for that slot never starves the pipe).
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kRows, kTileV, /*a_mn=*/false, /*b_mn=*/true);
-      const uint32_t a0 = smem_addr(sA);
+      const uint32_t idesc = idesc_bf16_f32(kRows, kTileN, /*a_mn=*/false, /*b_mn=*/true);
+      // B operand: a W2 slice as TMA wrote it, MN-major with 128-byte swizzle -- two
+      // 64-token column blocks sr * 128 bytes apart, 8-row groups 1024 bytes apart
+      const uint32_t lbo = static_cast<uint32_t>(sr) * 128u;
+      const uint64_t pol_w = l2_policy_evict_last();
+      const uint32_t w_bytes = 2u * kDraftBoxV * static_cast<uint32_t>(sr) * 2u;
+      const int total = p.K * nt * ns;  // W2 slices of the launch
+      int loaded = 0;                   // slices whose loads were issued
       bool ok = true;
-      int last_i = -1;
+      bool issued_any = false;
+      // load slice j (tile (j / ns) % nt of this CTA, rows [128 (j % ns), ...)) into its slot
+      auto load_slice = [&](int j) -> bool {
+        const int slot = j % kNumW2Slots;
+        if (!mbar_wait(&w_empty[slot], ((j / kNumW2Slots) & 1) ^ 1, p.timeout_ns, abort_flag,
+                       kBackoffControlNs))
+          return false;
+        const int s = j % ns, t = (j / ns) % nt;
+        const int v0 = (t_begin + t) * kTileN;
+        uint8_t* dst = sW + slot * kW2SlotBytes;
+        mbar_arrive_expect_tx(&w_full[slot], w_bytes);
+        tma_load_2d(dst, &args.tm_w2, v0, s * kDraftSliceRows, &w_full[slot], pol_w);
+        tma_load_2d(dst + sr * 128, &args.tm_w2, v0 + kDraftBoxV, s * kDraftSliceRows,
+                    &w_full[slot], pol_w);
+        return true;
+      };
+      while (ok && loaded < total && loaded < kNumW2Slots) ok = load_slice(loaded++);
       for (int k = 0; k < p.K && ok; ++k) {
         if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag, 32u)) {
           ok = false;
@@ -535,33 +533,39 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         tc_fence_after();
         for (int t = 0; t < nt; ++t) {
           const int i = k * nt + t;
-          const int s = i % kNumW2Stages, buf = i % kNumAcc;
-          if (nkk > 0 &&
-              !mbar_wait(&w_full[s], (i / kNumW2Stages) & 1, p.timeout_ns, abort_flag,
-                        kBackoffControlNs)) {
-            ok = false;
-            break;
-          }
+          const int buf = i % kNumAcc;
           if (!mbar_wait(&acc_empty[buf], ((i / kNumAcc) & 1) ^ 1, p.timeout_ns, abort_flag,
                          kBackoffControlNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (nkk > 0) {
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileV);
-            const uint32_t b0 = smem_addr(sW + s * kW2StageBytes);
-            for (int kk = 0; kk < nkk; ++kk) {
-              const uint64_t bd = smem_desc(b0 + kk * 2048, 1024, 1024);
+          if (nkk == 0) {
+            mbar_arrive(&acc_full[buf]);  // rank 0: the bias is zero, nothing to multiply
+            continue;
+          }
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
+          for (int s = 0; s < ns && ok; ++s) {
+            const int j = i * ns + s, slot = j % kNumW2Slots;
+            if (!mbar_wait(&w_full[slot], (j / kNumW2Slots) & 1, p.timeout_ns, abort_flag,
+                           kBackoffControlNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t b0 = smem_addr(sW + slot * kW2SlotBytes);
+            const int kk_end = nkk < (s + 1) * 8 ? nkk : (s + 1) * 8;
+            for (int kk = s * 8; kk < kk_end; ++kk) {
+              const uint64_t bd = smem_desc(b0 + (kk - s * 8) * 2048, lbo, 1024);
               umma_bf16_ts(d_tmem, tmem_base + kTmemA + static_cast<uint32_t>(kk * 8), bd, idesc,
                            kk > 0 ? 1u : 0u);
             }
-            umma_commit(&w_empty[s]);
-            umma_commit(&acc_full[buf]);
-            last_i = i;
-          } else {
-            mbar_arrive(&acc_full[buf]);  // rank 0: the bias is zero, nothing to multiply
+            issued_any = true;
+            umma_commit(&w_empty[slot]);
+            if (loaded < total && loaded <= j + kNumW2Slots - 1) ok = load_slice(loaded++);
           }
+          if (!ok) break;
+          umma_commit(&acc_full[buf]);
         }
         if (!ok) break;
         if (nkk > 0) {
@@ -573,93 +577,82 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       if (!ok) {
         *abort_flag = 1;
         record_error(p.status, kStatusTimeout);
+        // Drain: every copy and every MMA this lane issued must finish before the CTA
+        // exits and TMEM is released (on the normal path the epilogue waited for all)
+        for (int j = loaded - 1; j >= 0 && j >= loaded - kNumW2Slots; --j)
+          mbar_wait(&w_full[j % kNumW2Slots], (j / kNumW2Slots) & 1, p.timeout_ns, nullptr);
+        if (issued_any) {
+          umma_commit(mma_drain);
+          mbar_wait(mma_drain, 0, p.timeout_ns, nullptr);
+        }
       }
-      // Drain: the last MMA batch must finish before TMEM is released.
-      if (last_i >= 0)
-        mbar_wait(&acc_full[last_i % kNumAcc], (last_i / kNumAcc) & 1, p.timeout_ns, nullptr);
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
-    const int e = warp - 2;          // 0 .. 15
+    const int e = warp - kCtlWarps;  // 0 .. 7
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
-    const int g = e >> 2;            // 16-token column group of the 64-token tile
+    const int g = e >> 2;            // 32-token half of a 64-token sub-tile
     const int rpc = COPIES ? rows_per_copy(p.B) : kRows;
     const int ncopy = COPIES ? kRows / rpc : 1;  // copies of the batch in the MMA rows
-    const int b = (q * 32 + lane) & (rpc - 1);  // request of this thread's TMEM lane
-    const int copy = (q * 32) / rpc;  // its copy: it reads tiles i (global index) with
-                                      // i % ncopy == copy
-    const int etid = threadIdx.x - 64;
+    const int b = (q * 32 + lane) & (rpc - 1);   // request of this thread's TMEM lane
+    const int copy = (q * 32) / rpc;  // its copy: it reads sub-tile `copy` of every tile
+    const int sub_lo = COPIES ? copy : 0;
+    constexpr int nsub = COPIES ? 1 : 2;
+    const int etid = threadIdx.x - kCtlWarps * 32;
     const bool row_ok = b < p.B;
     const uint32_t b_global = static_cast<uint32_t>(p.b_global0 + b);
     const float scale2 = p.inv_t * kLog2e;
-    const float inv_scale2 = 1.0f / scale2;  // logit of the winner from its scaled value
-    float* merge = reinterpret_cast<float*>(sA);  // reused after a step's MMAs completed
-    // this thread's four 16-byte pieces of its U row within a stage (128B swizzle)
-    uint32_t u_off[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      u_off[c] = (g >> 1) * ubox + b * 128 + ((((g & 1) * 4 + c) ^ (b & 7)) << 4);
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // this thread's row within a 32-token box of a ring slot (128B swizzle: 16-byte unit u
+    // of row b at unit u ^ (b & 7))
+    const uint32_t row_off = static_cast<uint32_t>(b) * 128u;
+    const uint32_t swz = static_cast<uint32_t>(b & 7);
     bool fail = false;
     bool aborted = false;
-    int u_stage = 0;        // U ring slot of the next tile
-    uint32_t u_phase = 0;   // its mbarrier phase parity
 
+    // this thread's piece of the MMA operand: K chunks 2g and 2g + 1 of its row
+    uint32_t wv0[32], wv1[32];
     unsigned long long spec_key = 0ull;  // winner key this thread's row was gathered for
+    auto store_operand = [&]() {
+      tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64), wv0);
+      tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32), wv1);
+    };
+    auto gather_operand = [&](int kpos, bool live, int32_t tok) {
+      load_embedding(p, kpos, b, live, 2 * g, tok, wv0);
+      load_embedding(p, kpos, b, live, 2 * g + 1, tok, wv1);
+    };
     for (int k = 0; k < p.K; ++k) {
-      // ---- the step's embeddings: position 0 is gathered here; later positions were
-      // gathered speculatively before the previous grid barrier and are re-checked now
+      // ---- the step's operand: position 0 is gathered here; later positions were written
+      // speculatively before the previous grid barrier and are re-checked now
       if (etid == 0) trace_stamp(p, cta, k, 0);
-      {
-        const int grow = (etid >> 2) & (rpc - 1);  // request of this thread's gather row
+      if (!fail) {
         if (k == 0) {
           int32_t tok = 0;
-          if (grow < p.B) {
-            tok = kTF ? __ldg(p.prev + static_cast<size_t>(grow) * p.K) : __ldg(p.anchors + grow);
+          if (row_ok) {
+            tok = kTF ? __ldg(p.prev + static_cast<size_t>(b) * p.K) : __ldg(p.anchors + b);
             if (tok < 0 || tok >= p.V) {
               record_error(p.status, kStatusDeviceOob);
               tok = 0;
             }
           }
-          if (!fail) gather_embeddings(sA, p, 0, etid, tok);
-        } else if (!kTF && grow < p.B) {
-          cp_async_wait_all();  // the speculative copy must land before any rewrite
-          const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + grow);
+          gather_operand(0, row_ok, tok);
+        } else if (!kTF && row_ok) {
+          const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + b);
           if (key != spec_key) {  // the winner changed after the speculative gather
             int32_t tok = key_token(key);
             if (key_epoch(key) != p.epoch || tok < 0 || tok >= p.V) {
               record_error(p.status, kStatusDeviceOob);
               tok = 0;
             }
-            if (!fail) gather_embeddings(sA, p, k, etid, tok);
+            gather_operand(k, true, tok);
           }
         }
-        if (etid < kRows) s_bound[etid] = 0ull;
-        cp_async_wait_all();
+        store_operand();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      if (etid < kRows) s_bound[etid] = 0ull;
       named_bar_sync(kEpiBarrier, kEpiThreads);
-      {
-        // copy the operand into TMEM: each warp its lane quadrant's rows m = q*32 + lane,
-        // K chunk e / 4 (64 bf16 = 32 columns); the previous position's MMAs finished
-        // with the TMEM copy before the speculative gather (a_empty)
-        const int m = q * 32 + lane, cc = e >> 2;
-        const uint8_t* src = sA + cc * 16384 + (m >> 3) * 1024 + (m & 7) * 128;
-        uint32_t wv[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = *reinterpret_cast<const uint4*>(src + ((u ^ (m & 7)) << 4));
-          wv[4 * u + 0] = x.x;
-          wv[4 * u + 1] = x.y;
-          wv[4 * u + 2] = x.z;
-          wv[4 * u + 3] = x.w;
-        }
-        tmem_st_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kTmemA +
-                        static_cast<uint32_t>(cc * 32),
-                    wv);
-        tmem_wait_st();
-        tc_fence_before();
-        named_bar_sync(kEpiBarrier, kEpiThreads);
-      }
       if (etid == 0) {
         mbar_arrive(a_full);
         trace_stamp(p, cta, k, 1);
@@ -681,210 +674,22 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         res_pos = rr.pos;
         res_excl = rr.excl;
       }
-      float yb = -INFINITY, lb = 0.f;  // best score (G, or y when greedy) and its logit
-      int vb = 0x7FFFFFFF;
-      unsigned long long bkey = 0ull;  // key of (yb, vb)
-      unsigned long long gkey = 0ull;  // global key of this request and step, as last read
-      uint32_t nz[4] = {0u, 0u, 0u, 0u};  // Philox words of this thread's current tile pair
-      unsigned long long kpre = 0ull;  // global key, read one tile ahead of its use
-      int tt = -1;                      // tiles of this step this thread has taken
-      int nz_pair = -1;                 // tile pair whose Philox words nz holds
+      // this thread's best block of the position so far (score, first token, stage-2 word);
+      // its values are in the shared best-block store
+      float best = -INFINITY;
+      int best_v = 0;
+      uint32_t best_w = 0u;
+      float4* my_best = s_best + etid;
+      // Philox words of this thread's two blocks (2g, 2g + 1 within a sub-tile) of a tile:
+      // words 0, 1 serve sub-tile 0, words 2, 3 sub-tile 1; lE = log2(E) of the four blocks
+      uint32_t nza[4] = {0u, 0u, 0u, 0u}, nzb[4] = {0u, 0u, 0u, 0u};
+      float lE[4] = {0.f, 0.f, 0.f, 0.f};
+      bool first = true;
       for (int t = 0; t < nt && !fail; ++t) {
         const int i = k * nt + t;
-        const int buf = i & (kNumAcc - 1);
-        const int su = u_stage;
-        const uint32_t uph = u_phase;
-        if (++u_stage == nus) {
-          u_stage = 0;
-          u_phase ^= 1u;
-        }
-        if (COPIES && (i & (ncopy - 1)) != copy) continue;  // another copy's tile
-        ++tt;
-        if (kRace && row_ok) {
-          // every other tile, refresh the bound with the key read a tile earlier, so
-          // the load's latency is covered by a whole tile's work
-          if (tt > 0 && (tt & (kBoundRefresh - 1)) == 0 && key_epoch(kpre) == p.epoch &&
-              kpre > gkey)
-            gkey = kpre;
-          if (((tt + 1) & (kBoundRefresh - 1)) == 0) kpre = __ldcg(p.keys + k * kRows + b);
-        }
-        if (MODE == kModeResidual) {
-          // the verification draw: this thread's 16 tokens [16 g, 16 g + 16) of tile i
-          // (one block) come from fill 2 i + g / 2; every warp waits for and releases
-          // both fills, so each slot keeps one group of readers taking its fills in order
-          bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
-          ok = __all_sync(0xFFFFFFFFu, ok);
-          if (!ok) {
-            fail = true;
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          uint32_t acc[16];
-          if (nkk > 0) {
-            tmem_ld_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                            static_cast<uint32_t>(buf * kTileV + g * 16),
-                        acc);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0u;
-          }
-          float uval[16], pt[16];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = 2 * i + h, sh = j % nus;
-            bool okh = mbar_wait(&u_full[sh], static_cast<uint32_t>(j / nus) & 1u, p.timeout_ns,
-                                 abort_flag);
-            okh = __all_sync(0xFFFFFFFFu, okh);
-            if (!okh) {
-              fail = true;
-              *abort_flag = 1;
-              break;
-            }
-            uint32_t dep = 0u;
-            if (h == (g >> 1)) {
-              const uint8_t* row = sU + sh * 2 * ubox + b * 128;
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint32_t off = static_cast<uint32_t>((((g & 1) * 4 + c) ^ (b & 7)) << 4);
-                const float4 x = *reinterpret_cast<const float4*>(row + off);
-                const float4 z = *reinterpret_cast<const float4*>(row + ubox + off);
-                uval[4 * c + 0] = x.x;
-                uval[4 * c + 1] = x.y;
-                uval[4 * c + 2] = x.z;
-                uval[4 * c + 3] = x.w;
-                pt[4 * c + 0] = z.x;
-                pt[4 * c + 1] = z.y;
-                pt[4 * c + 2] = z.z;
-                pt[4 * c + 3] = z.w;
-                dep ^= __float_as_uint(x.x) ^ __float_as_uint(z.x);
-              }
-            }
-            arrive_after_reads(&u_empty[sh], dep, s_sink, lane);
-          }
-          if (fail) break;
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
-          if (!row_ok) continue;
-          const int tile = t_begin + t;
-          const int vbase = tile * kTileV + g * 16;
-          // weights max(0, p - q) (p alone for a bonus draw), relative to 2^0
-          float w[16];
-          float bsum = 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float lj = uval[j] + __uint_as_float(acc[j]);
-            const float pj = ex2_approx(fmaf(pt[j], p.target_scale2, offp2));
-            const float qj = ex2_approx(fmaf(lj, scale2, offq2));  // 0 when offq2 = -inf
-            float wj = fmaxf(0.f, pj - qj);
-            if (vbase + j >= p.V || vbase + j == res_excl) wj = 0.f;
-            w[j] = wj;
-            bsum += wj;
-          }
-          if ((tile >> 1) != nz_pair) {
-            nz_pair = tile >> 1;
-            philox4x32_10_rk(static_cast<uint32_t>(tile >> 1), static_cast<uint32_t>(res_pos),
-                             b_global, 9u + static_cast<uint32_t>(g), p.round_key0, p.round_key1,
-                             nz);
-          }
-          race_block(w, w, 0.f, bsum, (tile & 1) ? nz[2] : nz[0], (tile & 1) ? nz[3] : nz[1],
-                     vbase, p.epoch, inv_scale2, &s_bound[b], gkey, bkey, yb, vb, lb);
-          if ((tt & 1) == 1 && g == 0) {
-            const unsigned long long mine = s_bound[b];
-            if (mine > gkey) {
-              atomicMax(p.keys + k * kRows + b, mine);
-              gkey = mine;
-            }
-          }
-          continue;
-        }
-        if (kHalf) {
-          // label: tile i is ring fills 2 i (tokens 0-31) and 2 i + 1 (32-63), each
-          // holding U and the target; this thread takes tokens 8 g .. 8 g + 7 of both
-          bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
-          ok = __all_sync(0xFFFFFFFFu, ok);
-          if (!ok) {
-            fail = true;
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          uint32_t acc[16];
-          if (nkk > 0) {
-            const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>(buf * kTileV + g * 8);
-            tmem_ld_x8(ta, acc);
-            tmem_ld_x8(ta + 32, acc + 8);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0u;
-          }
-          float uval[16], pt[16];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = 2 * i + h, sh = j % nus;
-            bool okh = mbar_wait(&u_full[sh], static_cast<uint32_t>(j / nus) & 1u, p.timeout_ns,
-                                 abort_flag);
-            okh = __all_sync(0xFFFFFFFFu, okh);
-            if (!okh) {
-              fail = true;
-              *abort_flag = 1;
-              break;
-            }
-            const uint8_t* row = sU + sh * 2 * ubox + b * 128;
-            uint32_t dep = 0u;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const uint32_t off = static_cast<uint32_t>(((2 * g + c) ^ (b & 7)) << 4);
-              const float4 x = *reinterpret_cast<const float4*>(row + off);
-              const float4 y = *reinterpret_cast<const float4*>(row + ubox + off);
-              uval[8 * h + 4 * c + 0] = x.x;
-              uval[8 * h + 4 * c + 1] = x.y;
-              uval[8 * h + 4 * c + 2] = x.z;
-              uval[8 * h + 4 * c + 3] = x.w;
-              pt[8 * h + 4 * c + 0] = y.x;
-              pt[8 * h + 4 * c + 1] = y.y;
-              pt[8 * h + 4 * c + 2] = y.z;
-              pt[8 * h + 4 * c + 3] = y.w;
-              dep ^= __float_as_uint(x.x) ^ __float_as_uint(y.x);
-            }
-            arrive_after_reads(&u_empty[sh], dep, s_sink, lane);
-          }
-          if (fail) break;
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
-          if (!row_ok) continue;
-          // past V the boxes read zeros; the target side is masked to p = 0
-          const int vt = (t_begin + t) * kTileV;
-          if (vt + kTileV > p.V) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (vt + (j >> 3) * 32 + g * 8 + (j & 7) >= p.V) pt[j] = -INFINITY;
-          }
-          // sum of min(q, p) over the thread's columns
-          const float2 sq = make_float2(scale2, scale2), oq = make_float2(offq2, offq2);
-          const float2 sp = make_float2(p.target_scale2, p.target_scale2);
-          const float2 op = make_float2(offp2, offp2);
-          float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
-                                         make_float2(__uint_as_float(acc[j]),
-                                                     __uint_as_float(acc[j + 1])));
-            const float2 aq = __ffma2_rn(lj, sq, oq);
-            const float2 ap = __ffma2_rn(make_float2(pt[j], pt[j + 1]), sp, op);
-            acc2 = __fadd2_rn(acc2, make_float2(ex2_approx(fminf(aq.x, ap.x)),
-                                                ex2_approx(fminf(aq.y, ap.y))));
-          }
-          sum += acc2.x + acc2.y;
-          continue;
-        }
+        const int buf = i % kNumAcc;
+        const int tile = t_begin + t;
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
-        ok = ok && mbar_wait(&u_full[su], uph, p.timeout_ns, abort_flag);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
           fail = true;
@@ -892,163 +697,285 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           break;
         }
         tc_fence_after();
-        if (tt == 0 && etid == 0) trace_stamp(p, cta, k, 2);
-        uint32_t acc[16];
-        if (nkk > 0) {
-          tmem_ld_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(buf * kTileV + g * 16),
-                      acc);
-          tmem_wait_ld();
-        } else {
+        if (first && etid == 0) trace_stamp(p, cta, k, 2);
+        first = false;
+        if (kRace && row_ok) {
+          const uint32_t c1 = static_cast<uint32_t>(MODE == kModeResidual ? res_pos : k);
+          const uint32_t tag = (MODE == kModeResidual ? 9u : 1u) + 2u * static_cast<uint32_t>(g);
+          philox4x32_10_rk2(static_cast<uint32_t>(tile), c1, b_global, tag, tag + 1u,
+                            p.round_key0, p.round_key1, nza, nzb);
+          // stage 1's exponentials E = -ln u1 of the thread's blocks, as log2 E
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = 0u;
-        }
-        float uval[16];
-        {
-          const uint8_t* ubase = sU + su * 2 * ubox;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float4 x = *reinterpret_cast<const float4*>(ubase + u_off[c]);
-            uval[4 * c + 0] = x.x;
-            uval[4 * c + 1] = x.y;
-            uval[4 * c + 2] = x.z;
-            uval[4 * c + 3] = x.w;
+          for (int s = 0; s < 2; ++s) {
+            lE[2 * s] = lg2_approx(neg_log_uniform_fast(nza[2 * s]));
+            lE[2 * s + 1] = lg2_approx(neg_log_uniform_fast(nzb[2 * s]));
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);  // tcgen05.wait::ld returned the values
-        arrive_after_reads(&u_empty[su],
-                           __float_as_uint(uval[0]) ^ __float_as_uint(uval[4]) ^
-                               __float_as_uint(uval[8]) ^ __float_as_uint(uval[12]),
-                           s_sink, lane);
-        if (!row_ok) continue;
-
-        const int vbase = (t_begin + t) * kTileV + g * 16;
-        const bool full_chunk = vbase + 16 <= p.V;  // warp-uniform
-        float y[16];
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
-                                       make_float2(__uint_as_float(acc[j]),
-                                                   __uint_as_float(acc[j + 1])));
-          if (MODE == kModeTeacherForced) {
-            uval[j] = lj.x;  // keep the logits for the store below
-            uval[j + 1] = lj.y;
-          }
-          const float2 yj = __fmul2_rn(lj, make_float2(scale2, scale2));
-          y[j] = yj.x;
-          y[j + 1] = yj.y;
-        }
-        if (!full_chunk) {
+        for (int s = 0; s < nsub; ++s) {
+          if (fail) break;
+          const int sub = sub_lo + s;
+          const int jsub = 2 * i + sub;                   // sub-tile index in ring order
+          const int vbase = tile * kTileN + sub * kSubV + 32 * g;  // this thread's first token
+          // this sub-tile's 32 accumulator columns (the half-tile modes read them in two
+          // 16-column pieces after the ring slots); after the last sub-tile of the tile the
+          // buffer goes back
+          const uint32_t acc_col =
+              lane_base + static_cast<uint32_t>(buf * kTileN + sub * kSubV + 32 * g);
+          uint32_t acc[32];
+          if (!kHalf) {
+            if (nkk == 0) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (vbase + j >= p.V) y[j] = -INFINITY;
-        }
-        if (MODE == kModeTeacherForced) {
-          float* dst = p.logits + (static_cast<size_t>(b) * p.K + k) * p.V + vbase;
-          if (full_chunk) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              reinterpret_cast<float4*>(dst)[c] =
-                  make_float4(uval[4 * c], uval[4 * c + 1], uval[4 * c + 2], uval[4 * c + 3]);
-          } else {
-            for (int j = 0; j < 16 && vbase + j < p.V; ++j) dst[j] = uval[j];
-          }
-        }
-        // chunk maximum (tree)
-        float mx[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mx[j] = fmaxf(y[j], y[j + 8]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], mx[j + 4]);
-        const float cmax = fmaxf(fmaxf(mx[0], mx[2]), fmaxf(mx[1], mx[3]));
-        if (cmax == -INFINITY) continue;  // nothing in this chunk can be drawn
-        if (cmax > m2) {
-          sum *= ex2_approx(m2 - cmax);
-          m2 = cmax;
-        }
-        float w[16];
-        float bsum;  // the block's mass relative to 2^m2
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float2 dj = __fadd2_rn(make_float2(y[j], y[j + 1]), make_float2(-m2, -m2));
-          w[j] = ex2_approx(dj.x);
-          w[j + 1] = ex2_approx(dj.y);
-        }
-        {
-          float2 s0 = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
-          float2 s1 = __fadd2_rn(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
-          float2 s2 = __fadd2_rn(make_float2(w[8], w[9]), make_float2(w[10], w[11]));
-          float2 s3 = __fadd2_rn(make_float2(w[12], w[13]), make_float2(w[14], w[15]));
-          s0 = __fadd2_rn(__fadd2_rn(s0, s1), __fadd2_rn(s2, s3));
-          bsum = s0.x + s0.y;
-          sum += bsum;
-        }
-        if (MODE == kModeSample) {
-          const int tile = t_begin + t;
-          if ((tile >> 1) != nz_pair) {
-            nz_pair = tile >> 1;
-            philox4x32_10_rk(static_cast<uint32_t>(tile >> 1), static_cast<uint32_t>(k), b_global,
-                             1u + static_cast<uint32_t>(g), p.round_key0, p.round_key1, nz);
-          }
-          race_block(w, y, m2, bsum, (tile & 1) ? nz[2] : nz[0], (tile & 1) ? nz[3] : nz[1], vbase,
-                     p.epoch, inv_scale2, &s_bound[b], gkey, bkey, yb, vb, lb);
-          if ((tt & 1) == 1 && g == 0) {
-            // share this CTA's best with the other CTAs (rate-limited)
-            const unsigned long long mine = s_bound[b];
-            if (mine > gkey) {
-              atomicMax(p.keys + k * kRows + b, mine);
-              gkey = mine;
+              for (int j = 0; j < 32; ++j) acc[j] = 0u;
+            } else {
+              tmem_ld_x32(acc_col, acc);
+              tmem_wait_ld();
+            }
+            if (s == nsub - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[buf]);  // wait::ld returned the values
             }
           }
-        } else if (MODE == kModeGreedy) {
-          if (cmax > yb) {
-            int jb = 15;
+          float uval[32], pt[32];
+          if (kHalf) {
+            // half sub-tiles: fill 2 jsub + h holds U and the target for tokens
+            // [32 h, 32 h + 32); this thread reads half g, every warp takes and releases
+            // both, so each slot keeps one group of readers taking its fills in order
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int j = 2 * jsub + h, sh = j % nus;
+              bool okh = mbar_wait(&u_full[sh], static_cast<uint32_t>(j / nus) & 1u,
+                                   p.timeout_ns, abort_flag);
+              okh = __all_sync(0xFFFFFFFFu, okh);
+              if (!okh) {
+                fail = true;
+                *abort_flag = 1;
+                break;
+              }
+              uint32_t dep = 0u;
+              if (h == g) {
+                const uint8_t* row = sU + sh * 2 * ubox + row_off;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const uint32_t off = static_cast<uint32_t>(u ^ swz) << 4;
+                  const float4 x = *reinterpret_cast<const float4*>(row + off);
+                  const float4 z = *reinterpret_cast<const float4*>(row + ubox + off);
+                  uval[4 * u + 0] = x.x;
+                  uval[4 * u + 1] = x.y;
+                  uval[4 * u + 2] = x.z;
+                  uval[4 * u + 3] = x.w;
+                  pt[4 * u + 0] = z.x;
+                  pt[4 * u + 1] = z.y;
+                  pt[4 * u + 2] = z.z;
+                  pt[4 * u + 3] = z.w;
+                  if (u == 0 || u == 7) dep ^= __float_as_uint(x.x) ^ __float_as_uint(z.w);
+                }
+              }
+              arrive_after_reads(&u_empty[sh], dep, s_sink, lane);
+            }
+            if (fail) break;
+          } else {
+            const int su = jsub % nus;
+            bool oku = mbar_wait(&u_full[su], static_cast<uint32_t>(jsub / nus) & 1u,
+                                 p.timeout_ns, abort_flag);
+            oku = __all_sync(0xFFFFFFFFu, oku);
+            if (!oku) {
+              fail = true;
+              *abort_flag = 1;
+              break;
+            }
+            const uint8_t* row = sU + su * 2 * ubox + g * ubox + row_off;
+            uint32_t dep = 0u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 x =
+                  *reinterpret_cast<const float4*>(row + (static_cast<uint32_t>(u ^ swz) << 4));
+              uval[4 * u + 0] = x.x;
+              uval[4 * u + 1] = x.y;
+              uval[4 * u + 2] = x.z;
+              uval[4 * u + 3] = x.w;
+              if (u == 0 || u == 7) dep ^= __float_as_uint(x.x) ^ __float_as_uint(x.w);
+            }
+            arrive_after_reads(&u_empty[su], dep, s_sink, lane);
+          }
+          const bool full_chunk = vbase + 32 <= p.V;  // warp-uniform
+          if (kHalf) {
+            // two 16-token pieces (the residual draw's two blocks); every lane reads the
+            // accumulator (a warp-wide load), a lane with no request only wastes its work
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t a16[16];
+              if (nkk == 0) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a16[j] = 0u;
+              } else {
+                tmem_ld_x16(acc_col + static_cast<uint32_t>(16 * hh), a16);
+                tmem_wait_ld();
+              }
+              if (hh == 1 && s == nsub - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+              }
+              const int v0 = vbase + 16 * hh;
+              if (MODE == kModeLabel) {
+                // sum of min(q, p) over the 16 tokens (past V the target is masked)
+                const float2 sq = make_float2(scale2, scale2), oq = make_float2(offq2, offq2);
+                const float2 sp = make_float2(p.target_scale2, p.target_scale2);
+                const float2 op = make_float2(offp2, offp2);
+                float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                  const float2 lj = __fadd2_rn(
+                      make_float2(uval[16 * hh + j], uval[16 * hh + j + 1]),
+                      make_float2(__uint_as_float(a16[j]), __uint_as_float(a16[j + 1])));
+                  const float2 aq = __ffma2_rn(lj, sq, oq);
+                  float2 pv = make_float2(pt[16 * hh + j], pt[16 * hh + j + 1]);
+                  if (!full_chunk) {
+                    if (v0 + j >= p.V) pv.x = -INFINITY;
+                    if (v0 + j + 1 >= p.V) pv.y = -INFINITY;
+                  }
+                  const float2 ap = __ffma2_rn(pv, sp, op);
+                  acc2 = __fadd2_rn(acc2, make_float2(ex2_approx(fminf(aq.x, ap.x)),
+                                                      ex2_approx(fminf(aq.y, ap.y))));
+                }
+                sum += acc2.x + acc2.y;
+              } else {
+                // the verification draw: weights max(0, p - q) (p alone for a bonus draw),
+                // relative to 2^0; stage 1 G = log2(block mass) - log2(E)
+                float w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const float lj = uval[16 * hh + j] + __uint_as_float(a16[j]);
+                  const float pj = ex2_approx(fmaf(pt[16 * hh + j], p.target_scale2, offp2));
+                  const float qj = ex2_approx(fmaf(lj, scale2, offq2));  // 0 if offq2 = -inf
+                  float wj = fmaxf(0.f, pj - qj);
+                  if (v0 + j >= p.V || v0 + j == res_excl) wj = 0.f;
+                  w[j] = wj;
+                }
+                const float bs = sum16(w);
+                const float G = bs > 0.f ? lg2_approx(bs) - lE[2 * sub + hh] : -INFINITY;
+                const uint32_t w2 = hh ? (sub ? nzb[3] : nzb[1]) : (sub ? nza[3] : nza[1]);
+                keep_best(G, v0, w2, w, my_best, kEpiThreads, best, best_v, best_w);
+              }
+            }
+            continue;
+          }
+          if (!row_ok) continue;
+          // sample, greedy, teacher-forced: calibrated logits l = U + bias
+          float l[32];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 lj = __fadd2_rn(make_float2(uval[j], uval[j + 1]),
+                                         make_float2(__uint_as_float(acc[j]),
+                                                     __uint_as_float(acc[j + 1])));
+            l[j] = lj.x;
+            l[j + 1] = lj.y;
+          }
+          if (MODE == kModeTeacherForced) {
+            float* dst = p.logits + (static_cast<size_t>(b) * p.K + k) * p.V + vbase;
+            if (full_chunk) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                reinterpret_cast<float4*>(dst)[c] =
+                    make_float4(l[4 * c], l[4 * c + 1], l[4 * c + 2], l[4 * c + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (vbase + j < p.V) dst[j] = l[j];
+            }
+          }
+          if (!full_chunk) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (vbase + j >= p.V) l[j] = -INFINITY;
+          }
+          const float mb0 = max16(l), mb1 = max16(l + 16);
+          const float lmax = fmaxf(mb0, mb1);
+          if (lmax == -INFINITY) continue;  // nothing here can be drawn
+          const float ymax = lmax * scale2;
+          if (ymax > m2) {
+            sum *= ex2_approx(m2 - ymax);
+            m2 = ymax;
+          }
+          // w = 2^(l scale2 - m2): the tokens' weights relative to the running maximum
+          float w[32];
+          {
+            const float2 s2 = make_float2(scale2, scale2), nm = make_float2(-m2, -m2);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float2 d = __ffma2_rn(make_float2(l[j], l[j + 1]), s2, nm);
+              w[j] = ex2_approx(d.x);
+              w[j + 1] = ex2_approx(d.y);
+            }
+          }
+          const float bs0 = sum16(w), bs1 = sum16(w + 16);
+          sum += bs0 + bs1;
+          if (MODE == kModeSample) {
+            // stage 1: G = m2 + log2(block mass) - log2(E); stage 2 runs once, after the sweep
+            const float G0 = bs0 > 0.f ? m2 + lg2_approx(bs0) - lE[2 * sub] : -INFINITY;
+            const float G1 = bs1 > 0.f ? m2 + lg2_approx(bs1) - lE[2 * sub + 1] : -INFINITY;
+            keep_best(G0, vbase, sub ? nza[3] : nza[1], l, my_best, kEpiThreads, best, best_v,
+                      best_w);
+            keep_best(G1, vbase + 16, sub ? nzb[3] : nzb[1], l + 16, my_best, kEpiThreads, best,
+                      best_v, best_w);
+          } else if (MODE == kModeGreedy) {
+            keep_best(mb0 * scale2, vbase, 0u, l, my_best, kEpiThreads, best, best_v, best_w);
+            keep_best(mb1 * scale2, vbase + 16, 0u, l + 16, my_best, kEpiThreads, best, best_v,
+                      best_w);
+          }
+        }
+      }
+
+      // ---- the thread's winner of the position: stage 2 of the race in its best block
+      // (the greedy maximum's first token), from the values kept in shared memory
+      float yb = -INFINITY, lb = 0.f;  // best score (G, or y when greedy) and its logit
+      int vb = 0x7FFFFFFF;
+      if ((kRace || MODE == kModeGreedy) && !fail && row_ok && best > -INFINITY) {
+        float v16[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 x = my_best[c * kEpiThreads];
+          v16[4 * c] = x.x;
+          v16[4 * c + 1] = x.y;
+          v16[4 * c + 2] = x.z;
+          v16[4 * c + 3] = x.w;
+        }
+        int js;
+        if (MODE == kModeResidual) {
+          js = race_stage2(v16, best_w);  // the weights themselves
+        } else {
+          const float vmax = max16(v16);
+          if (MODE == kModeSample) {
+            float w16[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w16[j] = ex2_approx((v16[j] - vmax) * scale2);
+            js = race_stage2(w16, best_w);
+          } else {
+            js = 15;
 #pragma unroll
             for (int j = 15; j >= 0; --j)
-              if (y[j] == cmax) jb = j;
-            yb = cmax;
-            vb = vbase + jb;
-            lb = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j == jb) lb = y[j];
-            lb *= inv_scale2;
-            atomicMax(&s_bound[b], make_key(p.epoch, yb, vb));
-          }
-          if ((tt & 1) == 1 && g == 0) {
-            // publish this CTA's best so far (lets other CTAs gather the next
-            // position's embeddings speculatively before the grid barrier)
-            const unsigned long long mine = s_bound[b];
-            if (mine > gkey) {
-              atomicMax(p.keys + k * kRows + b, mine);
-              gkey = mine;
-            }
+              if (v16[j] == vmax) js = j;
           }
         }
+        float lj = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j == js) lj = v16[j];
+        yb = best;
+        vb = best_v + js;
+        lb = lj;
       }
 
       // ---- merge the column groups (and copies) of each request, publish the CTA's
-      // partial; record slot sl = copy * 4 + g, rpc rows per record field
+      // partial; record slot sl = copy * 2 + g, rpc rows per record field
       if (etid == 0) trace_stamp(p, cta, k, 3);
-      // sampling a full batch: the global key of this thread's gather row is read now, so
-      // that the merge hides the load (greedy draws and batch copies keep the later,
-      // fresher read: measured faster there)
-      constexpr bool kEarlyKey = MODE == kModeSample && !COPIES;
-      const int grow_pre = (etid >> 2) & (rpc - 1);
+      // the global key of this thread's row, read now so that the merge hides the load
       const unsigned long long gk_pre =
-          (kEarlyKey && k + 1 < p.K && grow_pre < p.B)
-              ? __ldcg(p.keys + k * kRows + grow_pre)
-              : 0ull;
+          (kKeys && !kTF && row_ok) ? __ldcg(p.keys + k * kRows + b) : 0ull;
       const float score = yb;
-      const int slot = copy * 4 + g;
-      // the merge records live in the operand's memory: with several copies a warp can
-      // get here while the MMAs of other copies' last tiles still read it
-      if (!fail && !mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag)) {
-        fail = true;
-        *abort_flag = 1;
-      }
+      const int slot = copy * 2 + g;
       if (!fail) {
         merge[(slot * 5 + 0) * rpc + b] = m2;
         merge[(slot * 5 + 1) * rpc + b] = sum;
@@ -1061,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         float M = merge[0 * rpc + b], S = merge[1 * rpc + b];
         float best_s = merge[2 * rpc + b], best_l = merge[4 * rpc + b];
         int best_v = __float_as_int(merge[3 * rpc + b]);
-        for (int ss = 1; ss < 4 * ncopy; ++ss) {
+        for (int ss = 1; ss < 2 * ncopy; ++ss) {
           lse_merge(M, S, merge[(ss * 5 + 0) * rpc + b], merge[(ss * 5 + 1) * rpc + b]);
           const float s2 = merge[(ss * 5 + 2) * rpc + b];
           const int v2 = __float_as_int(merge[(ss * 5 + 3) * rpc + b]);
@@ -1075,7 +1002,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (kKeys && best_v != 0x7FFFFFFF) {
           key = make_key(p.epoch, best_s, best_v);
           atomicMax(p.keys + k * kRows + b, key);
-          if (!kTF && key >= gkey && k + 1 < p.K) {
+          s_bound[b] = key;  // the CTA's best: the speculative gather's fallback
+          if (!kTF && key > gk_pre && k + 1 < p.K) {
             // this CTA may hold the winner: pull its Markov embedding into L2 so that
             // every CTA's gather for the next position hits L2
             const char* row = reinterpret_cast<const char*>(p.W1 + static_cast<size_t>(best_v) * p.r);
@@ -1091,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
       named_bar_sync(kEpiBarrier, kEpiThreads);
 
-      // ---- arrive at the grid barrier (the wait comes after the speculative gather)
+      // ---- arrive at the grid barrier (the wait comes after the speculative operand)
       if (etid == 0 && !fail) {
         const bool skip = (p.debug_skip_cta == cta) && (k == 0);
         // the release add orders every epilogue thread's partial and key writes
@@ -1100,41 +1028,38 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
 
       if (etid == 0) trace_stamp(p, cta, k, 7);
-      // ---- speculative gather for the next position: the likely winner is the better
-      // of the global key (read before the merge) and this CTA's best (complete now);
-      // without a gate its row is copied asynchronously and lands while the grid
-      // barrier completes
+      // ---- speculative operand for the next position: the likely winner is the better of
+      // the global key (read after this CTA's arrival) and this CTA's best; its embedding
+      // loads are in flight while the grid barrier completes, and it is written to TMEM
+      // (after a re-check of the key) at the start of the next position
       if (k + 1 < p.K && !fail) {
-        if (!mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag)) {  // MMAs done reading E
+        bool ok = mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag);  // MMAs done with E
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
           fail = true;
           *abort_flag = 1;
         } else {
-          const int grow = (etid >> 2) & (rpc - 1);
+          tc_fence_after();
           int32_t tok = 0;
-          if (grow < p.B) {
+          if (row_ok) {
             if (kTF) {
-              tok = __ldg(p.prev + static_cast<size_t>(grow) * p.K + k + 1);
+              tok = __ldg(p.prev + static_cast<size_t>(b) * p.K + k + 1);
               if (tok < 0 || tok >= p.V) {
                 record_error(p.status, kStatusDeviceOob);
                 tok = 0;
               }
             } else {
-              const unsigned long long gk =
-                  kEarlyKey ? gk_pre : __ldcg(p.keys + k * kRows + grow);
-              const unsigned long long lk = s_bound[grow];
+              const unsigned long long gk = __ldcg(p.keys + k * kRows + b);
+              const unsigned long long lk = s_bound[b];
               spec_key = (key_epoch(gk) == p.epoch && gk > lk) ? gk : lk;
               tok = key_token(spec_key);
               if (key_epoch(spec_key) != p.epoch || tok < 0 || tok >= p.V) {
-                spec_key = ~0ull;  // never matches: refetched after the barrier
+                spec_key = ~0ull;  // never matches: gathered again after the barrier
                 tok = 0;
               }
             }
           }
-          if (p.H == nullptr) {
-            copy_embedding_async(sA, p, etid, tok);
-          } else {
-            gather_embeddings(sA, p, k + 1, etid, tok);
-          }
+          gather_operand(k + 1, row_ok, tok);
         }
       }
 
@@ -1254,6 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       }
       if (etid == 0) trace_stamp(p, cta, p.K - 1, 6);
     }
+    tmem_wait_st();  // no operand write may be in flight when TMEM is released
   }
 
   tc_fence_before();
@@ -1286,7 +1212,7 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
       fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, true>)
                   : reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, false>);
       break;
-    case kModeLabel:  // half-tile ring slots: always the 128-row instantiation
+    case kModeLabel:  // half-sub-tile ring slots: always the 128-row instantiation
       fn = reinterpret_cast<const void*>(&draft_kernel<kModeLabel, false>);
       break;
     case kModeResidual:

@@ -13,7 +13,11 @@ namespace dspark {
 constexpr int kMaxK = 64;           // block positions per call
 constexpr int kMaxRank = 256;       // Markov rank
 constexpr int kBatchChunk = 128;    // requests per draft launch (MMA M)
-constexpr int kDraftTileV = 64;     // vocabulary entries per draft tile (MMA N)
+constexpr int kDraftTileN = 128;    // vocabulary entries per draft MMA tile (MMA N)
+constexpr int kDraftBoxV = 64;      // W2 TMA box width: one 128-byte swizzled row of bf16
+constexpr int kDraftSliceRows = 128;  // W2 rows (the contraction dimension) per ring slot
+// rows of one W2 box (and ring slot): the whole rank when it fits, else 128
+inline int draft_slice_rows(int r) { return r < kDraftSliceRows ? r : kDraftSliceRows; }
 constexpr int kMaxTopk = 32;
 constexpr int kTopkPartUnits = 4096;  // per-piece top-k lists the context can hold
 constexpr int kTraceSlots = 8;      // timestamps per (CTA, step) in the draft trace
@@ -43,7 +47,7 @@ struct DraftParams {
   const float* H;           // gated: [B, K, r] (chunk) fp32, or null
   int B, K, V, r;
   int b_global0;            // index of the chunk's first request in the call (noise key)
-  int n_tiles;              // ceil(V / 64)
+  int n_tiles;              // ceil(V / 128)
   int box_rows;             // rows of the U TMA box (multiple of 8, >= B)
   float inv_t;              // 1 / T' (T' = T, or 1 when greedy)
   uint32_t seed_lo, seed_hi;
@@ -87,7 +91,7 @@ struct DraftParams {
 };
 
 struct DraftArgs {
-  CUtensorMap tm_w2;  // W2 [r, V] bf16, box {64, r}, 128B swizzle
+  CUtensorMap tm_w2;  // W2 [r, V] bf16, box {64, min(r, 128)}, 128B swizzle
   CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle;
                       // residual mode: U as rows [B K, V], box {32, 1} (gathered by four)
   CUtensorMap tm_p;   // label mode: target chunk [B, K+1, V] fp32, box {32, 1, box_rows},

@@ -185,7 +185,7 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, c
   // the array keeps the previous call's contents: clear what must start at zero
   if (cudaMemsetAsync(scratch, 0, kNaOffPartials, s) != cudaSuccess) return DSPARK_ERR_CUDA;
 
-  const int n_tiles = (V + dspark::kDraftTileV - 1) / dspark::kDraftTileV;
+  const int n_tiles = (V + dspark::kDraftTileN - 1) / dspark::kDraftTileN;
   int grid = n_tiles < sms ? n_tiles : sms;
   if (grid > kNaMaxGrid) grid = kNaMaxGrid;
   const float inv_t = temperature > 0.f ? 1.0f / temperature : 1.0f;
@@ -198,8 +198,8 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, c
     if (r > 0) {
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(r)};
       const cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
-      const cuuint32_t box[2] = {static_cast<cuuint32_t>(dspark::kDraftTileV),
-                                 static_cast<cuuint32_t>(r)};
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(dspark::kDraftBoxV),
+                                 static_cast<cuuint32_t>(dspark::draft_slice_rows(r))};
       if (!encode(&args.tm_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W2, 2, dims, strides, box))
         return DSPARK_ERR_CUDA;
     }

@@ -76,47 +76,49 @@ __host__ __device__ inline void philox_round_keys(uint32_t k0, uint32_t k1, uint
   }
 }
 
-// N Philox4x32-10 blocks with counters (c0 + q, c1, c2, 0), q = 0..N-1, and a
-// precomputed key schedule, interleaved round by round for instruction-level
-// parallelism; out[4 q + w] = word w of block q.  Round 0 of every block shares
-// the product M1 * c2, computed once.
-template <int N>
-__device__ __forceinline__ void philox4x32_10_xn(uint32_t c0, uint32_t c1, uint32_t c2,
-                                                 const uint32_t (&rk0)[10],
-                                                 const uint32_t (&rk1)[10],
-                                                 uint32_t (&out)[4 * N]) {
-  uint32_t x0[N], x1[N], x2[N], x3[N];
+// Two blocks with counters (c0, c1, c2, c3a) and (c0, c1, c2, c3b) and a precomputed key
+// schedule, interleaved round by round for instruction-level parallelism.  Round 0 of
+// both shares the products of words 0 and 2 (equal in both counters).
+__device__ __forceinline__ void philox4x32_10_rk2(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                  uint32_t c3a, uint32_t c3b,
+                                                  const uint32_t (&rk0)[10],
+                                                  const uint32_t (&rk1)[10], uint32_t (&oa)[4],
+                                                  uint32_t (&ob)[4]) {
+  const uint64_t pa0 = static_cast<uint64_t>(0xD2511F53u) * c0;
   const uint64_t pb0 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
-  const uint32_t n0_r0 = static_cast<uint32_t>(pb0 >> 32) ^ c1 ^ rk0[0];
-#pragma unroll
-  for (int q = 0; q < N; ++q) {
-    const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * (c0 + q);
-    x0[q] = n0_r0;
-    x1[q] = static_cast<uint32_t>(pb0);
-    x2[q] = static_cast<uint32_t>(pa >> 32) ^ rk1[0];  // word 3 of the counter is 0
-    x3[q] = static_cast<uint32_t>(pa);
-  }
+  uint32_t a0 = static_cast<uint32_t>(pb0 >> 32) ^ c1 ^ rk0[0];
+  uint32_t a1 = static_cast<uint32_t>(pb0);
+  uint32_t a2 = static_cast<uint32_t>(pa0 >> 32) ^ c3a ^ rk1[0];
+  uint32_t a3 = static_cast<uint32_t>(pa0);
+  uint32_t b0 = a0, b1 = a1, b3 = a3;
+  uint32_t b2 = static_cast<uint32_t>(pa0 >> 32) ^ c3b ^ rk1[0];
 #pragma unroll
   for (int round = 1; round < 10; ++round) {
-#pragma unroll
-    for (int q = 0; q < N; ++q) {
-      const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * x0[q];
-      const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * x2[q];
-      const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ x1[q] ^ rk0[round];
-      const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ x3[q] ^ rk1[round];
-      x1[q] = static_cast<uint32_t>(pb);
-      x3[q] = static_cast<uint32_t>(pa);
-      x0[q] = n0;
-      x2[q] = n2;
-    }
+    const uint64_t qa = static_cast<uint64_t>(0xD2511F53u) * a0;
+    const uint64_t qb = static_cast<uint64_t>(0xCD9E8D57u) * a2;
+    const uint64_t ra = static_cast<uint64_t>(0xD2511F53u) * b0;
+    const uint64_t rb = static_cast<uint64_t>(0xCD9E8D57u) * b2;
+    const uint32_t na0 = static_cast<uint32_t>(qb >> 32) ^ a1 ^ rk0[round];
+    const uint32_t na2 = static_cast<uint32_t>(qa >> 32) ^ a3 ^ rk1[round];
+    const uint32_t nb0 = static_cast<uint32_t>(rb >> 32) ^ b1 ^ rk0[round];
+    const uint32_t nb2 = static_cast<uint32_t>(ra >> 32) ^ b3 ^ rk1[round];
+    a1 = static_cast<uint32_t>(qb);
+    a3 = static_cast<uint32_t>(qa);
+    b1 = static_cast<uint32_t>(rb);
+    b3 = static_cast<uint32_t>(ra);
+    a0 = na0;
+    a2 = na2;
+    b0 = nb0;
+    b2 = nb2;
   }
-#pragma unroll
-  for (int q = 0; q < N; ++q) {
-    out[4 * q + 0] = x0[q];
-    out[4 * q + 1] = x1[q];
-    out[4 * q + 2] = x2[q];
-    out[4 * q + 3] = x3[q];
-  }
+  oa[0] = a0;
+  oa[1] = a1;
+  oa[2] = a2;
+  oa[3] = a3;
+  ob[0] = b0;
+  ob[1] = b1;
+  ob[2] = b2;
+  ob[3] = b3;
 }
 
 // t = 1 - u for the uniform u of `word`: with n = word & 0x7FFFFF,

@@ -49,7 +49,7 @@ def main() -> None:
     W2 = (torch.randn(R, V, device=dev, generator=g) * 0.02).to(torch.bfloat16)
     anc = torch.randint(0, V, (B,), device=dev, dtype=torch.int32, generator=g)
     T = 0.0 if args.mode == "greedy" else 1.0
-    grid = min(torch.cuda.get_device_properties(dev).multi_processor_count, (V + 63) // 64)
+    grid = min(torch.cuda.get_device_properties(dev).multi_processor_count, (V + 127) // 128)
     buf = torch.zeros(grid * K * SLOTS, dtype=torch.int64, device=dev)
     with binding.Context(0, B_max=B, V_max=V, K_max=K) as ctx:
         if args.mode == "label":
