@@ -74,6 +74,11 @@ def _bind(lib):
     lib.orc_markov_draft.restype = i32
     lib.orc_markov_logits.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P, P]
     lib.orc_markov_logits.restype = i32
+    lib.orc_rnn_draft.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, u64, i32, i32,
+                                  P, P, P, P, P]
+    lib.orc_rnn_draft.restype = i32
+    lib.orc_rnn_logits.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P, P]
+    lib.orc_rnn_logits.restype = i32
     lib.orc_confidence.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32, i32, i32, f64,
                                    P, P, P, P]
     lib.orc_confidence.restype = i32
@@ -251,6 +256,57 @@ class Oracle:
                                        float(temperature), b0, nb, _ptr(logits), _ptr(lse))
         if rc != 0:
             raise ValueError("oracle markov_logits rejected its arguments")
+        return dict(logits=logits, lse=lse)
+
+    def rnn_draft(self, U, W1, W2, anchors, A, *, G=None, temperature: float, seed: int,
+                  b0: int = 0, nb: Optional[int] = None, forced=None) -> dict:
+        """The RNN head's draft: state s_k = A_k (.) s_{k-1} + G_k (.) W1[x_{k-1}] (G None:
+        1), bias s_k W2.  A, G [B, K, r] gate values (fp64); outputs as markov_draft."""
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        W1 = _c(W1, np.uint16)
+        W2 = _c(W2, np.uint16)
+        r = W1.shape[1]
+        anchors = _c(anchors, np.int32)
+        A = _c(A, np.float64)
+        G = _c(G, np.float64)
+        assert A.shape == (B, K, r)
+        nb = B - b0 if nb is None else nb
+        forced = _c(forced, np.int32)
+        tokens = np.zeros((nb, K), np.int32)
+        logprobs = np.zeros((nb, K), np.float64)
+        margins = np.zeros((nb, K), np.float64)
+        flp = np.zeros((nb, K), np.float64) if forced is not None else None
+        rc = self._lib.orc_rnn_draft(_ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), _ptr(A), _ptr(G),
+                                     B, K, V, r, float(temperature), int(seed), b0, nb,
+                                     _ptr(forced), _ptr(tokens), _ptr(logprobs), _ptr(margins),
+                                     _ptr(flp))
+        if rc != 0:
+            raise ValueError("oracle rnn_draft rejected its arguments")
+        out = dict(tokens=tokens, logprobs=logprobs, margins=margins)
+        if forced is not None:
+            out["forced_logprobs"] = flp
+        return out
+
+    def rnn_logits(self, U, W1, W2, prev, A, *, G=None, temperature: float = 1.0, b0: int = 0,
+                   nb: Optional[int] = None) -> dict:
+        """Teacher-forced logits [nb, K, V] (fp64) and lse [nb, K] of the RNN head."""
+        U = _c(U, np.float32)
+        B, K, V = U.shape
+        W1 = _c(W1, np.uint16)
+        W2 = _c(W2, np.uint16)
+        r = W1.shape[1]
+        prev = _c(prev, np.int32)
+        A = _c(A, np.float64)
+        G = _c(G, np.float64)
+        nb = B - b0 if nb is None else nb
+        logits = np.zeros((nb, K, V), np.float64)
+        lse = np.zeros((nb, K), np.float64)
+        rc = self._lib.orc_rnn_logits(_ptr(U), _ptr(W1), _ptr(W2), _ptr(prev), _ptr(A), _ptr(G),
+                                      B, K, V, r, float(temperature), b0, nb, _ptr(logits),
+                                      _ptr(lse))
+        if rc != 0:
+            raise ValueError("oracle rnn_logits rejected its arguments")
         return dict(logits=logits, lse=lse)
 
     def confidence(self, h, W1, anchors, tokens, w, *, bias: float = 0.0, with_markov: bool = True,

@@ -197,13 +197,10 @@ void orc_gate(const uint16_t* h, const uint16_t* Wg, int64_t M, int d, int r, do
 /* the local softmax exp(z_k(v) + B(t_{k-1}, v)) / sum_u exp(...).      */
 /* Writes l[v] (calibrated logits) for v in [0, V).                     */
 /* ------------------------------------------------------------------ */
-static void calibrated_logits(const float* Urow, const uint16_t* W1, const uint16_t* W2,
-                              const double* Hrow, int V, int r, int32_t prev, double* e,
-                              double* l) {
-  for (int i = 0; i < r; ++i) {
-    double w1 = bf16_to_double(W1[(int64_t)prev * r + i]);
-    e[i] = Hrow ? w1 * Hrow[i] : w1;
-  }
+/* l[v] = U[v] + sum_i e[i] * W2[i, v] for v in [0, V): the bias of a head  */
+/* embedding e (length r) added to one row of base logits.                   */
+static void bias_logits(const float* Urow, const uint16_t* W2, const double* e, int V, int r,
+                        double* l) {
 #pragma omp parallel
   {
 #ifdef _OPENMP
@@ -224,6 +221,41 @@ static void calibrated_logits(const float* Urow, const uint16_t* W1, const uint1
       }
       for (int64_t v = v0; v < v1; ++v) l[v] = (double)Urow[v] + l[v];
     }
+  }
+}
+
+static void calibrated_logits(const float* Urow, const uint16_t* W1, const uint16_t* W2,
+                              const double* Hrow, int V, int r, int32_t prev, double* e,
+                              double* l) {
+  for (int i = 0; i < r; ++i) {
+    double w1 = bf16_to_double(W1[(int64_t)prev * r + i]);
+    e[i] = Hrow ? w1 * Hrow[i] : w1;
+  }
+  bias_logits(Urow, W2, e, V, r, l);
+}
+
+/* ------------------------------------------------------------------ */
+/* RNN head: one step of the recurrent state.                          */
+/* [EXPL] "The RNN head": a recurrent state s_k kept inside the block,  */
+/* mixing the previous state, the previous token's embedding and the    */
+/* current backbone hidden h_k; [FIX] "Fix 1" ("Two instantiations of   */
+/* B": the RNN head carries a recurrent state through the block,        */
+/* accumulating the in-block prefix); [VLLM] "Key Parameters"           */
+/* (--markov-head-type rnn).  The pages give no equations; the reading  */
+/* taken (the plainest gated linear recurrence that reduces to the      */
+/* Markov heads) is                                                     */
+/*   s_k = a_k (.) s_{k-1} + g_k (.) W1[x_{k-1}],   s_{-1} = 0,         */
+/*   a_k = sigmoid(h_k . Wa) (decay),  g_k = sigmoid(h_k . Wg) (input), */
+/*   bias_k = s_k W2,                                                   */
+/* so a = 0 is the gated head and a = 0, g = 1 the vanilla one.  The    */
+/* gates are inputs here (Arow, Grow: rows of orc_gate's output; Grow   */
+/* NULL means g = 1).  Updates s in place.                              */
+/* ------------------------------------------------------------------ */
+static void rnn_state_step(const uint16_t* W1, int r, int32_t prev, const double* Arow,
+                           const double* Grow, double* s) {
+  for (int i = 0; i < r; ++i) {
+    const double w1 = bf16_to_double(W1[(int64_t)prev * r + i]);
+    s[i] = Arow[i] * s[i] + (Grow ? w1 * Grow[i] : w1);
   }
 }
 
@@ -321,19 +353,28 @@ static int block_race_draw(const int32_t* ids, const double* z, double* w, int n
 /* Returns 0, or -1 on bad arguments / allocation failure.              */
 /* ------------------------------------------------------------------ */
 /* One request of the draft; buffers l, s ([V]) and e ([r]) are the caller's. */
+/* A != NULL: the RNN head (A the decay gates, H the input gates or NULL), */
+/* with e carrying the recurrent state across positions.                   */
 static int draft_one_request(const float* U, const uint16_t* W1, const uint16_t* W2,
-                             const int32_t* anchors, const double* H, int K, int V, int r,
-                             double temperature, uint64_t seed, int b, int bi,
+                             const int32_t* anchors, const double* H, const double* A, int K,
+                             int V, int r, double temperature, uint64_t seed, int b, int bi,
                              const int32_t* forced, int32_t* tokens, double* logprobs,
                              double* margins, double* forced_logprobs, double* l, double* s,
                              double* e) {
   const double Tp = temperature > 0.0 ? temperature : 1.0;
   int32_t prev = anchors[b];
+  if (A)
+    for (int i = 0; i < r; ++i) e[i] = 0.0; /* s_{-1} = 0 */
   for (int k = 0; k < K; ++k) {
     const float* Urow = U + ((int64_t)b * K + k) * V;
     const double* Hrow = H ? H + ((int64_t)b * K + k) * r : NULL;
     if (prev < 0 || prev >= V) return -1;
-    calibrated_logits(Urow, W1, W2, Hrow, V, r, prev, e, l);
+    if (A) {
+      rnn_state_step(W1, r, prev, A + ((int64_t)b * K + k) * r, Hrow, e);
+      bias_logits(Urow, W2, e, V, r, l);
+    } else {
+      calibrated_logits(Urow, W1, W2, Hrow, V, r, prev, e, l);
+    }
     const int64_t o = (int64_t)bi * K + k;
     int best = 0;
     if (temperature > 0.0) {
@@ -367,10 +408,10 @@ static int draft_one_request(const float* U, const uint16_t* W1, const uint16_t*
   return 0;
 }
 
-int orc_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
-                     const int32_t* anchors, const double* H, int B, int K, int V, int r,
-                     double temperature, uint64_t seed, int b0, int nb, const int32_t* forced,
-                     int32_t* tokens, double* logprobs, double* margins,
+static int run_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
+                     const int32_t* anchors, const double* H, const double* A, int B, int K,
+                     int V, int r, double temperature, uint64_t seed, int b0, int nb,
+                     const int32_t* forced, int32_t* tokens, double* logprobs, double* margins,
                      double* forced_logprobs) {
   if (B <= 0 || K <= 0 || V <= 0 || r < 0 || b0 < 0 || nb < 0 || b0 + nb > B) return -1;
   int bad = 0;
@@ -388,7 +429,7 @@ int orc_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
     } else {
 #pragma omp for schedule(static)
       for (int bi = 0; bi < nb; ++bi) {
-        if (draft_one_request(U, W1, W2, anchors, H, K, V, r, temperature, seed, b0 + bi, bi,
+        if (draft_one_request(U, W1, W2, anchors, H, A, K, V, r, temperature, seed, b0 + bi, bi,
                               forced, tokens, logprobs, margins, forced_logprobs, l, s, e) != 0)
           bad = 1;
       }
@@ -398,6 +439,26 @@ int orc_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
     free(e);
   }
   return bad ? -1 : 0;
+}
+
+int orc_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
+                     const int32_t* anchors, const double* H, int B, int K, int V, int r,
+                     double temperature, uint64_t seed, int b0, int nb, const int32_t* forced,
+                     int32_t* tokens, double* logprobs, double* margins,
+                     double* forced_logprobs) {
+  return run_draft(U, W1, W2, anchors, H, NULL, B, K, V, r, temperature, seed, b0, nb, forced,
+                   tokens, logprobs, margins, forced_logprobs);
+}
+
+/* The RNN head's draft (rnn_state_step above): A [B,K,r] decay gates     */
+/* (required), G [B,K,r] input gates or NULL; otherwise as orc_markov_draft. */
+int orc_rnn_draft(const float* U, const uint16_t* W1, const uint16_t* W2,
+                  const int32_t* anchors, const double* A, const double* G, int B, int K, int V,
+                  int r, double temperature, uint64_t seed, int b0, int nb, const int32_t* forced,
+                  int32_t* tokens, double* logprobs, double* margins, double* forced_logprobs) {
+  if (A == NULL || r <= 0) return -1;
+  return run_draft(U, W1, W2, anchors, G, A, B, K, V, r, temperature, seed, b0, nb, forced,
+                   tokens, logprobs, margins, forced_logprobs);
 }
 
 /* ------------------------------------------------------------------ */
@@ -429,6 +490,40 @@ int orc_markov_logits(const float* U, const uint16_t* W1, const uint16_t* W2,
     }
   }
   free(e);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* RNN head, teacher-forced: the recurrent state driven by the given   */
+/* predecessors prev [B, K] (x_0 .. x_{K-1}); A [B,K,r] decay gates, G  */
+/* [B,K,r] input gates or NULL.  Rows b0 .. b0+nb-1; outputs compact    */
+/* logits [nb, K, V] fp64, lse [nb, K] = log sum exp(l / T').           */
+/* ------------------------------------------------------------------ */
+int orc_rnn_logits(const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* prev,
+                   const double* A, const double* G, int B, int K, int V, int r,
+                   double temperature, int b0, int nb, double* logits, double* lse) {
+  if (B <= 0 || K <= 0 || V <= 0 || r <= 0 || A == NULL || b0 < 0 || nb < 0 || b0 + nb > B)
+    return -1;
+  double* st = (double*)malloc(sizeof(double) * (size_t)r);
+  if (!st) return -1;
+  const double Tp = temperature > 0.0 ? temperature : 1.0;
+  for (int bi = 0; bi < nb; ++bi) {
+    const int b = b0 + bi;
+    for (int i = 0; i < r; ++i) st[i] = 0.0;
+    for (int k = 0; k < K; ++k) {
+      const int32_t a = prev[(int64_t)b * K + k];
+      if (a < 0 || a >= V) {
+        free(st);
+        return -1;
+      }
+      const int64_t o = (int64_t)b * K + k;
+      rnn_state_step(W1, r, a, A + o * r, G ? G + o * r : NULL, st);
+      double* l = logits + ((int64_t)bi * K + k) * V;
+      bias_logits(U + o * V, W2, st, V, r, l);
+      lse[(int64_t)bi * K + k] = log_sum_exp_scaled(l, V, Tp);
+    }
+  }
+  free(st);
   return 0;
 }
 

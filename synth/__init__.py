@@ -95,12 +95,13 @@ class DraftInputs:
     w_conf: Optional[np.ndarray] = None  # uint16 (bf16) [d + r] (confidence head)
     A: Optional[np.ndarray] = None     # uint16 (bf16) [V, r] (selector)
     Bt: Optional[np.ndarray] = None    # uint16 (bf16) [V, r] (selector)
+    Wa: Optional[np.ndarray] = None    # uint16 (bf16) [d, r] (RNN head's decay gate)
 
 
 def make_inputs(seed: int, B: int, K: int, V: int, r: int = RANK, *, d: int = 0,
                 gated: bool = False, confidence: bool = False, selector: bool = False,
                 spikes: int = 8, weight_std: float = 0.02,
-                selector_tables_only: bool = False) -> DraftInputs:
+                selector_tables_only: bool = False, rnn: bool = False) -> DraftInputs:
     """Draw one synthetic workload from PCG64(seed) in a fixed order."""
     rng = np.random.default_rng(seed)
     U = base_logits(rng, B, K, V, spikes=spikes)
@@ -122,6 +123,9 @@ def make_inputs(seed: int, B: int, K: int, V: int, r: int = RANK, *, d: int = 0,
     if selector:
         inp.A = _normal_bf16(rng, (V, r), weight_std)
         inp.Bt = _normal_bf16(rng, (V, r), weight_std)
+    if rnn:  # drawn last, so the other arrays are those of the same call without it
+        assert d > 0
+        inp.Wa = _normal_bf16(rng, (d, r), weight_std)
     return inp
 
 
@@ -139,6 +143,10 @@ CONFIGS = {
     4: dict(name="selector-top16 B=256 K=16 V=151936 r=256 d=4096", B=256, K=16,
             V=VOCAB_FULL, r=256, d=4096, gated=True, selector=True, topk=16,
             temperatures=(1.0,), seeds=tuple(range(4))),
+    # the RNN head (no workload of the pages' own; the gated head's shapes, with both the
+    # decay gate Wa and the input gate Wg drawn like Wg)
+    5: dict(name="rnn B=64 K=16 V=151936 r=256 d=4096", B=64, K=16, V=VOCAB_FULL, r=256,
+            d=4096, gated=True, rnn=True, temperatures=(1.0,), seeds=tuple(range(4))),
 }
 
 
@@ -161,7 +169,7 @@ def config_inputs(cfg: int) -> DraftInputs:
     return make_inputs(1000 + cfg, c["B"], c["K"], c["V"], c["r"], d=c.get("d", 0),
                        gated=c.get("gated", False), confidence=c.get("confidence", False),
                        selector=c.get("selector", False),
-                       selector_tables_only=c.get("selector", False))
+                       selector_tables_only=c.get("selector", False), rnn=c.get("rnn", False))
 
 
 def schedule_inputs(seed: int, R: int, K: int):

@@ -82,6 +82,22 @@ MUTANTS = [
     ("label-predecessor-not-carried", "      label[(int64_t)b * K + k] = s;\n      prev = x;\n",
      "      label[(int64_t)b * K + k] = s;\n",
      ["test_accept_label_special_cases", "test_accept_label_is_the_verifier_acceptance_rate"]),
+    ("rnn-state-not-carried", "s[i] = Arow[i] * s[i] + (Grow ? w1 * Grow[i] : w1);",
+     "s[i] = (Grow ? w1 * Grow[i] : w1);",
+     ["test_rnn_state_is_a_geometric_series_under_constant_decay",
+      "test_rnn_unrolled_state_matches_teacher_forced_logits"]),
+    ("rnn-decay-on-the-input", "s[i] = Arow[i] * s[i] + (Grow ? w1 * Grow[i] : w1);",
+     "s[i] = s[i] + Arow[i] * (Grow ? w1 * Grow[i] : w1);",
+     ["test_rnn_state_is_a_geometric_series_under_constant_decay",
+      "test_rnn_with_zero_decay_is_the_markov_head"]),
+    ("rnn-input-gate-ignored", "s[i] = Arow[i] * s[i] + (Grow ? w1 * Grow[i] : w1);",
+     "s[i] = Arow[i] * s[i] + w1;",
+     ["test_rnn_unrolled_state_matches_teacher_forced_logits",
+      "test_rnn_with_zero_decay_is_the_markov_head"]),
+    ("rnn-state-not-reset-per-request", "    for (int i = 0; i < r; ++i) e[i] = 0.0; /* s_{-1} = 0 */",
+     "", ["test_rnn_sampler_matches_exhaustive_joint"]),
+    ("rnn-draft-predecessor-not-carried", "      prev = best;\n", "      prev = anchors[b];\n",
+     ["test_rnn_sampler_matches_exhaustive_joint"]),
 ]
 
 

@@ -135,6 +135,115 @@ def test_gated_head_with_unit_gate_equals_vanilla(orc):
             assert np.array_equal(a[key], g[key])
 
 
+# ---------------------------------------------------------------------- RNN head
+# Reading of the RNN head (DSpark explainer, "The RNN head"; "Repair the Joint",
+# "Fix 1"): s_k = a_k (.) s_{k-1} + g_k (.) W1[x_{k-1}], s_{-1} = 0, bias_k = s_k W2.
+def _rnn_unrolled(W1, prev, A, G):
+    """The recurrence's solution in closed form: s_k = sum_{j<=k} (prod_{j<i<=k} a_i) g_j
+    (.) W1[x_{j-1}], from cumulative products (no step-by-step update)."""
+    B, K, r = A.shape
+    E = f64(W1)[prev] * (1.0 if G is None else G)            # [B, K, r] inputs
+    S = np.zeros((B, K, r))
+    for k in range(K):
+        # weight of input j at position k: prod of a over positions j+1..k
+        w = np.ones((B, k + 1, r))
+        if k > 0:
+            rev = np.cumprod(A[:, k:0:-1], axis=1)[:, ::-1]  # [B, k, r]: prod_{i=j+1..k} a_i
+            w[:, :k] = rev
+        S[:, k] = (w * E[:, :k + 1]).sum(axis=1)
+    return S
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_rnn_with_zero_decay_is_the_markov_head(orc, gated):
+    """a = 0 removes the state: the RNN head is then the gated head (input gate g = H)
+    and, with g = 1, the vanilla Markov head -- bitwise, draft and teacher-forced."""
+    B, K, V, r, d = 5, 6, 128, 32, 16
+    inp = small_inputs(21, B, K, V, r, std=0.3, d=d, gated=True)
+    H = orc.gate(inp.h, inp.Wg) if gated else None
+    A = np.zeros((B, K, r))
+    for T in (1.0, 0.7, 0.0):
+        m = orc.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=T, seed=4, H=H)
+        n = orc.rnn_draft(inp.U, inp.W1, inp.W2, inp.anchors, A, G=H, temperature=T, seed=4)
+        for key in ("tokens", "logprobs", "margins"):
+            assert np.array_equal(m[key], n[key])
+    prev = np.random.default_rng(22).integers(0, V, size=(B, K)).astype(np.int32)
+    ml = orc.markov_logits(inp.U, inp.W1, inp.W2, prev, H=H)
+    nl = orc.rnn_logits(inp.U, inp.W1, inp.W2, prev, A, G=H)
+    assert np.array_equal(ml["logits"], nl["logits"]) and np.array_equal(ml["lse"], nl["lse"])
+
+
+@pytest.mark.parametrize("lam", [0.5, 0.75])
+def test_rnn_state_is_a_geometric_series_under_constant_decay(orc, lam):
+    """The same predecessor t at every position, a = lam, g = 1: the state is the partial
+    geometric series s_k = (1 - lam^(k+1)) / (1 - lam) W1[t]."""
+    B, K, V, r = 2, 7, 96, 32
+    inp = small_inputs(23, B, K, V, r, std=0.3)
+    prev = np.repeat(np.array([[5], [61]], np.int32), K, axis=1)
+    A = np.full((B, K, r), lam)
+    out = orc.rnn_logits(inp.U, inp.W1, inp.W2, prev, A)
+    coef = (1.0 - lam ** np.arange(1, K + 1)) / (1.0 - lam)            # [K]
+    bias_t = f64(inp.W1)[prev[:, 0]] @ f64(inp.W2)                       # [B, V]
+    ref = inp.U.astype(np.float64) + coef[None, :, None] * bias_t[:, None, :]
+    assert np.allclose(out["logits"], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_rnn_unrolled_state_matches_teacher_forced_logits(orc):
+    """Random gates and predecessors: logits_k = U_k + s_k W2 with s_k from the unrolled
+    (cumulative-product) solution of the recurrence."""
+    B, K, V, r, d = 4, 6, 80, 32, 24
+    inp = small_inputs(24, B, K, V, r, std=0.3, d=d, gated=True)
+    rng = np.random.default_rng(25)
+    prev = rng.integers(0, V, size=(B, K)).astype(np.int32)
+    A = rng.uniform(0.0, 1.0, (B, K, r))
+    G = orc.gate(inp.h, inp.Wg)
+    for T in (1.0, 0.7):
+        out = orc.rnn_logits(inp.U, inp.W1, inp.W2, prev, A, G=G, temperature=T)
+        ref = inp.U.astype(np.float64) + _rnn_unrolled(inp.W1, prev, A, G) @ f64(inp.W2)
+        assert np.allclose(out["logits"], ref, rtol=1e-12, atol=1e-12)
+        assert np.allclose(out["lse"], special.logsumexp(ref / T, axis=-1), rtol=0, atol=1e-11)
+    # the draft forced onto the same predecessors gives the same log-probabilities
+    forced = np.concatenate([prev[:, 1:], prev[:, :1]], axis=1)
+    anchors = prev[:, 0].copy()
+    dr = orc.rnn_draft(inp.U, inp.W1, inp.W2, anchors, A, G=G, temperature=1.0, seed=5,
+                       forced=forced)
+    lp = ref - special.logsumexp(ref, axis=-1)[..., None]
+    want = np.take_along_axis(lp, forced[..., None].astype(np.int64), axis=-1)[..., 0]
+    assert np.allclose(dr["forced_logprobs"], want, atol=1e-11)
+
+
+def test_rnn_sampler_matches_exhaustive_joint(orc):
+    """2 * 10^5 draws of a V = 8, K = 3 RNN head vs the exhaustive joint
+    prod_k softmax(U_k + s_k(x_{<k}) W2), s from the unrolled recurrence on each path."""
+    V, K, r, N = 8, 3, 8, 200_000
+    rng = np.random.default_rng(26)
+    U1 = rng.standard_normal((1, K, V)).astype(np.float32)
+    W1 = bf16_bits(rng.normal(0, 0.6, (V, r)).astype(np.float32))
+    W2 = bf16_bits(rng.normal(0, 0.6, (r, V)).astype(np.float32))
+    A1 = rng.uniform(0.3, 0.9, (1, K, r))
+    G1 = rng.uniform(0.5, 1.0, (1, K, r))
+    anchor = 3
+    U = np.ascontiguousarray(np.broadcast_to(U1, (N, K, V)))
+    A = np.ascontiguousarray(np.broadcast_to(A1, (N, K, r)))
+    G = np.ascontiguousarray(np.broadcast_to(G1, (N, K, r)))
+    out = orc.rnn_draft(U, W1, W2, np.full(N, anchor, np.int32), A, G=G, temperature=1.0, seed=7)
+    paths = out["tokens"].astype(np.int64)
+    cell = (paths[:, 0] * V + paths[:, 1]) * V + paths[:, 2]
+    counts = np.bincount(cell, minlength=V ** K).astype(np.float64)
+    P = np.zeros((V,) * K)
+    for x1 in range(V):
+        for x2 in range(V):
+            prev = np.array([[anchor, x1, x2]], np.int32)
+            S = _rnn_unrolled(W1, prev, A1, G1)[0]                    # [K, r]
+            l = U1[0].astype(np.float64) + S @ f64(W2)
+            p = special.softmax(l, axis=-1)
+            P[x1, x2, :] = p[0, x1] * p[1, x2] * p[2]
+    assert abs(P.sum() - 1) < 1e-12
+    assert _chi2_pvalue(counts, P.reshape(-1) * N) > 0.01
+    sel = slice(0, 2000)
+    assert np.allclose(out["logprobs"][sel].sum(1), np.log(P.reshape(-1)[cell[sel]]), atol=1e-10)
+
+
 # ----------------------------------------------------------------- sampling rule
 def _replicate(inp, n):
     U = np.ascontiguousarray(np.broadcast_to(inp.U[:1], (n,) + inp.U.shape[1:]))
