@@ -179,6 +179,36 @@ int dspark_gated_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1,
                        float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
                        const dspark_conf_args* conf, dspark_stream_t stream);
 
+/* RNN head: a recurrent state carried across the block's positions.
+ * Source: DSpark explainer, "The RNN head" (a recurrent state s_k inside the
+ * block mixing the previous state, the previous token's embedding and the
+ * current backbone hidden h_k); "DSpark: Repair the Joint, Meter the Verify",
+ * "Fix 1" ("Two instantiations of B": the RNN head carries a recurrent state
+ * through the block); vLLM guide, "Key Parameters" (--markov-head-type rnn).
+ * The pages give no equations; this library's reading is
+ *   s_k = a_k (.) s_{k-1} + g_k (.) W1[x_{k-1}],  s_{-1} = 0,
+ *   a_k = sigmoid(h_k . Wa) (decay),  g_k = sigmoid(h_k . Wg) (input; 1 when
+ *   Wg == NULL),  logits_k = U_k + s_k W2,
+ * so a = 0 gives the gated head and a = 0, g = 1 the vanilla one.  The state
+ * is carried as the bf16 MMA operand (rounded at every position).
+ *   h [B, K, d] bf16, Wa [d, r] bf16, Wg [d, r] bf16 or NULL; d and r
+ *   multiples of 64.  Other arguments as dspark_markov_draft; the fused
+ *   confidence head uses W1[x_{k-1}] as its Markov embedding.
+ * Launches one or two gate GEMMs with their finalisers, then the draft kernel. */
+int dspark_rnn_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1, const uint16_t* W2,
+                     const int32_t* anchors, const uint16_t* h, const uint16_t* Wa,
+                     const uint16_t* Wg, int d, int B, int K, int V, int r, float temperature,
+                     uint64_t seed, int32_t* tokens, float* logprobs,
+                     const dspark_conf_args* conf, dspark_stream_t stream);
+
+/* The RNN head's teacher-forced logits and LSE (parity mode): the state driven by
+ * the given predecessors prev_tokens [B, K] (x_0 .. x_{K-1}); outputs as
+ * dspark_markov_logits.  Source and reading as dspark_rnn_draft. */
+int dspark_rnn_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, const uint16_t* W2,
+                      const int32_t* prev_tokens, const uint16_t* h, const uint16_t* Wa,
+                      const uint16_t* Wg, int d, int B, int K, int V, int r, float temperature,
+                      float* logits, float* lse, dspark_stream_t stream);
+
 /* The gate alone: H[m, :] = sigmoid(h[m, :] . Wg) for m < M.
  * Source: equivalence page, "What the two methods do" (the gate H(h_t) is a
  * function of the current hidden state alone, so every (request, position)

@@ -33,7 +33,7 @@ EXPORTS = (
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
     "dspark_markov_draft_noalloc", "dspark_verify", "dspark_schedule", "dspark_accept_label",
-    "dspark_sts_fit",
+    "dspark_sts_fit", "dspark_rnn_draft", "dspark_rnn_logits",
 )
 
 
@@ -87,6 +87,8 @@ def load(path: str = LIB_PATH):
         "dspark_schedule": [P, P, I, I, P, I, P, P, P],
         "dspark_accept_label": [P, P, P, P, P, P, P, P, I, P, P, I, I, I, I, F, F, P, P],
         "dspark_sts_fit": [P, P, P, I, I, F, F, P, P, P],
+        "dspark_rnn_draft": [P, P, P, P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P],
+        "dspark_rnn_logits": [P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -245,6 +247,28 @@ def dspark_gated_draft(ctx: Context, U, W1, W2, anchors, h, Wg, d, B, K, V, r, t
         _ptr(tokens, (torch.int32,), "tokens"), _ptr(logprobs, (torch.float32,), "logprobs"),
         _conf_ref(conf), _stream(stream, ctx.device))
     _check(code, "dspark_gated_draft")
+
+
+def dspark_rnn_draft(ctx: Context, U, W1, W2, anchors, h, Wa, Wg, d, B, K, V, r, temperature,
+                     seed, tokens, logprobs, conf: Optional[Confidence] = None, stream=None):
+    code = ctx.lib.dspark_rnn_draft(
+        ctx.handle, _ptr(U, (torch.float32,), "U"), _ptr(W1, _BF16, "W1"),
+        _ptr(W2, _BF16, "W2"), _ptr(anchors, (torch.int32,), "anchors"), _ptr(h, _BF16, "h"),
+        _ptr(Wa, _BF16, "Wa"), _ptr(Wg, _BF16, "Wg"), d, B, K, V, r, float(temperature),
+        int(seed) & (2 ** 64 - 1), _ptr(tokens, (torch.int32,), "tokens"),
+        _ptr(logprobs, (torch.float32,), "logprobs"), _conf_ref(conf), _stream(stream, ctx.device))
+    _check(code, "dspark_rnn_draft")
+
+
+def dspark_rnn_logits(ctx: Context, U, W1, W2, prev_tokens, h, Wa, Wg, d, B, K, V, r, temperature,
+                      logits, lse, stream=None):
+    code = ctx.lib.dspark_rnn_logits(
+        ctx.handle, _ptr(U, (torch.float32,), "U"), _ptr(W1, _BF16, "W1"), _ptr(W2, _BF16, "W2"),
+        _ptr(prev_tokens, (torch.int32,), "prev_tokens"), _ptr(h, _BF16, "h"),
+        _ptr(Wa, _BF16, "Wa"), _ptr(Wg, _BF16, "Wg"), d, B, K, V, r, float(temperature),
+        _ptr(logits, (torch.float32,), "logits"), _ptr(lse, (torch.float32,), "lse"),
+        _stream(stream, ctx.device))
+    _check(code, "dspark_rnn_logits")
 
 
 def dspark_gate(ctx: Context, h, Wg, M, d, r, H, stream=None):
@@ -476,6 +500,36 @@ def schedule(ctx: Context, a, sps, stream=None) -> dict:
     theta = torch.empty(1, dtype=torch.float32, device=a.device)
     dspark_schedule(ctx, a, R, K, sps, ell, theta, stream)
     return dict(ell=ell, theta=theta)
+
+
+def rnn_draft(ctx: Context, U, W1, W2, anchors, h, Wa, *, Wg=None, temperature=1.0, seed=0,
+              conf: Optional[Confidence] = None, stream=None) -> dict:
+    """The RNN head's draft (decay gate from Wa, input gate from Wg or 1); returns tokens and
+    logprobs [B, K] (and the confidence head's outputs when conf is given)."""
+    B, K, V = U.shape
+    r = _rank(W1)
+    tokens = torch.empty(B, K, dtype=torch.int32, device=U.device)
+    logprobs = torch.empty(B, K, dtype=torch.float32, device=U.device)
+    if conf is not None:
+        conf.allocate(B, K)
+    dspark_rnn_draft(ctx, U, W1, W2, anchors, h, Wa, Wg, int(h.shape[-1]), B, K, V, r,
+                     temperature, seed, tokens, logprobs, conf, stream)
+    out = dict(tokens=tokens, logprobs=logprobs)
+    if conf is not None:
+        out.update(conf=conf.conf, cumprod=conf.cumprod, verify_len=conf.verify_len)
+    return out
+
+
+def rnn_logits(ctx: Context, U, W1, W2, prev_tokens, h, Wa, *, Wg=None, temperature=1.0,
+               stream=None) -> dict:
+    """The RNN head's teacher-forced logits [B, K, V] and LSE [B, K]."""
+    B, K, V = U.shape
+    r = _rank(W1)
+    logits = torch.empty(B, K, V, dtype=torch.float32, device=U.device)
+    lse = torch.empty(B, K, dtype=torch.float32, device=U.device)
+    dspark_rnn_logits(ctx, U, W1, W2, prev_tokens, h, Wa, Wg, int(h.shape[-1]), B, K, V, r,
+                      temperature, logits, lse, stream)
+    return dict(logits=logits, lse=lse)
 
 
 def markov_logits(ctx: Context, U, W1, W2, prev_tokens, *, temperature=1.0, h=None, Wg=None,

@@ -28,7 +28,8 @@ struct dspark_ctx {
   uint32_t* d_bar = nullptr;
   unsigned long long* d_keys = nullptr;  // [K_max][128]
   DraftPartial* d_partials = nullptr;    // [K_max][128][num_sms]
-  float* d_H = nullptr;                  // [B_max * K_max][256]
+  float* d_H = nullptr;                  // [B_max * K_max][256] gate (input gate of the RNN head)
+  float* d_A = nullptr;                  // [B_max * K_max][256] decay gate of the RNN head
   float* d_gate_part = nullptr;          // [kGateSplitsMax][B_max * K_max][256]
   int32_t* d_topk_part_i = nullptr;      // [kTopkPartUnits][kMaxTopk] per-piece top-k lists
   // verification scratch
@@ -198,7 +199,7 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
               const int32_t* anchors, const int32_t* prev, const float* H, int B, int K, int V,
               int r, float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
               float* logits, float* lse, const dspark_conf_args* conf, cudaStream_t stream,
-              const LabelIn* lab = nullptr) {
+              const LabelIn* lab = nullptr, const float* Agate = nullptr) {
   const int n_tiles = (V + dspark::kDraftTileN - 1) / dspark::kDraftTileN;
   const int grid = n_tiles < ctx->num_sms ? n_tiles : ctx->num_sms;
   const float inv_t = temperature > 0.f ? 1.0f / temperature : 1.0f;
@@ -232,6 +233,7 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.anchors = anchors + b0;
     p.prev = prev ? prev + static_cast<size_t>(b0) * K : nullptr;
     p.H = H ? H + static_cast<size_t>(b0) * K * r : nullptr;
+    p.A = Agate ? Agate + static_cast<size_t>(b0) * K * r : nullptr;
     p.B = Bc;
     p.K = K;
     p.V = V;
@@ -325,6 +327,28 @@ int check_gate_args(const uint16_t* h, const uint16_t* Wg, int d, int r) {
   return DSPARK_OK;
 }
 
+// Gates of the RNN head into the context: decay a = sigmoid(h . Wa) into d_A, and the
+// input gate g = sigmoid(h . Wg) into d_H when Wg is given (else g = 1: H stays null).
+int run_rnn_gates(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wa, const uint16_t* Wg,
+                  int M, int d, int r, const float** H, cudaStream_t s) {
+  int st = run_gate(ctx, h, Wa, M, d, r, ctx->d_A, s);
+  if (st != DSPARK_OK) return st;
+  *H = nullptr;
+  if (Wg != nullptr) {
+    st = run_gate(ctx, h, Wg, M, d, r, ctx->d_H, s);
+    if (st != DSPARK_OK) return st;
+    *H = ctx->d_H;
+  }
+  return DSPARK_OK;
+}
+
+int check_rnn_args(const uint16_t* h, const uint16_t* Wa, const uint16_t* Wg, int d, int r) {
+  int st = check_gate_args(h, Wa, d, r);
+  if (st != DSPARK_OK) return st;
+  if (Wg != nullptr && (st = check_gate_args(h, Wg, d, r)) != DSPARK_OK) return st;
+  return DSPARK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -374,6 +398,7 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
             cudaMalloc(&ctx->d_partials, sizeof(DraftPartial) * static_cast<size_t>(K_max) *
                                              dspark::kBatchChunk * ctx->num_sms) == cudaSuccess &&
             cudaMalloc(&ctx->d_H, sizeof(float) * rows * dspark::kMaxRank) == cudaSuccess &&
+            cudaMalloc(&ctx->d_A, sizeof(float) * rows * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_gate_part,
                        sizeof(float) * kGateSplitsMax * rows * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_topk_part_i, sizeof(int32_t) * dspark::kTopkPartUnits *
@@ -409,6 +434,7 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_keys);
   cudaFree(ctx->d_partials);
   cudaFree(ctx->d_H);
+  cudaFree(ctx->d_A);
   cudaFree(ctx->d_gate_part);
   cudaFree(ctx->d_topk_part_i);
   cudaFree(ctx->d_v_lse_t);
@@ -639,6 +665,50 @@ int dspark_markov_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, co
   return run_draft(ctx, dspark::kModeTeacherForced, U, W1, W2, prev_tokens, prev_tokens,
                    gated ? ctx->d_H : nullptr, B, K, V, r, temperature, 0, nullptr, nullptr,
                    logits, lse, nullptr, s);
+}
+
+int dspark_rnn_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1, const uint16_t* W2,
+                     const int32_t* anchors, const uint16_t* h, const uint16_t* Wa,
+                     const uint16_t* Wg, int d, int B, int K, int V, int r, float temperature,
+                     uint64_t seed, int32_t* tokens, float* logprobs,
+                     const dspark_conf_args* conf, dspark_stream_t stream) {
+  int st = check_draft_args(U, W1, W2, anchors, B, K, V, r, temperature, tokens, logprobs);
+  if (st != DSPARK_OK) return st;
+  if ((st = check_rnn_args(h, Wa, Wg, d, r)) != DSPARK_OK) return st;
+  if ((st = check_conf(conf, r)) != DSPARK_OK) return st;
+  if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
+  if (K > ctx->K_max || V > ctx->V_max ||
+      static_cast<int64_t>(B) * K > static_cast<int64_t>(ctx->B_max) * ctx->K_max)
+    return DSPARK_ERR_CAPACITY;
+  ctx->last_launches = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float* H = nullptr;
+  if ((st = run_rnn_gates(ctx, h, Wa, Wg, B * K, d, r, &H, s)) != DSPARK_OK) return st;
+  return run_draft(ctx, temperature > 0.f ? dspark::kModeSample : dspark::kModeGreedy, U, W1, W2,
+                   anchors, nullptr, H, B, K, V, r, temperature, seed, tokens, logprobs, nullptr,
+                   nullptr, conf, s, nullptr, ctx->d_A);
+}
+
+int dspark_rnn_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, const uint16_t* W2,
+                      const int32_t* prev_tokens, const uint16_t* h, const uint16_t* Wa,
+                      const uint16_t* Wg, int d, int B, int K, int V, int r, float temperature,
+                      float* logits, float* lse, dspark_stream_t stream) {
+  if (prev_tokens == nullptr) return DSPARK_ERR_INVALID_ARG;
+  int st = check_draft_args(U, W1, W2, prev_tokens, B, K, V, r, temperature, logits, lse);
+  if (st != DSPARK_OK) return st;
+  if ((st = check_rnn_args(h, Wa, Wg, d, r)) != DSPARK_OK) return st;
+  if (!aligned16(logits)) return DSPARK_ERR_INVALID_ARG;
+  if ((st = check_ctx(ctx)) != DSPARK_OK) return st;
+  if (K > ctx->K_max || V > ctx->V_max ||
+      static_cast<int64_t>(B) * K > static_cast<int64_t>(ctx->B_max) * ctx->K_max)
+    return DSPARK_ERR_CAPACITY;
+  ctx->last_launches = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float* H = nullptr;
+  if ((st = run_rnn_gates(ctx, h, Wa, Wg, B * K, d, r, &H, s)) != DSPARK_OK) return st;
+  return run_draft(ctx, dspark::kModeTeacherForced, U, W1, W2, prev_tokens, prev_tokens, H, B, K,
+                   V, r, temperature, 0, nullptr, nullptr, logits, lse, nullptr, s, nullptr,
+                   ctx->d_A);
 }
 
 int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,

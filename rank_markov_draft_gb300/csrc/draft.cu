@@ -217,6 +217,46 @@ __device__ __forceinline__ void load_embedding(const DraftParams& p, int k, int 
   }
 }
 
+// One K chunk of the RNN head's next state, s_k = a_k (.) s_{k-1} + g_k (.) W1[tok]
+// (a_k = A[req, k], g_k = H[req, k] or 1), rounded to bf16 and packed like
+// load_embedding's output.  sp holds the same chunk of s_{k-1} as the previous position's
+// operand (bf16 pairs, read back from TMEM; zeros before position 0): the state is carried
+// as the bf16 MMA operand.  A dead row and elements past r are zero.
+__device__ __forceinline__ void load_rnn_state(const DraftParams& p, int k, int req, bool live,
+                                               int cc, int32_t tok, const uint32_t (&sp)[32],
+                                               uint32_t (&wv)[32]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int kel = cc * 64 + u * 8;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (live && kel < p.r) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel));
+      const float* arow = p.A + (static_cast<size_t>(req) * p.K + k) * p.r + kel;
+      const float4 a0 = __ldg(reinterpret_cast<const float4*>(arow));
+      const float4 a1 = __ldg(reinterpret_cast<const float4*>(arow + 4));
+      float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+      if (p.H != nullptr) {
+        const float* grow = p.H + (static_cast<size_t>(req) * p.K + k) * p.r + kel;
+        g0 = __ldg(reinterpret_cast<const float4*>(grow));
+        g1 = __ldg(reinterpret_cast<const float4*>(grow + 4));
+      }
+      const uint32_t s0 = sp[4 * u], s1 = sp[4 * u + 1], s2 = sp[4 * u + 2], s3 = sp[4 * u + 3];
+      x.x = pack_bf16(fmaf(a0.x, bf16_lo(s0), g0.x * bf16_lo(w.x)),
+                      fmaf(a0.y, bf16_hi(s0), g0.y * bf16_hi(w.x)));
+      x.y = pack_bf16(fmaf(a0.z, bf16_lo(s1), g0.z * bf16_lo(w.y)),
+                      fmaf(a0.w, bf16_hi(s1), g0.w * bf16_hi(w.y)));
+      x.z = pack_bf16(fmaf(a1.x, bf16_lo(s2), g1.x * bf16_lo(w.z)),
+                      fmaf(a1.y, bf16_hi(s2), g1.y * bf16_hi(w.z)));
+      x.w = pack_bf16(fmaf(a1.z, bf16_lo(s3), g1.z * bf16_lo(w.w)),
+                      fmaf(a1.w, bf16_hi(s3), g1.w * bf16_hi(w.w)));
+    }
+    wv[4 * u + 0] = x.x;
+    wv[4 * u + 1] = x.y;
+    wv[4 * u + 2] = x.z;
+    wv[4 * u + 3] = x.w;
+  }
+}
+
 // Score of a key (the ordered float in its middle bits); -inf for "no key".
 __device__ __forceinline__ float key_score(unsigned long long key) {
   if (key == 0ull) return -INFINITY;
@@ -617,9 +657,28 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64), wv0);
       tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32), wv1);
     };
-    auto gather_operand = [&](int kpos, bool live, int32_t tok) {
-      load_embedding(p, kpos, b, live, 2 * g, tok, wv0);
-      load_embedding(p, kpos, b, live, 2 * g + 1, tok, wv1);
+    // the operand of position kpos: the Markov embedding of tok (gated: times H), or the RNN
+    // head's next state; `update` false leaves this lane's registers as they are (the RNN
+    // state's read-back from TMEM is a warp-wide load, so every lane takes part in it)
+    auto gather_operand = [&](int kpos, bool live, int32_t tok, bool update = true) {
+      if (p.A == nullptr) {
+        if (!update) return;
+        load_embedding(p, kpos, b, live, 2 * g, tok, wv0);
+        load_embedding(p, kpos, b, live, 2 * g + 1, tok, wv1);
+        return;
+      }
+      uint32_t sp[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (kpos == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sp[j] = 0u;  // s_{-1} = 0
+        } else {
+          tmem_ld_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32 * half), sp);
+          tmem_wait_ld();
+        }
+        if (update) load_rnn_state(p, kpos, b, live, 2 * g + half, tok, sp, half ? wv1 : wv0);
+      }
     };
     for (int k = 0; k < p.K; ++k) {
       // ---- the step's operand: position 0 is gathered here; later positions were written
@@ -636,15 +695,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
           }
           gather_operand(0, row_ok, tok);
-        } else if (!kTF && row_ok) {
-          const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + b);
-          if (key != spec_key) {  // the winner changed after the speculative gather
-            int32_t tok = key_token(key);
-            if (key_epoch(key) != p.epoch || tok < 0 || tok >= p.V) {
-              record_error(p.status, kStatusDeviceOob);
-              tok = 0;
+        } else if (!kTF) {
+          bool changed = false;
+          int32_t tok = 0;
+          if (row_ok) {
+            const unsigned long long key = __ldcg(p.keys + (k - 1) * kRows + b);
+            if (key != spec_key) {  // the winner changed after the speculative gather
+              changed = true;
+              tok = key_token(key);
+              if (key_epoch(key) != p.epoch || tok < 0 || tok >= p.V) {
+                record_error(p.status, kStatusDeviceOob);
+                tok = 0;
+              }
             }
-            gather_operand(k, true, tok);
+          }
+          if (__any_sync(0xFFFFFFFFu, changed)) {
+            tc_fence_after();
+            gather_operand(k, true, tok, changed);
           }
         }
         store_operand();

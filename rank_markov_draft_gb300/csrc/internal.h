@@ -44,7 +44,8 @@ struct DraftParams {
   const uint16_t* W1;       // [V, r]
   const int32_t* anchors;   // [B] (chunk)
   const int32_t* prev;      // teacher-forced predecessors [B, K] (chunk), or null
-  const float* H;           // gated: [B, K, r] (chunk) fp32, or null
+  const float* H;           // gated: [B, K, r] (chunk) fp32, or null (RNN head: input gate)
+  const float* A;           // RNN head: decay gate [B, K, r] (chunk) fp32, or null
   int B, K, V, r;
   int b_global0;            // index of the chunk's first request in the call (noise key)
   int n_tiles;              // ceil(V / 128)

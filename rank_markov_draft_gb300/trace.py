@@ -1,10 +1,12 @@
 """Phase trace of one draft-kernel launch (dspark_debug_trace), printed per position.
 
-    python -m rank_markov_draft_gb300.trace [--mode sample|greedy|label] [--B 128]
+    python -m rank_markov_draft_gb300.trace [--mode sample|greedy|label] [--B 128] [--gated]
 
 Runs the serving-size workload (K = 16, V = 151936, r = 256) on cuda:0 with
 synthetic inputs: U ~ 3 N(0, 1) with eight boosted tokens per row, weights
-N(0, 0.02) in bf16; for the label mode, target logits = U + N(0, 1).  After
+N(0, 0.02) in bf16; for the label mode, target logits = U + N(0, 1).  --gated
+adds the gate H = sigmoid(h . Wg), h ~ N(0, 1) [B, K, 4096] and Wg ~ N(0, 0.02)
+[4096, 256] (the trace covers the draft kernel, after the gate's kernels).  After
 three untraced calls it arms the trace for one call and prints, per position,
 the median and the largest across CTAs of each phase, then each CTA's spread.
 
@@ -38,6 +40,7 @@ def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--mode", choices=["sample", "greedy", "label"], default="sample")
     ap.add_argument("--B", type=int, default=128)
+    ap.add_argument("--gated", action="store_true")
     args = ap.parse_args()
     B = args.B
     dev = torch.device("cuda", 0)
@@ -59,6 +62,11 @@ def main() -> None:
             call = lambda: binding.accept_label(ctx, P, U, W1, W2, anc, dr["tokens"],
                                                 dr["logprobs"], draft_temperature=1.0,
                                                 target_temperature=1.0)
+        elif args.gated:
+            h = torch.randn(B, K, 4096, device=dev, generator=g).to(torch.bfloat16)
+            Wg = (torch.randn(4096, R, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+            call = lambda: binding.markov_draft(ctx, U, W1, W2, anc, temperature=T, seed=7,
+                                                h=h, Wg=Wg)
         else:
             call = lambda: binding.markov_draft(ctx, U, W1, W2, anc, temperature=T, seed=7)
         for _ in range(3):
@@ -71,7 +79,8 @@ def main() -> None:
     tr = buf.cpu().numpy().reshape(grid, K, SLOTS).astype(np.float64)
     t0 = tr[:, 0, 0][tr[:, 0, 0] > 0].min()
     tr = np.where(tr > 0, (tr - t0) / 1000.0, np.nan)  # microseconds from the first stamp
-    print(f"mode {args.mode}, B = {B}, {grid} CTAs, device status {status}")
+    print(f"mode {args.mode}{' gated' if args.gated else ''}, B = {B}, {grid} CTAs, "
+          f"device status {status}")
     print(f"launch span {np.nanmax(tr):.1f} us (median / largest across CTAs per phase, us)")
     for k in range(K):
         row = tr[:, k, :]
