@@ -60,6 +60,7 @@ WORKLOADS = {
     "serving": (2, "serving batch + confidence: B=128 K=16 V=151936 r=256 d=2048"),
     "single": (1, "single request: B=1 K=16 V=151936 r=256"),
     "gated": (3, "gated head: B=64 K=16 V=151936 r=256 d=4096"),
+    "rnn": (5, "RNN head (decay and input gates from h): B=64 K=16 V=151936 r=256 d=4096"),
     "selector": (4, "selector top-16 (gated): B=256 K=16 V=151936 r=256 d=4096"),
     "tiny": (0, "tiny: B=1 K=4 V=4096 r=256"),
     "verify": (2, "speculative verification of the serving batch: B=128 K=16 V=151936 r=256, "
@@ -127,6 +128,8 @@ def algorithmic_bytes(cfg: int, c: dict) -> int:
         total += B * K * c["d"] * 2
     if c.get("gated"):
         total += B * K * c["d"] * 2 + c["d"] * r * 2
+    if c.get("rnn"):
+        total += c["d"] * r * 2  # the decay gate's weights (h is counted once above)
     return total
 
 
@@ -296,6 +299,18 @@ def oracle_sample(inp, c, n_requests, b0=0, temperature=1.0, seed=0):
     """Run the fp64 oracle on requests b0 .. b0+n-1 of the workload; returns seconds."""
     import oracle
     t0 = time.perf_counter()
+    if c.get("gated"):
+        # the head's gates of the sampled requests, then their draft
+        sl = slice(b0, b0 + n_requests)
+        G = oracle.gate(inp.h[sl], inp.Wg)
+        if c.get("rnn"):
+            A = oracle.gate(inp.h[sl], inp.Wa)
+            out = oracle.rnn_draft(inp.U[sl], inp.W1, inp.W2, inp.anchors[sl], A, G=G,
+                                   temperature=temperature, seed=seed)
+        else:
+            out = oracle.markov_draft(inp.U[sl], inp.W1, inp.W2, inp.anchors[sl],
+                                      temperature=temperature, seed=seed, H=G)
+        return time.perf_counter() - t0
     out = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=temperature,
                               seed=seed, b0=b0, nb=n_requests)
     if c.get("confidence"):
@@ -642,11 +657,15 @@ def run_ours(args, rank, world, local):
                                       threshold=CONF_THRESHOLD).allocate(B, K)
         h = up(inp.h, True) if c.get("gated") else None
         Wg = up(inp.Wg, True) if c.get("gated") else None
+        Wa = up(inp.Wa, True) if c.get("rnn") else None
 
         def step(seed):
             if h is None:
                 binding.dspark_markov_draft(ctx, U, W1, W2, anchors, B, K, V, r, T, seed, tokens,
                                             logprobs, conf, stream)
+            elif Wa is not None:
+                binding.dspark_rnn_draft(ctx, U, W1, W2, anchors, h, Wa, Wg, c["d"], B, K, V, r,
+                                         T, seed, tokens, logprobs, conf, stream)
             else:
                 binding.dspark_gated_draft(ctx, U, W1, W2, anchors, h, Wg, c["d"], B, K, V, r, T,
                                            seed, tokens, logprobs, conf, stream)
@@ -700,13 +719,14 @@ def run_ours(args, rank, world, local):
                            "draw reading the draw rows in place)" if args.workload == "verify" else
                            "label step (target-row scan, per-row offsets, draft kernel in "
                            "label mode)" if args.workload == "label" else
+                           "gates + draft_kernel" if c.get("gated") and cfg != 4 else
                            "draft_kernel" if cfg != 4 else
                            "selector step (top-k scan, gate, pair scores, walk)"),
                 "median_launch_us": round(kernel_ms * 1000, 2)}
 
     # -------- end to end through the binding with host buffers
     e2e = None
-    if not args.skip_e2e and cfg != 4 and args.workload not in ("verify", "label"):
+    if not args.skip_e2e and cfg != 4 and args.workload not in ("verify", "label", "rnn"):
         e2e = run_e2e(args, ctx, inp, c, dev, stream, conf, W1, W2, h, Wg, world)
 
     line = None

@@ -18,6 +18,7 @@ def test_algorithmic_bytes_per_block():
     assert bench.algorithmic_bytes(2, CONFIGS[2]) == 2_498_756_608
     assert bench.algorithmic_bytes(3, CONFIGS[3]) == 1_877_999_616
     assert bench.algorithmic_bytes(4, CONFIGS[4]) == 2_596_536_320
+    assert bench.algorithmic_bytes(5, CONFIGS[5]) == 1_880_096_768  # gated + the decay gate
 
 
 def test_verify_and_label_bytes():
