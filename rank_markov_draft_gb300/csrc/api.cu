@@ -28,15 +28,16 @@ struct dspark_ctx {
   uint32_t* d_bar = nullptr;
   unsigned long long* d_keys = nullptr;  // [K_max][128]
   DraftPartial* d_partials = nullptr;    // [K_max][128][num_sms]
-  float* d_H = nullptr;                  // [B_max * K_max][256] gate (input gate of the RNN head)
-  float* d_A = nullptr;                  // [B_max * K_max][256] decay gate of the RNN head
+  float* d_H = nullptr;                  // [B_max * K_max][256] gate, fp32 (pair scores, preps)
+  uint16_t* d_Hb = nullptr;              // the gate in bf16 for the draft kernel (RNN: input gate)
+  uint16_t* d_Ab = nullptr;              // [B_max * K_max][256] bf16 decay gate of the RNN head
   float* d_gate_part = nullptr;          // [kGateSplitsMax][B_max * K_max][256]
   int32_t* d_topk_part_i = nullptr;      // [kTopkPartUnits][kMaxTopk] per-piece top-k lists
   // verification scratch
   float* d_v_lse_t = nullptr;            // [B_max][K_max + 1]
   int32_t* d_v_argmax_t = nullptr;       // [B_max][K_max + 1]
   dspark::VerifySel* d_v_sel = nullptr;  // [B_max]
-  float* d_v_H = nullptr;                // [B_max][256]
+  uint16_t* d_v_H = nullptr;             // [B_max][256] bf16
   int32_t* d_v_prev = nullptr;           // [B_max]
   dspark::ResRow* d_v_rows = nullptr;    // [B_max]
   // acceptance-label scratch
@@ -149,9 +150,10 @@ int next_epoch(dspark_ctx* ctx, cudaStream_t stream, uint32_t* epoch) {
   return DSPARK_OK;
 }
 
-// Gate prologue into H [M, r] (H may be the context's buffer).
+// Gate prologue into H [M, r] fp32 and/or Hb [M, r] bf16 (either may be null; they may be
+// the context's buffers).
 int run_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int d, int r,
-             float* H, cudaStream_t stream) {
+             float* H, uint16_t* Hb, cudaStream_t stream) {
   GateArgs ga{};
   if (!encode_2d(&ga.tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, static_cast<uint64_t>(d) * 2,
                  64, 128))
@@ -177,7 +179,7 @@ int run_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, int 
   ga.timeout_ns = ctx->timeout_ns;
   cudaError_t e = dspark::launch_gate_gemm(ga, stream);
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  e = dspark::launch_gate_finalize(ctx->d_gate_part, splits, static_cast<int64_t>(M) * r, H,
+  e = dspark::launch_gate_finalize(ctx->d_gate_part, splits, static_cast<int64_t>(M) * r, H, Hb,
                                    stream);
   ctx->last_launches += 2;
   return cuda_status(e);
@@ -196,10 +198,10 @@ struct LabelIn {
 
 // The persistent draft kernel over chunks of 128 requests.
 int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, const uint16_t* W2,
-              const int32_t* anchors, const int32_t* prev, const float* H, int B, int K, int V,
+              const int32_t* anchors, const int32_t* prev, const uint16_t* H, int B, int K, int V,
               int r, float temperature, uint64_t seed, int32_t* tokens, float* logprobs,
               float* logits, float* lse, const dspark_conf_args* conf, cudaStream_t stream,
-              const LabelIn* lab = nullptr, const float* Agate = nullptr) {
+              const LabelIn* lab = nullptr, const uint16_t* Agate = nullptr) {
   const int n_tiles = (V + dspark::kDraftTileN - 1) / dspark::kDraftTileN;
   const int grid = n_tiles < ctx->num_sms ? n_tiles : ctx->num_sms;
   const float inv_t = temperature > 0.f ? 1.0f / temperature : 1.0f;
@@ -327,17 +329,17 @@ int check_gate_args(const uint16_t* h, const uint16_t* Wg, int d, int r) {
   return DSPARK_OK;
 }
 
-// Gates of the RNN head into the context: decay a = sigmoid(h . Wa) into d_A, and the
-// input gate g = sigmoid(h . Wg) into d_H when Wg is given (else g = 1: H stays null).
+// Gates of the RNN head into the context, in bf16: decay a = sigmoid(h . Wa) into d_Ab, and
+// the input gate g = sigmoid(h . Wg) into d_Hb when Wg is given (else g = 1: H stays null).
 int run_rnn_gates(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wa, const uint16_t* Wg,
-                  int M, int d, int r, const float** H, cudaStream_t s) {
-  int st = run_gate(ctx, h, Wa, M, d, r, ctx->d_A, s);
+                  int M, int d, int r, const uint16_t** H, cudaStream_t s) {
+  int st = run_gate(ctx, h, Wa, M, d, r, nullptr, ctx->d_Ab, s);
   if (st != DSPARK_OK) return st;
   *H = nullptr;
   if (Wg != nullptr) {
-    st = run_gate(ctx, h, Wg, M, d, r, ctx->d_H, s);
+    st = run_gate(ctx, h, Wg, M, d, r, nullptr, ctx->d_Hb, s);
     if (st != DSPARK_OK) return st;
-    *H = ctx->d_H;
+    *H = ctx->d_Hb;
   }
   return DSPARK_OK;
 }
@@ -398,7 +400,8 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
             cudaMalloc(&ctx->d_partials, sizeof(DraftPartial) * static_cast<size_t>(K_max) *
                                              dspark::kBatchChunk * ctx->num_sms) == cudaSuccess &&
             cudaMalloc(&ctx->d_H, sizeof(float) * rows * dspark::kMaxRank) == cudaSuccess &&
-            cudaMalloc(&ctx->d_A, sizeof(float) * rows * dspark::kMaxRank) == cudaSuccess &&
+            cudaMalloc(&ctx->d_Hb, sizeof(uint16_t) * rows * dspark::kMaxRank) == cudaSuccess &&
+            cudaMalloc(&ctx->d_Ab, sizeof(uint16_t) * rows * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_gate_part,
                        sizeof(float) * kGateSplitsMax * rows * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_topk_part_i, sizeof(int32_t) * dspark::kTopkPartUnits *
@@ -408,7 +411,7 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
             cudaMalloc(&ctx->d_v_lse_t, sizeof(float) * B_max * (K_max + 1)) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_argmax_t, sizeof(int32_t) * B_max * (K_max + 1)) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_sel, sizeof(dspark::VerifySel) * B_max) == cudaSuccess &&
-            cudaMalloc(&ctx->d_v_H, sizeof(float) * B_max * dspark::kMaxRank) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_H, sizeof(uint16_t) * B_max * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_prev, sizeof(int32_t) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_rows, sizeof(dspark::ResRow) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_prev, sizeof(int32_t) * rows) == cudaSuccess &&
@@ -434,7 +437,8 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_keys);
   cudaFree(ctx->d_partials);
   cudaFree(ctx->d_H);
-  cudaFree(ctx->d_A);
+  cudaFree(ctx->d_Hb);
+  cudaFree(ctx->d_Ab);
   cudaFree(ctx->d_gate_part);
   cudaFree(ctx->d_topk_part_i);
   cudaFree(ctx->d_v_lse_t);
@@ -531,10 +535,10 @@ int dspark_gated_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1, cons
     return DSPARK_ERR_CAPACITY;
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+  st = run_gate(ctx, h, Wg, B * K, d, r, nullptr, ctx->d_Hb, s);
   if (st != DSPARK_OK) return st;
   return run_draft(ctx, temperature > 0.f ? dspark::kModeSample : dspark::kModeGreedy, U, W1, W2,
-                   anchors, nullptr, ctx->d_H, B, K, V, r, temperature, seed, tokens, logprobs,
+                   anchors, nullptr, ctx->d_Hb, B, K, V, r, temperature, seed, tokens, logprobs,
                    nullptr, nullptr, conf, s);
 }
 
@@ -548,7 +552,7 @@ int dspark_gate(dspark_ctx* ctx, const uint16_t* h, const uint16_t* Wg, int M, i
   if (static_cast<int64_t>(M) > static_cast<int64_t>(ctx->B_max) * ctx->K_max)
     return DSPARK_ERR_CAPACITY;
   ctx->last_launches = 0;
-  return run_gate(ctx, h, Wg, M, d, r, H, reinterpret_cast<cudaStream_t>(stream));
+  return run_gate(ctx, h, Wg, M, d, r, H, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dspark_selector_scores(dspark_ctx* ctx, const float* U, const uint16_t* A,
@@ -578,7 +582,7 @@ int dspark_selector_scores(dspark_ctx* ctx, const float* U, const uint16_t* A,
   ctx->last_launches += n_topk;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   if (gated) {
-    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, nullptr, s);
     if (st != DSPARK_OK) return st;
   }
   e = dspark::launch_pair_scores(cand, cand_U, A, Bt, anchors, gated ? ctx->d_H : nullptr, B, K,
@@ -659,11 +663,11 @@ int dspark_markov_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, co
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (gated) {
-    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+    st = run_gate(ctx, h, Wg, B * K, d, r, nullptr, ctx->d_Hb, s);
     if (st != DSPARK_OK) return st;
   }
   return run_draft(ctx, dspark::kModeTeacherForced, U, W1, W2, prev_tokens, prev_tokens,
-                   gated ? ctx->d_H : nullptr, B, K, V, r, temperature, 0, nullptr, nullptr,
+                   gated ? ctx->d_Hb : nullptr, B, K, V, r, temperature, 0, nullptr, nullptr,
                    logits, lse, nullptr, s);
 }
 
@@ -682,11 +686,11 @@ int dspark_rnn_draft(dspark_ctx* ctx, const float* U, const uint16_t* W1, const 
     return DSPARK_ERR_CAPACITY;
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const float* H = nullptr;
+  const uint16_t* H = nullptr;
   if ((st = run_rnn_gates(ctx, h, Wa, Wg, B * K, d, r, &H, s)) != DSPARK_OK) return st;
   return run_draft(ctx, temperature > 0.f ? dspark::kModeSample : dspark::kModeGreedy, U, W1, W2,
                    anchors, nullptr, H, B, K, V, r, temperature, seed, tokens, logprobs, nullptr,
-                   nullptr, conf, s, nullptr, ctx->d_A);
+                   nullptr, conf, s, nullptr, ctx->d_Ab);
 }
 
 int dspark_rnn_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, const uint16_t* W2,
@@ -704,11 +708,11 @@ int dspark_rnn_logits(dspark_ctx* ctx, const float* U, const uint16_t* W1, const
     return DSPARK_ERR_CAPACITY;
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const float* H = nullptr;
+  const uint16_t* H = nullptr;
   if ((st = run_rnn_gates(ctx, h, Wa, Wg, B * K, d, r, &H, s)) != DSPARK_OK) return st;
   return run_draft(ctx, dspark::kModeTeacherForced, U, W1, W2, prev_tokens, prev_tokens, H, B, K,
                    V, r, temperature, 0, nullptr, nullptr, logits, lse, nullptr, s, nullptr,
-                   ctx->d_A);
+                   ctx->d_Ab);
 }
 
 int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_t* W1,
@@ -731,7 +735,7 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (gated) {
-    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, nullptr, s);
     if (st != DSPARK_OK) return st;
   }
   dspark::VerifyArgs v{};
@@ -802,7 +806,7 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
   ctx->last_launches = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (gated) {
-    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, s);
+    st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, ctx->d_Hb, s);
     if (st != DSPARK_OK) return st;
   }
   // the target's normaliser (or argmax) of rows k < K
@@ -837,7 +841,7 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
     LabelIn lab{P, ctx->d_v_lse_t, ctx->d_l_offq2, label,
                 1.4426950408889634f / target_temperature, nullptr};
     st = run_draft(ctx, dspark::kModeLabel, U, W1, W2, anchors, ctx->d_l_prev,
-                   gated ? ctx->d_H : nullptr, B, K, V, r, draft_temperature, 0, nullptr, nullptr,
+                   gated ? ctx->d_Hb : nullptr, B, K, V, r, draft_temperature, 0, nullptr, nullptr,
                    nullptr, nullptr, nullptr, s, &lab);
     if (st != DSPARK_OK) return st;
   }

@@ -175,12 +175,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // row m serving request m mod 64, so that every TMEM lane quadrant holds real rows.
 __device__ __forceinline__ int rows_per_copy(int B) { return B <= 64 ? 64 : kRows; }
 
+// bf16 pair arithmetic on packed 32-bit words (two bf16 each, element 2j in the low half).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// a * s + g * w per element, in fp32, rounded to bf16 (the RNN head's state update).
+__device__ __forceinline__ uint32_t bf16x2_state(uint32_t a, uint32_t s, uint32_t g, uint32_t w) {
+  return pack_bf16(fmaf(bf16_lo(a), bf16_lo(s), bf16_lo(g) * bf16_lo(w)),
+                   fmaf(bf16_hi(a), bf16_hi(s), bf16_hi(g) * bf16_hi(w)));
+}
+
+// The bf16 gate row piece of chunk cc (elements [64 cc, 64 cc + 64)) of request req at
+// position k: eight 16-byte pieces (zeros past r or for a dead row).
+__device__ __forceinline__ void load_gate_chunk(const DraftParams& p, int k, int req, bool live,
+                                                int cc, uint4 (&gv)[8]) {
+  const uint16_t* hrow = p.H + (static_cast<size_t>(req) * p.K + k) * p.r;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int kel = cc * 64 + u * 8;
+    gv[u] = (live && kel < p.r) ? __ldg(reinterpret_cast<const uint4*>(hrow + kel))
+                                : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // One K chunk (elements [64 cc, 64 cc + 64)) of the Markov embedding of token `tok` --
-// gated: times H[req, k] and rounded to bf16 -- packed the way the MMA reads its A
-// operand from TMEM: elements 2j and 2j + 1 of the chunk in column j.  A dead row
-// (no request) and elements past r are zero.
-__device__ __forceinline__ void load_embedding(const DraftParams& p, int k, int req, bool live,
-                                               int cc, int32_t tok, uint32_t (&wv)[32]) {
+// gated (gv given): times the chunk's bf16 gate, rounded to bf16 -- packed the way the
+// MMA reads its A operand from TMEM: elements 2j and 2j + 1 of the chunk in column j.  A
+// dead row (no request) and elements past r are zero.
+__device__ __forceinline__ void load_embedding(const DraftParams& p, bool live, int cc,
+                                               int32_t tok, bool gated, const uint4 (&gv)[8],
+                                               uint32_t (&wv)[32]) {
   uint4 vals[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
@@ -191,21 +218,13 @@ __device__ __forceinline__ void load_embedding(const DraftParams& p, int k, int 
       vals[u] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  if (p.H != nullptr && live) {
-    const float* hrow = p.H + (static_cast<size_t>(req) * p.K + k) * p.r;
+  if (gated) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int kel = cc * 64 + u * 8;
-      if (kel < p.r) {
-        const float4 g0 = __ldg(reinterpret_cast<const float4*>(hrow + kel));
-        const float4 g1 = __ldg(reinterpret_cast<const float4*>(hrow + kel + 4));
-        uint4 x = vals[u];
-        x.x = pack_bf16(bf16_lo(x.x) * g0.x, bf16_hi(x.x) * g0.y);
-        x.y = pack_bf16(bf16_lo(x.y) * g0.z, bf16_hi(x.y) * g0.w);
-        x.z = pack_bf16(bf16_lo(x.z) * g1.x, bf16_hi(x.z) * g1.y);
-        x.w = pack_bf16(bf16_lo(x.w) * g1.z, bf16_hi(x.w) * g1.w);
-        vals[u] = x;
-      }
+      vals[u].x = bf16x2_mul(vals[u].x, gv[u].x);
+      vals[u].y = bf16x2_mul(vals[u].y, gv[u].y);
+      vals[u].z = bf16x2_mul(vals[u].z, gv[u].z);
+      vals[u].w = bf16x2_mul(vals[u].w, gv[u].w);
     }
   }
 #pragma unroll
@@ -218,42 +237,36 @@ __device__ __forceinline__ void load_embedding(const DraftParams& p, int k, int 
 }
 
 // One K chunk of the RNN head's next state, s_k = a_k (.) s_{k-1} + g_k (.) W1[tok]
-// (a_k = A[req, k], g_k = H[req, k] or 1), rounded to bf16 and packed like
+// (a_k = A[req, k], g_k = H[req, k] or 1, both bf16), rounded to bf16 and packed like
 // load_embedding's output.  sp holds the same chunk of s_{k-1} as the previous position's
 // operand (bf16 pairs, read back from TMEM; zeros before position 0): the state is carried
 // as the bf16 MMA operand.  A dead row and elements past r are zero.
 __device__ __forceinline__ void load_rnn_state(const DraftParams& p, int k, int req, bool live,
                                                int cc, int32_t tok, const uint32_t (&sp)[32],
                                                uint32_t (&wv)[32]) {
+  const size_t row = (static_cast<size_t>(req) * p.K + k) * p.r;
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int kel = cc * 64 + u * 8;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (live && kel < p.r) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel));
-      const float* arow = p.A + (static_cast<size_t>(req) * p.K + k) * p.r + kel;
-      const float4 a0 = __ldg(reinterpret_cast<const float4*>(arow));
-      const float4 a1 = __ldg(reinterpret_cast<const float4*>(arow + 4));
-      float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
-      if (p.H != nullptr) {
-        const float* grow = p.H + (static_cast<size_t>(req) * p.K + k) * p.r + kel;
-        g0 = __ldg(reinterpret_cast<const float4*>(grow));
-        g1 = __ldg(reinterpret_cast<const float4*>(grow + 4));
-      }
-      const uint32_t s0 = sp[4 * u], s1 = sp[4 * u + 1], s2 = sp[4 * u + 2], s3 = sp[4 * u + 3];
-      x.x = pack_bf16(fmaf(a0.x, bf16_lo(s0), g0.x * bf16_lo(w.x)),
-                      fmaf(a0.y, bf16_hi(s0), g0.y * bf16_hi(w.x)));
-      x.y = pack_bf16(fmaf(a0.z, bf16_lo(s1), g0.z * bf16_lo(w.y)),
-                      fmaf(a0.w, bf16_hi(s1), g0.w * bf16_hi(w.y)));
-      x.z = pack_bf16(fmaf(a1.x, bf16_lo(s2), g1.x * bf16_lo(w.z)),
-                      fmaf(a1.y, bf16_hi(s2), g1.y * bf16_hi(w.z)));
-      x.w = pack_bf16(fmaf(a1.z, bf16_lo(s3), g1.z * bf16_lo(w.w)),
-                      fmaf(a1.w, bf16_hi(s3), g1.w * bf16_hi(w.w)));
+  for (int half = 0; half < 2; ++half) {  // four 16-byte pieces of each input at a time
+    uint4 w[4], a[4], g[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int kel = cc * 64 + (4 * half + q) * 8;
+      const bool in = live && kel < p.r;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 one = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      w[q] = in ? __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel))
+                : z;
+      a[q] = in ? __ldg(reinterpret_cast<const uint4*>(p.A + row + kel)) : z;
+      g[q] = (in && p.H != nullptr) ? __ldg(reinterpret_cast<const uint4*>(p.H + row + kel)) : one;
     }
-    wv[4 * u + 0] = x.x;
-    wv[4 * u + 1] = x.y;
-    wv[4 * u + 2] = x.z;
-    wv[4 * u + 3] = x.w;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int u = 4 * half + q;
+      wv[4 * u + 0] = bf16x2_state(a[q].x, sp[4 * u + 0], g[q].x, w[q].x);
+      wv[4 * u + 1] = bf16x2_state(a[q].y, sp[4 * u + 1], g[q].y, w[q].y);
+      wv[4 * u + 2] = bf16x2_state(a[q].z, sp[4 * u + 2], g[q].z, w[q].z);
+      wv[4 * u + 3] = bf16x2_state(a[q].w, sp[4 * u + 3], g[q].w, w[q].w);
+    }
   }
 }
 
@@ -364,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   constexpr bool kRace = MODE == kModeSample || MODE == kModeResidual;
   // modes whose per-request winners are published as 64-bit keys
   constexpr bool kKeys = !kTF || MODE == kModeResidual;
+  // modes that can run the RNN head (verification and labels take no decay gate)
+  constexpr bool kRnnOk = !kHalf;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -657,14 +672,26 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64), wv0);
       tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32), wv1);
     };
-    // the operand of position kpos: the Markov embedding of tok (gated: times H), or the RNN
-    // head's next state; `update` false leaves this lane's registers as they are (the RNN
-    // state's read-back from TMEM is a warp-wide load, so every lane takes part in it)
+    // gated head (not the RNN head): the gate row pieces of the operand's next position are
+    // pulled into L1 ahead of the winner's key, so that their loads in gather_operand hit
+    const bool gated_op = p.H != nullptr && (!kRnnOk || p.A == nullptr);
+    auto prefetch_gates = [&](int kpos, bool live) {
+      if (!gated_op || !live) return;
+      const uint16_t* hrow = p.H + (static_cast<size_t>(b) * p.K + kpos) * p.r + 128 * g;
+      if (128 * g < p.r) asm volatile("prefetch.global.L1 [%0];" ::"l"(hrow));
+      if (128 * g + 64 < p.r) asm volatile("prefetch.global.L1 [%0];" ::"l"(hrow + 64));
+    };
+    // the operand of position kpos: the Markov embedding of tok (gated: times the gate), or
+    // the RNN head's next state; `update` false leaves this lane's registers as they are
+    // (the RNN state's read-back from TMEM is a warp-wide load, so every lane takes part)
     auto gather_operand = [&](int kpos, bool live, int32_t tok, bool update = true) {
-      if (p.A == nullptr) {
+      if (!kRnnOk || p.A == nullptr) {
         if (!update) return;
-        load_embedding(p, kpos, b, live, 2 * g, tok, wv0);
-        load_embedding(p, kpos, b, live, 2 * g + 1, tok, wv1);
+        uint4 gv[8];
+        load_gate_chunk(p, kpos, b, live && gated_op, 2 * g, gv);
+        load_embedding(p, live, 2 * g, tok, gated_op, gv, wv0);
+        load_gate_chunk(p, kpos, b, live && gated_op, 2 * g + 1, gv);
+        load_embedding(p, live, 2 * g + 1, tok, gated_op, gv, wv1);
         return;
       }
       uint32_t sp[32];
@@ -1099,35 +1126,41 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       // the global key (read after this CTA's arrival) and this CTA's best; its embedding
       // loads are in flight while the grid barrier completes, and it is written to TMEM
       // (after a re-check of the key) at the start of the next position
-      if (k + 1 < p.K && !fail) {
-        bool ok = mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag);  // MMAs done with E
+      // (The operand registers are written on every path, even past the last position or
+      // after a failure, so that they are plainly dead during the tile sweep.)
+      {
+        const bool next = k + 1 < p.K;
+        bool ok = next && !fail;
+        if (ok) ok = mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag);  // MMAs done with E
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) {
+        if (next && !fail && !ok) {
           fail = true;
           *abort_flag = 1;
-        } else {
-          tc_fence_after();
-          int32_t tok = 0;
-          if (row_ok) {
-            if (kTF) {
-              tok = __ldg(p.prev + static_cast<size_t>(b) * p.K + k + 1);
-              if (tok < 0 || tok >= p.V) {
-                record_error(p.status, kStatusDeviceOob);
-                tok = 0;
-              }
-            } else {
-              const unsigned long long gk = __ldcg(p.keys + k * kRows + b);
-              const unsigned long long lk = s_bound[b];
-              spec_key = (key_epoch(gk) == p.epoch && gk > lk) ? gk : lk;
-              tok = key_token(spec_key);
-              if (key_epoch(spec_key) != p.epoch || tok < 0 || tok >= p.V) {
-                spec_key = ~0ull;  // never matches: gathered again after the barrier
-                tok = 0;
-              }
+        }
+        if (ok) tc_fence_after();
+        const int knext = next ? k + 1 : k;
+        const bool live = ok && row_ok;
+        prefetch_gates(knext, live);
+        int32_t tok = 0;
+        if (live) {
+          if (kTF) {
+            tok = __ldg(p.prev + static_cast<size_t>(b) * p.K + k + 1);
+            if (tok < 0 || tok >= p.V) {
+              record_error(p.status, kStatusDeviceOob);
+              tok = 0;
+            }
+          } else {
+            const unsigned long long gk = __ldcg(p.keys + k * kRows + b);
+            const unsigned long long lk = s_bound[b];
+            spec_key = (key_epoch(gk) == p.epoch && gk > lk) ? gk : lk;
+            tok = key_token(spec_key);
+            if (key_epoch(spec_key) != p.epoch || tok < 0 || tok >= p.V) {
+              spec_key = ~0ull;  // never matches: gathered again after the barrier
+              tok = 0;
             }
           }
-          gather_operand(k + 1, row_ok, tok);
         }
+        gather_operand(knext, live, tok);
       }
 
       // ---- grid barrier (bounded); teacher-forced positions are independent, so

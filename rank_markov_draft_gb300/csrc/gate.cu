@@ -15,6 +15,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cuda_bf16.h>
 
 #include "internal.h"
 #include "sm103.cuh"
@@ -162,9 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1) gate_gemm_kernel(const __grid_con
 }
 
 // H = sigmoid(sum over splits, in split order); n4 float4 per split, all of a
-// thread's split loads in flight before the sum.
+// thread's split loads in flight before the sum.  H (fp32) and Hb (the same values
+// rounded to bf16, for the draft kernel's packed operand arithmetic) are each optional.
 __global__ void gate_finalize_kernel(const float4* __restrict__ partial, int splits, int64_t n4,
-                                     float4* __restrict__ H) {
+                                     float4* __restrict__ H, uint2* __restrict__ Hb) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 pv[8];
@@ -179,8 +181,15 @@ __global__ void gate_finalize_kernel(const float4* __restrict__ partial, int spl
       z.z += pv[s].z;
       z.w += pv[s].w;
     }
-    H[i] = make_float4(1.0f / (1.0f + expf(-z.x)), 1.0f / (1.0f + expf(-z.y)),
-                       1.0f / (1.0f + expf(-z.z)), 1.0f / (1.0f + expf(-z.w)));
+    const float4 g = make_float4(1.0f / (1.0f + expf(-z.x)), 1.0f / (1.0f + expf(-z.y)),
+                                 1.0f / (1.0f + expf(-z.z)), 1.0f / (1.0f + expf(-z.w)));
+    if (H != nullptr) H[i] = g;
+    if (Hb != nullptr) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(g.x, g.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(g.z, g.w);
+      Hb[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                         *reinterpret_cast<const uint32_t*>(&hi));
+    }
   }
 }
 
@@ -197,13 +206,14 @@ cudaError_t launch_gate_gemm(const GateArgs& args, cudaStream_t stream) {
 }
 
 cudaError_t launch_gate_finalize(const float* partial, int splits, int64_t n, float* H,
-                                 cudaStream_t stream) {
+                                 uint16_t* Hb, cudaStream_t stream) {
   // n = M * r is a multiple of 64 (r % 64 == 0) and splits <= 8
   const int64_t n4 = n / 4;
   int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 4096));
   if (blocks < 1) blocks = 1;
   gate_finalize_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(partial), splits,
-                                                   n4, reinterpret_cast<float4*>(H));
+                                                   n4, reinterpret_cast<float4*>(H),
+                                                   reinterpret_cast<uint2*>(Hb));
   return cudaGetLastError();
 }
 

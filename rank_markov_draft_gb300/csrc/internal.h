@@ -44,8 +44,8 @@ struct DraftParams {
   const uint16_t* W1;       // [V, r]
   const int32_t* anchors;   // [B] (chunk)
   const int32_t* prev;      // teacher-forced predecessors [B, K] (chunk), or null
-  const float* H;           // gated: [B, K, r] (chunk) fp32, or null (RNN head: input gate)
-  const float* A;           // RNN head: decay gate [B, K, r] (chunk) fp32, or null
+  const uint16_t* H;        // gated: [B, K, r] (chunk) bf16, or null (RNN head: input gate)
+  const uint16_t* A;        // RNN head: decay gate [B, K, r] (chunk) bf16, or null
   int B, K, V, r;
   int b_global0;            // index of the chunk's first request in the call (noise key)
   int n_tiles;              // ceil(V / 128)
@@ -123,7 +123,7 @@ struct GateArgs {
 };
 cudaError_t launch_gate_gemm(const GateArgs& args, cudaStream_t stream);
 cudaError_t launch_gate_finalize(const float* partial, int splits, int64_t n, float* H,
-                                 cudaStream_t stream);
+                                 uint16_t* Hb, cudaStream_t stream);
 
 // Top-k of each row of U [rows][V] (V a multiple of 4).  part_i / part_v: scratch
 // for up to part_units per-piece lists of kMaxTopk entries (null: whole rows
@@ -169,7 +169,7 @@ struct VerifyArgs {
   float* lse_t;               // [B, K+1]
   int32_t* argmax_t;          // [B, K+1]
   VerifySel* sel;             // [B]
-  float* H_sel;               // [B, r] gate rows at the draw position
+  uint16_t* H_sel;            // [B, r] bf16 gate rows at the draw position
   int32_t* prev_sel;          // [B]
   ResRow* rows;               // [B] the residual mode's per-row constants
 };

@@ -34,6 +34,7 @@
 // 9 + (beta & 3)), words 2h (stage 1) and 2h + 1 (stage 2), h = (beta >> 2) & 1.
 
 #include <cstdint>
+#include <cuda_bf16.h>
 
 #include "headlogit.cuh"
 #include "internal.h"
@@ -228,14 +229,15 @@ __global__ void verify_prep_kernel(const float* __restrict__ U, const uint16_t* 
                                    const float* __restrict__ logq, const float* __restrict__ lse_t,
                                    const VerifySel* __restrict__ sel, int B, int K, int V, int r,
                                    float inv_td, int draft_greedy, ResRow* __restrict__ rows,
-                                   float* __restrict__ H_sel, int32_t* __restrict__ prev_sel) {
+                                   uint16_t* __restrict__ H_sel, int32_t* __restrict__ prev_sel) {
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
   const VerifySel s = sel[b];
   if (H != nullptr) {  // a bonus row needs no q: any valid gate row will do
     const float* hs = H + (static_cast<size_t>(b) * K + min(s.pos, K - 1)) * r;
-    for (int i = lane; i < r; i += 32) H_sel[static_cast<size_t>(b) * r + i] = hs[i];
+    for (int i = lane; i < r; i += 32)
+      H_sel[static_cast<size_t>(b) * r + i] = __bfloat16_as_ushort(__float2bfloat16_rn(hs[i]));
   }
   if (lane == 0) prev_sel[b] = s.prev;
   ResRow rr;
