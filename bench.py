@@ -264,17 +264,27 @@ def measured_peaks():
 _HEADERS = ("sm103.cuh", "philox.cuh", "confidence.cuh", "internal.h")
 PROFILES = {
     "serving": ("draft_kernel_serving.md", ("draft.cu",) + _HEADERS),
+    "single": ("draft_kernel_single.md", ("draft.cu",) + _HEADERS),
     "label": ("label_step_serving.md", ("draft.cu", "label.cu", "verify.cu") + _HEADERS),
     "verify": ("verify_step_serving.md", ("draft.cu", "verify.cu") + _HEADERS),
     "selector": ("topk_stream_kernel_selector.md", ("selector.cu", "gate.cu") + _HEADERS),
 }
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source with its comments and blank space removed (none of the kernel
+    sources holds a string literal with a comment marker), so that editing a comment
+    does not retire a profile taken on the same code."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(workload: str = "serving") -> str:
     h = hashlib.sha256()
     for name in PROFILES[workload][1]:
-        with open(os.path.join(ROOT, "rank_markov_draft_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "rank_markov_draft_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

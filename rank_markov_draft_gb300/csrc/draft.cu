@@ -18,21 +18,25 @@
 //     M = 128 rows and K = 16 costs about the same time for N = 64, 128 or 256,
 //     so the tile is as wide as the tensor memory allows: three 128-column
 //     accumulators plus the 128 columns of the A operand fill the 512 columns;
-//   * warp 0 (one lane) streams W2 with TMA in slices of [128 rows x 128
-//     tokens] (a tile is one slice per 128 of the rank) into a 3-slot ring;
-//     warp 2 (one lane) streams U in 64-token sub-tiles [rows x 64] into its
-//     own ring.  Neither depends on sampled tokens, so both run ahead across
-//     step boundaries, and neither waits for the other's ring;
-//   * warp 1 (one lane) issues tcgen05.mma: D[128 requests x 128 tokens] =
-//     E[128 x r] * W2tile[r x 128] into one of three TMEM accumulators.  E,
-//     the gathered Markov embedding of every request, lives in TMEM (row m in
-//     lane m, two bf16 per column), written there by the epilogue threads
-//     straight from global memory (no shared-memory staging); W2 is the
-//     MN-major slice exactly as TMA wrote it;
-//   * warps 3..18 (the epilogue) read the accumulator (one request per TMEM
-//     lane, 16 tokens of each 64-token sub-tile per thread) and U from shared
-//     memory, and keep, per request, a running log-sum-exp and a running
-//     block-race winner, so the full-vocabulary logits never reach HBM;
+//   * warp 0 (one lane) streams U in 64-token sub-tiles [rows x 64] fp32 with TMA
+//     into its ring (two sub-tiles a tile); it never depends on sampled tokens,
+//     so it runs ahead across step boundaries;
+//   * warp 1 (one lane) streams W2 in slices of [128 rank rows x 128 tokens]
+//     bf16 (a tile is one slice per 128 of the rank) into a 3-slot ring, two
+//     slices ahead of its own MMAs, and issues tcgen05.mma: D[128 requests x
+//     128 tokens] = E[128 x r] * W2tile[r x 128] into one of three TMEM
+//     accumulators.  E, the step's operand for every request (the gathered
+//     Markov embedding, gated or not, or the RNN head's state), lives in TMEM
+//     (row m in lane m, two bf16 per column), written there by the epilogue
+//     threads straight from global memory (no shared-memory staging); W2 is
+//     the MN-major slice exactly as TMA wrote it;
+//   * warps 2..9 (the epilogue, two warps per TMEM lane quadrant) read the
+//     accumulator (one request per TMEM lane, 32 tokens -- two 16-token blocks
+//     -- of each 64-token sub-tile per thread) and U from shared memory, and
+//     keep, per request, a running log-sum-exp and each thread's best block of
+//     the race (its values parked in shared memory), so the full-vocabulary
+//     logits never reach HBM; stage 2 of the race runs once per step per
+//     thread, in that best block;
 //   * at the end of a step each CTA publishes, per request, a 64-bit key
 //     (epoch | ordered score | inverted token id) by atomicMax and its
 //     log-sum-exp partial; it arrives at a bounded grid barrier and, while the
@@ -65,11 +69,11 @@
 //   stage 1, a race between blocks: the block maximising
 //     G = m + log2(s) - log2(E),  E = -ln u1 (a unit exponential)
 //   wins with probability Z_beta / Z (argmax Z_beta / E_beta);
-//   stage 2, only for a block that can still beat the best G any thread has
-//   reached for the request: the first token whose cumulative w exceeds
-//   u2 * s.  Both uniforms of both of a thread's blocks in a tile come from one
-//   Philox call.  The (G, token) winner is merged across threads and CTAs as a
-//   key.
+//   stage 2, once per step in the thread's best block (its 16 weights kept in
+//   shared memory while the sweep goes on): the first token whose cumulative
+//   w exceeds u2 * s.  The four blocks' uniforms of a thread in a tile come
+//   from two interleaved Philox calls.  The (G, token) winner is merged across
+//   threads and CTAs as a key.
 //
 // Every wait is bounded (mbarrier waits and the grid barrier give up after
 // timeout_ns, set the device status word and make the CTA exit cleanly after

@@ -88,3 +88,13 @@ def test_two_rank_timing_reduction_with_gloo():
     # both ranks see the slowest rank's time and the same whole-job throughput
     assert res[0][1] == res[1][1] == 15.0
     assert res[0][2] == res[1][2] == pytest.approx(2 * 128 * 16 * 20 / 0.015)
+
+
+def test_profile_hash_ignores_comments_but_not_code():
+    """A committed ncu summary stays valid across comment edits of the kernel
+    sources and is retired by any change to their code."""
+    src = "int f(int x) {  // doubles x\n  /* body */ return 2 * x;\n}\n"
+    assert bench._code_only(src) == bench._code_only(
+        "// header comment\nint f(int x) {\n  return 2 * x;   /* changed note */\n}\n")
+    assert bench._code_only(src) != bench._code_only("int f(int x) {\n  return 3 * x;\n}\n")
+    assert len(bench.kernel_source_hash("serving")) == 16
