@@ -117,6 +117,15 @@ int dspark_get_status(dspark_ctx* ctx, int* device_status);
  * the knob off and timeout_ms <= 0 restores the default limit (2000 ms). */
 int dspark_debug_set(dspark_ctx* ctx, int cta, int timeout_ms);
 
+/* Testing knob: the next draft-kernel launch through this context asks the
+ * CUDA runtime for 1 KB more dynamic shared memory than the kernel allows, so
+ * the runtime refuses it on the host: the call returns DSPARK_ERR_CUDA, that
+ * launch enqueues nothing, the refusal's error is cleared from the CUDA
+ * runtime's last-error state, and the context stays usable (no reset needed).
+ * Covers one launch.  Source: none on the pages (a test aid for the host-side
+ * error path of a refused launch configuration). */
+int dspark_debug_refuse_next_launch(dspark_ctx* ctx);
+
 /* Profiling knob: the next draft launch (its first 128-request chunk) writes
  * global-timer stamps (ns) of every CTA's step phases into device_buffer,
  * laid out [grid][K][8] as unsigned 64-bit values: slot 0 step start, 1

@@ -18,6 +18,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libdspark.so")
+# the same library with the draft kernel's device-side offset checks compiled in
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libdspark_debug.so")
 
 STATUS = {
     0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_UNSUPPORTED",
@@ -29,7 +31,8 @@ OK, INVALID_ARG, UNSUPPORTED, CUDA, TIMEOUT, DEVICE_OOB, NO_DEVICE, POISONED, CA
 # Functions declared in include/dspark.h (checked against the header by the tests).
 EXPORTS = (
     "dspark_ctx_create", "dspark_ctx_destroy", "dspark_ctx_reset", "dspark_get_status",
-    "dspark_debug_set", "dspark_debug_trace", "dspark_strerror", "dspark_abi_version", "dspark_last_launch_count",
+    "dspark_debug_set", "dspark_debug_refuse_next_launch", "dspark_debug_trace", "dspark_strerror",
+    "dspark_abi_version", "dspark_last_launch_count",
     "dspark_markov_draft", "dspark_gated_draft", "dspark_gate", "dspark_selector_scores",
     "dspark_selector_walk", "dspark_confidence", "dspark_markov_logits",
     "dspark_markov_draft_noalloc", "dspark_verify", "dspark_schedule", "dspark_accept_label",
@@ -52,16 +55,15 @@ class ConfArgs(ctypes.Structure):
     ]
 
 
-_lib = None
+_libs = {}
 
 
 def load(path: str = LIB_PATH):
-    """Load libdspark.so; raise if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load libdspark.so (or its checked twin); raise if it has not been built."""
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
-        raise RuntimeError(f"libdspark.so not found at {path}: build it first "
+        raise RuntimeError(f"{os.path.basename(path)} not found at {path}: build it first "
                            "(python -c 'import __graft_entry__ as g; g.build()')")
     lib = ctypes.CDLL(path)
     P, I, F, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
@@ -71,6 +73,7 @@ def load(path: str = LIB_PATH):
         "dspark_ctx_reset": [P, P],
         "dspark_get_status": [P, ctypes.POINTER(I)],
         "dspark_debug_set": [P, I, I],
+        "dspark_debug_refuse_next_launch": [P],
         "dspark_debug_trace": [P, P, ctypes.c_int64],
         "dspark_strerror": [I],
         "dspark_abi_version": [],
@@ -94,7 +97,7 @@ def load(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_char_p if name == "dspark_strerror" else ctypes.c_int
-    _lib = lib
+    _libs[path] = lib
     return lib
 
 
@@ -139,8 +142,11 @@ def _check(code: int, where: str):
 class Context:
     """A dspark_ctx: per-device scratch for B_max requests, K_max positions, V_max tokens."""
 
-    def __init__(self, device: int = 0, B_max: int = 128, V_max: int = 151936, K_max: int = 16):
-        self.lib = load()
+    def __init__(self, device: int = 0, B_max: int = 128, V_max: int = 151936, K_max: int = 16,
+                 checked: bool = False):
+        # checked: run through libdspark_debug.so, whose draft kernel checks its on-chip
+        # offsets (a failed check is reported as DSPARK_ERR_DEVICE_OOB)
+        self.lib = load(DEBUG_LIB_PATH if checked else LIB_PATH)
         self.device = device
         self.B_max, self.V_max, self.K_max = B_max, V_max, K_max
         h = ctypes.c_void_p()
@@ -177,6 +183,11 @@ class Context:
 
     def debug_set(self, cta: int = -1, timeout_ms: int = 0):
         _check(self.lib.dspark_debug_set(self.handle, cta, timeout_ms), "dspark_debug_set")
+
+    def refuse_next_launch(self):
+        """The next draft-kernel launch is refused by the CUDA runtime (a test aid)."""
+        _check(self.lib.dspark_debug_refuse_next_launch(self.handle),
+               "dspark_debug_refuse_next_launch")
 
     def trace_next(self, buf: Optional[torch.Tensor]):
         """Record the next draft launch's phase stamps into buf (int64, >= grid * K * 8)."""

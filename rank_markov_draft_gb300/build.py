@@ -3,6 +3,10 @@
 Each .cu translation unit is compiled in parallel, then linked into one shared
 library (CUDA runtime linked statically, no libcuda link: the TMA descriptor
 encoder is fetched through the runtime's driver entry-point query).
+
+The same build links libdspark_debug.so: the draft kernel compiled with
+DSPARK_DEVICE_CHECKS (device-side checks of its TMEM and shared-memory
+offsets, reported as DSPARK_ERR_DEVICE_OOB), the other units shared.
 """
 
 from __future__ import annotations
@@ -17,6 +21,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdspark.so")
+LIB_DEBUG = os.path.join(BUILD, "libdspark_debug.so")
+CHECKED = "draft.cu"  # the unit that holds the checks
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "draft.cu", "gate.cu", "selector.cu", "confidence.cu", "noalloc.cu", "verify.cu",
@@ -38,9 +44,9 @@ def _inputs():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(LIB_DEBUG):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(LIB_DEBUG))
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
@@ -52,9 +58,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-diag-suppress", "1160", "-I", INCLUDE]
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, checked = job
+        stem = os.path.splitext(src)[0] + ("_checked" if checked else "")
+        obj = os.path.join(BUILD, stem + ".o")
+        flags = ["-DDSPARK_DEVICE_CHECKS=1"] if checked else []
+        cmd = [cc] + common + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{res.stdout}\n{res.stderr}")
@@ -62,14 +71,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stderr.write(res.stdout + res.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(CHECKED, True)] + [(src, False) for src in SOURCES]  # the longest unit first
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    checked_obj, objs = objs[0], objs[1:]
+    plain = [o for o, src in zip(objs, SOURCES) if src != CHECKED]
+    release = objs
+    debug = plain + [checked_obj]
+    for lib, parts in ((LIB, release), (LIB_DEBUG, debug)):
+        tmp = lib + f".{os.getpid()}.tmp"
+        cmd = [cc] + ARCH + ["-shared", "-o", tmp] + parts + ["-cudart", "static"]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

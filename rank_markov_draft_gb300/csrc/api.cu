@@ -48,6 +48,7 @@ struct dspark_ctx {
   uint32_t epoch = 0;                    // last key epoch used
   int poisoned = 0;
   int debug_skip_cta = -1;
+  bool debug_refuse_launch = false;  // the next draft launch asks for too much shared memory
   uint64_t timeout_ns = dspark::kDefaultTimeoutNs;
   int last_launches = 0;
   unsigned long long* trace = nullptr;  // caller's device buffer for the next draft's phase trace
@@ -293,8 +294,14 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     if (ctx->trace != nullptr &&
         static_cast<int64_t>(grid) * K * dspark::kTraceSlots <= ctx->trace_capacity && b0 == 0)
       p.trace = ctx->trace;
-    cudaError_t e = dspark::launch_draft(args, mode, grid, stream);
-    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    const uint32_t extra = ctx->debug_refuse_launch ? 1024u : 0u;
+    ctx->debug_refuse_launch = false;
+    cudaError_t e = dspark::launch_draft(args, mode, grid, stream, extra);
+    if (e != cudaSuccess) {
+      ctx->debug_skip_cta = -1;
+      ctx->trace = nullptr;
+      return DSPARK_ERR_CUDA;
+    }
     ctx->bar_counter += static_cast<uint32_t>(K) * static_cast<uint32_t>(grid);
     ctx->last_launches += 1;
   }
@@ -468,6 +475,7 @@ int dspark_ctx_reset(dspark_ctx* ctx, dspark_stream_t stream) {
   ctx->epoch = 0;
   ctx->poisoned = 0;
   ctx->debug_skip_cta = -1;
+  ctx->debug_refuse_launch = false;
   ctx->timeout_ns = dspark::kDefaultTimeoutNs;
   return DSPARK_OK;
 }
@@ -489,6 +497,12 @@ int dspark_debug_set(dspark_ctx* ctx, int cta, int timeout_ms) {
   ctx->debug_skip_cta = cta;
   ctx->timeout_ns = timeout_ms > 0 ? static_cast<uint64_t>(timeout_ms) * 1000000ull
                                    : dspark::kDefaultTimeoutNs;
+  return DSPARK_OK;
+}
+
+int dspark_debug_refuse_next_launch(dspark_ctx* ctx) {
+  if (ctx == nullptr) return DSPARK_ERR_INVALID_ARG;
+  ctx->debug_refuse_launch = true;
   return DSPARK_OK;
 }
 

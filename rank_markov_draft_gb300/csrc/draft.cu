@@ -82,6 +82,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "confidence.cuh"
 #include "internal.h"
 #include "philox.cuh"
@@ -138,6 +139,45 @@ static_assert((2 * kNumW2Slots + 2 * kNumUStagesSmall + 2 * kNumAcc + 6) * 8 + 2
                       kRows * 8 + 16 <=
                   kBarRegion,
               "barrier region too small");
+
+// On-chip offset checks of the debug library (compiled away in the release library): a
+// failed check records DSPARK_ERR_DEVICE_OOB and yields the region's first offset, so the
+// access stays in bounds and the launch ends with its status set.
+__device__ __forceinline__ uint32_t tmem_checked(uint32_t addr, uint32_t tmem_base, uint32_t width,
+                                                 uint32_t col_lo, uint32_t col_hi, uint32_t lane0,
+                                                 int* status) {
+  if constexpr (kDeviceChecks) {
+    const uint32_t rel = addr - tmem_base;
+    if (!tmem_span_ok(rel, width, col_lo, col_hi, lane0)) {
+      record_error(status, kStatusDeviceOob);
+      return tmem_base + tmem_or_first(rel, width, col_lo, col_hi, lane0);
+    }
+  }
+  return addr;
+}
+
+__device__ __forceinline__ uint32_t smem_checked(uint32_t off, uint32_t len, uint32_t limit,
+                                                 int* status) {
+  if constexpr (kDeviceChecks) {
+    if (!span_ok(off, len, limit)) {
+      record_error(status, kStatusDeviceOob);
+      return span_or_first(off, len, limit);
+    }
+  }
+  return off;
+}
+
+// (the same for an access that is skipped, not redirected, when its check fails)
+__device__ __forceinline__ bool smem_range_ok(uint32_t off, uint32_t len, uint32_t limit,
+                                              int* status) {
+  if constexpr (kDeviceChecks) {
+    if (!span_ok(off, len, limit)) {
+      record_error(status, kStatusDeviceOob);
+      return false;
+    }
+  }
+  return true;
+}
 
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   const uint32_t b = __float_as_uint(f);
@@ -495,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           if (!ok) break;
           const int x = (t_begin + t) * kTileN + 32 * f;
           if (mine) {
-            uint8_t* dst = sU + su * 2 * ubox + lane * 512;
+            uint8_t* dst = sU + smem_checked(su * 2 * ubox + lane * 512, ubox + 512,
+                                             kNumUStages * kUStageBytes, p.status);
             tma_gather4_2d(dst, &args.tm_u, x, draw_row(0, false), draw_row(1, false),
                            draw_row(2, false), draw_row(3, false), &u_full[su], pol_u);
             tma_gather4_2d(dst + ubox, &args.tm_p, x, draw_row(0, true), draw_row(1, true),
@@ -531,7 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               break;
             }
             mbar_arrive_expect_tx(&u_full[su], u_bytes);
-            uint8_t* dst = sU + su * 2 * ubox;
+            uint8_t* dst = sU + smem_checked(su * 2 * ubox, 2 * ubox, kNumUStages * kUStageBytes,
+                                             p.status);
             if (kHalf) {  // U and target tokens [x, x + 32)
               const int x = (t_begin + t) * kTileN + 32 * f;
               tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
@@ -576,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           return false;
         const int s = j % ns, t = (j / ns) % nt;
         const int v0 = (t_begin + t) * kTileN;
-        uint8_t* dst = sW + slot * kW2SlotBytes;
+        uint8_t* dst = sW + smem_checked(slot * kW2SlotBytes, w_bytes, kNumW2Slots * kW2SlotBytes,
+                                         p.status);
         mbar_arrive_expect_tx(&w_full[slot], w_bytes);
         tma_load_2d(dst, &args.tm_w2, v0, s * kDraftSliceRows, &w_full[slot], pol_w);
         tma_load_2d(dst + sr * 128, &args.tm_w2, v0 + kDraftBoxV, s * kDraftSliceRows,
@@ -603,7 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             mbar_arrive(&acc_full[buf]);  // rank 0: the bias is zero, nothing to multiply
             continue;
           }
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kTileN);
+          const uint32_t d_tmem = tmem_checked(tmem_base + static_cast<uint32_t>(buf * kTileN),
+                                               tmem_base, kTileN, 0, kTmemA, 0, p.status);
           for (int s = 0; s < ns && ok; ++s) {
             const int j = i * ns + s, slot = j % kNumW2Slots;
             if (!mbar_wait(&w_full[slot], (j / kNumW2Slots) & 1, p.timeout_ns, abort_flag,
@@ -616,8 +660,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             const int kk_end = nkk < (s + 1) * 8 ? nkk : (s + 1) * 8;
             for (int kk = s * 8; kk < kk_end; ++kk) {
               const uint64_t bd = smem_desc(b0 + (kk - s * 8) * 2048, lbo, 1024);
-              umma_bf16_ts(d_tmem, tmem_base + kTmemA + static_cast<uint32_t>(kk * 8), bd, idesc,
-                           kk > 0 ? 1u : 0u);
+              const uint32_t a_tmem =
+                  tmem_checked(tmem_base + kTmemA + static_cast<uint32_t>(kk * 8), tmem_base, 8,
+                               kTmemA, kTmemCols, 0, p.status);
+              umma_bf16_ts(d_tmem, a_tmem, bd, idesc, kk > 0 ? 1u : 0u);
             }
             issued_any = true;
             umma_commit(&w_empty[slot]);
@@ -673,8 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     uint32_t wv0[32], wv1[32];
     unsigned long long spec_key = 0ull;  // winner key this thread's row was gathered for
     auto store_operand = [&]() {
-      tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64), wv0);
-      tmem_st_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32), wv1);
+      const uint32_t op = tmem_checked(lane_base + kTmemA + static_cast<uint32_t>(g * 64),
+                                       tmem_base, 64, kTmemA, kTmemCols, q * 32, p.status);
+      tmem_st_x32(op, wv0);
+      tmem_st_x32(op + 32u, wv1);
     };
     // gated head (not the RNN head): the gate row pieces of the operand's next position are
     // pulled into L1 ahead of the winner's key, so that their loads in gather_operand hit
@@ -705,7 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 #pragma unroll
           for (int j = 0; j < 32; ++j) sp[j] = 0u;  // s_{-1} = 0
         } else {
-          tmem_ld_x32(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32 * half), sp);
+          tmem_ld_x32(tmem_checked(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32 * half),
+                                   tmem_base, 32, kTmemA, kTmemCols, q * 32, p.status),
+                      sp);
           tmem_wait_ld();
         }
         if (update) load_rnn_state(p, kpos, b, live, 2 * g + half, tok, sp, half ? wv1 : wv0);
@@ -777,7 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       float best = -INFINITY;
       int best_v = 0;
       uint32_t best_w = 0u;
-      float4* my_best = s_best + etid;
+      // (four float4 planes of kEpiThreads entries: the entry in plane 0 decides)
+      float4* my_best = s_best + smem_checked(static_cast<uint32_t>(etid) * 16u, 16,
+                                              kEpiThreads * 16u, p.status) / 16u;
       // Philox words of this thread's two blocks (2g, 2g + 1 within a sub-tile) of a tile:
       // words 0, 1 serve sub-tile 0, words 2, 3 sub-tile 1; lE = log2(E) of the four blocks
       uint32_t nza[4] = {0u, 0u, 0u, 0u}, nzb[4] = {0u, 0u, 0u, 0u};
@@ -818,8 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           // this sub-tile's 32 accumulator columns (the half-tile modes read them in two
           // 16-column pieces after the ring slots); after the last sub-tile of the tile the
           // buffer goes back
-          const uint32_t acc_col =
-              lane_base + static_cast<uint32_t>(buf * kTileN + sub * kSubV + 32 * g);
+          const uint32_t acc_col = tmem_checked(
+              lane_base + static_cast<uint32_t>(buf * kTileN + sub * kSubV + 32 * g), tmem_base,
+              32, 0, kTmemA, q * 32, p.status);
           uint32_t acc[32];
           if (!kHalf) {
             if (nkk == 0) {
@@ -853,7 +906,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               }
               uint32_t dep = 0u;
               if (h == g) {
-                const uint8_t* row = sU + sh * 2 * ubox + row_off;
+                const uint8_t* row = sU + smem_checked(sh * 2 * ubox + row_off, ubox + 128,
+                                                       kNumUStages * kUStageBytes, p.status);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                   const uint32_t off = static_cast<uint32_t>(u ^ swz) << 4;
@@ -883,7 +937,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               *abort_flag = 1;
               break;
             }
-            const uint8_t* row = sU + su * 2 * ubox + g * ubox + row_off;
+            const uint8_t* row = sU + smem_checked(su * 2 * ubox + g * ubox + row_off, 128,
+                                                   kNumUStages * kUStageBytes, p.status);
             uint32_t dep = 0u;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -1074,7 +1129,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           (kKeys && !kTF && row_ok) ? __ldcg(p.keys + k * kRows + b) : 0ull;
       const float score = yb;
       const int slot = copy * 2 + g;
-      if (!fail) {
+      // the record's five fields, rpc floats apart, inside the merge region
+      const bool rec_ok = smem_range_ok(static_cast<uint32_t>((slot * 5 * rpc + b) * 4),
+                                        static_cast<uint32_t>((4 * rpc + 1) * 4), kMergeBytes,
+                                        p.status);
+      if (!fail && rec_ok) {
         merge[(slot * 5 + 0) * rpc + b] = m2;
         merge[(slot * 5 + 1) * rpc + b] = sum;
         merge[(slot * 5 + 2) * rpc + b] = score;
@@ -1300,7 +1359,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 int draft_smem_bytes() { return static_cast<int>(kSmemBytes); }
 int draft_threads() { return kThreads; }
 
-cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream) {
+cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
+                         uint32_t extra_smem) {
   const void* fn = nullptr;
   const bool copies = args.p.B <= 64;  // small batches fill the MMA rows with copies
   switch (mode) {
@@ -1328,7 +1388,12 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
   void* kargs[] = {const_cast<DraftArgs*>(&args)};
-  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), kargs, kSmemBytes, stream);
+  err = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), kargs, kSmemBytes + extra_smem,
+                                    stream);
+  // a refused launch leaves its (non-sticky) error as the thread's last error: clear it, so
+  // that the caller's next CUDA error check does not see it again
+  if (err != cudaSuccess) (void)cudaGetLastError();
+  return err;
 }
 
 }  // namespace dspark

@@ -110,7 +110,10 @@ enum DraftMode {
 
 int draft_smem_bytes();
 int draft_threads();
-cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream);
+// extra_smem > 0 asks for that much more dynamic shared memory than the kernel allows, which
+// the runtime refuses (the refused-launch test); the refusal's error is cleared before return
+cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
+                         uint32_t extra_smem = 0);
 
 // Gate GEMM: partial[split][m][n] = sum_{j in split} h[m, j] * Wg[j, n].
 struct GateArgs {

@@ -42,6 +42,20 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"{name} declared in dspark.h but not exported"
 
 
+def test_checked_library_loads_and_exports_every_declared_symbol(lib):
+    """libdspark_debug.so (the draft kernel with its on-chip offset checks) is built
+    beside the release library and offers the same boundary."""
+    checked = binding.load(binding.DEBUG_LIB_PATH)
+    assert checked is not lib
+    for name in declared_functions():
+        assert hasattr(checked, name), f"{name} missing from the checked library"
+    assert checked.dspark_abi_version() == lib.dspark_abi_version()
+
+
+def test_refuse_next_launch_needs_a_context(lib):
+    assert lib.dspark_debug_refuse_next_launch(None) == binding.INVALID_ARG
+
+
 def test_abi_version_and_strerror(lib):
     assert lib.dspark_abi_version() == 2
     for code in range(9):
