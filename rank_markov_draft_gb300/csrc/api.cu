@@ -95,6 +95,22 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// U [Bc][K][V] fp32 as [Bc][K][V / 32][32] (V % 32 == 0), boxes of 2 chunks x box_rows rows
+// (at most 64): each box reads 256 contiguous bytes of every row it holds
+bool encode_u_rowpair(CUtensorMap* map, const float* base, int V, int K, int Bc, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {32, static_cast<cuuint64_t>(V) / 32, static_cast<cuuint64_t>(K),
+                              static_cast<cuuint64_t>(Bc)};
+  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(V) * 4,
+                                 static_cast<cuuint64_t>(K) * V * 4};
+  const cuuint32_t box[4] = {32, 2, 1, static_cast<cuuint32_t>(box_rows > 64 ? 64 : box_rows)};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t d0,
                uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
                uint32_t b2, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
@@ -216,6 +232,9 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
       return DSPARK_ERR_CUDA;
     const int box_rows = (Bc + 7) & ~7;
     const bool res = lab != nullptr && lab->rows != nullptr;
+    // row-pair U boxes for the modes that read U alone (not the label pass or the residual
+    // draw, whose slots pair U with the target's rows), where V allows them
+    const bool rowpair = lab == nullptr && V % 32 == 0;
     if (res) {
       // the draw rows are gathered in place: U and the target as plain row arrays
       const uint64_t Kr = static_cast<uint64_t>(lab->res_K);
@@ -223,6 +242,9 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
                      static_cast<uint64_t>(V) * 4, 32, 1) ||
           !encode_2d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, lab->target, V, B * (Kr + 1),
                      static_cast<uint64_t>(V) * 4, 32, 1))
+        return DSPARK_ERR_CUDA;
+    } else if (rowpair) {
+      if (!encode_u_rowpair(&args.tm_u, U + static_cast<size_t>(b0) * K * V, V, K, Bc, box_rows))
         return DSPARK_ERR_CUDA;
     } else {
       const float* Uc = U + static_cast<size_t>(b0) * K * V;
@@ -244,6 +266,7 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
     p.b_global0 = b0;
     p.n_tiles = n_tiles;
     p.box_rows = box_rows;
+    p.u_rowpair = rowpair ? 1 : 0;
     p.inv_t = inv_t;
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);

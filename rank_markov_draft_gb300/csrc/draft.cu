@@ -95,6 +95,7 @@ constexpr int kTileN = kDraftTileN;              // 128 tokens per MMA tile (MMA
 constexpr int kSubV = 64;                        // tokens per epilogue sub-tile (U ring slot)
 constexpr int kRows = kBatchChunk;               // 128 requests (MMA M)
 constexpr int kNumW2Slots = 3;                   // W2 ring: slices of [128 rows x 128 tokens]
+constexpr int kKSlice = kDraftSliceRows / 16;    // MMAs (K = 16 each) per W2 slice
 constexpr int kNumUStages = 3;                   // U ring slots of 32 KB (B > 64)
 constexpr int kNumUStagesSmall = 4;              // slots of 16 KB when B <= 64 (box <= 64 rows)
 constexpr int kNumAcc = 3;                       // TMEM accumulators, 128 columns each
@@ -556,7 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     // ------------------------------------------------------------ U producer
     if (lane == 0) {
       const uint64_t pol_u = l2_policy_evict_first();
-      const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
+      // a fill: 64 tokens of box_rows rows (row-pair boxes: one box of up to 64 rows, or two
+      // of 64 rows, the rows past the batch filled with zeros), or U and target for 32 tokens
+      const bool pair2 = p.u_rowpair && p.box_rows > 64;
+      const uint32_t u_bytes = pair2 ? 2u * 64u * 256u : 2u * static_cast<uint32_t>(p.box_rows) * 128u;
       // fills per tile: two sub-tiles (U boxes of 32 tokens, two per fill), or four half
       // sub-tiles of U and target (label mode)
       constexpr int kFills = kHalf ? 4 : 2;
@@ -578,6 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               const int x = (t_begin + t) * kTileN + 32 * f;
               tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
               tma_load_3d(dst + ubox, &args.tm_p, x, k, 0, &u_full[su], pol_u);
+            } else if (p.u_rowpair) {  // U tokens [x, x + 64): chunks x / 32, x / 32 + 1
+              const int c0 = ((t_begin + t) * kTileN + kSubV * f) / 32;
+              tma_load_4d(dst, &args.tm_u, 0, c0, k, 0, &u_full[su], pol_u);
+              if (pair2) tma_load_4d(dst + 16384, &args.tm_u, 0, c0, k, 64, &u_full[su], pol_u);
             } else {  // U tokens [x, x + 64)
               const int x = (t_begin + t) * kTileN + kSubV * f;
               tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
@@ -657,9 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
             tc_fence_after();
             const uint32_t b0 = smem_addr(sW + slot * kW2SlotBytes);
-            const int kk_end = nkk < (s + 1) * 8 ? nkk : (s + 1) * 8;
-            for (int kk = s * 8; kk < kk_end; ++kk) {
-              const uint64_t bd = smem_desc(b0 + (kk - s * 8) * 2048, lbo, 1024);
+            const int kk_end = nkk < (s + 1) * kKSlice ? nkk : (s + 1) * kKSlice;
+            for (int kk = s * kKSlice; kk < kk_end; ++kk) {
+              const uint64_t bd = smem_desc(b0 + (kk - s * kKSlice) * 2048, lbo, 1024);
               const uint32_t a_tmem =
                   tmem_checked(tmem_base + kTmemA + static_cast<uint32_t>(kk * 8), tmem_base, 8,
                                kTmemA, kTmemCols, 0, p.status);
@@ -708,10 +716,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     const uint32_t b_global = static_cast<uint32_t>(p.b_global0 + b);
     const float scale2 = p.inv_t * kLog2e;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    // this thread's row within a 32-token box of a ring slot (128B swizzle: 16-byte unit u
-    // of row b at unit u ^ (b & 7))
-    const uint32_t row_off = static_cast<uint32_t>(b) * 128u;
-    const uint32_t swz = static_cast<uint32_t>(b & 7);
+    // the 128-byte line of a ring slot that holds this thread's 32 U values (the half-tile
+    // modes: row b of a 32-token box; 32-token boxes: row b of box g; row-pair boxes: chunk
+    // g of row b mod 64 in box b / 64, whose 64-row boxes are 16 KB apart); the 128B
+    // swizzle puts 16-byte unit u of line L at unit u ^ (L & 7)
+    const uint32_t u_line =
+        kHalf ? static_cast<uint32_t>(b)
+              : (p.u_rowpair ? static_cast<uint32_t>((b >> 6) * 128 + 2 * (b & 63) + g)
+                             : static_cast<uint32_t>(g) * (ubox / 128u) + static_cast<uint32_t>(b));
+    const uint32_t row_off = u_line * 128u;
+    const uint32_t swz = u_line & 7u;
     bool fail = false;
     bool aborted = false;
 
@@ -727,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     // gated head (not the RNN head): the gate row pieces of the operand's next position are
     // pulled into L1 ahead of the winner's key, so that their loads in gather_operand hit
     const bool gated_op = p.H != nullptr && (!kRnnOk || p.A == nullptr);
+    const bool rnn_op = kRnnOk && p.A != nullptr;
     auto prefetch_gates = [&](int kpos, bool live) {
       if (!gated_op || !live) return;
       const uint16_t* hrow = p.H + (static_cast<size_t>(b) * p.K + kpos) * p.r + 128 * g;
@@ -839,6 +854,19 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         const int i = k * nt + t;
         const int buf = i % kNumAcc;
         const int tile = t_begin + t;
+        if (kRace && row_ok) {
+          const uint32_t c1 = static_cast<uint32_t>(MODE == kModeResidual ? res_pos : k);
+          const uint32_t tag = (MODE == kModeResidual ? 9u : 1u) + 2u * static_cast<uint32_t>(g);
+          philox4x32_10_rk2(static_cast<uint32_t>(tile), c1, b_global, tag, tag + 1u,
+                            p.round_key0, p.round_key1, nza, nzb);
+          // stage 1's exponentials E = -ln u1 of the thread's blocks, as log2 E (the noise
+          // needs no accumulator: it is drawn while the tile's MMAs may still be running)
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            lE[2 * s] = lg2_approx(neg_log_uniform_fast(nza[2 * s]));
+            lE[2 * s + 1] = lg2_approx(neg_log_uniform_fast(nzb[2 * s]));
+          }
+        }
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
@@ -849,18 +877,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         tc_fence_after();
         if (first && etid == 0) trace_stamp(p, cta, k, 2);
         first = false;
-        if (kRace && row_ok) {
-          const uint32_t c1 = static_cast<uint32_t>(MODE == kModeResidual ? res_pos : k);
-          const uint32_t tag = (MODE == kModeResidual ? 9u : 1u) + 2u * static_cast<uint32_t>(g);
-          philox4x32_10_rk2(static_cast<uint32_t>(tile), c1, b_global, tag, tag + 1u,
-                            p.round_key0, p.round_key1, nza, nzb);
-          // stage 1's exponentials E = -ln u1 of the thread's blocks, as log2 E
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            lE[2 * s] = lg2_approx(neg_log_uniform_fast(nza[2 * s]));
-            lE[2 * s + 1] = lg2_approx(neg_log_uniform_fast(nzb[2 * s]));
-          }
-        }
 #pragma unroll
         for (int s = 0; s < nsub; ++s) {
           if (fail) break;
@@ -937,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               *abort_flag = 1;
               break;
             }
-            const uint8_t* row = sU + smem_checked(su * 2 * ubox + g * ubox + row_off, 128,
+            const uint8_t* row = sU + smem_checked(su * 2 * ubox + row_off, 128,
                                                    kNumUStages * kUStageBytes, p.status);
             uint32_t dep = 0u;
 #pragma unroll
@@ -1158,7 +1174,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         unsigned long long key = 0ull;
         if (kKeys && best_v != 0x7FFFFFFF) {
           key = make_key(p.epoch, best_s, best_v);
-          atomicMax(p.keys + k * kRows + b, key);
+          // a CTA whose best is already beaten by the global key read at the start of the
+          // merge leaves the key alone (keys only grow), which keeps the atomics on the 128
+          // key words of the position from serialising behind every CTA's update
+          if (key > gk_pre) atomicMax(p.keys + k * kRows + b, key);
           s_bound[b] = key;  // the CTA's best: the speculative gather's fallback
           if (!kTF && key > gk_pre && k + 1 < p.K) {
             // this CTA may hold the winner: pull its Markov embedding into L2 so that
@@ -1212,6 +1231,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               record_error(p.status, kStatusDeviceOob);
               tok = 0;
             }
+          } else if (rnn_op) {
+            // the RNN head's next state is made after the barrier: speculating on it costs
+            // the state's read-back and both gates, and misses more often than it hits
+            spec_key = ~0ull;
           } else {
             const unsigned long long gk = __ldcg(p.keys + k * kRows + b);
             const unsigned long long lk = s_bound[b];
@@ -1223,7 +1246,12 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
           }
         }
-        gather_operand(knext, live, tok);
+        if (kTF || !rnn_op) {
+          gather_operand(knext, live, tok);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) wv0[j] = wv1[j] = 0u;
+        }
       }
 
       // ---- grid barrier (bounded); teacher-forced positions are independent, so

@@ -50,6 +50,10 @@ struct DraftParams {
   int b_global0;            // index of the chunk's first request in the call (noise key)
   int n_tiles;              // ceil(V / 128)
   int box_rows;             // rows of the U TMA box (multiple of 8, >= B)
+  // U boxes of row pairs: the map views U as [B][K][V / 32][32] and a box holds 64 tokens
+  // (two 32-token chunks) of up to 64 rows, each row's 256 bytes read contiguously (needs
+  // V % 32 == 0); otherwise boxes of 32 tokens of every row
+  int u_rowpair;
   float inv_t;              // 1 / T' (T' = T, or 1 when greedy)
   uint32_t seed_lo, seed_hi;
   uint32_t round_key0[10];  // Philox key schedule (seed_lo + i * Weyl0), host-computed

@@ -86,7 +86,7 @@ bool encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int rank
             const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint32_t elem[3] = {1, 1, 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};  // rank <= 4
   return fn(map, dt, rank, const_cast<void*>(base), dims, strides, box, elem,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -204,7 +204,18 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, c
         return DSPARK_ERR_CUDA;
     }
     const int box_rows = (Bc + 7) & ~7;
-    {
+    const bool rowpair = V % 32 == 0;  // U boxes of row pairs (256 contiguous bytes a row)
+    if (rowpair) {
+      const cuuint64_t dims[4] = {32, static_cast<cuuint64_t>(V) / 32,
+                                  static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(Bc)};
+      const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(V) * 4,
+                                     static_cast<cuuint64_t>(K) * V * 4};
+      const cuuint32_t box[4] = {32, 2, 1,
+                                 static_cast<cuuint32_t>(box_rows > 64 ? 64 : box_rows)};
+      if (!encode(&args.tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  U + static_cast<size_t>(b0) * K * V, 4, dims, strides, box))
+        return DSPARK_ERR_CUDA;
+    } else {
       const cuuint64_t dims[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(K),
                                   static_cast<cuuint64_t>(Bc)};
       const cuuint64_t strides[2] = {static_cast<cuuint64_t>(V) * 4,
@@ -224,6 +235,7 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, c
     p.b_global0 = b0;
     p.n_tiles = n_tiles;
     p.box_rows = box_rows;
+    p.u_rowpair = rowpair ? 1 : 0;
     p.inv_t = inv_t;
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);

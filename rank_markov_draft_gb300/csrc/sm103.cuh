@@ -171,6 +171,17 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, int32_t z, int32_t w, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
+      "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Four rows y0..y3 of a 2-D tensor map whose box is one row high, columns [x, x + box
 // width), landing one after another at smem_dst (tile::gather4); x * element size a
 // multiple of 16 bytes, the rows in range.
