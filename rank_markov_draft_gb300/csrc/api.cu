@@ -95,8 +95,9 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// U [Bc][K][V] fp32 as [Bc][K][V / 32][32] (V % 32 == 0), boxes of 2 chunks x box_rows rows
-// (at most 64): each box reads 256 contiguous bytes of every row it holds
+// A [Bc][K][V] fp32 array (U, or the target's [Bc][K + 1][V]) as [Bc][K][V / 32][32]
+// (V % 32 == 0), boxes of 2 chunks x min(box_rows, 64) rows: each box reads 256 contiguous
+// bytes of every row it holds
 bool encode_u_rowpair(CUtensorMap* map, const float* base, int V, int K, int Bc, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
@@ -232,9 +233,11 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
       return DSPARK_ERR_CUDA;
     const int box_rows = (Bc + 7) & ~7;
     const bool res = lab != nullptr && lab->rows != nullptr;
-    // row-pair U boxes for the modes that read U alone (not the label pass or the residual
-    // draw, whose slots pair U with the target's rows), where V allows them
-    const bool rowpair = lab == nullptr && V % 32 == 0;
+    // row-pair U boxes (256 contiguous bytes a row and box, against 128 for 32-token boxes:
+    // the U stream reaches about 6.3 TB/s instead of 4.5) where V allows them: for the label
+    // pass, and for the modes that read U alone above 64 requests (at 64 or fewer the batch
+    // copies' 32-token boxes measured faster); not for the residual draw's gathered rows
+    const bool rowpair = V % 32 == 0 && (lab != nullptr ? !res : Bc > 64);
     if (res) {
       // the draw rows are gathered in place: U and the target as plain row arrays
       const uint64_t Kr = static_cast<uint64_t>(lab->res_K);
@@ -244,7 +247,9 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
                      static_cast<uint64_t>(V) * 4, 32, 1))
         return DSPARK_ERR_CUDA;
     } else if (rowpair) {
-      if (!encode_u_rowpair(&args.tm_u, U + static_cast<size_t>(b0) * K * V, V, K, Bc, box_rows))
+      // (the label pass's fills take rows [0, 64) and [64, 128) in turn: 64-row boxes)
+      if (!encode_u_rowpair(&args.tm_u, U + static_cast<size_t>(b0) * K * V, V, K, Bc,
+                            lab != nullptr ? 64 : box_rows))
         return DSPARK_ERR_CUDA;
     } else {
       const float* Uc = U + static_cast<size_t>(b0) * K * V;
@@ -283,9 +288,10 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
         p.res_K = lab->res_K;
       } else {
         const float* tchunk = lab->target + static_cast<size_t>(b0) * (K + 1) * V;
-        if (!encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tchunk, V, K + 1, Bc,
-                       static_cast<uint64_t>(V) * 4, static_cast<uint64_t>(K + 1) * V * 4, 32,
-                       1, box_rows))
+        if (rowpair ? !encode_u_rowpair(&args.tm_p, tchunk, V, K + 1, Bc, 64)
+                    : !encode_3d(&args.tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tchunk, V, K + 1,
+                                 Bc, static_cast<uint64_t>(V) * 4,
+                                 static_cast<uint64_t>(K + 1) * V * 4, 32, 1, box_rows))
           return DSPARK_ERR_CUDA;
         p.target = tchunk;
         p.lse_t = lab->lse_t + static_cast<size_t>(b0) * (K + 1);

@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       const uint64_t pol_u = l2_policy_evict_first();
       // a fill: 64 tokens of box_rows rows (row-pair boxes: one box of up to 64 rows, or two
       // of 64 rows, the rows past the batch filled with zeros), or U and target for 32 tokens
-      const bool pair2 = p.u_rowpair && p.box_rows > 64;
+      const bool pair2 = p.u_rowpair && (kHalf || p.box_rows > 64);
       const uint32_t u_bytes = pair2 ? 2u * 64u * 256u : 2u * static_cast<uint32_t>(p.box_rows) * 128u;
       // fills per tile: two sub-tiles (U boxes of 32 tokens, two per fill), or four half
       // sub-tiles of U and target (label mode)
@@ -578,7 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             mbar_arrive_expect_tx(&u_full[su], u_bytes);
             uint8_t* dst = sU + smem_checked(su * 2 * ubox, 2 * ubox, kNumUStages * kUStageBytes,
                                              p.status);
-            if (kHalf) {  // U and target tokens [x, x + 32)
+            if (kHalf && p.u_rowpair) {  // U and target tokens [x, x + 64), rows [64 h, +64)
+              const int c0 = ((t_begin + t) * kTileN + kSubV * (f >> 1)) / 32, h = f & 1;
+              tma_load_4d(dst, &args.tm_u, 0, c0, k, 64 * h, &u_full[su], pol_u);
+              tma_load_4d(dst + ubox, &args.tm_p, 0, c0, k, 64 * h, &u_full[su], pol_u);
+            } else if (kHalf) {  // U and target tokens [x, x + 32)
               const int x = (t_begin + t) * kTileN + 32 * f;
               tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
               tma_load_3d(dst + ubox, &args.tm_p, x, k, 0, &u_full[su], pol_u);
@@ -720,10 +724,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     // modes: row b of a 32-token box; 32-token boxes: row b of box g; row-pair boxes: chunk
     // g of row b mod 64 in box b / 64, whose 64-row boxes are 16 KB apart); the 128B
     // swizzle puts 16-byte unit u of line L at unit u ^ (L & 7)
+    // (the label pass with row-pair boxes: a fill holds 64 tokens of U and of the target for
+    // rows [64 h, 64 h + 64), U's 64-row box then the target's, 16 KB apart; a thread reads
+    // fill h = b / 64, line 2 (b mod 64) + g)
     const uint32_t u_line =
-        kHalf ? static_cast<uint32_t>(b)
+        kHalf ? (p.u_rowpair ? static_cast<uint32_t>(2 * (b & 63) + g) : static_cast<uint32_t>(b))
               : (p.u_rowpair ? static_cast<uint32_t>((b >> 6) * 128 + 2 * (b & 63) + g)
                              : static_cast<uint32_t>(g) * (ubox / 128u) + static_cast<uint32_t>(b));
+    const int u_fill = (kHalf && p.u_rowpair) ? (b >> 6) : g;  // the half-tile fill it reads
     const uint32_t row_off = u_line * 128u;
     const uint32_t swz = u_line & 7u;
     bool fail = false;
@@ -907,7 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           float uval[32], pt[32];
           if (kHalf) {
             // half sub-tiles: fill 2 jsub + h holds U and the target for tokens
-            // [32 h, 32 h + 32); this thread reads half g, every warp takes and releases
+            // [32 h, 32 h + 32) of every row (row-pair boxes: 64 tokens of rows
+            // [64 h, 64 h + 64)); this thread reads fill u_fill, every warp takes and releases
             // both, so each slot keeps one group of readers taking its fills in order
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -921,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                 break;
               }
               uint32_t dep = 0u;
-              if (h == g) {
+              if (h == u_fill) {
                 const uint8_t* row = sU + smem_checked(sh * 2 * ubox + row_off, ubox + 128,
                                                        kNumUStages * kUStageBytes, p.status);
 #pragma unroll

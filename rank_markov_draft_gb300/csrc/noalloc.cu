@@ -204,7 +204,8 @@ extern "C" int dspark_markov_draft_noalloc(const float* U, const uint16_t* W1, c
         return DSPARK_ERR_CUDA;
     }
     const int box_rows = (Bc + 7) & ~7;
-    const bool rowpair = V % 32 == 0;  // U boxes of row pairs (256 contiguous bytes a row)
+    // U boxes of row pairs (256 contiguous bytes a row) above 64 requests
+    const bool rowpair = V % 32 == 0 && Bc > 64;
     if (rowpair) {
       const cuuint64_t dims[4] = {32, static_cast<cuuint64_t>(V) / 32,
                                   static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(Bc)};
