@@ -281,6 +281,40 @@ __device__ __forceinline__ void load_embedding(const DraftParams& p, bool live, 
   }
 }
 
+// The gated operand in two steps, so that the gate rows -- known before the winner is --
+// load while the winner's key is read: the chunk's gate, packed like load_embedding's output,
+// then (gate_times_embedding) its product with the chunk of W1[tok], rounded to bf16.
+__device__ __forceinline__ void load_gate_packed(const DraftParams& p, int k, int req, bool live,
+                                                 int cc, uint32_t (&wv)[32]) {
+  uint4 gv[8];
+  load_gate_chunk(p, k, req, live, cc, gv);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    wv[4 * u + 0] = gv[u].x;
+    wv[4 * u + 1] = gv[u].y;
+    wv[4 * u + 2] = gv[u].z;
+    wv[4 * u + 3] = gv[u].w;
+  }
+}
+
+__device__ __forceinline__ void gate_times_embedding(const DraftParams& p, bool live, int cc,
+                                                     int32_t tok, uint32_t (&wv)[32]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int kel = cc * 64 + u * 8;
+    if (live && kel < p.r) {
+      const uint4 v =
+          __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel));
+      wv[4 * u + 0] = bf16x2_mul(v.x, wv[4 * u + 0]);
+      wv[4 * u + 1] = bf16x2_mul(v.y, wv[4 * u + 1]);
+      wv[4 * u + 2] = bf16x2_mul(v.z, wv[4 * u + 2]);
+      wv[4 * u + 3] = bf16x2_mul(v.w, wv[4 * u + 3]);
+    } else {
+      wv[4 * u + 0] = wv[4 * u + 1] = wv[4 * u + 2] = wv[4 * u + 3] = 0u;
+    }
+  }
+}
+
 // One K chunk of the RNN head's next state, s_k = a_k (.) s_{k-1} + g_k (.) W1[tok]
 // (a_k = A[req, k], g_k = H[req, k] or 1, both bf16), rounded to bf16 and packed like
 // load_embedding's output.  sp holds the same chunk of s_{k-1} as the previous position's
@@ -411,7 +445,9 @@ __device__ __forceinline__ float sum16(const float* w) {
   return s0.x + s0.y;
 }
 
-template <int MODE, bool COPIES>
+// GATED: the launch may carry a gate (gated head) or decay and input gates (RNN head); the
+// plain instantiations compile the operand path without them
+template <int MODE, bool COPIES, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
   // teacher-forced modes take the predecessors from the caller
@@ -748,8 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     };
     // gated head (not the RNN head): the gate row pieces of the operand's next position are
     // pulled into L1 ahead of the winner's key, so that their loads in gather_operand hit
-    const bool gated_op = p.H != nullptr && (!kRnnOk || p.A == nullptr);
-    const bool rnn_op = kRnnOk && p.A != nullptr;
+    const bool gated_op = GATED && p.H != nullptr && (!kRnnOk || p.A == nullptr);
+    const bool rnn_op = GATED && kRnnOk && p.A != nullptr;
     auto prefetch_gates = [&](int kpos, bool live) {
       if (!gated_op || !live) return;
       const uint16_t* hrow = p.H + (static_cast<size_t>(b) * p.K + kpos) * p.r + 128 * g;
@@ -760,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     // the RNN head's next state; `update` false leaves this lane's registers as they are
     // (the RNN state's read-back from TMEM is a warp-wide load, so every lane takes part)
     auto gather_operand = [&](int kpos, bool live, int32_t tok, bool update = true) {
-      if (!kRnnOk || p.A == nullptr) {
+      if (!rnn_op) {
         if (!update) return;
         uint4 gv[8];
         load_gate_chunk(p, kpos, b, live && gated_op, 2 * g, gv);
@@ -1231,7 +1267,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (ok) tc_fence_after();
         const int knext = next ? k + 1 : k;
         const bool live = ok && row_ok;
-        prefetch_gates(knext, live);
+        // the gated head's sampled operand: its gate rows load before the key read
+        const bool gate_first = gated_op && !kTF;
+        if (gate_first) {
+          load_gate_packed(p, knext, b, live, 2 * g, wv0);
+          load_gate_packed(p, knext, b, live, 2 * g + 1, wv1);
+        } else {
+          prefetch_gates(knext, live);
+        }
         int32_t tok = 0;
         if (live) {
           if (kTF) {
@@ -1255,7 +1298,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
           }
         }
-        if (kTF || !rnn_op) {
+        if (gate_first) {
+          gate_times_embedding(p, live, 2 * g, tok, wv0);
+          gate_times_embedding(p, live, 2 * g + 1, tok, wv1);
+        } else if (kTF || !rnn_op) {
           gather_operand(knext, live, tok);
         } else {
 #pragma unroll
@@ -1400,27 +1446,36 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
                          uint32_t extra_smem) {
   const void* fn = nullptr;
   const bool copies = args.p.B <= 64;  // small batches fill the MMA rows with copies
+  const bool gated = args.p.H != nullptr || args.p.A != nullptr;
+  // the drafting modes come in plain and gated builds; the parity, label and residual modes
+  // take their gates at run time
+#define DSPARK_DRAFT_FN(M, C, G) reinterpret_cast<const void*>(&draft_kernel<M, C, G>)
   switch (mode) {
     case kModeSample:
-      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeSample, true>)
-                  : reinterpret_cast<const void*>(&draft_kernel<kModeSample, false>);
+      fn = copies ? (gated ? DSPARK_DRAFT_FN(kModeSample, true, true)
+                           : DSPARK_DRAFT_FN(kModeSample, true, false))
+                  : (gated ? DSPARK_DRAFT_FN(kModeSample, false, true)
+                           : DSPARK_DRAFT_FN(kModeSample, false, false));
       break;
     case kModeGreedy:
-      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeGreedy, true>)
-                  : reinterpret_cast<const void*>(&draft_kernel<kModeGreedy, false>);
+      fn = copies ? (gated ? DSPARK_DRAFT_FN(kModeGreedy, true, true)
+                           : DSPARK_DRAFT_FN(kModeGreedy, true, false))
+                  : (gated ? DSPARK_DRAFT_FN(kModeGreedy, false, true)
+                           : DSPARK_DRAFT_FN(kModeGreedy, false, false));
       break;
     case kModeTeacherForced:
-      fn = copies ? reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, true>)
-                  : reinterpret_cast<const void*>(&draft_kernel<kModeTeacherForced, false>);
+      fn = copies ? DSPARK_DRAFT_FN(kModeTeacherForced, true, true)
+                  : DSPARK_DRAFT_FN(kModeTeacherForced, false, true);
       break;
     case kModeLabel:  // half-sub-tile ring slots: always the 128-row instantiation
-      fn = reinterpret_cast<const void*>(&draft_kernel<kModeLabel, false>);
+      fn = DSPARK_DRAFT_FN(kModeLabel, false, true);
       break;
     case kModeResidual:
-      fn = reinterpret_cast<const void*>(&draft_kernel<kModeResidual, false>);
+      fn = DSPARK_DRAFT_FN(kModeResidual, false, true);
       break;
     default: return cudaErrorInvalidValue;
   }
+#undef DSPARK_DRAFT_FN
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
