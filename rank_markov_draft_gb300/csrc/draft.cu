@@ -349,6 +349,69 @@ __device__ __forceinline__ void load_rnn_state(const DraftParams& p, int k, int 
   }
 }
 
+// The RNN head's drafted update in two steps around the grid barrier.  Before it, for one K
+// chunk: t = a_{k} (.) s_{k-1} (exact in fp32: both factors are bf16) into 64 TMEM columns at
+// taddr (element e in column e), and the input gate g_k (1 without one) packed into gw.  After
+// it (rnn_finish_chunk): s_k = bf16(t + g_k (.) W1[tok]), the value load_rnn_state makes.
+__device__ __forceinline__ void rnn_decay_chunk(const DraftParams& p, int k, int req, bool live,
+                                                int cc, const uint32_t (&sp)[32], uint32_t taddr,
+                                                uint32_t (&gw)[32]) {
+  const size_t row = (static_cast<size_t>(req) * p.K + k) * p.r;
+#pragma unroll
+  for (int piece = 0; piece < 2; ++piece) {
+    uint32_t t[32];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int kel = cc * 64 + (4 * piece + qq) * 8;
+      const bool in = live && kel < p.r;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 one = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      const uint4 a = in ? __ldg(reinterpret_cast<const uint4*>(p.A + row + kel)) : z;
+      const uint4 g = in ? (p.H != nullptr ? __ldg(reinterpret_cast<const uint4*>(p.H + row + kel))
+                                           : one)
+                         : z;
+      const int j0 = 16 * piece + 4 * qq;
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        t[8 * qq + 2 * c] = __float_as_uint(bf16_lo(av[c]) * bf16_lo(sp[j0 + c]));
+        t[8 * qq + 2 * c + 1] = __float_as_uint(bf16_hi(av[c]) * bf16_hi(sp[j0 + c]));
+        gw[j0 + c] = gv[c];
+      }
+    }
+    tmem_st_x32(taddr + static_cast<uint32_t>(32 * piece), t);
+  }
+}
+
+// (All lanes take part: the TMEM loads are warp-wide; `update` false leaves gw as it is.)
+__device__ __forceinline__ void rnn_finish_chunk(const DraftParams& p, bool update, int cc,
+                                                 int32_t tok, uint32_t taddr, uint32_t (&wv)[32]) {
+#pragma unroll
+  for (int piece = 0; piece < 2; ++piece) {
+    uint32_t t[32];
+    tmem_ld_x32(taddr + static_cast<uint32_t>(32 * piece), t);
+    tmem_wait_ld();
+    if (!update) continue;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int kel = cc * 64 + (4 * piece + qq) * 8;
+      const uint4 w =
+          kel < p.r
+              ? __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.r + kel))
+              : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t wvv[4] = {w.x, w.y, w.z, w.w};
+      const int j0 = 16 * piece + 4 * qq;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t g = wv[j0 + c];
+        wv[j0 + c] = pack_bf16(
+            fmaf(bf16_lo(g), bf16_lo(wvv[c]), __uint_as_float(t[8 * qq + 2 * c])),
+            fmaf(bf16_hi(g), bf16_hi(wvv[c]), __uint_as_float(t[8 * qq + 2 * c + 1])));
+      }
+    }
+  }
+}
+
 // Score of a key (the ordered float in its middle bits); -inf for "no key".
 __device__ __forceinline__ float key_score(unsigned long long key) {
   if (key == 0ull) return -INFINITY;
@@ -849,7 +912,17 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
               }
             }
           }
-          if (__any_sync(0xFFFFFFFFu, changed)) {
+          if (rnn_op && !kTF) {
+            // the RNN head's state: the decayed part made before the barrier, plus the input
+            // (every live row: its state is never speculated)
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+              rnn_finish_chunk(p, changed, 2 * g + half, tok,
+                               tmem_checked(lane_base + static_cast<uint32_t>(g * 128 + 64 * half),
+                                            tmem_base, 64, 0, kTmemA, q * 32, p.status),
+                               half ? wv1 : wv0);
+          } else if (__any_sync(0xFFFFFFFFu, changed)) {
             tc_fence_after();
             gather_operand(k, true, tok, changed);
           }
@@ -1269,9 +1342,31 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         const bool live = ok && row_ok;
         // the gated head's sampled operand: its gate rows load before the key read
         const bool gate_first = gated_op && !kTF;
+        const bool rnn_first = rnn_op && !kTF;
         if (gate_first) {
           load_gate_packed(p, knext, b, live, 2 * g, wv0);
           load_gate_packed(p, knext, b, live, 2 * g + 1, wv1);
+        } else if (rnn_first) {
+          // the decayed state into this row's accumulator columns [128 g, 128 g + 128): every
+          // MMA of the position is done (a_empty) and every accumulator read
+          if (ok) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t sp[32];
+              tmem_ld_x32(tmem_checked(lane_base + kTmemA + static_cast<uint32_t>(g * 64 + 32 * half),
+                                       tmem_base, 32, kTmemA, kTmemCols, q * 32, p.status),
+                          sp);
+              tmem_wait_ld();
+              rnn_decay_chunk(p, knext, b, live, 2 * g + half, sp,
+                              tmem_checked(lane_base + static_cast<uint32_t>(g * 128 + 64 * half),
+                                           tmem_base, 64, 0, kTmemA, q * 32, p.status),
+                              half ? wv1 : wv0);
+            }
+            tmem_wait_st();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) wv0[j] = wv1[j] = 0u;
+          }
         } else {
           prefetch_gates(knext, live);
         }
@@ -1303,9 +1398,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           gate_times_embedding(p, live, 2 * g + 1, tok, wv1);
         } else if (kTF || !rnn_op) {
           gather_operand(knext, live, tok);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) wv0[j] = wv1[j] = 0u;
         }
       }
 
