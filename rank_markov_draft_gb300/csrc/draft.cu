@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], kEpiWarps);  // every epilogue warp reads every accumulator
     }
-    mbar_init(a_full, 1);
+    mbar_init(a_full, kEpiWarps);  // every epilogue warp's operand rows are in TMEM
     mbar_init(a_empty, 1);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
@@ -927,16 +927,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             gather_operand(k, true, tok, changed);
           }
         }
-        store_operand();
+        // (teacher-forced modes wrote the operand of positions k > 0 during the previous
+        // position's last tile)
+        if (!kTF || k == 0) store_operand();
       }
       tmem_wait_st();
       tc_fence_before();
       if (etid < kRows) s_bound[etid] = 0ull;
       named_bar_sync(kEpiBarrier, kEpiThreads);
-      if (etid == 0) {
-        mbar_arrive(a_full);
-        trace_stamp(p, cta, k, 1);
-      }
+      if (lane == 0 && (!kTF || k == 0)) mbar_arrive(a_full);
+      if (etid == 0) trace_stamp(p, cta, k, 1);
 
       // ---- stream the step's tiles
       float m2 = (MODE == kModeLabel) ? 0.f : -INFINITY, sum = 0.f;  // label: a plain sum
@@ -983,6 +983,33 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             lE[2 * s] = lg2_approx(neg_log_uniform_fast(nza[2 * s]));
             lE[2 * s + 1] = lg2_approx(neg_log_uniform_fast(nzb[2 * s]));
           }
+        }
+        if (kTF && t == nt - 1 && k + 1 < p.K) {
+          // teacher-forced: the predecessors are known, so the next position's operand goes to
+          // TMEM as soon as this position's MMAs are done with it (their last tile's), and the
+          // MMAs of the next position start while this one's last tile, merge and partial run
+          bool oka = mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag);
+          oka = __all_sync(0xFFFFFFFFu, oka);
+          if (!oka) {
+            fail = true;
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          int32_t tok = 0;
+          if (row_ok) {
+            tok = __ldg(p.prev + static_cast<size_t>(b) * p.K + k + 1);
+            if (tok < 0 || tok >= p.V) {
+              record_error(p.status, kStatusDeviceOob);
+              tok = 0;
+            }
+          }
+          gather_operand(k + 1, row_ok, tok);
+          store_operand();
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(a_full);
         }
         bool ok = mbar_wait(&acc_full[buf], (i / kNumAcc) & 1, p.timeout_ns, abort_flag);
         ok = __all_sync(0xFFFFFFFFu, ok);
@@ -1329,7 +1356,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       // (The operand registers are written on every path, even past the last position or
       // after a failure, so that they are plainly dead during the tile sweep.)
       {
-        const bool next = k + 1 < p.K;
+        // (teacher-forced modes prepared the next operand in the last tile: nothing here, and
+        // a_empty's phase is not waited for twice)
+        const bool next = k + 1 < p.K && !kTF;
         bool ok = next && !fail;
         if (ok) ok = mbar_wait(a_empty, k & 1, p.timeout_ns, abort_flag);  // MMAs done with E
         ok = __all_sync(0xFFFFFFFFu, ok);
@@ -1372,13 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         }
         int32_t tok = 0;
         if (live) {
-          if (kTF) {
-            tok = __ldg(p.prev + static_cast<size_t>(b) * p.K + k + 1);
-            if (tok < 0 || tok >= p.V) {
-              record_error(p.status, kStatusDeviceOob);
-              tok = 0;
-            }
-          } else if (rnn_op) {
+          if (rnn_op) {
             // the RNN head's next state is made after the barrier: speculating on it costs
             // the state's read-back and both gates, and misses more often than it hits
             spec_key = ~0ull;
@@ -1396,7 +1419,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (gate_first) {
           gate_times_embedding(p, live, 2 * g, tok, wv0);
           gate_times_embedding(p, live, 2 * g + 1, tok, wv1);
-        } else if (kTF || !rnn_op) {
+        } else if (!kTF && !rnn_op) {
           gather_operand(knext, live, tok);
         }
       }
