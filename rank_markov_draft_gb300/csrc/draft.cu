@@ -1562,8 +1562,7 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
   const void* fn = nullptr;
   const bool copies = args.p.B <= 64;  // small batches fill the MMA rows with copies
   const bool gated = args.p.H != nullptr || args.p.A != nullptr;
-  // the drafting modes come in plain and gated builds; the parity, label and residual modes
-  // take their gates at run time
+  // plain and gated builds (the teacher-forced parity mode takes its gates at run time)
 #define DSPARK_DRAFT_FN(M, C, G) reinterpret_cast<const void*>(&draft_kernel<M, C, G>)
   switch (mode) {
     case kModeSample:
@@ -1583,10 +1582,12 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
                   : DSPARK_DRAFT_FN(kModeTeacherForced, false, true);
       break;
     case kModeLabel:  // half-sub-tile ring slots: always the 128-row instantiation
-      fn = DSPARK_DRAFT_FN(kModeLabel, false, true);
+      fn = gated ? DSPARK_DRAFT_FN(kModeLabel, false, true)
+                 : DSPARK_DRAFT_FN(kModeLabel, false, false);
       break;
     case kModeResidual:
-      fn = DSPARK_DRAFT_FN(kModeResidual, false, true);
+      fn = gated ? DSPARK_DRAFT_FN(kModeResidual, false, true)
+                 : DSPARK_DRAFT_FN(kModeResidual, false, false);
       break;
     default: return cudaErrorInvalidValue;
   }
