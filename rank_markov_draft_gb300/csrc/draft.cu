@@ -95,6 +95,9 @@ constexpr int kTileN = kDraftTileN;              // 128 tokens per MMA tile (MMA
 constexpr int kSubV = 64;                        // tokens per epilogue sub-tile (U ring slot)
 constexpr int kRows = kBatchChunk;               // 128 requests (MMA M)
 constexpr int kNumW2Slots = 3;                   // W2 ring: slices of [128 rows x 128 tokens]
+// With batch copies (B <= 64) the U ring's four 16 KB slots leave the last 32 KB of its region
+// free: a fourth W2 slot goes there
+constexpr int kNumW2SlotsMax = 4;
 constexpr int kKSlice = kDraftSliceRows / 16;    // MMAs (K = 16 each) per W2 slice
 constexpr int kNumUStages = 3;                   // U ring slots of 32 KB (B > 64)
 constexpr int kNumUStagesSmall = 4;              // slots of 16 KB when B <= 64 (box <= 64 rows)
@@ -136,7 +139,7 @@ static_assert(kSmemBytes <= 232448, "draft kernel shared memory above the sm_103
 static_assert(kTmemA + kMaxRank / 2 <= kTmemCols, "TMEM columns");
 static_assert(kNumUStagesSmall * kUStageBytes / 2 <= kNumUStages * kUStageBytes, "U ring");
 static_assert(kTileN == 2 * kSubV, "a tile is two sub-tiles");
-static_assert((2 * kNumW2Slots + 2 * kNumUStagesSmall + 2 * kNumAcc + 6) * 8 + 2 * kMaxK * 4 +
+static_assert((2 * kNumW2SlotsMax + 2 * kNumUStagesSmall + 2 * kNumAcc + 6) * 8 + 2 * kMaxK * 4 +
                       kRows * 8 + 16 <=
                   kBarRegion,
               "barrier region too small");
@@ -523,6 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   constexpr bool kKeys = !kTF || MODE == kModeResidual;
   // modes that can run the RNN head (verification and labels take no decay gate)
   constexpr bool kRnnOk = !kHalf;
+  // W2 ring slots: a fourth one in the U region's free tail with batch copies
+  constexpr int kW2Slots = COPIES ? kNumW2SlotsMax : kNumW2Slots;
+  static_assert(kNumUStagesSmall * kUStageBytes / 2 + kW2SlotBytes <= kNumUStages * kUStageBytes,
+                "the fourth W2 slot lies in the U region");
+  // byte offset of W2 slot `slot` from the (aligned) shared memory base
+  auto w2_slot_off = [](int slot) -> uint32_t {
+    return slot < kNumW2Slots ? kOffW2 + static_cast<uint32_t>(slot) * kW2SlotBytes
+                              : kOffU + kNumUStagesSmall * kUStageBytes / 2;
+  };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -531,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   float* merge = reinterpret_cast<float*>(smem + kOffMerge);
   float4* s_best = reinterpret_cast<float4*>(smem + kOffBest);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* w_full = bars;                          // [kNumW2Slots]
-  uint64_t* w_empty = w_full + kNumW2Slots;         // [kNumW2Slots]
-  uint64_t* u_full = w_empty + kNumW2Slots;         // [kNumUStagesSmall]
+  uint64_t* w_full = bars;                          // [kNumW2SlotsMax]
+  uint64_t* w_empty = w_full + kNumW2SlotsMax;      // [kNumW2SlotsMax]
+  uint64_t* u_full = w_empty + kNumW2SlotsMax;      // [kNumUStagesSmall]
   uint64_t* u_empty = u_full + kNumUStagesSmall;    // [kNumUStagesSmall]
   uint64_t* acc_full = u_empty + kNumUStagesSmall;  // [kNumAcc]
   uint64_t* acc_empty = acc_full + kNumAcc;         // [kNumAcc]
@@ -564,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   const uint32_t ubox = COPIES ? kUBoxBytes / 2 : kUBoxBytes;  // one 32-token box
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNumW2Slots; ++s) {
+    for (int s = 0; s < kW2Slots; ++s) {
       mbar_init(&w_full[s], 1);
       mbar_init(&w_empty[s], 1);
     }
@@ -707,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------- MMA issuer and W2 producer (one lane)
-    // W2 slices are loaded kNumW2Slots - 1 ahead of the MMAs: slice j + 2 goes into the
+    // W2 slices are loaded kW2Slots - 1 ahead of the MMAs: slice j + kW2Slots - 1 goes into the
     // slot of slice j - 1 as soon as slice j's MMAs are issued (they queue behind slice
     // j - 1's in the tensor pipe, so waiting for that slot never starves the pipe).
     if (lane == 0) {
@@ -723,21 +735,20 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       bool issued_any = false;
       // load slice j (tile (j / ns) % nt of this CTA, rows [128 (j % ns), ...)) into its slot
       auto load_slice = [&](int j) -> bool {
-        const int slot = j % kNumW2Slots;
-        if (!mbar_wait(&w_empty[slot], ((j / kNumW2Slots) & 1) ^ 1, p.timeout_ns, abort_flag,
+        const int slot = j % kW2Slots;
+        if (!mbar_wait(&w_empty[slot], ((j / kW2Slots) & 1) ^ 1, p.timeout_ns, abort_flag,
                        kBackoffControlNs))
           return false;
         const int s = j % ns, t = (j / ns) % nt;
         const int v0 = (t_begin + t) * kTileN;
-        uint8_t* dst = sW + smem_checked(slot * kW2SlotBytes, w_bytes, kNumW2Slots * kW2SlotBytes,
-                                         p.status);
+        uint8_t* dst = smem + smem_checked(w2_slot_off(slot), w_bytes, kSmemBytes - 1024, p.status);
         mbar_arrive_expect_tx(&w_full[slot], w_bytes);
         tma_load_2d(dst, &args.tm_w2, v0, s * kDraftSliceRows, &w_full[slot], pol_w);
         tma_load_2d(dst + sr * 128, &args.tm_w2, v0 + kDraftBoxV, s * kDraftSliceRows,
                     &w_full[slot], pol_w);
         return true;
       };
-      while (ok && loaded < total && loaded < kNumW2Slots) ok = load_slice(loaded++);
+      while (ok && loaded < total && loaded < kW2Slots) ok = load_slice(loaded++);
       for (int k = 0; k < p.K && ok; ++k) {
         if (!mbar_wait(a_full, k & 1, p.timeout_ns, abort_flag, 32u)) {
           ok = false;
@@ -760,14 +771,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           const uint32_t d_tmem = tmem_checked(tmem_base + static_cast<uint32_t>(buf * kTileN),
                                                tmem_base, kTileN, 0, kTmemA, 0, p.status);
           for (int s = 0; s < ns && ok; ++s) {
-            const int j = i * ns + s, slot = j % kNumW2Slots;
-            if (!mbar_wait(&w_full[slot], (j / kNumW2Slots) & 1, p.timeout_ns, abort_flag,
+            const int j = i * ns + s, slot = j % kW2Slots;
+            if (!mbar_wait(&w_full[slot], (j / kW2Slots) & 1, p.timeout_ns, abort_flag,
                            kBackoffControlNs)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t b0 = smem_addr(sW + slot * kW2SlotBytes);
+            const uint32_t b0 = smem_addr(smem + w2_slot_off(slot));
             const int kk_end = nkk < (s + 1) * kKSlice ? nkk : (s + 1) * kKSlice;
             for (int kk = s * kKSlice; kk < kk_end; ++kk) {
               const uint64_t bd = smem_desc(b0 + (kk - s * kKSlice) * 2048, lbo, 1024);
@@ -778,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
             issued_any = true;
             umma_commit(&w_empty[slot]);
-            if (loaded < total && loaded <= j + kNumW2Slots - 1) ok = load_slice(loaded++);
+            if (loaded < total && loaded <= j + kW2Slots - 1) ok = load_slice(loaded++);
           }
           if (!ok) break;
           umma_commit(&acc_full[buf]);
@@ -795,8 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         record_error(p.status, kStatusTimeout);
         // Drain: every copy and every MMA this lane issued must finish before the CTA
         // exits and TMEM is released (on the normal path the epilogue waited for all)
-        for (int j = loaded - 1; j >= 0 && j >= loaded - kNumW2Slots; --j)
-          mbar_wait(&w_full[j % kNumW2Slots], (j / kNumW2Slots) & 1, p.timeout_ns, nullptr);
+        for (int j = loaded - 1; j >= 0 && j >= loaded - kW2Slots; --j)
+          mbar_wait(&w_full[j % kW2Slots], (j / kW2Slots) & 1, p.timeout_ns, nullptr);
         if (issued_any) {
           umma_commit(mma_drain);
           mbar_wait(mma_drain, 0, p.timeout_ns, nullptr);
