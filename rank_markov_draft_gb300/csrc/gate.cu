@@ -23,7 +23,7 @@
 namespace dspark {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 8;  // 192 KB of h and Wg in flight: the fills are L2-latency bound
 constexpr uint32_t kAStage = 128 * 64 * 2;  // 16 KB: 128 rows of h x 64 of d
 constexpr uint32_t kBStage = 64 * 64 * 2;   // 8 KB: 64 of d x 64 of r
 constexpr uint32_t kOffA = 0;
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(kThreads, 1) gate_gemm_kernel(const __grid_con
   uint8_t* sA = smem + kOffA;
   uint8_t* sB = smem + kOffB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;               // [4]
-  uint64_t* empty = bars + kStages;    // [4]
+  uint64_t* full = bars;               // [kStages]
+  uint64_t* empty = bars + kStages;    // [kStages]
   uint64_t* acc_full = bars + 2 * kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 2);
