@@ -566,6 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   const int t_begin = static_cast<int>(static_cast<int64_t>(cta) * p.n_tiles / ncta);
   const int t_end = static_cast<int>(static_cast<int64_t>(cta + 1) * p.n_tiles / ncta);
   const int nt = t_end - t_begin;
+  // The tiles of a position in the order they are streamed: ascending at even positions,
+  // descending at odd ones, so a position starts on the W2 tiles the previous one used last
+  // (still in L2 when the streams evict W2 from it)
+  auto tile_of = [&](int k, int t) { return t_begin + ((k & 1) ? nt - 1 - t : t); };
   const int nkk = p.r / 16;
   // W2 slices per tile and rows per slice
   const int sr = p.r < kDraftSliceRows ? p.r : kDraftSliceRows;
@@ -645,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           }
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
           if (!ok) break;
-          const int x = (t_begin + t) * kTileN + 32 * f;
+          const int x = tile_of(k, t) * kTileN + 32 * f;
           if (mine) {
             uint8_t* dst = sU + smem_checked(su * 2 * ubox + lane * 512, ubox + 512,
                                              kNumUStages * kUStageBytes, p.status);
@@ -690,19 +694,19 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             uint8_t* dst = sU + smem_checked(su * 2 * ubox, 2 * ubox, kNumUStages * kUStageBytes,
                                              p.status);
             if (kHalf && p.u_rowpair) {  // U and target tokens [x, x + 64), rows [64 h, +64)
-              const int c0 = ((t_begin + t) * kTileN + kSubV * (f >> 1)) / 32, h = f & 1;
+              const int c0 = (tile_of(k, t) * kTileN + kSubV * (f >> 1)) / 32, h = f & 1;
               tma_load_4d(dst, &args.tm_u, 0, c0, k, 64 * h, &u_full[su], pol_u);
               tma_load_4d(dst + ubox, &args.tm_p, 0, c0, k, 64 * h, &u_full[su], pol_u);
             } else if (kHalf) {  // U and target tokens [x, x + 32)
-              const int x = (t_begin + t) * kTileN + 32 * f;
+              const int x = tile_of(k, t) * kTileN + 32 * f;
               tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
               tma_load_3d(dst + ubox, &args.tm_p, x, k, 0, &u_full[su], pol_u);
             } else if (p.u_rowpair) {  // U tokens [x, x + 64): chunks x / 32, x / 32 + 1
-              const int c0 = ((t_begin + t) * kTileN + kSubV * f) / 32;
+              const int c0 = (tile_of(k, t) * kTileN + kSubV * f) / 32;
               tma_load_4d(dst, &args.tm_u, 0, c0, k, 0, &u_full[su], pol_u);
               if (pair2) tma_load_4d(dst + 16384, &args.tm_u, 0, c0, k, 64, &u_full[su], pol_u);
             } else {  // U tokens [x, x + 64)
-              const int x = (t_begin + t) * kTileN + kSubV * f;
+              const int x = tile_of(k, t) * kTileN + kSubV * f;
               tma_load_3d(dst, &args.tm_u, x, k, 0, &u_full[su], pol_u);
               tma_load_3d(dst + ubox, &args.tm_u, x + 32, k, 0, &u_full[su], pol_u);
             }
@@ -733,14 +737,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       int loaded = 0;                   // slices whose loads were issued
       bool ok = true;
       bool issued_any = false;
-      // load slice j (tile (j / ns) % nt of this CTA, rows [128 (j % ns), ...)) into its slot
+      // load slice j (the (j / ns) % nt-th tile its position streams, rows [128 (j % ns), ...))
+      // into its slot
       auto load_slice = [&](int j) -> bool {
         const int slot = j % kW2Slots;
         if (!mbar_wait(&w_empty[slot], ((j / kW2Slots) & 1) ^ 1, p.timeout_ns, abort_flag,
                        kBackoffControlNs))
           return false;
-        const int s = j % ns, t = (j / ns) % nt;
-        const int v0 = (t_begin + t) * kTileN;
+        const int s = j % ns, t = (j / ns) % nt, kj = j / (ns * nt);
+        const int v0 = tile_of(kj, t) * kTileN;
         uint8_t* dst = smem + smem_checked(w2_slot_off(slot), w_bytes, kSmemBytes - 1024, p.status);
         mbar_arrive_expect_tx(&w_full[slot], w_bytes);
         tma_load_2d(dst, &args.tm_w2, v0, s * kDraftSliceRows, &w_full[slot], pol_w);
@@ -981,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
       for (int t = 0; t < nt && !fail; ++t) {
         const int i = k * nt + t;
         const int buf = i % kNumAcc;
-        const int tile = t_begin + t;
+        const int tile = tile_of(k, t);
         if (kRace && row_ok) {
           const uint32_t c1 = static_cast<uint32_t>(MODE == kModeResidual ? res_pos : k);
           const uint32_t tag = (MODE == kModeResidual ? 9u : 1u) + 2u * static_cast<uint32_t>(g);
