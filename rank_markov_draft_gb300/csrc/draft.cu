@@ -20,10 +20,17 @@
 //     accumulators plus the 128 columns of the A operand fill the 512 columns;
 //   * warp 0 (one lane) streams U in 64-token sub-tiles [rows x 64] fp32 with TMA
 //     into its ring (two sub-tiles a tile); it never depends on sampled tokens,
-//     so it runs ahead across step boundaries;
+//     so it runs ahead across step boundaries.  Above 64 requests a sub-tile is
+//     two "row-pair" boxes of 64 rows x 64 tokens (256 contiguous bytes of each
+//     row, which DRAM serves far better than 128-byte pieces of rows 9.7 MB
+//     apart); otherwise two boxes of 32 tokens x every row;
+//   * the tiles of a step are streamed in ascending order at even steps and in
+//     descending order at odd ones, so a step starts on the W2 tiles the
+//     previous one used last;
 //   * warp 1 (one lane) streams W2 in slices of [128 rank rows x 128 tokens]
-//     bf16 (a tile is one slice per 128 of the rank) into a 3-slot ring, two
-//     slices ahead of its own MMAs, and issues tcgen05.mma: D[128 requests x
+//     bf16 (a tile is one slice per 128 of the rank) into a 3-slot ring (a
+//     fourth slot with batch copies, in the U ring's free tail), slices ahead
+//     of its own MMAs, and issues tcgen05.mma: D[128 requests x
 //     128 tokens] = E[128 x r] * W2tile[r x 128] into one of three TMEM
 //     accumulators.  E, the step's operand for every request (the gathered
 //     Markov embedding, gated or not, or the RNN head's state), lives in TMEM
@@ -38,10 +45,13 @@
 //     logits never reach HBM; stage 2 of the race runs once per step per
 //     thread, in that best block;
 //   * at the end of a step each CTA publishes, per request, a 64-bit key
-//     (epoch | ordered score | inverted token id) by atomicMax and its
-//     log-sum-exp partial; it arrives at a bounded grid barrier and, while the
-//     others finish, writes the next step's operand for the winners known so
-//     far; after the barrier only rows whose winner changed are rewritten;
+//     (epoch | ordered score | inverted token id) by atomicMax (only where it
+//     can still raise the key) and its log-sum-exp partial; it arrives at a
+//     bounded grid barrier and, while the others finish, gathers the next
+//     step's operand for the winners known so far (the gated head loads its
+//     gate rows before the winners' keys; the RNN head parks the decayed state
+//     a (.) s in free accumulator columns); after the barrier the operand goes
+//     to TMEM, re-gathered only for rows whose winner changed;
 //   * after the last step, CTA c reduces request c's partials into tokens and
 //     log-probabilities and runs the fused confidence head.
 //
@@ -49,18 +59,23 @@
 // m serves request m mod 64); copy c takes the 64-token sub-tile c of every
 // tile, so every TMEM lane quadrant holds real rows.
 //
+// Template parameters: MODE, COPIES (batch copies, B <= 64) and GATED (the launch
+// may carry gates; the plain build compiles the operand path without them).
+//
 // Teacher-forced modes take every position's predecessor from the caller, so
 // positions do not depend on one another: the next position's operand is
-// written as soon as the MMAs are done with the current one and the grid
-// barrier is waited on only before the final reduction.  The label mode
+// written during the current position's last tile, as soon as its MMAs are done
+// with the operand, and the grid barrier is waited on only before the final
+// reduction.  The label mode
 // (DSpark explainer, "Confidence-scheduled verification": c*_k = 1 - TV of the
 // draft head's and the target's distributions) streams the target's rows
 // beside U and sums 2^min(log2 q(v), log2 p(v)) over the vocabulary, both
 // normalisers known beforehand (the target's from a row scan, the draft's
 // from its own log-probability of the drafted token).  Its ring slots hold U
-// and target for half a sub-tile (32 tokens each), two slots per sub-tile;
-// every epilogue warp reads both halves (8 tokens of each per thread), so each
-// slot has one group of readers that takes its fills in order.
+// and target for half a sub-tile, two slots per sub-tile: 32 tokens of every
+// row, or with row-pair boxes 64 tokens of rows [64 h, 64 h + 64); every
+// epilogue warp waits for and releases both (reading the one that holds its
+// tokens), so each slot has one group of readers that takes its fills in order.
 //
 // Sampling epilogue (an exact draw from softmax(l / T) in two stages over
 // 16-token blocks; each thread's 16 columns of a sub-tile are one block beta):
