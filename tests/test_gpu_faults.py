@@ -125,3 +125,28 @@ def test_checked_library_runs_clean_and_matches_release(dsp, B, K, V, r):
         for key, t in res.items():
             if isinstance(t, torch.Tensor):
                 assert torch.equal(t, checked[name][key]), f"{name}.{key} differs"
+
+
+def test_checked_library_at_full_vocabulary():
+    """The offset checks over every tile of the full vocabulary (152 CTAs, one per SM): the
+    serving batch and the gated head's batch-copies build, drafted and greedy, run clean
+    (status 0) and equal the release library's outputs."""
+    from synth import config_inputs
+    for cfg in (2, 3):
+        inp = config_inputs(cfg)
+        B = inp.U.shape[0]
+        U, W1, W2, anchors = dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors)
+        gate = dict(h=bf(inp.h), Wg=bf(inp.Wg)) if cfg == 3 else {}
+        outs = []
+        for checked in (False, True):
+            with binding.Context(0, B_max=B, V_max=inp.U.shape[2], K_max=inp.U.shape[1],
+                                 checked=checked) as ctx:
+                res = [binding.markov_draft(ctx, U, W1, W2, anchors, temperature=T, seed=5,
+                                            **gate) for T in (1.0, 0.0)]
+                torch.cuda.synchronize()
+                assert ctx.status() == 0
+                outs.append(res)
+        for a, c in zip(*outs):
+            assert torch.equal(a["tokens"], c["tokens"])
+            assert torch.equal(a["logprobs"], c["logprobs"])
+        del U
