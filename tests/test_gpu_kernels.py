@@ -14,7 +14,8 @@ from scipy import special, stats
 import oracle
 from rank_markov_draft_gb300 import binding
 from synth import bf16_bits, make_inputs
-from tests.gpu_util import LOGPROB_TOL, bf, check_sequences, dev, first_difference, host
+from tests.gpu_util import (LOGPROB_TOL, assert_coverage, bf, check_sequences, dev,
+                            first_difference, host)
 
 pytestmark = pytest.mark.gpu
 
@@ -95,6 +96,26 @@ def test_draft_matches_oracle(dsp, B, K, V, r, T, seed):
     assert tok.min() >= 0 and tok.max() < V
     ref = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=T, seed=seed)
     check_sequences(tok, lp, ref)
+
+
+@pytest.mark.parametrize("B,K,V", [(3, 64, 4096), (2, 3, 1 << 18), (66, 2, 1 << 18)])
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_draft_at_the_limits(B, K, V, T):
+    """The largest block (K = 64: 64 key rows and partial planes) and the largest vocabulary
+    (V = 2^18: token ids use every bit of the key's 18-bit token field, 2048 tiles), with and
+    without batch copies; every position compared with the oracle."""
+    r = 256
+    inp = make_inputs(300 + K + B, B, K, V, r)
+    with binding.Context(0, B_max=B, V_max=V, K_max=K) as ctx:
+        out = binding.markov_draft(ctx, dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
+                                   temperature=T, seed=17)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        tok, lp = host(out["tokens"]), host(out["logprobs"])
+    assert tok.min() >= 0 and tok.max() < V
+    ref = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=T, seed=17)
+    d_, n_ = check_sequences(tok, lp, ref)
+    assert_coverage(f"limits B={B} K={K} V={V} T={T}", d_, n_, B * K)
 
 
 @pytest.mark.parametrize("T", [1.0, 0.0])
