@@ -124,6 +124,15 @@ constexpr int kCtlWarps = 2;                     // U producer; MMA issuer and W
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;      // 256
 constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;  // 320
+// The residual draw reads its rows with tile::gather4, whose copies one warp issues at about
+// one per 45 ns whatever their size: two more warps (10 and 11, still three warps on a
+// scheduler at most) share each fill's copies with warp 0.
+constexpr int kResCopyWarps = 2;
+constexpr int kResProducers = 1 + kResCopyWarps;
+template <int MODE>
+constexpr int threads_of() {
+  return kThreads + (MODE == kModeResidual ? kResCopyWarps * 32 : 0);
+}
 constexpr uint32_t kW2SlotBytes = kDraftSliceRows * kTileN * 2;  // 32 KB
 constexpr uint32_t kUBoxBytes = kRows * 32 * 4;              // 16 KB (32 tokens x 128 rows)
 constexpr uint32_t kUStageBytes = 2 * kUBoxBytes;            // 32 KB
@@ -529,7 +538,8 @@ __device__ __forceinline__ float sum16(const float* w) {
 // GATED: the launch may carry a gate (gated head) or decay and input gates (RNN head); the
 // plain instantiations compile the operand path without them
 template <int MODE, bool COPIES, bool GATED>
-__global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftArgs args) {
+__global__ void __launch_bounds__(threads_of<MODE>(), 1)
+    draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
   // teacher-forced modes take the predecessors from the caller
   constexpr bool kTF = MODE == kModeTeacherForced || MODE == kModeLabel || MODE == kModeResidual;
@@ -603,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     const uint32_t u_readers = COPIES ? static_cast<uint32_t>(kEpiWarps / 2) : kEpiWarps;
     static_assert(kEpiWarps % 2 == 0, "the copies split the epilogue warps");
     for (int s = 0; s < nus; ++s) {
-      mbar_init(&u_full[s], 1);
+      mbar_init(&u_full[s], MODE == kModeResidual ? kResProducers : 1);
       mbar_init(&u_empty[s], u_readers);
     }
     for (int s = 0; s < kNumAcc; ++s) {
@@ -628,29 +638,31 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0 && MODE == kModeResidual) {
-    // --------------------------------------------------- U producer, residual mode
-    // The draw rows are read in place: each request's base-logit row and target row at
-    // its own draw position (tile::gather4 over 2-D row maps of U [B K, V] and
-    // P [B (K + 1), V]), lane l fetching requests 4 l .. 4 l + 3 of every half
-    // sub-tile into the same slot layout as the 3-D boxes; lane 0 waits for the slots.
+  if (MODE == kModeResidual && (warp == 0 || warp >= kCtlWarps + kEpiWarps)) {
+    // --------------------------------------------------- U producers, residual mode
+    // The draw rows are read in place: each request's base-logit row and target row at its
+    // own draw position (tile::gather4 over 2-D row maps of U [B K, V] and P [B (K + 1), V],
+    // four rows an op, into the slot layout of the 3-D boxes). A fill's 64 copies (32 per
+    // tensor, copy i of a tensor taking rows 4 i .. 4 i + 3) are shared by three warps:
+    // lane l of producer w issues copy o = 3 l + w; each warp arrives on the slot's full
+    // barrier with the bytes of its own copies, and every warp takes every fill in order.
+    const int w = warp == 0 ? 0 : warp - (kCtlWarps + kEpiWarps) + 1;
+    const int o = kResProducers * lane + w;  // this lane's copy of every fill
+    const bool target = o >= 32;
+    const int rg = o & 31;                   // rows 4 rg .. 4 rg + 3
+    const bool mine = o < 64 && 4 * rg < p.box_rows;
+    const uint32_t w_bytes =
+        static_cast<uint32_t>(__popc(__ballot_sync(0xFFFFFFFFu, mine))) * 512u;
     const uint64_t pol_u = l2_policy_evict_first();
-    const uint32_t u_bytes = 2u * static_cast<uint32_t>(p.box_rows) * 128u;
-    const bool mine = 4 * lane < p.box_rows;
-    // the lane's four requests (past the batch: request 0 again, never read) and their draw
-    // positions, a byte each (a position is at most K <= 64)
-    uint32_t pos4 = 0;
+    // the copy's four rows (past the batch: request 0 again, never read); a bonus row reads
+    // no base logit: any valid row
+    int y[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int b = 4 * lane + q < p.B ? 4 * lane + q : 0;
-      pos4 |= static_cast<uint32_t>(p.rows[b].pos) << (8 * q);
+    for (int i = 0; i < 4; ++i) {
+      const int b = 4 * rg + i < p.B ? 4 * rg + i : 0;
+      const int gb = p.b_global0 + b, pos = mine ? p.rows[b].pos : 0;
+      y[i] = target ? gb * (p.res_K + 1) + pos : gb * p.res_K + min(pos, p.res_K - 1);
     }
-    // row of request q of the lane in U (a bonus row reads no q: any valid row) or P
-    auto draw_row = [&](int q, bool target) {
-      const int gb = p.b_global0 + (4 * lane + q < p.B ? 4 * lane + q : 0);
-      const int pos = static_cast<int>((pos4 >> (8 * q)) & 0xFFu);
-      return target ? gb * (p.res_K + 1) + pos : gb * p.res_K + min(pos, p.res_K - 1);
-    };
     bool ok = true;
     int issued = 0;
     for (int k = 0; k < p.K && ok; ++k) {
@@ -660,18 +672,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
           if (lane == 0) {
             ok = mbar_wait(&u_empty[su], ((j / nus) & 1) ^ 1, p.timeout_ns, abort_flag,
                            kBackoffControlNs);
-            if (ok) mbar_arrive_expect_tx(&u_full[su], u_bytes);
+            if (ok) mbar_arrive_expect_tx(&u_full[su], w_bytes);
           }
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
           if (!ok) break;
           const int x = tile_of(k, t) * kTileN + 32 * f;
           if (mine) {
-            uint8_t* dst = sU + smem_checked(su * 2 * ubox + lane * 512, ubox + 512,
+            uint8_t* dst = sU + smem_checked(su * 2 * ubox + (target ? ubox : 0u) + rg * 512, 512,
                                              kNumUStages * kUStageBytes, p.status);
-            tma_gather4_2d(dst, &args.tm_u, x, draw_row(0, false), draw_row(1, false),
-                           draw_row(2, false), draw_row(3, false), &u_full[su], pol_u);
-            tma_gather4_2d(dst + ubox, &args.tm_p, x, draw_row(0, true), draw_row(1, true),
-                           draw_row(2, true), draw_row(3, true), &u_full[su], pol_u);
+            tma_gather4_2d(dst, target ? &args.tm_p : &args.tm_u, x, y[0], y[1], y[2], y[3],
+                           &u_full[su], pol_u);
           }
           issued = j + 1;
         }
@@ -1586,7 +1596,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
 }  // namespace
 
 int draft_smem_bytes() { return static_cast<int>(kSmemBytes); }
-int draft_threads() { return kThreads; }
+int draft_threads(int mode) {
+  return mode == kModeResidual ? threads_of<kModeResidual>() : kThreads;
+}
 
 cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
                          uint32_t extra_smem) {
@@ -1627,8 +1639,8 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
   void* kargs[] = {const_cast<DraftArgs*>(&args)};
-  err = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), kargs, kSmemBytes + extra_smem,
-                                    stream);
+  err = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(draft_threads(mode)), kargs,
+                                    kSmemBytes + extra_smem, stream);
   // a refused launch leaves its (non-sticky) error as the thread's last error: clear it, so
   // that the caller's next CUDA error check does not see it again
   if (err != cudaSuccess) (void)cudaGetLastError();

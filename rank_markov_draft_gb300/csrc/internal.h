@@ -97,10 +97,12 @@ struct DraftParams {
 
 struct DraftArgs {
   CUtensorMap tm_w2;  // W2 [r, V] bf16, box {64, min(r, 128)}, 128B swizzle
-  CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle;
-                      // residual mode: U as rows [B K, V], box {32, 1} (gathered by four)
+  CUtensorMap tm_u;   // U chunk [B, K, V] fp32, box {32, 1, box_rows}, 128B swizzle (or
+                      // row-pair boxes); residual mode: U as rows [B K, V], box {32, 1}
+                      // (gathered by four)
   CUtensorMap tm_p;   // label mode: target chunk [B, K+1, V] fp32, box {32, 1, box_rows},
-                      // 128B swizzle; residual mode: P as rows [B (K + 1), V], box {32, 1}
+                      // 128B swizzle (or row-pair boxes); residual mode: P as rows
+                      // [B (K + 1), V], box {32, 1}
   DraftParams p;
 };
 
@@ -113,7 +115,7 @@ enum DraftMode {
 };
 
 int draft_smem_bytes();
-int draft_threads();
+int draft_threads(int mode);
 // extra_smem > 0 asks for that much more dynamic shared memory than the kernel allows, which
 // the runtime refuses (the refused-launch test); the refusal's error is cleared before return
 cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
