@@ -36,10 +36,12 @@ struct dspark_ctx {
   // verification scratch
   float* d_v_lse_t = nullptr;            // [B_max][K_max + 1]
   int32_t* d_v_argmax_t = nullptr;       // [B_max][K_max + 1]
-  dspark::VerifySel* d_v_sel = nullptr;  // [B_max]
   uint16_t* d_v_H = nullptr;             // [B_max][256] bf16
   int32_t* d_v_prev = nullptr;           // [B_max]
   dspark::ResRow* d_v_rows = nullptr;    // [B_max]
+  // verification's per-request scratch, zero between calls
+  unsigned long long* d_v_fail = nullptr;  // [B_max]
+  int* d_v_count = nullptr;                // [B_max]
   // acceptance-label scratch
   int32_t* d_l_prev = nullptr;           // [B_max * K_max] predecessors of the drafted tokens
   float* d_l_offq2 = nullptr;            // [B_max * K_max] log2 q offsets
@@ -446,16 +448,19 @@ int dspark_ctx_create(dspark_ctx** out, int device, int B_max, int V_max, int K_
                        sizeof(float) * dspark::kTopkPartUnits * dspark::kMaxTopk) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_lse_t, sizeof(float) * B_max * (K_max + 1)) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_argmax_t, sizeof(int32_t) * B_max * (K_max + 1)) == cudaSuccess &&
-            cudaMalloc(&ctx->d_v_sel, sizeof(dspark::VerifySel) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_H, sizeof(uint16_t) * B_max * dspark::kMaxRank) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_prev, sizeof(int32_t) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_v_rows, sizeof(dspark::ResRow) * B_max) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_fail, sizeof(unsigned long long) * B_max) == cudaSuccess &&
+            cudaMalloc(&ctx->d_v_count, sizeof(int) * B_max) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_prev, sizeof(int32_t) * rows) == cudaSuccess &&
             cudaMalloc(&ctx->d_l_offq2, sizeof(float) * rows) == cudaSuccess;
   ok = ok && cudaMemset(ctx->d_status, 0, sizeof(int)) == cudaSuccess &&
        cudaMemset(ctx->d_bar, 0, sizeof(uint32_t)) == cudaSuccess &&
        cudaMemset(ctx->d_keys, 0, sizeof(unsigned long long) * K_max * dspark::kBatchChunk) ==
            cudaSuccess &&
+       cudaMemset(ctx->d_v_fail, 0, sizeof(unsigned long long) * B_max) == cudaSuccess &&
+       cudaMemset(ctx->d_v_count, 0, sizeof(int) * B_max) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     dspark_ctx_destroy(ctx);
@@ -479,10 +484,11 @@ int dspark_ctx_destroy(dspark_ctx* ctx) {
   cudaFree(ctx->d_topk_part_i);
   cudaFree(ctx->d_v_lse_t);
   cudaFree(ctx->d_v_argmax_t);
-  cudaFree(ctx->d_v_sel);
   cudaFree(ctx->d_v_H);
   cudaFree(ctx->d_v_prev);
   cudaFree(ctx->d_v_rows);
+  cudaFree(ctx->d_v_fail);
+  cudaFree(ctx->d_v_count);
   cudaFree(ctx->d_l_prev);
   cudaFree(ctx->d_l_offq2);
   cudaFree(ctx->d_topk_part_v);
@@ -498,7 +504,10 @@ int dspark_ctx_reset(dspark_ctx* ctx, dspark_stream_t stream) {
             cudaMemsetAsync(ctx->d_bar, 0, sizeof(uint32_t), s) == cudaSuccess &&
             cudaMemsetAsync(ctx->d_keys, 0,
                             sizeof(unsigned long long) * ctx->K_max * dspark::kBatchChunk,
-                            s) == cudaSuccess;
+                            s) == cudaSuccess &&
+            cudaMemsetAsync(ctx->d_v_fail, 0, sizeof(unsigned long long) * ctx->B_max, s) ==
+                cudaSuccess &&
+            cudaMemsetAsync(ctx->d_v_count, 0, sizeof(int) * ctx->B_max, s) == cudaSuccess;
   if (!ok) return DSPARK_ERR_CUDA;
   ctx->bar_counter = 0;
   ctx->epoch = 0;
@@ -805,21 +814,18 @@ int dspark_verify(dspark_ctx* ctx, const float* P, const float* U, const uint16_
   v.status = ctx->d_status;
   v.lse_t = ctx->d_v_lse_t;
   v.argmax_t = ctx->d_v_argmax_t;
-  v.sel = ctx->d_v_sel;
   v.H_sel = ctx->d_v_H;
   v.prev_sel = ctx->d_v_prev;
-  v.rows = ctx->d_v_rows;
+  v.rows = target_temperature > 0.f ? ctx->d_v_rows : nullptr;
+  v.fail_mask = ctx->d_v_fail;
+  v.count = ctx->d_v_count;
   int n = 0;
   cudaError_t e = dspark::launch_verify(v, s, &n);
   ctx->last_launches += n;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   if (target_temperature > 0.f) {
-    // the draw: per-row constants, then the draft kernel's residual mode over one
-    // position, reading each request's draw rows of U and P in place (a greedy target's
-    // token is its argmax, set above)
-    e = dspark::launch_verify_prep(v, s);
-    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-    ctx->last_launches += 1;
+    // the draw: the draft kernel's residual mode over one position, reading each request's
+    // draw rows of U and P in place (a greedy target's token is its argmax, set above)
     LabelIn res{P, nullptr, nullptr, nullptr, 1.4426950408889634f / target_temperature,
                 ctx->d_v_rows, K};
     st = run_draft(ctx, dspark::kModeResidual, U, W1, W2, ctx->d_v_prev, ctx->d_v_prev,

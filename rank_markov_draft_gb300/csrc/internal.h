@@ -150,13 +150,6 @@ cudaError_t launch_walk(const int32_t* cand, const float* S, const int32_t* anch
                         float* logprobs, const dspark_conf_args* conf, int* status,
                         cudaStream_t stream);
 // ---- speculative verification (verify.cu)
-struct VerifySel {  // where a request's draw happens and what feeds it
-  int pos;          // position of the draw: the first rejection, or the window end (bonus)
-  int residual;     // 1: residual max(0, p - q) at a rejection; 0: bonus from p
-  int x;            // the rejected drafted token (residual), else -1
-  int prev;         // its predecessor (the anchor at position 0)
-};
-
 struct VerifyArgs {
   const float* P;             // [B, K+1, V] target logits
   const float* U;             // [B, K, V] base logits of the draft
@@ -177,15 +170,19 @@ struct VerifyArgs {
   // context scratch
   float* lse_t;               // [B, K+1]
   int32_t* argmax_t;          // [B, K+1]
-  VerifySel* sel;             // [B]
-  uint16_t* H_sel;            // [B, r] bf16 gate rows at the draw position
+  // the draw (sampled target): the residual mode's per-row constants, predecessors and
+  // gate rows at the draw position; rows null: no draw (a greedy target's token is its
+  // argmax)
+  uint16_t* H_sel;            // [B, r] bf16
   int32_t* prev_sel;          // [B]
-  ResRow* rows;               // [B] the residual mode's per-row constants
+  ResRow* rows;               // [B]
+  // per-request scratch, zero between calls (the request's last CTA clears it)
+  unsigned long long* fail_mask;  // [B] bit k: the test of position k failed
+  int* count;                     // [B] CTAs of the request done
 };
+// One kernel: the target-row scan with the acceptance tests and the draw's per-row
+// constants (the draft kernel's residual mode then reads the draw rows of U and P in place).
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches);
-// The draw's per-row constants, gate row and predecessor (one kernel; the draft kernel's
-// residual mode reads the draw rows of U and P in place).
-cudaError_t launch_verify_prep(const VerifyArgs& v, cudaStream_t stream);
 // Log-sum-exp of P / Tt (argmax when greedy) of the rows (b, k <= min(ell[b], kmax))
 // of P [B, K+1, V]; ell null: every request's rows up to kmax.
 cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,
