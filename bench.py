@@ -265,8 +265,10 @@ _HEADERS = ("sm103.cuh", "philox.cuh", "confidence.cuh", "internal.h")
 PROFILES = {
     "serving": ("draft_kernel_serving.md", ("draft.cu",) + _HEADERS),
     "single": ("draft_kernel_single.md", ("draft.cu",) + _HEADERS),
-    "label": ("label_step_serving.md", ("draft.cu", "label.cu", "verify.cu") + _HEADERS),
-    "verify": ("verify_step_serving.md", ("draft.cu", "verify.cu") + _HEADERS),
+    "label": ("label_step_serving.md",
+              ("draft.cu", "label.cu", "rowscan.cuh", "headlogit.cuh") + _HEADERS),
+    "verify": ("verify_step_serving.md",
+               ("draft.cu", "verify.cu", "rowscan.cuh", "headlogit.cuh") + _HEADERS),
     "selector": ("topk_stream_kernel_selector.md", ("selector.cu", "gate.cu") + _HEADERS),
 }
 
@@ -725,9 +727,10 @@ def run_ours(args, rank, world, local):
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
-                "kernel": ("verify step (target-row scan, acceptance, per-row prep, residual "
-                           "draw reading the draw rows in place)" if args.workload == "verify" else
-                           "label step (target-row scan, per-row offsets, draft kernel in "
+                "kernel": ("verify step (target-row scan with the acceptance tests and the "
+                           "draw's per-row prep, residual draw reading the draw rows in place)"
+                           if args.workload == "verify" else
+                           "label step (target-row scan with per-row offsets, draft kernel in "
                            "label mode)" if args.workload == "label" else
                            "gates + draft_kernel" if c.get("gated") and cfg != 4 else
                            "draft_kernel" if cfg != 4 else

@@ -858,11 +858,7 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
     st = run_gate(ctx, h, Wg, B * K, d, r, ctx->d_H, ctx->d_Hb, s);
     if (st != DSPARK_OK) return st;
   }
-  // the target's normaliser (or argmax) of rows k < K
-  cudaError_t e = dspark::launch_target_stats(P, nullptr, B, K, K - 1, V, target_temperature,
-                                              ctx->d_v_lse_t, ctx->d_v_argmax_t, s);
-  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  ctx->last_launches += 1;
+  // the target's normaliser (or argmax) of rows k < K and each row's preparation
   dspark::LabelPrepArgs a{};
   a.P = P;
   a.U = U;
@@ -884,7 +880,7 @@ int dspark_accept_label(dspark_ctx* ctx, const float* P, const float* U, const u
   a.offq2 = ctx->d_l_offq2;
   a.label = label;
   a.status = ctx->d_status;
-  if ((e = dspark::launch_label_prep(a, s)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dspark::launch_label_prep(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
   ctx->last_launches += 1;
   if (draft_temperature > 0.f && target_temperature > 0.f) {
     LabelIn lab{P, ctx->d_v_lse_t, ctx->d_l_offq2, label,

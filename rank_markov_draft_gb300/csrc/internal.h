@@ -183,11 +183,6 @@ struct VerifyArgs {
 // One kernel: the target-row scan with the acceptance tests and the draw's per-row
 // constants (the draft kernel's residual mode then reads the draw rows of U and P in place).
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches);
-// Log-sum-exp of P / Tt (argmax when greedy) of the rows (b, k <= min(ell[b], kmax))
-// of P [B, K+1, V]; ell null: every request's rows up to kmax.
-cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,
-                                float target_temperature, float* lse_t, int32_t* argmax_t,
-                                cudaStream_t stream);
 
 // ---- acceptance label (label.cu)
 // One warp per drafted position: its predecessor, the offset that turns the
@@ -202,8 +197,8 @@ struct LabelPrepArgs {
   const int32_t* anchors;     // [B]
   const int32_t* tokens;      // [B, K]
   const float* logq;          // [B, K] (draft T > 0)
-  const float* lse_t;         // [B, K+1] (target T > 0)
-  const int32_t* argmax_t;    // [B, K+1] (target T = 0)
+  float* lse_t;               // [B, K+1] out, rows k < K (target T > 0)
+  int32_t* argmax_t;          // [B, K+1] out, rows k < K (target T = 0)
   int B, K, V, r;
   float inv_td, inv_tt;       // 0: greedy
   int32_t* prev;              // [B, K] out
@@ -211,6 +206,8 @@ struct LabelPrepArgs {
   float* label;               // [B, K] out where one side is greedy
   int* status;
 };
+// One kernel: the scan of each drafted position's target row, then that row's
+// preparation (predecessor, log2 q offset, the label where one side is greedy).
 cudaError_t launch_label_prep(const LabelPrepArgs& a, cudaStream_t stream);
 
 // ---- load-aware prefix scheduler (schedule.cu)

@@ -8,7 +8,8 @@
 //
 // The sum over the vocabulary runs in the draft kernel's label mode, which
 // needs both distributions' normalisers before its single pass: the target's
-// comes from the row scan of the target logits, the draft's from the draft's
+// comes from a scan of each target row (the kernel here, one CTA a row, which
+// then prepares that row), the draft's from the draft's
 // own log-probability of the drafted token, log q(x) = l(x) / Td - log Z_q, so
 // that log2 q(v) = l(v) log2(e) / Td + offq2 with
 //     offq2 = (log q(x) - l(x) / Td) log2(e),
@@ -23,18 +24,41 @@
 
 #include "headlogit.cuh"
 #include "internal.h"
+#include "rowscan.cuh"
 #include "sm103.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr float kLog2eL = 1.4426950408889634f;
+constexpr float kLog2eL = kScanLog2e;
 
-__global__ void label_prep_kernel(const LabelPrepArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // b * K + k
-  if (row >= a.B * a.K) return;
+// One CTA per drafted row (b, k), k < K: the scan of target row (b, k) (its log-sum-exp of
+// P / Tt, or its argmax when the target is greedy), then, on warp 0, that row's
+// preparation: the predecessor, the draft's log2 q offset and, where one side is greedy,
+// the label itself.
+__global__ void __launch_bounds__(kScanThreads) label_prep_kernel(const LabelPrepArgs a) {
+  const int row = blockIdx.x;  // b * K + k
   const int b = row / a.K, k = row - b * a.K;
+  const size_t trow = static_cast<size_t>(b) * (a.K + 1) + k;  // target row of position k
+  __shared__ RowScanSmem sm;
+  __shared__ float s_lse;
+  __shared__ int s_argmax;
+  float lse = 0.f;
+  int am = 0;
+  scan_target_row(a.P + trow * a.V, a.V, a.inv_tt, a.inv_tt == 0.f, sm, lse, am);
+  if (threadIdx.x == 0) {
+    if (a.inv_tt == 0.f)
+      a.argmax_t[trow] = am;
+    else
+      a.lse_t[trow] = lse;
+    s_lse = lse;
+    s_argmax = am;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  lse = s_lse;
+  am = s_argmax;
   int x = __ldg(a.tokens + row);
   int prev = (k == 0) ? __ldg(a.anchors + b) : __ldg(a.tokens + row - 1);
   if (x < 0 || x >= a.V || prev < 0 || prev >= a.V) {
@@ -42,13 +66,11 @@ __global__ void label_prep_kernel(const LabelPrepArgs a) {
     x = 0;
     prev = 0;
   }
-  const size_t trow = static_cast<size_t>(b) * (a.K + 1) + k;  // target row of position k
   if (lane == 0) a.prev[row] = prev;
   if (a.inv_td == 0.f) {
     if (lane == 0) {
-      a.label[row] = (a.inv_tt == 0.f)
-                         ? ((x == __ldg(a.argmax_t + trow)) ? 1.f : 0.f)
-                         : expf(__ldg(a.P + trow * a.V + x) * a.inv_tt - __ldg(a.lse_t + trow));
+      a.label[row] = (a.inv_tt == 0.f) ? ((x == am) ? 1.f : 0.f)
+                                       : expf(__ldg(a.P + trow * a.V + x) * a.inv_tt - lse);
     }
     return;
   }
@@ -58,7 +80,6 @@ __global__ void label_prep_kernel(const LabelPrepArgs a) {
   const float offq2 = (__ldg(a.logq + row) - lx * a.inv_td) * kLog2eL;
   if (lane == 0) a.offq2[row] = offq2;
   if (a.inv_tt == 0.f) {
-    int am = __ldg(a.argmax_t + trow);
     if (am < 0 || am >= a.V) {  // a target row without a finite logit
       if (lane == 0) record_error(a.status, kStatusDeviceOob);
       am = 0;
@@ -71,8 +92,7 @@ __global__ void label_prep_kernel(const LabelPrepArgs a) {
 }  // namespace
 
 cudaError_t launch_label_prep(const LabelPrepArgs& a, cudaStream_t stream) {
-  const int rows = a.B * a.K;
-  label_prep_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(a);
+  label_prep_kernel<<<a.B * a.K, kScanThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -37,134 +37,48 @@
 #include "headlogit.cuh"
 #include "internal.h"
 #include "philox.cuh"
+#include "rowscan.cuh"
 #include "sm103.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr float kLog2eV = 1.4426950408889634f;
-constexpr float kLn2V = 0.69314718055994531f;
-constexpr int kStatsThreads = 256;
+constexpr float kLog2eV = kScanLog2e;
 
 __device__ __forceinline__ float uniform_of(uint32_t word) { return philox_uniform(word); }
 
-// Merge (ma, sa) with (mb, sb): log-sum-exp partials in base 2.
-__device__ __forceinline__ void lse2_merge(float& ma, float& sa, float mb, float sb) {
-  if (mb == -INFINITY) return;
-  if (ma == -INFINITY) {
-    ma = mb;
-    sa = sb;
-    return;
-  }
-  if (mb > ma) {
-    sa = sa * ex2_approx(ma - mb) + sb;
-    ma = mb;
-  } else {
-    sa += sb * ex2_approx(mb - ma);
-  }
-}
-
 // One CTA per row (b, k) of P [B, K+1, V]: the row's log-sum-exp of P / Tt (its argmax when
-// Tt = 0), for the rows k <= L_b = min(ell_b, kmax); later rows only take part in the count.
-// ACCEPT (verification): the CTA of a drafted position k < L_b then runs that position's
+// Tt = 0) for the rows k <= L_b = ell_b (the window; K without ell); later rows only take
+// part in the count.  The CTA of a drafted position k < L_b then runs that position's
 // acceptance test, and the last CTA of request b to finish resolves the request (the
 // accepted prefix ends at the first failed test) and, for a sampled target (v.rows set),
 // prepares the draw at that position for the draft kernel's residual mode: the offsets that
 // turn the draft head's logits and the target logits there into log2 q and log2 p (the
 // draft's normaliser from its own log-probability of the rejected token, l(x) rebuilt by a
 // dot product), and the draw position's predecessor and gate row.
-template <bool ACCEPT>
-__global__ void __launch_bounds__(kStatsThreads) verify_stats_kernel(
-    const float* __restrict__ P, const int32_t* __restrict__ ell, int K, int kmax, int V,
-    float inv_tt, int greedy, float* __restrict__ lse_t, int32_t* __restrict__ argmax_t,
-    const VerifyArgs v, float inv_td, int draft_greedy) {
-  const int row = blockIdx.x;             // b * (K + 1) + k
+__global__ void __launch_bounds__(kScanThreads) verify_stats_kernel(const VerifyArgs v,
+                                                                    float inv_tt, float inv_td,
+                                                                    int greedy, int draft_greedy) {
+  const int K = v.K, V = v.V;
+  const int row = blockIdx.x;  // b * (K + 1) + k
   const int b = row / (K + 1), k = row - b * (K + 1);
-  const int L = min(ell ? min(max(__ldg(ell + b), 0), K) : K, kmax);
-  if (!ACCEPT && k > L) return;
-  const float4* p4 = reinterpret_cast<const float4*>(P + static_cast<size_t>(row) * V);
-  const int n4 = V / 4;
-  __shared__ float s_m[kStatsThreads / 32], s_s[kStatsThreads / 32];
-  __shared__ int s_i[kStatsThreads / 32];
+  const int L = v.ell ? min(max(__ldg(v.ell + b), 0), K) : K;
+  const float* __restrict__ P = v.P;
+  __shared__ RowScanSmem sm;
   __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the row's statistic, final in thread 0: argmax (greedy) or log-sum-exp in nats
-  int bi = 0x7FFFFFFF;
+  // the row's statistic, final in thread 0
+  int bi = 0;
   float lse = 0.f;
-  if (k <= L && greedy) {
-    float bv = -INFINITY;
-    for (int i = threadIdx.x; i < n4; i += kStatsThreads) {
-      const float4 x = __ldcs(p4 + i);
-      const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (xs[c] > bv || (xs[c] == bv && 4 * i + c < bi)) {
-          bv = xs[c];
-          bi = 4 * i + c;
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      s_m[warp] = bv;
-      s_i[warp] = bi;
-    }
-    __syncthreads();
+  if (k <= L) {
+    scan_target_row(P + static_cast<size_t>(row) * V, V, inv_tt, greedy != 0, sm, lse, bi);
     if (threadIdx.x == 0) {
-      for (int w = 1; w < kStatsThreads / 32; ++w)
-        if (s_m[w] > bv || (s_m[w] == bv && s_i[w] < bi)) {
-          bv = s_m[w];
-          bi = s_i[w];
-        }
-      argmax_t[row] = bi;
-    }
-  } else if (k <= L) {
-    // online log-sum-exp of y = P * log2(e) / Tt, four float4 loads in flight
-    const float sc = inv_tt * kLog2eV;
-    float m = -INFINITY, s = 0.f;
-    for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kStatsThreads) {
-      float4 x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kStatsThreads;
-        x[u] = (i < n4) ? __ldcs(p4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
-      float cm = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)) * sc);
-      if (cm == -INFINITY) continue;
-      if (cm > m) {
-        s = (m == -INFINITY) ? 0.f : s * ex2_approx(m - cm);
-        m = cm;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        s += ex2_approx(x[u].x * sc - m) + ex2_approx(x[u].y * sc - m) +
-             ex2_approx(x[u].z * sc - m) + ex2_approx(x[u].w * sc - m);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      lse2_merge(m, s, __shfl_xor_sync(0xFFFFFFFFu, m, off), __shfl_xor_sync(0xFFFFFFFFu, s, off));
-    if (lane == 0) {
-      s_m[warp] = m;
-      s_s[warp] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kStatsThreads / 32; ++w) lse2_merge(m, s, s_m[w], s_s[w]);
-      lse = (m + log2f(s)) * kLn2V;  // natural-log units of P / Tt
-      lse_t[row] = lse;
+      if (greedy)
+        v.argmax_t[row] = bi;
+      else
+        v.lse_t[row] = lse;
     }
   }
-  if (!ACCEPT) return;
   if (threadIdx.x == 0) {
     if (k < L) {  // the acceptance test of drafted position k: accept with min(1, p / q)
       int x = __ldg(v.tokens + static_cast<size_t>(b) * K + k);
@@ -207,7 +121,7 @@ __global__ void __launch_bounds__(kStatsThreads) verify_stats_kernel(
   if (lane == 0) {
     v.n_acc[b] = n;
     v.fail_mask[b] = 0ull;  // ready for the next call
-    if (greedy) v.next_token[b] = __ldcg(argmax_t + static_cast<size_t>(b) * (K + 1) + pos);
+    if (greedy) v.next_token[b] = __ldcg(v.argmax_t + static_cast<size_t>(b) * (K + 1) + pos);
   }
   if (v.rows == nullptr) return;
   if (v.H != nullptr) {  // a bonus row needs no q: any valid gate row will do
@@ -218,7 +132,7 @@ __global__ void __launch_bounds__(kStatsThreads) verify_stats_kernel(
   if (lane == 0) v.prev_sel[b] = prev;
   ResRow rr;
   rr.pos = pos;
-  rr.offp2 = -__ldcg(lse_t + static_cast<size_t>(b) * (K + 1) + pos) * kLog2eV;
+  rr.offp2 = -__ldcg(v.lse_t + static_cast<size_t>(b) * (K + 1) + pos) * kLog2eV;
   rr.offq2 = -INFINITY;  // bonus, or a greedy draft: no draft mass to subtract
   rr.excl = (rejected && draft_greedy) ? x : -1;
   if (rejected && !draft_greedy) {
@@ -232,24 +146,14 @@ __global__ void __launch_bounds__(kStatsThreads) verify_stats_kernel(
 
 }  // namespace
 
-cudaError_t launch_target_stats(const float* P, const int32_t* ell, int B, int K, int kmax, int V,
-                                float target_temperature, float* lse_t, int32_t* argmax_t,
-                                cudaStream_t stream) {
-  const int greedy_t = target_temperature > 0.f ? 0 : 1;
-  const float inv_tt = greedy_t ? 1.f : 1.0f / target_temperature;
-  verify_stats_kernel<false><<<B * (K + 1), kStatsThreads, 0, stream>>>(
-      P, ell, K, kmax, V, inv_tt, greedy_t, lse_t, argmax_t, VerifyArgs{}, 1.f, 0);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_verify(const VerifyArgs& v, cudaStream_t stream, int* launches) {
   *launches = 0;
   const int greedy_t = v.target_temperature > 0.f ? 0 : 1;
   const int greedy_d = v.draft_temperature > 0.f ? 0 : 1;
   const float inv_tt = greedy_t ? 1.f : 1.0f / v.target_temperature;
   const float inv_td = greedy_d ? 1.f : 1.0f / v.draft_temperature;
-  verify_stats_kernel<true><<<v.B * (v.K + 1), kStatsThreads, 0, stream>>>(
-      v.P, v.ell, v.K, v.K, v.V, inv_tt, greedy_t, v.lse_t, v.argmax_t, v, inv_td, greedy_d);
+  verify_stats_kernel<<<v.B * (v.K + 1), kScanThreads, 0, stream>>>(v, inv_tt, inv_td, greedy_t,
+                                                                   greedy_d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;
