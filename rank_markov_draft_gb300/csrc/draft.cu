@@ -637,6 +637,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // launched as a programmatic dependent of the scan that writes its per-row inputs (label and
+  // residual modes): the prologue above overlapped the scan's last CTAs; nothing the scan
+  // writes is read before this point
+  griddep_wait();
 
   if (MODE == kModeResidual && (warp == 0 || warp >= kCtlWarps + kEpiWarps)) {
     // --------------------------------------------------- U producers, residual mode
@@ -1601,7 +1605,7 @@ int draft_threads(int mode) {
 }
 
 cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
-                         uint32_t extra_smem) {
+                         uint32_t extra_smem, bool dependent) {
   const void* fn = nullptr;
   const bool copies = args.p.B <= 64;  // small batches fill the MMA rows with copies
   const bool gated = args.p.H != nullptr || args.p.A != nullptr;
@@ -1639,6 +1643,23 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
   void* kargs[] = {const_cast<DraftArgs*>(&args)};
+  if (dependent && extra_smem == 0) {
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeCooperative;
+    attrs[0].val.cooperative = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(draft_threads(mode));
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelExC(&cfg, fn, kargs);
+    if (err == cudaSuccess) return err;
+    (void)cudaGetLastError();  // refused: the plain cooperative launch below
+  }
   err = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(draft_threads(mode)), kargs,
                                     kSmemBytes + extra_smem, stream);
   // a refused launch leaves its (non-sticky) error as the thread's last error: clear it, so

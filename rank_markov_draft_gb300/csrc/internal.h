@@ -118,8 +118,11 @@ int draft_smem_bytes();
 int draft_threads(int mode);
 // extra_smem > 0 asks for that much more dynamic shared memory than the kernel allows, which
 // the runtime refuses (the refused-launch test); the refusal's error is cleared before return
+// dependent: launched as a programmatic dependent of the preceding kernel of the stream (which
+// may then overlap the prologue; the kernel waits for it before reading any input), falling
+// back to a plain cooperative launch where the runtime refuses the combination
 cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
-                         uint32_t extra_smem = 0);
+                         uint32_t extra_smem = 0, bool dependent = false);
 
 // Gate GEMM: partial[split][m][n] = sum_{j in split} h[m, j] * Wg[j, n].
 struct GateArgs {

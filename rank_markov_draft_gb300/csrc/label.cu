@@ -37,6 +37,8 @@ constexpr float kLog2eL = kScanLog2e;
 // preparation: the predecessor, the draft's log2 q offset and, where one side is greedy,
 // the label itself.
 __global__ void __launch_bounds__(kScanThreads) label_prep_kernel(const LabelPrepArgs a) {
+  // the label pass that follows may start its prologue while the last rows are scanned
+  griddep_launch_dependents();
   const int row = blockIdx.x;  // b * K + k
   const int b = row / a.K, k = row - b * a.K;
   const size_t trow = static_cast<size_t>(b) * (a.K + 1) + k;  // target row of position k

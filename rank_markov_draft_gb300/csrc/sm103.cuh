@@ -129,6 +129,20 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Let the next kernel of the stream, if it was launched as a programmatic dependent, be
+// scheduled now (it still waits in griddep_wait for this grid's completion before it reads
+// what this grid writes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this one depends on have completed and their writes are visible (an
+// immediate return for a launch that is not a programmatic dependent).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -59,6 +59,8 @@ __device__ __forceinline__ float uniform_of(uint32_t word) { return philox_unifo
 __global__ void __launch_bounds__(kScanThreads) verify_stats_kernel(const VerifyArgs v,
                                                                     float inv_tt, float inv_td,
                                                                     int greedy, int draft_greedy) {
+  // the residual draw that follows may start its prologue while the last rows are scanned
+  griddep_launch_dependents();
   const int K = v.K, V = v.V;
   const int row = blockIdx.x;  // b * (K + 1) + k
   const int b = row / (K + 1), k = row - b * (K + 1);

@@ -104,34 +104,26 @@ def test_label_of_a_target_equal_to_the_draft_is_one(dsp):
     assert np.abs(host(lab) - 1.0).max() <= LABEL_TOL
 
 
-def test_label_full_size_sampled(dsp):
-    """Serving shape (B=128, K=16, V=151936, r=256) in one call; three requests
-    are drafted and labelled by the oracle, the others carry arbitrary valid
-    tokens (their labels are only checked to lie in [0, 1])."""
+def test_label_full_size(dsp):
+    """Serving shape (B=128, K=16, V=151936, r=256) in one call: the oracle drafts
+    every request and labels every drafted position, and all B K labels are
+    compared."""
     B, K, V, r = 128, 16, 151936, 256
     inp = make_inputs(78, B, K, V, r, weight_std=0.05)
     P = _target_logits(np.random.default_rng(79), inp.U, noise=1.0)
-    rng = np.random.default_rng(80)
-    tokens = rng.integers(0, V, (B, K)).astype(np.int32)
-    logq = np.full((B, K), -np.log(V), np.float32)
-    sample = [0, 77, 127]
-    ref = {}
-    for b in sample:
-        dr = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=4,
-                                 b0=b, nb=1)
-        tokens[b], logq[b] = dr["tokens"][0], dr["logprobs"][0]
-        ref[b] = oracle.accept_label(P[b:b + 1], inp.U[b:b + 1], inp.W1, inp.W2,
-                                     inp.anchors[b:b + 1], dr["tokens"], draft_temperature=1.0,
-                                     target_temperature=1.0)[0]
+    dr = oracle.markov_draft(inp.U, inp.W1, inp.W2, inp.anchors, temperature=1.0, seed=4)
+    ref = oracle.accept_label(P, inp.U, inp.W1, inp.W2, inp.anchors, dr["tokens"],
+                              draft_temperature=1.0, target_temperature=1.0)
     lab = binding.accept_label(dsp, dev(P), dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors),
-                               dev(tokens), dev(logq), draft_temperature=1.0,
-                               target_temperature=1.0)
+                               dev(dr["tokens"]), dev(dr["logprobs"].astype(np.float32)),
+                               draft_temperature=1.0, target_temperature=1.0)
     torch.cuda.synchronize()
     assert dsp.status() == 0
     lab = host(lab)
-    assert np.all((lab >= 0) & (lab <= 1))
-    for b in sample:
-        assert np.abs(lab[b] - ref[b]).max() <= LABEL_TOL, (b, np.abs(lab[b] - ref[b]).max())
+    assert lab.shape == (B, K) and np.all((lab >= 0) & (lab <= 1))
+    err = np.abs(lab - ref)
+    print(f"labels compared: {err.size} of {B * K}, max |error| {err.max():.2e}")
+    assert err.max() <= LABEL_TOL, (np.unravel_index(err.argmax(), err.shape), err.max())
 
 
 def test_label_argument_errors(dsp):
