@@ -327,10 +327,11 @@ int run_draft(dspark_ctx* ctx, int mode, const float* U, const uint16_t* W1, con
       p.trace = ctx->trace;
     const uint32_t extra = ctx->debug_refuse_launch ? 1024u : 0u;
     ctx->debug_refuse_launch = false;
-    // the label and residual passes of the first chunk directly follow the scan kernel that
-    // writes their per-row inputs: launched as its programmatic dependent (not after a key
+    // the first chunk of a call that has just run its own kernel (the label and residual
+    // passes after the scan that writes their per-row inputs, the gated and RNN heads after
+    // their gate GEMMs) is launched as that kernel's programmatic dependent (not after a key
     // reset, whose memset would then be the preceding work)
-    const bool dependent = lab != nullptr && b0 == 0 && p.epoch != 1;
+    const bool dependent = (lab != nullptr || H != nullptr) && b0 == 0 && p.epoch != 1;
     cudaError_t e = dspark::launch_draft(args, mode, grid, stream, extra, dependent);
     if (e != cudaSuccess) {
       ctx->debug_skip_cta = -1;

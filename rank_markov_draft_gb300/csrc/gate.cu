@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) gate_gemm_kernel(const __grid_con
 // rounded to bf16, for the draft kernel's packed operand arithmetic) are each optional.
 __global__ void gate_finalize_kernel(const float4* __restrict__ partial, int splits, int64_t n4,
                                      float4* __restrict__ H, uint2* __restrict__ Hb) {
+  // a draft launched as this kernel's programmatic dependent may start its prologue now
+  griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 pv[8];
