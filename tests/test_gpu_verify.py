@@ -68,6 +68,22 @@ def _check(inp, P, tokens, out, Td, Tt, seed, ell=None, H=None, requests=None):
     assert near <= max(1, (1 - COVERAGE) * n), f"{near} of {n} requests stopped at a near tie"
 
 
+def test_verify_repeated_calls_are_identical(dsp):
+    """The scan keeps per-request counters and failure masks in the context, which each
+    call's last CTA per request returns to zero: repeated calls on one context (with
+    windows, so some CTAs only count) give identical results, equal to the oracle's."""
+    B, K, V, r = 40, 6, 2048, 64
+    inp = make_inputs(67, B, K, V, r, weight_std=0.1)
+    P = _target_logits(np.random.default_rng(68), inp.U)
+    ell = np.random.default_rng(69).integers(0, K + 1, B).astype(np.int32)
+    runs = [_run(dsp, inp, P, 1.0, 1.0, seed=11, ell=ell) for _ in range(3)]
+    tokens, first = runs[0]
+    for _, out in runs[1:]:
+        for key in ("n_acc", "next_token", "accept_prob"):
+            assert np.array_equal(out[key], first[key]), key
+    _check(inp, P, tokens, first, 1.0, 1.0, seed=11, ell=ell)
+
+
 @pytest.mark.parametrize("Td,Tt", [(1.0, 1.0), (0.7, 1.3), (0.0, 1.0), (1.0, 0.0), (0.0, 0.0)])
 def test_verify_matches_oracle(dsp, Td, Tt):
     B, K, V, r = 12, 5, 1000, 64
