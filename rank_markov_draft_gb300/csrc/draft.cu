@@ -129,9 +129,21 @@ constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;  // 320
 // scheduler at most) share each fill's copies with warp 0.
 constexpr int kResCopyWarps = 2;
 constexpr int kResProducers = 1 + kResCopyWarps;
-template <int MODE>
-constexpr int threads_of() {
-  return kThreads + (MODE == kModeResidual ? kResCopyWarps * 32 : 0);
+// The sampling mode above 64 requests runs two more warps too (noise warps): they draw the
+// race's stage-1 exponentials of every epilogue thread's blocks, a tile ahead, into a
+// two-tile ring in shared memory, taking the two Philox calls per thread and tile off the
+// epilogue warps (with batch copies, a thread using one sub-tile of each tile, the handoff
+// measured slower than the calls).
+constexpr int kNoiseWarps = 2;
+template <int MODE, bool COPIES>
+__host__ __device__ constexpr bool noise_warps() {
+  return MODE == kModeSample && !COPIES;
+}
+template <int MODE, bool COPIES>
+__host__ __device__ constexpr int threads_of() {
+  return kThreads + (MODE == kModeResidual              ? kResCopyWarps * 32
+                     : noise_warps<MODE, COPIES>()      ? kNoiseWarps * 32
+                                                        : 0);
 }
 constexpr uint32_t kW2SlotBytes = kDraftSliceRows * kTileN * 2;  // 32 KB
 constexpr uint32_t kUBoxBytes = kRows * 32 * 4;              // 16 KB (32 tokens x 128 rows)
@@ -147,7 +159,10 @@ constexpr uint32_t kOffMerge = kOffU + kNumUStages * kUStageBytes;
 constexpr uint32_t kOffBest = kOffMerge + kMergeBytes;
 constexpr uint32_t kOffBar = kOffBest + kBestBytes;
 constexpr uint32_t kBarRegion = 2048;
-constexpr uint32_t kSmemBytes = kOffBar + kBarRegion + 1024;  // + alignment slack
+// the noise ring: two tiles of one float4 (log2 E of its four blocks) per epilogue thread
+constexpr uint32_t kOffNoise = kOffBar + kBarRegion;
+constexpr uint32_t kNoiseBytes = 2 * kEpiThreads * 16;       // 8 KB
+constexpr uint32_t kSmemBytes = kOffNoise + kNoiseBytes + 1024;  // + alignment slack
 // TMEM: kNumAcc accumulators of 128 columns, then the MMA's A operand ([128 x r] bf16,
 // two elements per column: r / 2 <= 128 columns)
 constexpr uint32_t kTmemA = kNumAcc * kTileN;                // 384
@@ -164,7 +179,7 @@ static_assert(kTmemA + kMaxRank / 2 <= kTmemCols, "TMEM columns");
 static_assert(kNumUStagesSmall * kUStageBytes / 2 <= kNumUStages * kUStageBytes, "U ring");
 static_assert(kTileN == 2 * kSubV, "a tile is two sub-tiles");
 static_assert((2 * kNumW2SlotsMax + 2 * kNumUStagesSmall + 2 * kNumAcc + 6) * 8 + 2 * kMaxK * 4 +
-                      kRows * 8 + 16 <=
+                      kRows * 8 + 8 + 4 * 8 <=
                   kBarRegion,
               "barrier region too small");
 
@@ -538,7 +553,7 @@ __device__ __forceinline__ float sum16(const float* w) {
 // GATED: the launch may carry a gate (gated head) or decay and input gates (RNN head); the
 // plain instantiations compile the operand path without them
 template <int MODE, bool COPIES, bool GATED>
-__global__ void __launch_bounds__(threads_of<MODE>(), 1)
+__global__ void __launch_bounds__(threads_of<MODE, COPIES>(), 1)
     draft_kernel(const __grid_constant__ DraftArgs args) {
   const DraftParams& p = args.p;
   // teacher-forced modes take the predecessors from the caller
@@ -551,6 +566,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
   constexpr bool kKeys = !kTF || MODE == kModeResidual;
   // modes that can run the RNN head (verification and labels take no decay gate)
   constexpr bool kRnnOk = !kHalf;
+  // the race's stage-1 noise comes from the noise warps
+  constexpr bool kNoise = noise_warps<MODE, COPIES>();
   // W2 ring slots: a fourth one in the U region's free tail with batch copies
   constexpr int kW2Slots = COPIES ? kNumW2SlotsMax : kNumW2Slots;
   static_assert(kNumUStagesSmall * kUStageBytes / 2 + kW2SlotBytes <= kNumUStages * kUStageBytes,
@@ -585,6 +602,9 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
   // request in the current step: a lower bound on the step's winner
   unsigned long long* s_bound = reinterpret_cast<unsigned long long*>(s_conf + kMaxK);  // [128]
   uint32_t* s_sink = reinterpret_cast<uint32_t*>(s_bound + kRows);  // scratch word (U releases)
+  uint64_t* noise_full = reinterpret_cast<uint64_t*>(s_bound + kRows) + 1;  // [2]
+  uint64_t* noise_empty = noise_full + 2;                                  // [2]
+  float4* s_noise = reinterpret_cast<float4*>(smem + kOffNoise);  // [2][kEpiThreads]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x, ncta = gridDim.x;
@@ -620,6 +640,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], kEpiWarps);  // every epilogue warp reads every accumulator
     }
+    if (kNoise) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&noise_full[s], kNoiseWarps);
+        mbar_init(&noise_empty[s], kEpiWarps);
+      }
+    }
     mbar_init(a_full, kEpiWarps);  // every epilogue warp's operand rows are in TMEM
     mbar_init(a_empty, 1);
     mbar_init(mma_drain, 1);
@@ -642,7 +668,59 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
   // writes is read before this point
   griddep_wait();
 
-  if (MODE == kModeResidual && (warp == 0 || warp >= kCtlWarps + kEpiWarps)) {
+  if (kNoise && warp >= kCtlWarps + kEpiWarps) {
+    // ------------------------------------------------------------ noise warps
+    // Noise warp n draws for epilogue warps 4 n .. 4 n + 3 (those of column group g = n):
+    // lane l for the epilogue threads 128 n + 32 j + l, j = 0..3, each the same Philox calls
+    // (counter (tile, k, request, 1 + 2 g) and (.., 2 + 2 g)) the thread would make, reduced
+    // to the four blocks' log2 E; the stage-2 word of a thread's best block is drawn again
+    // by the thread after the sweep.
+    const int n = warp - (kCtlWarps + kEpiWarps);
+    const int rpc = COPIES ? rows_per_copy(p.B) : kRows;
+    const uint32_t tag = 1u + 2u * static_cast<uint32_t>(n);
+    uint32_t bg[4];
+    bool rok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = (4 * n + j + kCtlWarps) & 3;  // the epilogue warp's TMEM lane quadrant
+      const int b = (q * 32 + lane) & (rpc - 1);
+      rok[j] = b < p.B;
+      bg[j] = static_cast<uint32_t>(p.b_global0 + b);
+    }
+    bool ok = true;
+    for (int k = 0; k < p.K && ok; ++k) {
+      for (int t = 0; t < nt; ++t) {
+        const int i = k * nt + t, slot = i & 1;
+        if (lane == 0)
+          ok = mbar_wait(&noise_empty[slot], ((i >> 1) & 1) ^ 1, p.timeout_ns, abort_flag,
+                         kBackoffControlNs);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        const uint32_t tile = static_cast<uint32_t>(tile_of(k, t));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float4 e4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (rok[j]) {
+            uint32_t za[4], zb[4];
+            philox4x32_10_rk2(tile, static_cast<uint32_t>(k), bg[j], tag, tag + 1u, p.round_key0,
+                              p.round_key1, za, zb);
+            e4 = make_float4(lg2_approx(neg_log_uniform_fast(za[0])),
+                             lg2_approx(neg_log_uniform_fast(zb[0])),
+                             lg2_approx(neg_log_uniform_fast(za[2])),
+                             lg2_approx(neg_log_uniform_fast(zb[2])));
+          }
+          s_noise[smem_checked(static_cast<uint32_t>(slot * kEpiThreads + 128 * n + 32 * j + lane),
+                               1, 2 * kEpiThreads, p.status)] = e4;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&noise_full[slot]);
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      record_error(p.status, kStatusTimeout);
+    }
+  } else if (MODE == kModeResidual && (warp == 0 || warp >= kCtlWarps + kEpiWarps)) {
     // --------------------------------------------------- U producers, residual mode
     // The draw rows are read in place: each request's base-logit row and target row at its
     // own draw position (tile::gather4 over 2-D row maps of U [B K, V] and P [B (K + 1), V],
@@ -1016,7 +1094,26 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
         const int i = k * nt + t;
         const int buf = i % kNumAcc;
         const int tile = tile_of(k, t);
-        if (kRace && row_ok) {
+        if (kNoise) {
+          // the stage-1 exponentials of this thread's blocks, drawn by the noise warps
+          const int slot = i & 1;
+          bool okn = mbar_wait(&noise_full[slot], static_cast<uint32_t>(i >> 1) & 1u,
+                               p.timeout_ns, abort_flag);
+          okn = __all_sync(0xFFFFFFFFu, okn);
+          if (!okn) {
+            fail = true;
+            *abort_flag = 1;
+            break;
+          }
+          const float4 e4 = s_noise[smem_checked(static_cast<uint32_t>(slot * kEpiThreads + etid),
+                                                 1, 2 * kEpiThreads, p.status)];
+          lE[0] = e4.x;
+          lE[1] = e4.y;
+          lE[2] = e4.z;
+          lE[3] = e4.w;
+          arrive_after_reads(&noise_empty[slot], __float_as_uint(e4.x) ^ __float_as_uint(e4.w),
+                             s_sink, lane);
+        } else if (kRace && row_ok) {
           const uint32_t c1 = static_cast<uint32_t>(MODE == kModeResidual ? res_pos : k);
           const uint32_t tag = (MODE == kModeResidual ? 9u : 1u) + 2u * static_cast<uint32_t>(g);
           philox4x32_10_rk2(static_cast<uint32_t>(tile), c1, b_global, tag, tag + 1u,
@@ -1275,10 +1372,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
             // stage 1: G = m2 + log2(block mass) - log2(E); stage 2 runs once, after the sweep
             const float G0 = bs0 > 0.f ? m2 + lg2_approx(bs0) - lE[2 * sub] : -INFINITY;
             const float G1 = bs1 > 0.f ? m2 + lg2_approx(bs1) - lE[2 * sub + 1] : -INFINITY;
-            keep_best(G0, vbase, sub ? nza[3] : nza[1], l, my_best, kEpiThreads, best, best_v,
-                      best_w);
-            keep_best(G1, vbase + 16, sub ? nzb[3] : nzb[1], l + 16, my_best, kEpiThreads, best,
-                      best_v, best_w);
+            // (with the noise warps the best block's stage-2 word is drawn again after the
+            // sweep, from best_v)
+            keep_best(G0, vbase, kNoise ? 0u : (sub ? nza[3] : nza[1]), l, my_best, kEpiThreads,
+                      best, best_v, best_w);
+            keep_best(G1, vbase + 16, kNoise ? 0u : (sub ? nzb[3] : nzb[1]), l + 16, my_best,
+                      kEpiThreads, best, best_v, best_w);
           } else if (MODE == kModeGreedy) {
             keep_best(mb0 * scale2, vbase, 0u, l, my_best, kEpiThreads, best, best_v, best_w);
             keep_best(mb1 * scale2, vbase + 16, 0u, l + 16, my_best, kEpiThreads, best, best_v,
@@ -1307,6 +1406,16 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
         } else {
           const float vmax = max16(v16);
           if (MODE == kModeSample) {
+            if (kNoise) {
+              // the stage-2 word of the best block (token best_v = 128 tile + 64 sub + 32 g +
+              // 16 h): word 3 (sub-tile 1) or 1 (sub-tile 0) of the call for block half h
+              const uint32_t tag = 1u + 2u * static_cast<uint32_t>(g);
+              uint32_t za[4], zb[4];
+              philox4x32_10_rk2(static_cast<uint32_t>(best_v >> 7), static_cast<uint32_t>(k),
+                                b_global, tag, tag + 1u, p.round_key0, p.round_key1, za, zb);
+              const bool s1 = ((best_v >> 6) & 1) != 0, h1 = ((best_v >> 4) & 1) != 0;
+              best_w = h1 ? (s1 ? zb[3] : zb[1]) : (s1 ? za[3] : za[1]);
+            }
             float w16[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) w16[j] = ex2_approx((v16[j] - vmax) * scale2);
@@ -1600,8 +1709,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 }  // namespace
 
 int draft_smem_bytes() { return static_cast<int>(kSmemBytes); }
-int draft_threads(int mode) {
-  return mode == kModeResidual ? threads_of<kModeResidual>() : kThreads;
+int draft_threads(int mode, bool copies) {
+  return mode == kModeResidual               ? threads_of<kModeResidual, false>()
+         : (mode == kModeSample && !copies) ? threads_of<kModeSample, false>()
+                                             : kThreads;
 }
 
 cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t stream,
@@ -1651,7 +1762,7 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(draft_threads(mode));
+    cfg.blockDim = dim3(draft_threads(mode, copies));
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attrs;
@@ -1660,7 +1771,7 @@ cudaError_t launch_draft(const DraftArgs& args, int mode, int grid, cudaStream_t
     if (err == cudaSuccess) return err;
     (void)cudaGetLastError();  // refused: the plain cooperative launch below
   }
-  err = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(draft_threads(mode)), kargs,
+  err = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(draft_threads(mode, copies)), kargs,
                                     kSmemBytes + extra_smem, stream);
   // a refused launch leaves its (non-sticky) error as the thread's last error: clear it, so
   // that the caller's next CUDA error check does not see it again

@@ -115,7 +115,7 @@ enum DraftMode {
 };
 
 int draft_smem_bytes();
-int draft_threads(int mode);
+int draft_threads(int mode, bool copies);
 // extra_smem > 0 asks for that much more dynamic shared memory than the kernel allows, which
 // the runtime refuses (the refused-launch test); the refusal's error is cleared before return
 // dependent: launched as a programmatic dependent of the preceding kernel of the stream (which
