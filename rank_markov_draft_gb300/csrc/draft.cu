@@ -44,6 +44,10 @@
 //     the race (its values parked in shared memory), so the full-vocabulary
 //     logits never reach HBM; stage 2 of the race runs once per step per
 //     thread, in that best block;
+//   * warps 10 and 11 exist in two builds only: in the sampling build above 64
+//     requests they draw the race's stage-1 noise of every epilogue thread's
+//     blocks a tile ahead into a two-tile shared-memory ring (noise warps); in
+//     the residual build they share the gathered-row copies with warp 0;
 //   * at the end of a step each CTA publishes, per request, a 64-bit key
 //     (epoch | ordered score | inverted token id) by atomicMax (only where it
 //     can still raise the key) and its log-sum-exp partial; it arrives at a
