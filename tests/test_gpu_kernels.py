@@ -81,6 +81,7 @@ DRAFT_CASES = [
     (130, 3, 520, 32),
     (3, 5, 8, 16),
     (2, 16, 151936, 256),
+    (96, 5, 40000, 64),     # one chunk above 64 requests, two or three tiles a CTA
 ]
 
 
