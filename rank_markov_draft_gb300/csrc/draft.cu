@@ -123,8 +123,9 @@ constexpr int kNumUStagesSmall = 4;              // slots of 16 KB when B <= 64 
 constexpr int kNumAcc = 3;                       // TMEM accumulators, 128 columns each
 constexpr int kCtlWarps = 2;                     // U producer; MMA issuer and W2 producer
 // Eight epilogue warps: two per TMEM lane quadrant, each thread taking 32 tokens (two
-// 16-token blocks) of every 64-token sub-tile.  Ten warps in all leave up to 168
-// registers a thread (three warps on a scheduler), enough for two blocks at once.
+// 16-token blocks) of every 64-token sub-tile.  Ten warps in all (twelve in the builds with
+// two more warps, below) leave up to 168 registers a thread (three warps on a scheduler),
+// enough for two blocks at once.
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;      // 256
 constexpr int kThreads = kCtlWarps * 32 + kEpiThreads;  // 320
