@@ -98,3 +98,15 @@ def test_profile_hash_ignores_comments_but_not_code():
         "// header comment\nint f(int x) {\n  return 2 * x;   /* changed note */\n}\n")
     assert bench._code_only(src) != bench._code_only("int f(int x) {\n  return 3 * x;\n}\n")
     assert len(bench.kernel_source_hash("serving")) == 16
+
+
+def test_profiles_name_existing_sources_and_carry_their_figures():
+    """Every workload with a committed ncu summary names kernel sources that exist, and the
+    summary carries the source hash and the per-launch DRAM bytes the bench reads."""
+    import re
+    for workload, (summary, sources) in bench.PROFILES.items():
+        for name in sources:
+            assert os.path.exists(os.path.join(bench.ROOT, "rank_markov_draft_gb300", "csrc", name)), name
+        text = open(os.path.join(bench.ROOT, "profiles", summary)).read()
+        assert re.search(r"kernel source hash:\s*`[0-9a-f]{16}`", text), summary
+        assert re.search(r"dram bytes per launch:\s*`[0-9]+`", text), summary
