@@ -22,8 +22,9 @@ from tests.gpu_util import bf, dev
 pytestmark = pytest.mark.gpu
 
 
-def test_barrier_timeout_is_reported_and_recoverable():
-    B, K, V, r = 4, 3, 4096, 256
+@pytest.mark.parametrize("B", [4, 96])  # the batch-copies build; the build with noise warps
+def test_barrier_timeout_is_reported_and_recoverable(B):
+    K, V, r = 3, 4096, 256
     inp = make_inputs(5, B, K, V, r)
     args = (dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors))
     with binding.Context(0, B_max=B, V_max=V, K_max=K) as ctx:
