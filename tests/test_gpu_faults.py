@@ -46,6 +46,39 @@ def test_barrier_timeout_is_reported_and_recoverable(B):
         assert torch.equal(again["logprobs"], clean["logprobs"])
 
 
+def test_verify_draw_timeout_is_reported_and_recoverable():
+    """The fault knob on the verification's draw (the residual-mode launch, whose row copies
+    three warps issue): the draw's waits run out and it exits, the context reports the
+    timeout, and after a reset the same call reproduces the clean result."""
+    B, K, V, r = 8, 4, 4096, 64
+    inp = make_inputs(7, B, K, V, r)
+    rng = np.random.default_rng(8)
+    P = np.empty((B, K + 1, V), np.float32)
+    P[:, :K] = inp.U + rng.standard_normal((B, K, V)).astype(np.float32)
+    P[:, K] = rng.standard_normal((B, V)).astype(np.float32)
+    U, W1, W2, anchors = dev(inp.U), bf(inp.W1), bf(inp.W2), dev(inp.anchors)
+    Pd = dev(P)
+    with binding.Context(0, B_max=B, V_max=V, K_max=K) as ctx:
+        d = binding.markov_draft(ctx, U, W1, W2, anchors, temperature=1.0, seed=3)
+        kw = dict(draft_temperature=1.0, target_temperature=1.0, seed=5)
+        clean = binding.verify(ctx, Pd, U, W1, W2, anchors, d["tokens"], d["logprobs"], **kw)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        ctx.debug_set(cta=0, timeout_ms=200)
+        binding.verify(ctx, Pd, U, W1, W2, anchors, d["tokens"], d["logprobs"], **kw)
+        torch.cuda.synchronize()          # returns: the draw exited on its own
+        assert ctx.status() == binding.TIMEOUT
+        with pytest.raises(binding.DSparkError) as err:
+            binding.verify(ctx, Pd, U, W1, W2, anchors, d["tokens"], d["logprobs"], **kw)
+        assert err.value.code == binding.POISONED
+        ctx.reset()
+        again = binding.verify(ctx, Pd, U, W1, W2, anchors, d["tokens"], d["logprobs"], **kw)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        for key in ("n_acc", "next_token", "accept_prob"):
+            assert torch.equal(again[key], clean[key]), key
+
+
 def test_refused_launch_returns_cuda_error_and_enqueues_nothing():
     """A launch configuration the CUDA runtime refuses (more dynamic shared memory than
     the kernel allows) comes back from the host call as DSPARK_ERR_CUDA: no kernel ran,
